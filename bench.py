@@ -1,0 +1,446 @@
+"""Benchmark of the Q4_K projection path on one GB300.
+
+Default workload (the headline): a 27B-class dense decoder layer at batch 1 --
+Q4_K projections QKV 5120->10240, O 8192->5120, gate and up 5120->17408, down
+17408->5120 -- repeated over 64 layers of distinct random weights (13.0 GB of
+Q4_K weights), all 320 projections back to back on one stream.  One step is one
+pass over the 64 layers.  Metric: achieved HBM GB/s (algorithmic bytes: every
+weight byte once, plus x and y).  Weights are far larger than L2, so nothing is
+served from cache between steps.
+
+Other configurations of the path (decode batch 4/16 on the same layers, the
+4096x4096 single GEMV over a rotating pool, the 512-token prefill GEMM and the
+routed-MoE decode) are measured in the same run and reported under "configs".
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--skip-extra]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+HIDDEN = 5120
+LAYER_SHAPES = [("qkv", 10240, 5120), ("o", 5120, 8192), ("gate", 17408, 5120),
+                ("up", 17408, 5120), ("down", 5120, 17408)]
+N_LAYERS = 64
+SEED_C1 = 1001
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def q4k_bytes(n, k):
+    return n * (k // 256) * 144
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[key] = float(v)
+            if "hbm_gbs" in out:
+                out["source"] = "measured"
+                return out
+        except Exception:
+            pass
+    out = dict(FALLBACK)
+    out["source"] = "fallback"
+    return out
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+class Layers:
+    """64 layers of distinct Q4_K weights for the five projections, on the GPU."""
+
+    def __init__(self, dev, n_layers=N_LAYERS, seed=SEED_C1):
+        self.mats = []
+        for layer in range(n_layers):
+            for pi, (name, n, k) in enumerate(LAYER_SHAPES):
+                w = synth.q4k_weight(n, k, seed=synth.derive_seed(seed, "w", layer, pi),
+                                     quants="normal", device=dev)
+                self.mats.append((name, n, k, w))
+
+    def algorithmic_bytes(self, batch):
+        return sum(q4k_bytes(n, k) + batch * k * 2 + batch * n * 4 for _, n, k, _ in self.mats)
+
+
+def make_inputs(layers, batch, dev, seed):
+    xs, ys = [], []
+    for i, (_, n, k, _) in enumerate(layers.mats):
+        xs.append(synth.bf16_normal((batch, k), seed=synth.derive_seed(seed, "x", batch, i),
+                                    device=dev))
+        ys.append(torch.empty((batch, n), dtype=torch.float32, device=dev))
+    return xs, ys
+
+
+def time_graph(fn, steps, warmup, stream):
+    """Capture fn into a CUDA graph; time `steps` replays with CUDA events."""
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    per = []
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            g.replay()
+            e.record(stream)
+            per.append((s, e))
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    per_ms = [s.elapsed_time(e) for s, e in per]
+    return total_ms / steps, per_ms, g
+
+
+def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None):
+    xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
+
+    def step():
+        for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
+            q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
+
+    if sampler is not None:
+        with sampler:
+            ms, per, g = time_graph(step, steps, warmup, stream)
+    else:
+        ms, per, g = time_graph(step, steps, warmup, stream)
+    del g
+    nbytes = layers.algorithmic_bytes(batch)
+    return {"ms_per_step": ms, "ms_min": min(per), "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "bytes_per_step": nbytes, "launches_per_step": len(layers.mats)}
+
+
+def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
+    """Same pass through the public API with host buffers: each step copies every
+    projection's x from pinned host memory and reads every y back."""
+    host_x, host_y, dx, dy = [], [], [], []
+    for i, (_, n, k, _) in enumerate(layers.mats):
+        x = synth.bf16_normal((batch, k), seed=synth.derive_seed(SEED_C1, "xe", i))
+        host_x.append(x.pin_memory())
+        host_y.append(torch.empty((batch, n), dtype=torch.float32).pin_memory())
+        dx.append(torch.empty((batch, k), dtype=torch.bfloat16, device=dev))
+        dy.append(torch.empty((batch, n), dtype=torch.float32, device=dev))
+    h2d = sum(t.numel() * 2 for t in host_x)
+    d2h = sum(t.numel() * 4 for t in host_y)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for (name, n, k, w), hx, hy, x, y in zip(layers.mats, host_x, host_y, dx, dy):
+                x.copy_(hx, non_blocking=True)
+                q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
+                hy.copy_(y, non_blocking=True)
+
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    stream.synchronize()
+    sec = (time.perf_counter() - t0) / steps
+    nbytes = layers.algorithmic_bytes(batch)
+    return {"value": round(nbytes / sec / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 4)}
+
+
+def bench_c0_pool(q4k, steps, warmup, dev, stream):
+    """4096x4096 single GEMV at batch 1 over a rotating pool of distinct matrices
+    (pool >> L2, so every call streams its weights from HBM)."""
+    n = k = 4096
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool = max(32, int(4 * l2 // q4k_bytes(n, k)) + 1)
+    ws = [synth.q4k_weight(n, k, seed=synth.derive_seed(1000, "w", i), device=dev)
+          for i in range(pool)]
+    x = synth.bf16_normal((1, k), seed=1000, device=dev)
+    ys = [torch.empty((1, n), device=dev) for _ in range(pool)]
+
+    def step():
+        for w, y in zip(ws, ys):
+            q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
+
+    ms, per, g = time_graph(step, steps, warmup, stream)
+    del g
+    nbytes = pool * (q4k_bytes(n, k) + k * 2 + n * 4)
+    return {"pool": pool, "us_per_gemv": ms * 1e3 / pool, "gbs": nbytes / (ms * 1e-3) / 1e9}
+
+
+# ------------------------------------------------------------------ CPU baseline
+
+def cpu_baseline(budget_s=12.0):
+    """The oracle as it stands, timed on the host cores, on a bounded sample of
+    the headline workload: the first 256 rows of each projection of as many
+    layers as fit the time budget (input generation is not timed)."""
+    import oracle
+    oracle.build()
+    nrows = 256
+
+    def sample(layer):
+        out = []
+        for pi, (name, n, k) in enumerate(LAYER_SHAPES):
+            w = synth.q4k_weight(nrows, k, seed=synth.derive_seed(SEED_C1, "w", layer, pi),
+                                 quants="normal").numpy()
+            x = synth.bf16_normal((1, k), seed=synth.derive_seed(SEED_C1, "x", 1, pi))
+            out.append((w, k, x.view(torch.int16).numpy().view(np.uint16)))
+        return out
+
+    elapsed, done_bytes, layers = 0.0, 0, 0
+    while elapsed < budget_s and layers < N_LAYERS:
+        for w, k, xb in sample(layers):
+            t = time.perf_counter()
+            oracle.gemv(w, nrows, k, xb)
+            elapsed += time.perf_counter() - t
+            done_bytes += q4k_bytes(nrows, k) + k * 2 + nrows * 4
+        layers += 1
+    return {"value": round(done_bytes / elapsed / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle GEMV, batch 1, first {nrows} rows of each of the 5 "
+                      f"projections of {layers} layer(s) ({done_bytes / 1e6:.1f} MB of Q4_K "
+                      f"weights), {elapsed:.1f} s of oracle time"}
+
+
+# ------------------------------------------------------------------ main
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle as it stands, on the host cores, on a
+    bounded sample of the headline workload per step."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    per_step = []
+    nbytes = 0
+    samples = []
+    for pi, (name, n, k) in enumerate(LAYER_SHAPES):
+        nrows = 64
+        w = synth.q4k_weight(nrows, k, seed=synth.derive_seed(SEED_C1, "w", 0, pi),
+                             quants="normal").numpy()
+        x = synth.bf16_normal((1, k), seed=synth.derive_seed(SEED_C1, "x", 1, pi))
+        samples.append((w, nrows, k, x.view(torch.int16).numpy().view(np.uint16)))
+        nbytes += q4k_bytes(nrows, k) + k * 2 + nrows * 4
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        for w, nrows, k, xb in samples:
+            oracle.gemv(w, nrows, k, xb)
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            per_step.append(dt)
+    sec = sum(per_step) / len(per_step)
+    value = nbytes / sec / 1e9
+    line = {"metric": "Q4_K GEMV achieved HBM GB/s (27B-class dense layer, batch 1)",
+            "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "27b_dense_layer_b1 (oracle sample: first 64 rows of each "
+                                   "projection of layer 0 per step)", "batch": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "first 64 rows of each of the 5 projections of layer 0"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--layers", type=int, default=N_LAYERS)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import bit_block_quantized_q4_gb300 as q4k
+    from bit_block_quantized_q4_gb300 import build as qb
+    if rank == 0:
+        qb.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    layers = Layers(dev, n_layers=args.layers)
+    sampler = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    head = bench_decode(q4k, layers, 1, args.steps, args.warmup, dev, stream, sampler)
+    ms = head["ms_per_step"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert q4k.q4k_get_device_error(stream) == 0
+    pk = peaks()
+    nbytes = head["bytes_per_step"]
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    total_value = achieved * world
+    launches = head["launches_per_step"]
+
+    e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
+    e2e["value"] = round(e2e["value"] * world, 2)
+
+    extra = {}
+    if not args.skip_extra:
+        for b in (4, 16):
+            r = bench_decode(q4k, layers, b, max(5, args.steps // 2), 3, dev, stream)
+            extra[f"decode_b{b}"] = {"gbs": round(r["gbs"], 1),
+                                     "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
+                                     "ms_per_step": round(r["ms_per_step"], 4)}
+        del layers
+        torch.cuda.empty_cache()
+        r = bench_c0_pool(q4k, max(5, args.steps // 2), 3, dev, stream)
+        extra["gemv_4096_b1_pool"] = {"gbs": round(r["gbs"], 1),
+                                      "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
+                                      "us_per_gemv": round(r["us_per_gemv"], 3), "pool": r["pool"]}
+    cpu = cpu_baseline() if rank == 0 else None
+    clocks = sampler.summary()
+
+    if rank == 0:
+        line = {
+            "metric": "Q4_K GEMV achieved HBM GB/s (27B-class dense layer, batch 1)",
+            "value": round(total_value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Q4_K fields; x ~ N(0,1) bf16)",
+            "config": {"workload": "27b_dense_layer_b1: 64 layers x {qkv 5120->10240, o 8192->5120, "
+                                   "gate/up 5120->17408, down 17408->5120}, batch 1",
+                       "batch": 1, "layers": args.layers, "weights_bytes": sum(
+                           q4k_bytes(n, k) for _, n, k in LAYER_SHAPES) * args.layers,
+                       "l2": "weights (13 GB) far exceed L2; no flush needed",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": pk["source"],
+                         "kernel": "gemv_b1_kernel (q4k_gemv, batch 1)",
+                         "note": "algorithmic bytes of the 320 launches / step time (includes "
+                                 "inter-launch gaps)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks,
+            "configs": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+"""Python binding of libq4k.so, the GB300 (sm_103a) Q4_K projection library.
+
+The functions here carry the C entry points' names and only marshal
+arguments: torch tensors in, raw device pointers, sizes and the current CUDA
+stream out.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback.  If libq4k.so is missing, importing works but every call
+raises.  Build it with ``python -m bit_block_quantized_q4_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libq4k.so")
+Q4K_VALUES = 256
+Q4K_BYTES = 144
+
+STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN",
+          4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA"}
+EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemm",
+           "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_get_device_error")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Q4KError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_str(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libq4k.so with argument types declared (raises if not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run python -m bit_block_quantized_q4_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        L.q4k_abi_version.restype = ctypes.c_int
+        L.q4k_abi_version.argtypes = []
+        L.q4k_status_str.restype = ctypes.c_char_p
+        L.q4k_status_str.argtypes = [ctypes.c_int]
+        L.q4k_dequant.restype = ctypes.c_int
+        L.q4k_dequant.argtypes = [P, I64, I64, P, ctypes.c_int, P]
+        L.q4k_gemv.restype = ctypes.c_int
+        L.q4k_gemv.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_gemm.restype = ctypes.c_int
+        L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_moe_workspace_size.restype = SZ
+        L.q4k_moe_workspace_size.argtypes = [I32, I32, I32, I64, I64]
+        L.q4k_moe_gemv.restype = ctypes.c_int
+        L.q4k_moe_gemv.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
+                                   P, SZ, P]
+        L.q4k_get_device_error.restype = ctypes.c_int
+        L.q4k_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        _lib = L
+        return L
+
+
+def status_str(status: int) -> str:
+    try:
+        return lib().q4k_status_str(int(status)).decode()
+    except RuntimeError:
+        return "library not built"
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise Q4KError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def q4k_abi_version() -> int:
+    return int(lib().q4k_abi_version())
+
+
+def q4k_dequant(w: torch.Tensor, n: int, k: int, out_dtype=torch.float32, out=None, stream=None):
+    """Dense N x K weights (fp32 or bf16) from an N x K Q4_K matrix on the GPU."""
+    if out is None:
+        out = torch.empty((n, k), dtype=out_dtype, device=w.device)
+    code = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
+    _check(lib().q4k_dequant(_ptr(w), n, k, _ptr(out), code, _stream(stream)), "q4k_dequant")
+    return out
+
+
+def q4k_gemv(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=None):
+    """Y[b] = W X[b] for X of shape [batch, K] (or [K]) bf16; returns fp32 [batch, N]."""
+    x2 = x.unsqueeze(0) if x.dim() == 1 else x
+    batch = x2.shape[0]
+    if out is None:
+        out = torch.empty((batch, n), dtype=torch.float32, device=x.device)
+    _check(lib().q4k_gemv(_ptr(w), n, k, _ptr(x2), batch, x2.stride(0), _ptr(out), out.stride(0),
+                          _stream(stream)), "q4k_gemv")
+    return out[0] if x.dim() == 1 else out
+
+
+def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=None):
+    """Y = X W^T for X [M, K] bf16; returns bf16 [M, N]."""
+    m = x.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().q4k_gemm(_ptr(w), n, k, _ptr(x), m, x.stride(0), _ptr(out), out.stride(0),
+                          _stream(stream)), "q4k_gemm")
+    return out
+
+
+def q4k_moe_workspace_size(n_experts: int, n_tokens: int, top_k: int, hidden: int, ffn: int) -> int:
+    return int(lib().q4k_moe_workspace_size(n_experts, n_tokens, top_k, hidden, ffn))
+
+
+def q4k_moe_gemv(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,
+                 x: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor, out=None, workspace=None,
+                 stream=None):
+    """Routed-expert FFN for decode tokens; returns fp32 [T, hidden]."""
+    T, top_k = ids.shape
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x.device)
+    ws_bytes = q4k_moe_workspace_size(n_experts, T, top_k, hidden, ffn)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().q4k_moe_gemv(_ptr(w_gate), _ptr(w_up), _ptr(w_down), expert_stride, n_experts,
+                              hidden, ffn, _ptr(x), T, x.stride(0), _ptr(ids), _ptr(wts), top_k,
+                              _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
+                              _stream(stream)), "q4k_moe_gemv")
+    return out
+
+
+def q4k_get_device_error(stream=None) -> int:
+    """Synchronizes the stream, returns and clears the device error word."""
+    bits = ctypes.c_uint32(0)
+    st = lib().q4k_get_device_error(_stream(stream), ctypes.byref(bits))
+    if st not in (0, 7):
+        raise Q4KError(st, "q4k_get_device_error")
+    return int(bits.value)

@@ -1,0 +1,203 @@
+// q4k_api.cu -- the extern "C" boundary of libq4k.so (declared in
+// include/q4k.h): argument checks, device checks, launch, error mapping.
+//
+// "spec: specialized model runtimes", section "Architecture": the runtime is
+// loaded in-process behind a C ABI; section "Prototype ABI scope": every
+// failure returns a clean value its caller already handles (no exceptions, no
+// aborts cross this boundary); section "Correctness and control": FFI pointer,
+// length and error-path behaviour is tested.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/q4k.h"
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+__device__ unsigned int g_device_error = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceFacts g_facts[kMaxDevices];
+std::once_flag g_facts_once[kMaxDevices];
+unsigned *g_err_ptr[kMaxDevices];
+std::once_flag g_err_once[kMaxDevices];
+
+void resolve_error_word(int dev) {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_ptr[dev] = static_cast<unsigned *>(p);
+}
+
+void query_facts(int dev) {
+  DeviceFacts &f = g_facts[dev];
+  f.device = dev;
+  cudaDeviceGetAttribute(&f.major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&f.minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&f.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&f.max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&f.l2_bytes, cudaDevAttrL2CacheSize, dev);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void resolve_encode() {
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device check shared by every compute entry point.
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q4K_ERR_CUDA;
+  const DeviceFacts *f = device_facts();
+  if (f->major != 10 || f->minor != 3) return Q4K_ERR_DEVICE;
+  return Q4K_OK;
+}
+
+int map_launch(cudaError_t e) { return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA; }
+
+}  // namespace
+
+const DeviceFacts *device_facts() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(g_facts_once[dev], query_facts, dev);
+  return &g_facts[dev];
+}
+
+unsigned *device_error_word() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_err_once[dev], resolve_error_word, dev);
+  return g_err_ptr[dev];
+}
+
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, void *addr,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                      CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (!g_encode) return CUDA_ERROR_NOT_FOUND;
+  cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+  return g_encode(map, type, rank, addr, reinterpret_cast<const cuuint64_t *>(dims),
+                  reinterpret_cast<const cuuint64_t *>(strides_bytes),
+                  reinterpret_cast<const cuuint32_t *>(box), elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace q4k
+
+using namespace q4k;
+
+extern "C" {
+
+int q4k_abi_version(void) { return Q4K_ABI_VERSION; }
+
+const char *q4k_status_str(int status) {
+  switch (status) {
+    case Q4K_OK: return "ok";
+    case Q4K_ERR_NULL: return "null pointer";
+    case Q4K_ERR_SHAPE: return "bad shape";
+    case Q4K_ERR_ALIGN: return "misaligned pointer or stride";
+    case Q4K_ERR_WORKSPACE: return "workspace missing or too small";
+    case Q4K_ERR_DEVICE: return "device is not sm_103";
+    case Q4K_ERR_CUDA: return "CUDA error";
+    case Q4K_ERR_DATA: return "a kernel reported bad data";
+    default: return "unknown status";
+  }
+}
+
+int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, void *stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || (out_dtype != 0 && out_dtype != 1)) return Q4K_ERR_SHAPE;
+  if (n == 0) return Q4K_OK;
+  if (!w || !out) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(out, 16)) return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_dequant(w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+             float *y, int64_t ldy, void *stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || batch < 0 || batch > 16) return Q4K_ERR_SHAPE;
+  if (n > INT32_MAX / 2 || k / kQK > INT32_MAX / kBlockBytes) return Q4K_ERR_SHAPE;
+  if (n == 0 || batch == 0) return Q4K_OK;
+  if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
+  if (!w || !x || !y) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4) || (ldx % 8) != 0) return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_gemv(w, n, k, x, batch, ldx, y, ldy, static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx, void *y,
+             int64_t ldy, void *stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || m < 0) return Q4K_ERR_SHAPE;
+  if (n > INT32_MAX / 2 || m > INT32_MAX / 2 || k > INT32_MAX / 2) return Q4K_ERR_SHAPE;
+  if (n == 0 || m == 0) return Q4K_OK;
+  if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
+  if (!w || !x || !y) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 16) || (ldx % 8) != 0 || (ldy % 8) != 0)
+    return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_gemm(w, n, k, x, m, ldx, y, ldy, static_cast<cudaStream_t>(stream)));
+}
+
+size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                              int64_t ffn) {
+  if (n_experts <= 0 || n_tokens < 0 || top_k <= 0 || hidden <= 0 || ffn <= 0) return 0;
+  return moe_workspace_size(n_experts, n_tokens, top_k, hidden, ffn);
+}
+
+int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64_t expert_stride,
+                 int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
+                 int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,
+                 int64_t ldy, void *workspace, size_t workspace_bytes, void *stream) {
+  if (n_experts <= 0 || hidden <= 0 || ffn <= 0 || (hidden % kQK) || (ffn % kQK) || n_tokens < 0 ||
+      n_tokens > 64 || top_k < 1 || top_k > 16)
+    return Q4K_ERR_SHAPE;
+  if (hidden > (1 << 20) || ffn > (1 << 20)) return Q4K_ERR_SHAPE;
+  if (expert_stride < (ffn * hidden / kQK) * kBlockBytes) return Q4K_ERR_SHAPE;
+  if (n_tokens == 0) return Q4K_OK;
+  if (ldx < hidden || ldy < hidden) return Q4K_ERR_SHAPE;
+  if (!w_gate || !w_up || !w_down || !x || !ids || !wts || !y) return Q4K_ERR_NULL;
+  if (!workspace ||
+      workspace_bytes < moe_workspace_size(n_experts, n_tokens, top_k, hidden, ffn))
+    return Q4K_ERR_WORKSPACE;
+  if (!aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) || (expert_stride % 16) ||
+      !aligned(x, 16) || (ldx % 8) || !aligned(y, 4) || !aligned(ids, 4) || !aligned(wts, 4) ||
+      !aligned(workspace, 16))
+    return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x,
+                               n_tokens, ldx, ids, wts, top_k, y, ldy, workspace,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_get_device_error(void *stream, uint32_t *bits) {
+  if (!bits) return Q4K_ERR_NULL;
+  *bits = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return Q4K_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return Q4K_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return Q4K_ERR_CUDA;
+  *bits = v;
+  return v ? Q4K_ERR_DATA : Q4K_OK;
+}
+
+}  // extern "C"

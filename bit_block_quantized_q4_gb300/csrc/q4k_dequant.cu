@@ -1,0 +1,82 @@
+// q4k_dequant.cu -- Q4_K -> fp32 / bf16 expansion ("spec: specialized model
+// runtimes", section "Architecture": the quant/dequant op of kernel tier T0).
+//
+// One warp per 144-byte super-block; lane i produces weights 8i .. 8i+7, which
+// all sit in sub-block j = i/4 and come from the 8 quant bytes 8(i%4) .. +7 of
+// chunk j/2 (low nibbles for even j, high nibbles for odd j).  The weight is
+// fma(d*sc_j, q, -dmin*m_j): d*sc_j and dmin*m_j are exact in fp32 (at most 17
+// significant bits), d*sc_j*q is exact (at most 21 bits), so the single rounding
+// of the fma is the round-to-nearest-even of the exact weight.  bf16 output
+// rounds that fp32 value to nearest even.  Streaming kernel: 144 B in, 1024 B
+// (fp32) or 512 B (bf16) out per super-block, fully coalesced 16-byte accesses.
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+template <int OUT_BF16>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w,
+                                                      int64_t nblocks, void *__restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int j = lane >> 2;            // sub-block
+  const int c = j >> 1;               // 32-byte quant chunk
+  const int shift = (j & 1) * 4;      // low or high nibbles
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks;
+       b += warps_total) {
+    const uint8_t *blk = w + b * kBlockBytes;
+    const uint4 h = __ldg(reinterpret_cast<const uint4 *>(blk));
+    const uint2 q8 = __ldg(reinterpret_cast<const uint2 *>(blk + kQsOffset + 32 * c + 8 * (lane & 3)));
+    uint32_t sc_lo, sc_hi, m_lo, m_hi;
+    scales_all(h.y, h.z, h.w, &sc_lo, &sc_hi, &m_lo, &m_hi);
+    const uint32_t scw = (j < 4) ? sc_lo : sc_hi;
+    const uint32_t mw = (j < 4) ? m_lo : m_hi;
+    const uint32_t sc = (scw >> (8 * (j & 3))) & 0xFFu;
+    const uint32_t mm = (mw >> (8 * (j & 3))) & 0xFFu;
+    const float ds = half_lo_to_float(h.x) * (float)sc;   // exact
+    const float dm = half_hi_to_float(h.x) * (float)mm;   // exact
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t word = e < 4 ? q8.x : q8.y;
+      const uint32_t q = (word >> (8 * (e & 3) + shift)) & 15u;
+      v[e] = fmaf(ds, (float)q, -dm);
+    }
+    if (OUT_BF16) {
+      uint4 o;
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
+      o.x = *reinterpret_cast<uint32_t *>(&p0);
+      o.y = *reinterpret_cast<uint32_t *>(&p1);
+      o.z = *reinterpret_cast<uint32_t *>(&p2);
+      o.w = *reinterpret_cast<uint32_t *>(&p3);
+      reinterpret_cast<uint4 *>(out)[b * 32 + lane] = o;
+    } else {
+      float4 *o = reinterpret_cast<float4 *>(out) + (b * 64 + lane * 2);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
+cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype,
+                           cudaStream_t stream) {
+  const DeviceFacts *f = device_facts();
+  const int64_t nblocks = n * (k / kQK);
+  const int warps_per_cta = 8;
+  int64_t grid = (nblocks + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = (int64_t)f->sm_count * 16;
+  if (grid > cap) grid = cap;
+  if (out_dtype == 1) {
+    dequant_kernel<1><<<(unsigned)grid, warps_per_cta * 32, 0, stream>>>(
+        static_cast<const uint8_t *>(w), nblocks, out);
+  } else {
+    dequant_kernel<0><<<(unsigned)grid, warps_per_cta * 32, 0, stream>>>(
+        static_cast<const uint8_t *>(w), nblocks, out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace q4k

@@ -1,0 +1,171 @@
+// q4k_device.cuh -- device-side building blocks shared by the sm_103a kernels:
+// the Q4_K block geometry, inline-PTX wrappers (mma.sync, mbarrier, TMA), the
+// bounded waits and the device error word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4k {
+
+constexpr int kQK = 256;          // weights per super-block
+constexpr int kBlockBytes = 144;  // bytes per super-block
+constexpr int kQsOffset = 16;     // first quant byte within a super-block
+
+// Device error word (bits Q4K_DEVERR_*): one per device, defined in q4k_api.cu;
+// kernels receive its address as an argument.
+constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrBadExpert = 2u;
+
+__device__ __forceinline__ void set_device_error(unsigned *err, unsigned bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Upper bound on mbarrier polls before a wait gives up (each poll may suspend
+// for a short hardware-chosen time, so this is of the order of a second).
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ----------------------------------------------------------------- mma.sync
+// D = A * B + C, m16n8k16, bf16 operands, fp32 accumulate.
+// A fragment: a[0] (row g, k 2t..2t+1), a[1] (row g+8, k 2t..), a[2] (row g,
+// k 2t+8..), a[3] (row g+8, k 2t+8..); B: b0 (k 2t.., col g), b1 (k 2t+8.., col
+// g); C/D: c[0..1] (row g, cols 2t..2t+1), c[2..3] (row g+8); g = lane/4,
+// t = lane%4, the lower k / column index in the low half of each register.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ----------------------------------------------------------------- nibbles
+// bf16 0x4300 is 128.0 with a unit last place, so (0x4300 | q) is exactly
+// 128 + q for q < 16.  These turn the low nibbles of bytes 0 and 2 of a word
+// (or the nibbles selected by a prior shift) into a bf16 pair (128+q0, 128+q2).
+constexpr uint32_t kBf16Magic = 0x43004300u;
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w) { return (w & 0x000F000Fu) | kBf16Magic; }
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
+  return ((w >> 4) & 0x000F000Fu) | kBf16Magic;
+}
+
+// ----------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar`; gives up after kSpinLimit polls, sets the
+// timeout bit of the device error word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  set_device_error(err, kDevErrTimeout);
+  return false;
+}
+
+// ----------------------------------------------------------------- TMA
+// Tiled tensor copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+// L2 policy for data read exactly once (weights streamed from HBM).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+
+// Prefetch a tensor map descriptor into the constant cache.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ----------------------------------------------------------------- scales
+// Scales and mins of sub-blocks 2t and 2t+1 (t = 0..3) of one super-block,
+// from its header words h1 = s[0..3], h2 = s[4..7], h3 = s[8..11].
+// Returns sc_{2t} | sc_{2t+1} << 8 in *sc2 and the mins likewise in *m2.
+__device__ __forceinline__ void scales_pair(uint32_t h1, uint32_t h2, uint32_t h3, int t,
+                                            uint32_t *sc2, uint32_t *m2) {
+  const uint32_t sh = (t & 1) * 16;  // byte 2(t&1) of the word
+  const uint32_t p1 = h1 >> sh, p2 = h2 >> sh, p3 = h3 >> sh;
+  if (t < 2) {  // sub-blocks 0..3: low six bits of s[j], s[j+4]
+    *sc2 = p1 & 0x3F3Fu;
+    *m2 = p2 & 0x3F3Fu;
+  } else {  // sub-blocks 4..7: low/high nibble of s[j+4], top two bits of s[j-4], s[j]
+    *sc2 = (p3 & 0x0F0Fu) | ((p1 >> 2) & 0x3030u);
+    *m2 = ((p3 >> 4) & 0x0F0Fu) | ((p2 >> 2) & 0x3030u);
+  }
+}
+
+// All eight scales/mins of a super-block: sc_j = byte j of (*sc_lo, *sc_hi)
+// (bytes 0..3 in lo, 4..7 in hi), mins likewise.
+__device__ __forceinline__ void scales_all(uint32_t h1, uint32_t h2, uint32_t h3, uint32_t *sc_lo,
+                                           uint32_t *sc_hi, uint32_t *m_lo, uint32_t *m_hi) {
+  *sc_lo = h1 & 0x3F3F3F3Fu;
+  *m_lo = h2 & 0x3F3F3F3Fu;
+  *sc_hi = (h3 & 0x0F0F0F0Fu) | ((h1 >> 2) & 0x30303030u);
+  *m_hi = ((h3 >> 4) & 0x0F0F0F0Fu) | ((h2 >> 2) & 0x30303030u);
+}
+
+__device__ __forceinline__ float half_lo_to_float(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi_to_float(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+}
+
+}  // namespace q4k

@@ -1,0 +1,545 @@
+// q4k_gemv.cu -- decode projection Y[b] = W X[b] for batch 1..16 with W in
+// Q4_K ("spec: specialized model runtimes", sections "Architecture" (T0 GEMM,
+// quant/dequant) and "Development sequence" (decode throughput); batched decode
+// steps: "PRD: Performant Concurrent Distributed GGUF Runtime", DGR-012).
+//
+// The weights are streamed from HBM exactly once.  Each warp owns 16*MT output
+// rows and a contiguous slice of super-blocks; a private ring of shared-memory
+// stages is filled by TMA (one 3-D box = 16*MT rows x one 144-byte
+// super-block per stage).  In registers, a 4-bit quant q becomes the bf16
+// value 128+q with one AND/OR (exact), and the contraction runs on the tensor
+// cores (mma.sync m16n8k16, bf16 x bf16 products are exact, fp32 accumulate):
+//     sum_i (d sc_j q_i - dmin m_j) x_i
+//         = d sc_j (sum_i (128+q_i) x_i - 128 X_j) - dmin m_j X_j,
+// X_j = sum_i x_i over sub-block j.  128 X_j is produced by the same MMA
+// path with a constant A = 128, so a sub-block whose quants are all zero
+// cancels exactly.  Per-sub-block scales are applied in fp32 once per
+// (row, sub-block, batch column).
+//
+// Batch 1: the eight MMA columns carry the eight sub-blocks of a super-block
+// (column j of B holds x only in the k-slots that carry sub-block j), so one
+// super-block needs 16 MMAs per 16 rows and each thread ends with exactly the
+// (row, sub-block) sums whose scales it decodes itself.
+// Batch 2..16: the MMA columns carry the batch rows (one or two n-tiles of 8);
+// every sub-block is its own 2-step accumulation and the scales are shared
+// within a thread quad by shuffles.
+//
+// Split-K: the warps of a CTA take consecutive super-block slices of the same
+// rows; partial sums meet in shared memory and are added in warp order, so the
+// result is deterministic.  Grids are sized so that every CTA is resident at
+// once (one wave) whenever the shape allows.
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+// Tuning knobs (compile time).
+#ifndef Q4K_GEMV_STAGES
+#define Q4K_GEMV_STAGES 3
+#endif
+#ifndef Q4K_GEMV_PROMO  // L2 promotion of the weight tensor map: 0 none, 1 128 B, 2 256 B
+#define Q4K_GEMV_PROMO 2
+#endif
+#ifndef Q4K_GEMV_EVICT_FIRST  // L2 evict-first hint on weight loads
+#define Q4K_GEMV_EVICT_FIRST 1
+#endif
+
+namespace q4k {
+
+namespace {
+
+constexpr int kRowsPerTile = 16;
+constexpr int kTileBytes = kRowsPerTile * kBlockBytes;  // 2304, a multiple of 128
+
+struct GemvArgs {
+  const __nv_bfloat16 *x;
+  float *y;
+  int64_t ldx, ldy;
+  int n;        // rows
+  int nsb;      // super-blocks per row
+  int ks;       // super-blocks per warp
+  int batch;
+  int warp_bytes;  // shared bytes per warp region
+  unsigned *err;   // device error word
+};
+
+__device__ __forceinline__ void load_tile(void *dst, const CUtensorMap *map, uint64_t *bar, int sb,
+                                          int row0, uint64_t policy) {
+#if Q4K_GEMV_EVICT_FIRST
+  tma_load_3d_hint(dst, map, bar, 0, sb, row0, policy);
+#else
+  (void)policy;
+  tma_load_3d(dst, map, bar, 0, sb, row0);
+#endif
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// ---------------------------------------------------------------- batch 1
+// Shared memory per warp: STAGES weight tiles | x of the warp's slice,
+// permuted so that word 2q of a sub-block holds (x[4q], x[4q+2]) and word 2q+1
+// holds (x[4q+1], x[4q+3]) | 16 zero words | STAGES mbarriers.
+template <int MT, int STAGES>
+__global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                      const GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int row0 = blockIdx.x * (MT * kRowsPerTile);
+  const int sb0 = warp * a.ks;
+  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);
+
+  uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
+  uint8_t *ring = wreg;
+  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * MT * kTileBytes);
+  uint32_t *xzero = xperm + a.ks * 128;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);
+  float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
+
+  if (lane == 0) {
+    prefetch_tmap(&wmap);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t policy = l2_evict_first_policy();
+  if (lane == 0) {
+    for (int s = 0; s < STAGES && s < nsteps; ++s) {
+      mbar_arrive_expect_tx(&bars[s], MT * kTileBytes);
+      load_tile(ring + s * MT * kTileBytes, &wmap, &bars[s], sb0 + s, row0, policy);
+    }
+  }
+  // x slice -> permuted shared copy (8 values per lane per iteration).
+  {
+    const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + (int64_t)sb0 * kQK);
+    for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
+      const uint4 u = __ldg(xs + c8);
+      uint4 o;
+      o.x = __byte_perm(u.x, u.y, 0x5410);
+      o.y = __byte_perm(u.x, u.y, 0x7632);
+      o.z = __byte_perm(u.z, u.w, 0x5410);
+      o.w = __byte_perm(u.z, u.w, 0x7632);
+      reinterpret_cast<uint4 *>(xperm)[c8] = o;
+    }
+    if (lane < 16) xzero[lane] = 0u;
+  }
+  __syncwarp();
+
+  // B fragments: lane (g, t) carries sub-block g iff g/2 == t, in b0 for even g
+  // and in b1 for odd g; every other lane feeds zeros.
+  const bool own = (t == (g >> 1));
+  const uint32_t *pb0 = (own && !(g & 1)) ? xperm + g * 16 : xzero;
+  const uint32_t *pb1 = (own && (g & 1)) ? xperm + g * 16 : xzero;
+  const int adv0 = (own && !(g & 1)) ? 128 : 0;
+  const int adv1 = (own && (g & 1)) ? 128 : 0;
+
+  float yacc[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) yacc[mt][0] = yacc[mt][1] = 0.f;
+
+  bool ok = true;
+  for (int i = 0; i < nsteps; ++i) {
+    const int stage = i % STAGES;
+    if (!mbar_wait(&bars[stage], (uint32_t)((i / STAGES) & 1), a.err)) {
+      ok = false;
+      break;
+    }
+    const uint8_t *st = ring + stage * MT * kTileBytes;
+    uint4 hdr[MT][2], qa[MT][2][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kBlockBytes;
+        hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
+        qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
+        qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + STAGES < nsteps) {
+      mbar_arrive_expect_tx(&bars[stage], MT * kTileBytes);
+      load_tile(ring + stage * MT * kTileBytes, &wmap, &bars[stage], sb0 + i + STAGES, row0, policy);
+    }
+
+    float acc[MT][4];
+    float c128[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    const uint32_t *p0 = pb0 + i * adv0;
+    const uint32_t *p1 = pb1 + i * adv1;
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      const uint4 bb0 = reinterpret_cast<const uint4 *>(p0)[G];
+      const uint4 bb1 = reinterpret_cast<const uint4 *>(p1)[G];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int wi = 2 * G + (e >> 1);      // quant word (4 bytes of the chunk)
+        const int sh = (e & 1) * 8;           // positions (o, o+2) or (o+1, o+3)
+        const uint32_t b0 = word_of(bb0, e), b1 = word_of(bb1, e);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t w0 = word_of(qa[mt][0][wi >> 2], wi & 3) >> sh;
+          const uint32_t w1 = word_of(qa[mt][1][wi >> 2], wi & 3) >> sh;
+          mma_bf16(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
+        }
+        mma_bf16(c128, kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0, b1);
+      }
+    }
+    // c128[0], c128[1] = 128 X of sub-blocks 2t, 2t+1.
+    const float X0 = c128[0] * (1.f / 128.f), X1 = c128[1] * (1.f / 128.f);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint4 h = hdr[mt][r];
+        uint32_t sc2, m2;
+        scales_pair(h.y, h.z, h.w, t, &sc2, &m2);
+        const float d = half_lo_to_float(h.x), dmin = half_hi_to_float(h.x);
+        const float ta = acc[mt][2 * r] - c128[0];
+        const float tb = acc[mt][2 * r + 1] - c128[1];
+        const float u = fmaf((float)(sc2 >> 8), tb, (float)(sc2 & 0xFFu) * ta);
+        const float v = fmaf((float)(m2 >> 8), X1, (float)(m2 & 0xFFu) * X0);
+        yacc[mt][r] = fmaf(d, u, yacc[mt][r]);
+        yacc[mt][r] = fmaf(-dmin, v, yacc[mt][r]);
+      }
+    }
+  }
+
+  // Quad reduction (sub-blocks 2t, 2t+1 -> the row), then across warps.
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float v = yacc[mt][r];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
+    }
+  }
+  __syncwarp();
+  if (!ok && lane == 0) red[warp * (MT * kRowsPerTile)] = __int_as_float(0x7fc00000);
+  __syncthreads();
+  if (threadIdx.x < MT * kRowsPerTile) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red[w * (MT * kRowsPerTile) + threadIdx.x];
+    const int row = row0 + threadIdx.x;
+    if (row < a.n) a.y[row] = s;
+  }
+}
+
+// ---------------------------------------------------------------- batch 2..16
+// MMA columns = batch rows (NT n-tiles of 8).  Sub-block j = 2c+hi, step s:
+// thread t's k-slots (2t, 2t+1) carry positions (o, o+2) and (2t+8, 2t+9)
+// positions (o+1, o+3), o = 8t + 4s, i.e. quant bytes 8t .. 8t+7 of chunk c.
+template <int MT, int NT, int STAGES>
+__global__ void __launch_bounds__(512) gemv_bn_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                      const GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int row0 = blockIdx.x * (MT * kRowsPerTile);
+  const int sb0 = warp * a.ks;
+  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);
+  constexpr int kCols = NT * 8;
+
+  uint8_t *ring = smem + (size_t)warp * a.warp_bytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + STAGES * MT * kTileBytes);
+  float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
+
+  if (lane == 0) {
+    prefetch_tmap(&wmap);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t policy = l2_evict_first_policy();
+  if (lane == 0) {
+    for (int s = 0; s < STAGES && s < nsteps; ++s) {
+      mbar_arrive_expect_tx(&bars[s], MT * kTileBytes);
+      load_tile(ring + s * MT * kTileBytes, &wmap, &bars[s], sb0 + s, row0, policy);
+    }
+  }
+  // x rows of this lane's batch columns (g and g+8); rows past the batch read
+  // zeros.
+  const uint4 *xrow[NT];
+  bool xval[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int b = nt * 8 + g;
+    xval[nt] = b < a.batch;
+    xrow[nt] = reinterpret_cast<const uint4 *>(a.x + (int64_t)(xval[nt] ? b : 0) * a.ldx);
+  }
+
+  float yacc[MT][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) yacc[mt][nt][0] = yacc[mt][nt][1] = yacc[mt][nt][2] = yacc[mt][nt][3] = 0.f;
+
+  bool ok = true;
+  for (int i = 0; i < nsteps; ++i) {
+    const int stage = i % STAGES;
+    const int sb = sb0 + i;
+    if (!mbar_wait(&bars[stage], (uint32_t)((i / STAGES) & 1), a.err)) {
+      ok = false;
+      break;
+    }
+    const uint8_t *st = ring + stage * MT * kTileBytes;
+    uint4 hdr[MT][2];
+    uint2 qw[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kBlockBytes;
+        hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          qw[mt][r][c] = *reinterpret_cast<const uint2 *>(rp + kQsOffset + 32 * c + 8 * t);
+      }
+    __syncwarp();
+    if (lane == 0 && i + STAGES < nsteps) {
+      mbar_arrive_expect_tx(&bars[stage], MT * kTileBytes);
+      load_tile(ring + stage * MT * kTileBytes, &wmap, &bars[stage], sb + STAGES, row0, policy);
+    }
+    // This lane decodes sub-blocks 2t, 2t+1 of rows g, g+8 (per m-tile).
+    float dsA[MT][2], dsB[MT][2], dmA[MT][2], dmB[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        uint32_t sc2, m2;
+        scales_pair(hdr[mt][r].y, hdr[mt][r].z, hdr[mt][r].w, t, &sc2, &m2);
+        const float d = half_lo_to_float(hdr[mt][r].x), dmin = half_hi_to_float(hdr[mt][r].x);
+        dsA[mt][r] = d * (float)(sc2 & 0xFFu);
+        dsB[mt][r] = d * (float)(sc2 >> 8);
+        dmA[mt][r] = dmin * (float)(m2 & 0xFFu) * (1.f / 128.f);
+        dmB[mt][r] = dmin * (float)(m2 >> 8) * (1.f / 128.f);
+      }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = j >> 1;
+      const bool hi = j & 1;
+      // x of this sub-block: positions 8t .. 8t+7 of the lane's batch rows.
+      uint4 xv[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        xv[nt] = xval[nt] ? __ldg(xrow[nt] + ((int64_t)sb * kQK + 32 * j + 8 * t) / 8)
+                          : make_uint4(0, 0, 0, 0);
+      float acc[MT][NT][4];
+      float c128[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        c128[nt][0] = c128[nt][1] = c128[nt][2] = c128[nt][3] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+      }
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t lo = s ? xv[nt].z : xv[nt].x;
+          const uint32_t hi2 = s ? xv[nt].w : xv[nt].y;
+          b0[nt] = __byte_perm(lo, hi2, 0x5410);
+          b1[nt] = __byte_perm(lo, hi2, 0x7632);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t w0 = s ? qw[mt][0][c].y : qw[mt][0][c].x;
+          const uint32_t w1 = s ? qw[mt][1][c].y : qw[mt][1][c].x;
+          const uint32_t a0 = hi ? nib_hi(w0) : nib_lo(w0);
+          const uint32_t a1 = hi ? nib_hi(w1) : nib_lo(w1);
+          const uint32_t a2 = hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8);
+          const uint32_t a3 = hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16(c128[nt], kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0[nt], b1[nt]);
+      }
+      // Scales of sub-block j for rows g, g+8 live in lane (g, j/2).
+      const int src = (lane & ~3) | (j >> 1);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mt][r] : dsA[mt][r], src);
+          const float dm = __shfl_sync(0xffffffffu, hi ? dmB[mt][r] : dmA[mt][r], src);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float cv = acc[mt][nt][2 * r + e];
+              const float c1 = c128[nt][e];
+              yacc[mt][nt][2 * r + e] = fmaf(ds, cv - c1, yacc[mt][nt][2 * r + e]);
+              yacc[mt][nt][2 * r + e] = fmaf(-dm, c1, yacc[mt][nt][2 * r + e]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // Across warps: red[warp][row][col].
+  const int tile_rows = MT * kRowsPerTile;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = mt * kRowsPerTile + g + 8 * (e >> 1);
+        const int col = nt * 8 + 2 * t + (e & 1);
+        red[(warp * tile_rows + row) * kCols + col] = yacc[mt][nt][e];
+      }
+  __syncwarp();
+  if (!ok && lane == 0) red[(warp * tile_rows) * kCols] = __int_as_float(0x7fc00000);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < tile_rows * kCols; idx += blockDim.x) {
+    const int row = idx / kCols, col = idx % kCols;
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red[(w * tile_rows + row) * kCols + col];
+    const int grow = row0 + row;
+    if (grow < a.n && col < a.batch) a.y[(int64_t)col * a.ldy + grow] = s;
+  }
+}
+
+// ---------------------------------------------------------------- launch
+constexpr int kStages = Q4K_GEMV_STAGES;
+
+struct Plan {
+  int mt = 1, wk = 1, ks = 1, warp_bytes = 0, smem = 0, grid = 0;
+};
+
+int warp_bytes_b1(int mt, int ks) {
+  int b = kStages * mt * kTileBytes + ks * 512 + 64 + kStages * 8;
+  return (b + 127) / 128 * 128;
+}
+int warp_bytes_bn(int mt) {
+  int b = kStages * mt * kTileBytes + kStages * 8;
+  return (b + 127) / 128 * 128;
+}
+
+template <typename K>
+int occupancy(K kernel, int threads, int smem) {
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess)
+    return 0;
+  return blocks;
+}
+
+// Choose the split of K across the warps of a CTA: prefer one resident wave,
+// then more warps in flight (up to 32 per SM), then an even split.
+template <typename K>
+Plan plan_for(K kernel, bool b1, int mt, int n, int nsb, int cols, const DeviceFacts *f) {
+  Plan best;
+  double best_score = -1e30;
+  const int tile_rows = mt * kRowsPerTile;
+  const int grid = (n + tile_rows - 1) / tile_rows;
+  for (int wk = 1; wk <= 16; ++wk) {
+    const int ks = (nsb + wk - 1) / wk;
+    if ((nsb + ks - 1) / ks != wk) continue;  // no empty warps
+    if (ks < 2 && nsb >= 2) continue;
+    const int wb = b1 ? warp_bytes_b1(mt, ks) : warp_bytes_bn(mt);
+    const int smem = wk * wb + wk * tile_rows * cols * 4;
+    if (smem > f->max_smem_optin) continue;
+    const int occ = occupancy(kernel, wk * 32, smem);
+    if (occ <= 0) continue;
+    const int slots = occ * f->sm_count;
+    const int waves = (grid + slots - 1) / slots;
+    const int per_sm = std::min(occ, (grid + f->sm_count - 1) / f->sm_count);
+    const int warps_sm = per_sm * wk;
+    const double balance = (double)nsb / (double)(ks * wk);  // 1.0 = even split
+    const double score = -1000.0 * waves + std::min(warps_sm, 32) + 8.0 * balance;
+    if (score > best_score) {
+      best_score = score;
+      best.mt = mt;
+      best.wk = wk;
+      best.ks = ks;
+      best.warp_bytes = wb;
+      best.smem = smem;
+      best.grid = grid;
+    }
+  }
+  return best;
+}
+
+std::once_flag g_attr_once;
+
+template <typename K>
+void allow_smem(K kernel, const DeviceFacts *f) {
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f->max_smem_optin);
+}
+
+void set_attributes(const DeviceFacts *f) {
+  allow_smem(gemv_b1_kernel<1, kStages>, f);
+  allow_smem(gemv_b1_kernel<2, kStages>, f);
+  allow_smem(gemv_bn_kernel<1, 1, kStages>, f);
+  allow_smem(gemv_bn_kernel<1, 2, kStages>, f);
+  allow_smem(gemv_bn_kernel<2, 1, kStages>, f);
+  allow_smem(gemv_bn_kernel<2, 2, kStages>, f);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+                        int64_t ldx, float *y, int64_t ldy, cudaStream_t stream) {
+  const DeviceFacts *f = device_facts();
+  std::call_once(g_attr_once, set_attributes, f);
+  const int nsb = (int)(k / kQK);
+  const int mt = (batch == 1) ? (n >= 32 * f->sm_count * 2 ? 2 : 1) : (n >= 32 * f->sm_count ? 2 : 1);
+
+  // W viewed as [n rows][nsb super-blocks][144 bytes].
+  CUtensorMap map;
+  const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
+  const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)(mt * kRowsPerTile)};
+  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
+                   box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   Q4K_GEMV_PROMO == 0   ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                   : Q4K_GEMV_PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                         : CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  GemvArgs args;
+  args.x = static_cast<const __nv_bfloat16 *>(x);
+  args.y = y;
+  args.ldx = ldx;
+  args.ldy = ldy;
+  args.n = (int)n;
+  args.nsb = nsb;
+  args.batch = (int)batch;
+  args.err = device_error_word();
+
+  if (batch == 1) {
+    auto kern = (mt == 2) ? gemv_b1_kernel<2, kStages> : gemv_b1_kernel<1, kStages>;
+    const Plan p = plan_for(kern, true, mt, (int)n, nsb, 1, f);
+    if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    args.ks = p.ks;
+    args.warp_bytes = p.warp_bytes;
+    kern<<<p.grid, p.wk * 32, p.smem, stream>>>(map, args);
+  } else {
+    const int nt = batch <= 8 ? 1 : 2;
+    auto kern = (mt == 2) ? (nt == 1 ? gemv_bn_kernel<2, 1, kStages> : gemv_bn_kernel<2, 2, kStages>)
+                          : (nt == 1 ? gemv_bn_kernel<1, 1, kStages> : gemv_bn_kernel<1, 2, kStages>);
+    const Plan p = plan_for(kern, false, mt, (int)n, nsb, nt * 8, f);
+    if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    args.ks = p.ks;
+    args.warp_bytes = p.warp_bytes;
+    kern<<<p.grid, p.wk * 32, p.smem, stream>>>(map, args);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace q4k

@@ -1,0 +1,48 @@
+// q4k_internal.h -- host-side declarations shared by the library's translation
+// units (launchers and the per-device facts they size their grids with).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace q4k {
+
+struct DeviceFacts {
+  int device = -1;
+  int major = 0, minor = 0;
+  int sm_count = 0;
+  int max_smem_optin = 0;     // bytes of dynamic shared memory a block may opt into
+  int max_smem_per_sm = 0;
+  int l2_bytes = 0;
+};
+
+// Facts of the current device (queried once per device).
+const DeviceFacts *device_facts();
+
+// Device address of the current device's error word (Q4K_DEVERR_* bits).
+unsigned *device_error_word();
+
+// cuTensorMapEncodeTiled, resolved from the driver once.
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, void *addr,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                      CUtensorMapSwizzle swizzle,
+                      CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+
+cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype,
+                           cudaStream_t stream);
+cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+                        int64_t ldx, float *y, int64_t ldy, cudaStream_t stream);
+cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
+                        void *y, int64_t ldy, cudaStream_t stream);
+size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                          int64_t ffn);
+cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
+                       int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                       const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                       const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
+                       cudaStream_t stream);
+
+}  // namespace q4k

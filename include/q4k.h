@@ -1,0 +1,180 @@
+/*
+ * q4k.h -- C ABI of the GB300 (sm_103a) Q4_K quantized-weight projection
+ * library (libq4k.so).
+ *
+ * What the library computes
+ *   The projection step of LLM serving with block-quantized weights: a weight
+ *   matrix stored as GGUF Q4_K super-blocks is dequantized and contracted with
+ *   bf16 activations.
+ *   - "spec: specialized model runtimes", section "Architecture": the kernel
+ *     tier T0 ("GEMM, attention/GDN, quant/dequant, norms, RoPE") is the source
+ *     of the expected speedup; the runtime is loaded in-process behind a C ABI;
+ *     section "Non-goals": no CPU offload and no multi-GPU inside one
+ *     specialization.
+ *   - "spec: specialized model runtimes", section "Prototype ABI scope": a
+ *     failing call returns a clean failure value that its caller handles.
+ *   - "Layer Package Repository Spec", sections "Repository Identity" and
+ *     "Repository Layout": the weight artifact is a Q4_K ("UD-Q4_K_XL") GGUF
+ *     model split into per-layer tensors, loaded directly.
+ *   - "Layer Package Repository Spec", section "Policy Resolution" (GLM MoE
+ *     fixture): a routed-FFN decode layer is dominated (96%) by the routed
+ *     gate/up/down expert matmuls, followed by a fused SwiGLU and the
+ *     route-weighted sum.
+ *
+ * Q4_K super-block (256 weights in 144 bytes, little-endian; the GGUF layout)
+ *    bytes   0..1   d     binary16      bytes 2..3  dmin  binary16
+ *    bytes   4..15  12 bytes holding eight 6-bit scales sc_j and mins m_j:
+ *                   j < 4:  sc_j = s[j] & 63,  m_j = s[j+4] & 63
+ *                   j >= 4: sc_j = (s[j+4] & 15) | ((s[j-4] >> 6) << 4)
+ *                           m_j  = (s[j+4] >> 4) | ((s[j]   >> 6) << 4)
+ *    bytes  16..143 128 bytes of 4-bit quants: byte 32c+l holds weight 64c+l
+ *                   (low nibble) and weight 64c+32+l (high nibble)
+ *    weight i (sub-block j = i/32):  w = d * sc_j * q - dmin * m_j
+ *
+ * Matrix layout: an N x K weight matrix (N outputs, K inputs, K a multiple of
+ * 256) is N rows of K/256 consecutive super-blocks, rows contiguous, so row r
+ * starts at byte r * (K/256) * 144.  y = W x.
+ *
+ * Conventions for every call
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer.  Outputs must not alias inputs.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on that stream and never synchronize, except
+ *     q4k_get_device_error.  They keep no per-call state and are thread-safe.
+ *   - Strides (ldx, ldy) are in elements.
+ *   - Argument errors are reported before anything is launched (nothing runs).
+ *     An empty problem (n == 0, batch/m/tokens == 0) returns Q4K_OK and
+ *     launches nothing.
+ *   - Kernels never trap.  Bad data found on the device (an expert id out of
+ *     range, a wait that gave up) sets a device-side error word, read and
+ *     cleared with q4k_get_device_error.
+ *   - Numerics: dequantized weights are the exact value rounded once to fp32
+ *     (q4k_dequant is bit-exact).  Contractions accumulate in fp32; GEMV and
+ *     MoE results satisfy |y - y_ref| <= 2e-3 * sum_k |w_k| |x_k| per element,
+ *     the prefill GEMM (bf16 tensor-core operands) 1e-2 * sum_k |w_k||x_k|.
+ */
+#ifndef Q4K_H
+#define Q4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4K_ABI_VERSION 1
+
+/* Return codes of every entry point. */
+enum q4k_status {
+    Q4K_OK = 0,
+    Q4K_ERR_NULL = 1,      /* a required pointer is NULL                              */
+    Q4K_ERR_SHAPE = 2,     /* K not a positive multiple of 256, negative size, batch
+                              out of range, stride smaller than the row              */
+    Q4K_ERR_ALIGN = 3,     /* a pointer or stride breaks the alignment stated below   */
+    Q4K_ERR_WORKSPACE = 4, /* workspace NULL or smaller than the size query says      */
+    Q4K_ERR_DEVICE = 5,    /* current device is not sm_103 (GB300)                    */
+    Q4K_ERR_CUDA = 6,      /* a CUDA call or kernel launch failed                      */
+    Q4K_ERR_DATA = 7       /* q4k_get_device_error: a kernel reported bad data         */
+};
+
+/* Bits of the device error word (q4k_get_device_error). */
+#define Q4K_DEVERR_TIMEOUT 1u    /* a bounded wait on an asynchronous copy gave up */
+#define Q4K_DEVERR_BAD_EXPERT 2u /* an expert id outside [0, n_experts) was skipped */
+
+int q4k_abi_version(void);
+const char *q4k_status_str(int status);
+
+/*
+ * q4k_dequant -- expand an N x K Q4_K matrix to dense weights.
+ * ("spec: specialized model runtimes", section "Architecture": the
+ *  quant/dequant op of kernel tier T0.)
+ *   w       device, N x K Q4_K (16-byte aligned)
+ *   out     device, N x K row-major; out_dtype 0 = fp32 (bit-exact: the exact
+ *           weight rounded once to nearest even), 1 = bf16 (that fp32 value
+ *           rounded to nearest even bf16).  16-byte aligned.
+ * Errors: NULL, SHAPE (k % 256, n < 0, out_dtype not 0/1), ALIGN, DEVICE, CUDA.
+ */
+int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, void *stream);
+
+/*
+ * q4k_gemv -- decode projection, Y[b, :] = W X[b, :] for b < batch, batch 1..16.
+ * ("spec: specialized model runtimes", sections "Architecture" (T0 GEMM) and
+ *  "Development sequence" (decode throughput is the metric); batching of decode
+ *  steps: "PRD: Performant Concurrent Distributed GGUF Runtime", DGR-012.)
+ * Each super-block is read from memory once and contracted with every batch row.
+ *   w       device, N x K Q4_K, 16-byte aligned
+ *   x       device, batch x K bf16, row stride ldx >= K; x 16-byte aligned and
+ *           ldx a multiple of 8
+ *   y       device, batch x N fp32, row stride ldy >= N; 4-byte aligned
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+             float *y, int64_t ldy, void *stream);
+
+/*
+ * q4k_gemm -- prefill projection, Y = X W^T for m tokens (any m >= 1).
+ * ("spec: specialized model runtimes", section "Feasibility gate": one
+ *  quantized GEMM; prefill throughput and TTFT are reported metrics in "PRD:
+ *  Performant Concurrent Distributed GGUF Runtime", DGR-001.)
+ * Weight tiles are dequantized to bf16 in shared memory and multiplied on the
+ * tensor cores (tcgen05) with fp32 accumulation; the output is rounded to bf16.
+ *   w       device, N x K Q4_K, 16-byte aligned
+ *   x       device, m x K bf16, row stride ldx >= K (ldx multiple of 8, x 16-byte
+ *           aligned)
+ *   y       device, m x N bf16, row stride ldy >= N (ldy multiple of 8, y 16-byte
+ *           aligned)
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
+             void *y, int64_t ldy, void *stream);
+
+/*
+ * q4k_moe_workspace_size -- bytes of device workspace q4k_moe_gemv needs.
+ */
+size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                              int64_t ffn);
+
+/*
+ * q4k_moe_gemv -- routed mixture-of-experts FFN for decode tokens.
+ * ("Layer Package Repository Spec", section "Policy Resolution": routed
+ *  gate/up/down expert matmuls, fused SwiGLU, route-weighted sum.)
+ * For token t and slot j with expert e = ids[t*top_k + j]:
+ *     h = silu(Wg_e x_t) * (Wu_e x_t)           (ffn values, fp32)
+ *     Y[t, :] = sum_j wts[t*top_k + j] * (Wd_e h)   (slots summed in order j)
+ * Tokens are grouped per expert so each active expert's weights are read once
+ * for all of its tokens.
+ *   w_gate, w_up   device; expert e's ffn x hidden Q4_K matrix starts at byte
+ *                  e * expert_stride
+ *   w_down         device; expert e's hidden x ffn Q4_K matrix starts at byte
+ *                  e * expert_stride
+ *   expert_stride  bytes, >= (ffn * hidden / 256) * 144, multiple of 16
+ *   hidden, ffn    multiples of 256
+ *   x              device, n_tokens x hidden bf16, row stride ldx (mult. of 8)
+ *   ids, wts       device, n_tokens x top_k int32 / fp32 (top_k 1..16, n_tokens
+ *                  1..64).  An id outside [0, n_experts) contributes nothing and
+ *                  sets Q4K_DEVERR_BAD_EXPERT.
+ *   y              device, n_tokens x hidden fp32, row stride ldy
+ *   workspace      device, >= q4k_moe_workspace_size(...) bytes, 16-byte aligned;
+ *                  no initial contents needed; calls sharing one workspace
+ *                  must not overlap on the GPU.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, DEVICE, CUDA.
+ */
+int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64_t expert_stride,
+                 int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
+                 int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,
+                 int64_t ldy, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q4k_get_device_error -- synchronize `stream`, return the device error word
+ * (Q4K_DEVERR_* bits) in *bits and clear it.  Returns Q4K_ERR_DATA when any bit
+ * was set, Q4K_OK otherwise, Q4K_ERR_NULL if bits is NULL, Q4K_ERR_CUDA on a
+ * CUDA failure.  The word is per device and shared by all calls on it.
+ */
+int q4k_get_device_error(void *stream, uint32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4K_H */

@@ -1,0 +1,139 @@
+"""The C-ABI boundary: the library loads, exports what include/q4k.h declares,
+and rejects bad arguments before launching anything ("spec: specialized model
+runtimes", section "Correctness and control": FFI pointer, length and
+error-path tests).  The CPU-only tests never reach a CUDA call: every argument
+error is reported before the device is touched.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4k.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_block_quantized_q4_gb300 import build
+    build.build()
+    import bit_block_quantized_q4_gb300 as q4k
+    return q4k.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4k_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls_and_helpers():
+    names = _declared()
+    for n in ("q4k_dequant", "q4k_gemv", "q4k_gemm", "q4k_moe_gemv", "q4k_moe_workspace_size",
+              "q4k_get_device_error", "q4k_abi_version", "q4k_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_binding_names_match_the_c_entry_points():
+    import bit_block_quantized_q4_gb300 as q4k
+    for name in _declared():
+        if name in ("q4k_status_str",):
+            continue
+        assert hasattr(q4k, name), name
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.q4k_abi_version() == 1
+    for s in range(8):
+        assert L.q4k_status_str(s).decode()
+    assert L.q4k_status_str(99).decode() == "unknown status"
+
+
+P = 0x10000  # a non-null, 64 KiB-aligned pointer value; never dereferenced
+
+
+def test_dequant_argument_errors(L):
+    assert L.q4k_dequant(P, 4, 255, P, 0, None) == 2
+    assert L.q4k_dequant(P, -1, 256, P, 0, None) == 2
+    assert L.q4k_dequant(P, 4, 256, P, 2, None) == 2
+    assert L.q4k_dequant(P, 0, 256, P, 0, None) == 0          # empty: no-op
+    assert L.q4k_dequant(None, 4, 256, P, 0, None) == 1
+    assert L.q4k_dequant(P, 4, 256, None, 0, None) == 1
+    assert L.q4k_dequant(P + 8, 4, 256, P, 0, None) == 3
+    assert L.q4k_dequant(P, 4, 256, P + 4, 0, None) == 3
+
+
+def test_gemv_argument_errors(L):
+    assert L.q4k_gemv(P, 4, 0, P, 1, 256, P, 4, None) == 2
+    assert L.q4k_gemv(P, 4, 300, P, 1, 304, P, 4, None) == 2
+    assert L.q4k_gemv(P, 4, 256, P, 17, 256, P, 4, None) == 2
+    assert L.q4k_gemv(P, 4, 256, P, -1, 256, P, 4, None) == 2
+    assert L.q4k_gemv(P, 4, 256, P, 1, 128, P, 4, None) == 2    # ldx < k
+    assert L.q4k_gemv(P, 4, 256, P, 1, 256, P, 2, None) == 2    # ldy < n
+    assert L.q4k_gemv(P, 0, 256, P, 1, 256, P, 4, None) == 0
+    assert L.q4k_gemv(P, 4, 256, P, 0, 256, P, 4, None) == 0
+    assert L.q4k_gemv(None, 4, 256, P, 1, 256, P, 4, None) == 1
+    assert L.q4k_gemv(P, 4, 256, None, 1, 256, P, 4, None) == 1
+    assert L.q4k_gemv(P, 4, 256, P, 1, 256, None, 4, None) == 1
+    assert L.q4k_gemv(P + 4, 4, 256, P, 1, 256, P, 4, None) == 3
+    assert L.q4k_gemv(P, 4, 256, P + 2, 1, 256, P, 4, None) == 3
+    assert L.q4k_gemv(P, 4, 256, P, 2, 260, P, 4, None) == 3     # ldx not a multiple of 8
+    assert L.q4k_gemv(P, 4, 256, P, 1, 256, P + 2, 4, None) == 3
+
+
+def test_gemm_argument_errors(L):
+    assert L.q4k_gemm(P, 4, 100, P, 8, 104, P, 8, None) == 2
+    assert L.q4k_gemm(P, 8, 256, P, -2, 256, P, 8, None) == 2
+    assert L.q4k_gemm(P, 8, 256, P, 0, 256, P, 8, None) == 0
+    assert L.q4k_gemm(P, 8, 256, P, 4, 256, P, 4, None) == 2     # ldy < n
+    assert L.q4k_gemm(None, 8, 256, P, 4, 256, P, 8, None) == 1
+    assert L.q4k_gemm(P, 8, 256, P, 4, 256, P + 8, 8, None) == 3
+    assert L.q4k_gemm(P, 8, 256, P, 4, 260, P, 8, None) == 3
+
+
+def test_moe_argument_errors(L):
+    E, H, F = 8, 256, 512
+    stride = F * H // 256 * 144
+    ws = L.q4k_moe_workspace_size(E, 4, 2, H, F)
+    assert ws > 0
+    args = [P, P, P, stride, E, H, F, P, 4, H, P, P, 2, P, H, P, ws, None]
+
+    def call(**kw):
+        a = list(args)
+        names = ["wg", "wu", "wd", "stride", "E", "H", "F", "x", "T", "ldx", "ids", "wts", "k",
+                 "y", "ldy", "ws", "wsb", "stream"]
+        for key, v in kw.items():
+            a[names.index(key)] = v
+        return L.q4k_moe_gemv(*a)
+
+    assert call(H=300) == 2
+    assert call(k=0) == 2
+    assert call(k=17) == 2
+    assert call(T=65) == 2
+    assert call(stride=stride - 16) == 2
+    assert call(T=0) == 0
+    assert call(ids=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsb=ws - 1) == 4
+    assert call(stride=stride + 8) == 3
+    assert call(x=P + 2) == 3
+
+
+def test_get_device_error_rejects_null(L):
+    assert L.q4k_get_device_error(None, None) == 1
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import bit_block_quantized_q4_gb300 as q4k
+    monkeypatch.setattr(q4k, "_lib", None)
+    monkeypatch.setattr(q4k, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        q4k.lib()

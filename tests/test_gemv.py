@@ -1,0 +1,142 @@
+"""q4k_gemv (decode, batch 1..16) on the GPU against the oracle.
+
+Bound: |y - y_ref| <= 2e-3 * sum_k |w_k||x_k| per element (fp32-accumulate
+path).  Shapes span several row tiles, ragged row tails and split-K slices;
+the full-size 27B-class projections are checked on sampled rows.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import DEV, check_bound, xbits
+from _q4k_fields import pack_block, random_fields
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def q4k():
+    from bit_block_quantized_q4_gb300 import build
+    build.build()
+    import bit_block_quantized_q4_gb300 as m
+    return m
+
+
+def _run(q4k, w, n, k, x):
+    y = q4k.q4k_gemv(w.to(DEV), n, k, x.to(DEV))
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    return y.cpu().numpy()
+
+
+CASES = [(1, 256, 1), (7, 512, 1), (129, 1280, 1), (597, 5120, 1), (33, 17408, 1),
+         (4096, 4096, 1), (1000, 2560, 2), (597, 5120, 3), (300, 4096, 4), (130, 1536, 8),
+         (129, 5120, 9), (597, 5120, 16), (40, 8192, 16)]
+
+
+@pytest.mark.parametrize("n,k,batch", CASES)
+def test_gemv_matches_oracle(q4k, n, k, batch):
+    w = synth.q4k_weight(n, k, seed=1000 + n + k + batch, quants="normal" if n % 2 else "uniform")
+    x = synth.bf16_normal((batch, k), seed=2000 + n + batch)
+    y = _run(q4k, w, n, k, x)
+    yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+    check_bound(y, yref, s, TOL, f"gemv {n}x{k} b{batch}")
+
+
+@pytest.mark.parametrize("batch", [1, 5, 16])
+def test_gemv_strided_x_and_y(q4k, batch):
+    n, k = 77, 1024
+    w = synth.q4k_weight(n, k, seed=3)
+    xs = synth.bf16_normal((batch, k + 64), seed=4).to(DEV)
+    x = xs[:, 8:8 + k]                                   # ldx = k + 64, offset 16 bytes
+    out = torch.full((batch, n + 5), float("nan"), device=DEV)
+    q4k.q4k_gemv(w.to(DEV), n, k, x, out=out[:, :n])
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.all(np.isnan(got[:, n:]))                  # nothing written past the row
+    yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+    check_bound(got[:, :n], yref, s, TOL, "strided")
+
+
+def test_gemv_zero_quant_rows_and_zero_blocks(q4k):
+    rng = np.random.default_rng(11)
+    k = 1024
+    rows = []
+    for r in range(40):
+        blks = []
+        for b in range(k // 256):
+            d, dm, sc, m, q = random_fields(rng)
+            if r % 3 == 0:
+                q = [0] * 256                            # zero quants: w = -dmin*m
+            if r % 5 == 0:
+                d, dm = 0, 0                             # zero block: w = 0
+            blks.append(pack_block(d, dm, sc, m, q))
+        rows.append(b"".join(blks))
+    n = len(rows)
+    w = torch.frombuffer(bytearray(b"".join(rows)), dtype=torch.uint8).view(n, -1)
+    for batch in (1, 4):
+        x = synth.bf16_normal((batch, k), seed=12 + batch)
+        y = _run(q4k, w, n, k, x)
+        yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+        check_bound(y, yref, s, TOL, f"zero-quant b{batch}")
+        assert np.all(y[:, ::5] == 0.0)                  # d = dmin = 0 rows are exactly 0
+
+
+def test_gemv_unit_vectors_pick_columns(q4k):
+    n, k = 64, 768
+    w = synth.q4k_weight(n, k, seed=13)
+    wq = oracle.dequant_f64(w.numpy(), n, k)
+    cols = [0, 2, 31, 32, 100, 255, 256, 511, 767]
+    x = torch.zeros((len(cols), k), dtype=torch.bfloat16)
+    for i, c in enumerate(cols):
+        x[i, c] = 1.0
+    y = _run(q4k, w, n, k, x)
+    for i, c in enumerate(cols):
+        assert np.allclose(y[i], wq[:, c], rtol=1e-6, atol=1e-6)
+    y1 = _run(q4k, w, n, k, x[3:4])
+    assert np.allclose(y1[0], wq[:, cols[3]], rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("batch", [1, 6])
+def test_gemv_homogeneous_and_deterministic_bitwise(q4k, batch):
+    n, k = 300, 2048
+    w = synth.q4k_weight(n, k, seed=14).to(DEV)
+    x = synth.bf16_normal((batch, k), seed=15).to(DEV)
+    y1 = q4k.q4k_gemv(w, n, k, x).clone()
+    y1b = q4k.q4k_gemv(w, n, k, x).clone()
+    y2 = q4k.q4k_gemv(w, n, k, (x.float() * 4).to(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y1b)
+    assert torch.equal(y2, y1 * 4)
+
+
+def test_gemv_zero_activations(q4k):
+    n, k = 50, 512
+    w = synth.q4k_weight(n, k, seed=16)
+    y = _run(q4k, w, n, k, torch.zeros((2, k), dtype=torch.bfloat16))
+    assert np.all(y == 0.0)
+
+
+# 27B-class dense decoder layer shapes (hidden 5120): QKV, O, gate/up, down.
+LAYER = [(10240, 5120), (5120, 8192), (17408, 5120), (5120, 17408)]
+
+
+@pytest.mark.parametrize("n,k", LAYER)
+@pytest.mark.parametrize("batch", [1, 4, 16])
+def test_gemv_full_size_sampled_rows(q4k, n, k, batch):
+    w = synth.q4k_weight(n, k, seed=n * 3 + k, quants="normal", device=DEV)
+    x = synth.bf16_normal((batch, k), seed=n + batch, device=DEV)
+    y = q4k.q4k_gemv(w, n, k, x)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    rows = np.sort(np.random.default_rng(n + k).choice(n, 96, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, n - 1]]))
+    wsub = w[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    yref, s = oracle.gemv(wsub, len(rows), k, xbits(x))
+    check_bound(y[:, torch.from_numpy(rows).to(DEV)].cpu().numpy(), yref, s, TOL,
+                f"full {n}x{k} b{batch}")
