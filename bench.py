@@ -186,12 +186,16 @@ def time_graph(fn, steps, warmup, stream):
     return total_ms / steps, per_ms, g
 
 
-def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None):
+def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, overlap=True):
+    """One pass = the 320 projections back to back, captured in a CUDA graph.
+    With `overlap` each projection may start streaming its (static) weights
+    while the previous one finishes (Q4K_FLAG_OVERLAP_WEIGHTS)."""
     xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
+    flags = q4k.Q4K_FLAG_OVERLAP_WEIGHTS if overlap else 0
 
     def step():
         for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
-            q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
+            q4k.q4k_gemv_ex(w, n, k, x, flags, out=y, stream=stream)
 
     if sampler is not None:
         with sampler:
@@ -395,6 +399,10 @@ def main():
     e2e["value"] = round(e2e["value"] * world, 2)
 
     extra = {}
+    r = bench_decode(q4k, layers, 1, max(5, args.steps // 2), 3, dev, stream, overlap=False)
+    extra["decode_b1_no_overlap"] = {"gbs": round(r["gbs"], 1),
+                                     "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
+                                     "ms_per_step": round(r["ms_per_step"], 4)}
     if not args.skip_extra:
         for b in (4, 16):
             r = bench_decode(q4k, layers, b, max(5, args.steps // 2), 3, dev, stream)

@@ -22,7 +22,8 @@ Q4K_BYTES = 144
 
 STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN",
           4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA"}
-EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemm",
+Q4K_FLAG_OVERLAP_WEIGHTS = 1
+EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex", "q4k_gemm",
            "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_get_device_error")
 
 _lock = threading.Lock()
@@ -53,6 +54,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_dequant.argtypes = [P, I64, I64, P, ctypes.c_int, P]
         L.q4k_gemv.restype = ctypes.c_int
         L.q4k_gemv.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_gemv_ex.restype = ctypes.c_int
+        L.q4k_gemv_ex.argtypes = [P, I64, I64, P, I64, I64, P, I64, ctypes.c_uint32, P]
         L.q4k_gemm.restype = ctypes.c_int
         L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
@@ -112,11 +115,24 @@ def q4k_gemv(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=
     return out[0] if x.dim() == 1 else out
 
 
+def q4k_gemv_ex(w: torch.Tensor, n: int, k: int, x: torch.Tensor, flags: int, out=None,
+                stream=None):
+    """q4k_gemv with flags (Q4K_FLAG_OVERLAP_WEIGHTS)."""
+    x2 = x.unsqueeze(0) if x.dim() == 1 else x
+    batch = x2.shape[0]
+    if out is None:
+        out = torch.empty((batch, n), dtype=torch.float32, device=x.device)
+    _check(lib().q4k_gemv_ex(_ptr(w), n, k, _ptr(x2), batch, x2.stride(0), _ptr(out),
+                             out.stride(0), flags, _stream(stream)), "q4k_gemv_ex")
+    return out[0] if x.dim() == 1 else out
+
+
 def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=None):
     """Y = X W^T for X [M, K] bf16; returns bf16 [M, N]."""
     m = x.shape[0]
-    if out is None:
-        out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    if out is None:  # the C ABI wants a row stride that is a multiple of 8
+        ld = (n + 7) // 8 * 8
+        out = torch.empty((m, ld), dtype=torch.bfloat16, device=x.device)[:, :n]
     _check(lib().q4k_gemm(_ptr(w), n, k, _ptr(x), m, x.stride(0), _ptr(out), out.stride(0),
                           _stream(stream)), "q4k_gemm")
     return out

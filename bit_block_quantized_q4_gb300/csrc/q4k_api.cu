@@ -130,17 +130,25 @@ int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, v
   return map_launch(launch_dequant(w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
-int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
-             float *y, int64_t ldy, void *stream) {
+int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+                float *y, int64_t ldy, uint32_t flags, void *stream) {
   if (n < 0 || k <= 0 || (k % kQK) != 0 || batch < 0 || batch > 16) return Q4K_ERR_SHAPE;
   if (n > INT32_MAX / 2 || k / kQK > INT32_MAX / kBlockBytes) return Q4K_ERR_SHAPE;
+  if (flags & ~(uint32_t)Q4K_FLAG_OVERLAP_WEIGHTS) return Q4K_ERR_SHAPE;
   if (n == 0 || batch == 0) return Q4K_OK;
   if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
   if (!w || !x || !y) return Q4K_ERR_NULL;
   if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4) || (ldx % 8) != 0) return Q4K_ERR_ALIGN;
   int st = check_device();
   if (st != Q4K_OK) return st;
-  return map_launch(launch_gemv(w, n, k, x, batch, ldx, y, ldy, static_cast<cudaStream_t>(stream)));
+  return map_launch(launch_gemv(w, n, k, x, batch, ldx, y, ldy,
+                                (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+             float *y, int64_t ldy, void *stream) {
+  return q4k_gemv_ex(w, n, k, x, batch, ldx, y, ldy, 0u, stream);
 }
 
 int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx, void *y,
@@ -167,8 +175,8 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
                  int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
                  int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,
                  int64_t ldy, void *workspace, size_t workspace_bytes, void *stream) {
-  if (n_experts <= 0 || hidden <= 0 || ffn <= 0 || (hidden % kQK) || (ffn % kQK) || n_tokens < 0 ||
-      n_tokens > 64 || top_k < 1 || top_k > 16)
+  if (n_experts <= 0 || n_experts > 2048 || hidden <= 0 || ffn <= 0 || (hidden % kQK) ||
+      (ffn % kQK) || n_tokens < 0 || n_tokens > 64 || top_k < 1 || top_k > 16)
     return Q4K_ERR_SHAPE;
   if (hidden > (1 << 20) || ffn > (1 << 20)) return Q4K_ERR_SHAPE;
   if (expert_stride < (ffn * hidden / kQK) * kBlockBytes) return Q4K_ERR_SHAPE;

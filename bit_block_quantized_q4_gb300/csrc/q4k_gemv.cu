@@ -37,7 +37,7 @@
 
 // Tuning knobs (compile time).
 #ifndef Q4K_GEMV_STAGES
-#define Q4K_GEMV_STAGES 3
+#define Q4K_GEMV_STAGES 4
 #endif
 #ifndef Q4K_GEMV_PROMO  // L2 promotion of the weight tensor map: 0 none, 1 128 B, 2 256 B
 #define Q4K_GEMV_PROMO 2
@@ -65,13 +65,15 @@ struct GemvArgs {
   unsigned *err;   // device error word
 };
 
+// W is viewed as a 2-D array of 8-byte elements, [n rows][nsb * 18]; one box
+// covers S super-blocks (S * 144 contiguous bytes) of 16*MT rows.
 __device__ __forceinline__ void load_tile(void *dst, const CUtensorMap *map, uint64_t *bar, int sb,
                                           int row0, uint64_t policy) {
 #if Q4K_GEMV_EVICT_FIRST
-  tma_load_3d_hint(dst, map, bar, 0, sb, row0, policy);
+  tma_load_2d_hint(dst, map, bar, sb * (kBlockBytes / 8), row0, policy);
 #else
   (void)policy;
-  tma_load_3d(dst, map, bar, 0, sb, row0);
+  tma_load_2d(dst, map, bar, sb * (kBlockBytes / 8), row0);
 #endif
 }
 
@@ -80,12 +82,15 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 }
 
 // ---------------------------------------------------------------- batch 1
-// Shared memory per warp: STAGES weight tiles | x of the warp's slice,
-// permuted so that word 2q of a sub-block holds (x[4q], x[4q+2]) and word 2q+1
-// holds (x[4q+1], x[4q+3]) | 16 zero words | STAGES mbarriers.
-template <int MT, int STAGES>
+// Shared memory per warp: STAGES weight tiles (16*MT rows x S super-blocks,
+// row stride S*144 bytes) | x of the warp's slice, permuted so that word 2q of
+// a sub-block holds (x[4q], x[4q+2]) and word 2q+1 holds (x[4q+1], x[4q+3]) |
+// the fp32 sums X_j of its sub-blocks | 16 zero words | STAGES mbarriers.
+template <int MT, int S, int STAGES>
 __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const GemvArgs a) {
+  constexpr int kStageBytes = MT * S * kTileBytes;
+  constexpr int kRowBytes = S * kBlockBytes;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -93,12 +98,14 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   const int g = lane >> 2, t = lane & 3;
   const int row0 = blockIdx.x * (MT * kRowsPerTile);
   const int sb0 = warp * a.ks;
-  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);
+  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);  // super-blocks of this warp
+  const int nstages = (nsteps + S - 1) / S;
 
   uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
   uint8_t *ring = wreg;
-  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * MT * kTileBytes);
-  uint32_t *xzero = xperm + a.ks * 128;
+  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * kStageBytes);
+  float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
+  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);
   uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);
   float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
 
@@ -110,12 +117,16 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   __syncwarp();
   const uint64_t policy = l2_evict_first_policy();
   if (lane == 0) {
-    for (int s = 0; s < STAGES && s < nsteps; ++s) {
-      mbar_arrive_expect_tx(&bars[s], MT * kTileBytes);
-      load_tile(ring + s * MT * kTileBytes, &wmap, &bars[s], sb0 + s, row0, policy);
+    for (int s = 0; s < STAGES && s < nstages; ++s) {
+      mbar_arrive_expect_tx(&bars[s], kStageBytes);
+      load_tile(ring + s * kStageBytes, &wmap, &bars[s], sb0 + s * S, row0, policy);
     }
   }
-  // x slice -> permuted shared copy (8 values per lane per iteration).
+  // The weights above do not depend on earlier kernels; x does.
+  grid_dependency_wait();
+  grid_launch_dependents();
+  // x slice -> permuted shared copy and per-sub-block sums (8 values per lane
+  // per iteration; lanes 4j..4j+3 hold sub-block j of a 256-value step).
   {
     const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + (int64_t)sb0 * kQK);
     for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
@@ -126,6 +137,14 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
       o.z = __byte_perm(u.z, u.w, 0x5410);
       o.w = __byte_perm(u.z, u.w, 0x7632);
       reinterpret_cast<uint4 *>(xperm)[c8] = o;
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z));
+      const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.w));
+      float sum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      if ((lane & 3) == 0) xsum[c8 >> 2] = sum;
     }
     if (lane < 16) xzero[lane] = 0u;
   }
@@ -139,76 +158,113 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   const int adv0 = (own && !(g & 1)) ? 128 : 0;
   const int adv1 = (own && (g & 1)) ? 128 : 0;
 
-  float yacc[MT][2];
+  // Scale/min decode of sub-blocks 2t, 2t+1, branch-free: lanes t < 2 read the
+  // low six bits of s[j], s[j+4]; lanes t >= 2 combine a nibble of s[j+4] with
+  // the top two bits of s[j-4] (scales) or s[j] (mins).
+  const bool upper = t >= 2;
+  const uint32_t sh = (t & 1) * 16;
+  const uint32_t sh_m = upper ? sh + 4 : sh;
+  const uint32_t mlo = upper ? 0x0F0Fu : 0x3F3Fu;
+  const uint32_t mhi = upper ? 0x3030u : 0u;
+
+  float2 yacc[MT];  // rows (g, g+8)
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) yacc[mt][0] = yacc[mt][1] = 0.f;
+  for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
 
   bool ok = true;
-  for (int i = 0; i < nsteps; ++i) {
-    const int stage = i % STAGES;
-    if (!mbar_wait(&bars[stage], (uint32_t)((i / STAGES) & 1), a.err)) {
+  int stage = 0;
+  uint32_t phase = 0;
+  const uint32_t *p0 = pb0, *p1 = pb1;
+  for (int it = 0; it < nstages && ok; ++it) {
+    if (!mbar_wait(&bars[stage], phase, a.err)) {
       ok = false;
       break;
     }
-    const uint8_t *st = ring + stage * MT * kTileBytes;
-    uint4 hdr[MT][2], qa[MT][2][2];
+    uint8_t *st = ring + stage * kStageBytes;
+    const int cnt = min(S, nsteps - it * S);
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int u = 0; u < S; ++u) {
+      if (u >= cnt) break;
+      const int i = it * S + u;  // super-block index within the slice
+      uint4 hdr[MT][2], qa[MT][2][2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kBlockBytes;
-        hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
-        qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
-        qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
-      }
-    }
-    __syncwarp();
-    if (lane == 0 && i + STAGES < nsteps) {
-      mbar_arrive_expect_tx(&bars[stage], MT * kTileBytes);
-      load_tile(ring + stage * MT * kTileBytes, &wmap, &bars[stage], sb0 + i + STAGES, row0, policy);
-    }
-
-    float acc[MT][4];
-    float c128[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    const uint32_t *p0 = pb0 + i * adv0;
-    const uint32_t *p1 = pb1 + i * adv1;
-#pragma unroll
-    for (int G = 0; G < 4; ++G) {
-      const uint4 bb0 = reinterpret_cast<const uint4 *>(p0)[G];
-      const uint4 bb1 = reinterpret_cast<const uint4 *>(p1)[G];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int wi = 2 * G + (e >> 1);      // quant word (4 bytes of the chunk)
-        const int sh = (e & 1) * 8;           // positions (o, o+2) or (o+1, o+3)
-        const uint32_t b0 = word_of(bb0, e), b1 = word_of(bb1, e);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t w0 = word_of(qa[mt][0][wi >> 2], wi & 3) >> sh;
-          const uint32_t w1 = word_of(qa[mt][1][wi >> 2], wi & 3) >> sh;
-          mma_bf16(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
+        for (int r = 0; r < 2; ++r) {
+          const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kRowBytes + u * kBlockBytes;
+          hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
+          qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
+          qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
         }
-        mma_bf16(c128, kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0, b1);
+      }
+      if (u == cnt - 1) {  // stage fully read: refill it
+        __syncwarp();
+        if (lane == 0 && it + STAGES < nstages) {
+          mbar_arrive_expect_tx(&bars[stage], kStageBytes);
+          load_tile(st, &wmap, &bars[stage], sb0 + (it + STAGES) * S, row0, policy);
+        }
+      }
+
+      float acc[MT][4];
+      const float2 xs2 = reinterpret_cast<const float2 *>(xsum + i * 8)[t];  // X_{2t}, X_{2t+1}
+#pragma unroll
+      for (int G = 0; G < 4; ++G) {
+        const uint4 bb0 = reinterpret_cast<const uint4 *>(p0)[G];
+        const uint4 bb1 = reinterpret_cast<const uint4 *>(p1)[G];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int wi = 2 * G + (e >> 1);  // quant word (4 bytes of the chunk)
+          const int sh8 = (e & 1) * 8;      // positions (o, o+2) or (o+1, o+3)
+          const uint32_t b0 = word_of(bb0, e), b1 = word_of(bb1, e);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t w0 = word_of(qa[mt][0][wi >> 2], wi & 3) >> sh8;
+            const uint32_t w1 = word_of(qa[mt][1][wi >> 2], wi & 3) >> sh8;
+            if (G == 0 && e == 0)
+              mma_bf16_zc(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
+            else
+              mma_bf16(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
+          }
+        }
+      }
+      p0 += adv0;
+      p1 += adv1;
+      // acc = sum (128+q) x per (row, sub-block); subtract 128 X, apply the
+      // scales.  Rows g and g+8 are handled as a pair with packed fp32x2 math.
+      const float2 nC0 = make_float2(-128.f * xs2.x, -128.f * xs2.x);
+      const float2 nC1 = make_float2(-128.f * xs2.y, -128.f * xs2.y);
+      const float2 nX0 = make_float2(-xs2.x, -xs2.x);
+      const float2 nX1 = make_float2(-xs2.y, -xs2.y);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t sc2[2], m2[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint4 h = hdr[mt][r];
+          const uint32_t srcS = upper ? h.w : h.y;
+          const uint32_t srcM = upper ? h.w : h.z;
+          sc2[r] = ((srcS >> sh) & mlo) | ((h.y >> (sh + 2)) & mhi);
+          m2[r] = ((srcM >> sh_m) & mlo) | ((h.z >> (sh + 2)) & mhi);
+        }
+        const float2 sca = make_float2((float)(sc2[0] & 0xFFu), (float)(sc2[1] & 0xFFu));
+        const float2 scb = make_float2((float)(sc2[0] >> 8), (float)(sc2[1] >> 8));
+        const float2 ma = make_float2((float)(m2[0] & 0xFFu), (float)(m2[1] & 0xFFu));
+        const float2 mb = make_float2((float)(m2[0] >> 8), (float)(m2[1] >> 8));
+        const float2 dd =
+            make_float2(half_lo_to_float(hdr[mt][0].x), half_lo_to_float(hdr[mt][1].x));
+        const float2 dm =
+            make_float2(half_hi_to_float(hdr[mt][0].x), half_hi_to_float(hdr[mt][1].x));
+        const float2 ta = __fadd2_rn(make_float2(acc[mt][0], acc[mt][2]), nC0);
+        const float2 tb = __fadd2_rn(make_float2(acc[mt][1], acc[mt][3]), nC1);
+        const float2 uu = __ffma2_rn(scb, tb, __fmul2_rn(sca, ta));
+        const float2 vv = __ffma2_rn(mb, nX1, __fmul2_rn(ma, nX0));  // -(m_a X_a + m_b X_b)
+        yacc[mt] = __ffma2_rn(dd, uu, yacc[mt]);
+        yacc[mt] = __ffma2_rn(dm, vv, yacc[mt]);
       }
     }
-    // c128[0], c128[1] = 128 X of sub-blocks 2t, 2t+1.
-    const float X0 = c128[0] * (1.f / 128.f), X1 = c128[1] * (1.f / 128.f);
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint4 h = hdr[mt][r];
-        uint32_t sc2, m2;
-        scales_pair(h.y, h.z, h.w, t, &sc2, &m2);
-        const float d = half_lo_to_float(h.x), dmin = half_hi_to_float(h.x);
-        const float ta = acc[mt][2 * r] - c128[0];
-        const float tb = acc[mt][2 * r + 1] - c128[1];
-        const float u = fmaf((float)(sc2 >> 8), tb, (float)(sc2 & 0xFFu) * ta);
-        const float v = fmaf((float)(m2 >> 8), X1, (float)(m2 & 0xFFu) * X0);
-        yacc[mt][r] = fmaf(d, u, yacc[mt][r]);
-        yacc[mt][r] = fmaf(-dmin, v, yacc[mt][r]);
-      }
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
 
@@ -217,7 +273,7 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float v = yacc[mt][r];
+      float v = r ? yacc[mt].y : yacc[mt].x;
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
@@ -227,10 +283,10 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   if (!ok && lane == 0) red[warp * (MT * kRowsPerTile)] = __int_as_float(0x7fc00000);
   __syncthreads();
   if (threadIdx.x < MT * kRowsPerTile) {
-    float s = 0.f;
-    for (int w = 0; w < nwarps; ++w) s += red[w * (MT * kRowsPerTile) + threadIdx.x];
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) sum += red[w * (MT * kRowsPerTile) + threadIdx.x];
     const int row = row0 + threadIdx.x;
-    if (row < a.n) a.y[row] = s;
+    if (row < a.n) a.y[row] = sum;
   }
 }
 
@@ -268,6 +324,8 @@ __global__ void __launch_bounds__(512) gemv_bn_kernel(const __grid_constant__ CU
       load_tile(ring + s * MT * kTileBytes, &wmap, &bars[s], sb0 + s, row0, policy);
     }
   }
+  grid_dependency_wait();
+  grid_launch_dependents();
   // x rows of this lane's batch columns (g and g+8); rows past the batch read
   // zeros.
   const uint4 *xrow[NT];
@@ -416,14 +474,24 @@ __global__ void __launch_bounds__(512) gemv_bn_kernel(const __grid_constant__ CU
 }
 
 // ---------------------------------------------------------------- launch
-constexpr int kStages = Q4K_GEMV_STAGES;
+constexpr int kStages = Q4K_GEMV_STAGES;  // batch 2..16 (one super-block per stage)
+// Stages for batch 1 with S super-blocks per stage.
+template <int S> struct B1Stages { static constexpr int value = S == 1 ? 4 : (S == 2 ? 3 : 2); };
+
+#ifndef Q4K_GEMV_FORCE_S  // 0: choose per shape
+#define Q4K_GEMV_FORCE_S 0
+#endif
+#ifndef Q4K_GEMV_FORCE_MT
+#define Q4K_GEMV_FORCE_MT 0
+#endif
 
 struct Plan {
-  int mt = 1, wk = 1, ks = 1, warp_bytes = 0, smem = 0, grid = 0;
+  int mt = 1, s = 1, wk = 1, ks = 1, warp_bytes = 0, smem = 0, grid = 0;
+  double score = -1e30;
 };
 
-int warp_bytes_b1(int mt, int ks) {
-  int b = kStages * mt * kTileBytes + ks * 512 + 64 + kStages * 8;
+int warp_bytes_b1(int mt, int s, int stages, int ks) {
+  int b = stages * mt * s * kTileBytes + ks * (512 + 32) + 64 + stages * 8;
   return (b + 127) / 128 * 128;
 }
 int warp_bytes_bn(int mt) {
@@ -439,19 +507,21 @@ int occupancy(K kernel, int threads, int smem) {
   return blocks;
 }
 
-// Choose the split of K across the warps of a CTA: prefer one resident wave,
-// then more warps in flight (up to 32 per SM), then an even split.
+// Choose how the K dimension is split across the warps of a CTA.  Every CTA
+// should be resident at once (one wave); among those plans, prefer more weight
+// bytes in flight per SM (latency hiding), then an even split.
 template <typename K>
-Plan plan_for(K kernel, bool b1, int mt, int n, int nsb, int cols, const DeviceFacts *f) {
+Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int cols,
+              const DeviceFacts *f) {
   Plan best;
-  double best_score = -1e30;
   const int tile_rows = mt * kRowsPerTile;
   const int grid = (n + tile_rows - 1) / tile_rows;
   for (int wk = 1; wk <= 16; ++wk) {
-    const int ks = (nsb + wk - 1) / wk;
+    int ks = (nsb + wk - 1) / wk;
+    ks = (ks + s - 1) / s * s;
     if ((nsb + ks - 1) / ks != wk) continue;  // no empty warps
-    if (ks < 2 && nsb >= 2) continue;
-    const int wb = b1 ? warp_bytes_b1(mt, ks) : warp_bytes_bn(mt);
+    if (ks < 2 * s && nsb >= 2 * s) continue;
+    const int wb = b1 ? warp_bytes_b1(mt, s, stages, ks) : warp_bytes_bn(mt);
     const int smem = wk * wb + wk * tile_rows * cols * 4;
     if (smem > f->max_smem_optin) continue;
     const int occ = occupancy(kernel, wk * 32, smem);
@@ -460,11 +530,14 @@ Plan plan_for(K kernel, bool b1, int mt, int n, int nsb, int cols, const DeviceF
     const int waves = (grid + slots - 1) / slots;
     const int per_sm = std::min(occ, (grid + f->sm_count - 1) / f->sm_count);
     const int warps_sm = per_sm * wk;
+    const double inflight_kb = warps_sm * (stages - 1) * mt * s * kTileBytes / 1024.0;
     const double balance = (double)nsb / (double)(ks * wk);  // 1.0 = even split
-    const double score = -1000.0 * waves + std::min(warps_sm, 32) + 8.0 * balance;
-    if (score > best_score) {
-      best_score = score;
+    const double score = -1000.0 * waves + std::min(inflight_kb, 96.0) / 8.0 +
+                         0.5 * std::min(warps_sm, 24) + 6.0 * balance + (mt == 2 ? 1.0 : 0.0);
+    if (score > best.score) {
+      best.score = score;
       best.mt = mt;
+      best.s = s;
       best.wk = wk;
       best.ks = ks;
       best.warp_bytes = wb;
@@ -482,35 +555,68 @@ void allow_smem(K kernel, const DeviceFacts *f) {
   cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f->max_smem_optin);
 }
 
+template <int MT, int S>
+constexpr auto b1_kernel() {
+  return gemv_b1_kernel<MT, S, B1Stages<S>::value>;
+}
+
 void set_attributes(const DeviceFacts *f) {
-  allow_smem(gemv_b1_kernel<1, kStages>, f);
-  allow_smem(gemv_b1_kernel<2, kStages>, f);
+  allow_smem(b1_kernel<1, 1>(), f);
+  allow_smem(b1_kernel<1, 2>(), f);
+  allow_smem(b1_kernel<1, 4>(), f);
+  allow_smem(b1_kernel<2, 1>(), f);
+  allow_smem(b1_kernel<2, 2>(), f);
   allow_smem(gemv_bn_kernel<1, 1, kStages>, f);
   allow_smem(gemv_bn_kernel<1, 2, kStages>, f);
   allow_smem(gemv_bn_kernel<2, 1, kStages>, f);
   allow_smem(gemv_bn_kernel<2, 2, kStages>, f);
 }
 
+using GemvKernel = void (*)(CUtensorMap, GemvArgs);
+
+GemvKernel b1_select(int mt, int s) {
+  if (mt == 2) return s == 2 ? b1_kernel<2, 2>() : b1_kernel<2, 1>();
+  return s == 4 ? b1_kernel<1, 4>() : s == 2 ? b1_kernel<1, 2>() : b1_kernel<1, 1>();
+}
+
 }  // namespace
 
+template <typename K>
+cudaError_t launch(K kernel, const Plan &p, const CUtensorMap &map, const GemvArgs &args, bool pdl,
+                   cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)(p.wk * 32), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, map, args);
+}
+
 cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
-                        int64_t ldx, float *y, int64_t ldy, cudaStream_t stream) {
+                        int64_t ldx, float *y, int64_t ldy, bool overlap, cudaStream_t stream) {
   const DeviceFacts *f = device_facts();
   std::call_once(g_attr_once, set_attributes, f);
   const int nsb = (int)(k / kQK);
-  const int mt = (batch == 1) ? (n >= 32 * f->sm_count * 2 ? 2 : 1) : (n >= 32 * f->sm_count ? 2 : 1);
+  const int mt_bn = n >= 32 * f->sm_count ? 2 : 1;
 
-  // W viewed as [n rows][nsb super-blocks][144 bytes].
+  // W viewed as [n rows][nsb super-blocks][144 bytes]; one box = 16*mt rows
+  // of one super-block.
   CUtensorMap map;
-  const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
-  const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
-  const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)(mt * kRowsPerTile)};
-  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
-                   box, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   Q4K_GEMV_PROMO == 0   ? CU_TENSOR_MAP_L2_PROMOTION_NONE
-                   : Q4K_GEMV_PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-                                         : CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  auto encode = [&](int mt, int s) {
+    const uint64_t dims[2] = {(uint64_t)nsb * (kBlockBytes / 8), (uint64_t)n};
+    const uint64_t strides[1] = {(uint64_t)nsb * kBlockBytes};
+    const uint32_t box[2] = {(uint32_t)(s * (kBlockBytes / 8)), (uint32_t)(mt * kRowsPerTile)};
+    return encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(w), dims,
+                        strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        Q4K_GEMV_PROMO == 0   ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                        : Q4K_GEMV_PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                              : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  };
 
   GemvArgs args;
   args.x = static_cast<const __nv_bfloat16 *>(x);
@@ -523,21 +629,35 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   args.err = device_error_word();
 
   if (batch == 1) {
-    auto kern = (mt == 2) ? gemv_b1_kernel<2, kStages> : gemv_b1_kernel<1, kStages>;
-    const Plan p = plan_for(kern, true, mt, (int)n, nsb, 1, f);
+    Plan p;
+    const int cand[5][2] = {{1, 1}, {1, 2}, {1, 4}, {2, 1}, {2, 2}};
+    for (const auto &c : cand) {
+      if (Q4K_GEMV_FORCE_MT && c[0] != Q4K_GEMV_FORCE_MT) continue;
+      if (Q4K_GEMV_FORCE_S && c[1] != Q4K_GEMV_FORCE_S) continue;
+      const int stages = c[1] == 1 ? B1Stages<1>::value : c[1] == 2 ? B1Stages<2>::value
+                                                                     : B1Stages<4>::value;
+      const Plan q = plan_for(b1_select(c[0], c[1]), true, c[0], c[1], stages, (int)n, nsb, 1, f);
+      if (q.grid && q.score > p.score) p = q;
+    }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    GemvKernel kern = b1_select(p.mt, p.s);
+    if (encode(p.mt, p.s) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
-    kern<<<p.grid, p.wk * 32, p.smem, stream>>>(map, args);
+    cudaError_t e = launch(kern, p, map, args, overlap, stream);
+    if (e != cudaSuccess) return e;
   } else {
+    const int mt = mt_bn;
     const int nt = batch <= 8 ? 1 : 2;
     auto kern = (mt == 2) ? (nt == 1 ? gemv_bn_kernel<2, 1, kStages> : gemv_bn_kernel<2, 2, kStages>)
                           : (nt == 1 ? gemv_bn_kernel<1, 1, kStages> : gemv_bn_kernel<1, 2, kStages>);
-    const Plan p = plan_for(kern, false, mt, (int)n, nsb, nt * 8, f);
+    const Plan p = plan_for(kern, false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    if (encode(mt, 1) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
-    kern<<<p.grid, p.wk * 32, p.smem, stream>>>(map, args);
+    cudaError_t e = launch(kern, p, map, args, overlap, stream);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

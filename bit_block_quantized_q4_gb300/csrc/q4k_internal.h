@@ -34,7 +34,7 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank,
 cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype,
                            cudaStream_t stream);
 cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
-                        int64_t ldx, float *y, int64_t ldy, cudaStream_t stream);
+                        int64_t ldx, float *y, int64_t ldy, bool overlap, cudaStream_t stream);
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
 size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

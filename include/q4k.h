@@ -113,6 +113,23 @@ int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, 
              float *y, int64_t ldy, void *stream);
 
 /*
+ * q4k_gemv_ex -- q4k_gemv with flags.
+ *   Q4K_FLAG_OVERLAP_WEIGHTS: the kernel is launched as a programmatic
+ *     dependent of the kernel launched before it on `stream` and starts
+ *     streaming W while that kernel is still finishing.  X is read and Y
+ *     written only after the earlier kernel has completed, so stream order
+ *     holds for them; the caller guarantees that no kernel still running ahead
+ *     of this call on the stream writes W (true for model weights, which are
+ *     loaded once).  Consecutive decode projections overlap their start-up
+ *     latency this way ("spec: specialized model runtimes", section
+ *     "Development sequence": graph-captured decode).
+ * Other flag bits -> Q4K_ERR_SHAPE.  Everything else as q4k_gemv.
+ */
+#define Q4K_FLAG_OVERLAP_WEIGHTS 1u
+int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+                float *y, int64_t ldy, uint32_t flags, void *stream);
+
+/*
  * q4k_gemm -- prefill projection, Y = X W^T for m tokens (any m >= 1).
  * ("spec: specialized model runtimes", section "Feasibility gate": one
  *  quantized GEMM; prefill throughput and TTFT are reported metrics in "PRD:
@@ -148,6 +165,7 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k
  *                  e * expert_stride
  *   w_down         device; expert e's hidden x ffn Q4_K matrix starts at byte
  *                  e * expert_stride
+ *   n_experts      1..2048
  *   expert_stride  bytes, >= (ffn * hidden / 256) * 144, multiple of 16
  *   hidden, ffn    multiples of 256
  *   x              device, n_tokens x hidden bf16, row stride ldx (mult. of 8)

@@ -1,0 +1,157 @@
+"""q4k_moe_gemv (routed-expert decode FFN) on the GPU against the oracle.
+
+Bound: the fp32-path tolerance 2e-3 * sum|w||x| of every matmul stage,
+propagated through SiLU(g)*u (|silu'| <= 1.1), the down projection and the
+route-weighted sum:
+  dh_k  = 1.1 dg_k |u_k| + |silu(g_k)| du_k + 1.1 dg_k du_k + 2^-15 |h_k|
+  |dy|  <= sum_j |r_j| (2e-3 |Wd| |h| + 1.002 |Wd| dh)
+with dg = 2e-3 |Wg||x|, du = 2e-3 |Wu||x| (the 2^-15 term covers h entering
+the down MMA as two bf16 parts).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import DEV, xbits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q4k():
+    from bit_block_quantized_q4_gb300 import build
+    build.build()
+    import bit_block_quantized_q4_gb300 as m
+    return m
+
+
+def _make(E, H, F, T, K, seed, quants="uniform"):
+    stride = F * (H // 256) * 144
+    wg = synth.q4k_weight(E * F, H, seed=seed, quants=quants).reshape(-1)
+    wu = synth.q4k_weight(E * F, H, seed=seed + 1, quants=quants).reshape(-1)
+    wd = synth.q4k_weight(E * H, F, seed=seed + 2, quants=quants).reshape(-1)
+    x = synth.bf16_normal((T, H), seed=seed + 3)
+    ids, wts = synth.zipf_routing(T, E, K, seed=seed + 4)
+    return dict(wg=wg, wu=wu, wd=wd, stride=stride, E=E, H=H, F=F, x=x, ids=ids, wts=wts)
+
+
+def _gpu(q4k, c, ids=None, wts=None):
+    ids = c["ids"] if ids is None else ids
+    wts = c["wts"] if wts is None else wts
+    y = q4k.q4k_moe_gemv(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"], c["E"],
+                         c["H"], c["F"], c["x"].to(DEV), ids.to(DEV), wts.to(DEV))
+    torch.cuda.synchronize()
+    err = q4k.q4k_get_device_error()
+    return y.cpu().numpy().astype(np.float64), err
+
+
+def _bound(c, ids, wts, tokens):
+    """Reference y and the propagated error bound for the listed tokens."""
+    E, H, F, s = c["E"], c["H"], c["F"], c["stride"]
+    wg, wu, wd = (c[k].numpy() for k in ("wg", "wu", "wd"))
+    xb = xbits(c["x"])
+    xf = c["x"].to(torch.float64).numpy()
+    ids_n = ids.numpy()
+    wts_n = wts.numpy().astype(np.float64)
+    yref = oracle.moe(wg, wu, wd, s, E, H, F, xb[tokens], ids_n[tokens], wts_n[tokens].astype(np.float32))
+    bound = np.zeros((len(tokens), H))
+    for ti, t in enumerate(tokens):
+        for j in range(ids_n.shape[1]):
+            e = int(ids_n[t, j])
+            if e < 0 or e >= E:
+                continue
+            ge, ue, de = (m[e * s:(e + 1) * s] for m in (wg, wu, wd))
+            g = oracle.gemv_f64(ge, F, H, xf[t])[0]
+            u = oracle.gemv_f64(ue, F, H, xf[t])[0]
+            dg = 2e-3 * oracle.gemv_f64(ge, F, H, np.abs(xf[t]), use_abs=True)[0]
+            du = 2e-3 * oracle.gemv_f64(ue, F, H, np.abs(xf[t]), use_abs=True)[0]
+            sg = g / (1.0 + np.exp(-g))
+            h = sg * u
+            dh = 1.1 * dg * np.abs(u) + np.abs(sg) * du + 1.1 * dg * du + 2.0 ** -15 * np.abs(h)
+            awd_h = oracle.gemv_f64(de, H, F, np.abs(h), use_abs=True)[0]
+            awd_dh = oracle.gemv_f64(de, H, F, dh, use_abs=True)[0]
+            bound[ti] += abs(wts_n[t, j]) * (2e-3 * awd_h + 1.002 * awd_dh)
+    return yref, bound
+
+
+def _check(y, yref, bound, what):
+    err = np.abs(y - yref)
+    bad = ~(err <= bound + 1e-30)
+    assert not bad.any(), f"{what}: {bad.sum()} outside, worst {np.max(err - bound)}"
+
+
+@pytest.mark.parametrize("E,H,F,T,K", [(8, 256, 256, 1, 1), (8, 512, 512, 3, 2), (16, 1024, 512, 16, 8),
+                                       (32, 512, 768, 9, 4)])
+def test_moe_matches_oracle(q4k, E, H, F, T, K):
+    c = _make(E, H, F, T, K, seed=E + H + F + T + K)
+    y, err = _gpu(q4k, c)
+    assert err == 0
+    tokens = list(range(T))
+    yref, bound = _bound(c, c["ids"], c["wts"], tokens)
+    _check(y[tokens], yref, bound, f"moe E{E} H{H} F{F} T{T} k{K}")
+
+
+def test_moe_one_expert_for_all_tokens_spans_slots(q4k):
+    # 20 tokens all routed (top-1) to expert 3: more pairs than one work slot holds
+    c = _make(6, 512, 256, 20, 1, seed=5)
+    ids = torch.full((20, 1), 3, dtype=torch.int32)
+    wts = torch.ones((20, 1), dtype=torch.float32)
+    y, err = _gpu(q4k, c, ids, wts)
+    assert err == 0
+    yref, bound = _bound(c, ids, wts, list(range(20)))
+    _check(y, yref, bound, "single expert")
+
+
+def test_moe_duplicate_ids_and_bad_ids(q4k):
+    c = _make(8, 512, 256, 4, 3, seed=7)
+    ids = c["ids"].clone()
+    ids[0, 1] = ids[0, 0]          # the same expert twice for one token
+    ids[1, 2] = 8                  # out of range: skipped, flagged
+    ids[2, 0] = -5
+    y, err = _gpu(q4k, c, ids, c["wts"])
+    assert err == 2                # Q4K_DEVERR_BAD_EXPERT
+    yref, bound = _bound(c, ids, c["wts"], list(range(4)))
+    _check(y, yref, bound, "dup/bad ids")
+
+
+def test_moe_relabel_invariance_and_determinism(q4k):
+    c = _make(8, 512, 256, 5, 2, seed=9)
+    y1, _ = _gpu(q4k, c)
+    y1b, _ = _gpu(q4k, c)
+    assert np.array_equal(y1, y1b)
+    perm = np.array([3, 7, 0, 1, 6, 2, 5, 4])   # new slot p holds old expert perm[p]
+    inv = torch.from_numpy(np.argsort(perm).astype(np.int32))
+    s = c["stride"]
+
+    def permute(w):
+        wn = w.numpy()
+        return torch.from_numpy(np.concatenate([wn[perm[p] * s:(perm[p] + 1) * s] for p in range(8)]))
+
+    c2 = dict(c, wg=permute(c["wg"]), wu=permute(c["wu"]), wd=permute(c["wd"]))
+    y2, _ = _gpu(q4k, c2, inv[c["ids"].long()], c["wts"])
+    assert np.array_equal(y1, y2)      # same pairs, same per-column arithmetic
+
+
+def test_moe_235b_class_sampled_tokens(q4k):
+    # 128 experts, hidden 4096, expert ffn 1536, 16 decode tokens, top-8 Zipf(1.1)
+    E, H, F, T, K = 128, 4096, 1536, 16, 8
+    stride = F * (H // 256) * 144
+    wg = synth.q4k_weight(E * F, H, seed=41, device=DEV).reshape(-1)
+    wu = synth.q4k_weight(E * F, H, seed=42, device=DEV).reshape(-1)
+    wd = synth.q4k_weight(E * H, F, seed=43, device=DEV).reshape(-1)
+    x = synth.bf16_normal((T, H), seed=44)
+    ids, wts = synth.zipf_routing(T, E, K, seed=45)
+    y = q4k.q4k_moe_gemv(wg, wu, wd, stride, E, H, F, x.to(DEV), ids.to(DEV), wts.to(DEV))
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    tokens = [0, 7, 15]
+    used = sorted({int(e) for t in tokens for e in ids[t].tolist()})
+    # oracle on the experts these tokens use (copied to the host)
+    c = dict(wg=wg.cpu(), wu=wu.cpu(), wd=wd.cpu(), stride=stride, E=E, H=H, F=F, x=x)
+    yref, bound = _bound(c, ids, wts, tokens)
+    _check(y.cpu().numpy().astype(np.float64)[tokens], yref, bound, "235B-class")
+    assert len(used) > 1
