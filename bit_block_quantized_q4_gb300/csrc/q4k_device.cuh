@@ -45,6 +45,22 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A * B + C, m16n8k16, fp16 operands, fp32 accumulate (same fragments).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // Same with C = 0 (starts a fresh accumulation).
 __device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                             uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -62,6 +78,23 @@ constexpr uint32_t kBf16Magic = 0x43004300u;
 __device__ __forceinline__ uint32_t nib_lo(uint32_t w) { return (w & 0x000F000Fu) | kBf16Magic; }
 __device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
   return ((w >> 4) & 0x000F000Fu) | kBf16Magic;
+}
+// (w & 0x000F000F) | magic as one LOP3 (lookup 0xEA = (a & b) | c), with the
+// magic held in a register so that the mask can be the immediate operand.
+__device__ __forceinline__ uint32_t lop_nib(uint32_t w, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;\n" : "=r"(d) : "r"(w), "r"(magic_reg));
+  return d;
+}
+// fp16 0x6400 is 1024.0 with a unit last place and ten mantissa bits, so
+// (w & 0x000F000F) | 0x64006400 is the pair (1024+q0, 1024+q2) of the low
+// nibbles of bytes 0 and 2, and (w & 0x00F000F0) | 0x64006400 the pair
+// (1024+16 q0', 1024+16 q2') of their high nibbles -- no shift needed.
+constexpr uint32_t kF16Magic = 0x64006400u;
+__device__ __forceinline__ uint32_t lop_nib_hi16(uint32_t w, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;\n" : "=r"(d) : "r"(w), "r"(magic_reg));
+  return d;
 }
 
 // ----------------------------------------------------------------- mbarrier

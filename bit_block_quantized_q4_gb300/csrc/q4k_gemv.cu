@@ -82,12 +82,21 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 }
 
 // ---------------------------------------------------------------- batch 1
+// MMA mapping (per super-block, 16 steps s = 2G + e, G = 0..7):
+//   thread (g, t) owns quant chunk t of rows g and g+8; word G of the chunk
+//   holds positions 4G..4G+3 of sub-blocks 2t (low nibbles) and 2t+1 (high).
+//   Step e = 0 feeds the low nibbles, e = 1 the high ones: k-slots (2t, 2t+1)
+//   carry positions (4G, 4G+2) and k-slots (2t+8, 2t+9) positions
+//   (4G+1, 4G+3) of sub-block 2t+e.
+//   MMA column n is sub-block n: lane (g, t) feeds x of sub-block g in both
+//   b0 and b1 when g = 2t + e, zeros otherwise, so accumulator column n sums
+//   exactly sub-block n and thread t ends with sub-blocks 2t, 2t+1 of its rows.
 // Shared memory per warp: STAGES weight tiles (16*MT rows x S super-blocks,
-// row stride S*144 bytes) | x of the warp's slice, permuted so that word 2q of
-// a sub-block holds (x[4q], x[4q+2]) and word 2q+1 holds (x[4q+1], x[4q+3]) |
-// the fp32 sums X_j of its sub-blocks | 16 zero words | STAGES mbarriers.
+// row stride S*144 bytes) | x of the warp's slice, word 2G of a sub-block
+// holding (x[4G], x[4G+2]) and word 2G+1 (x[4G+1], x[4G+3]) | the fp32 sums X_j
+// of its sub-blocks | 64 zero bytes | STAGES mbarriers.
 template <int MT, int S, int STAGES>
-__global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const GemvArgs a) {
   constexpr int kStageBytes = MT * S * kTileBytes;
   constexpr int kRowBytes = S * kBlockBytes;
@@ -103,9 +112,9 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
 
   uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
   uint8_t *ring = wreg;
-  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * kStageBytes);
+  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * kStageBytes);  // ks*128 words
   float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);
+  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);              // 16 words
   uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);
   float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
 
@@ -125,23 +134,48 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   // The weights above do not depend on earlier kernels; x does.
   grid_dependency_wait();
   grid_launch_dependents();
-  // x slice -> permuted shared copy and per-sub-block sums (8 values per lane
-  // per iteration; lanes 4j..4j+3 hold sub-block j of a 256-value step).
+  // x slice -> shared copy as fp16 scaled by 2^s, with s chosen so that the
+  // slice's largest magnitude lands in [2^14, 2^15): the scaled value is exact
+  // for every entry within 2^28 of that maximum.  The copy is permuted so that
+  // word 2q of a sub-block holds (x[4q], x[4q+2]) and word 2q+1 holds
+  // (x[4q+1], x[4q+3]); the fp32 sums X_j of the scaled values go next to it.
+  // 8 values per lane per iteration; lanes 4j..4j+3 cover sub-block j.
+  float unscale;
   {
     const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + (int64_t)sb0 * kQK);
+    uint32_t mx = 0;
     for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
       const uint4 u = __ldg(xs + c8);
-      uint4 o;
-      o.x = __byte_perm(u.x, u.y, 0x5410);
-      o.y = __byte_perm(u.x, u.y, 0x7632);
-      o.z = __byte_perm(u.z, u.w, 0x5410);
-      o.w = __byte_perm(u.z, u.w, 0x7632);
-      reinterpret_cast<uint4 *>(xperm)[c8] = o;
+      const uint32_t m01 = max(u.x & 0x7FFFu, (u.x >> 16) & 0x7FFFu);
+      const uint32_t m23 = max(u.y & 0x7FFFu, (u.y >> 16) & 0x7FFFu);
+      const uint32_t m45 = max(u.z & 0x7FFFu, (u.z >> 16) & 0x7FFFu);
+      const uint32_t m67 = max(u.w & 0x7FFFu, (u.w >> 16) & 0x7FFFu);
+      mx = max(mx, max(max(m01, m23), max(m45, m67)));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int emax = mx ? (int)(mx >> 7) - 127 : 0;  // exponent of the largest |x|
+    const int sh2 = min(126, max(-126, 14 - emax));
+    const float scale = __int_as_float((127 + sh2) << 23);
+    unscale = __int_as_float((127 - sh2) << 23);
+    for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
+      const uint4 u = __ldg(xs + c8);
       const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
       const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
       const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z));
       const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.w));
-      float sum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+      const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
+      const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
+      const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
+      const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
+      uint4 o;
+      o.x = *reinterpret_cast<const uint32_t *>(&h02);
+      o.y = *reinterpret_cast<const uint32_t *>(&h13);
+      o.z = *reinterpret_cast<const uint32_t *>(&h46);
+      o.w = *reinterpret_cast<const uint32_t *>(&h57);
+      reinterpret_cast<uint4 *>(xperm)[c8] = o;
+      const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
+      const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
+      float sum = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       if ((lane & 3) == 0) xsum[c8 >> 2] = sum;
@@ -150,13 +184,14 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   }
   __syncwarp();
 
-  // B fragments: lane (g, t) carries sub-block g iff g/2 == t, in b0 for even g
-  // and in b1 for odd g; every other lane feeds zeros.
+  // B fragments: lane (g, t) with t == g/2 carries sub-block g on the steps of
+  // parity g & 1 (pointer pe for even steps, po for odd steps); all other
+  // (lane, step) combinations read zeros.
   const bool own = (t == (g >> 1));
-  const uint32_t *pb0 = (own && !(g & 1)) ? xperm + g * 16 : xzero;
-  const uint32_t *pb1 = (own && (g & 1)) ? xperm + g * 16 : xzero;
-  const int adv0 = (own && !(g & 1)) ? 128 : 0;
-  const int adv1 = (own && (g & 1)) ? 128 : 0;
+  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
+  const uint32_t *pe = own_e ? xperm + g * 16 : xzero;
+  const uint32_t *po = own_o ? xperm + g * 16 : xzero;
+  const int adv_e = own_e ? 128 : 0, adv_o = own_o ? 128 : 0;
 
   // Scale/min decode of sub-blocks 2t, 2t+1, branch-free: lanes t < 2 read the
   // low six bits of s[j], s[j+4]; lanes t >= 2 combine a nibble of s[j+4] with
@@ -170,101 +205,110 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   float2 yacc[MT];  // rows (g, g+8)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
+  // The magic constant lives in a register so each nibble op is one LOP3.
+  uint32_t magic;
+  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
 
   bool ok = true;
-  int stage = 0;
   uint32_t phase = 0;
-  const uint32_t *p0 = pb0, *p1 = pb1;
-  for (int it = 0; it < nstages && ok; ++it) {
-    if (!mbar_wait(&bars[stage], phase, a.err)) {
-      ok = false;
-      break;
-    }
-    uint8_t *st = ring + stage * kStageBytes;
-    const int cnt = min(S, nsteps - it * S);
+  const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
+  for (int base = 0; base < nstages && ok; base += STAGES, phase ^= 1u) {
 #pragma unroll
-    for (int u = 0; u < S; ++u) {
-      if (u >= cnt) break;
-      const int i = it * S + u;  // super-block index within the slice
-      uint4 hdr[MT][2], qa[MT][2][2];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kRowBytes + u * kBlockBytes;
-          hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
-          qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
-          qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
-        }
+    for (int stage = 0; stage < STAGES; ++stage) {
+      const int it = base + stage;
+      if (it >= nstages) break;
+      if (!mbar_wait(&bars[stage], phase, a.err)) {
+        ok = false;
+        break;
       }
-      if (u == cnt - 1) {  // stage fully read: refill it
-        __syncwarp();
-        if (lane == 0 && it + STAGES < nstages) {
-          mbar_arrive_expect_tx(&bars[stage], kStageBytes);
-          load_tile(st, &wmap, &bars[stage], sb0 + (it + STAGES) * S, row0, policy);
+      uint8_t *st = ring + stage * kStageBytes;
+      const int cnt = min(S, nsteps - it * S);
+#pragma unroll
+      for (int u = 0; u < S; ++u) {
+        if (u >= cnt) break;
+        const int i = it * S + u;  // super-block index within the slice
+        uint4 hdr[MT][2], qa[MT][2][2];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint8_t *rp =
+                st + (mt * kRowsPerTile + g + 8 * r) * kRowBytes + u * kBlockBytes;
+            hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
+            qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
+            qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
+          }
         }
-      }
+        if (u == cnt - 1) {  // stage fully read: refill it
+          __syncwarp();
+          if (lane == 0 && it + STAGES < nstages) {
+            mbar_arrive_expect_tx(&bars[stage], kStageBytes);
+            load_tile(st, &wmap, &bars[stage], sb0 + (it + STAGES) * S, row0, policy);
+          }
+        }
 
-      float acc[MT][4];
-      const float2 xs2 = reinterpret_cast<const float2 *>(xsum + i * 8)[t];  // X_{2t}, X_{2t+1}
+        float acc[MT][4];
+        const float2 xs2 = px[4 * i];  // X_{2t}, X_{2t+1} of super-block i
 #pragma unroll
-      for (int G = 0; G < 4; ++G) {
-        const uint4 bb0 = reinterpret_cast<const uint4 *>(p0)[G];
-        const uint4 bb1 = reinterpret_cast<const uint4 *>(p1)[G];
+        for (int G2 = 0; G2 < 4; ++G2) {
+          const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // words 4G2 .. 4G2+3
+          const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int wi = 2 * G + (e >> 1);  // quant word (4 bytes of the chunk)
-          const int sh8 = (e & 1) * 8;      // positions (o, o+2) or (o+1, o+3)
-          const uint32_t b0 = word_of(bb0, e), b1 = word_of(bb1, e);
+          for (int h = 0; h < 2; ++h) {
+            const int G = 2 * G2 + h;  // quant word of the chunk
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t w0 = word_of(qa[mt][0][wi >> 2], wi & 3) >> sh8;
-            const uint32_t w1 = word_of(qa[mt][1][wi >> 2], wi & 3) >> sh8;
-            if (G == 0 && e == 0)
-              mma_bf16_zc(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
-            else
-              mma_bf16(acc[mt], nib_lo(w0), nib_lo(w1), nib_hi(w0), nib_hi(w1), b0, b1);
+            for (int e = 0; e < 2; ++e) {
+              const uint4 &bb = e ? bo : be;
+              const uint32_t b0 = h ? bb.z : bb.x, b1 = h ? bb.w : bb.y;
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
+                const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
+                uint32_t a0, a1, a2, a3;
+                if (e == 0) {  // low nibbles, 1024+q: sub-block 2t
+                  a0 = lop_nib(w0, magic);
+                  a1 = lop_nib(w1, magic);
+                  a2 = lop_nib(w0 >> 8, magic);
+                  a3 = lop_nib(w1 >> 8, magic);
+                } else {       // high nibbles, 1024+16q: sub-block 2t+1
+                  a0 = lop_nib_hi16(w0, magic);
+                  a1 = lop_nib_hi16(w1, magic);
+                  a2 = lop_nib_hi16(w0 >> 8, magic);
+                  a3 = lop_nib_hi16(w1 >> 8, magic);
+                }
+                if (G == 0 && e == 0)
+                  mma_f16_zc(acc[mt], a0, a1, a2, a3, b0, b1);
+                else
+                  mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+              }
+            }
+          }
+        }
+        pe += adv_e;
+        po += adv_o;
+        // acc = sum (1024 + q) x (sub-block 2t) and sum (1024 + 16 q) x
+        // (sub-block 2t+1) per row: subtract 1024 X, undo the 16, apply the
+        // scales (lanes own sub-blocks 2t, 2t+1 of rows g, g+8).
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint4 h = hdr[mt][r];
+            const uint32_t srcS = upper ? h.w : h.y;
+            const uint32_t srcM = upper ? h.w : h.z;
+            const uint32_t sc2 = ((srcS >> sh) & mlo) | ((h.y >> (sh + 2)) & mhi);
+            const uint32_t m2 = ((srcM >> sh_m) & mlo) | ((h.z >> (sh + 2)) & mhi);
+            const float d = half_lo_to_float(h.x), dmin = half_hi_to_float(h.x);
+            const float ta = fmaf(-1024.f, xs2.x, acc[mt][2 * r]);
+            const float tb = fmaf(-1024.f, xs2.y, acc[mt][2 * r + 1]) * 0.0625f;
+            const float uu = fmaf((float)(sc2 >> 8), tb, (float)(sc2 & 0xFFu) * ta);
+            const float vv = fmaf((float)(m2 >> 8), xs2.y, (float)(m2 & 0xFFu) * xs2.x);
+            float &yv = r ? yacc[mt].y : yacc[mt].x;
+            yv = fmaf(d, uu, yv);
+            yv = fmaf(-dmin, vv, yv);
           }
         }
       }
-      p0 += adv0;
-      p1 += adv1;
-      // acc = sum (128+q) x per (row, sub-block); subtract 128 X, apply the
-      // scales.  Rows g and g+8 are handled as a pair with packed fp32x2 math.
-      const float2 nC0 = make_float2(-128.f * xs2.x, -128.f * xs2.x);
-      const float2 nC1 = make_float2(-128.f * xs2.y, -128.f * xs2.y);
-      const float2 nX0 = make_float2(-xs2.x, -xs2.x);
-      const float2 nX1 = make_float2(-xs2.y, -xs2.y);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t sc2[2], m2[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint4 h = hdr[mt][r];
-          const uint32_t srcS = upper ? h.w : h.y;
-          const uint32_t srcM = upper ? h.w : h.z;
-          sc2[r] = ((srcS >> sh) & mlo) | ((h.y >> (sh + 2)) & mhi);
-          m2[r] = ((srcM >> sh_m) & mlo) | ((h.z >> (sh + 2)) & mhi);
-        }
-        const float2 sca = make_float2((float)(sc2[0] & 0xFFu), (float)(sc2[1] & 0xFFu));
-        const float2 scb = make_float2((float)(sc2[0] >> 8), (float)(sc2[1] >> 8));
-        const float2 ma = make_float2((float)(m2[0] & 0xFFu), (float)(m2[1] & 0xFFu));
-        const float2 mb = make_float2((float)(m2[0] >> 8), (float)(m2[1] >> 8));
-        const float2 dd =
-            make_float2(half_lo_to_float(hdr[mt][0].x), half_lo_to_float(hdr[mt][1].x));
-        const float2 dm =
-            make_float2(half_hi_to_float(hdr[mt][0].x), half_hi_to_float(hdr[mt][1].x));
-        const float2 ta = __fadd2_rn(make_float2(acc[mt][0], acc[mt][2]), nC0);
-        const float2 tb = __fadd2_rn(make_float2(acc[mt][1], acc[mt][3]), nC1);
-        const float2 uu = __ffma2_rn(scb, tb, __fmul2_rn(sca, ta));
-        const float2 vv = __ffma2_rn(mb, nX1, __fmul2_rn(ma, nX0));  // -(m_a X_a + m_b X_b)
-        yacc[mt] = __ffma2_rn(dd, uu, yacc[mt]);
-        yacc[mt] = __ffma2_rn(dm, vv, yacc[mt]);
-      }
-    }
-    if (++stage == STAGES) {
-      stage = 0;
-      phase ^= 1u;
     }
   }
 
@@ -273,7 +317,7 @@ __global__ void __launch_bounds__(512) gemv_b1_kernel(const __grid_constant__ CU
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float v = r ? yacc[mt].y : yacc[mt].x;
+      float v = (r ? yacc[mt].y : yacc[mt].x) * unscale;
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
@@ -516,7 +560,7 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
   Plan best;
   const int tile_rows = mt * kRowsPerTile;
   const int grid = (n + tile_rows - 1) / tile_rows;
-  for (int wk = 1; wk <= 16; ++wk) {
+  for (int wk = 1; wk <= (b1 ? 8 : 16); ++wk) {
     int ks = (nsb + wk - 1) / wk;
     ks = (ks + s - 1) / s * s;
     if ((nsb + ks - 1) / ks != wk) continue;  // no empty warps
