@@ -54,6 +54,8 @@ constexpr int kRowsPerTile = 16;
 constexpr int kTileBytes = kRowsPerTile * kBlockBytes;  // 2304, a multiple of 128
 
 struct GemvArgs {
+  const uint8_t *w;      // weights (row-major super-blocks)
+  int64_t row_bytes;     // bytes per weight row
   const __nv_bfloat16 *x;
   float *y;
   int64_t ldx, ldy;
@@ -79,6 +81,182 @@ __device__ __forceinline__ void load_tile(void *dst, const CUtensorMap *map, uin
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Lane constants of the batch-1 scale/min decode (sub-blocks 2t, 2t+1).
+struct B1Lane {
+  bool upper;     // t >= 2: sub-blocks 4..7
+  uint32_t psel;  // PRMT selector gathering bytes k0, k0+1 of rows g and g+8
+  uint32_t mlo4, mhi4;
+};
+
+__device__ __forceinline__ B1Lane b1_lane(int t) {
+  B1Lane l;
+  l.upper = t >= 2;
+  const uint32_t k0 = 2 * (t & 1);  // byte of sub-block 2t within its word
+  l.psel = k0 | ((k0 + 1) << 4) | ((k0 + 4) << 8) | ((k0 + 5) << 12);
+  l.mlo4 = l.upper ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+  l.mhi4 = l.upper ? 0x30303030u : 0u;
+  return l;
+}
+
+// One super-block of 16*MT rows for batch 1: hdr/qa hold the two rows (g, g+8)
+// of each m-tile (header; quant chunk t), pe/po the B fragments of the even /
+// odd steps, xs2 the scaled sums (X_{2t}, X_{2t+1}).  Adds the super-block's
+// contribution (in scaled units) to yacc[mt] = (row g, row g+8).
+template <int MT>
+__device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const uint4 (&qa)[MT][2][2],
+                                               const uint32_t *pe, const uint32_t *po,
+                                               const float2 xs2, const B1Lane &lc, uint32_t magic,
+                                               float2 (&yacc)[MT]) {
+  const bool upper = lc.upper;
+  const uint32_t psel = lc.psel, mlo4 = lc.mlo4, mhi4 = lc.mhi4;
+        // Two accumulator sets: even steps add only to column 2t (accE[0], [2]),
+  // odd steps only to column 2t+1 (accO[1], [3]), so splitting them halves
+  // the dependent MMA chain at no cost.
+  float accE[MT][4], accO[MT][4];
+#pragma unroll
+  for (int G2 = 0; G2 < 4; ++G2) {
+    const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // words 4G2 .. 4G2+3
+    const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int G = 2 * G2 + h;  // quant word of the chunk
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
+        const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
+        const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
+        // low nibbles, 1024+q: sub-block 2t
+        const uint32_t be0 = h ? be.z : be.x, be1 = h ? be.w : be.y;
+        if (G == 0)
+          mma_f16_zc(accE[mt], lop_nib(w0, magic), lop_nib(w1, magic), lop_nib(w0s, magic),
+                     lop_nib(w1s, magic), be0, be1);
+        else
+          mma_f16(accE[mt], lop_nib(w0, magic), lop_nib(w1, magic), lop_nib(w0s, magic),
+                  lop_nib(w1s, magic), be0, be1);
+        // high nibbles, 1024+16q: sub-block 2t+1
+        const uint32_t bo0 = h ? bo.z : bo.x, bo1 = h ? bo.w : bo.y;
+        if (G == 0)
+          mma_f16_zc(accO[mt], lop_nib_hi16(w0, magic), lop_nib_hi16(w1, magic),
+                     lop_nib_hi16(w0s, magic), lop_nib_hi16(w1s, magic), bo0, bo1);
+        else
+          mma_f16(accO[mt], lop_nib_hi16(w0, magic), lop_nib_hi16(w1, magic),
+                  lop_nib_hi16(w0s, magic), lop_nib_hi16(w1s, magic), bo0, bo1);
+      }
+    }
+  }
+  // accE[.][0|2] = sum (1024 + q) x of sub-block 2t, accO[.][1|3] =
+  // sum (1024 + 16 q) x of sub-block 2t+1 (rows g | g+8): subtract
+  // 1024 X, undo the 16, apply the scales.  The scale/min bytes of both
+  // rows are gathered into one word each with PRMT.
+  const float n1024X0 = -1024.f * xs2.x, n1024X1 = -1024.f * xs2.y;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const uint4 h0 = hdr[mt][0], h1 = hdr[mt][1];
+    const uint32_t py = __byte_perm(h0.y, h1.y, psel);  // s[k0], s[k0+1] of g, g+8
+    const uint32_t pz = __byte_perm(h0.z, h1.z, psel);  // s[k0+4], s[k0+5]
+    const uint32_t pw = __byte_perm(h0.w, h1.w, psel);  // s[k0+8], s[k0+9]
+    // lanes t < 2: sc = s[j] & 63, m = s[j+4] & 63; lanes t >= 2:
+    // sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4
+    const uint32_t sc4 = ((upper ? pw : py) & mlo4) | ((py >> 2) & mhi4);
+    const uint32_t m4 = ((upper ? (pw >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t h = r ? h1.x : h0.x;
+      const float d = half_lo_to_float(h), dmin = half_hi_to_float(h);
+      const float sca = (float)((sc4 >> (16 * r)) & 0xFFu);
+      const float scb = (float)((sc4 >> (16 * r + 8)) & 0xFFu);
+      const float ma = (float)((m4 >> (16 * r)) & 0xFFu);
+      const float mb = (float)((m4 >> (16 * r + 8)) & 0xFFu);
+      const float ta = accE[mt][2 * r] + n1024X0;
+      const float tb = (accO[mt][2 * r + 1] + n1024X1) * 0.0625f;
+      const float uu = fmaf(scb, tb, sca * ta);
+      const float vv = fmaf(mb, xs2.y, ma * xs2.x);
+      float &yv = r ? yacc[mt].y : yacc[mt].x;
+      yv = fmaf(d, uu, yv);
+      yv = fmaf(-dmin, vv, yv);
+    }
+  }
+}
+
+// Stage a warp's x slice (nsb super-blocks of bf16 x at xs) for batch 1: an
+// fp16 copy scaled by 2^s, s chosen so that the slice's largest magnitude lands
+// in [2^14, 2^15) (the scaled value is exact for every entry within 2^28 of that
+// maximum), permuted so that word 2G of a sub-block holds (x[4G], x[4G+2]) and
+// word 2G+1 (x[4G+1], x[4G+3]); the fp32 sums X_j of the scaled values; 16 zero
+// words.  8 values per lane per iteration; lanes 4j..4j+3 cover sub-block j.
+// Returns 2^-s.
+__device__ __forceinline__ float b1_stage_x(const __nv_bfloat16 *x, int nsb, uint32_t *xperm,
+                                            float *xsum, uint32_t *xzero, int lane) {
+  const uint4 *xs = reinterpret_cast<const uint4 *>(x);
+  uint32_t mx = 0;
+  for (int c8 = lane; c8 < nsb * 32; c8 += 32) {
+    const uint4 u = __ldg(xs + c8);
+    const uint32_t m01 = max(u.x & 0x7FFFu, (u.x >> 16) & 0x7FFFu);
+    const uint32_t m23 = max(u.y & 0x7FFFu, (u.y >> 16) & 0x7FFFu);
+    const uint32_t m45 = max(u.z & 0x7FFFu, (u.z >> 16) & 0x7FFFu);
+    const uint32_t m67 = max(u.w & 0x7FFFu, (u.w >> 16) & 0x7FFFu);
+    mx = max(mx, max(max(m01, m23), max(m45, m67)));
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  const int emax = mx ? (int)(mx >> 7) - 127 : 0;  // exponent of the largest |x|
+  const int sh2 = min(126, max(-126, 14 - emax));
+  const float scale = __int_as_float((127 + sh2) << 23);
+  for (int c8 = lane; c8 < nsb * 32; c8 += 32) {
+    const uint4 u = __ldg(xs + c8);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z));
+    const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.w));
+    const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
+    const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
+    const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
+    const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
+    uint4 o;
+    o.x = *reinterpret_cast<const uint32_t *>(&h02);
+    o.y = *reinterpret_cast<const uint32_t *>(&h13);
+    o.z = *reinterpret_cast<const uint32_t *>(&h46);
+    o.w = *reinterpret_cast<const uint32_t *>(&h57);
+    reinterpret_cast<uint4 *>(xperm)[c8] = o;
+    const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
+    const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
+    float sum = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if ((lane & 3) == 0) xsum[c8 >> 2] = sum;
+  }
+  if (lane < 16) xzero[lane] = 0u;
+  __syncwarp();
+  return __int_as_float((127 - sh2) << 23);
+}
+
+// Batch 1 epilogue: quad reduction (sub-blocks 2t, 2t+1 -> the row), then the
+// split-K partials of the CTA's warps in warp order, store y.
+template <int MT>
+__device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], float unscale, bool ok,
+                                          float *red, int row0, const GemvArgs &a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float v = (r ? yacc[mt].y : yacc[mt].x) * unscale;
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
+    }
+  }
+  __syncwarp();
+  if (!ok && lane == 0) red[warp * (MT * kRowsPerTile)] = __int_as_float(0x7fc00000);
+  __syncthreads();
+  if (threadIdx.x < MT * kRowsPerTile) {
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) sum += red[w * (MT * kRowsPerTile) + threadIdx.x];
+    const int row = row0 + threadIdx.x;
+    if (row < a.n) a.y[row] = sum;
+  }
 }
 
 // ---------------------------------------------------------------- batch 1
@@ -134,55 +312,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   // The weights above do not depend on earlier kernels; x does.
   grid_dependency_wait();
   grid_launch_dependents();
-  // x slice -> shared copy as fp16 scaled by 2^s, with s chosen so that the
-  // slice's largest magnitude lands in [2^14, 2^15): the scaled value is exact
-  // for every entry within 2^28 of that maximum.  The copy is permuted so that
-  // word 2q of a sub-block holds (x[4q], x[4q+2]) and word 2q+1 holds
-  // (x[4q+1], x[4q+3]); the fp32 sums X_j of the scaled values go next to it.
-  // 8 values per lane per iteration; lanes 4j..4j+3 cover sub-block j.
-  float unscale;
-  {
-    const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + (int64_t)sb0 * kQK);
-    uint32_t mx = 0;
-    for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
-      const uint4 u = __ldg(xs + c8);
-      const uint32_t m01 = max(u.x & 0x7FFFu, (u.x >> 16) & 0x7FFFu);
-      const uint32_t m23 = max(u.y & 0x7FFFu, (u.y >> 16) & 0x7FFFu);
-      const uint32_t m45 = max(u.z & 0x7FFFu, (u.z >> 16) & 0x7FFFu);
-      const uint32_t m67 = max(u.w & 0x7FFFu, (u.w >> 16) & 0x7FFFu);
-      mx = max(mx, max(max(m01, m23), max(m45, m67)));
-    }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    const int emax = mx ? (int)(mx >> 7) - 127 : 0;  // exponent of the largest |x|
-    const int sh2 = min(126, max(-126, 14 - emax));
-    const float scale = __int_as_float((127 + sh2) << 23);
-    unscale = __int_as_float((127 - sh2) << 23);
-    for (int c8 = lane; c8 < nsteps * 32; c8 += 32) {
-      const uint4 u = __ldg(xs + c8);
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z));
-      const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.w));
-      const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
-      const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
-      const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
-      const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
-      uint4 o;
-      o.x = *reinterpret_cast<const uint32_t *>(&h02);
-      o.y = *reinterpret_cast<const uint32_t *>(&h13);
-      o.z = *reinterpret_cast<const uint32_t *>(&h46);
-      o.w = *reinterpret_cast<const uint32_t *>(&h57);
-      reinterpret_cast<uint4 *>(xperm)[c8] = o;
-      const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
-      const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
-      float sum = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      if ((lane & 3) == 0) xsum[c8 >> 2] = sum;
-    }
-    if (lane < 16) xzero[lane] = 0u;
-  }
-  __syncwarp();
+  const float unscale = b1_stage_x(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xzero, lane);
 
   // B fragments: lane (g, t) with t == g/2 carries sub-block g on the steps of
   // parity g & 1 (pointer pe for even steps, po for odd steps); all other
@@ -196,11 +326,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   // Scale/min decode of sub-blocks 2t, 2t+1, branch-free: lanes t < 2 read the
   // low six bits of s[j], s[j+4]; lanes t >= 2 combine a nibble of s[j+4] with
   // the top two bits of s[j-4] (scales) or s[j] (mins).
-  const bool upper = t >= 2;
-  const uint32_t sh = (t & 1) * 16;
-  const uint32_t sh_m = upper ? sh + 4 : sh;
-  const uint32_t mlo = upper ? 0x0F0Fu : 0x3F3Fu;
-  const uint32_t mhi = upper ? 0x3030u : 0u;
+  const B1Lane lc = b1_lane(t);
 
   float2 yacc[MT];  // rows (g, g+8)
 #pragma unroll
@@ -247,91 +373,100 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
           }
         }
 
-        float acc[MT][4];
-        const float2 xs2 = px[4 * i];  // X_{2t}, X_{2t+1} of super-block i
-#pragma unroll
-        for (int G2 = 0; G2 < 4; ++G2) {
-          const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // words 4G2 .. 4G2+3
-          const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int G = 2 * G2 + h;  // quant word of the chunk
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const uint4 &bb = e ? bo : be;
-              const uint32_t b0 = h ? bb.z : bb.x, b1 = h ? bb.w : bb.y;
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
-                const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
-                uint32_t a0, a1, a2, a3;
-                if (e == 0) {  // low nibbles, 1024+q: sub-block 2t
-                  a0 = lop_nib(w0, magic);
-                  a1 = lop_nib(w1, magic);
-                  a2 = lop_nib(w0 >> 8, magic);
-                  a3 = lop_nib(w1 >> 8, magic);
-                } else {       // high nibbles, 1024+16q: sub-block 2t+1
-                  a0 = lop_nib_hi16(w0, magic);
-                  a1 = lop_nib_hi16(w1, magic);
-                  a2 = lop_nib_hi16(w0 >> 8, magic);
-                  a3 = lop_nib_hi16(w1 >> 8, magic);
-                }
-                if (G == 0 && e == 0)
-                  mma_f16_zc(acc[mt], a0, a1, a2, a3, b0, b1);
-                else
-                  mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
-              }
-            }
-          }
-        }
+        b1_super_block<MT>(hdr, qa, pe, po, px[4 * i], lc, magic, yacc);
         pe += adv_e;
         po += adv_o;
-        // acc = sum (1024 + q) x (sub-block 2t) and sum (1024 + 16 q) x
-        // (sub-block 2t+1) per row: subtract 1024 X, undo the 16, apply the
-        // scales (lanes own sub-blocks 2t, 2t+1 of rows g, g+8).
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const uint4 h = hdr[mt][r];
-            const uint32_t srcS = upper ? h.w : h.y;
-            const uint32_t srcM = upper ? h.w : h.z;
-            const uint32_t sc2 = ((srcS >> sh) & mlo) | ((h.y >> (sh + 2)) & mhi);
-            const uint32_t m2 = ((srcM >> sh_m) & mlo) | ((h.z >> (sh + 2)) & mhi);
-            const float d = half_lo_to_float(h.x), dmin = half_hi_to_float(h.x);
-            const float ta = fmaf(-1024.f, xs2.x, acc[mt][2 * r]);
-            const float tb = fmaf(-1024.f, xs2.y, acc[mt][2 * r + 1]) * 0.0625f;
-            const float uu = fmaf((float)(sc2 >> 8), tb, (float)(sc2 & 0xFFu) * ta);
-            const float vv = fmaf((float)(m2 >> 8), xs2.y, (float)(m2 & 0xFFu) * xs2.x);
-            float &yv = r ? yacc[mt].y : yacc[mt].x;
-            yv = fmaf(d, uu, yv);
-            yv = fmaf(-dmin, vv, yv);
-          }
-        }
       }
     }
   }
 
-  // Quad reduction (sub-blocks 2t, 2t+1 -> the row), then across warps.
+  b1_finish<MT>(yacc, unscale, ok, red, row0, a);
+}
+
+// 16-byte read of streamed weights (read once: L2 evict-first).
+__device__ __forceinline__ uint4 ldg_stream(const void *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+// Batch 1 with the weights streamed by plain 16-byte loads into registers (one
+// super-block ahead, two register buffers) instead of a TMA ring: shared
+// memory holds only the staged x slice, so residency is bound by registers.
+// Same MMA mapping, x staging and epilogue as gemv_b1_kernel.
+template <int MT>
+__global__ void __launch_bounds__(256) gemv_b1_ldg_kernel(const GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int row0 = blockIdx.x * (MT * kRowsPerTile);
+  const int sb0 = warp * a.ks;
+  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);
+
+  uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
+  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg);
+  float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
+  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);
+  float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
+
+  // Rows past n read row n-1; their results are never stored.
+  const uint8_t *rp[MT][2];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float v = (r ? yacc[mt].y : yacc[mt].x) * unscale;
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
+      const int row = min(row0 + mt * kRowsPerTile + g + 8 * r, a.n - 1);
+      rp[mt][r] = a.w + (int64_t)row * a.row_bytes + (int64_t)sb0 * kBlockBytes;
     }
+  const uint64_t policy = l2_evict_first_policy();
+  uint4 hA[MT][2], qA[MT][2][2], hB[MT][2], qB[MT][2][2];
+  auto load = [&](uint4 (&h)[MT][2], uint4 (&q)[MT][2][2], int i) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint8_t *p = rp[mt][r] + (int64_t)i * kBlockBytes;
+        h[mt][r] = ldg_stream(p, policy);
+        q[mt][r][0] = ldg_stream(p + kQsOffset + 32 * t, policy);
+        q[mt][r][1] = ldg_stream(p + kQsOffset + 32 * t + 16, policy);
+      }
+  };
+  // The weights do not depend on earlier kernels; x does.
+  if (nsteps > 0) load(hA, qA, 0);
+  if (nsteps > 1) load(hB, qB, 1);
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const float unscale = b1_stage_x(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xzero, lane);
+
+  const bool own = (t == (g >> 1));
+  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
+  const uint32_t *pe = own_e ? xperm + g * 16 : xzero;
+  const uint32_t *po = own_o ? xperm + g * 16 : xzero;
+  const int adv_e = own_e ? 128 : 0, adv_o = own_o ? 128 : 0;
+  const B1Lane lc = b1_lane(t);
+  const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
+  uint32_t magic;
+  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
+
+  float2 yacc[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
+  for (int i = 0; i < nsteps; i += 2) {
+    b1_super_block<MT>(hA, qA, pe, po, px[4 * i], lc, magic, yacc);
+    pe += adv_e;
+    po += adv_o;
+    if (i + 2 < nsteps) load(hA, qA, i + 2);
+    if (i + 1 >= nsteps) break;
+    b1_super_block<MT>(hB, qB, pe, po, px[4 * (i + 1)], lc, magic, yacc);
+    pe += adv_e;
+    po += adv_o;
+    if (i + 3 < nsteps) load(hB, qB, i + 3);
   }
-  __syncwarp();
-  if (!ok && lane == 0) red[warp * (MT * kRowsPerTile)] = __int_as_float(0x7fc00000);
-  __syncthreads();
-  if (threadIdx.x < MT * kRowsPerTile) {
-    float sum = 0.f;
-    for (int w = 0; w < nwarps; ++w) sum += red[w * (MT * kRowsPerTile) + threadIdx.x];
-    const int row = row0 + threadIdx.x;
-    if (row < a.n) a.y[row] = sum;
-  }
+  b1_finish<MT>(yacc, unscale, true, red, row0, a);
 }
 
 // ---------------------------------------------------------------- batch 2..16
@@ -528,6 +663,9 @@ template <int S> struct B1Stages { static constexpr int value = S == 1 ? 4 : (S 
 #ifndef Q4K_GEMV_FORCE_MT
 #define Q4K_GEMV_FORCE_MT 0
 #endif
+#ifndef Q4K_GEMV_LDG  // batch 1: 1 = weights by 16-byte loads, 0 = TMA ring
+#define Q4K_GEMV_LDG 0
+#endif
 
 struct Plan {
   int mt = 1, s = 1, wk = 1, ks = 1, warp_bytes = 0, smem = 0, grid = 0;
@@ -574,7 +712,9 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
     const int waves = (grid + slots - 1) / slots;
     const int per_sm = std::min(occ, (grid + f->sm_count - 1) / f->sm_count);
     const int warps_sm = per_sm * wk;
-    const double inflight_kb = warps_sm * (stages - 1) * mt * s * kTileBytes / 1024.0;
+    // stages == 0: register-streamed kernel, about 1.5 super-blocks in flight
+    const double inflight_kb =
+        warps_sm * (stages ? stages - 1 : 1.5) * mt * s * kTileBytes / 1024.0;
     const double balance = (double)nsb / (double)(ks * wk);  // 1.0 = even split
     const double score = -1000.0 * waves + std::min(inflight_kb, 96.0) / 8.0 +
                          0.5 * std::min(warps_sm, 24) + 6.0 * balance + (mt == 2 ? 1.0 : 0.0);
@@ -610,6 +750,8 @@ void set_attributes(const DeviceFacts *f) {
   allow_smem(b1_kernel<1, 4>(), f);
   allow_smem(b1_kernel<2, 1>(), f);
   allow_smem(b1_kernel<2, 2>(), f);
+  allow_smem(gemv_b1_ldg_kernel<1>, f);
+  allow_smem(gemv_b1_ldg_kernel<2>, f);
   allow_smem(gemv_bn_kernel<1, 1, kStages>, f);
   allow_smem(gemv_bn_kernel<1, 2, kStages>, f);
   allow_smem(gemv_bn_kernel<2, 1, kStages>, f);
@@ -625,9 +767,8 @@ GemvKernel b1_select(int mt, int s) {
 
 }  // namespace
 
-template <typename K>
-cudaError_t launch(K kernel, const Plan &p, const CUtensorMap &map, const GemvArgs &args, bool pdl,
-                   cudaStream_t stream) {
+template <typename K, typename... Args>
+cudaError_t launch(K kernel, const Plan &p, bool pdl, cudaStream_t stream, Args... kargs) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
   cfg.blockDim = dim3((unsigned)(p.wk * 32), 1, 1);
@@ -638,7 +779,7 @@ cudaError_t launch(K kernel, const Plan &p, const CUtensorMap &map, const GemvAr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, map, args);
+  return cudaLaunchKernelEx(&cfg, kernel, kargs...);
 }
 
 cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
@@ -663,6 +804,8 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   };
 
   GemvArgs args;
+  args.w = static_cast<const uint8_t *>(w);
+  args.row_bytes = (int64_t)nsb * kBlockBytes;
   args.x = static_cast<const __nv_bfloat16 *>(x);
   args.y = y;
   args.ldx = ldx;
@@ -672,7 +815,21 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   args.batch = (int)batch;
   args.err = device_error_word();
 
-  if (batch == 1) {
+  if (batch == 1 && Q4K_GEMV_LDG) {
+    Plan p;
+    for (int mt = 1; mt <= 2; ++mt) {
+      if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
+      const Plan q = plan_for(mt == 2 ? gemv_b1_ldg_kernel<2> : gemv_b1_ldg_kernel<1>, true, mt, 1,
+                              0, (int)n, nsb, 1, f);
+      if (q.grid && q.score > p.score) p = q;
+    }
+    if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    args.ks = p.ks;
+    args.warp_bytes = p.warp_bytes;
+    cudaError_t e = launch(p.mt == 2 ? gemv_b1_ldg_kernel<2> : gemv_b1_ldg_kernel<1>, p, overlap,
+                           stream, args);
+    if (e != cudaSuccess) return e;
+  } else if (batch == 1) {
     Plan p;
     const int cand[5][2] = {{1, 1}, {1, 2}, {1, 4}, {2, 1}, {2, 2}};
     for (const auto &c : cand) {
@@ -688,7 +845,7 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     if (encode(p.mt, p.s) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
-    cudaError_t e = launch(kern, p, map, args, overlap, stream);
+    cudaError_t e = launch(kern, p, overlap, stream, map, args);
     if (e != cudaSuccess) return e;
   } else {
     const int mt = mt_bn;
@@ -700,7 +857,7 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     if (encode(mt, 1) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
-    cudaError_t e = launch(kern, p, map, args, overlap, stream);
+    cudaError_t e = launch(kern, p, overlap, stream, map, args);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
