@@ -524,3 +524,48 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
 }
 
 }  // namespace q4k
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Its workspace is a file-scope device array of a
+// fixed size, so a caller that cannot call cudaMalloc gets a working MoE call
+// without handing in memory.  Every GPU that loads the library holds this array
+// until the process exits.  All calls on a device share it: it keeps the last
+// call's contents, every byte a call reads is first written by that same call
+// (nothing needs clearing), and calls that overlap on the GPU race on it.
+namespace q4k {
+
+__device__ __align__(256) uint8_t g_moe_scratch[kMoeScratchBytes];
+
+namespace {
+
+void *g_scratch_ptr[64];
+cudaError_t g_scratch_status[64];
+std::once_flag g_scratch_once[64];
+
+// Host code may not use g_moe_scratch as an address (it names a host-side
+// stand-in); the device address is resolved once per device, with that device
+// current, on the first call made on it.
+void resolve_scratch(int dev) {
+  void *p = nullptr;
+  g_scratch_status[dev] = cudaGetSymbolAddress(&p, g_moe_scratch);
+  g_scratch_ptr[dev] = (g_scratch_status[dev] == cudaSuccess) ? p : nullptr;
+}
+
+}  // namespace
+
+cudaError_t launch_moe_scratch(const void *w_gate, const void *w_up, const void *w_down,
+                               int64_t expert_stride, int32_t n_experts, int64_t hidden,
+                               int64_t ffn, const void *x, int32_t n_tokens, int64_t ldx,
+                               const int32_t *ids, const float *wts, int32_t top_k, float *y,
+                               int64_t ldy, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(g_scratch_once[dev], resolve_scratch, dev);
+  if (g_scratch_ptr[dev] == nullptr) return g_scratch_status[dev];
+  return launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x, n_tokens, ldx,
+                    ids, wts, top_k, y, ldy, g_scratch_ptr[dev], stream);
+}
+
+}  // namespace q4k

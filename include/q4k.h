@@ -184,6 +184,30 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
                  int64_t ldy, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4k_moe_gemv_noalloc -- q4k_moe_gemv without a caller-provided workspace.
+ * (The pages have no counterpart of this call; it is a convenience of this
+ *  library.)  For callers that cannot allocate device memory per call: engines
+ * that carve all device memory into their own arena at start-up, or plugin and
+ * host code that does not own the allocator.  The workspace is instead a
+ * device array inside the library of Q4K_MOE_NOALLOC_SCRATCH_BYTES bytes,
+ * held on every GPU that loads the library until the process exits.
+ *   - Arguments, results and errors as q4k_moe_gemv; a problem whose
+ *     q4k_moe_workspace_size(...) exceeds the array returns Q4K_ERR_WORKSPACE
+ *     before anything runs.  It allocates nothing (no cudaMalloc, no cudaFree,
+ *     no allocating library routine).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array: calls that overlap on the
+ *     GPU (different streams, or concurrent host threads) race on it.  Each
+ *     call writes every workspace byte it reads, so no clearing is needed.
+ */
+#define Q4K_MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int q4k_moe_gemv_noalloc(const void *w_gate, const void *w_up, const void *w_down,
+                         int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                         const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                         const float *wts, int32_t top_k, float *y, int64_t ldy, void *stream);
+
+/*
  * q4k_get_device_error -- synchronize `stream`, return the device error word
  * (Q4K_DEVERR_* bits) in *bits and clear it.  Returns Q4K_ERR_DATA when any bit
  * was set, Q4K_OK otherwise, Q4K_ERR_NULL if bits is NULL, Q4K_ERR_CUDA on a
