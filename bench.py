@@ -264,39 +264,139 @@ def bench_c0_pool(q4k, steps, warmup, dev, stream):
 
 # ------------------------------------------------------------------ CPU baseline
 
-def cpu_baseline(budget_s=12.0):
+def cpu_baseline(layers, budget_s=12.0):
     """The oracle as it stands, timed on the host cores, on a bounded sample of
-    the headline workload: the first 256 rows of each projection of as many
-    layers as fit the time budget (input generation is not timed)."""
+    the headline workload: the same weights and activations (copied to the
+    host), whole projections in pass order until about budget_s of oracle time
+    (copies are not timed)."""
     import oracle
     oracle.build()
-    nrows = 256
-
-    def sample(layer):
-        out = []
-        for pi, (name, n, k) in enumerate(LAYER_SHAPES):
-            w = synth.q4k_weight(nrows, k, seed=synth.derive_seed(SEED_C1, "w", layer, pi),
-                                 quants="normal").numpy()
-            x = synth.bf16_normal((1, k), seed=synth.derive_seed(SEED_C1, "x", 1, pi))
-            out.append((w, k, x.view(torch.int16).numpy().view(np.uint16)))
-        return out
-
-    elapsed, done_bytes, layers = 0.0, 0, 0
-    while elapsed < budget_s and layers < N_LAYERS:
-        for w, k, xb in sample(layers):
-            t = time.perf_counter()
-            oracle.gemv(w, nrows, k, xb)
-            elapsed += time.perf_counter() - t
-            done_bytes += q4k_bytes(nrows, k) + k * 2 + nrows * 4
-        layers += 1
+    elapsed, done_bytes, nproj = 0.0, 0, 0
+    for i, (name, n, k, w) in enumerate(layers.mats):
+        if elapsed >= budget_s:
+            break
+        wh = w.cpu().numpy()
+        x = synth.bf16_normal((1, k), seed=synth.derive_seed(SEED_C1 + 1, "x", 1, i))
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        oracle.gemv(wh, n, k, xb)
+        elapsed += time.perf_counter() - t
+        done_bytes += q4k_bytes(n, k) + k * 2 + n * 4
+        nproj += 1
     return {"value": round(done_bytes / elapsed / 1e9, 4), "unit": "GB/s",
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle GEMV, batch 1, first {nrows} rows of each of the 5 "
-                      f"projections of {layers} layer(s) ({done_bytes / 1e6:.1f} MB of Q4_K "
-                      f"weights), {elapsed:.1f} s of oracle time"}
+            "sample": f"fp64 oracle GEMV, batch 1, the first {nproj} projections of the pass "
+                      f"({done_bytes / 1e9:.2f} GB of Q4_K weights), {elapsed:.1f} s of oracle time"}
+
+
+def bench_prefill(q4k, dev, stream, reps=20):
+    """512-token prefill: gate (5120 -> 17408) and down (17408 -> 5120), each
+    timed on its own (events around `reps` launches; weights 50 MB each, X
+    5-18 MB, so L2 holds them across launches -- the GEMM is tensor-bound)."""
+    out = {}
+    m = 512
+    for name, n, k in (("gate", 17408, 5120), ("down", 5120, 17408)):
+        w = synth.q4k_weight(n, k, seed=synth.derive_seed(1003, "w", name), quants="normal", device=dev)
+        x = synth.bf16_normal((m, k), seed=synth.derive_seed(1003, "x", name), sigma=0.5, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                q4k.q4k_gemm(w, n, k, x, out=y, stream=stream)
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for _ in range(reps):
+                q4k.q4k_gemm(w, n, k, x, out=y, stream=stream)
+            e.record(stream)
+        torch.cuda.synchronize()
+        us = s.elapsed_time(e) * 1e3 / reps
+        flop = 2.0 * m * n * k
+        out[name] = {"us": round(us, 2), "tflops": round(flop / us / 1e6, 1)}
+    return out
+
+
+def bench_moe(q4k, dev, stream, reps=20):
+    """235B-A22B-class routed MoE decode: 128 experts, hidden 4096, expert ffn
+    1536, 16 tokens, top-8 Zipf(1.1).  Touched bytes = the distinct experts'
+    gate/up/down weights + x + y; the 1.36 GB expert pool exceeds L2."""
+    E, H, F, T, K = 128, 4096, 1536, 16, 8
+    stride = F * (H // 256) * 144
+    wg = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1004, "g"), device=dev).reshape(-1)
+    wu = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1004, "u"), device=dev).reshape(-1)
+    wd = synth.q4k_weight(E * H, F, seed=synth.derive_seed(1004, "d"), device=dev).reshape(-1)
+    x = synth.bf16_normal((T, H), seed=synth.derive_seed(1004, "x"), device=dev)
+    ids, wts = synth.zipf_routing(T, E, K, seed=1005)
+    distinct = len(set(ids.reshape(-1).tolist()))
+    ids_d, wts_d = ids.to(dev), wts.to(dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(q4k.q4k_moe_workspace_size(E, T, K, H, F), dtype=torch.uint8, device=dev)
+
+    def step():
+        q4k.q4k_moe_gemv(wg, wu, wd, stride, E, H, F, x, ids_d, wts_d, out=y, workspace=ws,
+                         stream=stream)
+
+    ms, per, g = time_graph(step, reps, 3, stream)
+    del g
+    nbytes = distinct * 3 * q4k_bytes(F, H) + T * H * 2 + T * H * 4
+    return {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_8tbs": round(nbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "distinct_experts": distinct, "bytes": nbytes}
+
+
+def profiled_traffic():
+    """Per-launch DRAM traffic of the batch-1 GEMV from the committed ncu summary
+    (profiles/gemv_b1_27b_layer.md), or None when the kernel source has changed
+    since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemv_b1_27b_layer.md")
+    src = os.path.join(ROOT, "bit_block_quantized_q4_gb300", "csrc", "q4k_gemv.cu")
+    if not os.path.exists(path):
+        return None
+    want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != want:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ------------------------------------------------------------------ main
+
+def run_case(case):
+    """One small instance of a kernel, for ncu captures (no timing): one 27B-class
+    layer of batch-1 projections (203 MB of weights), one 512-token gate
+    prefill, or one routed-MoE decode step."""
+    import bit_block_quantized_q4_gb300 as q4k
+    from bit_block_quantized_q4_gb300 import build as qb
+    qb.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    if case == "gemv_layer":
+        layers = Layers(dev, n_layers=1)
+        xs, ys = make_inputs(layers, 1, dev, seed=SEED_C1 + 1)
+        torch.cuda.synchronize()
+        for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
+            q4k.q4k_gemv(w, n, k, x, out=y)
+    elif case == "gemm_prefill":
+        n, k, m = 17408, 5120, 512
+        w = synth.q4k_weight(n, k, seed=synth.derive_seed(1003, "w", "gate"), quants="normal",
+                             device=dev)
+        x = synth.bf16_normal((m, k), seed=synth.derive_seed(1003, "x", "gate"), sigma=0.5,
+                              device=dev)
+        torch.cuda.synchronize()
+        q4k.q4k_gemm(w, n, k, x)
+    else:
+        bench_moe(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    print(f"case {case} ok")
+
 
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle as it stands, on the host cores, on a
@@ -347,7 +447,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemm_prefill", "moe"],
+                    help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -398,6 +503,7 @@ def main():
     e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
     e2e["value"] = round(e2e["value"] * world, 2)
 
+    cpu = cpu_baseline(layers) if rank == 0 else None
     extra = {}
     r = bench_decode(q4k, layers, 1, max(5, args.steps // 2), 3, dev, stream, overlap=False)
     extra["decode_b1_no_overlap"] = {"gbs": round(r["gbs"], 1),
@@ -415,7 +521,14 @@ def main():
         extra["gemv_4096_b1_pool"] = {"gbs": round(r["gbs"], 1),
                                       "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
                                       "us_per_gemv": round(r["us_per_gemv"], 3), "pool": r["pool"]}
-    cpu = cpu_baseline() if rank == 0 else None
+        torch.cuda.empty_cache()
+        pf = bench_prefill(q4k, dev, stream)
+        for nm, v in pf.items():
+            v["frac_of_measured_bf16"] = round(v["tflops"] / pk["bf16_tflops"], 4)
+            v["frac_of_sustained_bf16"] = round(v["tflops"] / pk["bf16_tflops_sustained"], 4)
+        extra["prefill_512"] = pf
+        torch.cuda.empty_cache()
+        extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
     clocks = sampler.summary()
 
     if rank == 0:
@@ -434,7 +547,8 @@ def main():
             "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                         "traffic": None, "peak_source": pk["source"],
+                         "traffic": profiled_traffic(), "peak_source": pk["source"],
+                         "algorithmic_bytes_per_launch": round(nbytes / launches),
                          "kernel": "gemv_b1_kernel (q4k_gemv, batch 1)",
                          "note": "algorithmic bytes of the 320 launches / step time (includes "
                                  "inter-launch gaps)"},
