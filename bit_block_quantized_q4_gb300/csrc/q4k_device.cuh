@@ -153,6 +153,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 }
 
 // ----------------------------------------------------------------- TMA
+// Untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
+// aligned, bytes a multiple of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 // Tiled tensor copy global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2) {

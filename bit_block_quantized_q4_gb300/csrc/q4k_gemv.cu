@@ -29,6 +29,7 @@
 // result is deterministic.  Grids are sized so that every CTA is resident at
 // once (one wave) whenever the shape allows.
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 #include <vector>
 
@@ -41,6 +42,12 @@
 #endif
 #ifndef Q4K_GEMV_PROMO  // L2 promotion of the weight tensor map: 0 none, 1 128 B, 2 256 B
 #define Q4K_GEMV_PROMO 2
+#endif
+#ifndef Q4K_GEMV_PRE_STAGES  // batch 1: weight stages issued before x and the dependency wait
+#define Q4K_GEMV_PRE_STAGES 2
+#endif
+#ifndef Q4K_GEMV_X_FIRST  // batch 1: 0 ring right after x, 1 ring once x has landed, 2 CTA barrier between
+#define Q4K_GEMV_X_FIRST 0
 #endif
 #ifndef Q4K_GEMV_EVICT_FIRST  // L2 evict-first hint on weight loads
 #define Q4K_GEMV_EVICT_FIRST 1
@@ -79,6 +86,10 @@ __device__ __forceinline__ void load_tile(void *dst, const CUtensorMap *map, uin
 #endif
 }
 
+// Count rounded up to a multiple of 4 (keeps what follows an fp32 array of
+// that many entries on a 16-byte boundary).
+__host__ __device__ __forceinline__ int pad4(int n) { return (n + 3) & ~3; }
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -107,11 +118,11 @@ __device__ __forceinline__ B1Lane b1_lane(int t) {
 template <int MT>
 __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const uint4 (&qa)[MT][2][2],
                                                const uint32_t *pe, const uint32_t *po,
-                                               const float2 xs2, const B1Lane &lc, uint32_t magic,
-                                               float2 (&yacc)[MT]) {
+                                               const float2 xs2, float us, const B1Lane &lc,
+                                               uint32_t magic, float2 (&yacc)[MT]) {
   const bool upper = lc.upper;
   const uint32_t psel = lc.psel, mlo4 = lc.mlo4, mhi4 = lc.mhi4;
-        // Two accumulator sets: even steps add only to column 2t (accE[0], [2]),
+  // Two accumulator sets: even steps add only to column 2t (accE[0], [2]),
   // odd steps only to column 2t+1 (accO[1], [3]), so splitting them halves
   // the dependent MMA chain at no cost.
   float accE[MT][4], accO[MT][4];
@@ -174,67 +185,92 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
       const float uu = fmaf(scb, tb, sca * ta);
       const float vv = fmaf(mb, xs2.y, ma * xs2.x);
       float &yv = r ? yacc[mt].y : yacc[mt].x;
-      yv = fmaf(d, uu, yv);
-      yv = fmaf(-dmin, vv, yv);
+      yv = fmaf(us, fmaf(-dmin, vv, d * uu), yv);  // back from the 2^s scaled units
     }
   }
 }
 
-// Stage a warp's x slice (nsb super-blocks of bf16 x at xs) for batch 1: an
-// fp16 copy scaled by 2^s, s chosen so that the slice's largest magnitude lands
-// in [2^14, 2^15) (the scaled value is exact for every entry within 2^28 of that
-// maximum), permuted so that word 2G of a sub-block holds (x[4G], x[4G+2]) and
-// word 2G+1 (x[4G+1], x[4G+3]); the fp32 sums X_j of the scaled values; 16 zero
-// words.  8 values per lane per iteration; lanes 4j..4j+3 cover sub-block j.
-// Returns 2^-s.
-__device__ __forceinline__ float b1_stage_x(const __nv_bfloat16 *x, int nsb, uint32_t *xperm,
-                                            float *xsum, uint32_t *xzero, int lane) {
+// Stage a warp's x slice (nsb super-blocks of bf16 x) for batch 1.  For each
+// super-block i: an fp16 copy of its 256 values scaled by 2^s_i, with s_i chosen
+// so that the super-block's largest magnitude lands in [2^14, 2^15) (the scaled
+// value is exact for every entry within 2^28 of that maximum), permuted so that
+// word 2G of a sub-block holds (x[4G], x[4G+2]) and word 2G+1 (x[4G+1],
+// x[4G+3]); the fp32 sums X_j of its scaled sub-blocks; unscale[i] = 2^-s_i.
+// Then 16 zero words.  Lane l handles values 8l .. 8l+7 of each super-block
+// (lanes 4j..4j+3 cover sub-block j); the loads of up to 8 super-blocks are all
+// issued before any of them is used.
+// kInPlace: x is the raw bf16 slice already copied into xperm's own words (each
+// lane rewrites only the 16 bytes it read); otherwise x is global memory.
+template <bool kInPlace>
+__device__ __forceinline__ void b1_stage_x(const __nv_bfloat16 *x, int nsb, uint32_t *xperm,
+                                           float *xsum, float *unscale, uint32_t *xzero, int lane) {
   const uint4 *xs = reinterpret_cast<const uint4 *>(x);
-  uint32_t mx = 0;
-  for (int c8 = lane; c8 < nsb * 32; c8 += 32) {
-    const uint4 u = __ldg(xs + c8);
-    const uint32_t m01 = max(u.x & 0x7FFFu, (u.x >> 16) & 0x7FFFu);
-    const uint32_t m23 = max(u.y & 0x7FFFu, (u.y >> 16) & 0x7FFFu);
-    const uint32_t m45 = max(u.z & 0x7FFFu, (u.z >> 16) & 0x7FFFu);
-    const uint32_t m67 = max(u.w & 0x7FFFu, (u.w >> 16) & 0x7FFFu);
-    mx = max(mx, max(max(m01, m23), max(m45, m67)));
-  }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  const int emax = mx ? (int)(mx >> 7) - 127 : 0;  // exponent of the largest |x|
-  const int sh2 = min(126, max(-126, 14 - emax));
-  const float scale = __int_as_float((127 + sh2) << 23);
-  for (int c8 = lane; c8 < nsb * 32; c8 += 32) {
-    const uint4 u = __ldg(xs + c8);
-    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z));
-    const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.w));
-    const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
-    const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
-    const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
-    const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
-    uint4 o;
-    o.x = *reinterpret_cast<const uint32_t *>(&h02);
-    o.y = *reinterpret_cast<const uint32_t *>(&h13);
-    o.z = *reinterpret_cast<const uint32_t *>(&h46);
-    o.w = *reinterpret_cast<const uint32_t *>(&h57);
-    reinterpret_cast<uint4 *>(xperm)[c8] = o;
-    const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
-    const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
-    float sum = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    if ((lane & 3) == 0) xsum[c8 >> 2] = sum;
+  constexpr int kChunk = 8;  // super-blocks in flight together (no early exit: full ILP)
+  for (int base = 0; base < nsb; base += kChunk) {
+    uint4 u[kChunk];
+    uint32_t mx[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      u[j] = (base + j >= nsb) ? make_uint4(0, 0, 0, 0)
+             : kInPlace     ? xs[(base + j) * 32 + lane]
+                            : __ldg(xs + (base + j) * 32 + lane);
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const uint4 v = u[j];
+      const uint32_t m01 = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
+      const uint32_t m23 = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+      const uint32_t m45 = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
+      const uint32_t m67 = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+      mx[j] = max(max(m01, m23), max(m45, m67));
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) mx[j] = __reduce_max_sync(0xffffffffu, mx[j]);
+    float sum[kChunk];
+    int sh2[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const uint4 v = u[j];
+      const int emax = mx[j] ? (int)(mx[j] >> 7) - 127 : 0;  // exponent of the largest |x|
+      sh2[j] = min(126, max(-126, 14 - emax));
+      const float scale = __int_as_float((127 + sh2[j]) << 23);
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z));
+      const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.w));
+      const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
+      const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
+      const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
+      const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
+      u[j].x = *reinterpret_cast<const uint32_t *>(&h02);
+      u[j].y = *reinterpret_cast<const uint32_t *>(&h13);
+      u[j].z = *reinterpret_cast<const uint32_t *>(&h46);
+      u[j].w = *reinterpret_cast<const uint32_t *>(&h57);
+      const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
+      const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
+      sum[j] = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], 1);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], 2);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      if (base + j < nsb) {
+        reinterpret_cast<uint4 *>(xperm)[(base + j) * 32 + lane] = u[j];
+        if ((lane & 3) == 0) xsum[(base + j) * 8 + (lane >> 2)] = sum[j];
+        if (lane == 0) unscale[base + j] = __int_as_float((127 - sh2[j]) << 23);
+      }
+    }
   }
   if (lane < 16) xzero[lane] = 0u;
   __syncwarp();
-  return __int_as_float((127 - sh2) << 23);
 }
 
 // Batch 1 epilogue: quad reduction (sub-blocks 2t, 2t+1 -> the row), then the
 // split-K partials of the CTA's warps in warp order, store y.
 template <int MT>
-__device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], float unscale, bool ok,
+__device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], bool ok,
                                           float *red, int row0, const GemvArgs &a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -242,7 +278,7 @@ __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], float unscal
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float v = (r ? yacc[mt].y : yacc[mt].x) * unscale;
+      float v = r ? yacc[mt].y : yacc[mt].x;
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
@@ -259,6 +295,23 @@ __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], float unscal
   }
 }
 
+// After a timed-out wait in a batch-1 warp: give the copies it may still have
+// in flight (the x slice when x_pending; the weight stages of iterations it ..
+// end-1) the same bounded time to land before the CTA exits and its
+// shared memory is handed to another CTA.
+template <int STAGES>
+__device__ __noinline__ void b1_drain(uint64_t *bars, int it, int end, bool x_pending) {
+  const uint64_t t0 = global_ns();
+  auto landed = [&](uint64_t *b, uint32_t parity) {
+    while (!mbar_try_wait(b, parity, 1000u))
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+  };
+  if (x_pending && !landed(&bars[STAGES], 0)) return;
+  for (int j = it; j < end; ++j)
+    if (!landed(&bars[j % STAGES], (j / STAGES) & 1)) return;
+}
+
 // ---------------------------------------------------------------- batch 1
 // MMA mapping (per super-block, 16 steps s = 2G + e, G = 0..7):
 //   thread (g, t) owns quant chunk t of rows g and g+8; word G of the chunk
@@ -272,7 +325,8 @@ __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], float unscal
 // Shared memory per warp: STAGES weight tiles (16*MT rows x S super-blocks,
 // row stride S*144 bytes) | x of the warp's slice, word 2G of a sub-block
 // holding (x[4G], x[4G+2]) and word 2G+1 (x[4G+1], x[4G+3]) | the fp32 sums X_j
-// of its sub-blocks | 64 zero bytes | STAGES mbarriers.
+// of its sub-blocks | 2^-s_i of each super-block (padded to 16 bytes) | 64 zero
+// bytes | STAGES + 1 mbarriers (the ring, x).
 template <int MT, int S, int STAGES>
 __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const GemvArgs a) {
@@ -292,27 +346,53 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   uint8_t *ring = wreg;
   uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * kStageBytes);  // ks*128 words
   float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);              // 16 words
-  uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);
+  float *xuns = xsum + a.ks * 8;                           // ks floats, padded to 16 bytes
+  uint32_t *xzero = reinterpret_cast<uint32_t *>(xuns + pad4(a.ks));            // 16 words
+  uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);  // STAGES ring + 1 for x
   float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
 
   if (lane == 0) {
     prefetch_tmap(&wmap);
-    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s <= STAGES; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
   const uint64_t policy = l2_evict_first_policy();
+  // Copy order on the warp's TMA queue: kPre weight stages (they do not depend
+  // on earlier kernels, so they go out before the dependency wait), then the x
+  // slice, then the rest of the ring.  x is small and read by every CTA, and a
+  // copy queued behind a full ring of weights waits for that ring to drain
+  // from DRAM; this order keeps x near the head.
+  constexpr int kPre = Q4K_GEMV_PRE_STAGES < STAGES ? Q4K_GEMV_PRE_STAGES : STAGES;
   if (lane == 0) {
-    for (int s = 0; s < STAGES && s < nstages; ++s) {
+    for (int s = 0; s < kPre && s < nstages; ++s) {
       mbar_arrive_expect_tx(&bars[s], kStageBytes);
       load_tile(ring + s * kStageBytes, &wmap, &bars[s], sb0 + s * S, row0, policy);
     }
   }
-  // The weights above do not depend on earlier kernels; x does.
   grid_dependency_wait();
+  if (lane == 0 && nsteps > 0) {
+    mbar_arrive_expect_tx(&bars[STAGES], nsteps * kQK * 2);
+    bulk_load(xperm, a.x + (int64_t)sb0 * kQK, nsteps * kQK * 2, &bars[STAGES]);
+  }
+  bool ok = true;
+  if (Q4K_GEMV_X_FIRST == 1) ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
+  if (Q4K_GEMV_X_FIRST == 2) __syncthreads();  // every warp's x ahead of the CTA's ring
+  const int issued = ok ? min(STAGES, nstages) : min(kPre, nstages);
+  if (lane == 0 && ok) {
+    for (int s = kPre; s < STAGES && s < nstages; ++s) {
+      mbar_arrive_expect_tx(&bars[s], kStageBytes);
+      load_tile(ring + s * kStageBytes, &wmap, &bars[s], sb0 + s * S, row0, policy);
+    }
+  }
   grid_launch_dependents();
-  const float unscale = b1_stage_x(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xzero, lane);
+  if (Q4K_GEMV_X_FIRST != 1) ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
+  if (ok) {
+    b1_stage_x<true>(reinterpret_cast<const __nv_bfloat16 *>(xperm), nsteps, xperm, xsum, xuns,
+                     xzero, lane);
+  } else if (lane == 0) {
+    b1_drain<STAGES>(bars, 0, issued, true);
+  }
 
   // B fragments: lane (g, t) with t == g/2 carries sub-block g on the steps of
   // parity g & 1 (pointer pe for even steps, po for odd steps); all other
@@ -335,7 +415,6 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   uint32_t magic;
   asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
 
-  bool ok = true;
   uint32_t phase = 0;
   const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
   for (int base = 0; base < nstages && ok; base += STAGES, phase ^= 1u) {
@@ -345,6 +424,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
       if (it >= nstages) break;
       if (!mbar_wait(&bars[stage], phase, a.err)) {
         ok = false;
+        if (lane == 0) b1_drain<STAGES>(bars, it, min(it + STAGES, nstages), false);
         break;
       }
       uint8_t *st = ring + stage * kStageBytes;
@@ -373,14 +453,14 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
           }
         }
 
-        b1_super_block<MT>(hdr, qa, pe, po, px[4 * i], lc, magic, yacc);
+        b1_super_block<MT>(hdr, qa, pe, po, px[4 * i], xuns[i], lc, magic, yacc);
         pe += adv_e;
         po += adv_o;
       }
     }
   }
 
-  b1_finish<MT>(yacc, unscale, ok, red, row0, a);
+  b1_finish<MT>(yacc, ok, red, row0, a);
 }
 
 // 16-byte read of streamed weights (read once: L2 evict-first).
@@ -410,7 +490,8 @@ __global__ void __launch_bounds__(256) gemv_b1_ldg_kernel(const GemvArgs a) {
   uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
   uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg);
   float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  uint32_t *xzero = reinterpret_cast<uint32_t *>(xsum + a.ks * 8);
+  float *xuns = xsum + a.ks * 8;
+  uint32_t *xzero = reinterpret_cast<uint32_t *>(xuns + pad4(a.ks));
   float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
 
   // Rows past n read row n-1; their results are never stored.
@@ -440,7 +521,7 @@ __global__ void __launch_bounds__(256) gemv_b1_ldg_kernel(const GemvArgs a) {
   if (nsteps > 1) load(hB, qB, 1);
   grid_dependency_wait();
   grid_launch_dependents();
-  const float unscale = b1_stage_x(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xzero, lane);
+  b1_stage_x<false>(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xuns, xzero, lane);
 
   const bool own = (t == (g >> 1));
   const bool own_e = own && !(g & 1), own_o = own && (g & 1);
@@ -456,17 +537,17 @@ __global__ void __launch_bounds__(256) gemv_b1_ldg_kernel(const GemvArgs a) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
   for (int i = 0; i < nsteps; i += 2) {
-    b1_super_block<MT>(hA, qA, pe, po, px[4 * i], lc, magic, yacc);
+    b1_super_block<MT>(hA, qA, pe, po, px[4 * i], xuns[i], lc, magic, yacc);
     pe += adv_e;
     po += adv_o;
     if (i + 2 < nsteps) load(hA, qA, i + 2);
     if (i + 1 >= nsteps) break;
-    b1_super_block<MT>(hB, qB, pe, po, px[4 * (i + 1)], lc, magic, yacc);
+    b1_super_block<MT>(hB, qB, pe, po, px[4 * (i + 1)], xuns[i + 1], lc, magic, yacc);
     pe += adv_e;
     po += adv_o;
     if (i + 3 < nsteps) load(hB, qB, i + 3);
   }
-  b1_finish<MT>(yacc, unscale, true, red, row0, a);
+  b1_finish<MT>(yacc, true, red, row0, a);
 }
 
 // ---------------------------------------------------------------- batch 2..16
@@ -655,7 +736,25 @@ __global__ void __launch_bounds__(512) gemv_bn_kernel(const __grid_constant__ CU
 // ---------------------------------------------------------------- launch
 constexpr int kStages = Q4K_GEMV_STAGES;  // batch 2..16 (one super-block per stage)
 // Stages for batch 1 with S super-blocks per stage.
-template <int S> struct B1Stages { static constexpr int value = S == 1 ? 4 : (S == 2 ? 3 : 2); };
+#ifndef Q4K_GEMV_B1_STAGES_S1  // batch-1 ring depth (stages) for S = 1, 2, 4 super-blocks a stage
+#define Q4K_GEMV_B1_STAGES_S1 4
+#endif
+#ifndef Q4K_GEMV_B1_STAGES_S2
+#define Q4K_GEMV_B1_STAGES_S2 3
+#endif
+#ifndef Q4K_GEMV_B1_STAGES_S4
+#define Q4K_GEMV_B1_STAGES_S4 2
+#endif
+#ifndef Q4K_GEMV_INFLIGHT_KB  // planner: weight bytes in flight per SM worth having, at most
+#define Q4K_GEMV_INFLIGHT_KB 96
+#endif
+#ifndef Q4K_GEMV_LOG_PLAN  // 1: print each batch-1 plan to stderr (tuning aid)
+#define Q4K_GEMV_LOG_PLAN 0
+#endif
+template <int S> struct B1Stages {
+  static constexpr int value =
+      S == 1 ? Q4K_GEMV_B1_STAGES_S1 : (S == 2 ? Q4K_GEMV_B1_STAGES_S2 : Q4K_GEMV_B1_STAGES_S4);
+};
 
 #ifndef Q4K_GEMV_FORCE_S  // 0: choose per shape
 #define Q4K_GEMV_FORCE_S 0
@@ -673,7 +772,7 @@ struct Plan {
 };
 
 int warp_bytes_b1(int mt, int s, int stages, int ks) {
-  int b = stages * mt * s * kTileBytes + ks * (512 + 32) + 64 + stages * 8;
+  int b = stages * mt * s * kTileBytes + ks * (512 + 32) + 4 * pad4(ks) + 64 + (stages + 1) * 8;
   return (b + 127) / 128 * 128;
 }
 int warp_bytes_bn(int mt) {
@@ -716,7 +815,7 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
     const double inflight_kb =
         warps_sm * (stages ? stages - 1 : 1.5) * mt * s * kTileBytes / 1024.0;
     const double balance = (double)nsb / (double)(ks * wk);  // 1.0 = even split
-    const double score = -1000.0 * waves + std::min(inflight_kb, 96.0) / 8.0 +
+    const double score = -1000.0 * waves + std::min(inflight_kb, (double)Q4K_GEMV_INFLIGHT_KB) / 8.0 +
                          0.5 * std::min(warps_sm, 24) + 6.0 * balance + (mt == 2 ? 1.0 : 0.0);
     if (score > best.score) {
       best.score = score;
@@ -842,6 +941,10 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
     GemvKernel kern = b1_select(p.mt, p.s);
+    static int logged = 0;
+    if (Q4K_GEMV_LOG_PLAN && logged < 64 && ++logged)
+      fprintf(stderr, "q4k_gemv plan n=%lld k=%lld: mt=%d s=%d warps=%d ks=%d smem=%d grid=%d\n",
+              (long long)n, (long long)k, p.mt, p.s, p.wk, p.ks, p.smem, p.grid);
     if (encode(p.mt, p.s) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
