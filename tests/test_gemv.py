@@ -27,8 +27,8 @@ def q4k():
     return m
 
 
-def _run(q4k, w, n, k, x):
-    y = q4k.q4k_gemv(w.to(DEV), n, k, x.to(DEV))
+def _run(q4k, w, n, k, x, flags=0):
+    y = q4k.q4k_gemv_ex(w.to(DEV), n, k, x.to(DEV), flags)
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     return y.cpu().numpy()
@@ -39,13 +39,52 @@ CASES = [(1, 256, 1), (7, 512, 1), (129, 1280, 1), (597, 5120, 1), (33, 17408, 1
          (129, 5120, 9), (597, 5120, 16), (40, 8192, 16)]
 
 
+# flags 0: plain launches; Q4K_FLAG_OVERLAP_WEIGHTS: programmatic dependent
+# launch (weights streamed before the dependency wait).
+FLAGS = [0, 1]
+
+
+@pytest.mark.parametrize("flags", FLAGS)
 @pytest.mark.parametrize("n,k,batch", CASES)
-def test_gemv_matches_oracle(q4k, n, k, batch):
+def test_gemv_matches_oracle(q4k, n, k, batch, flags):
     w = synth.q4k_weight(n, k, seed=1000 + n + k + batch, quants="normal" if n % 2 else "uniform")
     x = synth.bf16_normal((batch, k), seed=2000 + n + batch)
-    y = _run(q4k, w, n, k, x)
+    y = _run(q4k, w, n, k, x, flags)
     yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
-    check_bound(y, yref, s, TOL, f"gemv {n}x{k} b{batch}")
+    check_bound(y, yref, s, TOL, f"gemv {n}x{k} b{batch} flags{flags}")
+
+
+@pytest.mark.parametrize("n,k", [(16 * 152 * 2 + 5, 1280), (5000, 2560), (16 * 152, 256), (3000, 17408)])
+def test_gemv_many_row_tiles(q4k, n, k):
+    # many row tiles (more than one per SM), ragged last tile, both launch modes
+    w = synth.q4k_weight(n, k, seed=n + k, quants="normal")
+    x = synth.bf16_normal((1, k), seed=n + 7)
+    y = _run(q4k, w, n, k, x, flags=1)
+    yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+    check_bound(y, yref, s, TOL, f"overlap {n}x{k}")
+    y0 = _run(q4k, w, n, k, x, flags=0)
+    check_bound(y0, yref, s, TOL, f"per-tile {n}x{k}")
+
+
+def test_gemv_overlap_chain_reads_the_previous_output(q4k):
+    # y1 = W1 x0; x1 = bf16(y1) by a torch kernel; y2 = W2 x1, all queued on
+    # one stream with programmatic dependent launch: the second projection
+    # must see x1 as written, even though its weights stream early.
+    n1, k1, n2 = 2048, 1024, 700
+    w1 = synth.q4k_weight(n1, k1, seed=21).to(DEV)
+    w2 = synth.q4k_weight(n2, n1, seed=22).to(DEV)
+    x0 = synth.bf16_normal((1, k1), seed=23).to(DEV)
+    flags = q4k.Q4K_FLAG_OVERLAP_WEIGHTS
+    for _ in range(3):
+        y1 = q4k.q4k_gemv_ex(w1, n1, k1, x0, flags)
+        x1 = (y1 * 0.05).to(torch.bfloat16)
+        y2 = q4k.q4k_gemv_ex(w2, n2, n1, x1, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    yref1, s1 = oracle.gemv(w1.cpu().numpy(), n1, k1, xbits(x0.cpu()))
+    check_bound(y1.cpu().numpy(), yref1, s1, TOL, "chain first")
+    yref2, s2 = oracle.gemv(w2.cpu().numpy(), n2, n1, xbits(x1.cpu()))
+    check_bound(y2.cpu().numpy(), yref2, s2, TOL, "chain second")
 
 
 @pytest.mark.parametrize("batch", [1, 5, 16])
@@ -102,14 +141,14 @@ def test_gemv_unit_vectors_pick_columns(q4k):
     assert np.allclose(y1[0], wq[:, cols[3]], rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("batch", [1, 6])
-def test_gemv_homogeneous_and_deterministic_bitwise(q4k, batch):
+@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (6, 0)])
+def test_gemv_homogeneous_and_deterministic_bitwise(q4k, batch, flags):
     n, k = 300, 2048
     w = synth.q4k_weight(n, k, seed=14).to(DEV)
     x = synth.bf16_normal((batch, k), seed=15).to(DEV)
-    y1 = q4k.q4k_gemv(w, n, k, x).clone()
-    y1b = q4k.q4k_gemv(w, n, k, x).clone()
-    y2 = q4k.q4k_gemv(w, n, k, (x.float() * 4).to(torch.bfloat16))
+    y1 = q4k.q4k_gemv_ex(w, n, k, x, flags).clone()
+    y1b = q4k.q4k_gemv_ex(w, n, k, x, flags).clone()
+    y2 = q4k.q4k_gemv_ex(w, n, k, (x.float() * 4).to(torch.bfloat16), flags)
     torch.cuda.synchronize()
     assert torch.equal(y1, y1b)
     assert torch.equal(y2, y1 * 4)
@@ -127,11 +166,11 @@ LAYER = [(10240, 5120), (5120, 8192), (17408, 5120), (5120, 17408)]
 
 
 @pytest.mark.parametrize("n,k", LAYER)
-@pytest.mark.parametrize("batch", [1, 4, 16])
-def test_gemv_full_size_sampled_rows(q4k, n, k, batch):
+@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (4, 0), (16, 0)])
+def test_gemv_full_size_sampled_rows(q4k, n, k, batch, flags):
     w = synth.q4k_weight(n, k, seed=n * 3 + k, quants="normal", device=DEV)
     x = synth.bf16_normal((batch, k), seed=n + batch, device=DEV)
-    y = q4k.q4k_gemv(w, n, k, x)
+    y = q4k.q4k_gemv_ex(w, n, k, x, flags)
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     rows = np.sort(np.random.default_rng(n + k).choice(n, 96, replace=False))
@@ -139,4 +178,4 @@ def test_gemv_full_size_sampled_rows(q4k, n, k, batch):
     wsub = w[torch.from_numpy(rows).to(DEV)].cpu().numpy()
     yref, s = oracle.gemv(wsub, len(rows), k, xbits(x))
     check_bound(y[:, torch.from_numpy(rows).to(DEV)].cpu().numpy(), yref, s, TOL,
-                f"full {n}x{k} b{batch}")
+                f"full {n}x{k} b{batch} flags{flags}")
