@@ -8,14 +8,15 @@
 //               sort; experts ordered by id, at most 16 pairs per work slot, so a
 //               heavily used expert spans several slots), validates ids (an id
 //               out of range is skipped and flagged in the device error word).
-//   2. gate/up  one CTA per (slot, 16-row tile of ffn): the expert's gate and up
-//               rows are streamed once (TMA) and contracted with all of the
-//               slot's tokens on the tensor cores (MMA columns = tokens); the
-//               epilogue writes h = silu(g) * u in fp32.
-//   3. down     one CTA per (slot, 128-row tile of hidden): h of the slot's pairs
-//               is staged once in shared memory as two bf16 columns per pair,
-//               h_hi = bf16(h) and h_lo = bf16(h - h_hi) (together 16
-//               significant bits), and each of the 8 warps streams 16 down rows.
+//   2. gate/up  per work slot, warp streams of 16-row tiles of ffn: the
+//               expert's gate and up rows are streamed once (TMA) and contracted
+//               with all of the slot's tokens on the tensor cores (MMA columns =
+//               tokens); the epilogue writes h = silu(g) * u in fp32 and as two
+//               bf16 columns per pair, h_hi = bf16(h) and h_lo = bf16(h - h_hi)
+//               (together 16 significant bits), stored in MMA fragment order.
+//   3. down     per work slot, warp streams of 16-row tiles of hidden, full K
+//               (ffn) per tile; MMA columns = (h_hi, h_lo) of each pair; the
+//               epilogue writes p = Wd h per pair.
 //   4. combine  y[t] = sum_j w[t, j] * p[t, j] in slot order j = 0..k-1.
 // Grids are sized for the worst case; CTAs whose slot is not in use exit at
 // once.  Results do not depend on the order of pairs inside a group (columns of
@@ -33,6 +34,7 @@ namespace {
 constexpr int kRows = 16;                    // rows per CTA (one MMA m-tile)
 constexpr int kTile = kRows * kBlockBytes;   // 2304 bytes per super-block stage
 constexpr int kStagesMoe = 4;
+constexpr int kMoeWarps = 4;                 // warps (weight streams) per expert CTA
 constexpr int kMaxExperts = 2048;
 constexpr int kSlotPairs = 16;               // pairs per work slot
 
@@ -165,26 +167,27 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
 }
 
 // ---------------------------------------------------------------- 2./3. experts
-// One CTA = (work slot blockIdx.y, 16*WM output rows from blockIdx.x).  Warp w
-// takes m-tile w / WK and the (w % WK)-th super-block slice of K; slices of an
-// m-tile meet in shared memory.  MMA columns are the slot's pairs:
+// One CTA = kMoeWarps warps of work slot blockIdx.y.  Warp stream
+// s = blockIdx.x * kMoeWarps + warp takes the slot's 16-row m-tiles s, s + S,
+// s + 2S, ... (S = gridDim.x * kMoeWarps), each over the full K; its ring of
+// weight stages and its x fragments run ahead continuously across those tiles,
+// and each tile's result is written straight from the accumulators.  MMA
+// columns are the slot's pairs:
 //   gate/up (DOWN = false): column c = x row of the c-th pair's token;
 //   down    (DOWN = true):  column 2i = h_hi, column 2i+1 = h_lo of pair i.
 // Thread t's k-slots (2t, 2t+1) carry positions (o, o+2) and (2t+8, 2t+9)
 // positions (o+1, o+3) of a sub-block, o = 8t + 4s for step s = 0/1: quant
 // bytes 8t .. 8t+7 of the sub-block's 32-byte chunk.
-template <int NT, bool DOWN, int WM, int WK>
-__global__ void __launch_bounds__(WM * WK * 32) moe_expert_kernel(
-    const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
-    const MoeArgs a, int nsb, int ks, int rows_total) {
-  constexpr int NM = DOWN ? 1 : 2;  // weight matrices per CTA (gate and up)
-  constexpr int kCols = NT * 8;
+// One CTA's work for a slot with at most 8 NT MMA columns.
+template <int NT, bool DOWN>
+__device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUtensorMap *map1p,
+                                            const MoeArgs &a, int nsb, int rows_total,
+                                            uint8_t *smem, int slot) {
+  const CUtensorMap &map0 = *map0p, &map1 = *map1p;
+  constexpr int NM = DOWN ? 1 : 2;  // weight matrices per stage (gate and up)
   constexpr int kStageBytes = NM * kTile;
   // TMA destinations must be 128-byte aligned: round each warp's region up.
   constexpr int kWarpBytes = (kStagesMoe * kStageBytes + 64 + 127) / 128 * 128;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int slot = blockIdx.y;
-  if (slot >= a.meta[0]) return;  // slot not in use (uniform per CTA)
   const int expert = a.slot_expert[slot];
   const int pstart = a.slot_start[slot];
   const int np = a.slot_start[slot + 1] - pstart;  // pairs of this slot (<= 16)
@@ -192,13 +195,12 @@ __global__ void __launch_bounds__(WM * WK * 32) moe_expert_kernel(
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int mtile = warp / WK, kslice = warp % WK;
-  const int row0 = blockIdx.x * (kRows * WM) + mtile * kRows;
-  const int sb0 = kslice * ks;
-  const int nsteps = max(0, min(nsb, sb0 + ks) - sb0);
+  const int ntiles = (rows_total + kRows - 1) / kRows;
+  const int sid = blockIdx.x * kMoeWarps + warp, nsid = gridDim.x * kMoeWarps;
+  const int ntl = sid < ntiles ? (ntiles - sid + nsid - 1) / nsid : 0;  // tiles of this warp
+  const int total = ntl * nsb;                                          // ring iterations
   uint8_t *ring = smem + warp * kWarpBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kStagesMoe * kStageBytes);
-  float *red = reinterpret_cast<float *>(smem + WM * WK * kWarpBytes);
 
   if (lane == 0) {
     prefetch_tmap(&map0);
@@ -208,16 +210,20 @@ __global__ void __launch_bounds__(WM * WK * 32) moe_expert_kernel(
   }
   __syncwarp();
   const uint64_t policy = l2_evict_first_policy();
-  auto issue = [&](int stage, int sb) {
+  // Ring iteration q = super-block q % nsb of this warp's tile q / nsb.
+  auto issue = [&](int q) {
+    const int j = q / nsb, u = q - j * nsb;
+    const int row0 = (sid + j * nsid) * kRows;
+    const int stage = q % kStagesMoe;
     mbar_arrive_expect_tx(&bars[stage], kStageBytes);
     uint8_t *dst = ring + stage * kStageBytes;
-    tma_load_3d_hint(dst, &map0, &bars[stage], sb * (kBlockBytes / 8), row0, expert, policy);
+    tma_load_3d_hint(dst, &map0, &bars[stage], u * (kBlockBytes / 8), row0, expert, policy);
     if (NM == 2)
-      tma_load_3d_hint(dst + kTile, &map1, &bars[stage], sb * (kBlockBytes / 8), row0, expert,
+      tma_load_3d_hint(dst + kTile, &map1, &bars[stage], u * (kBlockBytes / 8), row0, expert,
                        policy);
   };
   if (lane == 0)
-    for (int s = 0; s < kStagesMoe && s < nsteps; ++s) issue(s, sb0 + s);
+    for (int q = 0; q < kStagesMoe && q < total; ++q) issue(q);
 
   // bf16 source of this lane's column nt*8 + g (rows of K values).
   const __nv_bfloat16 *src[NT];
@@ -232,165 +238,209 @@ __global__ void __launch_bounds__(WM * WK * 32) moe_expert_kernel(
     else
       src[nt] = a.x + (int64_t)a.pair_token[pstart + cc] * a.ldx;
   }
-
-  float yacc[NM][NT][4];
+  // x (or h) fragments of CJ sub-blocks for this lane's columns, loaded one
+  // chunk ahead of their use so the L2 latency stays off the MMA path.  They
+  // depend only on the super-block, not on the row tile.
+  constexpr int CJ = NT <= 2 ? 4 : 2;  // sub-blocks per chunk
+  constexpr int NCH = 8 / CJ;          // chunks per super-block (even)
+  auto load_x = [&](uint4(&dst)[CJ][NT], int q, int ch) {
+    const int u = q % nsb;
 #pragma unroll
-  for (int mi = 0; mi < NM; ++mi)
+    for (int jj = 0; jj < CJ; ++jj)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      yacc[mi][nt][0] = yacc[mi][nt][1] = yacc[mi][nt][2] = yacc[mi][nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int64_t off = (int64_t)u * kQK + 32 * (ch * CJ + jj) + 8 * t;
+        dst[jj][nt] = (cval[nt] && q < total)
+                          ? __ldg(reinterpret_cast<const uint4 *>(src[nt] + off))
+                          : make_uint4(0, 0, 0, 0);
+      }
+  };
+  uint4 xbuf[2][CJ][NT];
+  load_x(xbuf[0], 0, 0);
 
   bool ok = true;
-  int stage = 0;
-  uint32_t phase = 0;
-  for (int i = 0; i < nsteps; ++i) {
-    const int sb = sb0 + i;
-    if (!mbar_wait(&bars[stage], phase, a.err)) {
-      ok = false;
-      break;
-    }
-    const uint8_t *st = ring + stage * kStageBytes;
-    uint4 hdr[NM][2];
-    uint2 qw[NM][2][4];
+  for (int j = 0; j < ntl; ++j) {
+    const int row0 = (sid + j * nsid) * kRows;
+    float yacc[NM][NT][4];
 #pragma unroll
     for (int mi = 0; mi < NM; ++mi)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint8_t *rp = st + mi * kTile + (g + 8 * r) * kBlockBytes;
-        hdr[mi][r] = *reinterpret_cast<const uint4 *>(rp);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          qw[mi][r][c] = *reinterpret_cast<const uint2 *>(rp + kQsOffset + 32 * c + 8 * t);
-      }
-    __syncwarp();
-    if (lane == 0 && i + kStagesMoe < nsteps) issue(stage, sb + kStagesMoe);
-    if (++stage == kStagesMoe) {
-      stage = 0;
-      phase ^= 1u;
-    }
-    // This lane decodes sub-blocks 2t, 2t+1 of rows g, g+8; the other lanes of
-    // its quad fetch them by shuffle.
-    float dsA[NM][2], dsB[NM][2], dmA[NM][2], dmB[NM][2];
-#pragma unroll
-    for (int mi = 0; mi < NM; ++mi)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        uint32_t sc2, m2;
-        scales_pair(hdr[mi][r].y, hdr[mi][r].z, hdr[mi][r].w, t, &sc2, &m2);
-        const float d = half_lo_to_float(hdr[mi][r].x), dmin = half_hi_to_float(hdr[mi][r].x);
-        dsA[mi][r] = d * (float)(sc2 & 0xFFu);
-        dsB[mi][r] = d * (float)(sc2 >> 8);
-        dmA[mi][r] = dmin * (float)(m2 & 0xFFu);
-        dmB[mi][r] = dmin * (float)(m2 >> 8);
-      }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = j >> 1;
-      const bool hi = j & 1;
-      uint32_t b0[NT][2], b1[NT][2];
-      float xs[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int64_t off = (int64_t)sb * kQK + 32 * j + 8 * t;
-        const uint4 v = cval[nt] ? __ldg(reinterpret_cast<const uint4 *>(src[nt] + off))
-                                 : make_uint4(0, 0, 0, 0);
-        b0[nt][0] = __byte_perm(v.x, v.y, 0x5410);
-        b1[nt][0] = __byte_perm(v.x, v.y, 0x7632);
-        b0[nt][1] = __byte_perm(v.z, v.w, 0x5410);
-        b1[nt][1] = __byte_perm(v.z, v.w, 0x7632);
-        const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
-        const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
-        const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z));
-        const float2 p3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.w));
-        xs[nt] = ((p0.x + p0.y) + (p1.x + p1.y)) + ((p2.x + p2.y) + (p3.x + p3.y));
-      }
-      // X_j of column nt*8+g is its quad's sum; accumulator column 2t+e needs the
-      // sum of column 2t+e, held by the quad of lane 4(2t+e).
-      float Xc[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float sum = xs[nt];
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        Xc[nt][0] = __shfl_sync(0xffffffffu, sum, 4 * (2 * t));
-        Xc[nt][1] = __shfl_sync(0xffffffffu, sum, 4 * (2 * t + 1));
-      }
-      const int srcl = (lane & ~3) | (j >> 1);
-#pragma unroll
-      for (int mi = 0; mi < NM; ++mi) {
-        float acc[NT][4];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const uint32_t w0 = s ? qw[mi][0][c].y : qw[mi][0][c].x;
-          const uint32_t w1 = s ? qw[mi][1][c].y : qw[mi][1][c].x;
-          const uint32_t a0 = hi ? nib_hi(w0) : nib_lo(w0);
-          const uint32_t a1 = hi ? nib_hi(w1) : nib_lo(w1);
-          const uint32_t a2 = hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8);
-          const uint32_t a3 = hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (s == 0)
-              mma_bf16_zc(acc[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
-            else
-              mma_bf16(acc[nt], a0, a1, a2, a3, b0[nt][1], b1[nt][1]);
-          }
+      for (int nt = 0; nt < NT; ++nt)
+        yacc[mi][nt][0] = yacc[mi][nt][1] = yacc[mi][nt][2] = yacc[mi][nt][3] = 0.f;
+    for (int u = 0; u < nsb && ok; ++u) {
+      const int q = j * nsb + u;
+      const int stage = q % kStagesMoe;
+      if (!mbar_wait(&bars[stage], (uint32_t)((q / kStagesMoe) & 1), a.err)) {
+        ok = false;
+        if (lane == 0) {  // let this warp's copies in flight land (bounded)
+          const uint64_t t0 = global_ns();
+          for (int r = q; r < min(q + kStagesMoe, total); ++r)
+            while (!mbar_try_wait(&bars[r % kStagesMoe], (uint32_t)((r / kStagesMoe) & 1), 1000u))
+              if (global_ns() - t0 > kWaitLimitNs) break;
         }
+        break;
+      }
+      const uint8_t *st = ring + stage * kStageBytes;
+      uint4 hdr[NM][2];
+      uint2 qw[NM][2][4];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mi][r] : dsA[mi][r], srcl);
-          const float dm = __shfl_sync(0xffffffffu, hi ? dmB[mi][r] : dmA[mi][r], srcl);
+          const uint8_t *rp = st + mi * kTile + (g + 8 * r) * kBlockBytes;
+          hdr[mi][r] = *reinterpret_cast<const uint4 *>(rp);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float X = Xc[nt][e];
-              float &yv = yacc[mi][nt][2 * r + e];
-              yv = fmaf(ds, fmaf(-128.f, X, acc[nt][2 * r + e]), yv);
-              yv = fmaf(-dm, X, yv);
-            }
+          for (int c = 0; c < 4; ++c)
+            qw[mi][r][c] = *reinterpret_cast<const uint2 *>(rp + kQsOffset + 32 * c + 8 * t);
         }
+      __syncwarp();
+      if (lane == 0 && q + kStagesMoe < total) issue(q + kStagesMoe);
+      // This lane decodes sub-blocks 2t, 2t+1 of rows g, g+8; the other lanes of
+      // its quad fetch them by shuffle.
+      float dsA[NM][2], dsB[NM][2], dmA[NM][2], dmB[NM][2];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          uint32_t sc2, m2;
+          scales_pair(hdr[mi][r].y, hdr[mi][r].z, hdr[mi][r].w, t, &sc2, &m2);
+          const float d = half_lo_to_float(hdr[mi][r].x), dmin = half_hi_to_float(hdr[mi][r].x);
+          dsA[mi][r] = d * (float)(sc2 & 0xFFu);
+          dsB[mi][r] = d * (float)(sc2 >> 8);
+          dmA[mi][r] = dmin * (float)(m2 & 0xFFu) * (1.f / 128.f);
+          dmB[mi][r] = dmin * (float)(m2 >> 8) * (1.f / 128.f);
+        }
+      auto sub_block = [&](int jb, const uint4(&xv)[NT]) {
+        const int c = jb >> 1;
+        const bool hi = jb & 1;
+        // B fragments: (x[o], x[o+2]) and (x[o+1], x[o+3]).  h of the down
+        // projection is stored in that order already; x needs a byte permute.
+        uint32_t b0[NT][2], b1[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 v = xv[nt];
+          if (DOWN) {
+            b0[nt][0] = v.x;
+            b1[nt][0] = v.y;
+            b0[nt][1] = v.z;
+            b1[nt][1] = v.w;
+          } else {
+            b0[nt][0] = __byte_perm(v.x, v.y, 0x5410);
+            b1[nt][0] = __byte_perm(v.x, v.y, 0x7632);
+            b0[nt][1] = __byte_perm(v.z, v.w, 0x5410);
+            b1[nt][1] = __byte_perm(v.z, v.w, 0x7632);
+          }
+        }
+        // 128 X_j of every column by one more MMA per step (A = 128 everywhere):
+        // every row of c128 holds it, so column 2t+e is c128[nt][e].
+        float c128[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_zc(c128[nt], kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0[nt][0], b1[nt][0]);
+          mma_bf16(c128[nt], kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0[nt][1], b1[nt][1]);
+        }
+        const int srcl = (lane & ~3) | (jb >> 1);
+#pragma unroll
+        for (int mi = 0; mi < NM; ++mi) {
+          float acc[NT][4];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const uint32_t w0 = s ? qw[mi][0][c].y : qw[mi][0][c].x;
+            const uint32_t w1 = s ? qw[mi][1][c].y : qw[mi][1][c].x;
+            const uint32_t a0 = hi ? nib_hi(w0) : nib_lo(w0);
+            const uint32_t a1 = hi ? nib_hi(w1) : nib_lo(w1);
+            const uint32_t a2 = hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8);
+            const uint32_t a3 = hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (s == 0)
+                mma_bf16_zc(acc[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
+              else
+                mma_bf16(acc[nt], a0, a1, a2, a3, b0[nt][1], b1[nt][1]);
+            }
+          }
+          // acc = sum (128 + q) x: subtract 128 X_j, apply d*sc; the min term
+          // takes X_j = c128 / 128 (the 1/128 is folded into dm).
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mi][r] : dsA[mi][r], srcl);
+            const float dm = __shfl_sync(0xffffffffu, hi ? dmB[mi][r] : dmA[mi][r], srcl);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float c1 = c128[nt][e];
+                float &yv = yacc[mi][nt][2 * r + e];
+                yv = fmaf(ds, acc[nt][2 * r + e] - c1, yv);
+                yv = fmaf(-dm, c1, yv);
+              }
+          }
+        }
+      };
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        if (ch + 1 < NCH)
+          load_x(xbuf[(ch + 1) & 1], q, ch + 1);
+        else
+          load_x(xbuf[0], q + 1, 0);
+#pragma unroll
+        for (int jj = 0; jj < CJ; ++jj) sub_block(ch * CJ + jj, xbuf[ch & 1][jj]);
       }
     }
-  }
-
-  // Split-K partials of each m-tile: red[mi][warp][row][col].
-#pragma unroll
-  for (int mi = 0; mi < NM; ++mi)
+    // This tile's outputs: thread (g, t) holds rows g, g+8 and columns
+    // nt*8 + 2t + e.  After a timed-out wait the warp's remaining rows read NaN.
+    const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = g + 8 * (e >> 1);
-        const int col = nt * 8 + 2 * t + (e & 1);
-        red[((mi * WM * WK + warp) * kRows + row) * kCols + col] = yacc[mi][nt][e];
+      for (int r = 0; r < 2; ++r) {
+        const int grow = row0 + g + 8 * r;
+        if (grow >= rows_total) continue;
+        if (DOWN) {
+          const int pr = nt * 4 + t;  // columns 2pr (h_hi) and 2pr+1 (h_lo)
+          if (pr < np)
+            a.p[(size_t)(pstart + pr) * a.hidden + grow] =
+                ok ? yacc[0][nt][2 * r] + yacc[0][nt][2 * r + 1] : nan;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pr = nt * 8 + 2 * t + e;
+            if (pr >= np) continue;
+            const float gg = yacc[0][nt][2 * r + e], uu = yacc[NM - 1][nt][2 * r + e];
+            const float hv = ok ? gg / (1.f + __expf(-gg)) * uu : nan;
+            const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
+            const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
+            // h_hi / h_lo in B-fragment order: positions 1 and 2 of each group
+            // of four swapped, so that 32-bit words hold (h[o], h[o+2]) and
+            // (h[o+1], h[o+3]).
+            const int pos = (grow & ~3) | ((grow & 1) << 1) | ((grow >> 1) & 1);
+            a.h[(size_t)(pstart + pr) * a.ffn + grow] = hv;
+            a.h_hi[(size_t)(pstart + pr) * a.ffn + pos] = hh;
+            a.h_lo[(size_t)(pstart + pr) * a.ffn + pos] = hl;
+          }
+        }
       }
-  __syncwarp();
-  if (!ok && lane == 0) red[(warp * kRows) * kCols] = __int_as_float(0x7fc00000);
-  __syncthreads();
-  const int nout = DOWN ? np : ncols;  // outputs per row: pairs
-  for (int idx = threadIdx.x; idx < WM * kRows * nout; idx += blockDim.x) {
-    const int m = idx / (kRows * nout);
-    const int row = (idx / nout) % kRows;
-    const int pr = idx % nout;
-    const int grow = blockIdx.x * (kRows * WM) + m * kRows + row;
-    if (grow >= rows_total) continue;
-    auto part = [&](int mi, int col) {
-      float v = 0.f;
-      for (int k = 0; k < WK; ++k) v += red[((mi * WM * WK + m * WK + k) * kRows + row) * kCols + col];
-      return v;
-    };
-    if (DOWN) {
-      a.p[(size_t)(pstart + pr) * a.hidden + grow] = part(0, 2 * pr) + part(0, 2 * pr + 1);
-    } else {
-      const float gg = part(0, pr), uu = part(1, pr);
-      const float hv = gg / (1.f + __expf(-gg)) * uu;
-      const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
-      const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
-      a.h[(size_t)(pstart + pr) * a.ffn + grow] = hv;
-      a.h_hi[(size_t)(pstart + pr) * a.ffn + grow] = hh;
-      a.h_lo[(size_t)(pstart + pr) * a.ffn + grow] = hl;
-    }
   }
+}
+
+// The MMA width follows the slot: 8 columns when its pairs fit, else 16 or 32
+// (NTMAX n-tiles of 8 at most), so a slot with few pairs does no work for
+// empty columns.  The choice is uniform per CTA.
+template <int NTMAX, bool DOWN>
+__global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
+    const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+    const MoeArgs a, int nsb, int rows_total) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int slot = blockIdx.y;
+  if (slot >= a.meta[0]) return;  // slot not in use
+  const int np = a.slot_start[slot + 1] - a.slot_start[slot];
+  const int ncols = DOWN ? 2 * np : np;
+  if (ncols <= 8 || NTMAX == 1)
+    expert_body<1, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
+  else if (ncols <= 16 || NTMAX == 2)
+    expert_body<(NTMAX >= 2 ? 2 : 1), DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
+  else
+    expert_body<NTMAX, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
 }
 
 // ---------------------------------------------------------------- 4. combine
@@ -408,34 +458,36 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 }
 
 std::once_flag g_moe_attr;
-constexpr int kGuWK = 4;  // gate/up: 4 warps split K (hidden)
-constexpr int kDnWM = 4;  // down: 4 m-tiles per CTA, full K (ffn) per warp
+constexpr int kGuTiles = 2;  // gate/up: m-tiles per warp stream
+constexpr int kDnTiles = 4;  // down: m-tiles per warp stream
 
-template <int NT, bool DOWN, int WM, int WK>
+template <int NT, bool DOWN>
 constexpr int expert_smem() {
-  return WM * WK * ((kStagesMoe * (DOWN ? 1 : 2) * kTile + 64 + 127) / 128 * 128) +
-         (DOWN ? 1 : 2) * WM * WK * kRows * NT * 8 * 4;
+  return kMoeWarps * ((kStagesMoe * (DOWN ? 1 : 2) * kTile + 64 + 127) / 128 * 128);
 }
 
-template <int NT, bool DOWN, int WM, int WK>
+template <int NT, bool DOWN>
 void allow() {
-  cudaFuncSetAttribute(moe_expert_kernel<NT, DOWN, WM, WK>,
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, expert_smem<NT, DOWN, WM, WK>());
+  cudaFuncSetAttribute(moe_expert_kernel<NT, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       expert_smem<NT, DOWN>());
 }
 
 void moe_attributes() {
-  allow<1, false, 1, kGuWK>();
-  allow<2, false, 1, kGuWK>();
-  allow<1, true, kDnWM, 1>();
-  allow<2, true, kDnWM, 1>();
-  allow<4, true, kDnWM, 1>();
+  allow<1, false>();
+  allow<2, false>();
+  allow<1, true>();
+  allow<2, true>();
+  allow<4, true>();
 }
 
-template <int NT, bool DOWN, int WM, int WK>
-void launch_expert(dim3 grid, const CUtensorMap &m0, const CUtensorMap &m1, const MoeArgs &a,
-                   int nsb, int ks, int rows, cudaStream_t stream) {
-  moe_expert_kernel<NT, DOWN, WM, WK><<<grid, WM * WK * 32, expert_smem<NT, DOWN, WM, WK>(),
-                                       stream>>>(m0, m1, a, nsb, ks, rows);
+template <int NT, bool DOWN>
+void launch_expert(int rows, int tiles_per_warp, int max_slots, const CUtensorMap &m0,
+                   const CUtensorMap &m1, const MoeArgs &a, int nsb, cudaStream_t stream) {
+  const int ntiles = (rows + kRows - 1) / kRows;
+  const int per_cta = kMoeWarps * tiles_per_warp;
+  dim3 grid((unsigned)((ntiles + per_cta - 1) / per_cta), (unsigned)max_slots);
+  moe_expert_kernel<NT, DOWN><<<grid, kMoeWarps * 32, expert_smem<NT, DOWN>(), stream>>>(
+      m0, m1, a, nsb, rows);
 }
 
 CUresult expert_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int64_t stride,
@@ -497,24 +549,21 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   moe_route_kernel<<<1, 1024, 0, stream>>>(a);
   const int max_slots = MoeLayout::max_slots(n_experts, P);
   const int cap = std::min(P, kSlotPairs);  // pairs per slot at most
-  {  // gate/up: K = hidden
+  {  // gate/up: K = hidden, one column per pair
     const int nsb = (int)(hidden / kQK);
-    const int ks = (nsb + kGuWK - 1) / kGuWK;
-    dim3 grid((unsigned)((ffn + kRows - 1) / kRows), (unsigned)max_slots);
     if (cap <= 8)
-      launch_expert<1, false, 1, kGuWK>(grid, mg, mu, a, nsb, ks, (int)ffn, stream);
+      launch_expert<1, false>((int)ffn, kGuTiles, max_slots, mg, mu, a, nsb, stream);
     else
-      launch_expert<2, false, 1, kGuWK>(grid, mg, mu, a, nsb, ks, (int)ffn, stream);
+      launch_expert<2, false>((int)ffn, kGuTiles, max_slots, mg, mu, a, nsb, stream);
   }
   {  // down: K = ffn, two columns per pair
     const int nsb = (int)(ffn / kQK);
-    dim3 grid((unsigned)((hidden + kRows * kDnWM - 1) / (kRows * kDnWM)), (unsigned)max_slots);
     if (2 * cap <= 8)
-      launch_expert<1, true, kDnWM, 1>(grid, md, md, a, nsb, nsb, (int)hidden, stream);
+      launch_expert<1, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
     else if (2 * cap <= 16)
-      launch_expert<2, true, kDnWM, 1>(grid, md, md, a, nsb, nsb, (int)hidden, stream);
+      launch_expert<2, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
     else
-      launch_expert<4, true, kDnWM, 1>(grid, md, md, a, nsb, nsb, (int)hidden, stream);
+      launch_expert<4, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
   }
   {
     dim3 grid((unsigned)((hidden + 255) / 256), (unsigned)n_tokens);
