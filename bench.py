@@ -370,8 +370,8 @@ def profiled_traffic():
 
 def run_case(case):
     """One small instance of a kernel, for ncu captures (no timing): one 27B-class
-    layer of batch-1 projections (203 MB of weights), one 512-token gate
-    prefill, or one routed-MoE decode step."""
+    layer of batch-1 projections (203 MB of weights), the 512-token gate and
+    down prefill GEMMs, or one routed-MoE decode step."""
     import bit_block_quantized_q4_gb300 as q4k
     from bit_block_quantized_q4_gb300 import build as qb
     qb.build()
@@ -384,13 +384,14 @@ def run_case(case):
         for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
             q4k.q4k_gemv(w, n, k, x, out=y)
     elif case == "gemm_prefill":
-        n, k, m = 17408, 5120, 512
-        w = synth.q4k_weight(n, k, seed=synth.derive_seed(1003, "w", "gate"), quants="normal",
-                             device=dev)
-        x = synth.bf16_normal((m, k), seed=synth.derive_seed(1003, "x", "gate"), sigma=0.5,
-                              device=dev)
-        torch.cuda.synchronize()
-        q4k.q4k_gemm(w, n, k, x)
+        m = 512
+        for name, n, k in (("gate", 17408, 5120), ("down", 5120, 17408)):
+            w = synth.q4k_weight(n, k, seed=synth.derive_seed(1003, "w", name), quants="normal",
+                                 device=dev)
+            x = synth.bf16_normal((m, k), seed=synth.derive_seed(1003, "x", name), sigma=0.5,
+                                  device=dev)
+            torch.cuda.synchronize()
+            q4k.q4k_gemm(w, n, k, x)
     else:
         bench_moe(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
     torch.cuda.synchronize()

@@ -30,11 +30,17 @@ namespace q4k {
 
 namespace {
 
+#ifndef Q4K_GEMM_XK  // k width of an X stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
+#define Q4K_GEMM_XK 64
+#endif
 constexpr int kSub = 4;                 // 128-token sub-tiles per CTA
 constexpr int kTokens = 128 * kSub;     // tokens per CTA
-constexpr int kBK = 64;                 // k per block = one 128-byte swizzle panel
-constexpr int kXStageBytes = kTokens * kBK * 2;  // 65536
-constexpr int kXStages = 2;
+constexpr int kBK = 64;                 // k per weight block = one 128-byte swizzle panel
+constexpr int kXK = Q4K_GEMM_XK;        // k per X stage (one swizzle panel of X)
+constexpr int kXPanels = kBK / kXK;     // X stages per weight block
+constexpr int kXSubBytes = 128 * kXK * 2;        // one 128-token sub-tile of an X stage
+constexpr int kXStageBytes = kSub * kXSubBytes;  // 32768 or 65536
+constexpr int kXStages = 131072 / kXStageBytes;  // 128 KB of X in flight either way
 constexpr int kBStages = 3;
 constexpr int kRawStages = 2;
 constexpr int kThreads = 256;
@@ -61,15 +67,62 @@ struct GemmArgs {
   unsigned *err;
 };
 
+// Address of the same shared-memory byte in CTA `rank` of the cluster, and a
+// 32-bit load from there.
+__device__ __forceinline__ uint32_t peer_smem(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int BN, int CS>
+// Stores 16 fp32 accumulator values of row m, columns n .. n+15, as bf16.
+__device__ __forceinline__ void store_y16(const GemmArgs &a, int m, int n, const float (&v)[16]) {
+  if (m >= a.m || n >= a.n) return;
+  __nv_bfloat16 *yrow = a.y + (int64_t)m * a.ldy;
+  uint4 o0, o1;
+  o0.x = pack_bf16(v[0], v[1]);
+  o0.y = pack_bf16(v[2], v[3]);
+  o0.z = pack_bf16(v[4], v[5]);
+  o0.w = pack_bf16(v[6], v[7]);
+  o1.x = pack_bf16(v[8], v[9]);
+  o1.y = pack_bf16(v[10], v[11]);
+  o1.z = pack_bf16(v[12], v[13]);
+  o1.w = pack_bf16(v[14], v[15]);
+  if (n + 16 <= a.n) {
+    *reinterpret_cast<uint4 *>(yrow + n) = o0;
+    *reinterpret_cast<uint4 *>(yrow + n + 8) = o1;
+  } else {
+    const uint32_t w[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    for (int e = 0; e < 16 && n + e < a.n; ++e)
+      yrow[n + e] = __ushort_as_bfloat16((unsigned short)(w[e >> 1] >> (16 * (e & 1))));
+  }
+}
+
+// A cluster is CS x KS CTAs, rank = n + CS z.  The CS CTAs with the same z
+// take consecutive 128-row weight tiles over the same K range and share X
+// (TMA multicast).  The KS CTAs with the same n split K: CTA z contracts
+// super-blocks [z nsb / KS, (z+1) nsb / KS) into its own TMEM, and the partial
+// tiles meet through distributed shared memory in the z = 0 CTA, which adds
+// them in z order and stores Y.
+template <int BN, int CS, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmArgs a) {
+  static_assert(2 * BN * 128 * 4 <= kXStages * kXStageBytes, "split-K exchange buffer");
+  static_assert(BN % 16 == 0, "16-column epilogue chunks");
   using L = GemmSmem<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -88,10 +141,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * kTokens;
-  const int nkb = a.k / kBK;
-  const int nsb = a.k / kQK;
-  const uint32_t rank = (CS > 1) ? cluster_ctarank() : 0u;
-  constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
+  const uint32_t crank = (CS * KS > 1) ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank % CS;   // position among the CTAs sharing X
+  const uint32_t krank = crank / CS;  // K range of this CTA
+  // This CTA's super-blocks [sb_lo, sb_lo + nsb); every loop below runs over
+  // indices relative to the range (k-block kb covers k = 64 (kb_lo + kb) ..).
+  const int nsb_all = a.k / kQK;
+  const int sb_lo = (int)((int64_t)krank * nsb_all / KS);
+  const int nsb = (int)((int64_t)(krank + 1) * nsb_all / KS) - sb_lo;
+  const int nkb = nsb * (kQK / kBK);
+  const int kb_lo = sb_lo * (kQK / kBK);
+  const uint16_t kMask = (uint16_t)(((1u << CS) - 1u) << (krank * CS));  // X sharers
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&xmap);
@@ -117,26 +177,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CS > 1) cluster_sync();
+  if (CS * KS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  bool acc_ready = false;  // dequant warps: the accumulator tile is complete
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kXStages;
-        const uint32_t ph = (uint32_t)((kb / kXStages) & 1);
+      for (int xp = 0; xp < nkb * kXPanels; ++xp) {
+        const int s = xp % kXStages;
+        const uint32_t ph = (uint32_t)((xp / kXStages) & 1);
         if (!mbar_wait(&xempty[s], ph ^ 1u, a.err)) { ok = false; break; }
         mbar_arrive_expect_tx(&xfull[s], kXStageBytes);
         uint8_t *dst = smem + L::kX + s * kXStageBytes;
+        const int kx = kb_lo * kBK + xp * kXK;
         for (int sub = (int)rank; sub < kSub; sub += CS) {
           if (CS > 1)
-            tma_load_2d_mc(dst + sub * (128 * 128), &xmap, &xfull[s], kb * kBK, m0 + 128 * sub,
-                           kMask);
+            tma_load_2d_mc(dst + sub * kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub, kMask);
           else
-            tma_load_2d(dst + sub * (128 * 128), &xmap, &xfull[s], kb * kBK, m0 + 128 * sub);
+            tma_load_2d(dst + sub * kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub);
         }
       }
     }
@@ -146,26 +207,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       const uint32_t xbase = smem_u32(smem + L::kX);
       const uint32_t bbase = smem_u32(smem + L::kB);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int xs = kb % kXStages, bs = kb % kBStages;
-        if (!mbar_wait(&xfull[xs], (uint32_t)((kb / kXStages) & 1), a.err)) { ok = false; break; }
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int bs = kb % kBStages;
         if (!mbar_wait(&bfull[bs], (uint32_t)((kb / kBStages) & 1), a.err)) { ok = false; break; }
-        tc_fence_after();
+        for (int h = 0; h < kXPanels; ++h) {
+          const int xp = kb * kXPanels + h, xs = xp % kXStages;
+          if (!mbar_wait(&xfull[xs], (uint32_t)((xp / kXStages) & 1), a.err)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int k16 = 0; k16 < kBK / 16; ++k16) {
-          const uint64_t bdesc = sdesc_sw128(bbase + bs * L::kBStageBytes + k16 * 32, 1024);
+          for (int k16 = 0; k16 < kXK / 16; ++k16) {
+            const uint64_t bdesc =
+                sdesc_sw128(bbase + bs * L::kBStageBytes + (h * (kXK / 16) + k16) * 32, 1024);
 #pragma unroll
-          for (int sub = 0; sub < kSub; ++sub) {
-            const uint64_t adesc =
-                sdesc_sw128(xbase + xs * kXStageBytes + sub * (128 * 128) + k16 * 32, 1024);
-            tc_mma_f16(tmem + sub * BN, adesc, bdesc, idesc, (kb | k16) != 0);
+            for (int sub = 0; sub < kSub; ++sub) {
+              const uint32_t xa = xbase + xs * kXStageBytes + sub * kXSubBytes + k16 * 32;
+              const uint64_t adesc = kXK == 64 ? sdesc_sw128(xa, 1024) : sdesc_sw64(xa, 512);
+              tc_mma_f16(tmem + sub * BN, adesc, bdesc, idesc, (kb | h | k16) != 0);
+            }
           }
+          if (CS > 1)
+            tc_commit_mc(&xempty[xs], kMask);
+          else
+            tc_commit(&xempty[xs]);
         }
+        if (!ok) break;
         tc_commit(&bempty[bs]);
-        if (CS > 1)
-          tc_commit_mc(&xempty[xs], kMask);
-        else
-          tc_commit(&xempty[xs]);
       }
       tc_commit(accfull);
     }
@@ -177,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)((sb / kRawStages) & 1);
         if (!mbar_wait(&rempty[s], ph ^ 1u, a.err)) { ok = false; break; }
         mbar_arrive_expect_tx(&rfull[s], L::kRawBytes);
-        tma_load_3d(smem + L::kRaw + s * L::kRawBytes, &wmap, &rfull[s], 0, sb, n0);
+        tma_load_3d(smem + L::kRaw + s * L::kRawBytes, &wmap, &rfull[s], 0, sb_lo + sb, n0);
       }
     }
   } else if (warp >= 4) {
@@ -242,45 +308,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && mbar_wait(accfull, 0u, a.err)) {
+    acc_ready = ok && mbar_wait(accfull, 0u, a.err);
+    if (KS == 1 && acc_ready) {
       tc_fence_after();
       const int q = warp & 3;  // TMEM lane quarter of this warp
       for (int sub = 0; sub < kSub; ++sub) {
         const int m = m0 + 128 * sub + 32 * q + lane;
-        __nv_bfloat16 *yrow = a.y + (int64_t)m * a.ldy;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           uint32_t r[16];
           tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + c0), r);
           tmem_ld_wait();
-          const int n = n0 + c0;
-          if (m < a.m && n < a.n) {
-            uint4 o0, o1;
-            o0.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
-            o0.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
-            o0.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
-            o0.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
-            o1.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
-            o1.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
-            o1.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
-            o1.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
-            if (n + 16 <= a.n) {
-              *reinterpret_cast<uint4 *>(yrow + n) = o0;
-              *reinterpret_cast<uint4 *>(yrow + n + 8) = o1;
-            } else {
-              const uint32_t v[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-              for (int e = 0; e < 16 && n + e < a.n; ++e)
-                yrow[n + e] = __ushort_as_bfloat16((unsigned short)(v[e >> 1] >> (16 * (e & 1))));
-            }
-          }
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+          store_y16(a, m, n0 + c0, v);
         }
       }
     }
   }
 
+  if constexpr (KS > 1) {
+    // ---------------------------------------------------------- split-K sum
+    // Two rounds of two 128-token sub-tiles.  Every CTA copies its partials
+    // from TMEM into its own X stage area (idle now); after a cluster barrier
+    // each CTA takes the 16-column chunks i with i % KS == its K rank, adds the
+    // KS partials of those in K-rank order (its own from TMEM, the others from
+    // the peers' shared memory) and stores Y; a second barrier frees the
+    // buffers.  Every thread of every CTA passes both barriers of each round,
+    // whatever happened before.  Layout: 16 columns of a row are four 16-byte
+    // units, unit u stored at slot u ^ ((row >> 1) & 3) so that eight
+    // consecutive rows hit eight different bank groups.
+    float4 *buf = reinterpret_cast<float4 *>(smem + L::kX);  // [s2][c0/16][row][4]
+    const bool epi = warp >= 4;
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const int swz = (row >> 1) & 3;
+    constexpr int kChunks = 2 * (BN / 16);  // 16-column chunks per round
+    auto unit = [&](int idx, int u) { return (idx * 128 + row) * 4 + (u ^ swz); };
+    if (epi && acc_ready) tc_fence_after();
+    for (int p = 0; p < kSub / 2; ++p) {
+      if (epi && acc_ready) {
+#pragma unroll 1
+        for (int idx = 0; idx < kChunks; ++idx) {
+          if (idx % KS == (int)krank) continue;  // kept in TMEM, read there below
+          const int s2 = idx / (BN / 16), c0 = (idx % (BN / 16)) * 16;
+          uint32_t r[16];
+          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((2 * p + s2) * BN + c0), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            buf[unit(idx, u)] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                            __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        }
+      }
+      cluster_sync();
+      if (epi && acc_ready) {
+#pragma unroll 1
+        for (int idx = (int)krank; idx < kChunks; idx += KS) {
+          const int s2 = idx / (BN / 16), c0 = (idx % (BN / 16)) * 16;
+          float4 pv[KS][4];
+#pragma unroll
+          for (int z = 0; z < KS; ++z)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (z != (int)krank)
+                pv[z][u] = ld_peer_v4(peer_smem(smem_u32(&buf[unit(idx, u)]), rank + CS * (uint32_t)z));
+          uint32_t r[16];
+          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((2 * p + s2) * BN + c0), r);
+          tmem_ld_wait();
+          float v[16];
+#pragma unroll
+          for (int z = 0; z < KS; ++z) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const bool mine = z == (int)krank;
+              const float t0 = mine ? __uint_as_float(r[4 * u]) : pv[z][u].x;
+              const float t1 = mine ? __uint_as_float(r[4 * u + 1]) : pv[z][u].y;
+              const float t2 = mine ? __uint_as_float(r[4 * u + 2]) : pv[z][u].z;
+              const float t3 = mine ? __uint_as_float(r[4 * u + 3]) : pv[z][u].w;
+              v[4 * u] = z ? v[4 * u] + t0 : t0;
+              v[4 * u + 1] = z ? v[4 * u + 1] + t1 : t1;
+              v[4 * u + 2] = z ? v[4 * u + 2] + t2 : t2;
+              v[4 * u + 3] = z ? v[4 * u + 3] + t3 : t3;
+            }
+          }
+          store_y16(a, m0 + 128 * (2 * p + s2) + row, n0 + c0, v);
+        }
+      }
+      cluster_sync();
+    }
+  }
+
   tc_fence_before();
   __syncthreads();
-  if (CS > 1) cluster_sync();  // no peer may still multicast into this CTA
+  if (CS * KS > 1) cluster_sync();  // no peer may still multicast into this CTA
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -291,21 +413,33 @@ constexpr int kBN = 128;
 
 std::once_flag g_gemm_attr;
 
+template <int CS, int KS>
+void gemm_allow() {
+  cudaFuncSetAttribute(gemm_kernel<kBN, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       GemmSmem<kBN>::kAlloc);
+  if (CS * KS > 8)
+    cudaFuncSetAttribute(gemm_kernel<kBN, CS, KS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 void gemm_attributes() {
-  cudaFuncSetAttribute(gemm_kernel<kBN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<kBN>::kAlloc);
-  cudaFuncSetAttribute(gemm_kernel<kBN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<kBN>::kAlloc);
-  cudaFuncSetAttribute(gemm_kernel<kBN, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<kBN>::kAlloc);
-  cudaFuncSetAttribute(gemm_kernel<kBN, 2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  cudaFuncSetAttribute(gemm_kernel<kBN, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  gemm_allow<1, 1>();
+  gemm_allow<2, 1>();
+  gemm_allow<4, 1>();
+  gemm_allow<1, 2>();
+  gemm_allow<1, 3>();
+  gemm_allow<1, 4>();
+  gemm_allow<2, 2>();
+  gemm_allow<2, 3>();
+  gemm_allow<2, 4>();
 }
 
 }  // namespace
 
 #ifndef Q4K_GEMM_CLUSTER
 #define Q4K_GEMM_CLUSTER 2
+#endif
+#ifndef Q4K_GEMM_SPLITK  // split K across a cluster when the output tiles cannot fill the SMs
+#define Q4K_GEMM_SPLITK 1
 #endif
 
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
@@ -316,9 +450,11 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   {
     const uint64_t dims[2] = {(uint64_t)k, (uint64_t)m};
     const uint64_t strides[1] = {(uint64_t)ldx * 2};
-    const uint32_t box[2] = {(uint32_t)kBK, 128u};
+    const uint32_t box[2] = {(uint32_t)kXK, 128u};
     if (encode_tiled(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims,
-                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+                     strides, box,
+                     kXK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) !=
+        CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
@@ -338,13 +474,20 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   args.err = device_error_word();
 
   int ntiles = (int)((n + kBN - 1) / kBN);
-  int cs = Q4K_GEMM_CLUSTER;
-  while (cs > 1 && ntiles < 2 * cs) cs >>= 1;
-  ntiles = (ntiles + cs - 1) / cs * cs;
   const int mtiles = (int)((m + kTokens - 1) / kTokens);
+  // Too few output tiles to fill the SMs (a wide-K projection such as the
+  // 17408 -> 5120 down projection): split K across a cluster instead.
+  int ks = 1;
+  if (Q4K_GEMM_SPLITK) {
+    ks = std::max(1, std::min(4, device_facts()->sm_count / std::max(1, ntiles * mtiles)));
+    while (ks > 1 && nsb < 2 * ks) --ks;
+  }
+  int cs = Q4K_GEMM_CLUSTER;
+  while (cs > 1 && (ntiles < 2 * cs || cs * ks > 8)) cs >>= 1;
+  ntiles = (ntiles + cs - 1) / cs * cs;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, 1);
+  cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, (unsigned)ks);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = GemmSmem<kBN>::kAlloc;
   cfg.stream = stream;
@@ -352,12 +495,21 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cs == 4) return cudaLaunchKernelEx(&cfg, gemm_kernel<kBN, 4>, xmap, wmap, args);
-  if (cs == 2) return cudaLaunchKernelEx(&cfg, gemm_kernel<kBN, 2>, xmap, wmap, args);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<kBN, 1>, xmap, wmap, args);
+  auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, xmap, wmap, args); };
+  if (cs == 2) {
+    if (ks == 4) return go(gemm_kernel<kBN, 2, 4>);
+    if (ks == 3) return go(gemm_kernel<kBN, 2, 3>);
+    if (ks == 2) return go(gemm_kernel<kBN, 2, 2>);
+    return go(gemm_kernel<kBN, 2, 1>);
+  }
+  if (cs == 4) return go(gemm_kernel<kBN, 4, 1>);
+  if (ks == 4) return go(gemm_kernel<kBN, 1, 4>);
+  if (ks == 3) return go(gemm_kernel<kBN, 1, 3>);
+  if (ks == 2) return go(gemm_kernel<kBN, 1, 2>);
+  return go(gemm_kernel<kBN, 1, 1>);
 }
 
 }  // namespace q4k

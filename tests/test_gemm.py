@@ -52,8 +52,13 @@ def _check(q4k, w, n, k, x, sigma_note=""):
     return got
 
 
+# Few output tiles with enough K take the cluster split-K path, K split 2, 3 or 4
+# ways (uneven ranges included), alone or with X shared by pairs of weight tiles:
+# (128, 256, 1024) 1x2, (512, 384, 2048) 1x4, (64, 300, 1792) 1x3, (700, 130, 2560)
+# 1x4, (513, 1024, 1536) 2x3, (256, 2048, 5120) 2x4, (64, 7680, 1024) 2x2.
 CASES = [(1, 128, 256), (77, 200, 512), (128, 256, 1024), (512, 384, 2048), (600, 130, 768),
-         (513, 1024, 1536), (256, 2048, 5120)]
+         (513, 1024, 1536), (256, 2048, 5120), (64, 300, 1792), (700, 130, 2560),
+         (64, 7680, 1024)]
 
 
 @pytest.mark.parametrize("m,n,k", CASES)
