@@ -377,12 +377,12 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   }
   __syncwarp();
   const uint64_t policy = l2_evict_first_policy();
-  // Copy order on the warp's TMA queue: kPre weight stages (they do not depend
-  // on earlier kernels, so they go out before the dependency wait), then the x
-  // slice, then the rest of the ring.  x is small and read by every CTA, and a
+  // Copy order on the warp's TMA queue: a.pre weight stages (they do not depend
+  // on earlier kernels, so with programmatic dependent launch they go out before
+  // the dependency wait), then the x slice, then the rest of the ring.  x is small and read by every CTA, and a
   // copy queued behind a full ring of weights waits for that ring to drain
   // from DRAM; this order keeps x near the head.
-  constexpr int kPre = Q4K_GEMV_PRE_STAGES < STAGES ? Q4K_GEMV_PRE_STAGES : STAGES;
+  const int kPre = min(a.pre, STAGES);  // 0 unless launched with programmatic dependence
   if (lane == 0) {
     for (int s = 0; s < kPre && s < nstages; ++s) {
       mbar_arrive_expect_tx(&bars[s], kStageBytes);
@@ -1154,7 +1154,7 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
                                               : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   };
 
-  GemvArgs args;
+  GemvArgs args = {};
   args.w = static_cast<const uint8_t *>(w);
   args.row_bytes = (int64_t)nsb * kBlockBytes;
   args.x = static_cast<const __nv_bfloat16 *>(x);
@@ -1217,6 +1217,7 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
     GemvKernel kern = b1_select(p.mt, p.s);
+    args.pre = overlap ? Q4K_GEMV_PRE_STAGES : 0;
     static int logged = 0;
     if (Q4K_GEMV_LOG_PLAN && logged < 64 && ++logged)
       fprintf(stderr, "q4k_gemv plan n=%lld k=%lld: mt=%d s=%d warps=%d ks=%d smem=%d grid=%d\n",
