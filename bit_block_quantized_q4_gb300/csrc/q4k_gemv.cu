@@ -5,29 +5,36 @@
 //
 // The weights are streamed from HBM exactly once.  Each warp owns 16*MT output
 // rows and a contiguous slice of super-blocks; a private ring of shared-memory
-// stages is filled by TMA (one 3-D box = 16*MT rows x one 144-byte
-// super-block per stage).  In registers, a 4-bit quant q becomes the bf16
-// value 128+q with one AND/OR (exact), and the contraction runs on the tensor
-// cores (mma.sync m16n8k16, bf16 x bf16 products are exact, fp32 accumulate):
-//     sum_i (d sc_j q_i - dmin m_j) x_i
-//         = d sc_j (sum_i (128+q_i) x_i - 128 X_j) - dmin m_j X_j,
-// X_j = sum_i x_i over sub-block j.  128 X_j is produced by the same MMA
-// path with a constant A = 128, so a sub-block whose quants are all zero
-// cancels exactly.  Per-sub-block scales are applied in fp32 once per
-// (row, sub-block, batch column).
+// stages is filled by TMA (one 2-D box = 16*MT rows x S 144-byte super-blocks
+// per stage).  The contraction runs on the tensor cores (mma.sync m16n8k16,
+// fp32 accumulate) in the factored form
+//     sum_i (d sc_j q_i - dmin m_j) x_i = d sc_j S_j - dmin m_j X_j,
+// S_j = sum_i q_i x_i, X_j = sum_i x_i over sub-block j, with the scales
+// applied in fp32 once per (row, sub-block, batch column).
 //
-// Batch 1: the eight MMA columns carry the eight sub-blocks of a super-block
+// Batch 1 (fp16 operands): each warp copies its x slice into shared memory with
+// one bulk copy and converts it in place, per 256-value super-block, to fp16
+// scaled by a power of two 2^s (largest magnitude in [2^14, 2^15): exact for
+// every value within 2^28 of that maximum), plus the sums X_j.  A quant
+// becomes the fp16 value 1024+q (low nibble) or 1024+16q (high nibble) with
+// one LOP3.  The eight MMA columns carry the eight sub-blocks of a super-block
 // (column j of B holds x only in the k-slots that carry sub-block j), so one
 // super-block needs 16 MMAs per 16 rows and each thread ends with exactly the
-// (row, sub-block) sums whose scales it decodes itself.
-// Batch 2..16: the MMA columns carry the batch rows (one or two n-tiles of 8);
-// every sub-block is its own 2-step accumulation and the scales are shared
-// within a thread quad by shuffles.
+// (row, sub-block) sums whose scales it decodes itself; each super-block's
+// contribution is multiplied by 2^-s before it joins the row sum.
+// Batch 2..16 (bf16 operands): a quant becomes the bf16 value 128+q (exact);
+// the MMA columns carry the batch rows (one or two n-tiles of 8); every
+// sub-block is its own 2-step accumulation, 128 X_j comes from the same MMA
+// path with a constant A = 128 (so an all-zero sub-block cancels exactly), and
+// the scales are shared within a thread quad by shuffles.  The x fragments are
+// loaded from L2 half a super-block ahead of their use.
 //
 // Split-K: the warps of a CTA take consecutive super-block slices of the same
 // rows; partial sums meet in shared memory and are added in warp order, so the
 // result is deterministic.  Grids are sized so that every CTA is resident at
-// once (one wave) whenever the shape allows.
+// once (one wave) whenever the shape allows.  With programmatic dependent
+// launch (Q4K_FLAG_OVERLAP_WEIGHTS) the first weight stages are requested
+// before the wait for the previous kernel; x only after it.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -46,9 +53,6 @@
 #ifndef Q4K_GEMV_PRE_STAGES  // batch 1: weight stages issued before x and the dependency wait
 #define Q4K_GEMV_PRE_STAGES 2
 #endif
-#ifndef Q4K_GEMV_X_FIRST  // batch 1: 0 ring right after x, 1 ring once x has landed, 2 CTA barrier between
-#define Q4K_GEMV_X_FIRST 0
-#endif
 #ifndef Q4K_GEMV_EVICT_FIRST  // L2 evict-first hint on weight loads
 #define Q4K_GEMV_EVICT_FIRST 1
 #endif
@@ -59,7 +63,6 @@ namespace {
 
 constexpr int kRowsPerTile = 16;
 constexpr int kTileBytes = kRowsPerTile * kBlockBytes;  // 2304, a multiple of 128
-constexpr int kSmemReservedPerCta = 1024;  // shared memory the runtime keeps per resident CTA
 
 struct GemvArgs {
   const uint8_t *w;      // weights (row-major super-blocks)
@@ -73,9 +76,7 @@ struct GemvArgs {
   int batch;
   int warp_bytes;  // shared bytes per warp region
   unsigned *err;   // device error word
-  int stages;      // persistent batch 1: weight stages in each warp's ring
-  int pre;         // persistent batch 1: stages issued before the dependency wait
-  int ntiles;      // persistent batch 1: row tiles of 16*MT rows
+  int pre;         // batch 1: weight stages issued before the dependency wait
 };
 
 // W is viewed as a 2-D array of 8-byte elements, [n rows][nsb * 18]; one box
@@ -203,21 +204,18 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
 // Then 16 zero words.  Lane l handles values 8l .. 8l+7 of each super-block
 // (lanes 4j..4j+3 cover sub-block j); the loads of up to 8 super-blocks are all
 // issued before any of them is used.
-// kInPlace: x is the raw bf16 slice already copied into xperm's own words (each
-// lane rewrites only the 16 bytes it read); otherwise x is global memory.
-template <bool kInPlace>
-__device__ __forceinline__ void b1_stage_x(const __nv_bfloat16 *x, int nsb, uint32_t *xperm,
-                                           float *xsum, float *unscale, uint32_t *xzero, int lane) {
-  const uint4 *xs = reinterpret_cast<const uint4 *>(x);
+// On entry xperm holds the raw bf16 slice (one bulk copy); each lane rewrites
+// only the 16 bytes it read.
+__device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float *xsum, float *unscale,
+                                           uint32_t *xzero, int lane) {
+  const uint4 *xs = reinterpret_cast<const uint4 *>(xperm);
   constexpr int kChunk = 8;  // super-blocks in flight together (no early exit: full ILP)
   for (int base = 0; base < nsb; base += kChunk) {
     uint4 u[kChunk];
     uint32_t mx[kChunk];
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      u[j] = (base + j >= nsb) ? make_uint4(0, 0, 0, 0)
-             : kInPlace     ? xs[(base + j) * 32 + lane]
-                            : __ldg(xs + (base + j) * 32 + lane);
+      u[j] = (base + j < nsb) ? xs[(base + j) * 32 + lane] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
@@ -299,25 +297,10 @@ __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], bool ok,
   }
 }
 
-// After a timed-out wait in a batch-1 warp: give the copies it may still have
-// in flight (the x slice when x_pending; the weight stages of iterations it ..
-// end-1) the same bounded time to land before the CTA exits and its
+// After a timed-out wait: give the copies a warp may still have in flight (the
+// x slice when xbar is given, then ring iterations it .. end-1 of a ring of
+// `stages` slots) the same bounded time to land before the CTA exits and its
 // shared memory is handed to another CTA.
-template <int STAGES>
-__device__ __noinline__ void b1_drain(uint64_t *bars, int it, int end, bool x_pending) {
-  const uint64_t t0 = global_ns();
-  auto landed = [&](uint64_t *b, uint32_t parity) {
-    while (!mbar_try_wait(b, parity, 1000u))
-      if (global_ns() - t0 > kWaitLimitNs) return false;
-    return true;
-  };
-  if (x_pending && !landed(&bars[STAGES], 0)) return;
-  for (int j = it; j < end; ++j)
-    if (!landed(&bars[j % STAGES], (j / STAGES) & 1)) return;
-}
-
-// As b1_drain, for a ring of runtime depth: iterations it .. end-1 of a ring of
-// `stages` slots, then (when given) the x barrier.
 __device__ __noinline__ void b1_drain_ring(uint64_t *bars, int stages, int it, int end,
                                            uint64_t *xbar) {
   const uint64_t t0 = global_ns();
@@ -394,23 +377,18 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
     mbar_arrive_expect_tx(&bars[STAGES], nsteps * kQK * 2);
     bulk_load(xperm, a.x + (int64_t)sb0 * kQK, nsteps * kQK * 2, &bars[STAGES]);
   }
-  bool ok = true;
-  if (Q4K_GEMV_X_FIRST == 1) ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
-  if (Q4K_GEMV_X_FIRST == 2) __syncthreads();  // every warp's x ahead of the CTA's ring
-  const int issued = ok ? min(STAGES, nstages) : min(kPre, nstages);
-  if (lane == 0 && ok) {
+  if (lane == 0) {
     for (int s = kPre; s < STAGES && s < nstages; ++s) {
       mbar_arrive_expect_tx(&bars[s], kStageBytes);
       load_tile(ring + s * kStageBytes, &wmap, &bars[s], sb0 + s * S, row0, policy);
     }
   }
   grid_launch_dependents();
-  if (Q4K_GEMV_X_FIRST != 1) ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
+  bool ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
   if (ok) {
-    b1_stage_x<true>(reinterpret_cast<const __nv_bfloat16 *>(xperm), nsteps, xperm, xsum, xuns,
-                     xzero, lane);
+    b1_stage_x(nsteps, xperm, xsum, xuns, xzero, lane);
   } else if (lane == 0) {
-    b1_drain<STAGES>(bars, 0, issued, true);
+    b1_drain_ring(bars, STAGES, 0, min(STAGES, nstages), &bars[STAGES]);
   }
 
   // B fragments: lane (g, t) with t == g/2 carries sub-block g on the steps of
@@ -443,7 +421,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
       if (it >= nstages) break;
       if (!mbar_wait(&bars[stage], phase, a.err)) {
         ok = false;
-        if (lane == 0) b1_drain<STAGES>(bars, it, min(it + STAGES, nstages), false);
+        if (lane == 0) b1_drain_ring(bars, STAGES, it, min(it + STAGES, nstages), nullptr);
         break;
       }
       uint8_t *st = ring + stage * kStageBytes;
@@ -480,243 +458,6 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   }
 
   b1_finish<MT>(yacc, ok, red, row0, a);
-}
-
-// Batch 1, persistent: one CTA per SM walks the row tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ...; its warps split K into contiguous slices as in
-// gemv_b1_kernel.  Each warp stages its x slice once per launch and keeps one
-// ring of a.stages weight stages running across all of its tiles, so there is
-// no per-tile start-up; the partials of a tile meet in a double-buffered shared
-// array behind one CTA barrier per tile.  With programmatic dependent launch
-// the first a.pre stages go out before the dependency wait: a CTA that is
-// resident while the previous projection still runs fills its ring early.
-// Shared memory per warp: a.stages weight stages | x slice | sums X_j | 2^-s_i
-// (padded to 16 bytes) | 64 zero bytes | a.stages + 1 mbarriers (ring, x);
-// then the CTA's two partial arrays.
-template <int MT, int S>
-__global__ void __launch_bounds__(384) gemv_b1p_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                       const GemvArgs a) {
-  constexpr int kStageBytes = MT * S * kTileBytes;
-  constexpr int kRowBytes = S * kBlockBytes;
-  constexpr int kRows = MT * kRowsPerTile;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int stages = a.stages;
-  const int sb0 = warp * a.ks;
-  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);  // super-blocks of this warp
-  const int nstg = (nsteps + S - 1) / S;                     // ring stages per tile
-  const int ntl = (int)blockIdx.x < a.ntiles
-                      ? (a.ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
-                      : 0;                                   // tiles of this CTA
-  const int total = ntl * nstg;                              // ring iterations of this warp
-
-  uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
-  uint8_t *ring = wreg;
-  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + stages * kStageBytes);  // ks*128 words
-  float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  float *xuns = xsum + a.ks * 8;
-  uint32_t *xzero = reinterpret_cast<uint32_t *>(xuns + pad4(a.ks));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);  // ring + 1 for x
-  uint64_t *xbar = bars + stages;
-  float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);  // [2][nwarps][kRows]
-
-  if (lane == 0) {
-    prefetch_tmap(&wmap);
-    for (int s = 0; s <= stages; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  const uint64_t policy = l2_evict_first_policy();
-  // Ring iteration q holds stage q % nstg of this CTA's tile q / nstg.
-  auto issue = [&](int q) {
-    const int j = q / nstg, u = q - j * nstg;
-    const int slot = q % stages;
-    const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kRows;
-    mbar_arrive_expect_tx(&bars[slot], kStageBytes);
-    load_tile(ring + slot * kStageBytes, &wmap, &bars[slot], sb0 + u * S, row0, policy);
-  };
-  const int first = min(stages, total);
-  const int pre = min(a.pre, first);
-  if (lane == 0)
-    for (int q = 0; q < pre; ++q) issue(q);
-  grid_dependency_wait();
-  if (lane == 0) {
-    if (nsteps > 0 && ntl > 0) {
-      mbar_arrive_expect_tx(xbar, nsteps * kQK * 2);
-      bulk_load(xperm, a.x + (int64_t)sb0 * kQK, nsteps * kQK * 2, xbar);
-    }
-    for (int q = pre; q < first; ++q) issue(q);
-  }
-  grid_launch_dependents();
-  bool ok = ntl == 0 || nsteps == 0 || mbar_wait(xbar, 0, a.err);
-  if (ok) {
-    b1_stage_x<true>(reinterpret_cast<const __nv_bfloat16 *>(xperm), nsteps, xperm, xsum, xuns,
-                     xzero, lane);
-  } else if (lane == 0) {
-    b1_drain_ring(bars, stages, 0, first, xbar);
-  }
-
-  const bool own = (t == (g >> 1));
-  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
-  const uint32_t *pe0 = own_e ? xperm + g * 16 : xzero;
-  const uint32_t *po0 = own_o ? xperm + g * 16 : xzero;
-  const int adv_e = own_e ? 128 : 0, adv_o = own_o ? 128 : 0;
-  const B1Lane lc = b1_lane(t);
-  const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
-  uint32_t magic;
-  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
-
-  int q = 0;  // ring iteration
-  for (int j = 0; j < ntl; ++j) {
-    float2 yacc[MT];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
-    for (int u = 0; u < nstg && ok; ++u, ++q) {
-      const int slot = q % stages;
-      if (!mbar_wait(&bars[slot], (q / stages) & 1, a.err)) {
-        ok = false;
-        if (lane == 0) b1_drain_ring(bars, stages, q, min(q + stages, total), nullptr);
-        break;
-      }
-      const uint8_t *st = ring + slot * kStageBytes;
-      const int cnt = min(S, nsteps - u * S);
-      uint4 hdr[S][MT][2], qa[S][MT][2][2];
-#pragma unroll
-      for (int v = 0; v < S; ++v) {
-        if (v >= cnt) break;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const uint8_t *rp = st + (mt * kRowsPerTile + g + 8 * r) * kRowBytes + v * kBlockBytes;
-            hdr[v][mt][r] = *reinterpret_cast<const uint4 *>(rp);
-            qa[v][mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
-            qa[v][mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
-          }
-        }
-      }
-      __syncwarp();  // the stage is in registers: refill it
-      if (lane == 0 && q + stages < total) issue(q + stages);
-#pragma unroll
-      for (int v = 0; v < S; ++v) {
-        if (v >= cnt) break;
-        const int i = u * S + v;  // super-block within the slice
-        b1_super_block<MT>(hdr[v], qa[v], pe0 + i * adv_e, po0 + i * adv_o, px[4 * i], xuns[i], lc,
-                           magic, yacc);
-      }
-    }
-    // Tile epilogue: quad reduction, partials in warp order, one barrier.
-    float *rb = red + (j & 1) * (nwarps * kRows);
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float v = r ? yacc[mt].y : yacc[mt].x;
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        if (t == 0) rb[warp * kRows + mt * kRowsPerTile + g + 8 * r] = v;
-      }
-    }
-    __syncwarp();
-    if (!ok && lane == 0) rb[warp * kRows] = __int_as_float(0x7fc00000);
-    __syncthreads();
-    if ((int)threadIdx.x < kRows) {
-      float sum = 0.f;
-      for (int w = 0; w < nwarps; ++w) sum += rb[w * kRows + threadIdx.x];
-      const int row = ((int)blockIdx.x + j * (int)gridDim.x) * kRows + (int)threadIdx.x;
-      if (row < a.n) a.y[row] = sum;
-    }
-  }
-}
-
-// 16-byte read of streamed weights (read once: L2 evict-first).
-__device__ __forceinline__ uint4 ldg_stream(const void *p, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(policy));
-  return v;
-}
-
-// Batch 1 with the weights streamed by plain 16-byte loads into registers (one
-// super-block ahead, two register buffers) instead of a TMA ring: shared
-// memory holds only the staged x slice, so residency is bound by registers.
-// Same MMA mapping, x staging and epilogue as gemv_b1_kernel.
-template <int MT>
-__global__ void __launch_bounds__(256) gemv_b1_ldg_kernel(const GemvArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int row0 = blockIdx.x * (MT * kRowsPerTile);
-  const int sb0 = warp * a.ks;
-  const int nsteps = max(0, min(a.nsb, sb0 + a.ks) - sb0);
-
-  uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
-  uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg);
-  float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  float *xuns = xsum + a.ks * 8;
-  uint32_t *xzero = reinterpret_cast<uint32_t *>(xuns + pad4(a.ks));
-  float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
-
-  // Rows past n read row n-1; their results are never stored.
-  const uint8_t *rp[MT][2];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = min(row0 + mt * kRowsPerTile + g + 8 * r, a.n - 1);
-      rp[mt][r] = a.w + (int64_t)row * a.row_bytes + (int64_t)sb0 * kBlockBytes;
-    }
-  const uint64_t policy = l2_evict_first_policy();
-  uint4 hA[MT][2], qA[MT][2][2], hB[MT][2], qB[MT][2][2];
-  auto load = [&](uint4 (&h)[MT][2], uint4 (&q)[MT][2][2], int i) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint8_t *p = rp[mt][r] + (int64_t)i * kBlockBytes;
-        h[mt][r] = ldg_stream(p, policy);
-        q[mt][r][0] = ldg_stream(p + kQsOffset + 32 * t, policy);
-        q[mt][r][1] = ldg_stream(p + kQsOffset + 32 * t + 16, policy);
-      }
-  };
-  // The weights do not depend on earlier kernels; x does.
-  if (nsteps > 0) load(hA, qA, 0);
-  if (nsteps > 1) load(hB, qB, 1);
-  grid_dependency_wait();
-  grid_launch_dependents();
-  b1_stage_x<false>(a.x + (int64_t)sb0 * kQK, nsteps, xperm, xsum, xuns, xzero, lane);
-
-  const bool own = (t == (g >> 1));
-  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
-  const uint32_t *pe = own_e ? xperm + g * 16 : xzero;
-  const uint32_t *po = own_o ? xperm + g * 16 : xzero;
-  const int adv_e = own_e ? 128 : 0, adv_o = own_o ? 128 : 0;
-  const B1Lane lc = b1_lane(t);
-  const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
-  uint32_t magic;
-  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
-
-  float2 yacc[MT];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) yacc[mt] = make_float2(0.f, 0.f);
-  for (int i = 0; i < nsteps; i += 2) {
-    b1_super_block<MT>(hA, qA, pe, po, px[4 * i], xuns[i], lc, magic, yacc);
-    pe += adv_e;
-    po += adv_o;
-    if (i + 2 < nsteps) load(hA, qA, i + 2);
-    if (i + 1 >= nsteps) break;
-    b1_super_block<MT>(hB, qB, pe, po, px[4 * (i + 1)], xuns[i + 1], lc, magic, yacc);
-    pe += adv_e;
-    po += adv_o;
-    if (i + 3 < nsteps) load(hB, qB, i + 3);
-  }
-  b1_finish<MT>(yacc, true, red, row0, a);
 }
 
 // ---------------------------------------------------------------- batch 2..16
@@ -931,12 +672,6 @@ constexpr int kStages = Q4K_GEMV_STAGES;  // batch 2..16 (one super-block per st
 #ifndef Q4K_GEMV_INFLIGHT_KB  // planner: weight bytes in flight per SM worth having, at most
 #define Q4K_GEMV_INFLIGHT_KB 96
 #endif
-#ifndef Q4K_GEMV_OVERLAP_SMEM_PCT  // batch 1 with overlap: share of each SM's shared memory a launch may hold
-#define Q4K_GEMV_OVERLAP_SMEM_PCT 100
-#endif
-#ifndef Q4K_GEMV_PERSIST  // batch 1 with overlap: persistent one-CTA-per-SM kernel
-#define Q4K_GEMV_PERSIST 0
-#endif
 #ifndef Q4K_GEMV_LOG_PLAN  // 1: print each batch-1 plan to stderr (tuning aid)
 #define Q4K_GEMV_LOG_PLAN 0
 #endif
@@ -950,9 +685,6 @@ template <int S> struct B1Stages {
 #endif
 #ifndef Q4K_GEMV_FORCE_MT
 #define Q4K_GEMV_FORCE_MT 0
-#endif
-#ifndef Q4K_GEMV_LDG  // batch 1: 1 = weights by 16-byte loads, 0 = TMA ring
-#define Q4K_GEMV_LDG 0
 #endif
 
 struct Plan {
@@ -982,7 +714,7 @@ int occupancy(K kernel, int threads, int smem) {
 // bytes in flight per SM (latency hiding), then an even split.
 template <typename K>
 Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int cols,
-              const DeviceFacts *f, int smem_budget_sm = 0) {
+              const DeviceFacts *f) {
   Plan best;
   const int tile_rows = mt * kRowsPerTile;
   const int grid = (n + tile_rows - 1) / tile_rows;
@@ -994,10 +726,7 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
     const int wb = b1 ? warp_bytes_b1(mt, s, stages, ks) : warp_bytes_bn(mt);
     const int smem = wk * wb + wk * tile_rows * cols * 4;
     if (smem > f->max_smem_optin) continue;
-    int occ = occupancy(kernel, wk * 32, smem);
-    // With overlap, leave part of every SM to the next projection's CTAs so
-    // they can be resident (and stream their weights) while this one runs.
-    if (smem_budget_sm > 0) occ = std::min(occ, smem_budget_sm / (smem + kSmemReservedPerCta));
+    const int occ = occupancy(kernel, wk * 32, smem);
     if (occ <= 0) continue;
     const int slots = occ * f->sm_count;
     const int waves = (grid + slots - 1) / slots;
@@ -1041,11 +770,6 @@ void set_attributes(const DeviceFacts *f) {
   allow_smem(b1_kernel<1, 4>(), f);
   allow_smem(b1_kernel<2, 1>(), f);
   allow_smem(b1_kernel<2, 2>(), f);
-  allow_smem(gemv_b1_ldg_kernel<1>, f);
-  allow_smem(gemv_b1p_kernel<1, 1>, f);
-  allow_smem(gemv_b1p_kernel<1, 2>, f);
-  allow_smem(gemv_b1p_kernel<2, 1>, f);
-  allow_smem(gemv_b1_ldg_kernel<2>, f);
   allow_smem(gemv_bn_kernel<1, 1, kStages>, f);
   allow_smem(gemv_bn_kernel<1, 2, kStages>, f);
   allow_smem(gemv_bn_kernel<2, 1, kStages>, f);
@@ -1054,63 +778,6 @@ void set_attributes(const DeviceFacts *f) {
 
 using GemvKernel = void (*)(CUtensorMap, GemvArgs);
 
-// Persistent batch-1 plan: one CTA per SM (grid = min(tiles, SMs)).  Among
-// tile heights MT, stage widths S and warp counts, take the smallest per-warp
-// serial work (tile rounds x super-blocks per warp x MT), then more warps, then
-// a deeper ring.  The ring fills the shared-memory budget; with overlap the
-// budget is under half an SM and two CTAs must fit per SM, so the next
-// projection's CTA can be resident alongside.
-struct PPlan {
-  int mt = 0, s = 0, wk = 0, ks = 0, stages = 0, warp_bytes = 0, smem = 0, grid = 0, ntiles = 0;
-  long est = 0;
-};
-using GemvKernelP = void (*)(const CUtensorMap, const GemvArgs);
-GemvKernelP b1p_select(int mt, int s) {
-  if (mt == 2) return gemv_b1p_kernel<2, 1>;
-  return s == 2 ? gemv_b1p_kernel<1, 2> : gemv_b1p_kernel<1, 1>;
-}
-PPlan plan_b1p(int n, int nsb, bool overlap, const DeviceFacts *f) {
-  PPlan best;
-  const int budget = overlap ? f->max_smem_per_sm / 2 - kSmemReservedPerCta : f->max_smem_optin;
-  const int cand[3][2] = {{1, 1}, {1, 2}, {2, 1}};
-  for (const auto &c : cand) {
-    const int mt = c[0], s = c[1];
-    if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
-    if (Q4K_GEMV_FORCE_S && s != Q4K_GEMV_FORCE_S) continue;
-    GemvKernelP kern = b1p_select(mt, s);
-    const int rows = mt * kRowsPerTile;
-    const int ntiles = (n + rows - 1) / rows;
-    const int grid = std::min(ntiles, f->sm_count);
-    const int rounds = (ntiles + grid - 1) / grid;
-    const int stage_bytes = mt * s * kTileBytes;
-    for (int wk = 1; wk <= 12; ++wk) {
-      int ks = (nsb + wk - 1) / wk;
-      ks = (ks + s - 1) / s * s;
-      if ((nsb + ks - 1) / ks != wk) continue;  // no empty warps
-      const int red_bytes = 2 * wk * rows * 4;
-      const int fixed = ks * (512 + 32) + 4 * pad4(ks) + 64 + 8;
-      const int per_warp = (budget - red_bytes) / wk - 127;  // 127: rounding to 128
-      int stages = (per_warp - fixed) / (stage_bytes + 8);
-      const int need = rounds * ((ks + s - 1) / s);  // ring iterations of a warp
-      stages = std::min(std::min(stages, 16), need);
-      if (stages < 2 && need >= 2) continue;
-      stages = std::max(stages, 1);
-      const int wb = (stages * stage_bytes + fixed + stages * 8 + 127) / 128 * 128;
-      const int smem = wk * wb + red_bytes;
-      if (smem > budget || smem > f->max_smem_optin) continue;
-      const int occ = occupancy(kern, wk * 32, smem);
-      if (occ < (overlap ? 2 : 1)) continue;
-      const long est = (long)rounds * ks * mt;
-      const bool better = best.grid == 0 || est < best.est ||
-                          (est == best.est && (wk > best.wk || (wk == best.wk && stages > best.stages)));
-      if (better) {
-        best.mt = mt; best.s = s; best.wk = wk; best.ks = ks; best.stages = stages;
-        best.warp_bytes = wb; best.smem = smem; best.grid = grid; best.ntiles = ntiles; best.est = est;
-      }
-    }
-  }
-  return best;
-}
 GemvKernel b1_select(int mt, int s) {
   if (mt == 2) return s == 2 ? b1_kernel<2, 2>() : b1_kernel<2, 1>();
   return s == 4 ? b1_kernel<1, 4>() : s == 2 ? b1_kernel<1, 2>() : b1_kernel<1, 1>();
@@ -1166,53 +833,15 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   args.batch = (int)batch;
   args.err = device_error_word();
 
-  if (batch == 1 && Q4K_GEMV_LDG) {
+  if (batch == 1) {
     Plan p;
-    for (int mt = 1; mt <= 2; ++mt) {
-      if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
-      const Plan q = plan_for(mt == 2 ? gemv_b1_ldg_kernel<2> : gemv_b1_ldg_kernel<1>, true, mt, 1,
-                              0, (int)n, nsb, 1, f);
-      if (q.grid && q.score > p.score) p = q;
-    }
-    if (p.grid == 0) return cudaErrorInvalidConfiguration;
-    args.ks = p.ks;
-    args.warp_bytes = p.warp_bytes;
-    cudaError_t e = launch(p.mt == 2 ? gemv_b1_ldg_kernel<2> : gemv_b1_ldg_kernel<1>, p, overlap,
-                           stream, args);
-    if (e != cudaSuccess) return e;
-  } else if (batch == 1 && overlap && Q4K_GEMV_PERSIST) {
-    const PPlan pp = plan_b1p((int)n, nsb, overlap, f);
-    if (pp.grid == 0) return cudaErrorInvalidConfiguration;
-    static int logged_p = 0;
-    if (Q4K_GEMV_LOG_PLAN && logged_p < 64 && ++logged_p)
-      fprintf(stderr, "q4k_gemv persistent plan n=%lld k=%lld: mt=%d s=%d warps=%d ks=%d stages=%d "
-              "smem=%d grid=%d tiles=%d\n", (long long)n, (long long)k, pp.mt, pp.s, pp.wk, pp.ks,
-              pp.stages, pp.smem, pp.grid, pp.ntiles);
-    if (encode(pp.mt, pp.s) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    args.ks = pp.ks;
-    args.warp_bytes = pp.warp_bytes;
-    args.stages = pp.stages;
-    args.pre = pp.stages;
-    args.ntiles = pp.ntiles;
-    Plan lp;
-    lp.grid = pp.grid;
-    lp.wk = pp.wk;
-    lp.smem = pp.smem;
-    cudaError_t e = launch(b1p_select(pp.mt, pp.s), lp, overlap, stream, map, args);
-    if (e != cudaSuccess) return e;
-  } else if (batch == 1) {
-    Plan p;
-    const int budget = overlap && Q4K_GEMV_OVERLAP_SMEM_PCT < 100
-                           ? f->max_smem_per_sm * Q4K_GEMV_OVERLAP_SMEM_PCT / 100
-                           : 0;
     const int cand[5][2] = {{1, 1}, {1, 2}, {1, 4}, {2, 1}, {2, 2}};
     for (const auto &c : cand) {
       if (Q4K_GEMV_FORCE_MT && c[0] != Q4K_GEMV_FORCE_MT) continue;
       if (Q4K_GEMV_FORCE_S && c[1] != Q4K_GEMV_FORCE_S) continue;
       const int stages = c[1] == 1 ? B1Stages<1>::value : c[1] == 2 ? B1Stages<2>::value
                                                                      : B1Stages<4>::value;
-      const Plan q = plan_for(b1_select(c[0], c[1]), true, c[0], c[1], stages, (int)n, nsb, 1, f,
-                              budget);
+      const Plan q = plan_for(b1_select(c[0], c[1]), true, c[0], c[1], stages, (int)n, nsb, 1, f);
       if (q.grid && q.score > p.score) p = q;
     }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;

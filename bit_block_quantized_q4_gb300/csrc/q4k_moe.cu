@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
 template <int NT, bool DOWN>
 __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUtensorMap *map1p,
                                             const MoeArgs &a, int nsb, int rows_total,
-                                            uint8_t *smem, int slot) {
+                                            uint8_t *smem, int slot, int ctas) {
   const CUtensorMap &map0 = *map0p, &map1 = *map1p;
   constexpr int NM = DOWN ? 1 : 2;  // weight matrices per stage (gate and up)
   constexpr int kStageBytes = NM * kTile;
@@ -196,7 +196,7 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int ntiles = (rows_total + kRows - 1) / kRows;
-  const int sid = blockIdx.x * kMoeWarps + warp, nsid = gridDim.x * kMoeWarps;
+  const int sid = blockIdx.x * kMoeWarps + warp, nsid = ctas * kMoeWarps;
   const int ntl = sid < ntiles ? (ntiles - sid + nsid - 1) / nsid : 0;  // tiles of this warp
   const int total = ntl * nsb;                                          // ring iterations
   uint8_t *ring = smem + warp * kWarpBytes;
@@ -425,7 +425,10 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
 
 // The MMA width follows the slot: 8 columns when its pairs fit, else 16 or 32
 // (NTMAX n-tiles of 8 at most), so a slot with few pairs does no work for
-// empty columns.  The choice is uniform per CTA.
+// empty columns.  A slot with nt n-tiles gets nt times the warp streams (each
+// with 1/nt of the row tiles), so every stream does about the same work; the
+// grid is sized for the widest class (one tile per stream at NTMAX) and the
+// CTAs a slot does not need exit.  The choice is uniform per CTA.
 template <int NTMAX, bool DOWN>
 __global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
@@ -435,12 +438,15 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
   if (slot >= a.meta[0]) return;  // slot not in use
   const int np = a.slot_start[slot + 1] - a.slot_start[slot];
   const int ncols = DOWN ? 2 * np : np;
-  if (ncols <= 8 || NTMAX == 1)
-    expert_body<1, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
-  else if (ncols <= 16 || NTMAX == 2)
-    expert_body<(NTMAX >= 2 ? 2 : 1), DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
+  const int nt = ncols <= 8 ? 1 : ncols <= 16 ? 2 : 4;  // n-tiles this slot needs
+  const int ctas = (int)gridDim.x * min(nt, NTMAX) / NTMAX;  // CTAs of this slot
+  if ((int)blockIdx.x >= ctas) return;
+  if (nt == 1 || NTMAX == 1)
+    expert_body<1, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
+  else if (nt == 2 || NTMAX == 2)
+    expert_body<(NTMAX >= 2 ? 2 : 1), DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
   else
-    expert_body<NTMAX, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot);
+    expert_body<NTMAX, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
 }
 
 // ---------------------------------------------------------------- 4. combine
@@ -480,12 +486,16 @@ void moe_attributes() {
   allow<4, true>();
 }
 
+// tiles_per_warp: row tiles per warp stream of an 8-column slot; a slot with
+// nt n-tiles has nt times the streams.  The grid holds NT times the streams
+// of an 8-column slot, rounded to a multiple of NT CTAs.
 template <int NT, bool DOWN>
 void launch_expert(int rows, int tiles_per_warp, int max_slots, const CUtensorMap &m0,
                    const CUtensorMap &m1, const MoeArgs &a, int nsb, cudaStream_t stream) {
   const int ntiles = (rows + kRows - 1) / kRows;
   const int per_cta = kMoeWarps * tiles_per_warp;
-  dim3 grid((unsigned)((ntiles + per_cta - 1) / per_cta), (unsigned)max_slots);
+  const int base = (ntiles + per_cta - 1) / per_cta;  // CTAs of an 8-column slot
+  dim3 grid((unsigned)(base * NT), (unsigned)max_slots);
   moe_expert_kernel<NT, DOWN><<<grid, kMoeWarps * 32, expert_smem<NT, DOWN>(), stream>>>(
       m0, m1, a, nsb, rows);
 }
