@@ -370,19 +370,21 @@ def profiled_traffic():
 
 def run_case(case):
     """One small instance of a kernel, for ncu captures (no timing): one 27B-class
-    layer of batch-1 projections (203 MB of weights), the 512-token gate and
+    layer of batch-1 projections (203 MB of weights) or of batch-4 and batch-16
+    projections, the 512-token gate and
     down prefill GEMMs, or one routed-MoE decode step."""
     import bit_block_quantized_q4_gb300 as q4k
     from bit_block_quantized_q4_gb300 import build as qb
     qb.build()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    if case == "gemv_layer":
+    if case in ("gemv_layer", "gemv_layer_batched"):
         layers = Layers(dev, n_layers=1)
-        xs, ys = make_inputs(layers, 1, dev, seed=SEED_C1 + 1)
-        torch.cuda.synchronize()
-        for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
-            q4k.q4k_gemv(w, n, k, x, out=y)
+        for batch in ((1,) if case == "gemv_layer" else (4, 16)):
+            xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
+            torch.cuda.synchronize()
+            for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
+                q4k.q4k_gemv(w, n, k, x, out=y)
     elif case == "gemm_prefill":
         m = 512
         for name, n, k in (("gate", 17408, 5120), ("down", 5120, 17408)):
@@ -448,7 +450,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--layers", type=int, default=N_LAYERS)
-    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemm_prefill", "moe"],
+    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "moe"],
                     help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
     if args.case:

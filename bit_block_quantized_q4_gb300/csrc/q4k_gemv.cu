@@ -805,7 +805,6 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   const DeviceFacts *f = device_facts();
   std::call_once(g_attr_once, set_attributes, f);
   const int nsb = (int)(k / kQK);
-  const int mt_bn = n >= 32 * f->sm_count ? 2 : 1;
 
   // W viewed as [n rows][nsb super-blocks][144 bytes]; one box = 16*mt rows
   // of one super-block.
@@ -857,12 +856,23 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     cudaError_t e = launch(kern, p, overlap, stream, map, args);
     if (e != cudaSuccess) return e;
   } else {
-    const int mt = mt_bn;
     const int nt = batch <= 8 ? 1 : 2;
-    auto kern = (mt == 2) ? (nt == 1 ? gemv_bn_kernel<2, 1, kStages> : gemv_bn_kernel<2, 2, kStages>)
-                          : (nt == 1 ? gemv_bn_kernel<1, 1, kStages> : gemv_bn_kernel<1, 2, kStages>);
-    const Plan p = plan_for(kern, false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
+    auto bn_select = [&](int mt) {
+      return (mt == 2) ? (nt == 1 ? gemv_bn_kernel<2, 1, kStages> : gemv_bn_kernel<2, 2, kStages>)
+                       : (nt == 1 ? gemv_bn_kernel<1, 1, kStages> : gemv_bn_kernel<1, 2, kStages>);
+    };
+    Plan p;
+    for (int mt = 1; mt <= 2; ++mt) {  // the tile height is part of the plan, as at batch 1
+      if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
+      const Plan q = plan_for(bn_select(mt), false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
+      if (q.grid && q.score > p.score) p = q;
+    }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
+    const int mt = p.mt;
+    auto kern = bn_select(mt);
+    if (Q4K_GEMV_LOG_PLAN)
+      fprintf(stderr, "q4k_gemv batched plan n=%lld k=%lld b=%lld: mt=%d warps=%d ks=%d smem=%d grid=%d\n",
+              (long long)n, (long long)k, (long long)batch, mt, p.wk, p.ks, p.smem, p.grid);
     if (encode(mt, 1) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     args.ks = p.ks;
     args.warp_bytes = p.warp_bytes;
