@@ -316,17 +316,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t sbo
   d |= (uint64_t)2u << 61;                                  // SWIZZLE_128B
   return d;
 }
-// K-major operand in the 64-byte swizzle (8-row atoms of 64-byte rows; the
-// stride byte offset is the distance between atoms).
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t smem_addr, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1u << 16;                                  // leading byte offset (unused)
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;        // stride byte offset
-  d |= (uint64_t)1u << 46;                                  // version
-  d |= (uint64_t)4u << 61;                                  // SWIZZLE_64B
-  return d;
-}
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
 // K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {

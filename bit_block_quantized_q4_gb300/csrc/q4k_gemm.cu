@@ -3,7 +3,8 @@
 // prefill throughput is a reported metric in "PRD: Performant Concurrent
 // Distributed GGUF Runtime", DGR-001).
 //
-// One CTA computes a 512-token x BN-weight-row output tile, so every weight is
+// One CTA computes a 512-token x BN-weight-row output tile (BN = 128, or 112
+// when that spreads a narrow projection over more SMs), so every weight is
 // dequantized exactly once per 512 tokens.  Warp roles:
 //   warp 0      TMA producer of X k-blocks (512 x 64 bf16, 128-byte swizzle),
 //               optionally multicast across a cluster of CTAs that share X
@@ -30,23 +31,20 @@ namespace q4k {
 
 namespace {
 
-#ifndef Q4K_GEMM_XK  // k width of an X stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
-#define Q4K_GEMM_XK 64
-#endif
-constexpr int kSub = 4;                 // 128-token sub-tiles per CTA
-constexpr int kTokens = 128 * kSub;     // tokens per CTA
-constexpr int kBK = 64;                 // k per weight block = one 128-byte swizzle panel
-constexpr int kXK = Q4K_GEMM_XK;        // k per X stage (one swizzle panel of X)
-constexpr int kXPanels = kBK / kXK;     // X stages per weight block
-constexpr int kXSubBytes = 128 * kXK * 2;        // one 128-token sub-tile of an X stage
-constexpr int kXStageBytes = kSub * kXSubBytes;  // 32768 or 65536
-constexpr int kXStages = 131072 / kXStageBytes;  // 128 KB of X in flight either way
-constexpr int kBStages = 3;
-constexpr int kRawStages = 2;
-constexpr int kThreads = 256;
+constexpr int kBK = 64;  // k per block = one 128-byte swizzle panel (X stage and weight stage)
 
-template <int BN>
+// Shared-memory plan of one CTA: SUB 128-token sub-tiles of X per stage, BN
+// weight rows (dequantized bf16 stage + raw Q4_K stage), barriers, TMEM slot.
+template <int BN, int SUB>
 struct GemmSmem {
+  static constexpr int kTokens = 128 * SUB;
+  static constexpr int kDqWarps = (BN > 128 ? BN : 128) / 32;  // one weight row per thread
+  static constexpr int kThreads = 128 + 32 * kDqWarps;
+  static constexpr int kXSubBytes = 128 * kBK * 2;
+  static constexpr int kXStageBytes = SUB * kXSubBytes;
+  static constexpr int kXStages = 2;
+  static constexpr int kBStages = SUB == 4 ? 3 : 2;
+  static constexpr int kRawStages = 2;
   static constexpr int kBStageBytes = BN * kBK * 2;
   static constexpr int kRawBytes = BN * kBlockBytes;
   static constexpr int kX = 0;
@@ -112,18 +110,19 @@ __device__ __forceinline__ void store_y16(const GemmArgs &a, int m, int n, const
 }
 
 // A cluster is CS x KS CTAs, rank = n + CS z.  The CS CTAs with the same z
-// take consecutive 128-row weight tiles over the same K range and share X
-// (TMA multicast).  The KS CTAs with the same n split K: CTA z contracts
+// take consecutive BN-row weight tiles over the same K range and share X (TMA
+// multicast).  The KS CTAs with the same n split K: CTA z contracts
 // super-blocks [z nsb / KS, (z+1) nsb / KS) into its own TMEM, and the partial
-// tiles meet through distributed shared memory in the z = 0 CTA, which adds
-// them in z order and stores Y.
-template <int BN, int CS, int KS>
-__global__ void __launch_bounds__(kThreads, 1)
+// tiles are summed through distributed shared memory (below).
+template <int BN, int SUB, int CS, int KS>
+__global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmArgs a) {
-  static_assert(2 * BN * 128 * 4 <= kXStages * kXStageBytes, "split-K exchange buffer");
-  static_assert(BN % 16 == 0, "16-column epilogue chunks");
-  using L = GemmSmem<BN>;
+  using L = GemmSmem<BN, SUB>;
+  static_assert(BN % 16 == 0 && BN <= 256 && SUB * BN <= 512, "MMA shape / TMEM columns");
+  static_assert(BN / 16 * 128 * 64 <= L::kBars, "split-K exchange buffer");
+  constexpr int kXStages = L::kXStages, kBStages = L::kBStages, kRawStages = L::kRawStages;
+  constexpr int kDqWarps = L::kDqWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * kTokens;
+  const int m0 = blockIdx.y * L::kTokens;
   const uint32_t crank = (CS * KS > 1) ? cluster_ctarank() : 0u;
   const uint32_t rank = crank % CS;   // position among the CTAs sharing X
   const uint32_t krank = crank / CS;  // K range of this CTA
@@ -161,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&xempty[s], CS);
     }
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(&bfull[s], 4);
+      mbar_init(&bfull[s], kDqWarps);
       mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(&rfull[s], 1);
-      mbar_init(&rempty[s], 4);
+      mbar_init(&rempty[s], kDqWarps);
     }
     mbar_init(accfull, 1);
     fence_mbar_init();
@@ -186,18 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
     if (lane == 0) {
-      for (int xp = 0; xp < nkb * kXPanels; ++xp) {
-        const int s = xp % kXStages;
-        const uint32_t ph = (uint32_t)((xp / kXStages) & 1);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kXStages;
+        const uint32_t ph = (uint32_t)((kb / kXStages) & 1);
         if (!mbar_wait(&xempty[s], ph ^ 1u, a.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(&xfull[s], kXStageBytes);
-        uint8_t *dst = smem + L::kX + s * kXStageBytes;
-        const int kx = kb_lo * kBK + xp * kXK;
-        for (int sub = (int)rank; sub < kSub; sub += CS) {
+        mbar_arrive_expect_tx(&xfull[s], L::kXStageBytes);
+        uint8_t *dst = smem + L::kX + s * L::kXStageBytes;
+        const int kx = (kb_lo + kb) * kBK;
+        for (int sub = (int)rank; sub < SUB; sub += CS) {
           if (CS > 1)
-            tma_load_2d_mc(dst + sub * kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub, kMask);
+            tma_load_2d_mc(dst + sub * L::kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub, kMask);
           else
-            tma_load_2d(dst + sub * kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub);
+            tma_load_2d(dst + sub * L::kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub);
         }
       }
     }
@@ -207,31 +206,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       const uint32_t xbase = smem_u32(smem + L::kX);
       const uint32_t bbase = smem_u32(smem + L::kB);
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int bs = kb % kBStages;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int xs = kb % kXStages, bs = kb % kBStages;
+        if (!mbar_wait(&xfull[xs], (uint32_t)((kb / kXStages) & 1), a.err)) { ok = false; break; }
         if (!mbar_wait(&bfull[bs], (uint32_t)((kb / kBStages) & 1), a.err)) { ok = false; break; }
-        for (int h = 0; h < kXPanels; ++h) {
-          const int xp = kb * kXPanels + h, xs = xp % kXStages;
-          if (!mbar_wait(&xfull[xs], (uint32_t)((xp / kXStages) & 1), a.err)) { ok = false; break; }
-          tc_fence_after();
+        tc_fence_after();
 #pragma unroll
-          for (int k16 = 0; k16 < kXK / 16; ++k16) {
-            const uint64_t bdesc =
-                sdesc_sw128(bbase + bs * L::kBStageBytes + (h * (kXK / 16) + k16) * 32, 1024);
+        for (int k16 = 0; k16 < kBK / 16; ++k16) {
+          const uint64_t bdesc = sdesc_sw128(bbase + bs * L::kBStageBytes + k16 * 32, 1024);
 #pragma unroll
-            for (int sub = 0; sub < kSub; ++sub) {
-              const uint32_t xa = xbase + xs * kXStageBytes + sub * kXSubBytes + k16 * 32;
-              const uint64_t adesc = kXK == 64 ? sdesc_sw128(xa, 1024) : sdesc_sw64(xa, 512);
-              tc_mma_f16(tmem + sub * BN, adesc, bdesc, idesc, (kb | h | k16) != 0);
-            }
+          for (int sub = 0; sub < SUB; ++sub) {
+            const uint64_t adesc =
+                sdesc_sw128(xbase + xs * L::kXStageBytes + sub * L::kXSubBytes + k16 * 32, 1024);
+            tc_mma_f16(tmem + sub * BN, adesc, bdesc, idesc, (kb | k16) != 0);
           }
-          if (CS > 1)
-            tc_commit_mc(&xempty[xs], kMask);
-          else
-            tc_commit(&xempty[xs]);
         }
-        if (!ok) break;
         tc_commit(&bempty[bs]);
+        if (CS > 1)
+          tc_commit_mc(&xempty[xs], kMask);
+        else
+          tc_commit(&xempty[xs]);
       }
       tc_commit(accfull);
     }
@@ -249,12 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ---------------------------------------------------------- dequantize
     const int row = threadIdx.x - 128;  // weight row within the tile
+    const bool live = row < BN;         // threads past BN only keep the barrier protocol
     const int r8 = row & 7;
-    uint8_t *brow0 = smem + L::kB + (row >> 3) * 1024 + r8 * 128;
+    uint8_t *brow0 = smem + L::kB + (live ? row >> 3 : 0) * 1024 + r8 * 128;
     for (int sb = 0; sb < nsb && ok; ++sb) {
       const int rs = sb % kRawStages;
       if (!mbar_wait(&rfull[rs], (uint32_t)((sb / kRawStages) & 1), a.err)) { ok = false; break; }
-      const uint8_t *raw = smem + L::kRaw + rs * L::kRawBytes + row * kBlockBytes;
+      const uint8_t *raw = smem + L::kRaw + rs * L::kRawBytes + (live ? row : 0) * kBlockBytes;
       const uint4 h = *reinterpret_cast<const uint4 *>(raw);
       uint32_t sc_lo, sc_hi, m_lo, m_hi;
       scales_all(h.y, h.z, h.w, &sc_lo, &sc_hi, &m_lo, &m_hi);
@@ -300,82 +295,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.y = pack_bf16(fmaf(ds, q[2], -dm), fmaf(ds, q[3], -dm));
           o.z = pack_bf16(fmaf(ds, q[4], -dm), fmaf(ds, q[5], -dm));
           o.w = pack_bf16(fmaf(ds, q[6], -dm), fmaf(ds, q[7], -dm));
-          *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
+          if (live) *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bfull[bs]);
       }
     }
-    // ---------------------------------------------------------- epilogue
     acc_ready = ok && mbar_wait(accfull, 0u, a.err);
-    if (KS == 1 && acc_ready) {
-      tc_fence_after();
-      const int q = warp & 3;  // TMEM lane quarter of this warp
-      for (int sub = 0; sub < kSub; ++sub) {
-        const int m = m0 + 128 * sub + 32 * q + lane;
+  }
+
+  // ------------------------------------------------------------ epilogue
+  // Dequant warp w drains TMEM lane quarter w % 4 (tokens 32 (w % 4) ..) and
+  // columns [128 h, 128 h + 128) with h = (w - 4) / 4, in 16-column chunks.
+  const bool epi = warp >= 4;
+  const int q = warp & 3;
+  const int row = 32 * q + lane;  // token within a sub-tile
+  const int c_lo = epi ? ((warp - 4) >> 2) * 8 : 0;     // first 16-column chunk
+  const int c_hi = epi ? min(BN / 16, c_lo + 8) : 0;    // end of this warp's chunks
+  if (epi && acc_ready) tc_fence_after();
+  if constexpr (KS == 1) {
+    if (epi && acc_ready) {
+      for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c = c_lo; c < c_hi; ++c) {
           uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + c0), r);
+          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
           tmem_ld_wait();
           float v[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-          store_y16(a, m, n0 + c0, v);
+          store_y16(a, m0 + 128 * sub + row, n0 + 16 * c, v);
         }
       }
     }
-  }
-
-  if constexpr (KS > 1) {
-    // ---------------------------------------------------------- split-K sum
-    // Two rounds of two 128-token sub-tiles.  Every CTA copies its partials
-    // from TMEM into its own X stage area (idle now); after a cluster barrier
-    // each CTA takes the 16-column chunks i with i % KS == its K rank, adds the
-    // KS partials of those in K-rank order (its own from TMEM, the others from
-    // the peers' shared memory) and stores Y; a second barrier frees the
-    // buffers.  Every thread of every CTA passes both barriers of each round,
-    // whatever happened before.  Layout: 16 columns of a row are four 16-byte
-    // units, unit u stored at slot u ^ ((row >> 1) & 3) so that eight
-    // consecutive rows hit eight different bank groups.
-    float4 *buf = reinterpret_cast<float4 *>(smem + L::kX);  // [s2][c0/16][row][4]
-    const bool epi = warp >= 4;
-    const int q = warp & 3;
-    const int row = 32 * q + lane;
+  } else {
+    // Split-K sum, one round per 128-token sub-tile.  Every CTA copies its
+    // partials of the chunks it does not own from TMEM into its own shared
+    // memory (idle now: all copies and MMAs are done); after a cluster barrier
+    // each CTA takes the chunks c with c % KS == its K rank, adds the KS
+    // partials in K-rank order (its own from TMEM, the others from the peers'
+    // shared memory) and stores Y; a second barrier frees the buffers.  Every
+    // thread of every CTA passes both barriers of each round, whatever happened
+    // before.  Layout: 16 columns of a row are four 16-byte units, unit u stored
+    // at slot u ^ ((row >> 1) & 3) so that eight consecutive rows hit eight
+    // different bank groups.
+    float4 *buf = reinterpret_cast<float4 *>(smem);  // [chunk][row][4]
     const int swz = (row >> 1) & 3;
-    constexpr int kChunks = 2 * (BN / 16);  // 16-column chunks per round
-    auto unit = [&](int idx, int u) { return (idx * 128 + row) * 4 + (u ^ swz); };
-    if (epi && acc_ready) tc_fence_after();
-    for (int p = 0; p < kSub / 2; ++p) {
+    auto unit = [&](int c, int u) { return (c * 128 + row) * 4 + (u ^ swz); };
+    for (int sub = 0; sub < SUB; ++sub) {
       if (epi && acc_ready) {
 #pragma unroll 1
-        for (int idx = 0; idx < kChunks; ++idx) {
-          if (idx % KS == (int)krank) continue;  // kept in TMEM, read there below
-          const int s2 = idx / (BN / 16), c0 = (idx % (BN / 16)) * 16;
+        for (int c = c_lo; c < c_hi; ++c) {
+          if (c % KS == (int)krank) continue;  // kept in TMEM, read there below
           uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((2 * p + s2) * BN + c0), r);
+          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            buf[unit(idx, u)] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                            __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+            buf[unit(c, u)] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                          __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
         }
       }
       cluster_sync();
       if (epi && acc_ready) {
 #pragma unroll 1
-        for (int idx = (int)krank; idx < kChunks; idx += KS) {
-          const int s2 = idx / (BN / 16), c0 = (idx % (BN / 16)) * 16;
+        for (int c = c_lo; c < c_hi; ++c) {
+          if (c % KS != (int)krank) continue;
           float4 pv[KS][4];
 #pragma unroll
           for (int z = 0; z < KS; ++z)
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               if (z != (int)krank)
-                pv[z][u] = ld_peer_v4(peer_smem(smem_u32(&buf[unit(idx, u)]), rank + CS * (uint32_t)z));
+                pv[z][u] = ld_peer_v4(peer_smem(smem_u32(&buf[unit(c, u)]), rank + CS * (uint32_t)z));
           uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((2 * p + s2) * BN + c0), r);
+          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
           tmem_ld_wait();
           float v[16];
 #pragma unroll
@@ -393,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[4 * u + 3] = z ? v[4 * u + 3] + t3 : t3;
             }
           }
-          store_y16(a, m0 + 128 * (2 * p + s2) + row, n0 + c0, v);
+          store_y16(a, m0 + 128 * sub + row, n0 + 16 * c, v);
         }
       }
       cluster_sync();
@@ -409,28 +404,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kBN = 128;
-
 std::once_flag g_gemm_attr;
 
-template <int CS, int KS>
+template <int BN, int SUB, int CS, int KS>
 void gemm_allow() {
-  cudaFuncSetAttribute(gemm_kernel<kBN, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<kBN>::kAlloc);
-  if (CS * KS > 8)
-    cudaFuncSetAttribute(gemm_kernel<kBN, CS, KS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(gemm_kernel<BN, SUB, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       GemmSmem<BN, SUB>::kAlloc);
+}
+
+template <int BN, int SUB>
+void gemm_allow_all() {
+  gemm_allow<BN, SUB, 1, 1>();
+  gemm_allow<BN, SUB, 2, 1>();
+  gemm_allow<BN, SUB, 1, 2>();
+  gemm_allow<BN, SUB, 1, 3>();
+  gemm_allow<BN, SUB, 1, 4>();
+  gemm_allow<BN, SUB, 2, 2>();
+  gemm_allow<BN, SUB, 2, 3>();
+  gemm_allow<BN, SUB, 2, 4>();
 }
 
 void gemm_attributes() {
-  gemm_allow<1, 1>();
-  gemm_allow<2, 1>();
-  gemm_allow<4, 1>();
-  gemm_allow<1, 2>();
-  gemm_allow<1, 3>();
-  gemm_allow<1, 4>();
-  gemm_allow<2, 2>();
-  gemm_allow<2, 3>();
-  gemm_allow<2, 4>();
+  gemm_allow_all<128, 4>();
+  gemm_allow_all<112, 4>();
+}
+
+template <int BN, int SUB>
+cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &xmap,
+                    const CUtensorMap &wmap, const GemmArgs &args) {
+  cfg.dynamicSmemBytes = GemmSmem<BN, SUB>::kAlloc;
+  cfg.blockDim = dim3((unsigned)GemmSmem<BN, SUB>::kThreads, 1, 1);
+  auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, xmap, wmap, args); };
+  if (cs == 2) {
+    if (ks == 4) return go(gemm_kernel<BN, SUB, 2, 4>);
+    if (ks == 3) return go(gemm_kernel<BN, SUB, 2, 3>);
+    if (ks == 2) return go(gemm_kernel<BN, SUB, 2, 2>);
+    return go(gemm_kernel<BN, SUB, 2, 1>);
+  }
+  if (ks == 4) return go(gemm_kernel<BN, SUB, 1, 4>);
+  if (ks == 3) return go(gemm_kernel<BN, SUB, 1, 3>);
+  if (ks == 2) return go(gemm_kernel<BN, SUB, 1, 2>);
+  return go(gemm_kernel<BN, SUB, 1, 1>);
 }
 
 }  // namespace
@@ -441,6 +455,9 @@ void gemm_attributes() {
 #ifndef Q4K_GEMM_SPLITK  // split K across a cluster when the output tiles cannot fill the SMs
 #define Q4K_GEMM_SPLITK 1
 #endif
+#ifndef Q4K_GEMM_SHAPE  // 0: choose the tile per call; 128 or 112: force that weight-tile width
+#define Q4K_GEMM_SHAPE 0
+#endif
 
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream) {
@@ -450,19 +467,9 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   {
     const uint64_t dims[2] = {(uint64_t)k, (uint64_t)m};
     const uint64_t strides[1] = {(uint64_t)ldx * 2};
-    const uint32_t box[2] = {(uint32_t)kXK, 128u};
+    const uint32_t box[2] = {(uint32_t)kBK, 128u};
     if (encode_tiled(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims,
-                     strides, box,
-                     kXK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
-    const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
-    const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)kBN};
-    if (encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
-                     box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   GemmArgs args;
@@ -473,23 +480,53 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   args.k = (int)k;
   args.err = device_error_word();
 
-  int ntiles = (int)((n + kBN - 1) / kBN);
-  const int mtiles = (int)((m + kTokens - 1) / kTokens);
-  // Too few output tiles to fill the SMs (a wide-K projection such as the
-  // 17408 -> 5120 down projection): split K across a cluster instead.
-  int ks = 1;
-  if (Q4K_GEMM_SPLITK) {
-    ks = std::max(1, std::min(4, device_facts()->sm_count / std::max(1, ntiles * mtiles)));
-    while (ks > 1 && nsb < 2 * ks) --ks;
+  // Tile shape, K split and X sharing.  Candidates: 512 tokens x 128 or 112
+  // weight rows (112 spreads a narrow projection over more SMs).  K is split
+  // across a cluster when the output tiles cannot fill the SMs.  Estimated time =
+  // waves x k-blocks per CTA x the larger of the X feed (SUB x 16 KB at ~64 GB/s
+  // per SM, measured) and the MMA time (~12.7 TFLOP/s per SM).  A 256 x 256 tile
+  // (half the X bytes per flop, weights dequantized once per 256 tokens) was
+  // measured slower on both 512-token projections and is not offered.
+  const int sms = device_facts()->sm_count;
+  struct Shape { int bn, sub; };
+  const Shape shapes[2] = {{128, 4}, {112, 4}};
+  int bn = 128, cs = 1, ks = 1, ntiles = 0, mtiles = 0;
+  double best = -1;
+  for (const Shape &c : shapes) {
+    if (Q4K_GEMM_SHAPE && c.bn != Q4K_GEMM_SHAPE) continue;
+    const int mt = (int)((m + 128 * c.sub - 1) / (128 * c.sub));
+    int nt = (int)((n + c.bn - 1) / c.bn);
+    int kk = 1;
+    if (Q4K_GEMM_SPLITK) {
+      kk = std::max(1, std::min(4, sms / std::max(1, nt * mt)));
+      while (kk > 1 && nsb < 2 * kk) --kk;
+    }
+    int cc = Q4K_GEMM_CLUSTER > 1 ? 2 : 1;
+    while (cc > 1 && (nt < 2 * cc || cc * kk > 8)) cc >>= 1;
+    nt = (nt + cc - 1) / cc * cc;
+    const long ctas = (long)nt * mt * kk;
+    const double t_kb = std::max(c.sub * 16384.0 / 64.0, 2.0 * 128 * c.sub * c.bn * kBK / 12.7e3);
+    const double est = (double)((ctas + sms - 1) / sms) * ((nsb + kk - 1) / kk) * 4 * t_kb;
+    if (best < 0 || est < best) {
+      best = est;
+      bn = c.bn;
+      cs = cc;
+      ks = kk;
+      ntiles = nt;
+      mtiles = mt;
+    }
   }
-  int cs = Q4K_GEMM_CLUSTER;
-  while (cs > 1 && (ntiles < 2 * cs || cs * ks > 8)) cs >>= 1;
-  ntiles = (ntiles + cs - 1) / cs * cs;
+  {
+    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
+    const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
+    const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)bn};
+    if (encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, (unsigned)ks);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = GemmSmem<kBN>::kAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -498,18 +535,8 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, xmap, wmap, args); };
-  if (cs == 2) {
-    if (ks == 4) return go(gemm_kernel<kBN, 2, 4>);
-    if (ks == 3) return go(gemm_kernel<kBN, 2, 3>);
-    if (ks == 2) return go(gemm_kernel<kBN, 2, 2>);
-    return go(gemm_kernel<kBN, 2, 1>);
-  }
-  if (cs == 4) return go(gemm_kernel<kBN, 4, 1>);
-  if (ks == 4) return go(gemm_kernel<kBN, 1, 4>);
-  if (ks == 3) return go(gemm_kernel<kBN, 1, 3>);
-  if (ks == 2) return go(gemm_kernel<kBN, 1, 2>);
-  return go(gemm_kernel<kBN, 1, 1>);
+  if (bn == 112) return gemm_go<112, 4>(cfg, cs, ks, xmap, wmap, args);
+  return gemm_go<128, 4>(cfg, cs, ks, xmap, wmap, args);
 }
 
 }  // namespace q4k
