@@ -17,6 +17,7 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--skip-e
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import statistics
@@ -40,6 +41,16 @@ N_LAYERS = 64
 SEED_C1 = 1001
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+@contextlib.contextmanager
+def nvtx(name):
+    """An NVTX range around one configuration (visible to profilers)."""
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 def q4k_bytes(n, k):
@@ -489,7 +500,8 @@ def main():
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    head = bench_decode(q4k, layers, 1, args.steps, args.warmup, dev, stream, sampler)
+    with nvtx("decode_b1 pass (timed)"):
+        head = bench_decode(q4k, layers, 1, args.steps, args.warmup, dev, stream, sampler)
     ms = head["ms_per_step"]
     if world > 1:
         import torch.distributed as dist
@@ -503,35 +515,41 @@ def main():
     total_value = achieved * world
     launches = head["launches_per_step"]
 
-    e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
+    with nvtx("decode_b1 pass e2e"):
+        e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
     e2e["value"] = round(e2e["value"] * world, 2)
 
     cpu = cpu_baseline(layers) if rank == 0 else None
     extra = {}
-    r = bench_decode(q4k, layers, 1, max(5, args.steps // 2), 3, dev, stream, overlap=False)
+    with nvtx("decode_b1 pass, plain launches"):
+        r = bench_decode(q4k, layers, 1, max(5, args.steps // 2), 3, dev, stream, overlap=False)
     extra["decode_b1_no_overlap"] = {"gbs": round(r["gbs"], 1),
                                      "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
                                      "ms_per_step": round(r["ms_per_step"], 4)}
     if not args.skip_extra:
         for b in (4, 16):
-            r = bench_decode(q4k, layers, b, max(5, args.steps // 2), 3, dev, stream)
+            with nvtx(f"decode_b{b} pass"):
+                r = bench_decode(q4k, layers, b, max(5, args.steps // 2), 3, dev, stream)
             extra[f"decode_b{b}"] = {"gbs": round(r["gbs"], 1),
                                      "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
                                      "ms_per_step": round(r["ms_per_step"], 4)}
         del layers
         torch.cuda.empty_cache()
-        r = bench_c0_pool(q4k, max(5, args.steps // 2), 3, dev, stream)
+        with nvtx("gemv 4096x4096 pool"):
+            r = bench_c0_pool(q4k, max(5, args.steps // 2), 3, dev, stream)
         extra["gemv_4096_b1_pool"] = {"gbs": round(r["gbs"], 1),
                                       "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
                                       "us_per_gemv": round(r["us_per_gemv"], 3), "pool": r["pool"]}
         torch.cuda.empty_cache()
-        pf = bench_prefill(q4k, dev, stream)
+        with nvtx("prefill 512"):
+            pf = bench_prefill(q4k, dev, stream)
         for nm, v in pf.items():
             v["frac_of_measured_bf16"] = round(v["tflops"] / pk["bf16_tflops"], 4)
             v["frac_of_sustained_bf16"] = round(v["tflops"] / pk["bf16_tflops_sustained"], 4)
         extra["prefill_512"] = pf
         torch.cuda.empty_cache()
-        extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
+        with nvtx("moe 235b t16"):
+            extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
     clocks = sampler.summary()
 
     if rank == 0:

@@ -25,7 +25,7 @@ STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN"
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex", "q4k_gemm",
            "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_moe_gemv_noalloc",
-           "q4k_get_device_error")
+           "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
                                            I64, P]
         L.q4k_get_device_error.restype = ctypes.c_int
         L.q4k_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        L.q4k_selftest_wait_timeout.restype = ctypes.c_int
+        L.q4k_selftest_wait_timeout.argtypes = [P]
         _lib = L
         return L
 
@@ -184,3 +186,8 @@ def q4k_get_device_error(stream=None) -> int:
     if st not in (0, 7):
         raise Q4KError(st, "q4k_get_device_error")
     return int(bits.value)
+
+
+def q4k_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self test (a wait nothing completes; ~2 s)."""
+    _check(lib().q4k_selftest_wait_timeout(_stream(stream)), "q4k_selftest_wait_timeout")

@@ -98,6 +98,21 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank,
                   swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+namespace {
+// One warp waits, through the same bounded wait every kernel uses, on an
+// mbarrier that no thread ever arrives at.  After the wall-clock limit the wait
+// gives up, sets the timeout bit of the device error word and the kernel ends.
+__global__ void selftest_wait_timeout_kernel(unsigned *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  (void)mbar_wait(&bar, 0, err);
+}
+}  // namespace
+
 }  // namespace q4k
 
 using namespace q4k;
@@ -219,6 +234,13 @@ int q4k_moe_gemv_noalloc(const void *w_gate, const void *w_up, const void *w_dow
   return map_launch(launch_moe_scratch(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn,
                                        x, n_tokens, ldx, ids, wts, top_k, y, ldy,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_selftest_wait_timeout(void *stream) {
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(device_error_word());
+  return map_launch(cudaGetLastError());
 }
 
 int q4k_get_device_error(void *stream, uint32_t *bits) {

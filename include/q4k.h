@@ -215,6 +215,15 @@ int q4k_moe_gemv_noalloc(const void *w_gate, const void *w_up, const void *w_dow
  */
 int q4k_get_device_error(void *stream, uint32_t *bits);
 
+/* Failure-path self test (no counterpart on the pages).  Launches one warp that
+ * waits, through the same bounded wait every kernel uses, on an mbarrier that
+ * nothing ever arrives at.  After the wait's wall-clock limit (about 2 s) it
+ * gives up, sets Q4K_DEVERR_TIMEOUT in the device error word and the kernel
+ * ends normally: the GPU context stays usable.  Asynchronous on `stream`; read
+ * the result with q4k_get_device_error.  Returns Q4K_ERR_DEVICE off sm_103 and
+ * Q4K_ERR_CUDA if the launch fails. */
+int q4k_selftest_wait_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif
