@@ -274,6 +274,7 @@ __device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float *xsum
 template <int MT>
 __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], bool ok,
                                           float *red, int row0, const GemvArgs &a) {
+  constexpr int kRows = MT * kRowsPerTile;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -283,16 +284,16 @@ __device__ __forceinline__ void b1_finish(const float2 (&yacc)[MT], bool ok,
       float v = r ? yacc[mt].y : yacc[mt].x;
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (t == 0) red[warp * (MT * kRowsPerTile) + mt * kRowsPerTile + g + 8 * r] = v;
+      if (t == 0) red[warp * kRows + mt * kRowsPerTile + g + 8 * r] = v;
     }
   }
   __syncwarp();
-  if (!ok && lane == 0) red[warp * (MT * kRowsPerTile)] = __int_as_float(0x7fc00000);
+  if (!ok && lane == 0) red[warp * kRows] = __int_as_float(0x7fc00000);
   __syncthreads();
-  if (threadIdx.x < MT * kRowsPerTile) {
+  if (threadIdx.x < kRows) {
     float sum = 0.f;
-    for (int w = 0; w < nwarps; ++w) sum += red[w * (MT * kRowsPerTile) + threadIdx.x];
-    const int row = row0 + threadIdx.x;
+    for (int w = 0; w < nwarps; ++w) sum += red[w * kRows + threadIdx.x];
+    const int row = row0 + (int)threadIdx.x;
     if (row < a.n) a.y[row] = sum;
   }
 }
@@ -754,6 +755,49 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
 
 std::once_flag g_attr_once;
 
+// Batch-1 plan.  A row tile's K is split over the wk warps of its CTA.  Every
+// CTA must be resident at once; among those plans take the smallest load of
+// the busiest SM: ceil(CTAs / SMs) x warps per CTA x super-blocks per warp x
+// rows per warp x the per-row cost of the tile height (an MT = 2 warp spends
+// 0.72 of an MT = 1 warp's instructions per row: 269 vs 373 per 16-row tile,
+// measured), plus a penalty for fewer than 8 resident warps per SM (too little
+// to hide latency).  (Splitting a tile's K further over a cluster of CTAs, with
+// the partials summed through distributed shared memory, balanced the SMs
+// better on paper but measured slower at every cluster size.)
+template <typename K>
+Plan plan_b1(K kernel, int mt, int s, int stages, int n, int nsb, const DeviceFacts *f) {
+  Plan best;
+  const int tile_rows = mt * kRowsPerTile;
+  const int tiles = (n + tile_rows - 1) / tile_rows;
+  for (int wk = 1; wk <= 8; ++wk) {
+    int ks = (nsb + wk - 1) / wk;
+    ks = (ks + s - 1) / s * s;
+    if ((nsb + ks - 1) / ks != wk) continue;  // every warp gets super-blocks
+    if (ks < 2 * s && nsb >= 2 * s) continue;
+    const int wb = warp_bytes_b1(mt, s, stages, ks);
+    const int smem = wk * wb + wk * tile_rows * 4;
+    if (smem > f->max_smem_optin) continue;
+    const int occ = occupancy(kernel, wk * 32, smem);
+    if (occ <= 0) continue;
+    if (tiles > occ * f->sm_count) continue;  // one wave
+    const long per_sm = (tiles + f->sm_count - 1) / f->sm_count;
+    const long warps_sm = per_sm * wk;
+    double load = (double)per_sm * wk * ks * mt * (mt == 2 ? 0.72 : 1.0);
+    if (warps_sm < 8) load *= 1.0 + 0.08 * (8 - warps_sm);
+    if (-load > best.score) {
+      best.score = -load;
+      best.mt = mt;
+      best.s = s;
+      best.wk = wk;
+      best.ks = ks;
+      best.warp_bytes = wb;
+      best.smem = smem;
+      best.grid = tiles;
+    }
+  }
+  return best;
+}
+
 template <typename K>
 void allow_smem(K kernel, const DeviceFacts *f) {
   cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f->max_smem_optin);
@@ -840,7 +884,7 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
       if (Q4K_GEMV_FORCE_S && c[1] != Q4K_GEMV_FORCE_S) continue;
       const int stages = c[1] == 1 ? B1Stages<1>::value : c[1] == 2 ? B1Stages<2>::value
                                                                      : B1Stages<4>::value;
-      const Plan q = plan_for(b1_select(c[0], c[1]), true, c[0], c[1], stages, (int)n, nsb, 1, f);
+      const Plan q = plan_b1(b1_select(c[0], c[1]), c[0], c[1], stages, (int)n, nsb, f);
       if (q.grid && q.score > p.score) p = q;
     }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
