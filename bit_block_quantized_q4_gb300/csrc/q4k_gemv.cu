@@ -673,6 +673,9 @@ constexpr int kStages = Q4K_GEMV_STAGES;  // batch 2..16 (one super-block per st
 #ifndef Q4K_GEMV_INFLIGHT_KB  // planner: weight bytes in flight per SM worth having, at most
 #define Q4K_GEMV_INFLIGHT_KB 96
 #endif
+#ifndef Q4K_GEMV_BN_MT2_COST  // batch 2..16: per-row cost of an MT = 2 warp relative to MT = 1
+#define Q4K_GEMV_BN_MT2_COST 0.8
+#endif
 #ifndef Q4K_GEMV_LOG_PLAN  // 1: print each batch-1 plan to stderr (tuning aid)
 #define Q4K_GEMV_LOG_PLAN 0
 #endif
@@ -764,6 +767,40 @@ std::once_flag g_attr_once;
 // to hide latency).  (Splitting a tile's K further over a cluster of CTAs, with
 // the partials summed through distributed shared memory, balanced the SMs
 // better on paper but measured slower at every cluster size.)
+// Batch 2..16: the same load objective; an MT = 2 warp shares its x
+// fragments between its two row tiles (taken as 0.8 of MT = 1's cost per row).
+template <typename K>
+Plan plan_bn(K kernel, int mt, int stages, int n, int nsb, int cols, const DeviceFacts *f) {
+  Plan best;
+  const int tile_rows = mt * kRowsPerTile;
+  const int tiles = (n + tile_rows - 1) / tile_rows;
+  for (int wk = 1; wk <= 8; ++wk) {
+    const int ks = (nsb + wk - 1) / wk;
+    if ((nsb + ks - 1) / ks != wk) continue;  // every warp gets super-blocks
+    const int wb = warp_bytes_bn(mt);
+    const int smem = wk * wb + wk * tile_rows * cols * 4;
+    if (smem > f->max_smem_optin) continue;
+    const int occ = occupancy(kernel, wk * 32, smem);
+    if (occ <= 0) continue;
+    if (tiles > occ * f->sm_count) continue;  // one wave
+    const long per_sm = (tiles + f->sm_count - 1) / f->sm_count;
+    const long warps_sm = per_sm * wk;
+    double load = (double)per_sm * wk * ks * mt * (mt == 2 ? Q4K_GEMV_BN_MT2_COST : 1.0);
+    if (warps_sm < 8) load *= 1.0 + 0.08 * (8 - warps_sm);
+    if (-load > best.score) {
+      best.score = -load;
+      best.mt = mt;
+      best.s = 1;
+      best.wk = wk;
+      best.ks = ks;
+      best.warp_bytes = wb;
+      best.smem = smem;
+      best.grid = tiles;
+    }
+  }
+  return best;
+}
+
 template <typename K>
 Plan plan_b1(K kernel, int mt, int s, int stages, int n, int nsb, const DeviceFacts *f) {
   Plan best;
@@ -908,7 +945,11 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
     Plan p;
     for (int mt = 1; mt <= 2; ++mt) {  // the tile height is part of the plan, as at batch 1
       if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
-      const Plan q = plan_for(bn_select(mt), false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
+      // Measured on the 64-layer pass: the busiest-SM load objective wins at
+      // 16 columns (B = 16: 1356 -> 1503 GB/s), the older score at 8 (B = 4:
+      // 1951 vs 1543 GB/s).
+      const Plan q = nt == 2 ? plan_bn(bn_select(mt), mt, kStages, (int)n, nsb, nt * 8, f)
+                             : plan_for(bn_select(mt), false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
       if (q.grid && q.score > p.score) p = q;
     }
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
