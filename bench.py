@@ -220,24 +220,36 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
 
 
 def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
-    """Same pass through the public API with host buffers: each step copies every
-    projection's x from pinned host memory and reads every y back."""
-    host_x, host_y, dx, dy = [], [], [], []
-    for i, (_, n, k, _) in enumerate(layers.mats):
+    """Same pass through the public API with host buffers, launched eagerly (no
+    graph): each step copies all projections' x from one pinned host buffer to
+    the device (one copy), runs the 320 calls, and reads all y back (one copy)."""
+    kx = [k for _, _, k, _ in layers.mats]
+    ny = [n for _, n, _, _ in layers.mats]
+    host_x = torch.empty(batch * sum(kx), dtype=torch.bfloat16).pin_memory()
+    host_y = torch.empty(batch * sum(ny), dtype=torch.float32).pin_memory()
+    off = 0
+    for i, k in enumerate(kx):
         x = synth.bf16_normal((batch, k), seed=synth.derive_seed(SEED_C1, "xe", i))
-        host_x.append(x.pin_memory())
-        host_y.append(torch.empty((batch, n), dtype=torch.float32).pin_memory())
-        dx.append(torch.empty((batch, k), dtype=torch.bfloat16, device=dev))
-        dy.append(torch.empty((batch, n), dtype=torch.float32, device=dev))
-    h2d = sum(t.numel() * 2 for t in host_x)
-    d2h = sum(t.numel() * 4 for t in host_y)
+        host_x[off:off + batch * k] = x.reshape(-1)
+        off += batch * k
+    dev_x = torch.empty_like(host_x, device=dev)
+    dev_y = torch.empty_like(host_y, device=dev)
+    xs, ys = [], []
+    ox = oy = 0
+    for k, n in zip(kx, ny):
+        xs.append(dev_x[ox:ox + batch * k].view(batch, k))
+        ys.append(dev_y[oy:oy + batch * n].view(batch, n))
+        ox += batch * k
+        oy += batch * n
+    h2d = host_x.numel() * 2
+    d2h = host_y.numel() * 4
 
     def step():
         with torch.cuda.stream(stream):
-            for (name, n, k, w), hx, hy, x, y in zip(layers.mats, host_x, host_y, dx, dy):
-                x.copy_(hx, non_blocking=True)
+            dev_x.copy_(host_x, non_blocking=True)
+            for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
                 q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
-                hy.copy_(y, non_blocking=True)
+            host_y.copy_(dev_y, non_blocking=True)
 
     for _ in range(max(warmup, 1)):
         step()

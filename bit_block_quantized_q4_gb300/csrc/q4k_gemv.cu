@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "q4k_device.cuh"
@@ -881,6 +882,42 @@ cudaError_t launch(K kernel, const Plan &p, bool pdl, cudaStream_t stream, Args.
   return cudaLaunchKernelEx(&cfg, kernel, kargs...);
 }
 
+namespace {
+// Plans depend only on (device, N, K, batch class); computing one takes a few
+// dozen occupancy queries, so they are kept per process.  Bounded: the cache is
+// cleared when it reaches kMaxPlans entries.
+struct PlanKey {
+  int dev, n, nsb, cls;
+  bool operator==(const PlanKey &o) const {
+    return dev == o.dev && n == o.n && nsb == o.nsb && cls == o.cls;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey &k) const {
+    uint64_t h = (uint64_t)(uint32_t)k.n * 0x9E3779B97F4A7C15ull;
+    h ^= ((uint64_t)(uint32_t)k.nsb << 20) ^ ((uint64_t)k.dev << 52) ^ ((uint64_t)k.cls << 44);
+    return (size_t)(h ^ (h >> 29));
+  }
+};
+constexpr size_t kMaxPlans = 4096;
+std::mutex g_plan_mu;
+std::unordered_map<PlanKey, Plan, PlanKeyHash> g_plans;
+
+template <typename F>
+Plan cached_plan(const PlanKey &key, F compute) {
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) return it->second;
+  }
+  const Plan p = compute();
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  if (g_plans.size() >= kMaxPlans) g_plans.clear();
+  g_plans.emplace(key, p);
+  return p;
+}
+}  // namespace
+
 cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
                         int64_t ldx, float *y, int64_t ldy, bool overlap, cudaStream_t stream) {
   const DeviceFacts *f = device_facts();
@@ -914,16 +951,19 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
   args.err = device_error_word();
 
   if (batch == 1) {
-    Plan p;
-    const int cand[5][2] = {{1, 1}, {1, 2}, {1, 4}, {2, 1}, {2, 2}};
-    for (const auto &c : cand) {
-      if (Q4K_GEMV_FORCE_MT && c[0] != Q4K_GEMV_FORCE_MT) continue;
-      if (Q4K_GEMV_FORCE_S && c[1] != Q4K_GEMV_FORCE_S) continue;
-      const int stages = c[1] == 1 ? B1Stages<1>::value : c[1] == 2 ? B1Stages<2>::value
-                                                                     : B1Stages<4>::value;
-      const Plan q = plan_b1(b1_select(c[0], c[1]), c[0], c[1], stages, (int)n, nsb, f);
-      if (q.grid && q.score > p.score) p = q;
-    }
+    const Plan p = cached_plan(PlanKey{f->device, (int)n, nsb, 1}, [&] {
+      Plan best;
+      const int cand[5][2] = {{1, 1}, {1, 2}, {1, 4}, {2, 1}, {2, 2}};
+      for (const auto &c : cand) {
+        if (Q4K_GEMV_FORCE_MT && c[0] != Q4K_GEMV_FORCE_MT) continue;
+        if (Q4K_GEMV_FORCE_S && c[1] != Q4K_GEMV_FORCE_S) continue;
+        const int stages = c[1] == 1 ? B1Stages<1>::value : c[1] == 2 ? B1Stages<2>::value
+                                                                       : B1Stages<4>::value;
+        const Plan q = plan_b1(b1_select(c[0], c[1]), c[0], c[1], stages, (int)n, nsb, f);
+        if (q.grid && q.score > best.score) best = q;
+      }
+      return best;
+    });
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
     GemvKernel kern = b1_select(p.mt, p.s);
     args.pre = overlap ? Q4K_GEMV_PRE_STAGES : 0;
@@ -942,16 +982,19 @@ cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int6
       return (mt == 2) ? (nt == 1 ? gemv_bn_kernel<2, 1, kStages> : gemv_bn_kernel<2, 2, kStages>)
                        : (nt == 1 ? gemv_bn_kernel<1, 1, kStages> : gemv_bn_kernel<1, 2, kStages>);
     };
-    Plan p;
-    for (int mt = 1; mt <= 2; ++mt) {  // the tile height is part of the plan, as at batch 1
-      if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
-      // Measured on the 64-layer pass: the busiest-SM load objective wins at
-      // 16 columns (B = 16: 1356 -> 1503 GB/s), the older score at 8 (B = 4:
-      // 1951 vs 1543 GB/s).
-      const Plan q = nt == 2 ? plan_bn(bn_select(mt), mt, kStages, (int)n, nsb, nt * 8, f)
-                             : plan_for(bn_select(mt), false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
-      if (q.grid && q.score > p.score) p = q;
-    }
+    const Plan p = cached_plan(PlanKey{f->device, (int)n, nsb, 1 + nt}, [&] {
+      Plan best;
+      for (int mt = 1; mt <= 2; ++mt) {  // the tile height is part of the plan, as at batch 1
+        if (Q4K_GEMV_FORCE_MT && mt != Q4K_GEMV_FORCE_MT) continue;
+        // Measured on the 64-layer pass: the busiest-SM load objective wins at
+        // 16 columns (B = 16: 1356 -> 1503 GB/s), the older score at 8 (B = 4:
+        // 1951 vs 1543 GB/s).
+        const Plan q = nt == 2 ? plan_bn(bn_select(mt), mt, kStages, (int)n, nsb, nt * 8, f)
+                               : plan_for(bn_select(mt), false, mt, 1, kStages, (int)n, nsb, nt * 8, f);
+        if (q.grid && q.score > best.score) best = q;
+      }
+      return best;
+    });
     if (p.grid == 0) return cudaErrorInvalidConfiguration;
     const int mt = p.mt;
     auto kern = bn_select(mt);
