@@ -31,14 +31,19 @@ namespace q4k {
 
 namespace {
 
+#ifndef Q4K_GEMM_DQ_WARPS  // dequantizing warps per CTA: 4 (a thread per weight row) or 8 (two; measured slower)
+#define Q4K_GEMM_DQ_WARPS 4
+#endif
 constexpr int kBK = 64;  // k per block = one 128-byte swizzle panel (X stage and weight stage)
 
 // Shared-memory plan of one CTA: SUB 128-token sub-tiles of X per stage, BN
 // weight rows (dequantized bf16 stage + raw Q4_K stage), barriers, TMEM slot.
-template <int BN, int SUB>
+template <int BN, int SUB, int DQ>
 struct GemmSmem {
   static constexpr int kTokens = 128 * SUB;
-  static constexpr int kDqWarps = (BN > 128 ? BN : 128) / 32;  // one weight row per thread
+  static constexpr int kDqWarps = DQ;                      // dequantizing warps
+  static constexpr int kRowSpan = BN > 128 ? BN : 128;     // weight rows one pass of them covers
+  static constexpr int kPerRow = 32 * DQ / kRowSpan;       // threads per weight row (1 or 2)
   static constexpr int kThreads = 128 + 32 * kDqWarps;
   static constexpr int kXSubBytes = 128 * kBK * 2;
   static constexpr int kXStageBytes = SUB * kXSubBytes;
@@ -98,11 +103,12 @@ __device__ __forceinline__ void store_y16(const GemmArgs &a, int m, int n, const
 // multicast).  The KS CTAs with the same n split K: CTA z contracts
 // super-blocks [z nsb / KS, (z+1) nsb / KS) into its own TMEM, and the partial
 // tiles are summed through distributed shared memory (below).
-template <int BN, int SUB, int CS, int KS>
-__global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
+template <int BN, int SUB, int DQ, int CS, int KS>
+__global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmArgs a) {
-  using L = GemmSmem<BN, SUB>;
+  using L = GemmSmem<BN, SUB, DQ>;
+  static_assert(L::kPerRow == 1 || L::kPerRow == 2, "one or two threads per weight row");
   static_assert(BN % 16 == 0 && BN <= 256 && SUB * BN <= 512, "MMA shape / TMEM columns");
   static_assert(BN / 16 * 128 * 64 <= L::kBars, "split-K exchange buffer");
   constexpr int kXStages = L::kXStages, kBStages = L::kBStages, kRawStages = L::kRawStages;
@@ -226,7 +232,9 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- dequantize
-    const int row = threadIdx.x - 128;  // weight row within the tile
+    const int dq = threadIdx.x - 128;
+    const int row = dq % L::kRowSpan;   // weight row within the tile
+    const int part = dq / L::kRowSpan;  // which chunks of a k block this thread writes
     const bool live = row < BN;         // threads past BN only keep the barrier protocol
     const int r8 = row & 7;
     uint8_t *brow0 = smem + L::kB + (live ? row >> 3 : 0) * 1024 + r8 * 128;
@@ -262,8 +270,9 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
         uint8_t *brow = brow0 + bs * L::kBStageBytes;
         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {     // 16-byte chunk j holds k = 8j .. 8j+7
-          const int hi = j >> 2;          // chunks 4..7: high nibbles
+        for (int jj = 0; jj < 8 / L::kPerRow; ++jj) {  // 16-byte chunk j holds k = 8j .. 8j+7
+          const int j = part * (8 / L::kPerRow) + jj;
+          const int hi = j >> 2;                        // chunks 4..7: high nibbles
           const uint32_t wa = words[2 * (j & 3)], wb = words[2 * (j & 3) + 1];
           const uint32_t ma = (hi ? (wa >> 4) : wa) & 0x0F0F0F0Fu;
           const uint32_t mb = (hi ? (wb >> 4) : wb) & 0x0F0F0F0Fu;
@@ -291,12 +300,13 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
 
   // ------------------------------------------------------------ epilogue
   // Dequant warp w drains TMEM lane quarter w % 4 (tokens 32 (w % 4) ..) and
-  // columns [128 h, 128 h + 128) with h = (w - 4) / 4, in 16-column chunks.
+  // its share h = (w - 4) / 4 of the 16-column chunks.
   const bool epi = warp >= 4;
   const int q = warp & 3;
   const int row = 32 * q + lane;  // token within a sub-tile
-  const int c_lo = epi ? ((warp - 4) >> 2) * 8 : 0;     // first 16-column chunk
-  const int c_hi = epi ? min(BN / 16, c_lo + 8) : 0;    // end of this warp's chunks
+  constexpr int kPerQuarter = (BN / 16 + DQ / 4 - 1) / (DQ / 4);  // chunks per warp of a quarter
+  const int c_lo = epi ? ((warp - 4) >> 2) * kPerQuarter : 0;     // first 16-column chunk
+  const int c_hi = epi ? min(BN / 16, c_lo + kPerQuarter) : 0;    // end of this warp's chunks
   if (epi && acc_ready) tc_fence_after();
   if constexpr (KS == 1) {
     if (epi && acc_ready) {
@@ -390,10 +400,12 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB>::kThreads, 1)
 
 std::once_flag g_gemm_attr;
 
+constexpr int kDQ = Q4K_GEMM_DQ_WARPS;
+
 template <int BN, int SUB, int CS, int KS>
 void gemm_allow() {
-  cudaFuncSetAttribute(gemm_kernel<BN, SUB, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<BN, SUB>::kAlloc);
+  cudaFuncSetAttribute(gemm_kernel<BN, SUB, kDQ, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       GemmSmem<BN, SUB, kDQ>::kAlloc);
 }
 
 template <int BN, int SUB>
@@ -416,19 +428,19 @@ void gemm_attributes() {
 template <int BN, int SUB>
 cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &xmap,
                     const CUtensorMap &wmap, const GemmArgs &args) {
-  cfg.dynamicSmemBytes = GemmSmem<BN, SUB>::kAlloc;
-  cfg.blockDim = dim3((unsigned)GemmSmem<BN, SUB>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = GemmSmem<BN, SUB, kDQ>::kAlloc;
+  cfg.blockDim = dim3((unsigned)GemmSmem<BN, SUB, kDQ>::kThreads, 1, 1);
   auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, xmap, wmap, args); };
   if (cs == 2) {
-    if (ks == 4) return go(gemm_kernel<BN, SUB, 2, 4>);
-    if (ks == 3) return go(gemm_kernel<BN, SUB, 2, 3>);
-    if (ks == 2) return go(gemm_kernel<BN, SUB, 2, 2>);
-    return go(gemm_kernel<BN, SUB, 2, 1>);
+    if (ks == 4) return go(gemm_kernel<BN, SUB, kDQ, 2, 4>);
+    if (ks == 3) return go(gemm_kernel<BN, SUB, kDQ, 2, 3>);
+    if (ks == 2) return go(gemm_kernel<BN, SUB, kDQ, 2, 2>);
+    return go(gemm_kernel<BN, SUB, kDQ, 2, 1>);
   }
-  if (ks == 4) return go(gemm_kernel<BN, SUB, 1, 4>);
-  if (ks == 3) return go(gemm_kernel<BN, SUB, 1, 3>);
-  if (ks == 2) return go(gemm_kernel<BN, SUB, 1, 2>);
-  return go(gemm_kernel<BN, SUB, 1, 1>);
+  if (ks == 4) return go(gemm_kernel<BN, SUB, kDQ, 1, 4>);
+  if (ks == 3) return go(gemm_kernel<BN, SUB, kDQ, 1, 3>);
+  if (ks == 2) return go(gemm_kernel<BN, SUB, kDQ, 1, 2>);
+  return go(gemm_kernel<BN, SUB, kDQ, 1, 1>);
 }
 
 }  // namespace
