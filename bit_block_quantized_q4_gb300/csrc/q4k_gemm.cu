@@ -3,22 +3,28 @@
 // prefill throughput is a reported metric in "PRD: Performant Concurrent
 // Distributed GGUF Runtime", DGR-001).
 //
-// One CTA computes a 512-token x BN-weight-row output tile (BN = 128, or 112
-// when that spreads a narrow projection over more SMs), so every weight is
-// dequantized exactly once per 512 tokens.  Warp roles:
-//   warp 0      TMA producer of X k-blocks (512 x 64 bf16, 128-byte swizzle),
-//               optionally multicast across a cluster of CTAs that share X
-//   warp 1      TMEM owner and single-thread tcgen05.mma issuer: four
-//               128 x BN x 16 MMAs per 16-wide k step (one per 128-token
-//               sub-tile) accumulate in fp32 in tensor memory
-//   warp 2      TMA producer of raw Q4_K super-blocks (BN rows x 144 bytes)
+// One CTA computes a 512-token x 128-weight-row output tile, so every weight
+// is dequantized exactly once per 512 tokens.  The MMA is oriented with the
+// weights as its A operand (M = 128 rows) and X as its B operand (N = 256
+// tokens): per 16-wide k step two 128 x 256 x 16 MMAs read 4 KB of weights
+// twice and 16 KB of X once from shared memory, where X as A would read the
+// weights four times.  Shared-memory bandwidth, not the tensor pipe, is what
+// bounds this kernel: the MMA operand reads, the X copies and the dequantized
+// weight stores all go through it.  Warp roles:
+//   warp 0      TMA producer of X k-blocks (512 x 64 bf16, 128-byte swizzle,
+//               each 256-token half with its own barriers), optionally
+//               multicast across a cluster of CTAs that share X
+//   warp 1      TMEM owner and single-thread tcgen05.mma issuer; the fp32
+//               accumulator D[row][token] fills all 512 TMEM columns
+//   warp 2      TMA producer of raw Q4_K super-blocks (128 rows x 144 bytes)
 //   warps 4..7  dequantize: thread = weight row; each 64-wide k-block is one
 //               32-byte quant chunk of a super-block (low nibbles: sub-block
 //               2c, high nibbles: 2c+1).  The weight is fma(d sc, q, -dmin m)
 //               in fp32 (the exact value rounded once), rounded to nearest-even
 //               bf16 and written in the 128-byte-swizzled K-major layout the MMA
-//               reads.  After the last k-block they drain TMEM (one lane
-//               quarter each), round to bf16 and store Y.
+//               reads.
+// After the last k-block all eight warps drain TMEM (warp w: lane quarter
+// w % 4, half w / 4 of the columns), round to bf16 and store Y.
 // Stages are chained by mbarriers; every wait is bounded and reports a
 // timeout through the device error word instead of hanging.
 #include <algorithm>
@@ -31,37 +37,47 @@ namespace q4k {
 
 namespace {
 
-#ifndef Q4K_GEMM_DQ_WARPS  // dequantizing warps per CTA: 4 (a thread per weight row) or 8 (two; measured slower)
-#define Q4K_GEMM_DQ_WARPS 4
-#endif
-constexpr int kBK = 64;  // k per block = one 128-byte swizzle panel (X stage and weight stage)
+constexpr int kBK = 64;        // k per block = one 128-byte swizzle panel (X stage and weight stage)
+constexpr int kBN = 128;       // weight rows per CTA = the MMA's M
+constexpr int kTokens = 512;   // tokens per CTA = two MMAs of N = 256
+constexpr int kSub = kTokens / 128;  // 128-token sub-tiles (one X copy each)
+constexpr int kDqWarps = 4;    // dequantizing warps, a thread per weight row
+constexpr int kThreads = 128 + 32 * kDqWarps;
 
-// Shared-memory plan of one CTA: SUB 128-token sub-tiles of X per stage, BN
-// weight rows (dequantized bf16 stage + raw Q4_K stage), barriers, TMEM slot.
-template <int BN, int SUB, int DQ>
+// Shared-memory plan of one CTA.
 struct GemmSmem {
-  static constexpr int kTokens = 128 * SUB;
-  static constexpr int kDqWarps = DQ;                      // dequantizing warps
-  static constexpr int kRowSpan = BN > 128 ? BN : 128;     // weight rows one pass of them covers
-  static constexpr int kPerRow = 32 * DQ / kRowSpan;       // threads per weight row (1 or 2)
-  static constexpr int kThreads = 128 + 32 * kDqWarps;
-  static constexpr int kXSubBytes = 128 * kBK * 2;
-  static constexpr int kXStageBytes = SUB * kXSubBytes;
+  static constexpr int kXSubBytes = 128 * kBK * 2;            // 16 KB
+  static constexpr int kXStageBytes = kSub * kXSubBytes;      // 64 KB
   static constexpr int kXStages = 2;
-  static constexpr int kBStages = SUB == 4 ? 3 : 2;
+  static constexpr int kXParts = 2;                           // 256-token halves per stage
+  static constexpr int kXPartBytes = kXStageBytes / kXParts;  // 32 KB
+  static constexpr int kBStages = 3;
   static constexpr int kRawStages = 2;
-  static constexpr int kBStageBytes = BN * kBK * 2;
-  static constexpr int kRawBytes = BN * kBlockBytes;
+  static constexpr int kBStageBytes = kBN * kBK * 2;          // 16 KB
+  static constexpr int kRawBytes = kBN * kBlockBytes;         // 18 KB
   static constexpr int kX = 0;
   static constexpr int kB = kX + kXStages * kXStageBytes;
   static constexpr int kRaw = kB + kBStages * kBStageBytes;
   static constexpr int kBars = kRaw + kRawStages * kRawBytes;
-  // barriers: xfull, xempty, bfull, bempty, rfull, rempty, acc
-  static constexpr int kNumBars = 2 * kXStages + 2 * kBStages + 2 * kRawStages + 1;
+  // barriers: xfull, xempty (per stage and half), bfull, bempty, rfull, rempty,
+  // acc, split-K partials received
+  static constexpr int kNumBars = 4 * kXStages + 2 * kBStages + 2 * kRawStages + 2;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
+static_assert(GemmSmem::kAlloc <= 227 * 1024, "shared memory per CTA");
+// Split-K: the 16-column chunks of the accumulator (8 per 128-token sub-tile)
+// are dealt out to the K ranks, chunk c to rank c % KS.  A rank receives the
+// other ranks' partials of its chunks into the stage memory below the barriers,
+// one 8 KB block (128 rows x 64 bytes) per (sub-tile, owned chunk, sender).
+__host__ __device__ constexpr int owned_max(int ks) { return (kBN / 16 + ks - 1) / ks; }
+__host__ __device__ constexpr int recv_bytes(int ks) {
+  return ks > 1 ? kSub * owned_max(ks) * (ks - 1) * 128 * 64 : 0;
+}
+static_assert(recv_bytes(2) <= GemmSmem::kBars && recv_bytes(3) <= GemmSmem::kBars &&
+                  recv_bytes(4) <= GemmSmem::kBars,
+              "split-K receive buffer");
 
 struct GemmArgs {
   __nv_bfloat16 *y;
@@ -75,61 +91,59 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Stores 16 fp32 accumulator values of row m, columns n .. n+15, as bf16.
-__device__ __forceinline__ void store_y16(const GemmArgs &a, int m, int n, const float (&v)[16]) {
-  if (m >= a.m || n >= a.n) return;
-  __nv_bfloat16 *yrow = a.y + (int64_t)m * a.ldy;
-  uint4 o0, o1;
-  o0.x = pack_bf16(v[0], v[1]);
-  o0.y = pack_bf16(v[2], v[3]);
-  o0.z = pack_bf16(v[4], v[5]);
-  o0.w = pack_bf16(v[6], v[7]);
-  o1.x = pack_bf16(v[8], v[9]);
-  o1.y = pack_bf16(v[10], v[11]);
-  o1.z = pack_bf16(v[12], v[13]);
-  o1.w = pack_bf16(v[14], v[15]);
-  if (n + 16 <= a.n) {
-    *reinterpret_cast<uint4 *>(yrow + n) = o0;
-    *reinterpret_cast<uint4 *>(yrow + n + 8) = o1;
-  } else {
-    const uint32_t w[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-    for (int e = 0; e < 16 && n + e < a.n; ++e)
-      yrow[n + e] = __ushort_as_bfloat16((unsigned short)(w[e >> 1] >> (16 * (e & 1))));
+// Stores 16 fp32 accumulator values of weight row n, tokens m .. m+15, as bf16.
+// Lanes 2i and 2i+1 hold adjacent rows: after one exchange the even lane writes
+// the (row n, row n+1) pairs of tokens m, m+2, .. and the odd lane those of
+// tokens m+1, m+3, .., four bytes per store.  Every lane of the warp calls it.
+__device__ __forceinline__ void store_y16_rows(const GemmArgs &a, int m, int n, const float (&v)[16]) {
+  const bool odd = (threadIdx.x & 1) != 0;
+  const int nn = odd ? n - 1 : n;  // first row of the pair
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    const float got = __shfl_xor_sync(0xffffffffu, odd ? v[e] : v[e + 1], 1);
+    const int mm = m + e + (odd ? 1 : 0);
+    const float lo = odd ? got : v[e];
+    const float hi = odd ? v[e + 1] : got;
+    if (mm < a.m && nn < a.n) {
+      __nv_bfloat16 *p = a.y + (int64_t)mm * a.ldy + nn;
+      if (nn + 1 < a.n)
+        *reinterpret_cast<uint32_t *>(p) = pack_bf16(lo, hi);
+      else
+        *p = __float2bfloat16_rn(lo);
+    }
   }
 }
 
 // A cluster is CS x KS CTAs, rank = n + CS z.  The CS CTAs with the same z
-// take consecutive BN-row weight tiles over the same K range and share X (TMA
+// take consecutive 128-row weight tiles over the same K range and share X (TMA
 // multicast).  The KS CTAs with the same n split K: CTA z contracts
 // super-blocks [z nsb / KS, (z+1) nsb / KS) into its own TMEM, and the partial
 // tiles are summed through distributed shared memory (below).
-template <int BN, int SUB, int DQ, int CS, int KS>
-__global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
+template <int CS, int KS>
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmArgs a) {
-  using L = GemmSmem<BN, SUB, DQ>;
-  static_assert(L::kPerRow == 1 || L::kPerRow == 2, "one or two threads per weight row");
-  static_assert(BN % 16 == 0 && BN <= 256 && SUB * BN <= 512, "MMA shape / TMEM columns");
-  static_assert(BN / 16 * 128 * 64 <= L::kBars, "split-K exchange buffer");
-  constexpr int kXStages = L::kXStages, kBStages = L::kBStages, kRawStages = L::kRawStages;
-  constexpr int kDqWarps = L::kDqWarps;
+  using L = GemmSmem;
+  constexpr int kXStages = L::kXStages, kXParts = L::kXParts;
+  constexpr int kBStages = L::kBStages, kRawStages = L::kRawStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-  uint64_t *xfull = bars;
-  uint64_t *xempty = xfull + kXStages;
-  uint64_t *bfull = xempty + kXStages;
+  uint64_t *xfull = bars;  // [stage * kXParts + half]
+  uint64_t *xempty = xfull + kXStages * kXParts;
+  uint64_t *bfull = xempty + kXStages * kXParts;
   uint64_t *bempty = bfull + kBStages;
   uint64_t *rfull = bempty + kBStages;
   uint64_t *rempty = rfull + kRawStages;
   uint64_t *accfull = rempty + kRawStages;
+  uint64_t *redfull = accfull + 1;  // split-K: all peer partials of the owned chunks landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * L::kTokens;
+  const int n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * kTokens;
   const uint32_t crank = (CS * KS > 1) ? cluster_ctarank() : 0u;
   const uint32_t rank = crank % CS;   // position among the CTAs sharing X
   const uint32_t krank = crank / CS;  // K range of this CTA
@@ -145,7 +159,7 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&xmap);
     prefetch_tmap(&wmap);
-    for (int s = 0; s < kXStages; ++s) {
+    for (int s = 0; s < kXStages * kXParts; ++s) {
       mbar_init(&xfull[s], 1);
       mbar_init(&xempty[s], CS);
     }
@@ -158,64 +172,77 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
       mbar_init(&rempty[s], kDqWarps);
     }
     mbar_init(accfull, 1);
+    mbar_init(redfull, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  // Every barrier below is reached by whole, reconverged warps: a warp whose
+  // lanes arrive separately would be counted more than once.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (CS * KS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
-  bool acc_ready = false;  // dequant warps: the accumulator tile is complete
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = 0; kb < nkb && ok; ++kb) {
         const int s = kb % kXStages;
         const uint32_t ph = (uint32_t)((kb / kXStages) & 1);
-        if (!mbar_wait(&xempty[s], ph ^ 1u, a.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(&xfull[s], L::kXStageBytes);
         uint8_t *dst = smem + L::kX + s * L::kXStageBytes;
         const int kx = (kb_lo + kb) * kBK;
-        for (int sub = (int)rank; sub < SUB; sub += CS) {
-          if (CS > 1)
-            tma_load_2d_mc(dst + sub * L::kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub, kMask);
-          else
-            tma_load_2d(dst + sub * L::kXSubBytes, &xmap, &xfull[s], kx, m0 + 128 * sub);
+        for (int h = 0; h < kXParts; ++h) {
+          uint64_t *full = &xfull[s * kXParts + h];
+          if (!mbar_wait(&xempty[s * kXParts + h], ph ^ 1u, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(full, L::kXPartBytes);
+          for (int sub = 2 * h + (int)rank; sub < 2 * h + 2; sub += CS) {
+            if (CS > 1)
+              tma_load_2d_mc(dst + sub * L::kXSubBytes, &xmap, full, kx, m0 + 128 * sub, kMask);
+            else
+              tma_load_2d(dst + sub * L::kXSubBytes, &xmap, full, kx, m0 + 128 * sub);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBN, 256);
       const uint32_t xbase = smem_u32(smem + L::kX);
       const uint32_t bbase = smem_u32(smem + L::kB);
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = 0; kb < nkb && ok; ++kb) {
         const int xs = kb % kXStages, bs = kb % kBStages;
-        if (!mbar_wait(&xfull[xs], (uint32_t)((kb / kXStages) & 1), a.err)) { ok = false; break; }
         if (!mbar_wait(&bfull[bs], (uint32_t)((kb / kBStages) & 1), a.err)) { ok = false; break; }
-        tc_fence_after();
 #pragma unroll
-        for (int k16 = 0; k16 < kBK / 16; ++k16) {
-          const uint64_t bdesc = sdesc_sw128(bbase + bs * L::kBStageBytes + k16 * 32, 1024);
-#pragma unroll
-          for (int sub = 0; sub < SUB; ++sub) {
-            const uint64_t adesc =
-                sdesc_sw128(xbase + xs * L::kXStageBytes + sub * L::kXSubBytes + k16 * 32, 1024);
-            tc_mma_f16(tmem + sub * BN, adesc, bdesc, idesc, (kb | k16) != 0);
+        for (int h = 0; h < kXParts; ++h) {
+          if (!mbar_wait(&xfull[xs * kXParts + h], (uint32_t)((kb / kXStages) & 1), a.err)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          // D[row][token] += W[row][k] X[token][k] for the tokens of half h:
+          // A = the 128 weight rows, B = sub-tiles 2h, 2h+1 (256 rows of 128
+          // bytes, contiguous), accumulated in TMEM columns 256 h ...
+#pragma unroll
+          for (int k16 = 0; k16 < kBK / 16; ++k16) {
+            const uint64_t wdesc = sdesc_sw128(bbase + bs * L::kBStageBytes + k16 * 32, 1024);
+            const uint64_t xdesc =
+                sdesc_sw128(xbase + xs * L::kXStageBytes + h * L::kXPartBytes + k16 * 32, 1024);
+            tc_mma_f16(tmem + h * 256, wdesc, xdesc, idesc, (kb | k16) != 0);
+          }
+          if (CS > 1)
+            tc_commit_mc(&xempty[xs * kXParts + h], kMask);
+          else
+            tc_commit(&xempty[xs * kXParts + h]);
         }
+        if (!ok) break;
         tc_commit(&bempty[bs]);
-        if (CS > 1)
-          tc_commit_mc(&xempty[xs], kMask);
-        else
-          tc_commit(&xempty[xs]);
       }
       tc_commit(accfull);
     }
@@ -232,16 +259,13 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- dequantize
-    const int dq = threadIdx.x - 128;
-    const int row = dq % L::kRowSpan;   // weight row within the tile
-    const int part = dq / L::kRowSpan;  // which chunks of a k block this thread writes
-    const bool live = row < BN;         // threads past BN only keep the barrier protocol
+    const int row = threadIdx.x - 128;  // weight row within the tile
     const int r8 = row & 7;
-    uint8_t *brow0 = smem + L::kB + (live ? row >> 3 : 0) * 1024 + r8 * 128;
+    uint8_t *brow0 = smem + L::kB + (row >> 3) * 1024 + r8 * 128;
     for (int sb = 0; sb < nsb && ok; ++sb) {
       const int rs = sb % kRawStages;
       if (!mbar_wait(&rfull[rs], (uint32_t)((sb / kRawStages) & 1), a.err)) { ok = false; break; }
-      const uint8_t *raw = smem + L::kRaw + rs * L::kRawBytes + (live ? row : 0) * kBlockBytes;
+      const uint8_t *raw = smem + L::kRaw + rs * L::kRawBytes + row * kBlockBytes;
       const uint4 h = *reinterpret_cast<const uint4 *>(raw);
       uint32_t sc_lo, sc_hi, m_lo, m_hi;
       scales_all(h.y, h.z, h.w, &sc_lo, &sc_hi, &m_lo, &m_hi);
@@ -270,9 +294,8 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
         uint8_t *brow = brow0 + bs * L::kBStageBytes;
         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int jj = 0; jj < 8 / L::kPerRow; ++jj) {  // 16-byte chunk j holds k = 8j .. 8j+7
-          const int j = part * (8 / L::kPerRow) + jj;
-          const int hi = j >> 2;                        // chunks 4..7: high nibbles
+        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
+          const int hi = j >> 2;       // chunks 4..7: high nibbles
           const uint32_t wa = words[2 * (j & 3)], wb = words[2 * (j & 3) + 1];
           const uint32_t ma = (hi ? (wa >> 4) : wa) & 0x0F0F0F0Fu;
           const uint32_t mb = (hi ? (wb >> 4) : wb) & 0x0F0F0F0Fu;
@@ -288,104 +311,124 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
           o.y = pack_bf16(fmaf(ds, q[2], -dm), fmaf(ds, q[3], -dm));
           o.z = pack_bf16(fmaf(ds, q[4], -dm), fmaf(ds, q[5], -dm));
           o.w = pack_bf16(fmaf(ds, q[6], -dm), fmaf(ds, q[7], -dm));
-          if (live) *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
+          *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bfull[bs]);
       }
     }
-    acc_ready = ok && mbar_wait(accfull, 0u, a.err);
   }
 
   // ------------------------------------------------------------ epilogue
-  // Dequant warp w drains TMEM lane quarter w % 4 (tokens 32 (w % 4) ..) and
-  // its share h = (w - 4) / 4 of the 16-column chunks.
-  const bool epi = warp >= 4;
+  // Warp w drains TMEM lane quarter w % 4 (weight rows 32 (w % 4) ..) and, of
+  // each 128-token sub-tile, the 16-column chunks [4 (w / 4), 4 (w / 4) + 4).
+  __syncwarp();
+  ok = __all_sync(0xffffffffu, ok);  // a role loop that timed out ran on lane 0 only
+  const bool acc_ready = ok && mbar_wait(accfull, 0u, a.err);
   const int q = warp & 3;
-  const int row = 32 * q + lane;  // token within a sub-tile
-  constexpr int kPerQuarter = (BN / 16 + DQ / 4 - 1) / (DQ / 4);  // chunks per warp of a quarter
-  const int c_lo = epi ? ((warp - 4) >> 2) * kPerQuarter : 0;     // first 16-column chunk
-  const int c_hi = epi ? min(BN / 16, c_lo + kPerQuarter) : 0;    // end of this warp's chunks
-  if (epi && acc_ready) tc_fence_after();
+  const int row = 32 * q + lane;  // weight row within the tile
+  const int c_lo = (warp >> 2) * 4, c_hi = c_lo + 4;
+  const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+  if (acc_ready) tc_fence_after();
   if constexpr (KS == 1) {
-    if (epi && acc_ready) {
-      for (int sub = 0; sub < SUB; ++sub) {
+    if (acc_ready) {
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; ++c) {
-          uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
-          tmem_ld_wait();
-          float v[16];
+      for (int sub = 0; sub < kSub; ++sub) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-          store_y16(a, m0 + 128 * sub + row, n0 + 16 * c, v);
+        for (int c = c_lo; c < c_hi; c += 2) {
+          uint32_t r0[16], r1[16];
+          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r0);
+          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c + 16), r1);
+          tmem_ld_wait();
+          float v0[16], v1[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            v0[e] = __uint_as_float(r0[e]);
+            v1[e] = __uint_as_float(r1[e]);
+          }
+          store_y16_rows(a, m0 + 128 * sub + 16 * c, n0 + row, v0);
+          store_y16_rows(a, m0 + 128 * sub + 16 * c + 16, n0 + row, v1);
         }
       }
     }
   } else {
-    // Split-K sum, one round per 128-token sub-tile.  Every CTA copies its
-    // partials of the chunks it does not own from TMEM into its own shared
-    // memory (idle now: all copies and MMAs are done); after a cluster barrier
-    // each CTA takes the chunks c with c % KS == its K rank, adds the KS
-    // partials in K-rank order (its own from TMEM, the others from the peers'
-    // shared memory) and stores Y; a second barrier frees the buffers.  Every
-    // thread of every CTA passes both barriers of each round, whatever happened
-    // before.  Layout: 16 columns of a row are four 16-byte units, unit u stored
-    // at slot u ^ ((row >> 1) & 3) so that eight consecutive rows hit eight
+    // Split-K sum.  After a cluster barrier (every CTA is done with its stage
+    // memory), each CTA pushes its partials of the chunks it does not own
+    // straight from TMEM into the owner's receive blocks (st.async, counted on
+    // the owner's redfull barrier); the owner waits for all of them, adds the
+    // KS partials in K-rank order (its own from TMEM) and stores Y.  Every
+    // thread of every CTA passes the cluster barriers whatever happened before.
+    // Block layout: 16 columns of a row are four 16-byte units, unit u stored at
+    // slot u ^ ((row >> 1) & 3) so that eight consecutive rows hit eight
     // different bank groups.
-    float4 *buf = reinterpret_cast<float4 *>(smem);  // [chunk][row][4]
+    constexpr int kOwn = owned_max(KS);
     const int swz = (row >> 1) & 3;
-    auto unit = [&](int c, int u) { return (c * 128 + row) * 4 + (u ^ swz); };
-    for (int sub = 0; sub < SUB; ++sub) {
-      if (epi && acc_ready) {
+    auto block_off = [&](int sub, int c, int sender_slot) {
+      return (uint32_t)(((sub * kOwn + c / KS) * (KS - 1) + sender_slot) * (128 * 64));
+    };
+    auto unit_off = [&](int u) { return (uint32_t)((row * 4 + (u ^ swz)) * 16); };
+    if (threadIdx.x == 0) {
+      const int own = (kBN / 16 - (int)krank + KS - 1) / KS;  // chunks c with c % KS == krank
+      mbar_arrive_expect_tx(redfull, (uint32_t)(kSub * own * (KS - 1) * 128 * 64));
+    }
+    cluster_sync();
+    const uint32_t base = smem_u32(smem);
+    if (acc_ready) {
+#pragma unroll 1
+      for (int sub = 0; sub < kSub; ++sub) {
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; ++c) {
-          if (c % KS == (int)krank) continue;  // kept in TMEM, read there below
+          const int owner = c % KS;
+          if (owner == (int)krank) continue;
           uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
+          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r);
           tmem_ld_wait();
+          const uint32_t peer = rank + CS * (uint32_t)owner;
+          const int slot = (int)krank < owner ? (int)krank : (int)krank - 1;
+          const uint32_t dst = peer_smem(base + block_off(sub, c, slot), peer);
+          const uint32_t bar = peer_smem(smem_u32(redfull), peer);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            buf[unit(c, u)] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                          __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+            st_async_v4(dst + unit_off(u),
+                        make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                    __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                        bar);
         }
       }
-      cluster_sync();
-      if (epi && acc_ready) {
+    }
+    const bool got = mbar_wait(redfull, 0u, a.err);
+    if (acc_ready && got) {
+#pragma unroll 1
+      for (int sub = 0; sub < kSub; ++sub) {
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; ++c) {
           if (c % KS != (int)krank) continue;
-          float4 pv[KS][4];
-#pragma unroll
-          for (int z = 0; z < KS; ++z)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (z != (int)krank)
-                pv[z][u] = ld_peer_v4(peer_smem(smem_u32(&buf[unit(c, u)]), rank + CS * (uint32_t)z));
           uint32_t r[16];
-          tmem_ld_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(sub * BN + 16 * c), r);
+          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r);
           tmem_ld_wait();
           float v[16];
 #pragma unroll
           for (int z = 0; z < KS; ++z) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const bool mine = z == (int)krank;
-              const float t0 = mine ? __uint_as_float(r[4 * u]) : pv[z][u].x;
-              const float t1 = mine ? __uint_as_float(r[4 * u + 1]) : pv[z][u].y;
-              const float t2 = mine ? __uint_as_float(r[4 * u + 2]) : pv[z][u].z;
-              const float t3 = mine ? __uint_as_float(r[4 * u + 3]) : pv[z][u].w;
-              v[4 * u] = z ? v[4 * u] + t0 : t0;
-              v[4 * u + 1] = z ? v[4 * u + 1] + t1 : t1;
-              v[4 * u + 2] = z ? v[4 * u + 2] + t2 : t2;
-              v[4 * u + 3] = z ? v[4 * u + 3] + t3 : t3;
+              float4 t;
+              if (z == (int)krank) {
+                t = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+              } else {
+                const int slot = z < (int)krank ? z : z - 1;
+                t = *reinterpret_cast<const float4 *>(smem + block_off(sub, c, slot) + unit_off(u));
+              }
+              v[4 * u] = z ? v[4 * u] + t.x : t.x;
+              v[4 * u + 1] = z ? v[4 * u + 1] + t.y : t.y;
+              v[4 * u + 2] = z ? v[4 * u + 2] + t.z : t.z;
+              v[4 * u + 3] = z ? v[4 * u + 3] + t.w : t.w;
             }
           }
-          store_y16(a, m0 + 128 * sub + row, n0 + 16 * c, v);
+          store_y16_rows(a, m0 + 128 * sub + 16 * c, n0 + row, v);
         }
       }
-      cluster_sync();
     }
   }
 
@@ -400,47 +443,38 @@ __global__ void __launch_bounds__(GemmSmem<BN, SUB, DQ>::kThreads, 1)
 
 std::once_flag g_gemm_attr;
 
-constexpr int kDQ = Q4K_GEMM_DQ_WARPS;
-
-template <int BN, int SUB, int CS, int KS>
+template <int CS, int KS>
 void gemm_allow() {
-  cudaFuncSetAttribute(gemm_kernel<BN, SUB, kDQ, CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       GemmSmem<BN, SUB, kDQ>::kAlloc);
-}
-
-template <int BN, int SUB>
-void gemm_allow_all() {
-  gemm_allow<BN, SUB, 1, 1>();
-  gemm_allow<BN, SUB, 2, 1>();
-  gemm_allow<BN, SUB, 1, 2>();
-  gemm_allow<BN, SUB, 1, 3>();
-  gemm_allow<BN, SUB, 1, 4>();
-  gemm_allow<BN, SUB, 2, 2>();
-  gemm_allow<BN, SUB, 2, 3>();
-  gemm_allow<BN, SUB, 2, 4>();
+  cudaFuncSetAttribute(gemm_kernel<CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       GemmSmem::kAlloc);
 }
 
 void gemm_attributes() {
-  gemm_allow_all<128, 4>();
-  gemm_allow_all<112, 4>();
+  gemm_allow<1, 1>();
+  gemm_allow<2, 1>();
+  gemm_allow<1, 2>();
+  gemm_allow<1, 3>();
+  gemm_allow<1, 4>();
+  gemm_allow<2, 2>();
+  gemm_allow<2, 3>();
+  gemm_allow<2, 4>();
 }
 
-template <int BN, int SUB>
 cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &xmap,
                     const CUtensorMap &wmap, const GemmArgs &args) {
-  cfg.dynamicSmemBytes = GemmSmem<BN, SUB, kDQ>::kAlloc;
-  cfg.blockDim = dim3((unsigned)GemmSmem<BN, SUB, kDQ>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = GemmSmem::kAlloc;
+  cfg.blockDim = dim3((unsigned)kThreads, 1, 1);
   auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, xmap, wmap, args); };
   if (cs == 2) {
-    if (ks == 4) return go(gemm_kernel<BN, SUB, kDQ, 2, 4>);
-    if (ks == 3) return go(gemm_kernel<BN, SUB, kDQ, 2, 3>);
-    if (ks == 2) return go(gemm_kernel<BN, SUB, kDQ, 2, 2>);
-    return go(gemm_kernel<BN, SUB, kDQ, 2, 1>);
+    if (ks == 4) return go(gemm_kernel<2, 4>);
+    if (ks == 3) return go(gemm_kernel<2, 3>);
+    if (ks == 2) return go(gemm_kernel<2, 2>);
+    return go(gemm_kernel<2, 1>);
   }
-  if (ks == 4) return go(gemm_kernel<BN, SUB, kDQ, 1, 4>);
-  if (ks == 3) return go(gemm_kernel<BN, SUB, kDQ, 1, 3>);
-  if (ks == 2) return go(gemm_kernel<BN, SUB, kDQ, 1, 2>);
-  return go(gemm_kernel<BN, SUB, kDQ, 1, 1>);
+  if (ks == 4) return go(gemm_kernel<1, 4>);
+  if (ks == 3) return go(gemm_kernel<1, 3>);
+  if (ks == 2) return go(gemm_kernel<1, 2>);
+  return go(gemm_kernel<1, 1>);
 }
 
 }  // namespace
@@ -450,9 +484,6 @@ cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &
 #endif
 #ifndef Q4K_GEMM_SPLITK  // split K across a cluster when the output tiles cannot fill the SMs
 #define Q4K_GEMM_SPLITK 1
-#endif
-#ifndef Q4K_GEMM_SHAPE  // 0: choose the tile per call; 128 or 112: force that weight-tile width
-#define Q4K_GEMM_SHAPE 0
 #endif
 
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
@@ -468,6 +499,14 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
                      strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  {
+    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
+    const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
+    const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)kBN};
+    if (encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   GemmArgs args;
   args.y = static_cast<__nv_bfloat16 *>(y);
   args.ldy = ldy;
@@ -476,53 +515,22 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   args.k = (int)k;
   args.err = device_error_word();
 
-  // Tile shape, K split and X sharing.  Candidates: 512 tokens x 128 or 112
-  // weight rows (112 spreads a narrow projection over more SMs).  K is split
-  // across a cluster when the output tiles cannot fill the SMs.  Estimated time =
-  // waves x k-blocks per CTA x the larger of the X feed (SUB x 16 KB at ~64 GB/s
-  // per SM, measured) and the MMA time (~12.7 TFLOP/s per SM).  A 256 x 256 tile
-  // (half the X bytes per flop, weights dequantized once per 256 tokens) was
-  // measured slower on both 512-token projections and is not offered.
+  // K is split across a cluster (up to 4 ways) when the output tiles cannot
+  // fill the SMs; pairs of CTAs over the same K range share X by multicast.
   const int sms = device_facts()->sm_count;
-  struct Shape { int bn, sub; };
-  const Shape shapes[2] = {{128, 4}, {112, 4}};
-  int bn = 128, cs = 1, ks = 1, ntiles = 0, mtiles = 0;
-  double best = -1;
-  for (const Shape &c : shapes) {
-    if (Q4K_GEMM_SHAPE && c.bn != Q4K_GEMM_SHAPE) continue;
-    const int mt = (int)((m + 128 * c.sub - 1) / (128 * c.sub));
-    int nt = (int)((n + c.bn - 1) / c.bn);
-    int kk = 1;
-    if (Q4K_GEMM_SPLITK) {
-      kk = std::max(1, std::min(4, sms / std::max(1, nt * mt)));
-      while (kk > 1 && nsb < 2 * kk) --kk;
-    }
-    int cc = Q4K_GEMM_CLUSTER > 1 ? 2 : 1;
-    while (cc > 1 && (nt < 2 * cc || cc * kk > 8)) cc >>= 1;
-    nt = (nt + cc - 1) / cc * cc;
-    const long ctas = (long)nt * mt * kk;
-    const double t_kb = std::max(c.sub * 16384.0 / 64.0, 2.0 * 128 * c.sub * c.bn * kBK / 12.7e3);
-    const double est = (double)((ctas + sms - 1) / sms) * ((nsb + kk - 1) / kk) * 4 * t_kb;
-    if (best < 0 || est < best) {
-      best = est;
-      bn = c.bn;
-      cs = cc;
-      ks = kk;
-      ntiles = nt;
-      mtiles = mt;
-    }
+  const int mt = (int)((m + kTokens - 1) / kTokens);
+  int nt = (int)((n + kBN - 1) / kBN);
+  int ks = 1;
+  if (Q4K_GEMM_SPLITK) {
+    ks = std::max(1, std::min(4, sms / std::max(1, nt * mt)));
+    while (ks > 1 && nsb < 2 * ks) --ks;
   }
-  {
-    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n};
-    const uint64_t strides[2] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes};
-    const uint32_t box[3] = {(uint32_t)kBlockBytes, 1u, (uint32_t)bn};
-    if (encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(w), dims, strides,
-                     box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  int cs = Q4K_GEMM_CLUSTER > 1 ? 2 : 1;
+  while (cs > 1 && (nt < 2 * cs || cs * ks > 8)) cs >>= 1;
+  nt = (nt + cs - 1) / cs * cs;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, (unsigned)ks);
+  cfg.gridDim = dim3((unsigned)nt, (unsigned)mt, (unsigned)ks);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -531,8 +539,7 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (bn == 112) return gemm_go<112, 4>(cfg, cs, ks, xmap, wmap, args);
-  return gemm_go<128, 4>(cfg, cs, ks, xmap, wmap, args);
+  return gemm_go(cfg, cs, ks, xmap, wmap, args);
 }
 
 }  // namespace q4k
