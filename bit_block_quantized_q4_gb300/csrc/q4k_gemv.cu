@@ -119,18 +119,21 @@ __device__ __forceinline__ B1Lane b1_lane(int t) {
 
 // One super-block of 16*MT rows for batch 1: hdr/qa hold the two rows (g, g+8)
 // of each m-tile (header; quant chunk t), pe/po the B fragments of the even /
-// odd steps, xs2 the scaled sums (X_{2t}, X_{2t+1}).  Adds the super-block's
-// contribution (in scaled units) to yacc[mt] = (row g, row g+8).
+// odd steps, xq = (-1024 X_{2t}, -1024 X_{2t+1}, the same again) from the scaled
+// sub-block sums X_j, us = 2^-s of the super-block.  Adds the super-block's
+// contribution to yacc[mt] = (row g, row g+8).
 template <int MT>
 __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const uint4 (&qa)[MT][2][2],
                                                const uint32_t *pe, const uint32_t *po,
-                                               const float2 xs2, float us, const B1Lane &lc,
+                                               const float4 xq, float us, const B1Lane &lc,
                                                uint32_t magic, float2 (&yacc)[MT]) {
   const bool upper = lc.upper;
   const uint32_t psel = lc.psel, mlo4 = lc.mlo4, mhi4 = lc.mhi4;
   // Two accumulator sets: even steps add only to column 2t (accE[0], [2]),
   // odd steps only to column 2t+1 (accO[1], [3]), so splitting them halves
-  // the dependent MMA chain at no cost.
+  // the dependent MMA chain at no cost.  Both start at xq, so that column 2t
+  // of accE ends at sum (1024 + q) x - 1024 X_{2t} = sum q x and column 2t+1
+  // of accO at sum (1024 + 16 q) x - 1024 X_{2t+1} = 16 sum q x.
   float accE[MT][4], accO[MT][4];
 #pragma unroll
   for (int G2 = 0; G2 < 4; ++G2) {
@@ -147,27 +150,28 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
         // low nibbles, 1024+q: sub-block 2t
         const uint32_t be0 = h ? be.z : be.x, be1 = h ? be.w : be.y;
         if (G == 0)
-          mma_f16_zc(accE[mt], lop_nib(w0, magic), lop_nib(w1, magic), lop_nib(w0s, magic),
-                     lop_nib(w1s, magic), be0, be1);
+          mma_f16_c(accE[mt], xq, lop_nib(w0, magic), lop_nib(w1, magic), lop_nib(w0s, magic),
+                    lop_nib(w1s, magic), be0, be1);
         else
           mma_f16(accE[mt], lop_nib(w0, magic), lop_nib(w1, magic), lop_nib(w0s, magic),
                   lop_nib(w1s, magic), be0, be1);
         // high nibbles, 1024+16q: sub-block 2t+1
         const uint32_t bo0 = h ? bo.z : bo.x, bo1 = h ? bo.w : bo.y;
         if (G == 0)
-          mma_f16_zc(accO[mt], lop_nib_hi16(w0, magic), lop_nib_hi16(w1, magic),
-                     lop_nib_hi16(w0s, magic), lop_nib_hi16(w1s, magic), bo0, bo1);
+          mma_f16_c(accO[mt], xq, lop_nib_hi16(w0, magic), lop_nib_hi16(w1, magic),
+                    lop_nib_hi16(w0s, magic), lop_nib_hi16(w1s, magic), bo0, bo1);
         else
           mma_f16(accO[mt], lop_nib_hi16(w0, magic), lop_nib_hi16(w1, magic),
                   lop_nib_hi16(w0s, magic), lop_nib_hi16(w1s, magic), bo0, bo1);
       }
     }
   }
-  // accE[.][0|2] = sum (1024 + q) x of sub-block 2t, accO[.][1|3] =
-  // sum (1024 + 16 q) x of sub-block 2t+1 (rows g | g+8): subtract
-  // 1024 X, undo the 16, apply the scales.  The scale/min bytes of both
-  // rows are gathered into one word each with PRMT.
-  const float n1024X0 = -1024.f * xs2.x, n1024X1 = -1024.f * xs2.y;
+  // Apply the scales: the scale/min bytes of both rows are gathered into one
+  // word each with PRMT, and each byte b becomes a float by placing it under
+  // the exponent of 2^23 (b exactly) or of 2^19 (b / 16 exactly, which also
+  // undoes the 16 of the high nibbles) and subtracting that power of two.
+  // xq carries -1024 X, so the mins meet dmin / 1024.
+  constexpr uint32_t kExp = 0x4B490000u;  // byte 7: 2^23, byte 6: 2^19
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const uint4 h0 = hdr[mt][0], h1 = hdr[mt][1];
@@ -181,17 +185,15 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const uint32_t h = r ? h1.x : h0.x;
-      const float d = half_lo_to_float(h), dmin = half_hi_to_float(h);
-      const float sca = (float)((sc4 >> (16 * r)) & 0xFFu);
-      const float scb = (float)((sc4 >> (16 * r + 8)) & 0xFFu);
-      const float ma = (float)((m4 >> (16 * r)) & 0xFFu);
-      const float mb = (float)((m4 >> (16 * r + 8)) & 0xFFu);
-      const float ta = accE[mt][2 * r] + n1024X0;
-      const float tb = (accO[mt][2 * r + 1] + n1024X1) * 0.0625f;
-      const float uu = fmaf(scb, tb, sca * ta);
-      const float vv = fmaf(mb, xs2.y, ma * xs2.x);
+      const float d = half_lo_to_float(h), dmn = half_hi_to_float(h) * (1.f / 1024.f);
+      const float sca = __uint_as_float(__byte_perm(sc4, kExp, 0x7440u + 2 * r)) - 8388608.f;
+      const float scb = __uint_as_float(__byte_perm(sc4, kExp, 0x6441u + 2 * r)) - 524288.f;
+      const float ma = __uint_as_float(__byte_perm(m4, kExp, 0x7440u + 2 * r)) - 8388608.f;
+      const float mb = __uint_as_float(__byte_perm(m4, kExp, 0x7441u + 2 * r)) - 8388608.f;
+      const float uu = fmaf(scb, accO[mt][2 * r + 1], sca * accE[mt][2 * r]);
+      const float vv = fmaf(mb, xq.y, ma * xq.x);
       float &yv = r ? yacc[mt].y : yacc[mt].x;
-      yv = fmaf(us, fmaf(-dmin, vv, d * uu), yv);  // back from the 2^s scaled units
+      yv = fmaf(us, fmaf(dmn, vv, d * uu), yv);  // back from the 2^s scaled units
     }
   }
 }
@@ -201,15 +203,19 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
 // so that the super-block's largest magnitude lands in [2^14, 2^15) (the scaled
 // value is exact for every entry within 2^28 of that maximum), permuted so that
 // word 2G of a sub-block holds (x[4G], x[4G+2]) and word 2G+1 (x[4G+1],
-// x[4G+3]); the fp32 sums X_j of its scaled sub-blocks; unscale[i] = 2^-s_i.
-// Then 16 zero words.  Lane l handles values 8l .. 8l+7 of each super-block
-// (lanes 4j..4j+3 cover sub-block j); the loads of up to 8 super-blocks are all
-// issued before any of them is used.
+// x[4G+3]); xq[4 i + t] = (-1024 X_{2t}, -1024 X_{2t+1}, the same again), X_j
+// the sum of scaled sub-block j; unscale[i] = 2^-s_i.  Then 16 zero words.
+// Lane l handles values 8l .. 8l+7 of each super-block, i.e. lane (g, t) holds
+// a quarter of sub-block g -- exactly the B fragment of column g of an
+// m16n8k16 MMA, so two MMAs with every A entry -1024 produce -1024 X_n in
+// column n of every row, and lane (g, t) ends with the quad it needs.  The
+// loads of up to 8 super-blocks are all issued before any of them is used.
 // On entry xperm holds the raw bf16 slice (one bulk copy); each lane rewrites
 // only the 16 bytes it read.
-__device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float *xsum, float *unscale,
+__device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float4 *xq, float *unscale,
                                            uint32_t *xzero, int lane) {
   const uint4 *xs = reinterpret_cast<const uint4 *>(xperm);
+  constexpr uint32_t kNeg1024 = 0xE400E400u;  // fp16 -1024 in both halves
   constexpr int kChunk = 8;  // super-blocks in flight together (no early exit: full ILP)
   for (int base = 0; base < nsb; base += kChunk) {
     uint4 u[kChunk];
@@ -219,17 +225,15 @@ __device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float *xsum
       u[j] = (base + j < nsb) ? xs[(base + j) * 32 + lane] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
+    for (int j = 0; j < kChunk; ++j) {  // largest |x| as bf16 bits (sign cleared, 16-bit lanes)
       const uint4 v = u[j];
-      const uint32_t m01 = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
-      const uint32_t m23 = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
-      const uint32_t m45 = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
-      const uint32_t m67 = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
-      mx[j] = max(max(m01, m23), max(m45, m67));
+      const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                  __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+      mx[j] = max(m & 0xFFFFu, m >> 16);
     }
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) mx[j] = __reduce_max_sync(0xffffffffu, mx[j]);
-    float sum[kChunk];
+    float4 c[kChunk];
     int sh2[kChunk];
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
@@ -249,19 +253,16 @@ __device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float *xsum
       u[j].y = *reinterpret_cast<const uint32_t *>(&h13);
       u[j].z = *reinterpret_cast<const uint32_t *>(&h46);
       u[j].w = *reinterpret_cast<const uint32_t *>(&h57);
-      const float2 g02 = __half22float2(h02), g13 = __half22float2(h13);
-      const float2 g46 = __half22float2(h46), g57 = __half22float2(h57);
-      sum[j] = ((g02.x + g02.y) + (g13.x + g13.y)) + ((g46.x + g46.y) + (g57.x + g57.y));
+      float acc[4];
+      mma_f16_zc(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].x, u[j].y);
+      mma_f16(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].z, u[j].w);
+      c[j] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], 1);
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], 2);
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
       if (base + j < nsb) {
         reinterpret_cast<uint4 *>(xperm)[(base + j) * 32 + lane] = u[j];
-        if ((lane & 3) == 0) xsum[(base + j) * 8 + (lane >> 2)] = sum[j];
+        if (lane < 4) xq[(base + j) * 4 + lane] = c[j];  // g = 0: t = lane
         if (lane == 0) unscale[base + j] = __int_as_float((127 - sh2[j]) << 23);
       }
     }
@@ -328,9 +329,10 @@ __device__ __noinline__ void b1_drain_ring(uint64_t *bars, int stages, int it, i
 //   exactly sub-block n and thread t ends with sub-blocks 2t, 2t+1 of its rows.
 // Shared memory per warp: STAGES weight tiles (16*MT rows x S super-blocks,
 // row stride S*144 bytes) | x of the warp's slice, word 2G of a sub-block
-// holding (x[4G], x[4G+2]) and word 2G+1 (x[4G+1], x[4G+3]) | the fp32 sums X_j
-// of its sub-blocks | 2^-s_i of each super-block (padded to 16 bytes) | 64 zero
-// bytes | STAGES + 1 mbarriers (the ring, x).
+// holding (x[4G], x[4G+2]) and word 2G+1 (x[4G+1], x[4G+3]) | per super-block
+// four quads (-1024 X_{2t}, -1024 X_{2t+1}, the same again), t = 0..3 | 2^-s_i of
+// each super-block (padded to 16 bytes) | 64 zero bytes | STAGES + 1 mbarriers
+// (the ring, x).
 template <int MT, int S, int STAGES>
 __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const GemvArgs a) {
@@ -349,8 +351,8 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   uint8_t *wreg = smem + (size_t)warp * a.warp_bytes;
   uint8_t *ring = wreg;
   uint32_t *xperm = reinterpret_cast<uint32_t *>(wreg + STAGES * kStageBytes);  // ks*128 words
-  float *xsum = reinterpret_cast<float *>(xperm + a.ks * 128);
-  float *xuns = xsum + a.ks * 8;                           // ks floats, padded to 16 bytes
+  float4 *xq = reinterpret_cast<float4 *>(xperm + a.ks * 128);                   // ks*4 quads
+  float *xuns = reinterpret_cast<float *>(xq + a.ks * 4);  // ks floats, padded to 16 bytes
   uint32_t *xzero = reinterpret_cast<uint32_t *>(xuns + pad4(a.ks));            // 16 words
   uint64_t *bars = reinterpret_cast<uint64_t *>(xzero + 16);  // STAGES ring + 1 for x
   float *red = reinterpret_cast<float *>(smem + (size_t)nwarps * a.warp_bytes);
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   grid_launch_dependents();
   bool ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
   if (ok) {
-    b1_stage_x(nsteps, xperm, xsum, xuns, xzero, lane);
+    b1_stage_x(nsteps, xperm, xq, xuns, xzero, lane);
   } else if (lane == 0) {
     b1_drain_ring(bars, STAGES, 0, min(STAGES, nstages), &bars[STAGES]);
   }
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kF16Magic));
 
   uint32_t phase = 0;
-  const float2 *px = reinterpret_cast<const float2 *>(xsum) + t;
+  const float4 *pq = xq + t;
   for (int base = 0; base < nstages && ok; base += STAGES, phase ^= 1u) {
 #pragma unroll
     for (int stage = 0; stage < STAGES; ++stage) {
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
           }
         }
 
-        b1_super_block<MT>(hdr, qa, pe, po, px[4 * i], xuns[i], lc, magic, yacc);
+        b1_super_block<MT>(hdr, qa, pe, po, pq[4 * i], xuns[i], lc, magic, yacc);
         pe += adv_e;
         po += adv_o;
       }
@@ -698,7 +700,7 @@ struct Plan {
 };
 
 int warp_bytes_b1(int mt, int s, int stages, int ks) {
-  int b = stages * mt * s * kTileBytes + ks * (512 + 32) + 4 * pad4(ks) + 64 + (stages + 1) * 8;
+  int b = stages * mt * s * kTileBytes + ks * (512 + 64) + 4 * pad4(ks) + 64 + (stages + 1) * 8;
   return (b + 127) / 128 * 128;
 }
 int warp_bytes_bn(int mt) {
