@@ -222,7 +222,9 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
 def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
     """Same pass through the public API with host buffers, launched eagerly (no
     graph): each step copies all projections' x from one pinned host buffer to
-    the device (one copy), runs the 320 calls, and reads all y back (one copy)."""
+    the device (one copy), runs the 320 projections with one q4k_gemv_seq call
+    (programmatic dependent launch between them), and reads all y back (one
+    copy)."""
     kx = [k for _, _, k, _ in layers.mats]
     ny = [n for _, n, _, _ in layers.mats]
     host_x = torch.empty(batch * sum(kx), dtype=torch.bfloat16).pin_memory()
@@ -243,12 +245,12 @@ def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
         oy += batch * n
     h2d = host_x.numel() * 2
     d2h = host_y.numel() * 4
+    ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])
 
     def step():
         with torch.cuda.stream(stream):
             dev_x.copy_(host_x, non_blocking=True)
-            for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
-                q4k.q4k_gemv(w, n, k, x, out=y, stream=stream)
+            q4k.q4k_gemv_seq(ops, batch, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
             host_y.copy_(dev_y, non_blocking=True)
 
     for _ in range(max(warmup, 1)):

@@ -23,12 +23,20 @@ Q4K_BYTES = 144
 STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN",
           4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA"}
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
-EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex", "q4k_gemm",
+EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
+           "q4k_gemv_seq", "q4k_gemm",
            "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_moe_gemv_noalloc",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class GemvOp(ctypes.Structure):
+    """One entry of q4k_gemv_seq's op array (struct q4k_gemv_op)."""
+    _fields_ = [("w", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("y", ctypes.c_void_p),
+                ("ldy", ctypes.c_int64)]
 
 
 class Q4KError(RuntimeError):
@@ -57,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_gemv.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_gemv_ex.restype = ctypes.c_int
         L.q4k_gemv_ex.argtypes = [P, I64, I64, P, I64, I64, P, I64, ctypes.c_uint32, P]
+        L.q4k_gemv_seq.restype = ctypes.c_int
+        L.q4k_gemv_seq.argtypes = [ctypes.POINTER(GemvOp), I64, I64, ctypes.c_uint32, P]
         L.q4k_gemm.restype = ctypes.c_int
         L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
@@ -131,6 +141,25 @@ def q4k_gemv_ex(w: torch.Tensor, n: int, k: int, x: torch.Tensor, flags: int, ou
     _check(lib().q4k_gemv_ex(_ptr(w), n, k, _ptr(x2), batch, x2.stride(0), _ptr(out),
                              out.stride(0), flags, _stream(stream)), "q4k_gemv_ex")
     return out[0] if x.dim() == 1 else out
+
+
+def gemv_ops(ops) -> ctypes.Array:
+    """The op array of q4k_gemv_seq from (w, n, k, x, y) tuples: x [batch, K]
+    bf16 and y [batch, N] fp32 on the device.  The array holds raw pointers;
+    keep the tensors alive while it is used.  Build it once and reuse it."""
+    arr = (GemvOp * len(ops))()
+    for i, (w, n, k, x, y) in enumerate(ops):
+        x2 = x.unsqueeze(0) if x.dim() == 1 else x
+        y2 = y.unsqueeze(0) if y.dim() == 1 else y
+        arr[i] = GemvOp(_ptr(w), n, k, _ptr(x2), x2.stride(0), _ptr(y2), y2.stride(0))
+    return arr
+
+
+def q4k_gemv_seq(ops, batch: int, flags: int = 0, stream=None) -> None:
+    """Launch a sequence of projections in order (ops: gemv_ops(...) or a
+    list of (w, n, k, x, y) tuples), as q4k_gemv_ex for each in turn."""
+    arr = ops if isinstance(ops, ctypes.Array) else gemv_ops(ops)
+    _check(lib().q4k_gemv_seq(arr, len(arr), batch, flags, _stream(stream)), "q4k_gemv_seq")
 
 
 def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=None):

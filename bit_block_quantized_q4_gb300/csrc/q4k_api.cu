@@ -145,16 +145,32 @@ int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, v
   return map_launch(launch_dequant(w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
-int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
-                float *y, int64_t ldy, uint32_t flags, void *stream) {
+namespace {
+// Argument checks of one projection; Q4K_OK with *empty set when there is
+// nothing to compute.
+int check_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+               const float *y, int64_t ldy, uint32_t flags, bool *empty) {
+  *empty = false;
   if (n < 0 || k <= 0 || (k % kQK) != 0 || batch < 0 || batch > 16) return Q4K_ERR_SHAPE;
   if (n > INT32_MAX / 2 || k / kQK > INT32_MAX / kBlockBytes) return Q4K_ERR_SHAPE;
   if (flags & ~(uint32_t)Q4K_FLAG_OVERLAP_WEIGHTS) return Q4K_ERR_SHAPE;
-  if (n == 0 || batch == 0) return Q4K_OK;
+  if (n == 0 || batch == 0) {
+    *empty = true;
+    return Q4K_OK;
+  }
   if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
   if (!w || !x || !y) return Q4K_ERR_NULL;
   if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4) || (ldx % 8) != 0) return Q4K_ERR_ALIGN;
-  int st = check_device();
+  return Q4K_OK;
+}
+}  // namespace
+
+int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
+                float *y, int64_t ldy, uint32_t flags, void *stream) {
+  bool empty = false;
+  int st = check_gemv(w, n, k, x, batch, ldx, y, ldy, flags, &empty);
+  if (st != Q4K_OK || empty) return st;
+  st = check_device();
   if (st != Q4K_OK) return st;
   return map_launch(launch_gemv(w, n, k, x, batch, ldx, y, ldy,
                                 (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0,
@@ -164,6 +180,33 @@ int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batc
 int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
              float *y, int64_t ldy, void *stream) {
   return q4k_gemv_ex(w, n, k, x, batch, ldx, y, ldy, 0u, stream);
+}
+
+int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t flags,
+                 void *stream) {
+  if (count < 0) return Q4K_ERR_SHAPE;
+  if (count == 0) return Q4K_OK;
+  if (!ops) return Q4K_ERR_NULL;
+  bool any = false;
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    bool empty = false;
+    const int st = check_gemv(o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, flags, &empty);
+    if (st != Q4K_OK) return st;
+    any = any || !empty;
+  }
+  if (!any) return Q4K_OK;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    if (o.n == 0) continue;
+    st = map_launch(launch_gemv(o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, overlap,
+                                static_cast<cudaStream_t>(stream)));
+    if (st != Q4K_OK) return st;
+  }
+  return Q4K_OK;
 }
 
 int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx, void *y,

@@ -45,6 +45,17 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Same with C given separately (starts an accumulation at C).
+__device__ __forceinline__ void mma_bf16_c(float (&d)[4], const float (&c)[4], uint32_t a0,
+                                           uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
 // D = A * B + C, m16n8k16, fp16 operands, fp32 accumulate (same fragments).
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -84,6 +95,7 @@ __device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t
 // 128 + q for q < 16.  These turn the low nibbles of bytes 0 and 2 of a word
 // (or the nibbles selected by a prior shift) into a bf16 pair (128+q0, 128+q2).
 constexpr uint32_t kBf16Magic = 0x43004300u;
+constexpr uint32_t kBf16Neg128 = 0xC300C300u;  // bf16 -128 in both halves
 __device__ __forceinline__ uint32_t nib_lo(uint32_t w) { return (w & 0x000F000Fu) | kBf16Magic; }
 __device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
   return ((w >> 4) & 0x000F000Fu) | kBf16Magic;

@@ -573,7 +573,70 @@ __global__ void __launch_bounds__(256) gemv_bn_kernel(const __grid_constant__ CU
         dmA[mt][r] = dmin * (float)(m2 & 0xFFu) * (1.f / 128.f);
         dmB[mt][r] = dmin * (float)(m2 >> 8) * (1.f / 128.f);
       }
-    auto sub_block = [&](int j, const uint4(&xv)[NT]) {
+    auto sub_block_seeded = [&](int j, const uint4(&xv)[NT]) {
+      const int c = j >> 1;
+      const bool hi = j & 1;
+      uint32_t b0[2][NT], b1[2][NT];
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t lo = s ? xv[nt].z : xv[nt].x;
+          const uint32_t hi2 = s ? xv[nt].w : xv[nt].y;
+          b0[s][nt] = __byte_perm(lo, hi2, 0x5410);
+          b1[s][nt] = __byte_perm(lo, hi2, 0x7632);
+        }
+      // -128 X_j of every column by MMAs with A = -128 everywhere (every row
+      // holds it, so column 2t+e is cneg[nt][e]); the weight MMAs start there,
+      // so acc = sum (128 + q) x - 128 X_j = sum q x.
+      float cneg[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16_zc(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[0][nt], b1[0][nt]);
+        mma_bf16(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[1][nt], b1[1][nt]);
+      }
+      float acc[MT][NT][4];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t w0 = s ? qw[mt][0][c].y : qw[mt][0][c].x;
+          const uint32_t w1 = s ? qw[mt][1][c].y : qw[mt][1][c].x;
+          const uint32_t a0 = hi ? nib_hi(w0) : nib_lo(w0);
+          const uint32_t a1 = hi ? nib_hi(w1) : nib_lo(w1);
+          const uint32_t a2 = hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8);
+          const uint32_t a3 = hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (s == 0)
+              mma_bf16_c(acc[mt][nt], cneg[nt], a0, a1, a2, a3, b0[0][nt], b1[0][nt]);
+            else
+              mma_bf16(acc[mt][nt], a0, a1, a2, a3, b0[1][nt], b1[1][nt]);
+          }
+        }
+      }
+      // Scales of sub-block j for rows g, g+8 live in lane (g, j/2); dm
+      // carries the 1/128 of cneg and meets it with the sign folded in.
+      const int src = (lane & ~3) | (j >> 1);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mt][r] : dsA[mt][r], src);
+          const float dm = __shfl_sync(0xffffffffu, hi ? dmB[mt][r] : dmA[mt][r], src);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float &yv = yacc[mt][nt][2 * r + e];
+              yv = fmaf(ds, acc[mt][nt][2 * r + e], yv);
+              yv = fmaf(dm, cneg[nt][e], yv);
+            }
+          }
+        }
+      }
+    };
+    auto sub_block_plain = [&](int j, const uint4(&xv)[NT]) {
       const int c = j >> 1;
       const bool hi = j & 1;
       float acc[MT][NT][4];
@@ -629,6 +692,15 @@ __global__ void __launch_bounds__(256) gemv_bn_kernel(const __grid_constant__ CU
           }
         }
       }
+    };
+    // One column tile: the weight MMAs start at -128 X_j (seeded).  Two: the
+    // column sums run beside the weight MMAs instead, which measured faster
+    // there (the seeded chain is one MMA pair deeper and holds more registers).
+    auto sub_block = [&](int j, const uint4(&xv)[NT]) {
+      if constexpr (NT == 1)
+        sub_block_seeded(j, xv);
+      else
+        sub_block_plain(j, xv);
     };
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) sub_block(jj, xA[jj]);

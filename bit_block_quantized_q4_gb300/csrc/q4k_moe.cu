@@ -331,13 +331,14 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
             b1[nt][1] = __byte_perm(v.z, v.w, 0x7632);
           }
         }
-        // 128 X_j of every column by one more MMA per step (A = 128 everywhere):
-        // every row of c128 holds it, so column 2t+e is c128[nt][e].
-        float c128[NT][4];
+        // -128 X_j of every column by one more MMA per step (A = -128
+        // everywhere): every row of cneg holds it, so column 2t+e is
+        // cneg[nt][e].  The weight MMAs start there, so acc = sum q x.
+        float cneg[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16_zc(c128[nt], kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0[nt][0], b1[nt][0]);
-          mma_bf16(c128[nt], kBf16Magic, kBf16Magic, kBf16Magic, kBf16Magic, b0[nt][1], b1[nt][1]);
+          mma_bf16_zc(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[nt][0], b1[nt][0]);
+          mma_bf16(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[nt][1], b1[nt][1]);
         }
         const int srcl = (lane & ~3) | (jb >> 1);
 #pragma unroll
@@ -354,13 +355,13 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               if (s == 0)
-                mma_bf16_zc(acc[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
+                mma_bf16_c(acc[nt], cneg[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
               else
                 mma_bf16(acc[nt], a0, a1, a2, a3, b0[nt][1], b1[nt][1]);
             }
           }
-          // acc = sum (128 + q) x: subtract 128 X_j, apply d*sc; the min term
-          // takes X_j = c128 / 128 (the 1/128 is folded into dm).
+          // acc = sum q x: apply d*sc; the min term takes X_j = -cneg / 128
+          // (the 1/128 is folded into dm, the sign into the fma).
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mi][r] : dsA[mi][r], srcl);
@@ -369,10 +370,9 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const float c1 = c128[nt][e];
                 float &yv = yacc[mi][nt][2 * r + e];
-                yv = fmaf(ds, acc[nt][2 * r + e] - c1, yv);
-                yv = fmaf(-dm, c1, yv);
+                yv = fmaf(ds, acc[nt][2 * r + e], yv);
+                yv = fmaf(dm, cneg[nt][e], yv);
               }
           }
         }

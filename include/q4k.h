@@ -130,6 +130,34 @@ int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batc
                 float *y, int64_t ldy, uint32_t flags, void *stream);
 
 /*
+ * q4k_gemv_seq -- a sequence of decode projections launched in order on one
+ * stream by one call: the same as calling q4k_gemv_ex for ops[0], ops[1], ..
+ * in turn with the same batch, flags and stream.  A decode step runs every
+ * projection of every layer ("spec: specialized model runtimes", section
+ * "Development sequence": decode throughput is the metric); one call keeps the
+ * host cost per projection to the library's own launch path.
+ *   ops     host array of `count` q4k_gemv_op, read during the call only; each
+ *           op's w, n, k, x, ldx, y, ldy mean what they mean for q4k_gemv
+ *   count   >= 0 (0: nothing to do)
+ *   batch   1..16, shared by all ops
+ *   flags   as q4k_gemv_ex; Q4K_FLAG_OVERLAP_WEIGHTS applies to every launch
+ * Every op is checked before the first launch: on a NULL, SHAPE or ALIGN error
+ * nothing is launched.  A launch failure (CUDA) stops the sequence; the ops
+ * before it stay enqueued.
+ * Errors: NULL (also ops == NULL with count > 0), SHAPE, ALIGN, DEVICE, CUDA.
+ */
+typedef struct q4k_gemv_op {
+  const void *w;
+  int64_t n, k;
+  const void *x;
+  int64_t ldx;
+  float *y;
+  int64_t ldy;
+} q4k_gemv_op;
+int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t flags,
+                 void *stream);
+
+/*
  * q4k_gemm -- prefill projection, Y = X W^T for m tokens (any m >= 1).
  * ("spec: specialized model runtimes", section "Feasibility gate": one
  *  quantized GEMM; prefill throughput and TTFT are reported metrics in "PRD:

@@ -89,6 +89,29 @@ def test_gemv_argument_errors(L):
     assert L.q4k_gemv(P, 4, 256, P, 1, 256, P + 2, 4, None) == 3
 
 
+def test_gemv_seq_checks_every_op_before_launching(L):
+    from bit_block_quantized_q4_gb300 import GemvOp
+    good = GemvOp(P, 4, 256, P, 256, P, 4)
+    ops = (GemvOp * 3)(good, good, good)
+    assert L.q4k_gemv_seq(ops, 0, 1, 0, None) == 0          # nothing to do
+    assert L.q4k_gemv_seq(None, 3, 1, 0, None) == 1
+    assert L.q4k_gemv_seq(ops, -1, 1, 0, None) == 2
+    assert L.q4k_gemv_seq(ops, 3, 17, 0, None) == 2         # batch shared by all ops
+    assert L.q4k_gemv_seq(ops, 3, 1, 2, None) == 2          # unknown flag bit
+    # an error in the last op is found before anything is launched (a launch
+    # on this GPU-less machine would report the device instead)
+    for bad, status in ((GemvOp(None, 4, 256, P, 256, P, 4), 1),
+                        (GemvOp(P, 4, 300, P, 304, P, 4), 2),
+                        (GemvOp(P, 4, 256, P, 128, P, 4), 2),
+                        (GemvOp(P + 4, 4, 256, P, 256, P, 4), 3),
+                        (GemvOp(P, 4, 256, P, 256, P + 2, 4), 3)):
+        ops[2] = bad
+        assert L.q4k_gemv_seq(ops, 3, 1, 0, None) == status
+    # empty ops only: nothing to launch
+    ops[0] = ops[1] = ops[2] = GemvOp(P, 0, 256, P, 256, P, 4)
+    assert L.q4k_gemv_seq(ops, 3, 1, 0, None) == 0
+
+
 def test_gemm_argument_errors(L):
     assert L.q4k_gemm(P, 4, 100, P, 8, 104, P, 8, None) == 2
     assert L.q4k_gemm(P, 8, 256, P, -2, 256, P, 8, None) == 2

@@ -66,6 +66,31 @@ def test_gemv_many_row_tiles(q4k, n, k):
     check_bound(y0, yref, s, TOL, f"per-tile {n}x{k}")
 
 
+@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (4, 1), (16, 0)])
+def test_gemv_seq_matches_oracle_and_single_calls(q4k, batch, flags):
+    # one q4k_gemv_seq call over projections of different shapes (an empty one
+    # among them) equals the oracle, and equals q4k_gemv_ex called per op
+    shapes = [(700, 1280), (0, 512), (2048, 4096), (129, 5120), (4096, 2304)]
+    ws, xs, ys = [], [], []
+    for i, (n, k) in enumerate(shapes):
+        ws.append(synth.q4k_weight(max(n, 1), k, seed=3100 + i, quants="normal"))
+        xs.append(synth.bf16_normal((batch, k), seed=3200 + i))
+        ys.append(torch.full((batch, max(n, 1)), 7.0, device=DEV))
+    dw, dx = [w.to(DEV) for w in ws], [x.to(DEV) for x in xs]
+    ops = q4k.gemv_ops([(w, n, k, x, y) for w, (n, k), x, y in zip(dw, shapes, dx, ys)])
+    q4k.q4k_gemv_seq(ops, batch, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    for i, ((n, k), w, x, y) in enumerate(zip(shapes, ws, xs, ys)):
+        if n == 0:
+            assert bool((y == 7.0).all()), "an empty op writes nothing"
+            continue
+        yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+        check_bound(y.cpu().numpy(), yref, s, TOL, f"seq op {i} {n}x{k} b{batch}")
+        single = _run(q4k, w, n, k, x, flags)
+        assert np.array_equal(single, y.cpu().numpy()), f"seq op {i} differs from a single call"
+
+
 def test_gemv_overlap_chain_reads_the_previous_output(q4k):
     # y1 = W1 x0; x1 = bf16(y1) by a torch kernel; y2 = W2 x1, all queued on
     # one stream with programmatic dependent launch: the second projection
