@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  // Launched as a programmatic dependent of the previous kernel on the stream:
+  // everything above overlaps its tail; no thread touches global memory before
+  // that kernel has completed.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
@@ -326,12 +330,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ok = __all_sync(0xffffffffu, ok);  // a role loop that timed out ran on lane 0 only
   const bool acc_ready = ok && mbar_wait(accfull, 0u, a.err);
+  grid_launch_dependents();  // the next kernel's CTAs may take this SM as soon as it is free
   const int q = warp & 3;
   const int row = 32 * q + lane;  // weight row within the tile
   const int c_lo = (warp >> 2) * 4, c_hi = c_lo + 4;
   const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
   if (acc_ready) tc_fence_after();
   if constexpr (KS == 1) {
+    // The bf16 tile is staged as [token][row] in shared memory (idle now: all
+    // copies and MMAs are done) and then written as whole 256-byte token rows;
+    // stores straight from the lanes (one weight row each) write 64 contiguous
+    // bytes at a time and measured ~10x slower.
+    __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem);  // [kTokens][kBN]
     if (acc_ready) {
 #pragma unroll 1
       for (int sub = 0; sub < kSub; ++sub) {
@@ -341,14 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r0);
           tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c + 16), r1);
           tmem_ld_wait();
-          float v0[16], v1[16];
+          __nv_bfloat16 *col = stage + (128 * sub + 16 * c) * kBN + row;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            v0[e] = __uint_as_float(r0[e]);
-            v1[e] = __uint_as_float(r1[e]);
+            col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]));
+            col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]));
           }
-          store_y16_rows(a, m0 + 128 * sub + 16 * c, n0 + row, v0);
-          store_y16_rows(a, m0 + 128 * sub + 16 * c + 16, n0 + row, v1);
+        }
+      }
+    }
+    if (__syncthreads_and(acc_ready)) {
+      const int seg = threadIdx.x & 15;  // 16-byte segment of a token row
+      const int n = n0 + 8 * seg;
+      for (int tok = threadIdx.x >> 4; tok < kTokens && m0 + tok < a.m; tok += kThreads / 16) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + tok * kBN + 8 * seg);
+        __nv_bfloat16 *dst = a.y + (int64_t)(m0 + tok) * a.ldy + n;
+        if (n + 8 <= a.n) {
+          *reinterpret_cast<uint4 *>(dst) = v;
+        } else {
+          const __nv_bfloat16 *e8 = reinterpret_cast<const __nv_bfloat16 *>(&v);
+          for (int e = 0; e < 8 && n + e < a.n; ++e) dst[e] = e8[e];
         }
       }
     }
@@ -532,13 +554,17 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nt, (unsigned)mt, (unsigned)ks);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = (unsigned)ks;
+  // Programmatic dependent launch is safe for any caller: the kernel waits for
+  // the previous kernel before its first global access.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return gemm_go(cfg, cs, ks, xmap, wmap, args);
 }
 

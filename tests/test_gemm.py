@@ -120,3 +120,24 @@ def test_gemm_full_size_sampled(q4k, n, k):
     yref, s = oracle.gemv(wsub, len(rows), k, xbits(x))
     got = y[:, idx].float().cpu().numpy().astype(np.float64)
     check_bound(got, yref, s, TOL, f"full gemm {n}x{k}")
+
+
+def test_gemm_chain_reads_the_previous_output(q4k):
+    # Y1 = X0 W1^T and Y2 = Y1 W2^T queued back to back on one stream (the
+    # GEMM is launched as a programmatic dependent of the kernel before it):
+    # the second GEMM must see Y1 complete, so Y2 equals the same GEMM run on a
+    # copy of Y1 taken after a synchronize (the kernel is deterministic).
+    m, k0, n1, n2 = 700, 1024, 2048, 640
+    w1 = synth.q4k_weight(n1, k0, seed=41, quants="normal").to(DEV)
+    w2 = synth.q4k_weight(n2, n1, seed=42, quants="normal").to(DEV)
+    x0 = synth.bf16_normal((m, k0), seed=43, sigma=0.5).to(DEV)
+    for _ in range(3):
+        y1 = q4k.q4k_gemm(w1, n1, k0, x0)
+        y2 = q4k.q4k_gemm(w2, n2, n1, y1)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    y1c = y1.clone()
+    torch.cuda.synchronize()
+    ref = q4k.q4k_gemm(w2, n2, n1, y1c)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, ref)
