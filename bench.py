@@ -219,12 +219,13 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
             "bytes_per_step": nbytes, "launches_per_step": len(layers.mats)}
 
 
-def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
+def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream, groups=4):
     """Same pass through the public API with host buffers, launched eagerly (no
-    graph): each step copies all projections' x from one pinned host buffer to
-    the device (one copy), runs the 320 projections with one q4k_gemv_seq call
-    (programmatic dependent launch between them), and reads all y back (one
-    copy)."""
+    graph).  Every step copies all projections' x from pinned host memory to the
+    device and reads all y back; the layers run in `groups` groups, each with one
+    q4k_gemv_seq call (programmatic dependent launch between its projections).
+    The copies run on a second stream, ordered by events: group g starts once
+    its x has landed, and its y is copied back while group g+1 computes."""
     kx = [k for _, _, k, _ in layers.mats]
     ny = [n for _, n, _, _ in layers.mats]
     host_x = torch.empty(batch * sum(kx), dtype=torch.bfloat16).pin_memory()
@@ -236,22 +237,42 @@ def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
         off += batch * k
     dev_x = torch.empty_like(host_x, device=dev)
     dev_y = torch.empty_like(host_y, device=dev)
-    xs, ys = [], []
+    nmat = len(layers.mats)
+    bounds = [nmat * g // groups for g in range(groups + 1)]
+    ops, xr, yr = [], [], []
     ox = oy = 0
-    for k, n in zip(kx, ny):
-        xs.append(dev_x[ox:ox + batch * k].view(batch, k))
-        ys.append(dev_y[oy:oy + batch * n].view(batch, n))
-        ox += batch * k
-        oy += batch * n
+    for g in range(groups):
+        tup = []
+        x0, y0 = ox, oy
+        for (name, n, k, w) in layers.mats[bounds[g]:bounds[g + 1]]:
+            x = dev_x[ox:ox + batch * k].view(batch, k)
+            y = dev_y[oy:oy + batch * n].view(batch, n)
+            tup.append((w, n, k, x, y))
+            ox += batch * k
+            oy += batch * n
+        ops.append(q4k.gemv_ops(tup))
+        xr.append((x0, ox))
+        yr.append((y0, oy))
     h2d = host_x.numel() * 2
     d2h = host_y.numel() * 4
-    ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])
+    copy = torch.cuda.Stream(device=dev)
+    landed = [torch.cuda.Event() for _ in range(groups)]
+    done = [torch.cuda.Event() for _ in range(groups)]
 
     def step():
-        with torch.cuda.stream(stream):
-            dev_x.copy_(host_x, non_blocking=True)
-            q4k.q4k_gemv_seq(ops, batch, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
-            host_y.copy_(dev_y, non_blocking=True)
+        with torch.cuda.stream(copy):
+            for g in range(groups):
+                a, b = xr[g]
+                dev_x[a:b].copy_(host_x[a:b], non_blocking=True)
+                landed[g].record(copy)
+        for g in range(groups):
+            stream.wait_event(landed[g])
+            q4k.q4k_gemv_seq(ops[g], batch, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
+            done[g].record(stream)
+            copy.wait_event(done[g])
+            with torch.cuda.stream(copy):
+                a, b = yr[g]
+                host_y[a:b].copy_(dev_y[a:b], non_blocking=True)
 
     for _ in range(max(warmup, 1)):
         step()
@@ -259,6 +280,7 @@ def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream):
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
+    copy.synchronize()
     stream.synchronize()
     sec = (time.perf_counter() - t0) / steps
     nbytes = layers.algorithmic_bytes(batch)

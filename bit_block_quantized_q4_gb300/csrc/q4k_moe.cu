@@ -76,6 +76,11 @@ struct MoeArgs {
 
 // ---------------------------------------------------------------- 1. route
 __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
+  // Each of the four kernels is launched as a programmatic dependent of the
+  // kernel before it and waits for it before touching global memory, so only
+  // the launch latency overlaps.
+  grid_dependency_wait();
+  grid_launch_dependents();
   __shared__ int cnt[kMaxExperts];
   __shared__ int fill[kMaxExperts];
   __shared__ int start[kMaxExperts + 1];
@@ -434,6 +439,8 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const MoeArgs a, int nsb, int rows_total) {
   extern __shared__ __align__(128) uint8_t smem[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int slot = blockIdx.y;
   if (slot >= a.meta[0]) return;  // slot not in use
   const int np = a.slot_start[slot + 1] - a.slot_start[slot];
@@ -451,6 +458,8 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
 
 // ---------------------------------------------------------------- 4. combine
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int t = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= a.hidden) return;
@@ -464,6 +473,22 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 }
 
 std::once_flag g_moe_attr;
+
+// Launch as a programmatic dependent of the previous kernel on the stream.
+template <typename K, typename... Args>
+void launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 constexpr int kGuTiles = 2;  // gate/up: m-tiles per warp stream
 constexpr int kDnTiles = 4;  // down: m-tiles per warp stream
 
@@ -496,8 +521,8 @@ void launch_expert(int rows, int tiles_per_warp, int max_slots, const CUtensorMa
   const int per_cta = kMoeWarps * tiles_per_warp;
   const int base = (ntiles + per_cta - 1) / per_cta;  // CTAs of an 8-column slot
   dim3 grid((unsigned)(base * NT), (unsigned)max_slots);
-  moe_expert_kernel<NT, DOWN><<<grid, kMoeWarps * 32, expert_smem<NT, DOWN>(), stream>>>(
-      m0, m1, a, nsb, rows);
+  launch_pdl(moe_expert_kernel<NT, DOWN>, grid, kMoeWarps * 32, (size_t)expert_smem<NT, DOWN>(),
+             stream, m0, m1, a, nsb, rows);
 }
 
 CUresult expert_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int64_t stride,
@@ -556,7 +581,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
       expert_map(&md, w_down, hidden, ffn, expert_stride, n_experts) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  moe_route_kernel<<<1, 1024, 0, stream>>>(a);
+  launch_pdl(moe_route_kernel, dim3(1), 1024, 0, stream, a);
   const int max_slots = MoeLayout::max_slots(n_experts, P);
   const int cap = std::min(P, kSlotPairs);  // pairs per slot at most
   {  // gate/up: K = hidden, one column per pair
@@ -577,7 +602,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   }
   {
     dim3 grid((unsigned)((hidden + 255) / 256), (unsigned)n_tokens);
-    moe_combine_kernel<<<grid, 256, 0, stream>>>(a);
+    launch_pdl(moe_combine_kernel, grid, 256, 0, stream, a);
   }
   return cudaGetLastError();
 }
