@@ -390,22 +390,39 @@ def bench_moe(q4k, dev, stream, reps=20):
             "distinct_experts": distinct, "bytes": nbytes}
 
 
+KERNEL_SOURCES = ("q4k_gemv.cu", "q4k_device.cuh", "q4k_internal.h")
+
+
+def kernel_fingerprint(read=None) -> str:
+    """sha256 (16 hex digits) of the batch-1 GEMV's sources with comments and
+    whitespace removed: it changes when the compiled kernel can, not when a
+    comment does.  `read(name)` returns a source's text (default: the tree)."""
+    import hashlib
+    import re
+    if read is None:
+        base = os.path.join(ROOT, "bit_block_quantized_q4_gb300", "csrc")
+        read = lambda name: open(os.path.join(base, name)).read()  # noqa: E731
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        text = re.sub(r"/\*.*?\*/", " ", read(name), flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic():
     """Per-launch DRAM traffic of the batch-1 GEMV from the committed ncu summary
-    (profiles/gemv_b1_27b_layer.md), or None when the kernel source has changed
-    since the counters were taken."""
-    import hashlib
+    (profiles/gemv_b1_27b_layer.md), or None when the kernel's sources have
+    changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "gemv_b1_27b_layer.md")
-    src = os.path.join(ROOT, "bit_block_quantized_q4_gb300", "csrc", "q4k_gemv.cu")
     if not os.path.exists(path):
         return None
-    want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     vals = {}
     for line in open(path):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != want:
+    if vals.get("kernel_fingerprint_16") != kernel_fingerprint():
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

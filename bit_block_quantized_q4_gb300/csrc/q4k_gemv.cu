@@ -15,7 +15,8 @@
 // Batch 1 (fp16 operands): each warp copies its x slice into shared memory with
 // one bulk copy and converts it in place, per 256-value super-block, to fp16
 // scaled by a power of two 2^s (largest magnitude in [2^14, 2^15): exact for
-// every value within 2^28 of that maximum), plus the sums X_j.  A quant
+// every value within 2^28 of that maximum), plus -1024 X_j from two MMAs with a
+// constant A operand; the weight MMAs start their accumulators there.  A quant
 // becomes the fp16 value 1024+q (low nibble) or 1024+16q (high nibble) with
 // one LOP3.  The eight MMA columns carry the eight sub-blocks of a super-block
 // (column j of B holds x only in the k-slots that carry sub-block j), so one
@@ -24,9 +25,10 @@
 // contribution is multiplied by 2^-s before it joins the row sum.
 // Batch 2..16 (bf16 operands): a quant becomes the bf16 value 128+q (exact);
 // the MMA columns carry the batch rows (one or two n-tiles of 8); every
-// sub-block is its own 2-step accumulation, 128 X_j comes from the same MMA
-// path with a constant A = 128 (so an all-zero sub-block cancels exactly), and
-// the scales are shared within a thread quad by shuffles.  The x fragments are
+// sub-block is its own 2-step accumulation, -128 X_j comes from the same MMA
+// path with a constant A = -128 (so an all-zero sub-block cancels exactly; with
+// one column tile it seeds the weight MMAs), and the scales are shared within a
+// thread quad by shuffles.  The x fragments are
 // loaded from L2 half a super-block ahead of their use.
 //
 // Split-K: the warps of a CTA take consecutive super-block slices of the same
@@ -838,7 +840,9 @@ std::once_flag g_attr_once;
 // the busiest SM: ceil(CTAs / SMs) x warps per CTA x super-blocks per warp x
 // rows per warp x the per-row cost of the tile height (an MT = 2 warp spends
 // 0.72 of an MT = 1 warp's instructions per row: 269 vs 373 per 16-row tile,
-// measured), plus a penalty for fewer than 8 resident warps per SM (too little
+// measured when the weight was fitted; a forced-plan sweep of the current
+// kernel still favours these choices except for qkv, where one tile per warp
+// ran 7% faster and o 16% slower), plus a penalty for fewer than 8 resident warps per SM (too little
 // to hide latency).  (Splitting a tile's K further over a cluster of CTAs, with
 // the partials summed through distributed shared memory, balanced the SMs
 // better on paper but measured slower at every cluster size.)
