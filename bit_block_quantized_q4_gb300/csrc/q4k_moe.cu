@@ -489,8 +489,14 @@ void launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stre
   cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, kernel, args...);
 }
-constexpr int kGuTiles = 2;  // gate/up: m-tiles per warp stream
-constexpr int kDnTiles = 4;  // down: m-tiles per warp stream
+#ifndef Q4K_MOE_GU_TILES  // gate/up: m-tiles per warp stream
+#define Q4K_MOE_GU_TILES 2
+#endif
+#ifndef Q4K_MOE_DN_TILES  // down: m-tiles per warp stream
+#define Q4K_MOE_DN_TILES 4
+#endif
+constexpr int kGuTiles = Q4K_MOE_GU_TILES;
+constexpr int kDnTiles = Q4K_MOE_DN_TILES;
 
 template <int NT, bool DOWN>
 constexpr int expert_smem() {
