@@ -24,9 +24,15 @@
 //               bf16 and written in the 128-byte-swizzled K-major layout the MMA
 //               reads.
 // After the last k-block all eight warps drain TMEM (warp w: lane quarter
-// w % 4, half w / 4 of the columns), round to bf16 and store Y.
+// w % 4, half w / 4 of the columns) and round to bf16; the tile is staged as
+// [token][row] in the idle shared memory and written as whole token rows.
+// With split K the CTAs of a weight tile first push the partials of the column
+// chunks they do not own into the owners' shared memory (below).
+// The kernel is launched as a programmatic dependent of the kernel before it
+// and touches no global memory before that kernel has completed.
 // Stages are chained by mbarriers; every wait is bounded and reports a
-// timeout through the device error word instead of hanging.
+// timeout through the device error word instead of hanging; after a timeout
+// the CTA writes no Y.
 #include <algorithm>
 #include <mutex>
 

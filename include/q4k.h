@@ -169,6 +169,11 @@ int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t 
  *           aligned)
  *   y       device, m x N bf16, row stride ldy >= N (ldy multiple of 8, y 16-byte
  *           aligned)
+ * Stream order holds: the kernel is launched as a programmatic dependent of the
+ * kernel before it on `stream` (its set-up overlaps that kernel's tail) but
+ * reads X and W and writes Y only after that kernel has completed.  Should a
+ * bounded wait inside the kernel time out, the affected output tiles are left
+ * unwritten and q4k_get_device_error reports it.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
