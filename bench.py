@@ -475,8 +475,10 @@ def run_reference(args, rank, world):
     per_step = []
     nbytes = 0
     samples = []
+    # 1024 rows of each projection (23.6 MB of Q4_K per step): enough rows for
+    # the oracle's threads to stay busy, a few ms per step on the host cores.
     for pi, (name, n, k) in enumerate(LAYER_SHAPES):
-        nrows = 64
+        nrows = 1024
         w = synth.q4k_weight(nrows, k, seed=synth.derive_seed(SEED_C1, "w", 0, pi),
                              quants="normal").numpy()
         x = synth.bf16_normal((1, k), seed=synth.derive_seed(SEED_C1, "x", 1, pi))
@@ -496,11 +498,11 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": "27b_dense_layer_b1 (oracle sample: first 64 rows of each "
+            "config": {"workload": "27b_dense_layer_b1 (oracle sample: first 1024 rows of each "
                                    "projection of layer 0 per step)", "batch": 1},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
                              "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": "first 64 rows of each of the 5 projections of layer 0"},
+                             "sample": "first 1024 rows of each of the 5 projections of layer 0"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
