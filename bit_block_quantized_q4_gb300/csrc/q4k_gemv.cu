@@ -200,76 +200,73 @@ __device__ __forceinline__ void b1_super_block(const uint4 (&hdr)[MT][2], const 
   }
 }
 
-// Stage a warp's x slice (nsb super-blocks of bf16 x) for batch 1.  For each
-// super-block i: an fp16 copy of its 256 values scaled by 2^s_i, with s_i chosen
+// Stage super-blocks first .. first+count-1 (count <= C) of a warp's x slice
+// for batch 1.  For each super-block i: an fp16 copy of its 256 values scaled by 2^s_i, with s_i chosen
 // so that the super-block's largest magnitude lands in [2^14, 2^15) (the scaled
 // value is exact for every entry within 2^28 of that maximum), permuted so that
 // word 2G of a sub-block holds (x[4G], x[4G+2]) and word 2G+1 (x[4G+1],
 // x[4G+3]); xq[4 i + t] = (-1024 X_{2t}, -1024 X_{2t+1}, the same again), X_j
-// the sum of scaled sub-block j; unscale[i] = 2^-s_i.  Then 16 zero words.
+// the sum of scaled sub-block j; unscale[i] = 2^-s_i.
 // Lane l handles values 8l .. 8l+7 of each super-block, i.e. lane (g, t) holds
 // a quarter of sub-block g -- exactly the B fragment of column g of an
 // m16n8k16 MMA, so two MMAs with every A entry -1024 produce -1024 X_n in
 // column n of every row, and lane (g, t) ends with the quad it needs.  The
-// loads of up to 8 super-blocks are all issued before any of them is used.
+// loads of the chunk are all issued before any of them is used.
 // On entry xperm holds the raw bf16 slice (one bulk copy); each lane rewrites
 // only the 16 bytes it read.
-__device__ __forceinline__ void b1_stage_x(int nsb, uint32_t *xperm, float4 *xq, float *unscale,
-                                           uint32_t *xzero, int lane) {
+template <int C>
+__device__ __forceinline__ void b1_stage_chunk(int first, int count, uint32_t *xperm, float4 *xq,
+                                               float *unscale, int lane) {
   const uint4 *xs = reinterpret_cast<const uint4 *>(xperm);
   constexpr uint32_t kNeg1024 = 0xE400E400u;  // fp16 -1024 in both halves
-  constexpr int kChunk = 8;  // super-blocks in flight together (no early exit: full ILP)
-  for (int base = 0; base < nsb; base += kChunk) {
-    uint4 u[kChunk];
-    uint32_t mx[kChunk];
+  uint4 u[C];
+  uint32_t mx[C];
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      u[j] = (base + j < nsb) ? xs[(base + j) * 32 + lane] : make_uint4(0, 0, 0, 0);
-    }
+  for (int j = 0; j < C; ++j) {
+    u[j] = (j < count) ? xs[(first + j) * 32 + lane] : make_uint4(0, 0, 0, 0);
+  }
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {  // largest |x| as bf16 bits (sign cleared, 16-bit lanes)
-      const uint4 v = u[j];
-      const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                  __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-      mx[j] = max(m & 0xFFFFu, m >> 16);
-    }
+  for (int j = 0; j < C; ++j) {  // largest |x| as bf16 bits (sign cleared, 16-bit lanes)
+    const uint4 v = u[j];
+    const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    mx[j] = max(m & 0xFFFFu, m >> 16);
+  }
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) mx[j] = __reduce_max_sync(0xffffffffu, mx[j]);
-    float4 c[kChunk];
-    int sh2[kChunk];
+  for (int j = 0; j < C; ++j) mx[j] = __reduce_max_sync(0xffffffffu, mx[j]);
+  float4 c[C];
+  int sh2[C];
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const uint4 v = u[j];
-      const int emax = mx[j] ? (int)(mx[j] >> 7) - 127 : 0;  // exponent of the largest |x|
-      sh2[j] = min(126, max(-126, 14 - emax));
-      const float scale = __int_as_float((127 + sh2[j]) << 23);
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
-      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z));
-      const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.w));
-      const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
-      const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
-      const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
-      const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
-      u[j].x = *reinterpret_cast<const uint32_t *>(&h02);
-      u[j].y = *reinterpret_cast<const uint32_t *>(&h13);
-      u[j].z = *reinterpret_cast<const uint32_t *>(&h46);
-      u[j].w = *reinterpret_cast<const uint32_t *>(&h57);
-      float acc[4];
-      mma_f16_zc(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].x, u[j].y);
-      mma_f16(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].z, u[j].w);
-      c[j] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
+  for (int j = 0; j < C; ++j) {
+    const uint4 v = u[j];
+    const int emax = mx[j] ? (int)(mx[j] >> 7) - 127 : 0;  // exponent of the largest |x|
+    sh2[j] = min(126, max(-126, 14 - emax));
+    const float scale = __int_as_float((127 + sh2[j]) << 23);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z));
+    const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.w));
+    const __half2 h02 = __floats2half2_rn(f0.x * scale, f1.x * scale);  // x0, x2
+    const __half2 h13 = __floats2half2_rn(f0.y * scale, f1.y * scale);  // x1, x3
+    const __half2 h46 = __floats2half2_rn(f2.x * scale, f3.x * scale);  // x4, x6
+    const __half2 h57 = __floats2half2_rn(f2.y * scale, f3.y * scale);  // x5, x7
+    u[j].x = *reinterpret_cast<const uint32_t *>(&h02);
+    u[j].y = *reinterpret_cast<const uint32_t *>(&h13);
+    u[j].z = *reinterpret_cast<const uint32_t *>(&h46);
+    u[j].w = *reinterpret_cast<const uint32_t *>(&h57);
+    float acc[4];
+    mma_f16_zc(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].x, u[j].y);
+    mma_f16(acc, kNeg1024, kNeg1024, kNeg1024, kNeg1024, u[j].z, u[j].w);
+    c[j] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      if (base + j < nsb) {
-        reinterpret_cast<uint4 *>(xperm)[(base + j) * 32 + lane] = u[j];
-        if (lane < 4) xq[(base + j) * 4 + lane] = c[j];  // g = 0: t = lane
-        if (lane == 0) unscale[base + j] = __int_as_float((127 - sh2[j]) << 23);
-      }
+  for (int j = 0; j < C; ++j) {
+    if (j < count) {
+      reinterpret_cast<uint4 *>(xperm)[(first + j) * 32 + lane] = u[j];
+      if (lane < 4) xq[(first + j) * 4 + lane] = c[j];  // g = 0: t = lane
+      if (lane == 0) unscale[first + j] = __int_as_float((127 - sh2[j]) << 23);
     }
   }
-  if (lane < 16) xzero[lane] = 0u;
   __syncwarp();
 }
 
@@ -391,8 +388,26 @@ __global__ void __launch_bounds__(256) gemv_b1_kernel(const __grid_constant__ CU
   }
   grid_launch_dependents();
   bool ok = nsteps == 0 || mbar_wait(&bars[STAGES], 0, a.err);
+  // The whole slice is converted before the main loop, in chunks of 8
+  // super-blocks and a last chunk of the smallest size in {1, 2, 4, 8} that
+  // covers the rest: a chunk's slots all do the full work, and a chunk of 8
+  // for 2 super-blocks made the 4096 x 4096 projection 9% slower.  (Converting
+  // a chunk one step ahead inside the main loop instead measured 1-3% slower
+  // on the 27B-class shapes.)
   if (ok) {
-    b1_stage_x(nsteps, xperm, xq, xuns, xzero, lane);
+    int b = 0;
+    for (; nsteps - b > 8; b += 8) b1_stage_chunk<8>(b, 8, xperm, xq, xuns, lane);
+    const int rest = nsteps - b;
+    if (rest > 4)
+      b1_stage_chunk<8>(b, rest, xperm, xq, xuns, lane);
+    else if (rest > 2)
+      b1_stage_chunk<4>(b, rest, xperm, xq, xuns, lane);
+    else if (rest == 2)
+      b1_stage_chunk<2>(b, rest, xperm, xq, xuns, lane);
+    else if (rest == 1)
+      b1_stage_chunk<1>(b, rest, xperm, xq, xuns, lane);
+    if (lane < 16) xzero[lane] = 0u;
+    __syncwarp();
   } else if (lane == 0) {
     b1_drain_ring(bars, STAGES, 0, min(STAGES, nstages), &bars[STAGES]);
   }
