@@ -465,6 +465,25 @@ def run_case(case):
     print(f"case {case} ok")
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of the ranks' values (every rank gets it); the value itself
+    when there is one rank.  Works on the gloo (CPU tensor) and nccl (device
+    tensor) backends."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_gbs(bytes_per_rank_step: float, ms_max: float, world: int) -> float:
+    """Whole-job GB/s of `world` replicas that each move `bytes_per_rank_step`
+    per step, timed by the slowest rank."""
+    return bytes_per_rank_step * world / (ms_max * 1e-3) / 1e9
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle as it stands, on the host cores, on a
     bounded sample of the headline workload per step."""
@@ -557,22 +576,18 @@ def main():
     torch.cuda.synchronize()
     with nvtx("decode_b1 pass (timed)"):
         head = bench_decode(q4k, layers, 1, args.steps, args.warmup, dev, stream, sampler)
-    ms = head["ms_per_step"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(head["ms_per_step"], world)
     assert q4k.q4k_get_device_error(stream) == 0
     pk = peaks()
     nbytes = head["bytes_per_step"]
-    achieved = nbytes / (ms * 1e-3) / 1e9
-    total_value = achieved * world
+    achieved = nbytes / (ms * 1e-3) / 1e9  # per GPU, by the slowest rank
+    total_value = replicas_gbs(nbytes, ms, world)
     launches = head["launches_per_step"]
 
     with nvtx("decode_b1 pass e2e"):
         e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
-    e2e["value"] = round(e2e["value"] * world, 2)
+    e2e["ms_per_step"] = round(max_over_ranks(e2e["ms_per_step"], world), 4)
+    e2e["value"] = round(replicas_gbs(layers.algorithmic_bytes(1), e2e["ms_per_step"], world), 2)
 
     cpu = cpu_baseline(layers) if rank == 0 else None
     extra = {}
