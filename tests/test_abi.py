@@ -160,3 +160,43 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q4k, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         q4k.lib()
+
+
+def test_header_compiles_as_c99_and_a_c_program_links(L, tmp_path):
+    # The boundary is a plain C ABI: a C99 program that calls every entry point
+    # compiles warning-free against include/q4k.h and links against libq4k.so
+    # (it is only built here, not run: running needs a GPU).
+    import shutil
+    import subprocess
+    import bit_block_quantized_q4_gb300 as q4k
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_q4k.c"
+    src.write_text(r'''
+#include "q4k.h"
+#include <stdio.h>
+int main(void) {
+  q4k_gemv_op ops[1] = {{0, 4, 256, 0, 256, 0, 4}};
+  uint32_t bits = 0;
+  int st = q4k_abi_version() == Q4K_ABI_VERSION ? Q4K_OK : -1;
+  st |= q4k_dequant(0, 4, 256, 0, 0, 0);
+  st |= q4k_gemv(0, 4, 256, 0, 1, 256, 0, 4, 0);
+  st |= q4k_gemv_ex(0, 4, 256, 0, 1, 256, 0, 4, Q4K_FLAG_OVERLAP_WEIGHTS, 0);
+  st |= q4k_gemv_seq(ops, 1, 1, 0u, 0);
+  st |= q4k_gemm(0, 4, 256, 0, 1, 256, 0, 8, 0);
+  st |= (int)q4k_moe_workspace_size(8, 1, 2, 256, 256);
+  st |= q4k_moe_gemv(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0, 0, 0);
+  st |= q4k_moe_gemv_noalloc(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0);
+  st |= q4k_get_device_error(0, &bits);
+  st |= q4k_selftest_wait_timeout(0);
+  printf("%s %d\n", q4k_status_str(st), st);
+  return 0;
+}
+''')
+    exe = tmp_path / "use_q4k"
+    lib_dir = os.path.dirname(q4k.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", lib_dir, "-lq4k", "-Wl,-rpath," + lib_dir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
