@@ -21,7 +21,6 @@ __device__ unsigned int g_device_error = 0u;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 DeviceFacts g_facts[kMaxDevices];
 std::once_flag g_facts_once[kMaxDevices];
 unsigned *g_err_ptr[kMaxDevices];

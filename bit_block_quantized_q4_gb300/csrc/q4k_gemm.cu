@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-std::once_flag g_gemm_attr;
+std::once_flag g_gemm_attr[kMaxDevices];  // cudaFuncSetAttribute acts on the current device
 
 template <int CS, int KS>
 void gemm_allow() {
@@ -516,7 +516,7 @@ cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &
 
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream) {
-  std::call_once(g_gemm_attr, gemm_attributes);
+  std::call_once(g_gemm_attr[device_facts()->device], gemm_attributes);
   const int nsb = (int)(k / kQK);
   CUtensorMap xmap, wmap;
   {

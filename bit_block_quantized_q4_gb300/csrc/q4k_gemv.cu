@@ -848,7 +848,7 @@ Plan plan_for(K kernel, bool b1, int mt, int s, int stages, int n, int nsb, int 
   return best;
 }
 
-std::once_flag g_attr_once;
+std::once_flag g_attr_once[kMaxDevices];  // cudaFuncSetAttribute acts on the current device
 
 // Batch-1 plan.  A row tile's K is split over the wk warps of its CTA.  Every
 // CTA must be resident at once; among those plans take the smallest load of
@@ -1014,7 +1014,7 @@ Plan cached_plan(const PlanKey &key, F compute) {
 cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
                         int64_t ldx, float *y, int64_t ldy, bool overlap, cudaStream_t stream) {
   const DeviceFacts *f = device_facts();
-  std::call_once(g_attr_once, set_attributes, f);
+  std::call_once(g_attr_once[f->device], set_attributes, f);
   const int nsb = (int)(k / kQK);
 
   // W viewed as [n rows][nsb super-blocks][144 bytes]; one box = 16*mt rows

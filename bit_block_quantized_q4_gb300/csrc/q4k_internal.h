@@ -10,6 +10,9 @@
 
 namespace q4k {
 
+// Devices the per-device tables below cover (device ordinals 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
 struct DeviceFacts {
   int device = -1;
   int major = 0, minor = 0;
@@ -19,7 +22,9 @@ struct DeviceFacts {
   int l2_bytes = 0;
 };
 
-// Facts of the current device (queried once per device).
+// Facts of the current device (queried once per device).  Kernel attributes
+// (shared-memory opt-in) are per device as well: each launcher sets them once
+// per device ordinal, device_facts()->device.
 const DeviceFacts *device_facts();
 
 // Device address of the current device's error word (Q4K_DEVERR_* bits).

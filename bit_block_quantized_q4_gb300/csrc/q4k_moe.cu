@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   a.y[(int64_t)t * a.ldy + i] = acc;
 }
 
-std::once_flag g_moe_attr;
+std::once_flag g_moe_attr[kMaxDevices];  // cudaFuncSetAttribute acts on the current device
 
 // Launch as a programmatic dependent of the previous kernel on the stream.
 template <typename K, typename... Args>
@@ -554,7 +554,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
                        cudaStream_t stream) {
   if (n_experts > kMaxExperts) return cudaErrorInvalidValue;
-  std::call_once(g_moe_attr, moe_attributes);
+  std::call_once(g_moe_attr[device_facts()->device], moe_attributes);
   const int P = n_tokens * top_k;
   const MoeLayout L(n_experts, P, hidden, ffn);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -630,7 +630,7 @@ namespace {
 
 void *g_scratch_ptr[64];
 cudaError_t g_scratch_status[64];
-std::once_flag g_scratch_once[64];
+std::once_flag g_scratch_once[kMaxDevices];
 
 // Host code may not use g_moe_scratch as an address (it names a host-side
 // stand-in); the device address is resolved once per device, with that device
@@ -651,7 +651,7 @@ cudaError_t launch_moe_scratch(const void *w_gate, const void *w_up, const void 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::call_once(g_scratch_once[dev], resolve_scratch, dev);
   if (g_scratch_ptr[dev] == nullptr) return g_scratch_status[dev];
   return launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x, n_tokens, ldx,
