@@ -67,6 +67,7 @@ def _load():
         lib.oracle_dequant_bf16.argtypes = [P, I64, I64, P]
         lib.oracle_gemv_bf16.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P]
         lib.oracle_gemv_f64.argtypes = [P, I64, I64, P, I64, I64, ctypes.c_int, P]
+        lib.oracle_gemv_glu.argtypes = [P, P, I64, I64, P, I64, I64, P, P, P, P, P]
         lib.oracle_moe.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32,
                                    P, P, P, P]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -192,6 +193,21 @@ def gemv_f64(w, n: int, k: int, x, use_abs: bool = False) -> np.ndarray:
     y = np.empty((xv.shape[0], n), np.float64)
     _load().oracle_gemv_f64(_ptr(a), n, k, _ptr(xv), xv.shape[0], k, 1 if use_abs else 0, _ptr(y))
     return y
+
+
+def gemv_glu(w_gate, w_up, n: int, k: int, x_bf16):
+    """Fused gate/up (oracle_gemv_glu): returns (h, g, u, sg, su), each
+    [batch, n] fp64: h = silu(g) * u, g = Wg x, u = Wu x, sg = |Wg||x|,
+    su = |Wu||x|."""
+    a = _check_w(w_gate, n, k)
+    b = _check_w(w_up, n, k)
+    x = np.ascontiguousarray(np.atleast_2d(np.asarray(x_bf16, dtype=np.uint16)))
+    assert x.shape[1] == k
+    batch = x.shape[0]
+    outs = [np.empty((batch, n), np.float64) for _ in range(5)]
+    if n:
+        _load().oracle_gemv_glu(_ptr(a), _ptr(b), n, k, _ptr(x), batch, k, *(_ptr(o) for o in outs))
+    return tuple(outs)
 
 
 def moe(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,

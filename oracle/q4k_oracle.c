@@ -228,6 +228,47 @@ void oracle_gemv_f64(const uint8_t *w, int64_t n, int64_t k, const double *x, in
 }
 
 /*
+ * Fused gate/up projection of a dense or shared-expert FFN ("Layer Package
+ * Repository Spec", section "Policy Resolution": the merged shared gate/up and
+ * the SwiGLU of the FFN; section "Execution Policy": merged shared gate/up):
+ *     g = sum_k wg[r, k] x[b, k],  u = sum_k wu[r, k] x[b, k]   (fp64)
+ *     h[b, r] = silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ * for bf16 activations x (batch rows, row stride ldx).  Outputs are
+ * [batch x n]; g, u, sg = sum_k |wg||x| and su = sum_k |wu||x| may be NULL.
+ */
+void oracle_gemv_glu(const uint8_t *wg, const uint8_t *wu, int64_t n, int64_t k,
+                     const uint16_t *x, int64_t batch, int64_t ldx, double *h, double *g_out,
+                     double *u_out, double *sg_out, double *su_out) {
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(batch * k));
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t i = 0; i < k; ++i) xd[b * k + i] = oracle_bf16_to_f64(x[b * ldx + i]);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n; ++r) {
+        double *wgr = (double *)malloc(sizeof(double) * (size_t)k);
+        double *wur = (double *)malloc(sizeof(double) * (size_t)k);
+        dequant_row_f64(wg, k, r, wgr);
+        dequant_row_f64(wu, k, r, wur);
+        for (int64_t b = 0; b < batch; ++b) {
+            double g = 0.0, u = 0.0, sg = 0.0, su = 0.0;
+            for (int64_t i = 0; i < k; ++i) {
+                g += wgr[i] * xd[b * k + i];
+                u += wur[i] * xd[b * k + i];
+                sg += fabs(wgr[i]) * fabs(xd[b * k + i]);
+                su += fabs(wur[i]) * fabs(xd[b * k + i]);
+            }
+            h[b * n + r] = g / (1.0 + exp(-g)) * u;
+            if (g_out) g_out[b * n + r] = g;
+            if (u_out) u_out[b * n + r] = u;
+            if (sg_out) sg_out[b * n + r] = sg;
+            if (su_out) su_out[b * n + r] = su;
+        }
+        free(wgr);
+        free(wur);
+    }
+    free(xd);
+}
+
+/*
  * Routed mixture-of-experts FFN for decode tokens ("Layer Package Repository
  * Spec", section "Policy Resolution": the routed gate/up/down expert matmuls,
  * the fused SwiGLU and the route-weighted sum of a routed FFN decode layer).

@@ -240,6 +240,78 @@ def test_gemv_row_subset_matches_full():
     assert np.array_equal(ys, y[:, rows]) and np.array_equal(ss, s[:, rows])
 
 
+def test_gemv_f64_abs_branch_matches_library():
+    # oracle_gemv_f64 with use_abs: |W| x, the scale of the MoE error bounds.
+    # Against numpy on the oracle's exact weights (pinned above); a dropped
+    # fabs would give W |x| instead, which differs on rows with mixed signs.
+    n, k = 13, 512
+    w = synth.q4k_weight(n, k, seed=31).numpy()
+    wq = oracle.dequant_f64(w, n, k)
+    xa = np.abs(np.random.default_rng(32).standard_normal((3, k)))
+    got = oracle.gemv_f64(w, n, k, xa, use_abs=True)
+    assert np.allclose(got, xa @ np.abs(wq).T, rtol=1e-12, atol=0)
+    plain = oracle.gemv_f64(w, n, k, xa)
+    assert np.all(np.abs(plain - xa @ wq.T) <= 1e-12 * (xa @ np.abs(wq).T))
+    assert np.all(got > np.abs(plain))      # mixed-sign rows: |W||x| > |W x|
+
+
+def _cancel_fields(rng, sc_c_m=((2, 4, 4), (6, 7, 21), (8, 15, 60), (14, 9, 63), (5, 0, 0))):
+    """Block fields whose weights are all exactly zero: d = 2^-6, dmin = 2^-5,
+    and in every sub-block q = c with d sc c = dmin m (sc c = 2 m)."""
+    picks = [sc_c_m[int(i)] for i in rng.integers(0, len(sc_c_m), 8)]
+    sc = [p[0] for p in picks]
+    m = [p[2] for p in picks]
+    q = [picks[i // 32][1] for i in range(256)]
+    return half_bits(2.0 ** -6), half_bits(2.0 ** -5), sc, m, q
+
+
+def test_cancelling_blocks_are_exactly_zero():
+    rng = np.random.default_rng(33)
+    rows = [b"".join(pack_block(*_cancel_fields(rng)) for _ in range(2)) for _ in range(3)]
+    w = np.frombuffer(b"".join(rows), np.uint8)
+    assert np.all(oracle.dequant_f64(w, 3, 512) == 0.0)
+    for fields in (_cancel_fields(rng) for _ in range(4)):
+        assert all(v == 0 for v in exact_weights(*fields))
+    y, s = oracle.gemv(w, 3, 512, _x_bits(synth.bf16_normal((2, 512), seed=34)))
+    assert np.all(y == 0.0) and np.all(s == 0.0)
+
+
+# ---------------------------------------------------------------- fused gate/up
+
+def test_glu_is_silu_of_gate_times_up():
+    # against two oracle GEMVs (pinned above) and the logistic function of a
+    # library; x small enough that g lies in SiLU's curved region
+    from scipy.special import expit
+    n, k, batch = 23, 768, 3
+    wg = synth.q4k_weight(n, k, seed=35).numpy()
+    wu = synth.q4k_weight(n, k, seed=36).numpy()
+    x = _x_bits(synth.bf16_normal((batch, k), seed=37, sigma=0.02))
+    h, g, u, sg, su = oracle.gemv_glu(wg, wu, n, k, x)
+    g2, sg2 = oracle.gemv(wg, n, k, x)
+    u2, su2 = oracle.gemv(wu, n, k, x)
+    assert np.array_equal(g, g2) and np.array_equal(u, u2)
+    assert np.array_equal(sg, sg2) and np.array_equal(su, su2)
+    assert np.allclose(h, g2 * expit(g2) * u2, rtol=1e-13, atol=0)
+    assert np.abs(g).min() < 4.0 and np.abs(g).max() > 0.1   # the curved region is exercised
+
+
+def test_glu_zero_gate_gives_exact_zero_and_large_gate_gives_up():
+    # gate rows of zero weights: silu(0) = 0; gate rows of one large positive
+    # weight against x = e_0: silu(g) = g (1 - O(e^-g)), so h = g u
+    rng = np.random.default_rng(38)
+    k = 256
+    zero = pack_block(0, 0, [1] * 8, [0] * 8, [0] * 256)
+    big = pack_block(half_bits(1.0), 0, [63] * 8, [0] * 8, [15] + [0] * 255)   # w_0 = 945
+    up_blocks = [pack_block(*random_fields(rng)) for _ in range(2)]
+    wg = np.frombuffer(zero + big, np.uint8)
+    wu = np.frombuffer(b"".join(up_blocks), np.uint8)
+    x = torch.zeros((1, k), dtype=torch.bfloat16)
+    x[0, 0] = 1.0
+    h, g, u, _, _ = oracle.gemv_glu(wg, wu, 2, k, _x_bits(x))
+    assert h[0, 0] == 0.0 and g[0, 0] == 0.0
+    assert g[0, 1] == 945.0 and h[0, 1] == 945.0 * u[0, 1]
+
+
 # ---------------------------------------------------------------- MoE
 
 def _moe_case(E=4, H=256, F=512, T=3, K=2, seed=20):
