@@ -198,15 +198,18 @@ def time_graph(fn, steps, warmup, stream):
 
 
 def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, overlap=True):
-    """One pass = the 320 projections back to back, captured in a CUDA graph.
-    With `overlap` each projection may start streaming its (static) weights
-    while the previous one finishes (Q4K_FLAG_OVERLAP_WEIGHTS)."""
+    """One pass = the 320 projections as one q4k_gemv_seq call (at batch 1 one
+    persistent launch that streams all 13 GB of weights back to back; at batch
+    4/16 one launch per projection), captured in a CUDA graph.  With `overlap`
+    a launch may start streaming its (static) weights while the previous one
+    finishes (Q4K_FLAG_OVERLAP_WEIGHTS).  After timing, sampled rows of the last
+    replay are checked against the oracle."""
     xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
     flags = q4k.Q4K_FLAG_OVERLAP_WEIGHTS if overlap else 0
+    ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])
 
     def step():
-        for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
-            q4k.q4k_gemv_ex(w, n, k, x, flags, out=y, stream=stream)
+        q4k.q4k_gemv_seq(ops, batch, flags, stream=stream)
 
     if sampler is not None:
         with sampler:
@@ -215,8 +218,33 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
         ms, per, g = time_graph(step, steps, warmup, stream)
     del g
     nbytes = layers.algorithmic_bytes(batch)
+    launches = (len(layers.mats) + 511) // 512 if batch == 1 else len(layers.mats)
     return {"ms_per_step": ms, "ms_min": min(per), "gbs": nbytes / (ms * 1e-3) / 1e9,
-            "bytes_per_step": nbytes, "launches_per_step": len(layers.mats)}
+            "bytes_per_step": nbytes, "launches_per_step": launches,
+            "verified": verify_decode(layers, xs, ys)}
+
+
+def verify_decode(layers, xs, ys, n_ops=5, rows=24, tol=2e-3):
+    """Sampled rows of sampled projections against the oracle, within the
+    fp32-path bound 2e-3 sum |w||x|; returns the worst error / bound ratio
+    (raises if any element is outside)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(2027)
+    worst = 0.0
+    picks = rng.choice(len(layers.mats), min(n_ops, len(layers.mats)), replace=False)
+    for i in sorted(int(p) for p in picks):
+        name, n, k, w = layers.mats[i]
+        ri = np.unique(np.concatenate([rng.choice(n, rows, replace=False), [0, n - 1]]))
+        rt = torch.from_numpy(ri).to(w.device)
+        xb = xs[i].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        yref, sref = oracle.gemv(w[rt].cpu().numpy(), len(ri), k, xb)
+        got = ys[i][:, rt].cpu().numpy().astype(np.float64)
+        err = np.abs(got - yref)
+        if not np.all(err <= tol * sref):
+            raise AssertionError(f"bench result check failed: op {i} ({name})")
+        worst = max(worst, float(np.max(err / (tol * sref))))
+    return round(worst, 4)
 
 
 def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream, groups=4):
@@ -289,8 +317,9 @@ def bench_decode_e2e(q4k, layers, batch, steps, warmup, dev, stream, groups=4):
 
 
 def bench_c0_pool(q4k, steps, warmup, dev, stream):
-    """4096x4096 single GEMV at batch 1 over a rotating pool of distinct matrices
-    (pool >> L2, so every call streams its weights from HBM)."""
+    """4096x4096 GEMV at batch 1 over a pool of distinct matrices (pool >> L2,
+    so every matrix streams its weights from HBM), run as one q4k_gemv_seq call;
+    also the time of one q4k_gemv call on one matrix (latency, L2-cold)."""
     n = k = 4096
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool = max(32, int(4 * l2 // q4k_bytes(n, k)) + 1)
@@ -299,14 +328,68 @@ def bench_c0_pool(q4k, steps, warmup, dev, stream):
     x = synth.bf16_normal((1, k), seed=1000, device=dev)
     ys = [torch.empty((1, n), device=dev) for _ in range(pool)]
 
-    def step():  # static weights: each call may stream them while the previous one runs
-        for w, y in zip(ws, ys):
-            q4k.q4k_gemv_ex(w, n, k, x, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, out=y, stream=stream)
+    ops = q4k.gemv_ops([(w, n, k, x, y) for w, y in zip(ws, ys)])
+
+    def step():  # the pool as one sequence: one persistent launch streams every matrix
+        q4k.q4k_gemv_seq(ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
 
     ms, per, g = time_graph(step, steps, warmup, stream)
     del g
     nbytes = pool * (q4k_bytes(n, k) + k * 2 + n * 4)
-    return {"pool": pool, "us_per_gemv": ms * 1e3 / pool, "gbs": nbytes / (ms * 1e-3) / 1e9}
+
+    def single():  # one matrix per call, a different one each call (graph of the pool)
+        for w, y in zip(ws, ys):
+            q4k.q4k_gemv_ex(w, n, k, x, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, out=y, stream=stream)
+
+    ms1, _, g1 = time_graph(single, max(3, steps // 2), 2, stream)
+    del g1
+    return {"pool": pool, "us_per_gemv": ms * 1e3 / pool, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "us_per_single_call": ms1 * 1e3 / pool}
+
+
+def bench_glu(q4k, dev, stream, steps, warmup, n_layers=N_LAYERS, batch=1):
+    """Fused gate/up (F1) on the 27B-class FFN: 64 layers of a 5120 -> 17408
+    gate/up pair (6.4 GB), each as one fused op of one q4k_gemv_seq call,
+    against the same matrices as two plain projections per layer."""
+    n, k = 17408, 5120
+    wg = [synth.q4k_weight(n, k, seed=synth.derive_seed(1006, "g", i), quants="normal", device=dev)
+          for i in range(n_layers)]
+    wu = [synth.q4k_weight(n, k, seed=synth.derive_seed(1006, "u", i), quants="normal", device=dev)
+          for i in range(n_layers)]
+    x = [synth.bf16_normal((batch, k), seed=synth.derive_seed(1006, "x", i), sigma=0.02, device=dev)
+         for i in range(n_layers)]
+    h = [torch.empty((batch, n), device=dev) for _ in range(n_layers)]
+    g2 = [torch.empty((batch, n), device=dev) for _ in range(2 * n_layers)]
+    fused = q4k.gemv_ops([(wg[i], n, k, x[i], h[i], wu[i]) for i in range(n_layers)])
+    plain = q4k.gemv_ops([(m, n, k, x[i // 2], g2[i]) for i, m in
+                          enumerate(v for pair in zip(wg, wu) for v in pair)])
+    flags = q4k.Q4K_FLAG_OVERLAP_WEIGHTS
+    ms_f, _, gf = time_graph(lambda: q4k.q4k_gemv_seq(fused, batch, flags, stream=stream),
+                             steps, warmup, stream)
+    del gf
+    ms_p, _, gp = time_graph(lambda: q4k.q4k_gemv_seq(plain, batch, flags, stream=stream),
+                             steps, warmup, stream)
+    del gp
+    nbytes = n_layers * (2 * q4k_bytes(n, k) + batch * (k * 2 + n * 4))
+    return {"batch": batch, "ms_fused": round(ms_f, 4), "gbs_fused": round(nbytes / (ms_f * 1e-3) / 1e9, 1),
+            "frac_of_8tbs_fused": round(nbytes / (ms_f * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "ms_two_projections": round(ms_p, 4),
+            "speedup_vs_two_projections": round(ms_p / ms_f, 3)}
+
+
+def bench_dequant(q4k, dev, stream, reps=20):
+    """q4k_dequant of the 17408 x 5120 gate matrix (50 MB of Q4_K) to fp32 and
+    bf16: GB/s over the bytes read and written."""
+    n, k = 17408, 5120
+    w = synth.q4k_weight(n, k, seed=1007, quants="normal", device=dev)
+    out = {}
+    for name, dt, ob in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        o = torch.empty((n, k), dtype=dt, device=dev)
+        ms, _, g = time_graph(lambda: q4k.q4k_dequant(w, n, k, out=o, stream=stream), reps, 3, stream)
+        del g
+        nbytes = q4k_bytes(n, k) + n * k * ob
+        out[name] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    return out
 
 
 # ------------------------------------------------------------------ CPU baseline
@@ -390,11 +473,11 @@ def bench_moe(q4k, dev, stream, reps=20):
             "distinct_experts": distinct, "bytes": nbytes}
 
 
-KERNEL_SOURCES = ("q4k_gemv.cu", "q4k_device.cuh", "q4k_internal.h")
+KERNEL_SOURCES = ("q4k_stream.cu", "q4k_device.cuh", "q4k_internal.h")
 
 
 def kernel_fingerprint(read=None) -> str:
-    """sha256 (16 hex digits) of the batch-1 GEMV's sources with comments and
+    """sha256 (16 hex digits) of the batch-1 stream kernel's sources with comments and
     whitespace removed: it changes when the compiled kernel can, not when a
     comment does.  `read(name)` returns a source's text (default: the tree)."""
     import hashlib
@@ -410,11 +493,13 @@ def kernel_fingerprint(read=None) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """Per-launch DRAM traffic of the batch-1 GEMV from the committed ncu summary
-    (profiles/gemv_b1_27b_layer.md), or None when the kernel's sources have
-    changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "gemv_b1_27b_layer.md")
+def profiled_traffic(pass_bytes: float):
+    """DRAM traffic of one launch of the batch-1 stream kernel over the decode
+    pass, from the committed ncu summary (profiles/gemv_stream_b1_27b_layer.md):
+    the captured launch is one 27B-class layer (the full 64-layer pass is too
+    large to capture), so its dram bytes are scaled to the pass by algorithmic
+    bytes.  None when the kernel's sources have changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "gemv_stream_b1_27b_layer.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -425,9 +510,11 @@ def profiled_traffic():
     if vals.get("kernel_fingerprint_16") != kernel_fingerprint():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        per_launch = float(vals["dram_bytes_per_launch"])
+        captured = float(vals["algorithmic_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+    return round(per_launch * pass_bytes / captured)
 
 
 # ------------------------------------------------------------------ main
@@ -443,12 +530,14 @@ def run_case(case):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     if case in ("gemv_layer", "gemv_layer_batched"):
+        # one layer's five projections as one q4k_gemv_seq call (at batch 1 one
+        # launch of the stream kernel over 203 MB of weights)
         layers = Layers(dev, n_layers=1)
         for batch in ((1,) if case == "gemv_layer" else (4, 16)):
             xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
+            ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])
             torch.cuda.synchronize()
-            for (name, n, k, w), x, y in zip(layers.mats, xs, ys):
-                q4k.q4k_gemv(w, n, k, x, out=y)
+            q4k.q4k_gemv_seq(ops, batch)
     elif case == "gemm_prefill":
         m = 512
         for name, n, k in (("gate", 17408, 5120), ("down", 5120, 17408)):
@@ -584,6 +673,8 @@ def main():
     total_value = replicas_gbs(nbytes, ms, world)
     launches = head["launches_per_step"]
 
+    # one launch per step: its CUDA-event duration is the kernel's own
+    kernel_ms = head["ms_per_step"] / head["launches_per_step"]
     with nvtx("decode_b1 pass e2e"):
         e2e = bench_decode_e2e(q4k, layers, 1, max(3, args.steps // 2), 2, dev, stream)
     e2e["ms_per_step"] = round(max_over_ranks(e2e["ms_per_step"], world), 4)
@@ -602,22 +693,34 @@ def main():
                 r = bench_decode(q4k, layers, b, max(5, args.steps // 2), 3, dev, stream)
             extra[f"decode_b{b}"] = {"gbs": round(r["gbs"], 1),
                                      "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
-                                     "ms_per_step": round(r["ms_per_step"], 4)}
+                                     "ms_per_step": round(r["ms_per_step"], 4),
+                                     "verified_worst_err_over_bound": r["verified"]}
         del layers
         torch.cuda.empty_cache()
         with nvtx("gemv 4096x4096 pool"):
             r = bench_c0_pool(q4k, max(5, args.steps // 2), 3, dev, stream)
         extra["gemv_4096_b1_pool"] = {"gbs": round(r["gbs"], 1),
                                       "frac_of_8tbs": round(r["gbs"] / NOMINAL_HBM_GBS, 4),
-                                      "us_per_gemv": round(r["us_per_gemv"], 3), "pool": r["pool"]}
+                                      "us_per_gemv": round(r["us_per_gemv"], 3), "pool": r["pool"],
+                                      "us_per_single_call": round(r["us_per_single_call"], 3)}
         torch.cuda.empty_cache()
-        with nvtx("prefill 512"):
-            pf = bench_prefill(q4k, dev, stream)
-        for nm, v in pf.items():
-            v["frac_of_measured_bf16"] = round(v["tflops"] / pk["bf16_tflops"], 4)
-            v["frac_of_sustained_bf16"] = round(v["tflops"] / pk["bf16_tflops_sustained"], 4)
-        extra["prefill_512"] = pf
+        with nvtx("fused gate/up"):
+            extra["glu_27b_gate_up_b1"] = bench_glu(q4k, dev, stream, max(5, args.steps // 2), 3)
         torch.cuda.empty_cache()
+        with nvtx("dequant"):
+            extra["dequant_17408x5120"] = bench_dequant(q4k, dev, stream)
+        torch.cuda.empty_cache()
+        if world == 1:
+            # the prefill GEMM's cluster multicast of X is for one-GPU runs only:
+            # replica runs on several GPUs leave it out
+            with nvtx("prefill 512"):
+                pf = bench_prefill(q4k, dev, stream)
+            for nm, v in pf.items():
+                v["frac_of_measured_bf16"] = round(v["tflops"] / pk["bf16_tflops"], 4)
+                v["frac_of_sustained_bf16"] = round(v["tflops"] / pk["bf16_tflops_sustained"], 4)
+                v["l2"] = "warm: the same 50 MB W and X relaunched back to back"
+            extra["prefill_512"] = pf
+            torch.cuda.empty_cache()
         with nvtx("moe 235b t16"):
             extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
     clocks = sampler.summary()
@@ -636,13 +739,16 @@ def main():
                        "l2": "weights (13 GB) far exceed L2; no flush needed",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                         "traffic": profiled_traffic(), "peak_source": pk["source"],
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / launches / (kernel_ms * 1e-3) / 1e9, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(nbytes / launches / (kernel_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                         "traffic": profiled_traffic(nbytes / launches), "peak_source": pk["source"],
                          "algorithmic_bytes_per_launch": round(nbytes / launches),
-                         "kernel": "gemv_b1_kernel (q4k_gemv, batch 1)",
-                         "note": "algorithmic bytes of the 320 launches / step time (includes "
-                                 "inter-launch gaps)"},
+                         "kernel": "gemv_stream_kernel (q4k_gemv_seq, batch 1: the 320 projections "
+                                   "as one persistent launch)",
+                         "note": "CUDA events around each graph replay of the one launch; "
+                                 "peak = measured copy bandwidth (read + write)"},
+            "verified_worst_err_over_bound": head["verified"],
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches * args.steps,

@@ -21,10 +21,11 @@ Q4K_VALUES = 256
 Q4K_BYTES = 144
 
 STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN",
-          4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA"}
+          4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA",
+          8: "Q4K_ERR_MEMORY"}
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
-           "q4k_gemv_seq", "q4k_gemm",
+           "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm",
            "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_moe_gemv_noalloc",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
@@ -33,10 +34,11 @@ _lib = None
 
 
 class GemvOp(ctypes.Structure):
-    """One entry of q4k_gemv_seq's op array (struct q4k_gemv_op)."""
+    """One entry of q4k_gemv_seq's op array (struct q4k_gemv_op); w_up is NULL
+    for a plain projection, the up matrix of a fused gate/up op otherwise."""
     _fields_ = [("w", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
                 ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("y", ctypes.c_void_p),
-                ("ldy", ctypes.c_int64)]
+                ("ldy", ctypes.c_int64), ("w_up", ctypes.c_void_p)]
 
 
 class Q4KError(RuntimeError):
@@ -65,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_gemv.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_gemv_ex.restype = ctypes.c_int
         L.q4k_gemv_ex.argtypes = [P, I64, I64, P, I64, I64, P, I64, ctypes.c_uint32, P]
+        L.q4k_gemv_glu.restype = ctypes.c_int
+        L.q4k_gemv_glu.argtypes = [P, P, I64, I64, P, I64, I64, P, I64, ctypes.c_uint32, P]
         L.q4k_gemv_seq.restype = ctypes.c_int
         L.q4k_gemv_seq.argtypes = [ctypes.POINTER(GemvOp), I64, I64, ctypes.c_uint32, P]
         L.q4k_gemm.restype = ctypes.c_int
@@ -143,15 +147,30 @@ def q4k_gemv_ex(w: torch.Tensor, n: int, k: int, x: torch.Tensor, flags: int, ou
     return out[0] if x.dim() == 1 else out
 
 
+def q4k_gemv_glu(w_gate: torch.Tensor, w_up: torch.Tensor, n: int, k: int, x: torch.Tensor,
+                 flags: int = 0, out=None, stream=None):
+    """H[b] = silu(Wg X[b]) * (Wu X[b]) for X [batch, K] (or [K]) bf16; fp32 [batch, N]."""
+    x2 = x.unsqueeze(0) if x.dim() == 1 else x
+    batch = x2.shape[0]
+    if out is None:
+        out = torch.empty((batch, n), dtype=torch.float32, device=x.device)
+    _check(lib().q4k_gemv_glu(_ptr(w_gate), _ptr(w_up), n, k, _ptr(x2), batch, x2.stride(0),
+                              _ptr(out), out.stride(0), flags, _stream(stream)), "q4k_gemv_glu")
+    return out[0] if x.dim() == 1 else out
+
+
 def gemv_ops(ops) -> ctypes.Array:
-    """The op array of q4k_gemv_seq from (w, n, k, x, y) tuples: x [batch, K]
-    bf16 and y [batch, N] fp32 on the device.  The array holds raw pointers;
-    keep the tensors alive while it is used.  Build it once and reuse it."""
+    """The op array of q4k_gemv_seq from (w, n, k, x, y) tuples, or
+    (w_gate, n, k, x, y, w_up) for a fused gate/up op: x [batch, K] bf16 and
+    y [batch, N] fp32 on the device.  The array holds raw pointers; keep the
+    tensors alive while it is used.  Build it once and reuse it."""
     arr = (GemvOp * len(ops))()
-    for i, (w, n, k, x, y) in enumerate(ops):
+    for i, op in enumerate(ops):
+        w, n, k, x, y = op[:5]
+        w_up = op[5] if len(op) > 5 else None
         x2 = x.unsqueeze(0) if x.dim() == 1 else x
         y2 = y.unsqueeze(0) if y.dim() == 1 else y
-        arr[i] = GemvOp(_ptr(w), n, k, _ptr(x2), x2.stride(0), _ptr(y2), y2.stride(0))
+        arr[i] = GemvOp(_ptr(w), n, k, _ptr(x2), x2.stride(0), _ptr(y2), y2.stride(0), _ptr(w_up))
     return arr
 
 

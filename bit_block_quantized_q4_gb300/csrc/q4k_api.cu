@@ -9,7 +9,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <mutex>
+#include <vector>
 
 #include "../../include/q4k.h"
 #include "q4k_device.cuh"
@@ -66,6 +68,28 @@ int check_device() {
 }
 
 int map_launch(cudaError_t e) { return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA; }
+
+// Q4K_OK when every non-null pointer is memory of the current device
+// (cudaMalloc'd, not host, pinned, managed or another GPU's memory).  The
+// kernels' TMA copies, and the prefill GEMM's cluster-multicast copy of X, are
+// built over these addresses; they must read this GPU's own memory only.
+int check_device_memory(std::initializer_list<const void *> ptrs) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
+  for (const void *p : ptrs) {
+    if (!p) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      (void)cudaGetLastError();  // the failed query leaves no error behind
+      return Q4K_ERR_MEMORY;
+    }
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) return Q4K_ERR_MEMORY;
+  }
+  return Q4K_OK;
+}
+
+static_assert(kMoeScratchBytes == Q4K_MOE_NOALLOC_SCRATCH_BYTES,
+              "the allocation-free MoE array and its documented size must agree");
 
 }  // namespace
 
@@ -130,6 +154,7 @@ const char *q4k_status_str(int status) {
     case Q4K_ERR_DEVICE: return "device is not sm_103";
     case Q4K_ERR_CUDA: return "CUDA error";
     case Q4K_ERR_DATA: return "a kernel reported bad data";
+    case Q4K_ERR_MEMORY: return "a pointer is not device memory of the current device";
     default: return "unknown status";
   }
 }
@@ -140,6 +165,8 @@ int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, v
   if (!w || !out) return Q4K_ERR_NULL;
   if (!aligned(w, 16) || !aligned(out, 16)) return Q4K_ERR_ALIGN;
   int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w, out});
   if (st != Q4K_OK) return st;
   return map_launch(launch_dequant(w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
 }
@@ -164,6 +191,22 @@ int check_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch
 }
 }  // namespace
 
+namespace {
+// One projection (plain, or fused gate/up when w_up is set) after its
+// arguments were checked: batch 1 runs in the stream kernel, 2..16 in the
+// batched kernel.
+int run_gemv(const void *w, const void *w_up, int64_t n, int64_t k, const void *x, int64_t batch,
+             int64_t ldx, float *y, int64_t ldy, uint32_t flags, void *stream) {
+  const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (batch == 1) {
+    const StreamOpDesc d = {w, w_up, x, y, n, k};
+    return map_launch(launch_stream(&d, 1, overlap, s));
+  }
+  return map_launch(launch_gemv(w, w_up, n, k, x, batch, ldx, y, ldy, overlap, s));
+}
+}  // namespace
+
 int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
                 float *y, int64_t ldy, uint32_t flags, void *stream) {
   bool empty = false;
@@ -171,14 +214,28 @@ int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batc
   if (st != Q4K_OK || empty) return st;
   st = check_device();
   if (st != Q4K_OK) return st;
-  return map_launch(launch_gemv(w, n, k, x, batch, ldx, y, ldy,
-                                (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0,
-                                static_cast<cudaStream_t>(stream)));
+  st = check_device_memory({w, x, y});
+  if (st != Q4K_OK) return st;
+  return run_gemv(w, nullptr, n, k, x, batch, ldx, y, ldy, flags, stream);
 }
 
 int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
              float *y, int64_t ldy, void *stream) {
   return q4k_gemv_ex(w, n, k, x, batch, ldx, y, ldy, 0u, stream);
+}
+
+int q4k_gemv_glu(const void *w_gate, const void *w_up, int64_t n, int64_t k, const void *x,
+                 int64_t batch, int64_t ldx, float *h, int64_t ldh, uint32_t flags, void *stream) {
+  bool empty = false;
+  int st = check_gemv(w_gate, n, k, x, batch, ldx, h, ldh, flags, &empty);
+  if (st != Q4K_OK || empty) return st;
+  if (!w_up) return Q4K_ERR_NULL;
+  if (!aligned(w_up, 16)) return Q4K_ERR_ALIGN;
+  st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w_gate, w_up, x, h});
+  if (st != Q4K_OK) return st;
+  return run_gemv(w_gate, w_up, n, k, x, batch, ldx, h, ldh, flags, stream);
 }
 
 int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t flags,
@@ -192,16 +249,32 @@ int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t 
     bool empty = false;
     const int st = check_gemv(o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, flags, &empty);
     if (st != Q4K_OK) return st;
+    if (!empty && o.w_up && !aligned(o.w_up, 16)) return Q4K_ERR_ALIGN;
     any = any || !empty;
   }
   if (!any) return Q4K_OK;
   int st = check_device();
   if (st != Q4K_OK) return st;
-  const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
   for (int64_t i = 0; i < count; ++i) {
     const q4k_gemv_op &o = ops[i];
     if (o.n == 0) continue;
-    st = map_launch(launch_gemv(o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, overlap,
+    st = check_device_memory({o.w, o.w_up, o.x, o.y});
+    if (st != Q4K_OK) return st;
+  }
+  const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
+  if (batch == 1) {  // one persistent launch streams every op's weights back to back
+    std::vector<StreamOpDesc> d;
+    d.reserve((size_t)count);
+    for (int64_t i = 0; i < count; ++i) {
+      const q4k_gemv_op &o = ops[i];
+      d.push_back(StreamOpDesc{o.w, o.w_up, o.x, o.y, o.n, o.k});
+    }
+    return map_launch(launch_stream(d.data(), count, overlap, static_cast<cudaStream_t>(stream)));
+  }
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    if (o.n == 0) continue;
+    st = map_launch(launch_gemv(o.w, o.w_up, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, overlap,
                                 static_cast<cudaStream_t>(stream)));
     if (st != Q4K_OK) return st;
   }
@@ -218,6 +291,8 @@ int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int6
   if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 16) || (ldx % 8) != 0 || (ldy % 8) != 0)
     return Q4K_ERR_ALIGN;
   int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w, x, y});
   if (st != Q4K_OK) return st;
   return map_launch(launch_gemm(w, n, k, x, m, ldx, y, ldy, static_cast<cudaStream_t>(stream)));
 }
@@ -249,6 +324,8 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
     return Q4K_ERR_ALIGN;
   int st = check_device();
   if (st != Q4K_OK) return st;
+  st = check_device_memory({w_gate, w_up, w_down, x, ids, wts, y, workspace});
+  if (st != Q4K_OK) return st;
   return map_launch(launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x,
                                n_tokens, ldx, ids, wts, top_k, y, ldy, workspace,
                                static_cast<cudaStream_t>(stream)));
@@ -272,6 +349,8 @@ int q4k_moe_gemv_noalloc(const void *w_gate, const void *w_up, const void *w_dow
       !aligned(x, 16) || (ldx % 8) || !aligned(y, 4) || !aligned(ids, 4) || !aligned(wts, 4))
     return Q4K_ERR_ALIGN;
   int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w_gate, w_up, w_down, x, ids, wts, y});
   if (st != Q4K_OK) return st;
   return map_launch(launch_moe_scratch(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn,
                                        x, n_tokens, ldx, ids, wts, top_k, y, ldy,

@@ -118,6 +118,22 @@ __device__ __forceinline__ uint32_t lop_nib_hi16(uint32_t w, uint32_t magic_reg)
   return d;
 }
 
+// (128 + q) - (128 + c) for both bf16 halves: with q in [0, 15] and c in
+// [0, 16] every input and the result are exact in bf16, so this is the exact
+// small integer q - c.
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Reciprocal, hardware approximation (about 1 ulp; +inf for +0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+  return r;
+}
+constexpr uint32_t kBf16One = 0x3F803F80u;  // bf16 1.0 in both halves
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
@@ -172,6 +188,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, err);
 }
+// The same wait for a warp that has nothing else to do meanwhile: between
+// polls it sleeps (32 ns, doubling up to max_ns), so that it leaves the issue
+// slots of its scheduler to warps that have work.
+static __device__ __noinline__ bool mbar_wait_sleepy_slow(uint64_t *bar, uint32_t parity,
+                                                          unsigned *err, uint32_t max_ns) {
+  const uint64_t t0 = global_ns();
+  uint32_t ns = 32;
+  for (;;) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity, 0u)) return true;
+    ns = ns < max_ns ? 2 * ns : max_ns;
+    if (global_ns() - t0 > kWaitLimitNs) break;
+  }
+  set_device_error(err, kDevErrTimeout);
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                 uint32_t max_ns) {
+  if (mbar_try_wait(bar, parity, 0u)) return true;
+  return mbar_wait_sleepy_slow(bar, parity, err, max_ns);
+}
 
 // ----------------------------------------------------------------- TMA
 // Untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
@@ -181,6 +218,15 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// The same with an L2 cache policy (createpolicy) for the source bytes.
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes,
+                                               uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 // Tiled tensor copy global -> shared, completion counted on `bar` in bytes.
@@ -387,6 +433,40 @@ __device__ __forceinline__ void scales_all(uint32_t h1, uint32_t h2, uint32_t h3
   *m_lo = h2 & 0x3F3F3F3Fu;
   *sc_hi = (h3 & 0x0F0F0F0Fu) | ((h1 >> 2) & 0x30303030u);
   *m_hi = ((h3 >> 4) & 0x0F0F0F0Fu) | ((h2 >> 2) & 0x30303030u);
+}
+
+// ----------------------------------------------------------------- offset form
+// Every weight of sub-block j of a super-block is w = ds (q - c) + e with
+//   ds = d sc_j,  dm = dmin m_j,  c = an integer in [0, 16] nearest to dm / ds
+//   (clamped), e = ds c - dm rounded once,
+// so  sum_i w_i x_i = ds sum_i (q_i - c) x_i + e sum_i x_i.  The tensor cores
+// take the small integers q - c (exact in bf16) against x, so a weight that is
+// exactly zero (ds q = dm) contributes an exact zero product, and the rounding
+// error of the whole sum stays proportional to sum |w| |x|: |ds (q - c)| <=
+// 2 |w| and |e| <= |w| for every weight of the sub-block.
+//
+// sc_magic / m_magic hold 0x4B000000 | byte (the float 2^23 + byte), nd23 /
+// ndm23 = -d 2^23 / -dmin 2^23: fma(d, 2^23 + sc, -d 2^23) is d sc exactly.
+// Outputs: ds, e, and sub = (128 + c) as bf16 in both halves (the value to
+// subtract from the 128 + q nibble operands).
+__device__ __forceinline__ void offset_form(float d, float nd23, float dmin, float ndm23,
+                                            uint32_t sc_magic, uint32_t m_magic, float &ds,
+                                            float &e, uint32_t &sub) {
+  ds = fmaf(d, __uint_as_float(sc_magic), nd23);
+  const float dm = fmaf(dmin, __uint_as_float(m_magic), ndm23);
+  // u = (dm/ds + 0.5) / 16 saturated to [0, 1] (NaN -> 0), v = 128 + 16 u in
+  // [128, 144]: the bf16 truncation of v is 128 + c with c = floor(dm/ds + 0.5)
+  // clamped to [0, 16] (exact for an integer ratio: the approximate
+  // reciprocal moves 128.5 + c by less than half an fp32 ulp).  ds = 0 makes
+  // the ratio NaN or +-inf, which the saturation maps to c = 0 or 16.
+  const float u = __saturatef(fmaf(dm, rcp_approx(16.f * ds), 0.03125f));
+  const uint32_t vb = __float_as_uint(fmaf(u, 16.f, 128.f));
+  sub = __byte_perm(vb, 0u, 0x3232u);
+  e = fmaf(ds, __uint_as_float(vb & 0xFFFF0000u) - 128.f, -dm);
+}
+// Byte i of w as the float 2^23 + byte (bit pattern 0x4B0000bb).
+__device__ __forceinline__ uint32_t byte_magic(uint32_t w, int i) {
+  return __byte_perm(w, 0x4B000000u, 0x7540u + (uint32_t)i);
 }
 
 __device__ __forceinline__ float half_lo_to_float(uint32_t h) {

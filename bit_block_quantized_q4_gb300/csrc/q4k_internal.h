@@ -38,8 +38,23 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank,
 
 cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype,
                            cudaStream_t stream);
-cudaError_t launch_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
-                        int64_t ldx, float *y, int64_t ldy, bool overlap, cudaStream_t stream);
+// Batch 2..16: Y = W X, or with w_up != nullptr Y = silu(W X) * (W_up X).
+cudaError_t launch_gemv(const void *w, const void *w_up, int64_t n, int64_t k, const void *x,
+                        int64_t batch, int64_t ldx, float *y, int64_t ldy, bool overlap,
+                        cudaStream_t stream);
+// One projection of a batch-1 stream launch: y = W x, or for a fused gate/up
+// op (w_up != nullptr) y = silu(W x) * (W_up x).
+struct StreamOpDesc {
+  const void *w;     // weights; the gate matrix of a fused gate/up op
+  const void *w_up;  // up matrix of a fused gate/up op, nullptr otherwise
+  const void *x;     // bf16 [k]
+  float *y;          // fp32 [n]
+  int64_t n, k;
+};
+// The ops, in order, as one persistent launch (several when count exceeds the
+// kernel's op table); ops with n == 0 are skipped.
+cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
+                          cudaStream_t stream);
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
 size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

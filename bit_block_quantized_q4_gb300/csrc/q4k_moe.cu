@@ -300,21 +300,28 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
         }
       __syncwarp();
       if (lane == 0 && q + kStagesMoe < total) issue(q + kStagesMoe);
-      // This lane decodes sub-blocks 2t, 2t+1 of rows g, g+8; the other lanes of
-      // its quad fetch them by shuffle.
-      float dsA[NM][2], dsB[NM][2], dmA[NM][2], dmB[NM][2];
+      // Offset forms (offset_form) of sub-blocks 2t, 2t+1 (e = 0, 1) of rows
+      // g, g+8 (r = 0, 1); the other lanes of the quad fetch them by shuffle.
+      // The bf16 subtrahends of both rows travel packed in one word per e.
+      float dsv[NM][2][2], eev[NM][2][2];
+      uint32_t subp[NM][2];
 #pragma unroll
-      for (int mi = 0; mi < NM; ++mi)
+      for (int mi = 0; mi < NM; ++mi) {
+        uint32_t sub[2][2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           uint32_t sc2, m2;
           scales_pair(hdr[mi][r].y, hdr[mi][r].z, hdr[mi][r].w, t, &sc2, &m2);
           const float d = half_lo_to_float(hdr[mi][r].x), dmin = half_hi_to_float(hdr[mi][r].x);
-          dsA[mi][r] = d * (float)(sc2 & 0xFFu);
-          dsB[mi][r] = d * (float)(sc2 >> 8);
-          dmA[mi][r] = dmin * (float)(m2 & 0xFFu) * (1.f / 128.f);
-          dmB[mi][r] = dmin * (float)(m2 >> 8) * (1.f / 128.f);
+          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            offset_form(d, nd23, dmin, ndm23, byte_magic(sc2, e), byte_magic(m2, e),
+                        dsv[mi][r][e], eev[mi][r][e], sub[r][e]);
         }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) subp[mi][e] = __byte_perm(sub[0][e], sub[1][e], 0x5410u);
+      }
       auto sub_block = [&](int jb, const uint4(&xv)[NT]) {
         const int c = jb >> 1;
         const bool hi = jb & 1;
@@ -336,48 +343,49 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
             b1[nt][1] = __byte_perm(v.z, v.w, 0x7632);
           }
         }
-        // -128 X_j of every column by one more MMA per step (A = -128
-        // everywhere): every row of cneg holds it, so column 2t+e is
-        // cneg[nt][e].  The weight MMAs start there, so acc = sum q x.
-        float cneg[NT][4];
+        // X_j of every column by two MMAs with A = 1 everywhere (every row
+        // holds it, so column 2t+e is xsum[nt][e]).
+        float xsum[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16_zc(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[nt][0], b1[nt][0]);
-          mma_bf16(cneg[nt], kBf16Neg128, kBf16Neg128, kBf16Neg128, kBf16Neg128, b0[nt][1], b1[nt][1]);
+          mma_bf16_zc(xsum[nt], kBf16One, kBf16One, kBf16One, kBf16One, b0[nt][0], b1[nt][0]);
+          mma_bf16(xsum[nt], kBf16One, kBf16One, kBf16One, kBf16One, b0[nt][1], b1[nt][1]);
         }
+        // Offset forms of sub-block jb for rows g, g+8 live in lane (g, jb/2).
         const int srcl = (lane & ~3) | (jb >> 1);
 #pragma unroll
         for (int mi = 0; mi < NM; ++mi) {
+          const uint32_t sp = __shfl_sync(0xffffffffu, hi ? subp[mi][1] : subp[mi][0], srcl);
+          const uint32_t sg = __byte_perm(sp, 0u, 0x1010u), sg8 = __byte_perm(sp, 0u, 0x3232u);
           float acc[NT][4];
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             const uint32_t w0 = s ? qw[mi][0][c].y : qw[mi][0][c].x;
             const uint32_t w1 = s ? qw[mi][1][c].y : qw[mi][1][c].x;
-            const uint32_t a0 = hi ? nib_hi(w0) : nib_lo(w0);
-            const uint32_t a1 = hi ? nib_hi(w1) : nib_lo(w1);
-            const uint32_t a2 = hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8);
-            const uint32_t a3 = hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8);
+            const uint32_t a0 = sub_bf16x2(hi ? nib_hi(w0) : nib_lo(w0), sg);
+            const uint32_t a1 = sub_bf16x2(hi ? nib_hi(w1) : nib_lo(w1), sg8);
+            const uint32_t a2 = sub_bf16x2(hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8), sg);
+            const uint32_t a3 = sub_bf16x2(hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8), sg8);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               if (s == 0)
-                mma_bf16_c(acc[nt], cneg[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
+                mma_bf16_zc(acc[nt], a0, a1, a2, a3, b0[nt][0], b1[nt][0]);
               else
                 mma_bf16(acc[nt], a0, a1, a2, a3, b0[nt][1], b1[nt][1]);
             }
           }
-          // acc = sum q x: apply d*sc; the min term takes X_j = -cneg / 128
-          // (the 1/128 is folded into dm, the sign into the fma).
+          // acc = sum (q - c) x over the sub-block: add ds * acc + e * X_j.
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float ds = __shfl_sync(0xffffffffu, hi ? dsB[mi][r] : dsA[mi][r], srcl);
-            const float dm = __shfl_sync(0xffffffffu, hi ? dmB[mi][r] : dmA[mi][r], srcl);
+            const float ds = __shfl_sync(0xffffffffu, hi ? dsv[mi][r][1] : dsv[mi][r][0], srcl);
+            const float ee = __shfl_sync(0xffffffffu, hi ? eev[mi][r][1] : eev[mi][r][0], srcl);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 float &yv = yacc[mi][nt][2 * r + e];
                 yv = fmaf(ds, acc[nt][2 * r + e], yv);
-                yv = fmaf(dm, cneg[nt][e], yv);
+                yv = fmaf(ee, xsum[nt][e], yv);
               }
           }
         }
@@ -628,17 +636,26 @@ __device__ __align__(256) uint8_t g_moe_scratch[kMoeScratchBytes];
 
 namespace {
 
-void *g_scratch_ptr[64];
-cudaError_t g_scratch_status[64];
-std::once_flag g_scratch_once[kMaxDevices];
+void *g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mu;
 
 // Host code may not use g_moe_scratch as an address (it names a host-side
-// stand-in); the device address is resolved once per device, with that device
-// current, on the first call made on it.
-void resolve_scratch(int dev) {
-  void *p = nullptr;
-  g_scratch_status[dev] = cudaGetSymbolAddress(&p, g_moe_scratch);
-  g_scratch_ptr[dev] = (g_scratch_status[dev] == cudaSuccess) ? p : nullptr;
+// stand-in); the device address is looked up with the device current, on the
+// first call made on it.  Only a successful look-up is kept: after a failure
+// the next call tries again.
+cudaError_t scratch_address(int dev, void **out) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -652,10 +669,11 @@ cudaError_t launch_moe_scratch(const void *w_gate, const void *w_up, const void 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], resolve_scratch, dev);
-  if (g_scratch_ptr[dev] == nullptr) return g_scratch_status[dev];
+  void *scratch = nullptr;
+  e = scratch_address(dev, &scratch);
+  if (e != cudaSuccess) return e;
   return launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x, n_tokens, ldx,
-                    ids, wts, top_k, y, ldy, g_scratch_ptr[dev], stream);
+                    ids, wts, top_k, y, ldy, scratch, stream);
 }
 
 }  // namespace q4k

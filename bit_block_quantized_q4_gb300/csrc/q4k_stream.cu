@@ -1,0 +1,726 @@
+// q4k_stream.cu -- batch-1 decode projections y = W x with W in Q4_K, any
+// number of them in one persistent launch ("spec: specialized model runtimes",
+// sections "Architecture" (T0 GEMM, quant/dequant) and "Development sequence"
+// (decode throughput is the metric; graph-captured decode)), and the fused
+// gate/up projection h = silu(Wg x) * (Wu x) of a dense or shared-expert FFN
+// ("Layer Package Repository Spec", section "Policy Resolution": merged shared
+// gate/up).
+//
+// Work: a tile is 16*MT weight rows of one op over the op's whole K (a GLU op's
+// tile is its gate rows, then the same up rows).  The ops of a launch form one
+// list of tiles in op order; each tile stream takes a contiguous run of it,
+// balanced by weight bytes, so a sequence of projections streams its weights
+// back to back with no launch boundary between them.  A stream is one warp
+// (KP = 1), or KP warps that split each tile's super-blocks and add their
+// partial sums in warp order through shared memory (for launches with too few
+// tiles to occupy the GPU).
+//
+// Each warp owns a ring of shared-memory stages: one super-block of each of its
+// 16*MT rows (one bulk copy per row) plus the 512 bytes of x of that
+// super-block, all completing on the stage's mbarrier.  The ring runs ahead
+// across tile, part and op boundaries; with programmatic dependent launch the
+// first weight stages are requested before the wait for the previous kernel,
+// x only after it.
+//
+// Contraction (tensor cores, mma.sync m16n8k16 bf16 -> fp32).  Sub-block j of a
+// row is taken in offset form: w = ds (q - c) + e with c the integer nearest to
+// dmin m_j / (d sc_j) (see offset_form), so the A operand is the exact small
+// integer q - c in bf16 ((128 + q) from one LOP3, minus 128 + c) and x enters
+// unconverted as bf16.  The eight MMA columns carry the eight sub-blocks of a
+// super-block: column n of B holds x only in the k-slots that carry
+// sub-block n, so one super-block is 16 MMAs per 16 rows and thread (g, t) ends
+// with exactly the (row, sub-block) sums of rows g, g+8 and sub-blocks 2t, 2t+1
+// whose scales it decodes itself.  X_j = sum of x over sub-block j comes from
+// two more MMAs with A = 1.  Per super-block the thread adds
+// ds * S_j + e * X_j for its four (row, sub-block) pairs; at the end of a tile a
+// quad shuffle adds the sub-blocks of a row.  Every sum is taken in a fixed
+// order: the result does not depend on timing.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+#ifndef Q4K_STREAM_STAGES_MT1  // ring stages per warp, 16-row tiles
+#define Q4K_STREAM_STAGES_MT1 2
+#endif
+#ifndef Q4K_STREAM_STAGES_MT2  // ring stages per warp, 32-row tiles
+#define Q4K_STREAM_STAGES_MT2 2
+#endif
+#ifndef Q4K_STREAM_MINB_MT1  // resident CTAs per SM the register budget is sized for
+#define Q4K_STREAM_MINB_MT1 4
+#endif
+#ifndef Q4K_STREAM_MINB_MT2
+#define Q4K_STREAM_MINB_MT2 4
+#endif
+#ifndef Q4K_STREAM_SB  // super-blocks per stage (one bulk copy of SB * 144 bytes per row)
+#define Q4K_STREAM_SB 2
+#endif
+#ifndef Q4K_STREAM_SLEEP_NS  // 0: poll the stage barrier; else sleep between polls, up to this many ns
+#define Q4K_STREAM_SLEEP_NS 256
+#endif
+#ifndef Q4K_STREAM_SHIFT_MUL  // 1: nibble shifts as multiply-high (FMA pipe) instead of shifts (ALU)
+#define Q4K_STREAM_SHIFT_MUL 0
+#endif
+#ifndef Q4K_STREAM_PRE  // weight stages requested before the dependency wait (PDL)
+#define Q4K_STREAM_PRE 2
+#endif
+#ifndef Q4K_STREAM_FORCE_MT  // 0: planner's choice
+#define Q4K_STREAM_FORCE_MT 0
+#endif
+#ifndef Q4K_STREAM_FORCE_KP
+#define Q4K_STREAM_FORCE_KP 0
+#endif
+
+namespace q4k {
+
+namespace {
+
+constexpr int kWarps = 4;              // warps per CTA
+constexpr int kXBytes = kQK * 2;       // bf16 x of one super-block
+constexpr int kPermStride = 20;        // words per sub-block in the permuted x (16 used)
+constexpr int kPermWords = 8 * kPermStride;
+constexpr int kMaxOps = 512;           // ops per launch (kernel parameter table)
+
+struct StreamOp {
+  const uint8_t *w;   // weights; the gate matrix of a GLU op
+  const uint8_t *w2;  // up matrix of a GLU op, nullptr for a plain projection
+  const __nv_bfloat16 *x;
+  float *y;
+  long long byte0;  // weight bytes of the ops before this one
+  int n, nsb, ntiles, parts;
+};
+
+template <int NOPS>
+struct StreamParams {
+  int nops;
+  int kp;        // warps per tile stream (split of each tile's super-blocks)
+  int pre;       // weight stages requested before the dependency wait
+  int nstreams;  // tile streams in the grid
+  long long total;
+  unsigned *err;
+  StreamOp op[NOPS];
+};
+
+template <int MT>
+struct StreamCfg {
+  static constexpr int kRows = 16 * MT;
+  static constexpr int kSB = Q4K_STREAM_SB;  // super-blocks per stage
+  static constexpr int kStages = MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2;
+  static constexpr int kRowBytes = kSB * kBlockBytes;  // a row's bytes in a stage
+  static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
+  static constexpr int kXStage = kSB * kXBytes;        // x bytes of a stage
+  // warp region: ring weights | ring x | 2 permuted-x buffers | 64 zero bytes |
+  // ring mbarriers
+  static constexpr int kOffX = kStages * kWBytes;
+  static constexpr int kOffPerm = kOffX + kStages * kXStage;
+  static constexpr int kOffZero = kOffPerm + 2 * kPermWords * 4;
+  static constexpr int kOffBar = kOffZero + 64;
+  static constexpr int kWarpBytes = (kOffBar + kStages * 8 + 127) / 128 * 128;
+  static constexpr int kRedBytes = 2 * kWarps * 2 * kRows * 4;  // split-K partials
+  static constexpr int kSmem = kWarps * kWarpBytes + kRedBytes;
+};
+
+// Position of a warp's next stage: super-blocks sb .. sb+SB-1 (at most kb1 - sb
+// of them) of part `part` of tile `tile` of op `op`; [kb0, kb1) is the warp's
+// share of the op's super-blocks.  For the current (op, tile, part) it keeps
+// this lane's weight row (nullptr when the tile has no row for the lane), the
+// op's x and the bytes of one super-block of the tile, so that issuing a stage
+// is a few instructions.
+struct Pos {
+  int op, tile, part, sb, kb0, kb1;
+  bool valid;
+  const uint8_t *src;
+  const __nv_bfloat16 *xsrc;
+  uint32_t bytes;
+};
+
+template <int NOPS>
+__device__ __forceinline__ long long tile_start(const StreamParams<NOPS> &p, int op, int tile,
+                                                int rows) {
+  const StreamOp &o = p.op[op];
+  return o.byte0 + (long long)tile * rows * o.nsb * kBlockBytes * o.parts;
+}
+
+__device__ __forceinline__ void krange(int nsb, int kp, int KP, int &kb0, int &kb1) {
+  const int ks = (nsb + KP - 1) / KP;
+  kb0 = min(nsb, kp * ks);
+  kb1 = min(nsb, kb0 + ks);
+}
+
+// First tile of a stream: the first tile that starts at or after byte lo.
+template <int NOPS>
+__device__ __forceinline__ void first_tile(const StreamParams<NOPS> &p, int rows, long long lo,
+                                           long long hi, int &op, int &tile, bool &valid) {
+  int a = 0, b = p.nops - 1;
+  while (a < b) {
+    const int m = (a + b + 1) >> 1;
+    if (p.op[m].byte0 <= lo) a = m; else b = m - 1;
+  }
+  op = a;
+  const StreamOp &o = p.op[op];
+  const long long cost = (long long)rows * o.nsb * kBlockBytes * o.parts;
+  tile = (int)((lo - o.byte0 + cost - 1) / cost);
+  if (lo <= o.byte0) tile = 0;
+  if (tile >= o.ntiles) {
+    ++op;
+    tile = 0;
+  }
+  valid = op < p.nops && tile_start(p, op, tile, rows) < hi;
+}
+
+template <int NOPS>
+__device__ __forceinline__ void next_tile(const StreamParams<NOPS> &p, int rows, long long hi,
+                                          int &op, int &tile, bool &valid) {
+  if (++tile >= p.op[op].ntiles) {
+    ++op;
+    tile = 0;
+  }
+  valid = op < p.nops && tile_start(p, op, tile, rows) < hi;
+}
+
+template <int NOPS>
+__device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, int lane, Pos &s) {
+  const StreamOp &o = p.op[s.op];
+  const int row0 = s.tile * rows;
+  const int nrows = min(rows, o.n - row0);
+  s.src = lane < nrows
+              ? (s.part ? o.w2 : o.w) + (size_t)(row0 + lane) * o.nsb * kBlockBytes
+              : nullptr;
+  s.xsrc = o.x;
+  s.bytes = (uint32_t)(nrows * kBlockBytes + kQK * 2);
+}
+
+// Producer walk over the non-empty stages of a stream, for warp kp of KP:
+// moves forward until the position names a stage (skips tiles whose share of
+// super-blocks is empty for this warp) and loads the lane's sources.
+template <int NOPS>
+__device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows, long long hi,
+                                        int kp, int lane, Pos &s) {
+  while (s.valid && s.sb >= s.kb1) {
+    if (++s.part < p.op[s.op].parts) {
+      s.sb = s.kb0;
+      continue;
+    }
+    next_tile(p, rows, hi, s.op, s.tile, s.valid);
+    if (!s.valid) break;
+    s.part = 0;
+    krange(p.op[s.op].nsb, kp, p.kp, s.kb0, s.kb1);
+    s.sb = s.kb0;
+  }
+  if (s.valid) pos_load(p, rows, lane, s);
+}
+
+template <int NOPS>
+__device__ __forceinline__ void pos_next(const StreamParams<NOPS> &p, int rows, long long hi,
+                                         int kp, int lane, Pos &s) {
+  if ((s.sb += Q4K_STREAM_SB) < s.kb1) return;
+  pos_settle(p, rows, hi, kp, lane, s);
+}
+
+// After a timed-out wait: give the copies still in flight on the ring (slots
+// of stages it .. end-1) the same bounded time to land before the warp moves on
+// or its CTA exits.
+__device__ __noinline__ void drain_ring(uint64_t *bars, int stages, int slot, uint32_t phase,
+                                        int inflight) {
+  const uint64_t t0 = global_ns();
+  for (int j = 0; j < inflight; ++j) {
+    while (!mbar_try_wait(&bars[slot], phase, 1000u))
+      if (global_ns() - t0 > kWaitLimitNs) return;
+    if (++slot == stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// w >> n, as a shift (ALU pipe) or as the high half of w * 2^(32-n) (FMA pipe).
+template <int N>
+__device__ __forceinline__ uint32_t shr(uint32_t w) {
+#if Q4K_STREAM_SHIFT_MUL
+  return __umulhi(w, 1u << (32 - N));
+#else
+  return w >> N;
+#endif
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.f + __expf(-g)) * u;
+}
+
+template <int MT, int NOPS>
+__global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
+    gemv_stream_kernel(
+    const __grid_constant__ StreamParams<NOPS> p) {
+  using C = StreamCfg<MT>;
+  constexpr int TR = C::kRows, ST = C::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int KP = p.kp;
+  const int kp = warp % KP;                        // this warp's share of each tile
+  const int sic = warp / KP;                       // stream within the CTA
+  const int sid = blockIdx.x * (kWarps / KP) + sic;  // stream id
+  const long long lo = p.total * sid / p.nstreams, hi = p.total * (sid + 1) / p.nstreams;
+
+  uint8_t *wreg = smem + (size_t)warp * C::kWarpBytes;
+  uint8_t *ringw = wreg;
+  uint8_t *ringx = wreg + C::kOffX;
+  uint32_t *perm = reinterpret_cast<uint32_t *>(wreg + C::kOffPerm);
+  const uint32_t *zeros = reinterpret_cast<const uint32_t *>(wreg + C::kOffZero);
+  uint64_t *full = reinterpret_cast<uint64_t *>(wreg + C::kOffBar);
+  float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * C::kWarpBytes);
+
+  if (lane == 0) {
+    for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  if (lane < 16) reinterpret_cast<uint32_t *>(wreg + C::kOffZero)[lane] = 0u;
+  __syncwarp();
+  const uint64_t policy = l2_evict_first_policy();
+
+  // ---- producer: the stream's stages in order, STAGES ahead of the consumer
+  Pos pp;
+  first_tile(p, TR, lo, hi, pp.op, pp.tile, pp.valid);
+  pp.part = 0;
+  if (pp.valid) krange(p.op[pp.op].nsb, kp, KP, pp.kb0, pp.kb1);
+  else pp.kb0 = pp.kb1 = 0;
+  pp.sb = pp.kb0;
+  pos_settle(p, TR, hi, kp, lane, pp);  // the first stage (when there is one)
+
+  constexpr int SB = C::kSB;
+  auto issue_w = [&](int slot, const Pos &s) {
+    const uint32_t cnt = (uint32_t)min(SB, s.kb1 - s.sb);
+    if (lane == 0) mbar_arrive_expect_tx(&full[slot], cnt * s.bytes);
+    __syncwarp();
+    if (s.src)
+      bulk_load_hint(ringw + slot * C::kWBytes + lane * C::kRowBytes,
+                     s.src + (size_t)s.sb * kBlockBytes, cnt * kBlockBytes, &full[slot], policy);
+  };
+  auto issue_x = [&](int slot, const Pos &s) {
+    const uint32_t cnt = (uint32_t)min(SB, s.kb1 - s.sb);
+    if (lane == 31)
+      bulk_load(ringx + slot * C::kXStage, s.xsrc + (size_t)s.sb * kQK, cnt * kXBytes, &full[slot]);
+  };
+
+  // With programmatic dependent launch the first p.pre stages' weights go out
+  // before the wait (weights are never written by earlier kernels), their x
+  // after it.
+  int npre = 0;
+  {
+    Pos q = pp;
+    for (; npre < p.pre && npre < ST && q.valid; ++npre) {
+      issue_w(npre, q);
+      pos_next(p, TR, hi, kp, lane, q);
+    }
+  }
+  grid_dependency_wait();
+  int inflight = 0;  // stages issued and not yet consumed
+  for (int s = 0; s < ST && pp.valid; ++s) {
+    if (s >= npre) issue_w(s, pp);
+    issue_x(s, pp);
+    pos_next(p, TR, hi, kp, lane, pp);
+    ++inflight;
+  }
+  grid_launch_dependents();
+
+  // ---- lane constants
+  // Scale/min decode of sub-blocks 2t, 2t+1 (branch-free): lanes t < 2 read
+  // the low six bits of s[j], s[j+4]; lanes t >= 2 combine a nibble of s[j+4]
+  // with the top two bits of s[j-4] (scales) or s[j] (mins).  psel gathers
+  // bytes k0, k0+1 of rows g (bytes 0, 1) and g+8 (bytes 2, 3).
+  const bool upper = t >= 2;
+  const uint32_t k0 = 2 * (t & 1);
+  const uint32_t psel = k0 | ((k0 + 1) << 4) | ((k0 + 4) << 8) | ((k0 + 5) << 12);
+  const uint32_t mlo4 = upper ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+  const uint32_t mhi4 = upper ? 0x30303030u : 0u;
+  // B fragments: lane (g, t) carries sub-block g on the steps of parity g & 1
+  // when t == g / 2 (its k-slots then hold sub-block 2t + (g & 1)); every
+  // other (lane, step) reads zeros.
+  const bool own = t == (g >> 1);
+  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
+  uint32_t magic;
+  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kBf16Magic));
+
+  // ---- consumer
+  int cslot = 0;
+  uint32_t phase = 0;
+  int pbuf = 0;
+  bool ok = true;
+  int op, tile;
+  bool tvalid;
+  first_tile(p, TR, lo, hi, op, tile, tvalid);
+  int par = 0;  // split-K partials buffer parity
+  for (; tvalid; next_tile(p, TR, hi, op, tile, tvalid), par ^= 1) {
+    const StreamOp &o = p.op[op];
+    int kb0, kb1;
+    krange(o.nsb, kp, KP, kb0, kb1);
+    float yv[2][MT][2];  // per part: rows (g, g+8) of each m-tile, partial over sub-blocks 2t, 2t+1
+#pragma unroll
+    for (int pt = 0; pt < 2; ++pt)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) yv[pt][mt][0] = yv[pt][mt][1] = 0.f;
+    for (int part = 0; part < o.parts; ++part) {
+      float yacc[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) yacc[mt][0] = yacc[mt][1] = 0.f;
+      for (int sb = kb0; sb < kb1 && ok; sb += SB) {
+#if Q4K_STREAM_SLEEP_NS
+        const bool landed = mbar_wait_sleepy(&full[cslot], phase, p.err, Q4K_STREAM_SLEEP_NS);
+#else
+        const bool landed = mbar_wait(&full[cslot], phase, p.err);
+#endif
+        if (!landed) {
+          ok = false;
+          if (lane == 0) drain_ring(full, ST, cslot, phase, inflight);
+          __syncwarp();
+          break;
+        }
+        const int cnt = min(SB, kb1 - sb);
+        const uint8_t *wstage = ringw + cslot * C::kWBytes;
+        const uint8_t *xstage = ringx + cslot * C::kXStage;
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+          if (u >= cnt) break;
+          const uint8_t *ws = wstage + u * kBlockBytes;
+          const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
+          // X_j of the eight sub-blocks: lane (g, t) holds values 8t .. 8t+7 of
+          // sub-block g, exactly the B fragment of column g of two MMAs.
+          float xs[4];
+          mma_bf16_zc(xs, kBf16One, kBf16One, kBf16One, kBf16One, raw.x, raw.y);
+          mma_bf16(xs, kBf16One, kBf16One, kBf16One, kBf16One, raw.z, raw.w);
+          // Permuted copy: word 2G of a sub-block holds (x[4G], x[4G+2]), word
+          // 2G+1 (x[4G+1], x[4G+3]) -- the pairs the nibble operands meet.
+          uint32_t *pw = perm + pbuf * kPermWords;
+          {
+            uint4 pm;
+            pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
+            pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
+            pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
+            pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
+            reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+          }
+          uint4 hdr[MT][2], qa[MT][2][2];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint8_t *rp = ws + (mt * 16 + g + 8 * r) * C::kRowBytes;
+              hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
+              qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
+              qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
+            }
+          __syncwarp();  // permuted x visible to every lane; the stage's last reads done
+          if (u == cnt - 1) {
+            --inflight;
+            if (pp.valid) {  // refill this slot with the stream's next stage
+              issue_w(cslot, pp);
+              issue_x(cslot, pp);
+              pos_next(p, TR, hi, kp, lane, pp);
+              ++inflight;
+            }
+          }
+
+          // Offset form of this thread's (row, sub-block) pairs.
+          float ds[MT][2][2], ee[MT][2][2];
+          uint32_t sub[MT][2][2];
+  #pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint4 h0 = hdr[mt][0], h1 = hdr[mt][1];
+            const uint32_t py = __byte_perm(h0.y, h1.y, psel);
+            const uint32_t pz = __byte_perm(h0.z, h1.z, psel);
+            const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
+            const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
+            const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint32_t hx = r ? h1.x : h0.x;
+              const float d = half_lo_to_float(hx), dmin = half_hi_to_float(hx);
+              const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+  #pragma unroll
+              for (int e = 0; e < 2; ++e)
+                offset_form(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e),
+                            byte_magic(m4, 2 * r + e), ds[mt][r][e], ee[mt][r][e], sub[mt][r][e]);
+            }
+          }
+
+          const uint32_t *pe = own_e ? pw + g * kPermStride : zeros;
+          const uint32_t *po = own_o ? pw + g * kPermStride : zeros;
+          float accE[MT][4], accO[MT][4];
+  #pragma unroll
+          for (int G2 = 0; G2 < 4; ++G2) {
+            const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // the zero block is 4 uint4
+            const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int G = 2 * G2 + h;
+              const uint32_t be0 = h ? be.z : be.x, be1 = h ? be.w : be.y;
+              const uint32_t bo0 = h ? bo.z : bo.x, bo1 = h ? bo.w : bo.y;
+  #pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
+                const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
+                // low nibbles: sub-block 2t, positions (4G, 4G+2) and (4G+1, 4G+3)
+                const uint32_t a0 = sub_bf16x2(lop_nib(w0, magic), sub[mt][0][0]);
+                const uint32_t a1 = sub_bf16x2(lop_nib(w1, magic), sub[mt][1][0]);
+                const uint32_t a2 = sub_bf16x2(lop_nib(shr<8>(w0), magic), sub[mt][0][0]);
+                const uint32_t a3 = sub_bf16x2(lop_nib(shr<8>(w1), magic), sub[mt][1][0]);
+                if (G == 0)
+                  mma_bf16_zc(accE[mt], a0, a1, a2, a3, be0, be1);
+                else
+                  mma_bf16(accE[mt], a0, a1, a2, a3, be0, be1);
+                // high nibbles: sub-block 2t+1
+                const uint32_t c0 = sub_bf16x2(lop_nib(shr<4>(w0), magic), sub[mt][0][1]);
+                const uint32_t c1 = sub_bf16x2(lop_nib(shr<4>(w1), magic), sub[mt][1][1]);
+                const uint32_t c2 = sub_bf16x2(lop_nib(shr<12>(w0), magic), sub[mt][0][1]);
+                const uint32_t c3 = sub_bf16x2(lop_nib(shr<12>(w1), magic), sub[mt][1][1]);
+                if (G == 0)
+                  mma_bf16_zc(accO[mt], c0, c1, c2, c3, bo0, bo1);
+                else
+                  mma_bf16(accO[mt], c0, c1, c2, c3, bo0, bo1);
+              }
+            }
+          }
+          // accE column 2t = sum (q - c) x over sub-block 2t (rows g: [0], g+8:
+          // [2]); accO column 2t+1 likewise for sub-block 2t+1 ([1], [3]).
+  #pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float v = yacc[mt][r];
+              v = fmaf(ds[mt][r][0], accE[mt][2 * r], v);
+              v = fmaf(ee[mt][r][0], xs[0], v);
+              v = fmaf(ds[mt][r][1], accO[mt][2 * r + 1], v);
+              v = fmaf(ee[mt][r][1], xs[1], v);
+              yacc[mt][r] = v;
+            }
+          pbuf ^= 1;
+        }
+        if (++cslot == ST) {
+          cslot = 0;
+          phase ^= 1u;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        yv[part & 1][mt][0] = yacc[mt][0];
+        yv[part & 1][mt][1] = yacc[mt][1];
+      }
+    }
+    // Rows: add the quad's sub-block pairs (t = 0..3).
+#pragma unroll
+    for (int pt = 0; pt < 2; ++pt)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float v = yv[pt][mt][r];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          yv[pt][mt][r] = v;
+        }
+    const int row0 = tile * TR;
+    if (KP == 1) {
+      if (ok && t == 0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int row = row0 + mt * 16 + g + 8 * r;
+            if (row < o.n)
+              o.y[row] = o.parts == 2 ? silu_mul(yv[0][mt][r], yv[1][mt][r]) : yv[0][mt][r];
+          }
+      }
+    } else {
+      // Split K: the KP warps of the stream add their partials in warp order.
+      float *rb = red + ((size_t)(par * kWarps + warp) * 2) * TR;
+      if (t == 0) {
+        const float nanv = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int rr = mt * 16 + g + 8 * r;
+            rb[rr] = ok ? yv[0][mt][r] : nanv;
+            rb[TR + rr] = ok ? yv[1][mt][r] : nanv;
+          }
+      }
+      asm volatile("bar.sync %0, %1;\n" ::"r"(1 + sic), "r"(32 * KP) : "memory");
+      if (kp == 0) {
+        const float *base = red + ((size_t)(par * kWarps + sic * KP) * 2) * TR;
+        for (int rr = lane; rr < TR; rr += 32) {
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < KP; ++w) {
+            gs += base[w * 2 * TR + rr];
+            us += base[w * 2 * TR + TR + rr];
+          }
+          const int row = row0 + rr;
+          if (row < o.n) o.y[row] = o.parts == 2 ? silu_mul(gs, us) : gs;
+        }
+      }
+    }
+  }
+  // A warp that gave up on a wait has let its copies land (drain_ring); a warp
+  // that finished normally has consumed every stage it issued.
+}
+
+// ---------------------------------------------------------------- host side
+
+std::once_flag g_stream_attr[kMaxDevices];
+// Resident CTAs per SM of the four kernels ([MT - 1][op table small/large]),
+// queried once per device after the attributes are set.
+int g_occ[kMaxDevices][2][2];
+
+template <int MT, int NOPS>
+constexpr auto stream_kernel() {
+  return gemv_stream_kernel<MT, NOPS>;
+}
+
+template <int MT, int NOPS>
+int stream_occupancy() {
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, stream_kernel<MT, NOPS>(),
+                                                    kWarps * 32, StreamCfg<MT>::kSmem) !=
+      cudaSuccess)
+    return 0;
+  return blocks;
+}
+
+void stream_attributes(int dev) {
+  cudaFuncSetAttribute(stream_kernel<1, 1>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       StreamCfg<1>::kSmem);
+  cudaFuncSetAttribute(stream_kernel<2, 1>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       StreamCfg<2>::kSmem);
+  cudaFuncSetAttribute(stream_kernel<1, kMaxOps>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       StreamCfg<1>::kSmem);
+  cudaFuncSetAttribute(stream_kernel<2, kMaxOps>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       StreamCfg<2>::kSmem);
+  g_occ[dev][0][0] = stream_occupancy<1, 1>();
+  g_occ[dev][0][1] = stream_occupancy<1, kMaxOps>();
+  g_occ[dev][1][0] = stream_occupancy<2, 1>();
+  g_occ[dev][1][1] = stream_occupancy<2, kMaxOps>();
+}
+
+struct StreamPlan {
+  int mt = 0, kp = 1, grid = 0;
+};
+
+// Split: the least splitting that still gives every resident warp a tile
+// (1, 2, else 4 warps per tile).  Tiles are 16 rows: 32-row tiles (fewer
+// resident warps, twice the registers) measured slower on the 27B-class pass.
+StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
+                       const DeviceFacts *f) {
+  const int cand[3][2] = {{Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 1},
+                          {Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 2},
+                          {Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 4}};
+  StreamPlan best;
+  for (const auto &c : cand) {
+    const int mt = c[0], kp = c[1];
+    if (Q4K_STREAM_FORCE_MT && mt != Q4K_STREAM_FORCE_MT) continue;
+    if (Q4K_STREAM_FORCE_KP && kp != Q4K_STREAM_FORCE_KP) continue;
+    const int occ = mt == 1 ? occ1 : occ2;
+    if (occ <= 0) continue;
+    const long long tiles = mt == 1 ? tiles1 : tiles2;
+    const long long warps = (long long)occ * f->sm_count * kWarps;
+    best.mt = mt;
+    best.kp = kp;
+    const long long ctas_needed = (tiles * kp + kWarps - 1) / kWarps;
+    best.grid = (int)std::min<long long>((long long)occ * f->sm_count, ctas_needed);
+    if (tiles * kp >= warps) break;
+  }
+  return best;
+}
+
+template <int MT, int NOPS>
+cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int kp, int grid,
+                                bool overlap, cudaStream_t stream) {
+  StreamParams<NOPS> prm;
+  memset(&prm, 0, sizeof prm);
+  const int TR = 16 * MT;
+  long long total = 0;
+  int nops = 0;
+  for (int i = 0; i < count; ++i) {
+    const StreamOpDesc &d = ops[i];
+    if (d.n <= 0) continue;
+    StreamOp &o = prm.op[nops++];
+    o.w = static_cast<const uint8_t *>(d.w);
+    o.w2 = static_cast<const uint8_t *>(d.w_up);
+    o.x = static_cast<const __nv_bfloat16 *>(d.x);
+    o.y = d.y;
+    o.n = (int)d.n;
+    o.nsb = (int)(d.k / kQK);
+    o.ntiles = (int)((d.n + TR - 1) / TR);
+    o.parts = d.w_up ? 2 : 1;
+    o.byte0 = total;
+    total += (long long)d.n * o.nsb * kBlockBytes * o.parts;
+  }
+  if (nops == 0) return cudaSuccess;
+  prm.nops = nops;
+  prm.kp = kp;
+  prm.pre = overlap ? Q4K_STREAM_PRE : 0;
+  prm.nstreams = grid * (kWarps / kp);
+  prm.total = total;
+  prm.err = device_error_word();
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)StreamCfg<MT>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, stream_kernel<MT, NOPS>(), prm);
+}
+
+}  // namespace
+
+cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
+                          cudaStream_t stream) {
+  const DeviceFacts *f = device_facts();
+  std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
+  int64_t i = 0;
+  while (i < count) {
+    // a chunk: up to kMaxOps ops with rows
+    int64_t j = i, used = 0;
+    long long tiles1 = 0, tiles2 = 0;
+    while (j < count && used < kMaxOps) {
+      if (ops[j].n > 0) {
+        ++used;
+        tiles1 += (ops[j].n + 15) / 16;
+        tiles2 += (ops[j].n + 31) / 32;
+      }
+      ++j;
+    }
+    if (used > 0) {
+      const bool single = used == 1;
+      const int occ1 = g_occ[f->device][0][single ? 0 : 1];
+      const int occ2 = g_occ[f->device][1][single ? 0 : 1];
+      const StreamPlan pl = plan_stream(tiles1, tiles2, occ1, occ2, f);
+      if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
+      const StreamOpDesc *chunk = ops + i;
+      const int n = (int)(j - i);
+      cudaError_t e;
+      if (single)
+        e = pl.mt == 1 ? launch_stream_chunk<1, 1>(chunk, n, pl.kp, pl.grid, overlap, stream)
+                       : launch_stream_chunk<2, 1>(chunk, n, pl.kp, pl.grid, overlap, stream);
+      else
+        e = pl.mt == 1 ? launch_stream_chunk<1, kMaxOps>(chunk, n, pl.kp, pl.grid, overlap, stream)
+                       : launch_stream_chunk<2, kMaxOps>(chunk, n, pl.kp, pl.grid, overlap, stream);
+      if (e != cudaSuccess) return e;
+    }
+    i = j;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace q4k

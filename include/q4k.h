@@ -36,8 +36,10 @@
  * starts at byte r * (K/256) * 144.  y = W x.
  *
  * Conventions for every call
- *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns
- *     every buffer.  Outputs must not alias inputs.
+ *   - All pointers are DEVICE pointers unless stated otherwise: memory of the
+ *     CURRENT device (cudaMalloc or a pool on it).  Host, pinned, managed or
+ *     another GPU's memory is rejected with Q4K_ERR_MEMORY before anything is
+ *     launched.  The caller owns every buffer.  Outputs must not alias inputs.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *     asynchronous on that stream and never synchronize, except
  *     q4k_get_device_error.  They keep no per-call state and are thread-safe.
@@ -51,7 +53,13 @@
  *   - Numerics: dequantized weights are the exact value rounded once to fp32
  *     (q4k_dequant is bit-exact).  Contractions accumulate in fp32; GEMV and
  *     MoE results satisfy |y - y_ref| <= 2e-3 * sum_k |w_k| |x_k| per element,
- *     the prefill GEMM (bf16 tensor-core operands) 1e-2 * sum_k |w_k||x_k|.
+ *     the prefill GEMM (bf16 tensor-core operands) 1e-2 * sum_k |w_k||x_k|,
+ *     for every finite input whose products and sums stay in fp32 range.  The
+ *     decode kernels take sub-block j of a row as w = ds (q - c) + e (ds =
+ *     d sc_j, c the integer in [0, 16] nearest to dmin m_j / ds, e = ds c -
+ *     dmin m_j), so exactly-zero weights give exactly-zero products and a row
+ *     whose weights all cancel gives exactly 0; x enters the tensor cores as
+ *     bf16, unscaled.
  */
 #ifndef Q4K_H
 #define Q4K_H
@@ -63,7 +71,7 @@
 extern "C" {
 #endif
 
-#define Q4K_ABI_VERSION 1
+#define Q4K_ABI_VERSION 2
 
 /* Return codes of every entry point. */
 enum q4k_status {
@@ -75,7 +83,8 @@ enum q4k_status {
     Q4K_ERR_WORKSPACE = 4, /* workspace NULL or smaller than the size query says      */
     Q4K_ERR_DEVICE = 5,    /* current device is not sm_103 (GB300)                    */
     Q4K_ERR_CUDA = 6,      /* a CUDA call or kernel launch failed                      */
-    Q4K_ERR_DATA = 7       /* q4k_get_device_error: a kernel reported bad data         */
+    Q4K_ERR_DATA = 7,      /* q4k_get_device_error: a kernel reported bad data         */
+    Q4K_ERR_MEMORY = 8     /* a pointer is not device memory of the current device     */
 };
 
 /* Bits of the device error word (q4k_get_device_error). */
@@ -93,7 +102,8 @@ const char *q4k_status_str(int status);
  *   out     device, N x K row-major; out_dtype 0 = fp32 (bit-exact: the exact
  *           weight rounded once to nearest even), 1 = bf16 (that fp32 value
  *           rounded to nearest even bf16).  16-byte aligned.
- * Errors: NULL, SHAPE (k % 256, n < 0, out_dtype not 0/1), ALIGN, DEVICE, CUDA.
+ * Errors: NULL, SHAPE (k % 256, n < 0, out_dtype not 0/1), ALIGN, DEVICE, MEMORY,
+ * CUDA.
  */
 int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, void *stream);
 
@@ -107,7 +117,7 @@ int q4k_dequant(const void *w, int64_t n, int64_t k, void *out, int out_dtype, v
  *   x       device, batch x K bf16, row stride ldx >= K; x 16-byte aligned and
  *           ldx a multiple of 8
  *   y       device, batch x N fp32, row stride ldy >= N; 4-byte aligned
- * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, MEMORY, CUDA.
  */
 int q4k_gemv(const void *w, int64_t n, int64_t k, const void *x, int64_t batch, int64_t ldx,
              float *y, int64_t ldy, void *stream);
@@ -130,21 +140,46 @@ int q4k_gemv_ex(const void *w, int64_t n, int64_t k, const void *x, int64_t batc
                 float *y, int64_t ldy, uint32_t flags, void *stream);
 
 /*
- * q4k_gemv_seq -- a sequence of decode projections launched in order on one
- * stream by one call: the same as calling q4k_gemv_ex for ops[0], ops[1], ..
- * in turn with the same batch, flags and stream.  A decode step runs every
- * projection of every layer ("spec: specialized model runtimes", section
- * "Development sequence": decode throughput is the metric); one call keeps the
- * host cost per projection to the library's own launch path.
+ * q4k_gemv_glu -- fused gate/up decode projection of a dense (or shared-expert)
+ * FFN: H[b, i] = silu((Wg X[b])_i) * (Wu X[b])_i, silu(g) = g / (1 + exp(-g)),
+ * for b < batch (1..16), computed in fp32 from the two fp32 projections.
+ * ("Layer Package Repository Spec", sections "Policy Resolution" and
+ *  "Execution Policy": merged shared gate/up.)  Both matrices are streamed in
+ * one pass and only H is written.
+ *   w_gate, w_up  device, each N x K Q4_K, 16-byte aligned
+ *   x             as q4k_gemv
+ *   h             device, batch x N fp32, row stride ldh >= N
+ *   flags         as q4k_gemv_ex
+ * Each of g = Wg x and u = Wu x is accurate to the GEMV bound; H is silu(g) u
+ * of those values.  Errors: as q4k_gemv_ex (NULL also for w_up == NULL).
+ */
+int q4k_gemv_glu(const void *w_gate, const void *w_up, int64_t n, int64_t k, const void *x,
+                 int64_t batch, int64_t ldx, float *h, int64_t ldh, uint32_t flags, void *stream);
+
+/*
+ * q4k_gemv_seq -- a sequence of decode projections run in order on one stream
+ * by one call: the same results as calling q4k_gemv_ex (or q4k_gemv_glu for an
+ * op whose w_up is set) for ops[0], ops[1], .. with the same batch, flags and
+ * stream.  A decode step runs every projection of every layer ("spec:
+ * specialized model runtimes", section "Development sequence": decode
+ * throughput is the metric).
  *   ops     host array of `count` q4k_gemv_op, read during the call only; each
- *           op's w, n, k, x, ldx, y, ldy mean what they mean for q4k_gemv
+ *           op's w, n, k, x, ldx, y, ldy mean what they mean for q4k_gemv; w_up
+ *           NULL for a plain projection, the up matrix of a fused gate/up op
+ *           (w is then the gate matrix and y receives silu(W x) * (W_up x))
  *   count   >= 0 (0: nothing to do)
  *   batch   1..16, shared by all ops
- *   flags   as q4k_gemv_ex; Q4K_FLAG_OVERLAP_WEIGHTS applies to every launch
- * Every op is checked before the first launch: on a NULL, SHAPE or ALIGN error
- * nothing is launched.  A launch failure (CUDA) stops the sequence; the ops
- * before it stay enqueued.
- * Errors: NULL (also ops == NULL with count > 0), SHAPE, ALIGN, DEVICE, CUDA.
+ *   flags   as q4k_gemv_ex
+ * At batch 1 the ops run as ONE persistent launch (a new launch every 512
+ * ops) that streams their weights back to back, and ops may run concurrently:
+ * no op of a sequence may read what another op of the same sequence writes
+ * (split dependent projections into separate calls; stream order holds between
+ * calls).  At batch 2..16 each op is its own launch, in order.
+ * Every op is checked before the first launch: on a NULL, SHAPE, ALIGN or
+ * MEMORY error nothing is launched.  A launch failure (CUDA) stops the
+ * sequence; the launches before it stay enqueued.
+ * Errors: NULL (also ops == NULL with count > 0), SHAPE, ALIGN, DEVICE, MEMORY,
+ * CUDA.
  */
 typedef struct q4k_gemv_op {
   const void *w;
@@ -153,6 +188,7 @@ typedef struct q4k_gemv_op {
   int64_t ldx;
   float *y;
   int64_t ldy;
+  const void *w_up; /* NULL, or the up matrix of a fused gate/up op (ABI 2) */
 } q4k_gemv_op;
 int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t flags,
                  void *stream);
@@ -174,7 +210,10 @@ int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t 
  * reads X and W and writes Y only after that kernel has completed.  Should a
  * bounded wait inside the kernel time out, the affected output tiles are left
  * unwritten and q4k_get_device_error reports it.
- * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ * The CTAs of a cluster that share X receive it by one TMA multicast copy; the
+ * tensor map of that copy covers only x, which must be memory of the current
+ * device (checked: Q4K_ERR_MEMORY otherwise).  A call involves one GPU only.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, MEMORY, CUDA.
  */
 int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
              void *y, int64_t ldy, void *stream);
@@ -209,7 +248,7 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k
  *   workspace      device, >= q4k_moe_workspace_size(...) bytes, 16-byte aligned;
  *                  no initial contents needed; calls sharing one workspace
  *                  must not overlap on the GPU.
- * Errors: NULL, SHAPE, ALIGN, WORKSPACE, DEVICE, CUDA.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, DEVICE, MEMORY, CUDA.
  */
 int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64_t expert_stride,
                  int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
@@ -230,6 +269,8 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
  *     no allocating library routine).
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     Should that look-up fail, the call returns Q4K_ERR_CUDA and the next
+ *     call on the device tries again.
  *   - All calls on a device share the one array: calls that overlap on the
  *     GPU (different streams, or concurrent host threads) race on it.  Each
  *     call writes every workspace byte it reads, so no clearing is needed.

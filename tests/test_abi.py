@@ -32,8 +32,9 @@ def _declared():
 
 def test_header_declares_the_four_calls_and_helpers():
     names = _declared()
-    for n in ("q4k_dequant", "q4k_gemv", "q4k_gemm", "q4k_moe_gemv", "q4k_moe_workspace_size",
-              "q4k_get_device_error", "q4k_abi_version", "q4k_status_str"):
+    for n in ("q4k_dequant", "q4k_gemv", "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm",
+              "q4k_moe_gemv", "q4k_moe_workspace_size", "q4k_get_device_error", "q4k_abi_version",
+              "q4k_status_str"):
         assert n in names
 
 
@@ -51,8 +52,8 @@ def test_binding_names_match_the_c_entry_points():
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.q4k_abi_version() == 1
-    for s in range(8):
+    assert L.q4k_abi_version() == 2
+    for s in range(9):
         assert L.q4k_status_str(s).decode()
     assert L.q4k_status_str(99).decode() == "unknown status"
 
@@ -89,6 +90,25 @@ def test_gemv_argument_errors(L):
     assert L.q4k_gemv(P, 4, 256, P, 1, 256, P + 2, 4, None) == 3
 
 
+def test_gemv_glu_argument_errors(L):
+    assert L.q4k_gemv_glu(P, P, 4, 300, P, 1, 304, P, 4, 0, None) == 2
+    assert L.q4k_gemv_glu(P, P, 4, 256, P, 17, 256, P, 4, 0, None) == 2
+    assert L.q4k_gemv_glu(P, P, 4, 256, P, 1, 256, P, 4, 2, None) == 2   # unknown flag bit
+    assert L.q4k_gemv_glu(P, P, 0, 256, P, 1, 256, P, 4, 0, None) == 0   # empty: no-op
+    assert L.q4k_gemv_glu(None, P, 4, 256, P, 1, 256, P, 4, 0, None) == 1
+    assert L.q4k_gemv_glu(P, None, 4, 256, P, 1, 256, P, 4, 0, None) == 1
+    assert L.q4k_gemv_glu(P, P + 8, 4, 256, P, 1, 256, P, 4, 0, None) == 3
+    assert L.q4k_gemv_glu(P, P, 4, 256, P + 2, 1, 256, P, 4, 0, None) == 3
+
+
+def test_gemv_op_struct_layout_matches_the_header():
+    # q4k_gemv_op: w, n, k, x, ldx, y, ldy, w_up -- eight 8-byte fields
+    from bit_block_quantized_q4_gb300 import GemvOp
+    assert ctypes.sizeof(GemvOp) == 64
+    assert [f[0] for f in GemvOp._fields_] == ["w", "n", "k", "x", "ldx", "y", "ldy", "w_up"]
+    assert GemvOp.w_up.offset == 56
+
+
 def test_gemv_seq_checks_every_op_before_launching(L):
     from bit_block_quantized_q4_gb300 import GemvOp
     good = GemvOp(P, 4, 256, P, 256, P, 4)
@@ -104,7 +124,8 @@ def test_gemv_seq_checks_every_op_before_launching(L):
                         (GemvOp(P, 4, 300, P, 304, P, 4), 2),
                         (GemvOp(P, 4, 256, P, 128, P, 4), 2),
                         (GemvOp(P + 4, 4, 256, P, 256, P, 4), 3),
-                        (GemvOp(P, 4, 256, P, 256, P + 2, 4), 3)):
+                        (GemvOp(P, 4, 256, P, 256, P + 2, 4), 3),
+                        (GemvOp(P, 4, 256, P, 256, P, 4, P + 8), 3)):   # misaligned w_up
         ops[2] = bad
         assert L.q4k_gemv_seq(ops, 3, 1, 0, None) == status
     # empty ops only: nothing to launch
@@ -177,12 +198,13 @@ def test_header_compiles_as_c99_and_a_c_program_links(L, tmp_path):
 #include "q4k.h"
 #include <stdio.h>
 int main(void) {
-  q4k_gemv_op ops[1] = {{0, 4, 256, 0, 256, 0, 4}};
+  q4k_gemv_op ops[1] = {{0, 4, 256, 0, 256, 0, 4, 0}};
   uint32_t bits = 0;
   int st = q4k_abi_version() == Q4K_ABI_VERSION ? Q4K_OK : -1;
   st |= q4k_dequant(0, 4, 256, 0, 0, 0);
   st |= q4k_gemv(0, 4, 256, 0, 1, 256, 0, 4, 0);
   st |= q4k_gemv_ex(0, 4, 256, 0, 1, 256, 0, 4, Q4K_FLAG_OVERLAP_WEIGHTS, 0);
+  st |= q4k_gemv_glu(0, 0, 4, 256, 0, 1, 256, 0, 4, 0u, 0);
   st |= q4k_gemv_seq(ops, 1, 1, 0u, 0);
   st |= q4k_gemm(0, 4, 256, 0, 1, 256, 0, 8, 0);
   st |= (int)q4k_moe_workspace_size(8, 1, 2, 256, 256);
@@ -190,6 +212,7 @@ int main(void) {
   st |= q4k_moe_gemv_noalloc(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0);
   st |= q4k_get_device_error(0, &bits);
   st |= q4k_selftest_wait_timeout(0);
+  st |= (int)sizeof(q4k_gemv_op) == 64 ? 0 : 1 << 20;
   printf("%s %d\n", q4k_status_str(st), st);
   return 0;
 }

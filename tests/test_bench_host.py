@@ -40,13 +40,15 @@ def test_traffic_is_reported_only_for_the_captured_sources(tmp_path, monkeypatch
     prof = tmp_path / "profiles"
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    # the summary's sources match the tree: the figure is used
-    (prof / "gemv_b1_27b_layer.md").write_text(
-        f"- dram_bytes_per_launch: 12345\n- kernel_fingerprint_16: {fp}\n")
+    # the summary's sources match the tree: the captured launch's traffic is
+    # scaled to the pass by algorithmic bytes (a 1-layer capture, 64 layers)
+    (prof / "gemv_stream_b1_27b_layer.md").write_text(
+        f"- dram_bytes_per_launch: 1000\n- algorithmic_bytes_per_launch: 990\n"
+        f"- kernel_fingerprint_16: {fp}\n")
     monkeypatch.setattr(bench, "kernel_fingerprint", lambda read=None: fp)
-    assert bench.profiled_traffic() == 12345.0
+    assert bench.profiled_traffic(990 * 64) == 1000 * 64
     # another fingerprint: the capture is stale and no figure is reported
-    (prof / "gemv_b1_27b_layer.md").write_text(
-        "- dram_bytes_per_launch: 12345\n- kernel_fingerprint_16: 0000000000000000\n")
-    assert bench.profiled_traffic() is None
-
+    (prof / "gemv_stream_b1_27b_layer.md").write_text(
+        "- dram_bytes_per_launch: 1000\n- algorithmic_bytes_per_launch: 990\n"
+        "- kernel_fingerprint_16: 0000000000000000\n")
+    assert bench.profiled_traffic(990 * 64) is None

@@ -67,28 +67,138 @@ def test_gemv_many_row_tiles(q4k, n, k):
 
 
 @pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (4, 1), (16, 0)])
-def test_gemv_seq_matches_oracle_and_single_calls(q4k, batch, flags):
+def test_gemv_seq_matches_oracle(q4k, batch, flags):
     # one q4k_gemv_seq call over projections of different shapes (an empty one
-    # among them) equals the oracle, and equals q4k_gemv_ex called per op
-    shapes = [(700, 1280), (0, 512), (2048, 4096), (129, 5120), (4096, 2304)]
-    ws, xs, ys = [], [], []
+    # and a fused gate/up op among them) matches the oracle; a second call gives
+    # bitwise the same result
+    shapes = [(700, 1280), (0, 512), (2048, 4096), (129, 5120), (4096, 2304), (333, 1536)]
+    glu = {5}
+    ws, wus, xs, ys = [], [], [], []
     for i, (n, k) in enumerate(shapes):
         ws.append(synth.q4k_weight(max(n, 1), k, seed=3100 + i, quants="normal"))
-        xs.append(synth.bf16_normal((batch, k), seed=3200 + i))
+        wus.append(synth.q4k_weight(max(n, 1), k, seed=3300 + i) if i in glu else None)
+        xs.append(synth.bf16_normal((batch, k), seed=3200 + i, sigma=0.05 if i in glu else 1.0))
         ys.append(torch.full((batch, max(n, 1)), 7.0, device=DEV))
     dw, dx = [w.to(DEV) for w in ws], [x.to(DEV) for x in xs]
-    ops = q4k.gemv_ops([(w, n, k, x, y) for w, (n, k), x, y in zip(dw, shapes, dx, ys)])
+    dwu = [None if w is None else w.to(DEV) for w in wus]
+    tup = []
+    for w, wu, (n, k), x, y in zip(dw, dwu, shapes, dx, ys):
+        tup.append((w, n, k, x, y) if wu is None else (w, n, k, x, y, wu))
+    ops = q4k.gemv_ops(tup)
     q4k.q4k_gemv_seq(ops, batch, flags)
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
-    for i, ((n, k), w, x, y) in enumerate(zip(shapes, ws, xs, ys)):
+    first = [y.clone() for y in ys]
+    for i, ((n, k), w, wu, x, y) in enumerate(zip(shapes, ws, wus, xs, ys)):
         if n == 0:
             assert bool((y == 7.0).all()), "an empty op writes nothing"
             continue
-        yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
-        check_bound(y.cpu().numpy(), yref, s, TOL, f"seq op {i} {n}x{k} b{batch}")
-        single = _run(q4k, w, n, k, x, flags)
-        assert np.array_equal(single, y.cpu().numpy()), f"seq op {i} differs from a single call"
+        if wu is None:
+            yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+            check_bound(y.cpu().numpy(), yref, s, TOL, f"seq op {i} {n}x{k} b{batch}")
+        else:
+            check_glu(y.cpu().numpy(), w, wu, n, k, x, f"seq glu op {i} {n}x{k} b{batch}")
+    q4k.q4k_gemv_seq(ops, batch, flags)
+    torch.cuda.synchronize()
+    for a, b in zip(first, ys):
+        assert torch.equal(a, b), "a sequence is deterministic"
+
+
+def check_glu(h, wg, wu, n, k, x, what):
+    """h = silu(g) u against the oracle, with g and u each within the GEMV
+    bound: |dh| <= 1.1 dg |u| + |silu(g)| du + 1.1 dg du + 2^-20 |h| (the last
+    term covers fp32 rounding of the SiLU and the product)."""
+    href, g, u, sg, su = oracle.gemv_glu(wg.numpy(), wu.numpy(), n, k, xbits(x))
+    dg, du = TOL * sg, TOL * su
+    sgl = g / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    bound = 1.1 * dg * np.abs(u) + np.abs(sgl) * du + 1.1 * dg * du + 2.0 ** -20 * np.abs(href)
+    err = np.abs(np.asarray(h, np.float64) - href)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{what}: {bad.sum()} outside, worst {np.max(err - bound)}"
+
+
+@pytest.mark.parametrize("n,k,batch", [(1, 256, 1), (77, 1024, 1), (1000, 2560, 1), (300, 4096, 4),
+                                       (130, 1536, 8), (129, 5120, 9), (597, 5120, 16)])
+@pytest.mark.parametrize("sigma", [1.0, 0.02])
+def test_gemv_glu_matches_oracle(q4k, n, k, batch, sigma):
+    # sigma 0.02: g in SiLU's curved region; 1.0: g large, SiLU near identity / 0
+    wg = synth.q4k_weight(n, k, seed=4100 + n + k, quants="normal")
+    wu = synth.q4k_weight(n, k, seed=4200 + n + k)
+    x = synth.bf16_normal((batch, k), seed=4300 + batch, sigma=sigma)
+    h = q4k.q4k_gemv_glu(wg.to(DEV), wu.to(DEV), n, k, x.to(DEV), q4k.Q4K_FLAG_OVERLAP_WEIGHTS)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    check_glu(h.cpu().numpy(), wg, wu, n, k, x, f"glu {n}x{k} b{batch} sigma {sigma}")
+
+
+@pytest.mark.parametrize("batch", [1, 4, 16])
+def test_gemv_glu_27b_gate_up_full_size_sampled_rows(q4k, batch):
+    # the 27B-class gate/up pair (5120 -> 17408), sampled rows
+    n, k = 17408, 5120
+    wg = synth.q4k_weight(n, k, seed=4401, quants="normal", device=DEV)
+    wu = synth.q4k_weight(n, k, seed=4402, quants="normal", device=DEV)
+    x = synth.bf16_normal((batch, k), seed=4403, sigma=0.02, device=DEV)
+    h = q4k.q4k_gemv_glu(wg, wu, n, k, x)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    rows = np.unique(np.concatenate([np.random.default_rng(4404).choice(n, 64, replace=False),
+                                     [0, n - 1]]))
+    ri = torch.from_numpy(rows).to(DEV)
+    check_glu(h[:, ri].cpu().numpy(), wg[ri].cpu(), wu[ri].cpu(), len(rows), k, x.cpu(),
+              f"27b glu b{batch}")
+
+
+def test_gemv_seq_graph_replay_matches_oracle(q4k):
+    # one 27B-class layer's five projections as one q4k_gemv_seq call with
+    # programmatic dependent launch, captured in a CUDA graph; the graph is
+    # replayed twice with x rewritten in between, and every replay's results
+    # match the oracle on sampled rows
+    shapes = [(10240, 5120), (5120, 8192), (17408, 5120), (17408, 5120), (5120, 17408)]
+    ws = [synth.q4k_weight(n, k, seed=4500 + i, quants="normal", device=DEV)
+          for i, (n, k) in enumerate(shapes)]
+    xs = [torch.empty((1, k), dtype=torch.bfloat16, device=DEV) for _, k in shapes]
+    ys = [torch.empty((1, n), dtype=torch.float32, device=DEV) for n, _ in shapes]
+    ops = q4k.gemv_ops([(w, n, k, x, y) for w, (n, k), x, y in zip(ws, shapes, xs, ys)])
+    stream = torch.cuda.Stream(device=DEV)
+    for x in xs:
+        x.normal_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        q4k.q4k_gemv_seq(ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)  # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        q4k.q4k_gemv_seq(ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
+    rng = np.random.default_rng(4600)
+    for rep in range(2):
+        for i, x in enumerate(xs):
+            x.copy_(synth.bf16_normal(x.shape, seed=4700 + 10 * rep + i, device=DEV))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert q4k.q4k_get_device_error() == 0
+        for i, ((n, k), w, x, y) in enumerate(zip(shapes, ws, xs, ys)):
+            rows = np.unique(np.concatenate([rng.choice(n, 48, replace=False), [0, n - 1]]))
+            ri = torch.from_numpy(rows).to(DEV)
+            yref, s = oracle.gemv(w[ri].cpu().numpy(), len(rows), k, xbits(x))
+            check_bound(y[:, ri].cpu().numpy(), yref, s, TOL, f"replay {rep} op {i}")
+
+
+def test_gemv_rejects_memory_of_the_host(q4k):
+    # a pinned host buffer is not device memory of the current device: the call
+    # fails with Q4K_ERR_MEMORY and launches nothing
+    n, k = 64, 512
+    w = synth.q4k_weight(n, k, seed=4800).to(DEV)
+    xh = synth.bf16_normal((1, k), seed=4801).pin_memory()
+    y = torch.full((1, n), 3.0, device=DEV)
+    L = q4k.lib()
+    st = L.q4k_gemv(w.data_ptr(), n, k, xh.data_ptr(), 1, k, y.data_ptr(), n, None)
+    assert st == 8
+    wh = w.cpu().pin_memory()
+    xd = xh.to(DEV)
+    assert L.q4k_gemv(wh.data_ptr(), n, k, xd.data_ptr(), 1, k, y.data_ptr(), n, None) == 8
+    torch.cuda.synchronize()
+    assert bool((y == 3.0).all())
 
 
 def test_gemv_overlap_chain_reads_the_previous_output(q4k):
