@@ -26,7 +26,8 @@ STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN"
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm",
-           "q4k_moe_workspace_size", "q4k_moe_gemv", "q4k_moe_gemv_noalloc",
+           "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
+           "q4k_moe_gemv_noalloc",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
 _lock = threading.Lock()
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
         L.q4k_moe_workspace_size.argtypes = [I32, I32, I32, I64, I64]
+        L.q4k_moe_workspace_views.restype = ctypes.c_int
+        L.q4k_moe_workspace_views.argtypes = [I32, I32, I32, I64, I64, ctypes.POINTER(ctypes.c_uint64)]
         L.q4k_moe_gemv.restype = ctypes.c_int
         L.q4k_moe_gemv.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
                                    P, SZ, P]
@@ -194,6 +197,16 @@ def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=
 
 def q4k_moe_workspace_size(n_experts: int, n_tokens: int, top_k: int, hidden: int, ffn: int) -> int:
     return int(lib().q4k_moe_workspace_size(n_experts, n_tokens, top_k, hidden, ffn))
+
+
+def q4k_moe_workspace_views(n_experts: int, n_tokens: int, top_k: int, hidden: int,
+                            ffn: int) -> dict:
+    """Byte offsets of the intermediate results q4k_moe_gemv leaves in its
+    workspace: pair index per (token, slot), g, u, h and the down outputs."""
+    arr = (ctypes.c_uint64 * 5)()
+    _check(lib().q4k_moe_workspace_views(n_experts, n_tokens, top_k, hidden, ffn, arr),
+           "q4k_moe_workspace_views")
+    return dict(zip(("tj_pair", "g", "u", "h", "p"), (int(v) for v in arr)))
 
 
 def q4k_moe_gemv(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,

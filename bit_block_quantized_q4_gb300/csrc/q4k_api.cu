@@ -303,6 +303,14 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k
   return moe_workspace_size(n_experts, n_tokens, top_k, hidden, ffn);
 }
 
+int q4k_moe_workspace_views(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                            int64_t ffn, uint64_t offsets[5]) {
+  if (!offsets) return Q4K_ERR_NULL;
+  if (n_experts <= 0 || n_tokens <= 0 || top_k <= 0 || hidden <= 0 || ffn <= 0) return Q4K_ERR_SHAPE;
+  moe_workspace_views(n_experts, n_tokens, top_k, hidden, ffn, offsets);
+  return Q4K_OK;
+}
+
 int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64_t expert_stride,
                  int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
                  int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,

@@ -59,6 +59,10 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
                         void *y, int64_t ldy, cudaStream_t stream);
 size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
                           int64_t ffn);
+// Byte offsets in the MoE workspace of: the pair index of every (token, slot)
+// (int32), g, u, h (fp32 [pair][ffn]) and the down outputs (fp32 [pair][hidden]).
+void moe_workspace_views(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                         int64_t ffn, uint64_t out[5]);
 cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
                        const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,

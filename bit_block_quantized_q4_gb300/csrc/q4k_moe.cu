@@ -40,7 +40,7 @@ constexpr int kSlotPairs = 16;               // pairs per work slot
 
 // Workspace layout (all offsets 256-byte aligned).
 struct MoeLayout {
-  size_t meta, slot_expert, slot_start, pair_token, tj_pair, h, h_hi, h_lo, p, total;
+  size_t meta, slot_expert, slot_start, pair_token, tj_pair, g, u, h, h_hi, h_lo, p, total;
   static int max_slots(int E, int P) { return std::min(E, P) + (P + kSlotPairs - 1) / kSlotPairs; }
   MoeLayout(int E, int P, int64_t H, int64_t F) {
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
@@ -51,6 +51,8 @@ struct MoeLayout {
     slot_start = o;  o = al(o + (S + 1) * sizeof(int));
     pair_token = o;  o = al(o + (size_t)P * sizeof(int));
     tj_pair = o;     o = al(o + (size_t)P * sizeof(int));
+    g = o;           o = al(o + (size_t)P * F * sizeof(float));
+    u = o;           o = al(o + (size_t)P * F * sizeof(float));
     h = o;           o = al(o + (size_t)P * F * sizeof(float));
     h_hi = o;        o = al(o + (size_t)P * F * 2);
     h_lo = o;        o = al(o + (size_t)P * F * 2);
@@ -69,7 +71,7 @@ struct MoeArgs {
   int n_experts, n_tokens, top_k;
   int hidden, ffn;
   int *meta, *slot_expert, *slot_start, *pair_token, *tj_pair;
-  float *h, *p;
+  float *g, *u, *h, *p;
   __nv_bfloat16 *h_hi, *h_lo;
   unsigned *err;
 };
@@ -427,6 +429,8 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
             // of four swapped, so that 32-bit words hold (h[o], h[o+2]) and
             // (h[o+1], h[o+3]).
             const int pos = (grow & ~3) | ((grow & 1) << 1) | ((grow >> 1) & 1);
+            a.g[(size_t)(pstart + pr) * a.ffn + grow] = ok ? gg : nan;
+            a.u[(size_t)(pstart + pr) * a.ffn + grow] = ok ? uu : nan;
             a.h[(size_t)(pstart + pr) * a.ffn + grow] = hv;
             a.h_hi[(size_t)(pstart + pr) * a.ffn + pos] = hh;
             a.h_lo[(size_t)(pstart + pr) * a.ffn + pos] = hl;
@@ -556,6 +560,16 @@ size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, in
   return MoeLayout(n_experts, n_tokens * top_k, hidden, ffn).total;
 }
 
+void moe_workspace_views(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                         int64_t ffn, uint64_t out[5]) {
+  const MoeLayout L(n_experts, n_tokens * top_k, hidden, ffn);
+  out[0] = L.tj_pair;
+  out[1] = L.g;
+  out[2] = L.u;
+  out[3] = L.h;
+  out[4] = L.p;
+}
+
 cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
                        const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
@@ -583,6 +597,8 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   a.slot_start = reinterpret_cast<int *>(ws + L.slot_start);
   a.pair_token = reinterpret_cast<int *>(ws + L.pair_token);
   a.tj_pair = reinterpret_cast<int *>(ws + L.tj_pair);
+  a.g = reinterpret_cast<float *>(ws + L.g);
+  a.u = reinterpret_cast<float *>(ws + L.u);
   a.h = reinterpret_cast<float *>(ws + L.h);
   a.h_hi = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_hi);
   a.h_lo = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_lo);

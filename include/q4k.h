@@ -225,6 +225,22 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k
                               int64_t ffn);
 
 /*
+ * q4k_moe_workspace_views -- where q4k_moe_gemv leaves its intermediate
+ * results in the workspace (no counterpart on the pages; for inspection and
+ * stage-by-stage checks).  After a call has completed, the workspace holds at
+ * these byte offsets:
+ *   offsets[0]  int32 [n_tokens * top_k]: the pair index of (token t, slot j)
+ *               at t * top_k + j, or -1 for a skipped (bad) expert id
+ *   offsets[1]  fp32 [pairs][ffn]: g = Wg_e x_t of each pair
+ *   offsets[2]  fp32 [pairs][ffn]: u = Wu_e x_t
+ *   offsets[3]  fp32 [pairs][ffn]: h = silu(g) * u
+ *   offsets[4]  fp32 [pairs][hidden]: Wd_e h (before the route weight)
+ * Errors: NULL, SHAPE.
+ */
+int q4k_moe_workspace_views(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
+                            int64_t ffn, uint64_t offsets[5]);
+
+/*
  * q4k_moe_gemv -- routed mixture-of-experts FFN for decode tokens.
  * ("Layer Package Repository Spec", section "Policy Resolution": routed
  *  gate/up/down expert matmuls, fused SwiGLU, route-weighted sum.)

@@ -65,3 +65,17 @@ def test_dequant_full_size_projection_sampled(q4k):
     ref = oracle.dequant_f32(wc, len(rows), k)
     assert np.array_equal(got[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint32),
                           ref.view(np.uint32))
+
+
+def test_dequant_4096x4096_every_block(q4k):
+    # the 4096 x 4096 single-matrix workload (uniform quants), every block in
+    # fp32 and bf16 against the oracle, bit for bit
+    n = k = 4096
+    w = synth.q4k_weight(n, k, seed=1000)
+    d32 = q4k.q4k_dequant(w.to(DEV), n, k)
+    d16 = q4k.q4k_dequant(w.to(DEV), n, k, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert np.array_equal(d32.cpu().numpy(), oracle.dequant_f32(w.numpy(), n, k))
+    got16 = d16.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got16, oracle.dequant_bf16(w.numpy(), n, k))
+

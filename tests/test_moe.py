@@ -29,12 +29,12 @@ def q4k():
     return m
 
 
-def _make(E, H, F, T, K, seed, quants="uniform"):
+def _make(E, H, F, T, K, seed, quants="uniform", sigma=1.0):
     stride = F * (H // 256) * 144
     wg = synth.q4k_weight(E * F, H, seed=seed, quants=quants).reshape(-1)
     wu = synth.q4k_weight(E * F, H, seed=seed + 1, quants=quants).reshape(-1)
     wd = synth.q4k_weight(E * H, F, seed=seed + 2, quants=quants).reshape(-1)
-    x = synth.bf16_normal((T, H), seed=seed + 3)
+    x = synth.bf16_normal((T, H), seed=seed + 3, sigma=sigma)
     ids, wts = synth.zipf_routing(T, E, K, seed=seed + 4)
     return dict(wg=wg, wu=wu, wd=wd, stride=stride, E=E, H=H, F=F, x=x, ids=ids, wts=wts)
 
@@ -69,7 +69,7 @@ def _bound(c, ids, wts, tokens):
             u = oracle.gemv_f64(ue, F, H, xf[t])[0]
             dg = 2e-3 * oracle.gemv_f64(ge, F, H, np.abs(xf[t]), use_abs=True)[0]
             du = 2e-3 * oracle.gemv_f64(ue, F, H, np.abs(xf[t]), use_abs=True)[0]
-            sg = g / (1.0 + np.exp(-g))
+            sg = g / (1.0 + np.exp(-np.clip(g, -700.0, 700.0)))
             h = sg * u
             dh = 1.1 * dg * np.abs(u) + np.abs(sg) * du + 1.1 * dg * du + 2.0 ** -15 * np.abs(h)
             awd_h = oracle.gemv_f64(de, H, F, np.abs(h), use_abs=True)[0]
@@ -155,3 +155,66 @@ def test_moe_235b_class_sampled_tokens(q4k):
     yref, bound = _bound(c, ids, wts, tokens)
     _check(y.cpu().numpy().astype(np.float64)[tokens], yref, bound, "235B-class")
     assert len(used) > 1
+
+
+def _gpu_stages(q4k, c, ids, wts):
+    """Run with an explicit workspace and read back the per-pair stages."""
+    E, H, F = c["E"], c["H"], c["F"]
+    T, K = ids.shape
+    ws = torch.zeros(q4k.q4k_moe_workspace_size(E, T, K, H, F), dtype=torch.uint8, device=DEV)
+    y = q4k.q4k_moe_gemv(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"], E, H, F,
+                         c["x"].to(DEV), ids.to(DEV), wts.to(DEV), workspace=ws)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    v = q4k.q4k_moe_workspace_views(E, T, K, H, F)
+    P = T * K
+    tj = ws[v["tj_pair"]:v["tj_pair"] + 4 * P].view(torch.int32).cpu().numpy()
+    st = {}
+    for name, width in (("g", F), ("u", F), ("h", F), ("p", H)):
+        st[name] = ws[v[name]:v[name] + 4 * P * width].view(torch.float32).view(P, width).cpu().numpy()
+    return y.cpu().numpy().astype(np.float64), tj, st
+
+
+@pytest.mark.parametrize("sigma", [1.0, 0.01])
+@pytest.mark.parametrize("E,H,F,T,K", [(16, 1024, 512, 16, 8), (8, 512, 768, 5, 3)])
+def test_moe_stagewise(q4k, E, H, F, T, K, sigma):
+    # every stage against the oracle on its own: g and u within the GEMV bound,
+    # h = silu(g) u of the GPU's own g and u, the down projection fed the GPU's
+    # own h, and y = the route-weighted sum of the GPU's own down outputs.
+    # sigma 0.01 keeps |g| small: SiLU's curved region.
+    c = _make(E, H, F, T, K, seed=E + H + T + int(1000 * sigma), sigma=sigma)
+    ids, wts = c["ids"], c["wts"]
+    y, tj, st = _gpu_stages(q4k, c, ids, wts)
+    s = c["stride"]
+    wg, wu, wd = (c[k].numpy() for k in ("wg", "wu", "wd"))
+    xb = xbits(c["x"])
+    _, (g_ref, u_ref, h_ref) = oracle.moe(wg, wu, wd, s, E, H, F, xb, ids.numpy(), wts.numpy(),
+                                           return_stages=True)
+    xf = c["x"].to(torch.float64).numpy()
+    gmax = 0.0
+    for t in range(T):
+        yt = np.zeros(H)
+        for j in range(K):
+            q, e = t * K + j, int(ids[t, j])
+            pos = int(tj[q])
+            assert pos >= 0
+            ge, ue, de = (m[e * s:(e + 1) * s] for m in (wg, wu, wd))
+            sg = oracle.gemv_f64(ge, F, H, np.abs(xf[t]), use_abs=True)[0]
+            su = oracle.gemv_f64(ue, F, H, np.abs(xf[t]), use_abs=True)[0]
+            g, u, h = (st[k][pos].astype(np.float64) for k in ("g", "u", "h"))
+            assert np.all(np.abs(g - g_ref[q]) <= 2e-3 * sg), f"g t{t} j{j}"
+            assert np.all(np.abs(u - u_ref[q]) <= 2e-3 * su), f"u t{t} j{j}"
+            hh = g / (1.0 + np.exp(-np.clip(g, -700, 700))) * u
+            assert np.all(np.abs(h - hh) <= 2.0 ** -18 * np.abs(hh) + 1e-30), f"h t{t} j{j}"
+            pd = oracle.gemv_f64(de, H, F, h)[0]
+            sd = oracle.gemv_f64(de, H, F, np.abs(h), use_abs=True)[0]
+            p = st["p"][pos].astype(np.float64)
+            assert np.all(np.abs(p - pd) <= (2e-3 + 2.0 ** -16) * sd), f"down t{t} j{j}"
+            yt += float(wts[t, j]) * p
+            gmax = max(gmax, float(np.abs(g).max()))
+        bound = 2.0 ** -20 * sum(abs(float(wts[t, j])) * np.abs(st["p"][int(tj[t * K + j])])
+                                 for j in range(K))
+        assert np.all(np.abs(y[t] - yt) <= bound + 1e-30), f"combine t{t}"
+    if sigma < 0.1:
+        assert gmax < 8.0          # the curved region of SiLU is what was tested
+

@@ -209,3 +209,36 @@ def test_gemm_activation_edges(q4k, case):
     assert q4k.q4k_get_device_error() == 0
     yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
     check_bound(y.float().cpu().numpy(), yref, s, 1e-2, f"gemm {case}")
+
+
+def test_moe_cancelling_rows(q4k):
+    # experts whose gate rows 0 mod 3 and down rows 0 mod 3 cancel exactly:
+    # g is exactly 0 there (read back from the workspace), and the hidden rows
+    # whose down rows cancel in every expert come out as exactly 0
+    from test_moe import _gpu_stages
+    E, H, F, T, K = 4, 512, 768, 6, 2
+    nsb_h, nsb_f = H // 256, F // 256
+    rng = np.random.default_rng(40)
+
+    def mat(rows, nsb):
+        out = []
+        for r in range(rows):
+            if r % 3 == 0:
+                out.append(b"".join(_cancel_block(rng) for _ in range(nsb)))
+            else:
+                out.append(b"".join(pack_block(*random_fields(rng)) for _ in range(nsb)))
+        return b"".join(out)
+
+    wg = torch.frombuffer(bytearray(b"".join(mat(F, nsb_h) for _ in range(E))), dtype=torch.uint8)
+    wu = synth.q4k_weight(E * F, H, seed=41).reshape(-1)
+    wd = torch.frombuffer(bytearray(b"".join(mat(H, nsb_f) for _ in range(E))), dtype=torch.uint8)
+    x = synth.bf16_normal((T, H), seed=42)
+    ids, wts = synth.zipf_routing(T, E, K, seed=43)
+    c = dict(wg=wg, wu=wu, wd=wd, stride=F * nsb_h * 144, E=E, H=H, F=F, x=x)
+    y, tj, st = _gpu_stages(q4k, c, ids, wts)
+    assert np.all(st["g"][:, 0::3] == 0.0) and np.all(st["h"][:, 0::3] == 0.0)
+    assert np.all(y[:, 0::3] == 0.0)
+    from test_moe import _bound, _check
+    yref, bound = _bound(c, ids, wts, list(range(T)))
+    _check(y, yref, bound, "moe cancel")
+

@@ -61,6 +61,22 @@ def test_noalloc_matches_workspace_call_twice_in_a_row(q4k):
 
 
 @pytest.mark.gpu
+def test_noalloc_allocates_no_device_memory(q4k):
+    # after one warm-up call (which looks up the array's address), further
+    # calls leave the device's free memory, as the driver reports it, unchanged
+    from test_moe import _make
+    c = _make(16, 1024, 512, 16, 8, seed=303)
+    _noalloc_c_abi(q4k, c, c["ids"], c["wts"])
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc_c_abi(q4k, c, c["ids"], c["wts"])
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
+@pytest.mark.gpu
 def test_noalloc_rejects_problems_larger_than_its_array(q4k):
     L = q4k.lib()
     E, H, F, T, K = 64, 8192, 4096, 64, 8      # workspace far above the fixed array
