@@ -419,6 +419,69 @@ def cpu_baseline(layers, budget_s=12.0):
                       f"({done_bytes / 1e9:.2f} GB of Q4_K weights), {elapsed:.1f} s of oracle time"}
 
 
+def cpu_table(budget_s: float = 6.0) -> dict:
+    """The oracle on the host cores, single-threaded and with every core, for
+    each configuration, on bounded samples (whole projections or rows of them,
+    stated per entry); no GPU involved.  Units: GB/s of Q4_K weights streamed
+    (GEMV, MoE) or GFLOP/s (prefill GEMM)."""
+    import oracle
+    oracle.build()
+    ncores = oracle.num_threads()
+    out = {"cores_all": ncores}
+
+    def timed(fn, min_s=0.5):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_s or reps >= 50:
+                return el / reps
+
+    def both(name, fn, amount, unit, sample):
+        res = {"unit": unit, "sample": sample}
+        for label, th in (("1_core", 1), ("all_cores", ncores)):
+            oracle.set_num_threads(th)
+            sec = timed(fn)
+            res[label] = round(amount / sec / 1e9, 4)
+        oracle.set_num_threads(ncores)
+        out[name] = res
+
+    def xbits(x):
+        return x.view(torch.int16).numpy().view(np.uint16)
+
+    w0 = synth.q4k_weight(1024, 4096, seed=synth.derive_seed(1000, "cpu")).numpy()
+    x0 = xbits(synth.bf16_normal((1, 4096), seed=1000))
+    both("c0_gemv_4096_b1", lambda: oracle.gemv(w0, 1024, 4096, x0), 1024 * 16 * 144, "GB/s",
+         "1024 of the 4096 rows of a 4096 x 4096 matrix")
+    rows = 512
+    lay = [(n, k, synth.q4k_weight(rows, k, seed=synth.derive_seed(SEED_C1, "cpu", i), quants="normal").numpy())
+           for i, (_, n, k) in enumerate(LAYER_SHAPES)]
+    for b in (1, 4, 16):
+        xs = [xbits(synth.bf16_normal((b, k), seed=synth.derive_seed(SEED_C1, "cpux", b, i)))
+              for i, (_, k, _) in enumerate(lay)]
+        nbytes = sum(q4k_bytes(rows, k) for _, k, _ in lay)
+        both(f"c{1 if b == 1 else 2}_27b_layer_b{b}",
+             lambda xs=xs: [oracle.gemv(w, rows, k, x) for (_, k, w), x in zip(lay, xs)], nbytes,
+             "GB/s", f"the first {rows} rows of each of the 5 projections of one layer, batch {b}")
+    m = 16
+    wg = synth.q4k_weight(256, 5120, seed=synth.derive_seed(1003, "cpu"), quants="normal").numpy()
+    xg = xbits(synth.bf16_normal((m, 5120), seed=1003, sigma=0.5))
+    both("c3_prefill_gate", lambda: oracle.gemv(wg, 256, 5120, xg), 2.0 * m * 256 * 5120, "GFLOP/s",
+         f"{m} tokens x 256 rows of the 512-token gate projection")
+    E, H, F, T, K = 16, 4096, 1536, 4, 8
+    stride = F * (H // 256) * 144
+    mg = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1004, "cg")).numpy().reshape(-1)
+    mu = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1004, "cu")).numpy().reshape(-1)
+    md = synth.q4k_weight(E * H, F, seed=synth.derive_seed(1004, "cd")).numpy().reshape(-1)
+    mx = xbits(synth.bf16_normal((T, H), seed=1004))
+    ids, wts = synth.zipf_routing(T, E, K, seed=1005)
+    both("c4_moe_235b", lambda: oracle.moe(mg, mu, md, stride, E, H, F, mx, ids.numpy(), wts.numpy()),
+         T * K * 3 * q4k_bytes(F, H), "GB/s",
+         f"{T} tokens, top-{K} of {E} experts (128-expert shapes), bytes counted per (token, slot)")
+    return out
+
+
 def bench_prefill(q4k, dev, stream, reps=20):
     """512-token prefill: gate (5120 -> 17408) and down (17408 -> 5120), each
     timed on its own (events around `reps` launches; weights 50 MB each, X
@@ -624,9 +687,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="time the oracle on the host cores for every configuration, then exit")
     ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "moe"],
                     help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
+    if args.cpu_table:
+        print(json.dumps(cpu_table()), flush=True)
+        return
     if args.case:
         run_case(args.case)
         return

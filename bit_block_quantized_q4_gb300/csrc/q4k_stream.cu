@@ -110,7 +110,9 @@ struct StreamCfg {
   static constexpr int kRows = 16 * MT;
   static constexpr int kSB = Q4K_STREAM_SB;  // super-blocks per stage
   static constexpr int kStages = MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2;
-  static constexpr int kRowBytes = kSB * kBlockBytes;  // a row's bytes in a stage
+  // a row's slot in a stage: its kSB super-blocks, padded by 16 bytes when
+  // kSB is even so that the 16*MT rows fall on different shared-memory banks
+  static constexpr int kRowBytes = kSB * kBlockBytes + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
   static constexpr int kXStage = kSB * kXBytes;        // x bytes of a stage
   // warp region: ring weights | ring x | 2 permuted-x buffers | 64 zero bytes |
@@ -244,8 +246,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 // w >> n, as a shift (ALU pipe) or as the high half of w * 2^(32-n) (FMA pipe).
 template <int N>
 __device__ __forceinline__ uint32_t shr(uint32_t w) {
-#if Q4K_STREAM_SHIFT_MUL
+#if Q4K_STREAM_SHIFT_MUL == 1
   return __umulhi(w, 1u << (32 - N));
+#elif Q4K_STREAM_SHIFT_MUL == 2
+  return N == 8 ? __umulhi(w, 1u << 24) : w >> N;
 #else
   return w >> N;
 #endif
