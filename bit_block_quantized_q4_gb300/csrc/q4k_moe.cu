@@ -3,24 +3,30 @@
 // routed-FFN decode layer is the routed gate/up/down expert matmuls (96% of its
 // time), a fused SwiGLU, and the route-weighted sum).
 //
-// Four launches on the caller's stream:
+// Two launches on the caller's stream:
 //   1. route    one CTA groups the T*k (token, slot) pairs by expert (counting
-//               sort; experts ordered by id, at most 16 pairs per work slot, so a
+//               sort; experts ordered by id, at most 8 pairs per work slot, so a
 //               heavily used expert spans several slots), validates ids (an id
-//               out of range is skipped and flagged in the device error word).
-//   2. gate/up  per work slot, warp streams of 16-row tiles of ffn: the
-//               expert's gate and up rows are streamed once (TMA) and contracted
-//               with all of the slot's tokens on the tensor cores (MMA columns =
-//               tokens); the epilogue writes h = silu(g) * u in fp32 and as two
-//               bf16 columns per pair, h_hi = bf16(h) and h_lo = bf16(h - h_hi)
-//               (together 16 significant bits), stored in MMA fragment order.
-//   3. down     per work slot, warp streams of 16-row tiles of hidden, full K
-//               (ffn) per tile; MMA columns = (h_hi, h_lo) of each pair; the
-//               epilogue writes p = Wd h per pair.
-//   4. combine  y[t] = sum_j w[t, j] * p[t, j] in slot order j = 0..k-1.
-// Grids are sized for the worst case; CTAs whose slot is not in use exit at
-// once.  Results do not depend on the order of pairs inside a group (columns of
-// an MMA are independent).
+//               out of range is skipped and flagged in the device error word)
+//               and clears the work counters of launch 2.
+//   2. experts  one persistent kernel, every CTA resident.  CTAs pull work items
+//               in order from a counter: first the gate/up items (work slot,
+//               64 rows of ffn), then the down items (work slot, 128 rows of
+//               hidden).  A gate/up item streams the expert's gate and up rows
+//               once (TMA) and contracts them with all of the slot's tokens on
+//               the tensor cores (MMA columns = tokens); it writes g, u and
+//               h = silu(g) * u in fp32, and h as two bf16 columns per pair,
+//               h_hi = bf16(h) and h_lo = bf16(h - h_hi) (16 significant bits
+//               together), in MMA fragment order.  A down item waits (bounded)
+//               until every gate/up item of its slot is done, streams the
+//               expert's down rows and writes p = Wd h per pair.  The CTA that
+//               completes the last down item of a 128-row group of hidden adds
+//               y[t] = sum_j w[t, j] * p[t, j] over the slots j = 0..k-1 of
+//               every token, in that order.
+// Items are claimed in order and every CTA is resident, so a down item only
+// waits on gate/up items already held by running CTAs.  Results do not depend
+// on which CTA runs which item (columns of an MMA are independent; the sums
+// are in fixed order).
 #include <algorithm>
 #include <mutex>
 
@@ -36,17 +42,36 @@ constexpr int kTile = kRows * kBlockBytes;   // 2304 bytes per super-block stage
 constexpr int kStagesMoe = 4;
 constexpr int kMoeWarps = 4;                 // warps (weight streams) per expert CTA
 constexpr int kMaxExperts = 2048;
-constexpr int kSlotPairs = 16;               // pairs per work slot
+#ifndef Q4K_MOE_SLOT_PAIRS  // pairs per work slot at most
+#define Q4K_MOE_SLOT_PAIRS 8
+#endif
+constexpr int kSlotPairs = Q4K_MOE_SLOT_PAIRS;
 
 // Workspace layout (all offsets 256-byte aligned).
+// Ring of a warp stream: kStagesMoe stages of kStageStride bytes (a gate and
+// an up tile per stage; a down stage uses the first half), then the stage
+// barriers; TMA destinations must be 128-byte aligned, so the region is
+// rounded up.
+constexpr int kStageStride = 2 * kTile;
+constexpr int kWarpBytes = (kStagesMoe * kStageStride + 8 * kStagesMoe + 127) / 128 * 128;
+constexpr int kMetaAbort = 2;  // workspace meta word: a wait timed out, stop taking items
+constexpr int kGuTilesPerItem = 4;  // 16-row tiles of ffn per gate/up item (one per warp)
+constexpr int kDnTilesPerItem = 8;  // 16-row tiles of hidden per down item (two per warp)
+
 struct MoeLayout {
-  size_t meta, slot_expert, slot_start, pair_token, tj_pair, g, u, h, h_hi, h_lo, p, total;
+  size_t meta, counters, slot_expert, slot_start, pair_token, tj_pair, g, u, h, h_hi, h_lo, p, total;
+  int n_counters;
   static int max_slots(int E, int P) { return std::min(E, P) + (P + kSlotPairs - 1) / kSlotPairs; }
+  static int dn_groups(int64_t H) { return (int)((H + 16 * kDnTilesPerItem - 1) / (16 * kDnTilesPerItem)); }
   MoeLayout(int E, int P, int64_t H, int64_t F) {
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t S = (size_t)max_slots(E, P);
+    // work counters: [0] next item, [1 .. 1+S) gate/up items done per slot,
+    // [1+S ..) down items done per 128-row group of hidden
+    n_counters = 1 + (int)S + dn_groups(H);
     size_t o = 0;
     meta = o;        o = al(o + 16 * sizeof(int));
+    counters = o;    o = al(o + (size_t)n_counters * sizeof(int));
     slot_expert = o; o = al(o + S * sizeof(int));
     slot_start = o;  o = al(o + (S + 1) * sizeof(int));
     pair_token = o;  o = al(o + (size_t)P * sizeof(int));
@@ -71,6 +96,8 @@ struct MoeArgs {
   int n_experts, n_tokens, top_k;
   int hidden, ffn;
   int *meta, *slot_expert, *slot_start, *pair_token, *tj_pair;
+  int *counters;
+  int n_counters, max_slots;
   float *g, *u, *h, *p;
   __nv_bfloat16 *h_hi, *h_lo;
   unsigned *err;
@@ -90,6 +117,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
   __shared__ int wsum[32], wact[32];
   const int E = a.n_experts, P = a.n_tokens * a.top_k;
   const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < a.n_counters; i += nt) a.counters[i] = 0;
   for (int e = tid; e < E; e += nt) cnt[e] = fill[e] = 0;
   __syncthreads();
   for (int q = tid; q < P; q += nt) {
@@ -154,6 +182,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
   if (tid == nt - 1) {
     a.meta[0] = run_a;  // work slots in use
     a.meta[1] = run_s;  // valid pairs
+    a.meta[kMetaAbort] = 0;
   }
   __syncthreads();
   for (int e = tid; e < E; e += nt) {
@@ -173,57 +202,51 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
   }
 }
 
-// ---------------------------------------------------------------- 2./3. experts
-// One CTA = kMoeWarps warps of work slot blockIdx.y.  Warp stream
-// s = blockIdx.x * kMoeWarps + warp takes the slot's 16-row m-tiles s, s + S,
-// s + 2S, ... (S = gridDim.x * kMoeWarps), each over the full K; its ring of
-// weight stages and its x fragments run ahead continuously across those tiles,
-// and each tile's result is written straight from the accumulators.  MMA
+// ---------------------------------------------------------------- expert contraction
+// A warp stream takes 16-row m-tiles of one slot's expert, each over the full
+// K; its ring of weight stages and its x fragments run ahead continuously
+// across those tiles, and each tile's result is written straight from the
+// accumulators.  MMA
 // columns are the slot's pairs:
 //   gate/up (DOWN = false): column c = x row of the c-th pair's token;
 //   down    (DOWN = true):  column 2i = h_hi, column 2i+1 = h_lo of pair i.
 // Thread t's k-slots (2t, 2t+1) carry positions (o, o+2) and (2t+8, 2t+9)
 // positions (o+1, o+3) of a sub-block, o = 8t + 4s for step s = 0/1: quant
 // bytes 8t .. 8t+7 of the sub-block's 32-byte chunk.
-// One CTA's work for a slot with at most 8 NT MMA columns.
+// One warp's tiles of a slot with at most 8 NT MMA columns: tiles sid, sid +
+// nsid, ... below tile_end.  The warp's ring (kStagesMoe stages of
+// kStageStride bytes at `ring`, barriers `bars`, initialised once per kernel)
+// carries on from ring iteration it0, which is advanced past this call's
+// iterations.  Returns false after a timed-out wait (its copies in flight
+// were given a bounded time to land; the ring must not be used again).
 template <int NT, bool DOWN>
-__device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUtensorMap *map1p,
+__device__ __forceinline__ bool expert_body(const CUtensorMap *map0p, const CUtensorMap *map1p,
                                             const MoeArgs &a, int nsb, int rows_total,
-                                            uint8_t *smem, int slot, int ctas) {
+                                            uint8_t *ring, uint64_t *bars, uint32_t &it0,
+                                            int slot, int sid, int nsid, int tile_end) {
   const CUtensorMap &map0 = *map0p, &map1 = *map1p;
   constexpr int NM = DOWN ? 1 : 2;  // weight matrices per stage (gate and up)
   constexpr int kStageBytes = NM * kTile;
-  // TMA destinations must be 128-byte aligned: round each warp's region up.
-  constexpr int kWarpBytes = (kStagesMoe * kStageBytes + 64 + 127) / 128 * 128;
   const int expert = a.slot_expert[slot];
   const int pstart = a.slot_start[slot];
-  const int np = a.slot_start[slot + 1] - pstart;  // pairs of this slot (<= 16)
+  const int np = a.slot_start[slot + 1] - pstart;  // pairs of this slot (<= kSlotPairs)
   const int ncols = DOWN ? 2 * np : np;
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int ntiles = (rows_total + kRows - 1) / kRows;
-  const int sid = blockIdx.x * kMoeWarps + warp, nsid = ctas * kMoeWarps;
+  const int ntiles = min((rows_total + kRows - 1) / kRows, tile_end);
   const int ntl = sid < ntiles ? (ntiles - sid + nsid - 1) / nsid : 0;  // tiles of this warp
   const int total = ntl * nsb;                                          // ring iterations
-  uint8_t *ring = smem + warp * kWarpBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kStagesMoe * kStageBytes);
-
-  if (lane == 0) {
-    prefetch_tmap(&map0);
-    if (NM == 2) prefetch_tmap(&map1);
-    for (int s = 0; s < kStagesMoe; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
+  const uint32_t base = it0;
   const uint64_t policy = l2_evict_first_policy();
-  // Ring iteration q = super-block q % nsb of this warp's tile q / nsb.
+  // Ring iteration q = super-block q % nsb of this warp's tile q / nsb; it
+  // uses stage (base + q) % kStagesMoe.
   auto issue = [&](int q) {
     const int j = q / nsb, u = q - j * nsb;
     const int row0 = (sid + j * nsid) * kRows;
-    const int stage = q % kStagesMoe;
+    const uint32_t stage = (base + (uint32_t)q) % kStagesMoe;
     mbar_arrive_expect_tx(&bars[stage], kStageBytes);
-    uint8_t *dst = ring + stage * kStageBytes;
+    uint8_t *dst = ring + stage * kStageStride;
     tma_load_3d_hint(dst, &map0, &bars[stage], u * (kBlockBytes / 8), row0, expert, policy);
     if (NM == 2)
       tma_load_3d_hint(dst + kTile, &map1, &bars[stage], u * (kBlockBytes / 8), row0, expert,
@@ -257,9 +280,11 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int64_t off = (int64_t)u * kQK + 32 * (ch * CJ + jj) + 8 * t;
-        dst[jj][nt] = (cval[nt] && q < total)
-                          ? __ldg(reinterpret_cast<const uint4 *>(src[nt] + off))
-                          : make_uint4(0, 0, 0, 0);
+        // h (down) is written by this kernel's gate/up items: read it through
+        // L2, not the read-only path; x is the caller's and read-only
+        const uint4 *ptr = reinterpret_cast<const uint4 *>(src[nt] + off);
+        dst[jj][nt] = (cval[nt] && q < total) ? (DOWN ? __ldcg(ptr) : __ldg(ptr))
+                                              : make_uint4(0, 0, 0, 0);
       }
   };
   uint4 xbuf[2][CJ][NT];
@@ -276,18 +301,23 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
         yacc[mi][nt][0] = yacc[mi][nt][1] = yacc[mi][nt][2] = yacc[mi][nt][3] = 0.f;
     for (int u = 0; u < nsb && ok; ++u) {
       const int q = j * nsb + u;
-      const int stage = q % kStagesMoe;
-      if (!mbar_wait(&bars[stage], (uint32_t)((q / kStagesMoe) & 1), a.err)) {
+      const uint32_t gq = base + (uint32_t)q;
+      const uint32_t stage = gq % kStagesMoe;
+      if (!mbar_wait(&bars[stage], (gq / kStagesMoe) & 1u, a.err)) {
         ok = false;
-        if (lane == 0) {  // let this warp's copies in flight land (bounded)
+        if (lane == 0) {
+          atomicExch(&a.meta[kMetaAbort], 1);  // every CTA stops taking items
+          // let this warp's copies in flight land (bounded)
           const uint64_t t0 = global_ns();
-          for (int r = q; r < min(q + kStagesMoe, total); ++r)
-            while (!mbar_try_wait(&bars[r % kStagesMoe], (uint32_t)((r / kStagesMoe) & 1), 1000u))
+          for (int r = q; r < min(q + kStagesMoe, total); ++r) {
+            const uint32_t gr = base + (uint32_t)r;
+            while (!mbar_try_wait(&bars[gr % kStagesMoe], (gr / kStagesMoe) & 1u, 1000u))
               if (global_ns() - t0 > kWaitLimitNs) break;
+          }
         }
         break;
       }
-      const uint8_t *st = ring + stage * kStageBytes;
+      const uint8_t *st = ring + stage * kStageStride;
       uint4 hdr[NM][2];
       uint2 qw[NM][2][4];
 #pragma unroll
@@ -438,57 +468,150 @@ __device__ __forceinline__ void expert_body(const CUtensorMap *map0p, const CUte
         }
       }
   }
+  it0 = base + (uint32_t)total;
+  return ok;
 }
 
-// The MMA width follows the slot: 8 columns when its pairs fit, else 16 or 32
-// (NTMAX n-tiles of 8 at most), so a slot with few pairs does no work for
-// empty columns.  A slot with nt n-tiles gets nt times the warp streams (each
-// with 1/nt of the row tiles), so every stream does about the same work; the
-// grid is sized for the widest class (one tile per stream at NTMAX) and the
-// CTAs a slot does not need exit.  The choice is uniform per CTA.
+// One slot's share of an item: the MMA width follows the slot's pair count
+// (8 columns when its pairs fit, else 16 or 32, NTMAX n-tiles of 8 at most),
+// so a slot with few pairs does no work for empty columns.  Warp w of the CTA
+// takes the item's tiles t0 + w, t0 + w + 4, ... below t0 + per_item.
 template <int NTMAX, bool DOWN>
-__global__ void __launch_bounds__(kMoeWarps * 32) moe_expert_kernel(
-    const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
-    const MoeArgs a, int nsb, int rows_total) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  grid_dependency_wait();
-  grid_launch_dependents();
-  const int slot = blockIdx.y;
-  if (slot >= a.meta[0]) return;  // slot not in use
+__device__ __forceinline__ bool slot_item(const CUtensorMap *m0, const CUtensorMap *m1,
+                                          const MoeArgs &a, int nsb, int rows, uint8_t *ring,
+                                          uint64_t *bars, uint32_t &it, int slot, int t0,
+                                          int per_item) {
   const int np = a.slot_start[slot + 1] - a.slot_start[slot];
   const int ncols = DOWN ? 2 * np : np;
   const int nt = ncols <= 8 ? 1 : ncols <= 16 ? 2 : 4;  // n-tiles this slot needs
-  const int ctas = (int)gridDim.x * min(nt, NTMAX) / NTMAX;  // CTAs of this slot
-  if ((int)blockIdx.x >= ctas) return;
+  const int sid = t0 + (int)(threadIdx.x >> 5);
   if (nt == 1 || NTMAX == 1)
-    expert_body<1, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
-  else if (nt == 2 || NTMAX == 2)
-    expert_body<(NTMAX >= 2 ? 2 : 1), DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
-  else
-    expert_body<NTMAX, DOWN>(&map0, &map1, a, nsb, rows_total, smem, slot, ctas);
+    return expert_body<1, DOWN>(m0, m1, a, nsb, rows, ring, bars, it, slot, sid, kMoeWarps,
+                                t0 + per_item);
+  if (nt == 2 || NTMAX == 2)
+    return expert_body<(NTMAX >= 2 ? 2 : 1), DOWN>(m0, m1, a, nsb, rows, ring, bars, it, slot, sid,
+                                                   kMoeWarps, t0 + per_item);
+  return expert_body<NTMAX, DOWN>(m0, m1, a, nsb, rows, ring, bars, it, slot, sid, kMoeWarps,
+                                  t0 + per_item);
 }
 
-// ---------------------------------------------------------------- 4. combine
-__global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
+__device__ __forceinline__ int load_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *count reaches target (acquire: the writes made before
+// the matching releases are visible afterwards).  Returns false at once when
+// another CTA has raised the abort word; after the wall-clock limit it sets
+// the timeout bit of the device error word, raises the abort word and
+// returns false.
+__device__ __forceinline__ bool wait_count(const int *count, int target, int *abort_word,
+                                           unsigned *err) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (load_acquire(count) >= target) return true;
+    if (load_acquire(abort_word) != 0) return false;
+    if (global_ns() - t0 > kWaitLimitNs) break;
+    __nanosleep(256);
+  }
+  set_device_error(err, kDevErrTimeout);
+  atomicExch(abort_word, 1);
+  return false;
+}
+
+// ---------------------------------------------------------------- 2. experts
+template <int NTGU, int NTDN>
+__global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
+    const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mu,
+    const __grid_constant__ CUtensorMap md, const MoeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_item, s_last, s_fail;
+  // Each warp's ring and barriers, set up once: items only carry the ring
+  // iteration count on, so no barrier is ever initialised twice and no copy
+  // lands in memory that held a barrier.
+  const int lane = threadIdx.x & 31;
+  uint8_t *ring = smem + (threadIdx.x >> 5) * kWarpBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kStagesMoe * kStageStride);
+  if (lane == 0) {
+    prefetch_tmap(&mg);
+    prefetch_tmap(&mu);
+    prefetch_tmap(&md);
+    for (int s = 0; s < kStagesMoe; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) s_fail = 0;
+  __syncthreads();
+  uint32_t it = 0;  // this warp's ring iterations so far
   grid_dependency_wait();
   grid_launch_dependents();
-  const int t = blockIdx.y;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= a.hidden) return;
-  float acc = 0.f;
-  for (int j = 0; j < a.top_k; ++j) {
-    const int q = t * a.top_k + j;
-    const int pos = a.tj_pair[q];
-    if (pos >= 0) acc = fmaf(a.wts[q], a.p[(size_t)pos * a.hidden + i], acc);
+  const int S = a.meta[0];  // work slots in use
+  const int nsb_gu = a.hidden / kQK, nsb_dn = a.ffn / kQK;
+  const int gu_tiles = (a.ffn + kRows - 1) / kRows, dn_tiles = (a.hidden + kRows - 1) / kRows;
+  const int gu_groups = (gu_tiles + kGuTilesPerItem - 1) / kGuTilesPerItem;
+  const int dn_groups = (dn_tiles + kDnTilesPerItem - 1) / kDnTilesPerItem;
+  const int n_gu = S * gu_groups, n_items = n_gu + S * dn_groups;
+  int *next = a.counters, *slot_done = a.counters + 1, *grp_done = a.counters + 1 + a.max_slots;
+  int *abort_word = a.meta + kMetaAbort;
+  for (;;) {
+    // after a timed-out wait anywhere, no CTA takes another item
+    if (threadIdx.x == 0) s_item = load_acquire(abort_word) ? n_items : atomicAdd(next, 1);
+    __syncthreads();
+    const int item = s_item;
+    __syncthreads();  // every thread has read s_item before it is written again
+    if (item >= n_items) break;
+    if (item < n_gu) {
+      const int slot = item / gu_groups, grp = item - slot * gu_groups;
+      if (!slot_item<NTGU, false>(&mg, &mu, a, nsb_gu, a.ffn, ring, bars, it, slot,
+                                  grp * kGuTilesPerItem, kGuTilesPerItem))
+        s_fail = 1;
+      __threadfence();  // this thread's g, u, h writes are visible GPU-wide ...
+      __syncthreads();  // ... for every thread of the CTA, before the count goes up
+      if (s_fail) break;
+      if (threadIdx.x == 0) atomicAdd(&slot_done[slot], 1);
+    } else {
+      const int j = item - n_gu, slot = j / dn_groups, grp = j - slot * dn_groups;
+      if (threadIdx.x == 0 && !wait_count(&slot_done[slot], gu_groups, abort_word, a.err))
+        s_fail = 1;
+      __syncthreads();
+      if (s_fail) break;
+      if (!slot_item<NTDN, true>(&md, &md, a, nsb_dn, a.hidden, ring, bars, it, slot,
+                                 grp * kDnTilesPerItem, kDnTilesPerItem))
+        s_fail = 1;
+      __threadfence();  // this thread's down outputs are visible GPU-wide ...
+      __syncthreads();  // ... before the group's count goes up
+      if (s_fail) break;
+      if (threadIdx.x == 0) {
+        s_last = atomicAdd(&grp_done[grp], 1) == S - 1;
+        __threadfence();
+      }
+      __syncthreads();
+      if (s_last) {
+        // Every slot's down outputs of this group of hidden rows are in: the
+        // route-weighted sum over each token's slots, in slot order.
+        const int r0 = grp * kDnTilesPerItem * kRows;
+        const int r1 = min(a.hidden, r0 + kDnTilesPerItem * kRows);
+        for (int idx = threadIdx.x; idx < (r1 - r0) * a.n_tokens; idx += blockDim.x) {
+          const int t = idx / (r1 - r0), i = r0 + idx - t * (r1 - r0);
+          float acc = 0.f;
+          for (int k = 0; k < a.top_k; ++k) {
+            const int q = t * a.top_k + k;
+            const int pos = a.tj_pair[q];
+            if (pos >= 0) acc = fmaf(a.wts[q], __ldcg(&a.p[(size_t)pos * a.hidden + i]), acc);
+          }
+          a.y[(int64_t)t * a.ldy + i] = acc;
+        }
+      }
+    }
   }
-  a.y[(int64_t)t * a.ldy + i] = acc;
 }
 
 std::once_flag g_moe_attr[kMaxDevices];  // cudaFuncSetAttribute acts on the current device
 
 // Launch as a programmatic dependent of the previous kernel on the stream.
 template <typename K, typename... Args>
-void launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stream, Args... args) {
+cudaError_t launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stream,
+                       Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -499,48 +622,22 @@ void launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-#ifndef Q4K_MOE_GU_TILES  // gate/up: m-tiles per warp stream
-#define Q4K_MOE_GU_TILES 2
-#endif
-#ifndef Q4K_MOE_DN_TILES  // down: m-tiles per warp stream
-#define Q4K_MOE_DN_TILES 4
-#endif
-constexpr int kGuTiles = Q4K_MOE_GU_TILES;
-constexpr int kDnTiles = Q4K_MOE_DN_TILES;
-
-template <int NT, bool DOWN>
-constexpr int expert_smem() {
-  return kMoeWarps * ((kStagesMoe * (DOWN ? 1 : 2) * kTile + 64 + 127) / 128 * 128);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int NT, bool DOWN>
-void allow() {
-  cudaFuncSetAttribute(moe_expert_kernel<NT, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       expert_smem<NT, DOWN>());
-}
+constexpr int kExpertSmem = kMoeWarps * kWarpBytes;  // shared memory of the persistent kernel
 
-void moe_attributes() {
-  allow<1, false>();
-  allow<2, false>();
-  allow<1, true>();
-  allow<2, true>();
-  allow<4, true>();
-}
+int g_moe_occ[kMaxDevices][2];
 
-// tiles_per_warp: row tiles per warp stream of an 8-column slot; a slot with
-// nt n-tiles has nt times the streams.  The grid holds NT times the streams
-// of an 8-column slot, rounded to a multiple of NT CTAs.
-template <int NT, bool DOWN>
-void launch_expert(int rows, int tiles_per_warp, int max_slots, const CUtensorMap &m0,
-                   const CUtensorMap &m1, const MoeArgs &a, int nsb, cudaStream_t stream) {
-  const int ntiles = (rows + kRows - 1) / kRows;
-  const int per_cta = kMoeWarps * tiles_per_warp;
-  const int base = (ntiles + per_cta - 1) / per_cta;  // CTAs of an 8-column slot
-  dim3 grid((unsigned)(base * NT), (unsigned)max_slots);
-  launch_pdl(moe_expert_kernel<NT, DOWN>, grid, kMoeWarps * 32, (size_t)expert_smem<NT, DOWN>(),
-             stream, m0, m1, a, nsb, rows);
+void moe_attributes(int dev) {
+  cudaFuncSetAttribute(moe_persistent_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kExpertSmem);
+  cudaFuncSetAttribute(moe_persistent_kernel<2, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kExpertSmem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_moe_occ[dev][0], moe_persistent_kernel<1, 2>,
+                                                kMoeWarps * 32, kExpertSmem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_moe_occ[dev][1], moe_persistent_kernel<2, 4>,
+                                                kMoeWarps * 32, kExpertSmem);
 }
 
 CUresult expert_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int64_t stride,
@@ -576,7 +673,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
                        cudaStream_t stream) {
   if (n_experts > kMaxExperts) return cudaErrorInvalidValue;
-  std::call_once(g_moe_attr[device_facts()->device], moe_attributes);
+  std::call_once(g_moe_attr[device_facts()->device], moe_attributes, device_facts()->device);
   const int P = n_tokens * top_k;
   const MoeLayout L(n_experts, P, hidden, ffn);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -593,6 +690,9 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   a.hidden = (int)hidden;
   a.ffn = (int)ffn;
   a.meta = reinterpret_cast<int *>(ws + L.meta);
+  a.counters = reinterpret_cast<int *>(ws + L.counters);
+  a.n_counters = L.n_counters;
+  a.max_slots = MoeLayout::max_slots(n_experts, P);
   a.slot_expert = reinterpret_cast<int *>(ws + L.slot_expert);
   a.slot_start = reinterpret_cast<int *>(ws + L.slot_start);
   a.pair_token = reinterpret_cast<int *>(ws + L.pair_token);
@@ -611,29 +711,28 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
       expert_map(&md, w_down, hidden, ffn, expert_stride, n_experts) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  launch_pdl(moe_route_kernel, dim3(1), 1024, 0, stream, a);
-  const int max_slots = MoeLayout::max_slots(n_experts, P);
+  cudaError_t e = launch_pdl(moe_route_kernel, dim3(1), 1024, 0, stream, a);
+  if (e != cudaSuccess) return e;
+  // The widest slot decides the instantiation: 8-column slots fit the <1, 2>
+  // kernel (gate/up one column per pair, down two), wider ones the <2, 4>.
+  // With 8-pair slots (the default) every call takes the <1, 2> kernel: it
+  // holds 3 CTAs per SM against 2, which outweighs reading an expert with more
+  // than 8 tokens once per 8 of them.
   const int cap = std::min(P, kSlotPairs);  // pairs per slot at most
-  {  // gate/up: K = hidden, one column per pair
-    const int nsb = (int)(hidden / kQK);
-    if (cap <= 8)
-      launch_expert<1, false>((int)ffn, kGuTiles, max_slots, mg, mu, a, nsb, stream);
-    else
-      launch_expert<2, false>((int)ffn, kGuTiles, max_slots, mg, mu, a, nsb, stream);
-  }
-  {  // down: K = ffn, two columns per pair
-    const int nsb = (int)(ffn / kQK);
-    if (2 * cap <= 8)
-      launch_expert<1, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
-    else if (2 * cap <= 16)
-      launch_expert<2, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
-    else
-      launch_expert<4, true>((int)hidden, kDnTiles, max_slots, md, md, a, nsb, stream);
-  }
-  {
-    dim3 grid((unsigned)((hidden + 255) / 256), (unsigned)n_tokens);
-    launch_pdl(moe_combine_kernel, grid, 256, 0, stream, a);
-  }
+  const int wide = cap > 8 ? 1 : 0;
+  const DeviceFacts *f = device_facts();
+  const int occ = g_moe_occ[f->device][wide];
+  if (occ <= 0) return cudaErrorInvalidConfiguration;
+  // every CTA resident; no more CTAs than there can be items
+  const int S_max = MoeLayout::max_slots(n_experts, P);
+  const long items = (long)S_max * (((ffn + kRows - 1) / kRows + kGuTilesPerItem - 1) / kGuTilesPerItem +
+                                    MoeLayout::dn_groups(hidden));
+  const int grid = (int)std::min<long>((long)occ * f->sm_count, items);
+  e = wide ? launch_pdl(moe_persistent_kernel<2, 4>, dim3((unsigned)grid), kMoeWarps * 32,
+                        (size_t)kExpertSmem, stream, mg, mu, md, a)
+           : launch_pdl(moe_persistent_kernel<1, 2>, dim3((unsigned)grid), kMoeWarps * 32,
+                        (size_t)kExpertSmem, stream, mg, mu, md, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
