@@ -69,7 +69,7 @@ def _load():
         lib.oracle_gemv_f64.argtypes = [P, I64, I64, P, I64, I64, ctypes.c_int, P]
         lib.oracle_gemv_glu.argtypes = [P, P, I64, I64, P, I64, I64, P, P, P, P, P]
         lib.oracle_moe.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32,
-                                   P, P, P, P]
+                                   P, P, P, P, ctypes.c_int]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -211,12 +211,13 @@ def gemv_glu(w_gate, w_up, n: int, k: int, x_bf16):
 
 
 def moe(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,
-        x_bf16, ids, wts, return_stages: bool = False):
+        x_bf16, ids, wts, return_stages: bool = False, weighted_down: bool = False):
     """Routed-expert FFN for decode tokens (oracle_moe).
 
     x_bf16 uint16 [T, hidden]; ids int32 [T, top_k]; wts float32 [T, top_k].
     Returns y [T, hidden] fp64, plus (g, u, h), each [T*top_k, ffn], when
-    return_stages is set.
+    return_stages is set.  weighted_down: the route weight scales h before the
+    down projection and the slots' outputs are summed unweighted.
     """
     g8, u8, d8 = _u8(w_gate), _u8(w_up), _u8(w_down)
     x = np.ascontiguousarray(np.atleast_2d(np.asarray(x_bf16, dtype=np.uint16)))
@@ -234,7 +235,7 @@ def moe(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, f
         gp = up = hp = None
     _load().oracle_moe(_ptr(g8), _ptr(u8), _ptr(d8), int(expert_stride), int(n_experts),
                        int(hidden), int(ffn), _ptr(x), int(T), int(hidden), _ptr(ids_a),
-                       _ptr(wts_a), int(top_k), _ptr(y), gp, up, hp)
+                       _ptr(wts_a), int(top_k), _ptr(y), gp, up, hp, int(bool(weighted_down)))
     if return_stages:
         return y, (g, u, h)
     return y

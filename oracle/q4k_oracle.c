@@ -278,16 +278,21 @@ void oracle_gemv_glu(const uint8_t *wg, const uint8_t *wu, int64_t n, int64_t k,
  *     h = silu(g) * u,  silu(g) = g / (1 + exp(-g))
  *     p = Wd_e h                             (hidden values)
  *     y_t = sum_j wts[t*top_k + j] * p       (slots in order j = 0 .. top_k-1)
+ * With weighted_down set, the route weight moves ahead of the down projection
+ * ("Layer Package Repository Spec", section "Execution Policy",
+ * experimental.moe_weighted_down):
+ *     p = Wd_e (wts[t*top_k + j] * h),  y_t = sum_j p   (same slot order)
+ * which equals the plain form in exact arithmetic (Wd is linear).
  * Expert e's matrices start at byte e * expert_stride of each weight array;
  * gate/up are ffn x hidden, down is hidden x ffn.  A slot whose id is outside
  * [0, n_experts) contributes nothing.  x is [n_tokens x ldx] bf16, y is
  * [n_tokens x hidden] fp64.  g, u, h (each [n_tokens*top_k x ffn], slot-major
- * within a token) may be NULL.
+ * within a token; h before any route weight) may be NULL.
  */
 void oracle_moe(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int64_t expert_stride,
                 int32_t n_experts, int64_t hidden, int64_t ffn, const uint16_t *x, int32_t n_tokens,
                 int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, double *y,
-                double *g_out, double *u_out, double *h_out) {
+                double *g_out, double *u_out, double *h_out, int weighted_down) {
     double *g = (double *)malloc(sizeof(double) * (size_t)ffn);
     double *u = (double *)malloc(sizeof(double) * (size_t)ffn);
     double *h = (double *)malloc(sizeof(double) * (size_t)ffn);
@@ -316,9 +321,15 @@ void oracle_moe(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int64_t
                 if (u_out) u_out[slot * ffn + f] = u[f];
                 if (h_out) h_out[slot * ffn + f] = h[f];
             }
-            oracle_gemv_f64(de, hidden, ffn, h, 1, ffn, 0, p);
             double r = (double)wts[slot];
-            for (int64_t i = 0; i < hidden; ++i) y[t * hidden + i] += r * p[i];
+            if (weighted_down) {
+                for (int64_t f = 0; f < ffn; ++f) h[f] *= r;
+                oracle_gemv_f64(de, hidden, ffn, h, 1, ffn, 0, p);
+                for (int64_t i = 0; i < hidden; ++i) y[t * hidden + i] += p[i];
+            } else {
+                oracle_gemv_f64(de, hidden, ffn, h, 1, ffn, 0, p);
+                for (int64_t i = 0; i < hidden; ++i) y[t * hidden + i] += r * p[i];
+            }
         }
     }
     free(g);

@@ -329,7 +329,8 @@ def _run_moe(c, **kw):
     args = dict(c)
     args.update(kw)
     return oracle.moe(args["wg"], args["wu"], args["wd"], args["stride"], args["E"], args["H"],
-                      args["F"], _x_bits(args["x"]), args["ids"], args["wts"], return_stages=True)
+                      args["F"], _x_bits(args["x"]), args["ids"], args["wts"], return_stages=True,
+                      weighted_down=args.get("weighted_down", False))
 
 
 def test_moe_matches_library_composition():
@@ -400,6 +401,47 @@ def test_moe_zero_gate_gives_zero_and_bad_ids_contribute_nothing():
     keep[1, 1] = 0
     y_ref, _ = _run_moe(c, wts=(c["wts"] * keep).astype(np.float32))
     assert np.allclose(y_bad, y_ref, rtol=0, atol=1e-12)
+
+
+def test_moe_weighted_down_with_unit_weights_is_the_plain_form_bit_for_bit():
+    # r = 1: r h = h and 1 * p = p exactly, so both orders give the same bits
+    c = _moe_case(seed=60)
+    ones = np.ones_like(c["wts"])
+    y0, st0 = _run_moe(c, wts=ones)
+    y1, st1 = _run_moe(c, wts=ones, weighted_down=True)
+    assert np.array_equal(y0, y1)
+    for a, b in zip(st0, st1):
+        assert np.array_equal(a, b)
+
+
+def test_moe_weighted_down_matches_library_composition_and_the_plain_form():
+    # Wd (r h) summed over slots, composed here from the dequantized matrices;
+    # the same as sum r (Wd h) up to fp64 rounding (Wd is linear); the staged
+    # h is the unweighted silu(g) u
+    from scipy.special import expit
+    c = _moe_case(seed=61, T=4, K=3, E=5)
+    y, (g, u, h) = _run_moe(c, weighted_down=True)
+    y_plain, (_, _, h_plain) = _run_moe(c)
+    E, H, F = c["E"], c["H"], c["F"]
+    Wg = oracle.dequant_f64(c["wg"], E * F, H).reshape(E, F, H)
+    Wu = oracle.dequant_f64(c["wu"], E * F, H).reshape(E, F, H)
+    Wd = oracle.dequant_f64(c["wd"], E * H, F).reshape(E, H, F)
+    xf = _x_f64(c["x"])
+    T, K = c["ids"].shape
+    yref = np.zeros((T, H))
+    scale = np.zeros((T, H))
+    for t in range(T):
+        for j in range(K):
+            e = c["ids"][t, j]
+            r = float(c["wts"][t, j])
+            gg, uu = Wg[e] @ xf[t], Wu[e] @ xf[t]
+            hh = gg * expit(gg) * uu
+            yref[t] += Wd[e] @ (r * hh)
+            scale[t] += abs(r) * (np.abs(Wd[e]) @ np.abs(hh))
+    assert np.array_equal(h, h_plain)
+    assert np.all(np.abs(y - yref) <= 1e-12 * scale + 1e-300)
+    assert np.all(np.abs(y - y_plain) <= 1e-12 * scale + 1e-300)
+    assert not np.array_equal(y, y_plain) or np.all(c["wts"] == 1)   # a distinct path
 
 
 # ---------------------------------------------------------------- generator sanity
