@@ -24,10 +24,11 @@ STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN"
           4: "Q4K_ERR_WORKSPACE", 5: "Q4K_ERR_DEVICE", 6: "Q4K_ERR_CUDA", 7: "Q4K_ERR_DATA",
           8: "Q4K_ERR_MEMORY"}
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
+Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm",
            "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
-           "q4k_moe_gemv_noalloc",
+           "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
 _lock = threading.Lock()
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.q4k_moe_gemv.restype = ctypes.c_int
         L.q4k_moe_gemv.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
                                    P, SZ, P]
+        L.q4k_moe_gemv_ex.restype = ctypes.c_int
+        L.q4k_moe_gemv_ex.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
+                                      ctypes.c_uint32, P, SZ, P]
         L.q4k_moe_gemv_noalloc.restype = ctypes.c_int
         L.q4k_moe_gemv_noalloc.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P,
                                            I64, P]
@@ -223,6 +227,23 @@ def q4k_moe_gemv(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidde
                               hidden, ffn, _ptr(x), T, x.stride(0), _ptr(ids), _ptr(wts), top_k,
                               _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
                               _stream(stream)), "q4k_moe_gemv")
+    return out
+
+
+def q4k_moe_gemv_ex(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int,
+                    ffn: int, x: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor, flags: int = 0,
+                    out=None, workspace=None, stream=None):
+    """q4k_moe_gemv with flags (Q4K_MOE_WEIGHTED_DOWN); returns fp32 [T, hidden]."""
+    T, top_k = ids.shape
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x.device)
+    ws_bytes = q4k_moe_workspace_size(n_experts, T, top_k, hidden, ffn)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().q4k_moe_gemv_ex(_ptr(w_gate), _ptr(w_up), _ptr(w_down), expert_stride, n_experts,
+                                 hidden, ffn, _ptr(x), T, x.stride(0), _ptr(ids), _ptr(wts), top_k,
+                                 _ptr(out), out.stride(0), flags, _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "q4k_moe_gemv_ex")
     return out
 
 

@@ -315,6 +315,16 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
                  int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
                  int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,
                  int64_t ldy, void *workspace, size_t workspace_bytes, void *stream) {
+  return q4k_moe_gemv_ex(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x, n_tokens,
+                         ldx, ids, wts, top_k, y, ldy, 0u, workspace, workspace_bytes, stream);
+}
+
+int q4k_moe_gemv_ex(const void *w_gate, const void *w_up, const void *w_down,
+                    int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                    const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                    const float *wts, int32_t top_k, float *y, int64_t ldy, uint32_t flags,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (flags & ~(uint32_t)Q4K_MOE_WEIGHTED_DOWN) return Q4K_ERR_SHAPE;
   if (n_experts <= 0 || n_experts > 2048 || hidden <= 0 || ffn <= 0 || (hidden % kQK) ||
       (ffn % kQK) || n_tokens < 0 || n_tokens > 64 || top_k < 1 || top_k > 16)
     return Q4K_ERR_SHAPE;
@@ -336,6 +346,7 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
   if (st != Q4K_OK) return st;
   return map_launch(launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x,
                                n_tokens, ldx, ids, wts, top_k, y, ldy, workspace,
+                               (flags & Q4K_MOE_WEIGHTED_DOWN) != 0,
                                static_cast<cudaStream_t>(stream)));
 }
 

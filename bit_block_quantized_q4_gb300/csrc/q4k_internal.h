@@ -67,7 +67,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
                        const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
                        const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
-                       cudaStream_t stream);
+                       bool weighted_down, cudaStream_t stream);
 
 // Workspace of the allocation-free MoE call (bytes of its device array).
 constexpr size_t kMoeScratchBytes = 8u << 20;

@@ -17,7 +17,10 @@
 //               the tensor cores (MMA columns = tokens); it writes g, u and
 //               h = silu(g) * u in fp32, and h as two bf16 columns per pair,
 //               h_hi = bf16(h) and h_lo = bf16(h - h_hi) (16 significant bits
-//               together), in MMA fragment order.  A down item waits (bounded)
+//               together), in MMA fragment order.  With the weighted-down
+//               order (Q4K_MOE_WEIGHTED_DOWN) the bf16 columns carry r * h,
+//               r the pair's route weight, and the final sum below takes the
+//               down outputs unweighted.  A down item waits (bounded)
 //               until every gate/up item of its slot is done, streams the
 //               expert's down rows and writes p = Wd h per pair.  The CTA that
 //               completes the last down item of a 128-row group of hidden adds
@@ -59,7 +62,8 @@ constexpr int kGuTilesPerItem = 4;  // 16-row tiles of ffn per gate/up item (one
 constexpr int kDnTilesPerItem = 8;  // 16-row tiles of hidden per down item (two per warp)
 
 struct MoeLayout {
-  size_t meta, counters, slot_expert, slot_start, pair_token, tj_pair, g, u, h, h_hi, h_lo, p, total;
+  size_t meta, counters, slot_expert, slot_start, pair_token, pair_q, tj_pair, g, u, h, h_hi, h_lo, p,
+      total;
   int n_counters;
   static int max_slots(int E, int P) { return std::min(E, P) + (P + kSlotPairs - 1) / kSlotPairs; }
   static int dn_groups(int64_t H) { return (int)((H + 16 * kDnTilesPerItem - 1) / (16 * kDnTilesPerItem)); }
@@ -75,6 +79,7 @@ struct MoeLayout {
     slot_expert = o; o = al(o + S * sizeof(int));
     slot_start = o;  o = al(o + (S + 1) * sizeof(int));
     pair_token = o;  o = al(o + (size_t)P * sizeof(int));
+    pair_q = o;      o = al(o + (size_t)P * sizeof(int));
     tj_pair = o;     o = al(o + (size_t)P * sizeof(int));
     g = o;           o = al(o + (size_t)P * F * sizeof(float));
     u = o;           o = al(o + (size_t)P * F * sizeof(float));
@@ -95,7 +100,8 @@ struct MoeArgs {
   int64_t ldy;
   int n_experts, n_tokens, top_k;
   int hidden, ffn;
-  int *meta, *slot_expert, *slot_start, *pair_token, *tj_pair;
+  int *meta, *slot_expert, *slot_start, *pair_token, *pair_q, *tj_pair;
+  int weighted_down;  // route weight applied to h before the down projection
   int *counters;
   int n_counters, max_slots;
   float *g, *u, *h, *p;
@@ -198,6 +204,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
       const int pos = start[e] + atomicAdd(&fill[e], 1);
       a.tj_pair[q] = pos;
       a.pair_token[pos] = q / a.top_k;
+      a.pair_q[pos] = q;
     }
   }
 }
@@ -453,8 +460,10 @@ __device__ __forceinline__ bool expert_body(const CUtensorMap *map0p, const CUte
             if (pr >= np) continue;
             const float gg = yacc[0][nt][2 * r + e], uu = yacc[NM - 1][nt][2 * r + e];
             const float hv = ok ? gg / (1.f + __expf(-gg)) * uu : nan;
-            const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
-            const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
+            // the down projection's input: h, or r h in the weighted-down order
+            const float hd = a.weighted_down ? hv * a.wts[a.pair_q[pstart + pr]] : hv;
+            const __nv_bfloat16 hh = __float2bfloat16_rn(hd);
+            const __nv_bfloat16 hl = __float2bfloat16_rn(hd - __bfloat162float(hh));
             // h_hi / h_lo in B-fragment order: positions 1 and 2 of each group
             // of four swapped, so that 32-bit words hold (h[o], h[o+2]) and
             // (h[o+1], h[o+3]).
@@ -597,7 +606,9 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
           for (int k = 0; k < a.top_k; ++k) {
             const int q = t * a.top_k + k;
             const int pos = a.tj_pair[q];
-            if (pos >= 0) acc = fmaf(a.wts[q], __ldcg(&a.p[(size_t)pos * a.hidden + i]), acc);
+            if (pos < 0) continue;
+            const float pv = __ldcg(&a.p[(size_t)pos * a.hidden + i]);
+            acc = a.weighted_down ? acc + pv : fmaf(a.wts[q], pv, acc);
           }
           a.y[(int64_t)t * a.ldy + i] = acc;
         }
@@ -671,7 +682,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
                        const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
                        const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
-                       cudaStream_t stream) {
+                       bool weighted_down, cudaStream_t stream) {
   if (n_experts > kMaxExperts) return cudaErrorInvalidValue;
   std::call_once(g_moe_attr[device_facts()->device], moe_attributes, device_facts()->device);
   const int P = n_tokens * top_k;
@@ -696,6 +707,8 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   a.slot_expert = reinterpret_cast<int *>(ws + L.slot_expert);
   a.slot_start = reinterpret_cast<int *>(ws + L.slot_start);
   a.pair_token = reinterpret_cast<int *>(ws + L.pair_token);
+  a.pair_q = reinterpret_cast<int *>(ws + L.pair_q);
+  a.weighted_down = weighted_down ? 1 : 0;
   a.tj_pair = reinterpret_cast<int *>(ws + L.tj_pair);
   a.g = reinterpret_cast<float *>(ws + L.g);
   a.u = reinterpret_cast<float *>(ws + L.u);
@@ -788,7 +801,7 @@ cudaError_t launch_moe_scratch(const void *w_gate, const void *w_up, const void 
   e = scratch_address(dev, &scratch);
   if (e != cudaSuccess) return e;
   return launch_moe(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn, x, n_tokens, ldx,
-                    ids, wts, top_k, y, ldy, scratch, stream);
+                    ids, wts, top_k, y, ldy, scratch, false, stream);
 }
 
 }  // namespace q4k

@@ -234,7 +234,8 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k
  *   offsets[1]  fp32 [pairs][ffn]: g = Wg_e x_t of each pair
  *   offsets[2]  fp32 [pairs][ffn]: u = Wu_e x_t
  *   offsets[3]  fp32 [pairs][ffn]: h = silu(g) * u
- *   offsets[4]  fp32 [pairs][hidden]: Wd_e h (before the route weight)
+ *   offsets[4]  fp32 [pairs][hidden]: Wd_e h (before the route weight;
+ *               Wd_e (wts * h) in the weighted-down order)
  * Errors: NULL, SHAPE.
  */
 int q4k_moe_workspace_views(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
@@ -270,6 +271,25 @@ int q4k_moe_gemv(const void *w_gate, const void *w_up, const void *w_down, int64
                  int32_t n_experts, int64_t hidden, int64_t ffn, const void *x, int32_t n_tokens,
                  int64_t ldx, const int32_t *ids, const float *wts, int32_t top_k, float *y,
                  int64_t ldy, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q4k_moe_gemv_ex -- q4k_moe_gemv with flags (flags 0: q4k_moe_gemv).
+ *   Q4K_MOE_WEIGHTED_DOWN: the weighted-down order ("Layer Package Repository
+ *     Spec", section "Execution Policy", experimental.moe_weighted_down): the
+ *     route weight scales h before the routed down projection and the slots'
+ *     down outputs are summed unweighted,
+ *         Y[t, :] = sum_j Wd_e (wts[t*top_k + j] * h)     (slots in order j).
+ *     Equal to q4k_moe_gemv's result in exact arithmetic; within the same
+ *     bound.  The workspace's h view keeps silu(g) * u; its down-output view
+ *     holds Wd_e (wts * h).
+ * Other flag bits: Q4K_ERR_SHAPE.  Everything else as q4k_moe_gemv.
+ */
+#define Q4K_MOE_WEIGHTED_DOWN 1u
+int q4k_moe_gemv_ex(const void *w_gate, const void *w_up, const void *w_down,
+                    int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                    const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                    const float *wts, int32_t top_k, float *y, int64_t ldy, uint32_t flags,
+                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * q4k_moe_gemv_noalloc -- q4k_moe_gemv without a caller-provided workspace.

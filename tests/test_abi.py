@@ -171,6 +171,29 @@ def test_moe_argument_errors(L):
     assert call(x=P + 2) == 3
 
 
+def test_moe_ex_flags(L):
+    # flags sit between ldy and the workspace; bits other than
+    # Q4K_MOE_WEIGHTED_DOWN are a SHAPE error before anything else is looked at
+    E, H, F = 8, 256, 512
+    stride = F * H // 256 * 144
+    ws = L.q4k_moe_workspace_size(E, 4, 2, H, F)
+
+    def call(flags, **kw):
+        a = dict(wg=P, wu=P, wd=P, stride=stride, E=E, H=H, F=F, x=P, T=4, ldx=H, ids=P, wts=P,
+                 k=2, y=P, ldy=H, flags=flags, ws=P, wsb=ws, stream=None)
+        a.update(kw)
+        return L.q4k_moe_gemv_ex(*a.values())
+
+    assert call(2) == 2
+    assert call(0x80000000) == 2
+    assert call(2, ids=None) == 2
+    assert call(1, ids=None) == 1
+    assert call(0, ids=None) == 1
+    assert call(1, T=0) == 0
+    assert call(1, ws=None) == 4
+    assert call(1, H=300) == 2
+
+
 def test_get_device_error_rejects_null(L):
     assert L.q4k_get_device_error(None, None) == 1
 
@@ -209,6 +232,8 @@ int main(void) {
   st |= q4k_gemm(0, 4, 256, 0, 1, 256, 0, 8, 0);
   st |= (int)q4k_moe_workspace_size(8, 1, 2, 256, 256);
   st |= q4k_moe_gemv(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0, 0, 0);
+  st |= q4k_moe_gemv_ex(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256,
+                        Q4K_MOE_WEIGHTED_DOWN, 0, 0, 0);
   st |= q4k_moe_gemv_noalloc(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0);
   st |= q4k_get_device_error(0, &bits);
   st |= q4k_selftest_wait_timeout(0);

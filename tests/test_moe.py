@@ -39,25 +39,28 @@ def _make(E, H, F, T, K, seed, quants="uniform", sigma=1.0):
     return dict(wg=wg, wu=wu, wd=wd, stride=stride, E=E, H=H, F=F, x=x, ids=ids, wts=wts)
 
 
-def _gpu(q4k, c, ids=None, wts=None):
+def _gpu(q4k, c, ids=None, wts=None, flags=0):
     ids = c["ids"] if ids is None else ids
     wts = c["wts"] if wts is None else wts
-    y = q4k.q4k_moe_gemv(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"], c["E"],
-                         c["H"], c["F"], c["x"].to(DEV), ids.to(DEV), wts.to(DEV))
+    y = q4k.q4k_moe_gemv_ex(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"],
+                            c["E"], c["H"], c["F"], c["x"].to(DEV), ids.to(DEV), wts.to(DEV),
+                            flags=flags)
     torch.cuda.synchronize()
     err = q4k.q4k_get_device_error()
     return y.cpu().numpy().astype(np.float64), err
 
 
-def _bound(c, ids, wts, tokens):
-    """Reference y and the propagated error bound for the listed tokens."""
+def _bound(c, ids, wts, tokens, weighted_down=False):
+    """Reference y and the propagated error bound for the listed tokens (the
+    same bound for both orders: |r| |Wd| |h| = |Wd| |r h|)."""
     E, H, F, s = c["E"], c["H"], c["F"], c["stride"]
     wg, wu, wd = (c[k].numpy() for k in ("wg", "wu", "wd"))
     xb = xbits(c["x"])
     xf = c["x"].to(torch.float64).numpy()
     ids_n = ids.numpy()
     wts_n = wts.numpy().astype(np.float64)
-    yref = oracle.moe(wg, wu, wd, s, E, H, F, xb[tokens], ids_n[tokens], wts_n[tokens].astype(np.float32))
+    yref = oracle.moe(wg, wu, wd, s, E, H, F, xb[tokens], ids_n[tokens],
+                      wts_n[tokens].astype(np.float32), weighted_down=weighted_down)
     bound = np.zeros((len(tokens), H))
     for ti, t in enumerate(tokens):
         for j in range(ids_n.shape[1]):
@@ -86,13 +89,14 @@ def _check(y, yref, bound, what):
 
 @pytest.mark.parametrize("E,H,F,T,K", [(8, 256, 256, 1, 1), (8, 512, 512, 3, 2), (16, 1024, 512, 16, 8),
                                        (32, 512, 768, 9, 4)])
-def test_moe_matches_oracle(q4k, E, H, F, T, K):
+@pytest.mark.parametrize("weighted_down", [False, True])
+def test_moe_matches_oracle(q4k, E, H, F, T, K, weighted_down):
     c = _make(E, H, F, T, K, seed=E + H + F + T + K)
-    y, err = _gpu(q4k, c)
+    y, err = _gpu(q4k, c, flags=int(weighted_down))
     assert err == 0
     tokens = list(range(T))
-    yref, bound = _bound(c, c["ids"], c["wts"], tokens)
-    _check(y[tokens], yref, bound, f"moe E{E} H{H} F{F} T{T} k{K}")
+    yref, bound = _bound(c, c["ids"], c["wts"], tokens, weighted_down)
+    _check(y[tokens], yref, bound, f"moe E{E} H{H} F{F} T{T} k{K} wd{int(weighted_down)}")
 
 
 def test_moe_one_expert_for_all_tokens_spans_slots(q4k):
@@ -136,7 +140,8 @@ def test_moe_relabel_invariance_and_determinism(q4k):
     assert np.array_equal(y1, y2)      # same pairs, same per-column arithmetic
 
 
-def test_moe_235b_class_sampled_tokens(q4k):
+@pytest.mark.parametrize("weighted_down", [False, True])
+def test_moe_235b_class_sampled_tokens(q4k, weighted_down):
     # 128 experts, hidden 4096, expert ffn 1536, 16 decode tokens, top-8 Zipf(1.1)
     E, H, F, T, K = 128, 4096, 1536, 16, 8
     stride = F * (H // 256) * 144
@@ -145,25 +150,27 @@ def test_moe_235b_class_sampled_tokens(q4k):
     wd = synth.q4k_weight(E * H, F, seed=43, device=DEV).reshape(-1)
     x = synth.bf16_normal((T, H), seed=44)
     ids, wts = synth.zipf_routing(T, E, K, seed=45)
-    y = q4k.q4k_moe_gemv(wg, wu, wd, stride, E, H, F, x.to(DEV), ids.to(DEV), wts.to(DEV))
+    y = q4k.q4k_moe_gemv_ex(wg, wu, wd, stride, E, H, F, x.to(DEV), ids.to(DEV), wts.to(DEV),
+                            flags=int(weighted_down))
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     tokens = [0, 7, 15]
     used = sorted({int(e) for t in tokens for e in ids[t].tolist()})
     # oracle on the experts these tokens use (copied to the host)
     c = dict(wg=wg.cpu(), wu=wu.cpu(), wd=wd.cpu(), stride=stride, E=E, H=H, F=F, x=x)
-    yref, bound = _bound(c, ids, wts, tokens)
+    yref, bound = _bound(c, ids, wts, tokens, weighted_down)
     _check(y.cpu().numpy().astype(np.float64)[tokens], yref, bound, "235B-class")
     assert len(used) > 1
 
 
-def _gpu_stages(q4k, c, ids, wts):
+def _gpu_stages(q4k, c, ids, wts, flags=0):
     """Run with an explicit workspace and read back the per-pair stages."""
     E, H, F = c["E"], c["H"], c["F"]
     T, K = ids.shape
     ws = torch.zeros(q4k.q4k_moe_workspace_size(E, T, K, H, F), dtype=torch.uint8, device=DEV)
-    y = q4k.q4k_moe_gemv(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"], E, H, F,
-                         c["x"].to(DEV), ids.to(DEV), wts.to(DEV), workspace=ws)
+    y = q4k.q4k_moe_gemv_ex(c["wg"].to(DEV), c["wu"].to(DEV), c["wd"].to(DEV), c["stride"], E, H,
+                            F, c["x"].to(DEV), ids.to(DEV), wts.to(DEV), flags=flags,
+                            workspace=ws)
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     v = q4k.q4k_moe_workspace_views(E, T, K, H, F)
@@ -175,16 +182,18 @@ def _gpu_stages(q4k, c, ids, wts):
     return y.cpu().numpy().astype(np.float64), tj, st
 
 
+@pytest.mark.parametrize("weighted_down", [False, True])
 @pytest.mark.parametrize("sigma", [1.0, 0.01])
 @pytest.mark.parametrize("E,H,F,T,K", [(16, 1024, 512, 16, 8), (8, 512, 768, 5, 3)])
-def test_moe_stagewise(q4k, E, H, F, T, K, sigma):
+def test_moe_stagewise(q4k, E, H, F, T, K, sigma, weighted_down):
     # every stage against the oracle on its own: g and u within the GEMV bound,
     # h = silu(g) u of the GPU's own g and u, the down projection fed the GPU's
-    # own h, and y = the route-weighted sum of the GPU's own down outputs.
+    # own h (times the route weight r in the weighted-down order), and y = the
+    # sum of the GPU's own down outputs (weighted by r in the plain order).
     # sigma 0.01 keeps |g| small: SiLU's curved region.
     c = _make(E, H, F, T, K, seed=E + H + T + int(1000 * sigma), sigma=sigma)
     ids, wts = c["ids"], c["wts"]
-    y, tj, st = _gpu_stages(q4k, c, ids, wts)
+    y, tj, st = _gpu_stages(q4k, c, ids, wts, flags=int(weighted_down))
     s = c["stride"]
     wg, wu, wd = (c[k].numpy() for k in ("wg", "wu", "wd"))
     xb = xbits(c["x"])
@@ -206,14 +215,16 @@ def test_moe_stagewise(q4k, E, H, F, T, K, sigma):
             assert np.all(np.abs(u - u_ref[q]) <= 2e-3 * su), f"u t{t} j{j}"
             hh = g / (1.0 + np.exp(-np.clip(g, -700, 700))) * u
             assert np.all(np.abs(h - hh) <= 2.0 ** -18 * np.abs(hh) + 1e-30), f"h t{t} j{j}"
-            pd = oracle.gemv_f64(de, H, F, h)[0]
-            sd = oracle.gemv_f64(de, H, F, np.abs(h), use_abs=True)[0]
+            r = float(wts[t, j])
+            hd = r * h if weighted_down else h     # r h is rounded once to fp32: 2^-24
+            pd = oracle.gemv_f64(de, H, F, hd)[0]
+            sd = oracle.gemv_f64(de, H, F, np.abs(hd), use_abs=True)[0]
             p = st["p"][pos].astype(np.float64)
-            assert np.all(np.abs(p - pd) <= (2e-3 + 2.0 ** -16) * sd), f"down t{t} j{j}"
-            yt += float(wts[t, j]) * p
+            assert np.all(np.abs(p - pd) <= (2e-3 + 2.0 ** -16 + 2.0 ** -24) * sd), f"down t{t} j{j}"
+            yt += p if weighted_down else r * p
             gmax = max(gmax, float(np.abs(g).max()))
-        bound = 2.0 ** -20 * sum(abs(float(wts[t, j])) * np.abs(st["p"][int(tj[t * K + j])])
-                                 for j in range(K))
+        bound = 2.0 ** -20 * sum((1.0 if weighted_down else abs(float(wts[t, j])))
+                                 * np.abs(st["p"][int(tj[t * K + j])]) for j in range(K))
         assert np.all(np.abs(y[t] - yt) <= bound + 1e-30), f"combine t{t}"
     if sigma < 0.1:
         assert gmax < 8.0          # the curved region of SiLU is what was tested
