@@ -70,6 +70,7 @@ def _load():
         lib.oracle_gemv_glu.argtypes = [P, P, I64, I64, P, I64, I64, P, P, P, P, P]
         lib.oracle_moe.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32,
                                    P, P, P, P, ctypes.c_int]
+        lib.oracle_rmsnorm_gemv.argtypes = [P, I64, I64, P, I64, I64, P, ctypes.c_float, P, P, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -208,6 +209,24 @@ def gemv_glu(w_gate, w_up, n: int, k: int, x_bf16):
     if n:
         _load().oracle_gemv_glu(_ptr(a), _ptr(b), n, k, _ptr(x), batch, k, *(_ptr(o) for o in outs))
     return tuple(outs)
+
+
+def rmsnorm_gemv(w, n: int, k: int, x_bf16, gamma, eps: float):
+    """Projection of RMS-normalised activations (oracle_rmsnorm_gemv): returns
+    (y, s, rinv) with y = W xh, s = |W| |xh| ([batch, n] fp64) and rinv
+    ([batch] fp64), xh = x * rinv * gamma, rinv = 1 / sqrt(mean(x^2) + eps)."""
+    a = _check_w(w, n, k)
+    x = np.ascontiguousarray(np.atleast_2d(np.asarray(x_bf16, dtype=np.uint16)))
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float32))
+    assert x.shape[1] == k and g.shape == (k,)
+    batch = x.shape[0]
+    y = np.empty((batch, n), np.float64)
+    s = np.empty((batch, n), np.float64)
+    rinv = np.empty(batch, np.float64)
+    if batch and n:
+        _load().oracle_rmsnorm_gemv(_ptr(a), n, k, _ptr(x), batch, k, _ptr(g), float(eps), _ptr(y),
+                                    _ptr(s), _ptr(rinv))
+    return y, s, rinv
 
 
 def moe(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,

@@ -338,6 +338,40 @@ void oracle_moe(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int64_t
     free(p);
 }
 
+/*
+ * Quantized projection of RMS-normalised activations ("spec: specialized model
+ * runtimes", section "Feasibility gate": one quantized GEMM plus fused
+ * RMSNorm; the norm is the prologue of the projection).  For each token b:
+ *     rinv_b  = 1 / sqrt( (1/k) sum_i x[b,i]^2 + eps )
+ *     xh[b,i] = x[b,i] * rinv_b * gamma[i]
+ *     y[b,r]  = sum_i w[r,i] xh[b,i],   s[b,r] = sum_i |w[r,i]| |xh[b,i]|
+ * in fp64 throughout (x bf16, gamma and eps fp32 as given).  y and s are
+ * [batch x n]; rinv_out ([batch]) may be NULL.
+ */
+void oracle_rmsnorm_gemv(const uint8_t *w, int64_t n, int64_t k, const uint16_t *x, int64_t batch,
+                         int64_t ldx, const float *gamma, float eps, double *y, double *s,
+                         double *rinv_out) {
+    double *xh = (double *)malloc(sizeof(double) * (size_t)(batch * k));
+    double *axh = (double *)malloc(sizeof(double) * (size_t)(batch * k));
+    for (int64_t b = 0; b < batch; ++b) {
+        double ss = 0.0;
+        for (int64_t i = 0; i < k; ++i) {
+            double v = oracle_bf16_to_f64(x[b * ldx + i]);
+            ss += v * v;
+        }
+        double rinv = 1.0 / sqrt(ss / (double)k + (double)eps);
+        if (rinv_out) rinv_out[b] = rinv;
+        for (int64_t i = 0; i < k; ++i) {
+            xh[b * k + i] = oracle_bf16_to_f64(x[b * ldx + i]) * rinv * (double)gamma[i];
+            axh[b * k + i] = fabs(xh[b * k + i]);
+        }
+    }
+    oracle_gemv_f64(w, n, k, xh, batch, k, 0, y);
+    oracle_gemv_f64(w, n, k, axh, batch, k, 1, s);
+    free(xh);
+    free(axh);
+}
+
 /* Threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

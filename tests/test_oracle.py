@@ -312,6 +312,67 @@ def test_glu_zero_gate_gives_exact_zero_and_large_gate_gives_up():
     assert g[0, 1] == 945.0 and h[0, 1] == 945.0 * u[0, 1]
 
 
+# ---------------------------------------------------------------- RMSNorm prologue
+
+def _signs(shape, seed):
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(np.where(rng.random(shape) < 0.5, -1.0, 1.0).astype(np.float32)).to(
+        torch.bfloat16)
+
+
+def test_rmsnorm_with_unit_rms_and_unit_gamma_is_the_plain_projection():
+    # x = +-1 everywhere, eps = 0: mean x^2 = 1, rinv = 1, xh = x exactly
+    n, k = 24, 512
+    w = synth.q4k_weight(n, k, seed=70).numpy()
+    x = _signs((3, k), 71)
+    y, s, rinv = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), np.ones(k, np.float32), 0.0)
+    y0, s0 = oracle.gemv(w, n, k, _x_bits(x))
+    assert np.all(rinv == 1.0)
+    assert np.array_equal(y, y0) and np.array_equal(s, s0)
+
+
+def test_rmsnorm_is_invariant_to_scaling_x_by_a_power_of_two():
+    n, k = 20, 768
+    w = synth.q4k_weight(n, k, seed=72).numpy()
+    x = synth.bf16_normal((2, k), seed=73)
+    gamma = np.random.default_rng(74).uniform(0.5, 1.5, k).astype(np.float32)
+    y1, s1, r1 = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), gamma, 0.0)
+    y4, s4, r4 = oracle.rmsnorm_gemv(w, n, k, _x_bits(x * 4), gamma, 0.0)
+    assert np.array_equal(r4 * 4, r1)
+    assert np.array_equal(y1, y4) and np.array_equal(s1, s4)
+
+
+def test_rmsnorm_single_nonzero_activation_closed_form():
+    # x = a e_j, eps = 0: rinv = sqrt(k) / |a|, so y = sign(a) sqrt(k) gamma_j W[:, j]
+    n, k, j = 16, 512, 137
+    w = synth.q4k_weight(n, k, seed=75).numpy()
+    gamma = np.random.default_rng(76).uniform(-2, 2, k).astype(np.float32)
+    x = torch.zeros((2, k), dtype=torch.bfloat16)
+    x[0, j] = -3.0
+    x[1, j] = 0.015625
+    y, s, rinv = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), gamma, 0.0)
+    col = oracle.dequant_f64(w, n, k)[:, j]
+    assert np.allclose(rinv, [np.sqrt(k) / 3.0, np.sqrt(k) / 0.015625], rtol=1e-15)
+    want = np.sqrt(k) * float(gamma[j]) * col
+    assert np.allclose(y[0], -want, rtol=1e-14, atol=0) and np.allclose(y[1], want, rtol=1e-14, atol=0)
+    assert np.allclose(s[0], np.abs(want), rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_eps_closed_form_and_linearity_in_gamma():
+    n, k = 12, 256
+    w = synth.q4k_weight(n, k, seed=77).numpy()
+    x = torch.full((1, k), 0.5, dtype=torch.bfloat16)            # mean x^2 = 0.25
+    g1 = np.random.default_rng(78).uniform(-1, 1, k).astype(np.float32)
+    g2 = np.random.default_rng(79).uniform(-1, 1, k).astype(np.float32)
+    eps = 1e-2
+    y1, s1, r = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), g1, eps)
+    assert np.isclose(r[0], 1.0 / np.sqrt(0.25 + float(np.float32(eps))), rtol=1e-15)
+    y2, s2, _ = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), g2, eps)
+    y12, _, _ = oracle.rmsnorm_gemv(w, n, k, _x_bits(x), (g1 + g2).astype(np.float32), eps)
+    # g1 + g2 is rounded to fp32 once: 2^-24 of |g1| + |g2| per entry
+    assert np.all(np.abs(y12 - (y1 + y2)) <= 1e-6 * (s1 + s2))
+
+
 # ---------------------------------------------------------------- MoE
 
 def _moe_case(E=4, H=256, F=512, T=3, K=2, seed=20):
