@@ -505,6 +505,22 @@ def bench_prefill(q4k, dev, stream, reps=20):
         us = s.elapsed_time(e) * 1e3 / reps
         flop = 2.0 * m * n * k
         out[name] = {"us": round(us, 2), "tflops": round(flop / us / 1e6, 1)}
+        # the same projection with the fused RMSNorm prologue (rinv kernel + GEMM
+        # with gamma in the dequant and rinv in the epilogue)
+        gamma = torch.rand(k, generator=torch.Generator().manual_seed(synth.derive_seed(1003, "g", name)))
+        gamma = (gamma + 0.5).to(dev)
+        rinv = torch.empty(m, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                q4k.q4k_gemm_rmsnorm(w, n, k, x, gamma, 1e-6, out=y, rinv=rinv, stream=stream)
+            s.record(stream)
+            for _ in range(reps):
+                q4k.q4k_gemm_rmsnorm(w, n, k, x, gamma, 1e-6, out=y, rinv=rinv, stream=stream)
+            e.record(stream)
+        torch.cuda.synchronize()
+        us_n = s.elapsed_time(e) * 1e3 / reps
+        out[name + "_rmsnorm"] = {"us": round(us_n, 2), "tflops": round(flop / us_n / 1e6, 1),
+                                  "vs_plain": round(us / us_n, 3)}
     return out
 
 
@@ -586,7 +602,8 @@ def run_case(case):
     """One small instance of a kernel, for ncu captures (no timing): one 27B-class
     layer of batch-1 projections (203 MB of weights) or of batch-4 and batch-16
     projections, the 512-token gate and
-    down prefill GEMMs, or one routed-MoE decode step."""
+    down prefill GEMMs (plain or with the RMSNorm prologue), or one routed-MoE
+    decode step."""
     import bit_block_quantized_q4_gb300 as q4k
     from bit_block_quantized_q4_gb300 import build as qb
     qb.build()
@@ -601,7 +618,7 @@ def run_case(case):
             ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])
             torch.cuda.synchronize()
             q4k.q4k_gemv_seq(ops, batch)
-    elif case == "gemm_prefill":
+    elif case in ("gemm_prefill", "gemm_prefill_rmsnorm"):
         m = 512
         for name, n, k in (("gate", 17408, 5120), ("down", 5120, 17408)):
             w = synth.q4k_weight(n, k, seed=synth.derive_seed(1003, "w", name), quants="normal",
@@ -609,7 +626,11 @@ def run_case(case):
             x = synth.bf16_normal((m, k), seed=synth.derive_seed(1003, "x", name), sigma=0.5,
                                   device=dev)
             torch.cuda.synchronize()
-            q4k.q4k_gemm(w, n, k, x)
+            if case == "gemm_prefill":
+                q4k.q4k_gemm(w, n, k, x)
+            else:
+                gamma = torch.full((k,), 1.25, dtype=torch.float32, device=dev)
+                q4k.q4k_gemm_rmsnorm(w, n, k, x, gamma, 1e-6)
     else:
         bench_moe(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
     torch.cuda.synchronize()
@@ -689,7 +710,7 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS)
     ap.add_argument("--cpu-table", action="store_true",
                     help="time the oracle on the host cores for every configuration, then exit")
-    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "moe"],
+    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "gemm_prefill_rmsnorm", "moe"],
                     help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
     if args.cpu_table:

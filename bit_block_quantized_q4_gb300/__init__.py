@@ -26,7 +26,7 @@ STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN"
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
 Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
-           "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm",
+           "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm", "q4k_gemm_rmsnorm",
            "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
            "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_gemv_seq.argtypes = [ctypes.POINTER(GemvOp), I64, I64, ctypes.c_uint32, P]
         L.q4k_gemm.restype = ctypes.c_int
         L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_gemm_rmsnorm.restype = ctypes.c_int
+        L.q4k_gemm_rmsnorm.argtypes = [P, I64, I64, P, I64, I64, P, ctypes.c_float, P, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
         L.q4k_moe_workspace_size.argtypes = [I32, I32, I32, I64, I64]
         L.q4k_moe_workspace_views.restype = ctypes.c_int
@@ -197,6 +199,22 @@ def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=
     _check(lib().q4k_gemm(_ptr(w), n, k, _ptr(x), m, x.stride(0), _ptr(out), out.stride(0),
                           _stream(stream)), "q4k_gemm")
     return out
+
+
+def q4k_gemm_rmsnorm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, gamma: torch.Tensor,
+                     eps: float, out=None, rinv=None, stream=None):
+    """Y = rinv * (X (W diag(gamma))^T), rinv = 1/sqrt(mean(X^2) + eps) per token;
+    returns (Y bf16 [M, N], rinv fp32 [M])."""
+    m = x.shape[0]
+    if out is None:
+        ld = (n + 7) // 8 * 8
+        out = torch.empty((m, ld), dtype=torch.bfloat16, device=x.device)[:, :n]
+    if rinv is None:
+        rinv = torch.empty(m, dtype=torch.float32, device=x.device)
+    _check(lib().q4k_gemm_rmsnorm(_ptr(w), n, k, _ptr(x), m, x.stride(0), _ptr(gamma), float(eps),
+                                  _ptr(rinv), _ptr(out), out.stride(0), _stream(stream)),
+           "q4k_gemm_rmsnorm")
+    return out, rinv
 
 
 def q4k_moe_workspace_size(n_experts: int, n_tokens: int, top_k: int, hidden: int, ffn: int) -> int:

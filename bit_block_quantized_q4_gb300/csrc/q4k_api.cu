@@ -297,6 +297,26 @@ int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int6
   return map_launch(launch_gemm(w, n, k, x, m, ldx, y, ldy, static_cast<cudaStream_t>(stream)));
 }
 
+int q4k_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
+                     const float *gamma, float eps, float *rinv, void *y, int64_t ldy,
+                     void *stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || m < 0) return Q4K_ERR_SHAPE;
+  if (n > INT32_MAX / 2 || m > INT32_MAX / 2 || k > INT32_MAX / 2) return Q4K_ERR_SHAPE;
+  if (!(eps >= 0.f) || eps > 3.0e38f) return Q4K_ERR_SHAPE;  // negative, NaN or infinite
+  if (n == 0 || m == 0) return Q4K_OK;
+  if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
+  if (!w || !x || !y || !gamma || !rinv) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 16) || (ldx % 8) != 0 || (ldy % 8) != 0 ||
+      !aligned(gamma, 16) || !aligned(rinv, 4))
+    return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w, x, y, gamma, rinv});
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_gemm_rmsnorm(w, n, k, x, m, ldx, gamma, eps, rinv, y, ldy,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
                               int64_t ffn) {
   if (n_experts <= 0 || n_tokens < 0 || top_k <= 0 || hidden <= 0 || ffn <= 0) return 0;

@@ -28,6 +28,12 @@
 // [token][row] in the idle shared memory and written as whole token rows.
 // With split K the CTAs of a weight tile first push the partials of the column
 // chunks they do not own into the owners' shared memory (below).
+// With an RMSNorm prologue (q4k_gemm_rmsnorm) the normalised activations are
+// never formed: Y[t, n] = rinv[t] sum_k (W[n, k] gamma[k]) X[t, k].  The raw W
+// producer also copies gamma of each super-block next to its raw rows, the
+// dequantizing warps round fma(d sc, q, -dmin m) * gamma[k] to bf16, and the
+// epilogue scales each token's accumulators by rinv[t] (computed beforehand by
+// rms_rinv_kernel, one warp per token).
 // The kernel is launched as a programmatic dependent of the kernel before it
 // and touches no global memory before that kernel has completed.
 // Stages are chained by mbarriers; every wait is bounded and reports a
@@ -64,7 +70,10 @@ struct GemmSmem {
   static constexpr int kX = 0;
   static constexpr int kB = kX + kXStages * kXStageBytes;
   static constexpr int kRaw = kB + kBStages * kBStageBytes;
-  static constexpr int kBars = kRaw + kRawStages * kRawBytes;
+  static constexpr int kGammaBytes = kQK * 4;                  // gamma of one super-block
+  static constexpr int kGamma = kRaw + kRawStages * kRawBytes;  // one per raw stage
+  static constexpr int kRinv = kGamma + kRawStages * kGammaBytes;  // rinv of the tile's tokens
+  static constexpr int kBars = kRinv + kTokens * 4;
   // barriers: xfull, xempty (per stage and half), bfull, bempty, rfull, rempty,
   // acc, split-K partials received
   static constexpr int kNumBars = 4 * kXStages + 2 * kBStages + 2 * kRawStages + 2;
@@ -89,6 +98,8 @@ struct GemmArgs {
   __nv_bfloat16 *y;
   int64_t ldy;
   int m, n, k;
+  const float *gamma;  // RMSNorm weights (k), or null: no norm
+  const float *rinv;   // per-token 1/rms (m), when gamma is set
   unsigned *err;
 };
 
@@ -263,14 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = sb % kRawStages;
         const uint32_t ph = (uint32_t)((sb / kRawStages) & 1);
         if (!mbar_wait(&rempty[s], ph ^ 1u, a.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(&rfull[s], L::kRawBytes);
+        mbar_arrive_expect_tx(&rfull[s], L::kRawBytes + (a.gamma ? L::kGammaBytes : 0));
         tma_load_3d(smem + L::kRaw + s * L::kRawBytes, &wmap, &rfull[s], 0, sb_lo + sb, n0);
+        if (a.gamma)
+          bulk_load(smem + L::kGamma + s * L::kGammaBytes, a.gamma + (size_t)(sb_lo + sb) * kQK,
+                    L::kGammaBytes, &rfull[s]);
       }
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- dequantize
     const int row = threadIdx.x - 128;  // weight row within the tile
     const int r8 = row & 7;
+    const bool norm = a.gamma != nullptr;
     uint8_t *brow0 = smem + L::kB + (row >> 3) * 1024 + r8 * 128;
     for (int sb = 0; sb < nsb && ok; ++sb) {
       const int rs = sb % kRawStages;
@@ -286,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bs = kb % kBStages;
         const uint4 q0 = *reinterpret_cast<const uint4 *>(raw + kQsOffset + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4 *>(raw + kQsOffset + 32 * c + 16);
-        if (c == 3) {  // raw stage fully read
+        if (c == 3 && !norm) {  // raw stage fully read (with gamma: after its last use)
           __syncwarp();
           if (lane == 0) mbar_arrive(&rempty[rs]);
         }
@@ -316,16 +331,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             q[e] = __uint_as_float(__byte_perm(ma, 0x4B000000u, 0x7540u + e)) - 8388608.f;
             q[4 + e] = __uint_as_float(__byte_perm(mb, 0x4B000000u, 0x7540u + e)) - 8388608.f;
           }
+          float wv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wv[e] = fmaf(ds, q[e], -dm);
+          if (norm) {  // gamma of k = 64 c + 8 j .. + 7 (the same for every row: broadcast)
+            const float4 *gp = reinterpret_cast<const float4 *>(
+                smem + L::kGamma + rs * L::kGammaBytes + 4 * (64 * c + 8 * j));
+            const float4 g0 = gp[0], g1 = gp[1];
+            wv[0] *= g0.x;
+            wv[1] *= g0.y;
+            wv[2] *= g0.z;
+            wv[3] *= g0.w;
+            wv[4] *= g1.x;
+            wv[5] *= g1.y;
+            wv[6] *= g1.z;
+            wv[7] *= g1.w;
+          }
           uint4 o;
-          o.x = pack_bf16(fmaf(ds, q[0], -dm), fmaf(ds, q[1], -dm));
-          o.y = pack_bf16(fmaf(ds, q[2], -dm), fmaf(ds, q[3], -dm));
-          o.z = pack_bf16(fmaf(ds, q[4], -dm), fmaf(ds, q[5], -dm));
-          o.w = pack_bf16(fmaf(ds, q[6], -dm), fmaf(ds, q[7], -dm));
+          o.x = pack_bf16(wv[0], wv[1]);
+          o.y = pack_bf16(wv[2], wv[3]);
+          o.z = pack_bf16(wv[4], wv[5]);
+          o.w = pack_bf16(wv[6], wv[7]);
           *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bfull[bs]);
+        if (c == 3 && norm) {  // raw rows and gamma of the stage fully read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rempty[rs]);
+        }
       }
     }
   }
@@ -342,6 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c_lo = (warp >> 2) * 4, c_hi = c_lo + 4;
   const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
   if (acc_ready) tc_fence_after();
+  // 1/rms of the tile's tokens, staged once (every role loop is done; the
+  // region is used by nothing else)
+  float *rinv_s = reinterpret_cast<float *>(smem + L::kRinv);
+  if (a.gamma) {
+    for (int i = threadIdx.x; i < kTokens; i += kThreads)
+      rinv_s[i] = (m0 + i < a.m) ? a.rinv[m0 + i] : 0.f;
+    __syncthreads();
+  }
   if constexpr (KS == 1) {
     // The bf16 tile is staged as [token][row] in shared memory (idle now: all
     // copies and MMAs are done) and then written as whole 256-byte token rows;
@@ -358,10 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c + 16), r1);
           tmem_ld_wait();
           __nv_bfloat16 *col = stage + (128 * sub + 16 * c) * kBN + row;
+          if (a.gamma) {
+            const float *rv = rinv_s + 128 * sub + 16 * c;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]));
-            col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]));
+            for (int e = 0; e < 16; ++e) {
+              col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]) * rv[e]);
+              col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]) * rv[16 + e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]));
+              col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]));
+            }
           }
         }
       }
@@ -454,6 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[4 * u + 3] = z ? v[4 * u + 3] + t.w : t.w;
             }
           }
+          if (a.gamma) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= rinv_s[128 * sub + 16 * c + e];
+          }
           store_y16_rows(a, m0 + 128 * sub + 16 * c, n0 + row, v);
         }
       }
@@ -505,8 +561,6 @@ cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &
   return go(gemm_kernel<1, 1>);
 }
 
-}  // namespace
-
 #ifndef Q4K_GEMM_CLUSTER
 #define Q4K_GEMM_CLUSTER 2
 #endif
@@ -514,8 +568,53 @@ cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &
 #define Q4K_GEMM_SPLITK 1
 #endif
 
+// 1/rms of each token row of X: one CTA of 256 threads per token (the whole
+// of X in flight at once), fp32 sum of squares in a fixed order (thread i
+// takes the 16-byte pieces i, i + 256, ...; a butterfly within each warp; the
+// eight warp sums added in warp order), rinv = 1 / sqrt(sum / k + eps) with
+// IEEE division and square root.  Launched as a programmatic dependent of the
+// kernel before it.
+__global__ void __launch_bounds__(256) rms_rinv_kernel(const __nv_bfloat16 *x, int64_t ldx, int m,
+                                                       int k, float eps, float *rinv) {
+  __shared__ float part[8];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4 *row = reinterpret_cast<const uint4 *>(x + (int64_t)t * ldx);
+  float s = 0.f;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < k / 8; i += 256) {
+    const uint4 v = row[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      s = fmaf(lo, lo, s);
+      s = fmaf(hi, hi, s);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = part[0];
+#pragma unroll
+    for (int w8 = 1; w8 < 8; ++w8) tot += part[w8];
+    rinv[t] = 1.f / sqrtf(tot / (float)k + eps);
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream) {
+  return launch_gemm_rmsnorm(w, n, k, x, m, ldx, nullptr, 0.f, nullptr, y, ldy, stream);
+}
+
+cudaError_t launch_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t m,
+                                int64_t ldx, const float *gamma, float eps, float *rinv, void *y,
+                                int64_t ldy, cudaStream_t stream) {
   std::call_once(g_gemm_attr[device_facts()->device], gemm_attributes);
   const int nsb = (int)(k / kQK);
   CUtensorMap xmap, wmap;
@@ -541,6 +640,8 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   args.m = (int)m;
   args.n = (int)n;
   args.k = (int)k;
+  args.gamma = gamma;
+  args.rinv = rinv;
   args.err = device_error_word();
 
   // K is split across a cluster (up to 4 ways) when the output tiles cannot
@@ -571,6 +672,18 @@ cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int6
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  if (gamma) {
+    cudaLaunchConfig_t pre = {};
+    pre.gridDim = dim3((unsigned)m, 1, 1);
+    pre.blockDim = dim3(256, 1, 1);
+    pre.stream = stream;
+    pre.attrs = &attr[1];  // programmatic dependent of the kernel before it
+    pre.numAttrs = 1;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&pre, rms_rinv_kernel, static_cast<const __nv_bfloat16 *>(x), ldx,
+                           (int)m, (int)k, eps, rinv);
+    if (e != cudaSuccess) return e;
+  }
   return gemm_go(cfg, cs, ks, xmap, wmap, args);
 }
 

@@ -57,6 +57,11 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
                           cudaStream_t stream);
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
+// The same with an RMSNorm prologue (gamma non-null): rinv (m floats) is
+// written first, then Y = rinv (X (W diag(gamma))^T).
+cudaError_t launch_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t m,
+                                int64_t ldx, const float *gamma, float eps, float *rinv, void *y,
+                                int64_t ldy, cudaStream_t stream);
 size_t moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
                           int64_t ffn);
 // Byte offsets in the MoE workspace of: the pair index of every (token, slot)

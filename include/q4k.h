@@ -219,6 +219,29 @@ int q4k_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int6
              void *y, int64_t ldy, void *stream);
 
 /*
+ * q4k_gemm_rmsnorm -- prefill projection of RMS-normalised activations
+ * ("spec: specialized model runtimes", section "Feasibility gate": one
+ *  quantized GEMM plus fused RMSNorm, the norm as the GEMM's prologue):
+ *     rinv[t] = 1 / sqrt( (1/K) sum_i X[t,i]^2 + eps )          (fp32, written)
+ *     Y[t, j] = bf16( rinv[t] * sum_i W[j,i] gamma[i] X[t,i] )
+ * The normalised activations are never formed: gamma scales each weight as it
+ * is dequantized (bf16(w * gamma[i])), and rinv scales the accumulators of
+ * token t.  A first kernel (one warp per token, programmatic dependent of the
+ * kernel before it) writes rinv; the GEMM follows as its programmatic
+ * dependent.  Accuracy: |Y - Y_ref| <= 1e-2 * sum_i |W[j,i]| |xh[t,i]| per
+ * element, xh = X rinv gamma (the q4k_gemm bound on the normalised input).
+ *   gamma   device, K fp32, 16-byte aligned
+ *   eps     finite, >= 0
+ *   rinv    device, m fp32, 4-byte aligned (written; also an output)
+ *   other arguments as q4k_gemm
+ * Errors: NULL, SHAPE (also a negative, NaN or infinite eps), ALIGN, DEVICE,
+ *         MEMORY, CUDA.
+ */
+int q4k_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
+                     const float *gamma, float eps, float *rinv, void *y, int64_t ldy,
+                     void *stream);
+
+/*
  * q4k_moe_workspace_size -- bytes of device workspace q4k_moe_gemv needs.
  */
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

@@ -194,6 +194,26 @@ def test_moe_ex_flags(L):
     assert call(1, H=300) == 2
 
 
+def test_gemm_rmsnorm_argument_errors(L):
+    m, n, k = 8, 128, 256
+
+    def call(**kw):
+        a = dict(w=P, n=n, k=k, x=P, m=m, ldx=k, gamma=P, eps=1e-6, rinv=P, y=P, ldy=n, stream=None)
+        a.update(kw)
+        return L.q4k_gemm_rmsnorm(*a.values())
+
+    assert call(eps=-1.0) == 2
+    assert call(eps=float("nan")) == 2
+    assert call(eps=float("inf")) == 2
+    assert call(k=300) == 2
+    assert call(m=0) == 0
+    assert call(gamma=None) == 1
+    assert call(rinv=None) == 1
+    assert call(gamma=P + 4) == 3
+    assert call(rinv=P + 2) == 3
+    assert call(x=P + 8) == 3
+
+
 def test_get_device_error_rejects_null(L):
     assert L.q4k_get_device_error(None, None) == 1
 
@@ -230,6 +250,7 @@ int main(void) {
   st |= q4k_gemv_glu(0, 0, 4, 256, 0, 1, 256, 0, 4, 0u, 0);
   st |= q4k_gemv_seq(ops, 1, 1, 0u, 0);
   st |= q4k_gemm(0, 4, 256, 0, 1, 256, 0, 8, 0);
+  st |= q4k_gemm_rmsnorm(0, 4, 256, 0, 1, 256, 0, 1e-6f, 0, 0, 8, 0);
   st |= (int)q4k_moe_workspace_size(8, 1, 2, 256, 256);
   st |= q4k_moe_gemv(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0, 0, 0);
   st |= q4k_moe_gemv_ex(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256,
