@@ -29,11 +29,11 @@
 // With split K the CTAs of a weight tile first push the partials of the column
 // chunks they do not own into the owners' shared memory (below).
 // With an RMSNorm prologue (q4k_gemm_rmsnorm) the normalised activations are
-// never formed: Y[t, n] = rinv[t] sum_k (W[n, k] gamma[k]) X[t, k].  The raw W
-// producer also copies gamma of each super-block next to its raw rows, the
-// dequantizing warps round fma(d sc, q, -dmin m) * gamma[k] to bf16, and the
-// epilogue scales each token's accumulators by rinv[t] (computed beforehand by
-// rms_rinv_kernel, one warp per token).
+// never formed: Y[t, n] = rinv[t] sum_k (W[n, k] gamma[k]) X[t, k].  The
+// dequantizing warps round fma(d sc, q, -dmin m) * gamma[k] to bf16 (gamma
+// through the read-only path: every lane of a warp reads the same address),
+// and the epilogue scales each token's accumulators by rinv[t], computed by
+// rms_rinv_kernel (one CTA per token) while the main loop runs.
 // The kernel is launched as a programmatic dependent of the kernel before it
 // and touches no global memory before that kernel has completed.
 // Stages are chained by mbarriers; every wait is bounded and reports a
@@ -70,9 +70,7 @@ struct GemmSmem {
   static constexpr int kX = 0;
   static constexpr int kB = kX + kXStages * kXStageBytes;
   static constexpr int kRaw = kB + kBStages * kBStageBytes;
-  static constexpr int kGammaBytes = kQK * 4;                  // gamma of one super-block
-  static constexpr int kGamma = kRaw + kRawStages * kRawBytes;  // one per raw stage
-  static constexpr int kRinv = kGamma + kRawStages * kGammaBytes;  // rinv of the tile's tokens
+  static constexpr int kRinv = kRaw + kRawStages * kRawBytes;  // rinv of the tile's tokens
   static constexpr int kBars = kRinv + kTokens * 4;
   // barriers: xfull, xempty (per stage and half), bfull, bempty, rfull, rempty,
   // acc, split-K partials received
@@ -207,8 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   // Launched as a programmatic dependent of the previous kernel on the stream:
   // everything above overlaps its tail; no thread touches global memory before
-  // that kernel has completed.
-  grid_dependency_wait();
+  // that kernel has completed.  With the RMSNorm prologue the previous kernel
+  // is rms_rinv_kernel, and this kernel cannot start before each of its CTAs
+  // has waited for the kernel before it (the producer of X) and only then let
+  // its dependents launch: X and W are complete here, and only rinv is waited
+  // for (before the epilogue), so the main loop overlaps the rinv pass.
+  if (!a.gamma) grid_dependency_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
@@ -274,11 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = sb % kRawStages;
         const uint32_t ph = (uint32_t)((sb / kRawStages) & 1);
         if (!mbar_wait(&rempty[s], ph ^ 1u, a.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(&rfull[s], L::kRawBytes + (a.gamma ? L::kGammaBytes : 0));
+        mbar_arrive_expect_tx(&rfull[s], L::kRawBytes);
         tma_load_3d(smem + L::kRaw + s * L::kRawBytes, &wmap, &rfull[s], 0, sb_lo + sb, n0);
-        if (a.gamma)
-          bulk_load(smem + L::kGamma + s * L::kGammaBytes, a.gamma + (size_t)(sb_lo + sb) * kQK,
-                    L::kGammaBytes, &rfull[s]);
       }
     }
   } else if (warp >= 4) {
@@ -301,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bs = kb % kBStages;
         const uint4 q0 = *reinterpret_cast<const uint4 *>(raw + kQsOffset + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4 *>(raw + kQsOffset + 32 * c + 16);
-        if (c == 3 && !norm) {  // raw stage fully read (with gamma: after its last use)
+        if (c == 3) {  // raw stage fully read
           __syncwarp();
           if (lane == 0) mbar_arrive(&rempty[rs]);
         }
@@ -334,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float wv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) wv[e] = fmaf(ds, q[e], -dm);
-          if (norm) {  // gamma of k = 64 c + 8 j .. + 7 (the same for every row: broadcast)
+          if (norm) {  // gamma of k = 64 c + 8 j .. + 7 (the same for every row)
             const float4 *gp = reinterpret_cast<const float4 *>(
-                smem + L::kGamma + rs * L::kGammaBytes + 4 * (64 * c + 8 * j));
-            const float4 g0 = gp[0], g1 = gp[1];
+                a.gamma + (size_t)(sb_lo + sb) * kQK + 64 * c + 8 * j);
+            const float4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
             wv[0] *= g0.x;
             wv[1] *= g0.y;
             wv[2] *= g0.z;
@@ -357,10 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bfull[bs]);
-        if (c == 3 && norm) {  // raw rows and gamma of the stage fully read
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&rempty[rs]);
-        }
       }
     }
   }
@@ -381,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // region is used by nothing else)
   float *rinv_s = reinterpret_cast<float *>(smem + L::kRinv);
   if (a.gamma) {
+    grid_dependency_wait();  // rms_rinv_kernel has completed: rinv is written
     for (int i = threadIdx.x; i < kTokens; i += kThreads)
       rinv_s[i] = (m0 + i < a.m) ? a.rinv[m0 + i] : 0.f;
     __syncthreads();
