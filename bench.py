@@ -552,6 +552,37 @@ def bench_moe(q4k, dev, stream, reps=20):
             "distinct_experts": distinct, "bytes": nbytes}
 
 
+def bench_moe_prefill(q4k, dev, stream, reps=10):
+    """235B-A22B-class routed MoE prefill: 128 experts, hidden 4096, expert ffn
+    1536, 512 tokens, top-8 Zipf(1.1) (4096 pairs): route, gather, grouped
+    tcgen05 GEMMs for gate/up/down, SiLU, weighted sum.  Useful flop = 2 x pairs
+    x 3 x ffn x hidden; touched bytes = the distinct experts' weights + x + y."""
+    E, H, F, T, K = 128, 4096, 1536, 512, 8
+    stride = F * (H // 256) * 144
+    wg = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1006, "g"), device=dev).reshape(-1)
+    wu = synth.q4k_weight(E * F, H, seed=synth.derive_seed(1006, "u"), device=dev).reshape(-1)
+    wd = synth.q4k_weight(E * H, F, seed=synth.derive_seed(1006, "d"), device=dev).reshape(-1)
+    x = synth.bf16_normal((T, H), seed=synth.derive_seed(1006, "x"), device=dev)
+    ids, wts = synth.zipf_routing(T, E, K, seed=1007)
+    distinct = len(set(ids.reshape(-1).tolist()))
+    ids_d, wts_d = ids.to(dev), wts.to(dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(q4k.q4k_moe_prefill_workspace_size(E, T, K, H, F), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        q4k.q4k_moe_prefill(wg, wu, wd, stride, E, H, F, x, ids_d, wts_d, out=y, workspace=ws,
+                            stream=stream)
+
+    ms, per, g = time_graph(step, reps, 3, stream)
+    del g
+    flop = 2.0 * T * K * 3 * F * H
+    nbytes = distinct * 3 * q4k_bytes(F, H) + T * H * 2 + T * H * 4
+    return {"us": round(ms * 1e3, 2), "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "distinct_experts": distinct,
+            "pairs": T * K}
+
+
 KERNEL_SOURCES = ("q4k_stream.cu", "q4k_device.cuh", "q4k_internal.h")
 
 
@@ -631,6 +662,8 @@ def run_case(case):
             else:
                 gamma = torch.full((k,), 1.25, dtype=torch.float32, device=dev)
                 q4k.q4k_gemm_rmsnorm(w, n, k, x, gamma, 1e-6)
+    elif case == "moe_prefill":
+        bench_moe_prefill(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
     else:
         bench_moe(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
     torch.cuda.synchronize()
@@ -710,7 +743,8 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS)
     ap.add_argument("--cpu-table", action="store_true",
                     help="time the oracle on the host cores for every configuration, then exit")
-    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "gemm_prefill_rmsnorm", "moe"],
+    ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "gemm_prefill_rmsnorm", "moe",
+                             "moe_prefill"],
                     help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
     if args.cpu_table:
@@ -812,6 +846,13 @@ def main():
             torch.cuda.empty_cache()
         with nvtx("moe 235b t16"):
             extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
+        torch.cuda.empty_cache()
+        if world == 1:
+            with nvtx("moe prefill 235b t512"):
+                mp = bench_moe_prefill(q4k, dev, stream)
+            mp["frac_of_measured_bf16"] = round(mp["tflops"] / pk["bf16_tflops"], 4)
+            mp["frac_of_measured_hbm"] = round(mp["gbs"] / pk["hbm_gbs"], 4)
+            extra["moe_prefill_235b_a22b_t512"] = mp
     clocks = sampler.summary()
 
     if rank == 0:

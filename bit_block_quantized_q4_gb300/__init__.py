@@ -28,7 +28,8 @@ Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm", "q4k_gemm_rmsnorm",
            "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
-           "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc",
+           "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc", "q4k_moe_prefill",
+           "q4k_moe_prefill_workspace_size",
            "q4k_get_device_error", "q4k_selftest_wait_timeout")
 
 _lock = threading.Lock()
@@ -87,6 +88,11 @@ def lib() -> ctypes.CDLL:
         L.q4k_moe_gemv_ex.restype = ctypes.c_int
         L.q4k_moe_gemv_ex.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
                                       ctypes.c_uint32, P, SZ, P]
+        L.q4k_moe_prefill_workspace_size.restype = SZ
+        L.q4k_moe_prefill_workspace_size.argtypes = [I32, I32, I32, I64, I64]
+        L.q4k_moe_prefill.restype = ctypes.c_int
+        L.q4k_moe_prefill.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P, I64,
+                                      P, SZ, P]
         L.q4k_moe_gemv_noalloc.restype = ctypes.c_int
         L.q4k_moe_gemv_noalloc.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32, P,
                                            I64, P]
@@ -262,6 +268,29 @@ def q4k_moe_gemv_ex(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hi
                                  hidden, ffn, _ptr(x), T, x.stride(0), _ptr(ids), _ptr(wts), top_k,
                                  _ptr(out), out.stride(0), flags, _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "q4k_moe_gemv_ex")
+    return out
+
+
+def q4k_moe_prefill_workspace_size(n_experts: int, n_tokens: int, top_k: int, hidden: int,
+                                   ffn: int) -> int:
+    return int(lib().q4k_moe_prefill_workspace_size(n_experts, n_tokens, top_k, hidden, ffn))
+
+
+def q4k_moe_prefill(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int,
+                    ffn: int, x: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor, out=None,
+                    workspace=None, stream=None):
+    """Routed-expert FFN for a block of tokens (grouped tensor-core GEMMs);
+    returns fp32 [T, hidden]."""
+    T, top_k = ids.shape
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x.device)
+    ws_bytes = q4k_moe_prefill_workspace_size(n_experts, T, top_k, hidden, ffn)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().q4k_moe_prefill(_ptr(w_gate), _ptr(w_up), _ptr(w_down), expert_stride, n_experts,
+                                 hidden, ffn, _ptr(x), T, x.stride(0), _ptr(ids), _ptr(wts), top_k,
+                                 _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "q4k_moe_prefill")
     return out
 
 

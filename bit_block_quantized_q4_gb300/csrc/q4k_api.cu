@@ -370,6 +370,43 @@ int q4k_moe_gemv_ex(const void *w_gate, const void *w_up, const void *w_down,
                                static_cast<cudaStream_t>(stream)));
 }
 
+size_t q4k_moe_prefill_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k,
+                                      int64_t hidden, int64_t ffn) {
+  if (n_experts <= 0 || n_tokens < 0 || top_k <= 0 || hidden <= 0 || ffn <= 0) return 0;
+  return moe_prefill_workspace_size(n_experts, n_tokens, top_k, hidden, ffn);
+}
+
+int q4k_moe_prefill(const void *w_gate, const void *w_up, const void *w_down,
+                    int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                    const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                    const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  if (n_experts <= 0 || n_experts > 2048 || hidden <= 0 || ffn <= 0 || (hidden % kQK) ||
+      (ffn % kQK) || n_tokens < 0 || n_tokens > 65535 || top_k < 1 || top_k > 16)
+    return Q4K_ERR_SHAPE;
+  if (hidden > (1 << 20) || ffn > (1 << 20)) return Q4K_ERR_SHAPE;
+  if ((int64_t)n_tokens * top_k * (hidden > ffn ? hidden : ffn) > ((int64_t)1 << 31))
+    return Q4K_ERR_SHAPE;
+  if (expert_stride < (ffn * hidden / kQK) * kBlockBytes) return Q4K_ERR_SHAPE;
+  if (n_tokens == 0) return Q4K_OK;
+  if (ldx < hidden || ldy < hidden) return Q4K_ERR_SHAPE;
+  if (!w_gate || !w_up || !w_down || !x || !ids || !wts || !y) return Q4K_ERR_NULL;
+  if (!workspace ||
+      workspace_bytes < moe_prefill_workspace_size(n_experts, n_tokens, top_k, hidden, ffn))
+    return Q4K_ERR_WORKSPACE;
+  if (!aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) || (expert_stride % 16) ||
+      !aligned(x, 16) || (ldx % 8) || !aligned(y, 4) || !aligned(ids, 4) || !aligned(wts, 4) ||
+      !aligned(workspace, 16))
+    return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w_gate, w_up, w_down, x, ids, wts, y, workspace});
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_moe_prefill(w_gate, w_up, w_down, expert_stride, n_experts, hidden, ffn,
+                                       x, n_tokens, ldx, ids, wts, top_k, y, ldy, workspace,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int q4k_moe_gemv_noalloc(const void *w_gate, const void *w_up, const void *w_down,
                          int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
                          const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,

@@ -34,6 +34,17 @@
 // through the read-only path: every lane of a warp reads the same address),
 // and the epilogue scales each token's accumulators by rinv[t], computed by
 // rms_rinv_kernel (one CTA per token) while the main loop runs.
+// Grouped (G = true; the expert matmuls of routed-MoE prefill): CTA (n-tile,
+// slot) multiplies the tokens of one work slot -- rows [p0, p0 + np) of an
+// expert-sorted X, np <= 256 -- by 128 rows of the slot's expert, whose Q4_K
+// matrix is reached through a fourth (expert) dimension of the weight tensor
+// map.  The slot table comes from the route kernel; a CTA whose slot is not in
+// use does nothing.  The slot's 128-row sub-tiles that hold tokens are copied
+// and multiplied with N = np rounded up to 16 (rows past the slot's end are
+// computed and not stored).  With so few tokens per weight tile the latency of
+// the X copies is what bounds the tile, so the X region holds four stages of
+// 256 tokens instead of two of 512.  Output rows are the slot's rows of an
+// expert-sorted Y.
 // The kernel is launched as a programmatic dependent of the kernel before it
 // and touches no global memory before that kernel has completed.
 // Stages are chained by mbarriers; every wait is bounded and reports a
@@ -74,6 +85,9 @@ struct GemmSmem {
   static constexpr int kBars = kRinv + kTokens * 4;
   // barriers: xfull, xempty (per stage and half), bfull, bempty, rfull, rempty,
   // acc, split-K partials received
+  // grouped tiles (at most 256 tokens) use the X region as 4 stages of one
+  // 256-token half each: the same 4 pairs of X barriers
+  static constexpr int kXStagesG = kXStages * kXParts;
   static constexpr int kNumBars = 4 * kXStages + 2 * kBStages + 2 * kRawStages + 2;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
@@ -98,6 +112,8 @@ struct GemmArgs {
   int m, n, k;
   const float *gamma;  // RMSNorm weights (k), or null: no norm
   const float *rinv;   // per-token 1/rms (m), when gamma is set
+  // grouped: the route kernel's slot table (meta[0] = slots in use)
+  const int *slot_expert, *slot_start, *meta;
   unsigned *err;
 };
 
@@ -134,16 +150,22 @@ __device__ __forceinline__ void store_y16_rows(const GemmArgs &a, int m, int n, 
 // multicast).  The KS CTAs with the same n split K: CTA z contracts
 // super-blocks [z nsb / KS, (z+1) nsb / KS) into its own TMEM, and the partial
 // tiles are summed through distributed shared memory (below).
-template <int CS, int KS>
+template <int CS, int KS, bool G = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmArgs a) {
+  static_assert(!G || (CS == 1 && KS == 1), "grouped tiles: one CTA per tile, no multicast");
   using L = GemmSmem;
-  constexpr int kXStages = L::kXStages, kXParts = L::kXParts;
+  // X stages: 2 of 512 tokens (two 256-token halves), or, grouped, 4 of 256
+  constexpr int kXStages = G ? L::kXStagesG : L::kXStages;
+  constexpr int kXParts = G ? 1 : L::kXParts;
+  constexpr int kXStride = G ? L::kXPartBytes : L::kXStageBytes;
   constexpr int kBStages = L::kBStages, kRawStages = L::kRawStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
+  auto raw_stage = [&](int s) -> uint8_t * { return smem + L::kRaw + s * L::kRawBytes; };
+  auto b_stage = [&](int s) -> uint8_t * { return smem + L::kB + s * L::kBStageBytes; };
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
   uint64_t *xfull = bars;  // [stage * kXParts + half]
   uint64_t *xempty = xfull + kXStages * kXParts;
@@ -158,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBN;
-  const int m0 = blockIdx.y * kTokens;
+  int m0 = G ? 0 : blockIdx.y * kTokens;
   const uint32_t crank = (CS * KS > 1) ? cluster_ctarank() : 0u;
   const uint32_t rank = crank % CS;   // position among the CTAs sharing X
   const uint32_t krank = crank / CS;  // K range of this CTA
@@ -166,9 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // indices relative to the range (k-block kb covers k = 64 (kb_lo + kb) ..).
   const int nsb_all = a.k / kQK;
   const int sb_lo = (int)((int64_t)krank * nsb_all / KS);
-  const int nsb = (int)((int64_t)(krank + 1) * nsb_all / KS) - sb_lo;
-  const int nkb = nsb * (kQK / kBK);
+  int nsb = (int)((int64_t)(krank + 1) * nsb_all / KS) - sb_lo;
+  int nkb = nsb * (kQK / kBK);
   const int kb_lo = sb_lo * (kQK / kBK);
+  int np = kTokens;  // tokens of this tile (grouped: of the slot)
+  int expert = 0;
   const uint16_t kMask = (uint16_t)(((1u << CS) - 1u) << (krank * CS));  // X sharers
 
   if (threadIdx.x == 0) {
@@ -211,6 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // its dependents launch: X and W are complete here, and only rinv is waited
   // for (before the epilogue), so the main loop overlaps the rinv pass.
   if (!a.gamma) grid_dependency_wait();
+  if constexpr (G) {
+    // the slot table is the route kernel's output: read after the wait
+    const int slot = blockIdx.y;
+    if (slot < a.meta[0]) {
+      m0 = a.slot_start[slot];
+      // at most 256 (the route kernel's slot size): one 256-token X stage
+      np = min(a.slot_start[slot + 1] - m0, 256);
+      expert = a.slot_expert[slot];
+    } else {
+      np = 0;
+    }
+    if (np <= 0) nsb = nkb = 0;  // every role loop below is empty
+  } else {
+    np = min(kTokens, a.m - m0);
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
@@ -218,13 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int s = kb % kXStages;
         const uint32_t ph = (uint32_t)((kb / kXStages) & 1);
-        uint8_t *dst = smem + L::kX + s * L::kXStageBytes;
+        uint8_t *dst = smem + L::kX + s * kXStride;
         const int kx = (kb_lo + kb) * kBK;
         for (int h = 0; h < kXParts; ++h) {
+          if (G && np <= 256 * h) break;  // no tokens in this half
           uint64_t *full = &xfull[s * kXParts + h];
           if (!mbar_wait(&xempty[s * kXParts + h], ph ^ 1u, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(full, L::kXPartBytes);
-          for (int sub = 2 * h + (int)rank; sub < 2 * h + 2; sub += CS) {
+          // grouped: only the 128-row sub-tiles that hold tokens
+          const int nsub = G ? min(2, (np - 256 * h + 127) / 128) : 2;
+          mbar_arrive_expect_tx(full, (uint32_t)nsub * L::kXSubBytes);
+          for (int sub = 2 * h + (int)rank; sub < 2 * h + nsub; sub += CS) {
             if (CS > 1)
               tma_load_2d_mc(dst + sub * L::kXSubBytes, &xmap, full, kx, m0 + 128 * sub, kMask);
             else
@@ -236,14 +278,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBN, 256);
+      // N = 256 per half; grouped: the half's tokens rounded up to 16
+      const uint32_t idesc0 = G ? idesc_bf16_f32(kBN, min(256, (np + 15) / 16 * 16))
+                                : idesc_bf16_f32(kBN, 256);
+      const uint32_t idesc1 = G ? idesc_bf16_f32(kBN, max(16, min(256, (np - 256 + 15) / 16 * 16)))
+                                : idesc_bf16_f32(kBN, 256);
       const uint32_t xbase = smem_u32(smem + L::kX);
-      const uint32_t bbase = smem_u32(smem + L::kB);
+
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int xs = kb % kXStages, bs = kb % kBStages;
         if (!mbar_wait(&bfull[bs], (uint32_t)((kb / kBStages) & 1), a.err)) { ok = false; break; }
 #pragma unroll
         for (int h = 0; h < kXParts; ++h) {
+          if (G && np <= 256 * h) break;  // no tokens in this half
+          const uint32_t idesc = h ? idesc1 : idesc0;
           if (!mbar_wait(&xfull[xs * kXParts + h], (uint32_t)((kb / kXStages) & 1), a.err)) {
             ok = false;
             break;
@@ -254,9 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // bytes, contiguous), accumulated in TMEM columns 256 h ...
 #pragma unroll
           for (int k16 = 0; k16 < kBK / 16; ++k16) {
-            const uint64_t wdesc = sdesc_sw128(bbase + bs * L::kBStageBytes + k16 * 32, 1024);
+            const uint64_t wdesc = sdesc_sw128(smem_u32(b_stage(bs)) + k16 * 32, 1024);
             const uint64_t xdesc =
-                sdesc_sw128(xbase + xs * L::kXStageBytes + h * L::kXPartBytes + k16 * 32, 1024);
+                sdesc_sw128(xbase + xs * kXStride + h * L::kXPartBytes + k16 * 32, 1024);
             tc_mma_f16(tmem + h * 256, wdesc, xdesc, idesc, (kb | k16) != 0);
           }
           if (CS > 1)
@@ -277,7 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)((sb / kRawStages) & 1);
         if (!mbar_wait(&rempty[s], ph ^ 1u, a.err)) { ok = false; break; }
         mbar_arrive_expect_tx(&rfull[s], L::kRawBytes);
-        tma_load_3d(smem + L::kRaw + s * L::kRawBytes, &wmap, &rfull[s], 0, sb_lo + sb, n0);
+        if (G)
+          tma_load_4d(raw_stage(s), &wmap, &rfull[s], 0, sb_lo + sb, n0, expert);
+        else
+          tma_load_3d(raw_stage(s), &wmap, &rfull[s], 0, sb_lo + sb, n0);
       }
     }
   } else if (warp >= 4) {
@@ -285,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x - 128;  // weight row within the tile
     const int r8 = row & 7;
     const bool norm = a.gamma != nullptr;
-    uint8_t *brow0 = smem + L::kB + (row >> 3) * 1024 + r8 * 128;
+    const int brow_off = (row >> 3) * 1024 + r8 * 128;
     for (int sb = 0; sb < nsb && ok; ++sb) {
       const int rs = sb % kRawStages;
       if (!mbar_wait(&rfull[rs], (uint32_t)((sb / kRawStages) & 1), a.err)) { ok = false; break; }
-      const uint8_t *raw = smem + L::kRaw + rs * L::kRawBytes + row * kBlockBytes;
+      const uint8_t *raw = raw_stage(rs) + row * kBlockBytes;
       const uint4 h = *reinterpret_cast<const uint4 *>(raw);
       uint32_t sc_lo, sc_hi, m_lo, m_hi;
       scales_all(h.y, h.z, h.w, &sc_lo, &sc_hi, &m_lo, &m_hi);
@@ -315,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t *brow = brow0 + bs * L::kBStageBytes;
+        uint8_t *brow = b_stage(bs) + brow_off;
         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
@@ -324,33 +375,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ma = (hi ? (wa >> 4) : wa) & 0x0F0F0F0Fu;
           const uint32_t mb = (hi ? (wb >> 4) : wb) & 0x0F0F0F0Fu;
           const float ds = hi ? ds1 : ds0, dm = hi ? dm1 : dm0;
-          float q[8];
+          // pairs of weights on the packed fp32 pipe (each lane of a pair
+          // rounds exactly as the scalar operation): 0x4B00000q is 2^23 + q
+          // exactly, so the subtraction gives q exactly; then fma(ds, q, -dm)
+          const float2 m23 = make_float2(-8388608.f, -8388608.f);
+          const float2 ds2 = make_float2(ds, ds), ndm2 = make_float2(-dm, -dm);
+          float2 wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {  // 0x4B00000q is 2^23 + q exactly
-            q[e] = __uint_as_float(__byte_perm(ma, 0x4B000000u, 0x7540u + e)) - 8388608.f;
-            q[4 + e] = __uint_as_float(__byte_perm(mb, 0x4B000000u, 0x7540u + e)) - 8388608.f;
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t src = e < 2 ? ma : mb;
+            const float2 qq = __fadd2_rn(
+                make_float2(__uint_as_float(__byte_perm(src, 0x4B000000u, 0x7540u + 2 * (e & 1))),
+                            __uint_as_float(__byte_perm(src, 0x4B000000u, 0x7541u + 2 * (e & 1)))),
+                m23);
+            wv[e] = __ffma2_rn(ds2, qq, ndm2);
           }
-          float wv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) wv[e] = fmaf(ds, q[e], -dm);
           if (norm) {  // gamma of k = 64 c + 8 j .. + 7 (the same for every row)
             const float4 *gp = reinterpret_cast<const float4 *>(
                 a.gamma + (size_t)(sb_lo + sb) * kQK + 64 * c + 8 * j);
             const float4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
-            wv[0] *= g0.x;
-            wv[1] *= g0.y;
-            wv[2] *= g0.z;
-            wv[3] *= g0.w;
-            wv[4] *= g1.x;
-            wv[5] *= g1.y;
-            wv[6] *= g1.z;
-            wv[7] *= g1.w;
+            wv[0] = __fmul2_rn(wv[0], make_float2(g0.x, g0.y));
+            wv[1] = __fmul2_rn(wv[1], make_float2(g0.z, g0.w));
+            wv[2] = __fmul2_rn(wv[2], make_float2(g1.x, g1.y));
+            wv[3] = __fmul2_rn(wv[3], make_float2(g1.z, g1.w));
           }
           uint4 o;
-          o.x = pack_bf16(wv[0], wv[1]);
-          o.y = pack_bf16(wv[2], wv[3]);
-          o.z = pack_bf16(wv[4], wv[5]);
-          o.w = pack_bf16(wv[6], wv[7]);
+          o.x = pack_bf16(wv[0].x, wv[0].y);
+          o.y = pack_bf16(wv[1].x, wv[1].y);
+          o.z = pack_bf16(wv[2].x, wv[2].y);
+          o.w = pack_bf16(wv[3].x, wv[3].y);
           *reinterpret_cast<uint4 *>(brow + ((j ^ r8) << 4)) = o;
         }
         fence_proxy_async_smem();
@@ -365,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // each 128-token sub-tile, the 16-column chunks [4 (w / 4), 4 (w / 4) + 4).
   __syncwarp();
   ok = __all_sync(0xffffffffu, ok);  // a role loop that timed out ran on lane 0 only
-  const bool acc_ready = ok && mbar_wait(accfull, 0u, a.err);
+  const bool acc_ready = ok && mbar_wait(accfull, 0u, a.err) && np > 0;
   grid_launch_dependents();  // the next kernel's CTAs may take this SM as soon as it is free
   const int q = warp & 3;
   const int row = 32 * q + lane;  // weight row within the tile
@@ -389,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem);  // [kTokens][kBN]
     if (acc_ready) {
 #pragma unroll 1
-      for (int sub = 0; sub < kSub; ++sub) {
+      for (int sub = 0; sub < kSub && 128 * sub < np; ++sub) {
 #pragma unroll
         for (int c = c_lo; c < c_hi; c += 2) {
           uint32_t r0[16], r1[16];
@@ -417,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__syncthreads_and(acc_ready)) {
       const int seg = threadIdx.x & 15;  // 16-byte segment of a token row
       const int n = n0 + 8 * seg;
-      for (int tok = threadIdx.x >> 4; tok < kTokens && m0 + tok < a.m; tok += kThreads / 16) {
+      for (int tok = threadIdx.x >> 4; tok < np; tok += kThreads / 16) {
         const uint4 v = *reinterpret_cast<const uint4 *>(stage + tok * kBN + 8 * seg);
         __nv_bfloat16 *dst = a.y + (int64_t)(m0 + tok) * a.ldy + n;
         if (n + 8 <= a.n) {
@@ -523,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 std::once_flag g_gemm_attr[kMaxDevices];  // cudaFuncSetAttribute acts on the current device
 
-template <int CS, int KS>
+template <int CS, int KS, bool G = false>
 void gemm_allow() {
-  cudaFuncSetAttribute(gemm_kernel<CS, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(gemm_kernel<CS, KS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        GemmSmem::kAlloc);
 }
 
@@ -538,6 +591,7 @@ void gemm_attributes() {
   gemm_allow<2, 2>();
   gemm_allow<2, 3>();
   gemm_allow<2, 4>();
+  gemm_allow<1, 1, true>();
 }
 
 cudaError_t gemm_go(cudaLaunchConfig_t &cfg, int cs, int ks, const CUtensorMap &xmap,
@@ -638,6 +692,7 @@ cudaError_t launch_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void 
   args.k = (int)k;
   args.gamma = gamma;
   args.rinv = rinv;
+  args.slot_expert = args.slot_start = args.meta = nullptr;
   args.err = device_error_word();
 
   // K is split across a cluster (up to 4 ways) when the output tiles cannot
@@ -681,6 +736,55 @@ cudaError_t launch_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void 
     if (e != cudaSuccess) return e;
   }
   return gemm_go(cfg, cs, ks, xmap, wmap, args);
+}
+
+cudaError_t launch_gemm_grouped(const void *w, int64_t expert_stride, int n_experts, int64_t n,
+                                int64_t k, const void *x, int64_t rows, int64_t ldx, void *y,
+                                int64_t ldy, const int *slot_expert, const int *slot_start,
+                                const int *meta, int max_slots, cudaStream_t stream) {
+  std::call_once(g_gemm_attr[device_facts()->device], gemm_attributes);
+  const int nsb = (int)(k / kQK);
+  CUtensorMap xmap, wmap;
+  {
+    const uint64_t dims[2] = {(uint64_t)k, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)ldx * 2};
+    const uint32_t box[2] = {(uint32_t)kBK, 128u};
+    if (encode_tiled(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims,
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // (byte of the super-block, super-block, row, expert)
+    const uint64_t dims[4] = {(uint64_t)kBlockBytes, (uint64_t)nsb, (uint64_t)n,
+                              (uint64_t)n_experts};
+    const uint64_t strides[3] = {(uint64_t)kBlockBytes, (uint64_t)nsb * kBlockBytes,
+                                 (uint64_t)expert_stride};
+    const uint32_t box[4] = {(uint32_t)kBlockBytes, 1u, (uint32_t)kBN, 1u};
+    if (encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(w), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  GemmArgs args = {};
+  args.y = static_cast<__nv_bfloat16 *>(y);
+  args.ldy = ldy;
+  args.m = (int)rows;
+  args.n = (int)n;
+  args.k = (int)k;
+  args.slot_expert = slot_expert;
+  args.slot_start = slot_start;
+  args.meta = meta;
+  args.err = device_error_word();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + kBN - 1) / kBN), (unsigned)max_slots, 1);
+  cfg.blockDim = dim3((unsigned)kThreads, 1, 1);
+  cfg.dynamicSmemBytes = GemmSmem::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<1, 1, true>, xmap, wmap, args);
 }
 
 }  // namespace q4k

@@ -57,6 +57,16 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
                           cudaStream_t stream);
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
+// Grouped expert GEMM (routed-MoE prefill): for each work slot s < meta[0],
+// rows [slot_start[s], slot_start[s+1]) (at most 256) of the expert-sorted X
+// (rows x k bf16, row stride ldx) times the n x k Q4_K matrix of expert
+// slot_expert[s] (at byte slot_expert[s] * expert_stride of w) into the same
+// rows of Y (bf16, row stride ldy).  Grid: n-tiles x max_slots.
+cudaError_t launch_gemm_grouped(const void *w, int64_t expert_stride, int n_experts, int64_t n,
+                                int64_t k, const void *x, int64_t rows, int64_t ldx, void *y,
+                                int64_t ldy, const int *slot_expert, const int *slot_start,
+                                const int *meta, int max_slots, cudaStream_t stream);
+
 // The same with an RMSNorm prologue (gamma non-null): rinv (m floats) is
 // written first, then Y = rinv (X (W diag(gamma))^T).
 cudaError_t launch_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t m,
@@ -73,6 +83,16 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                        const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
                        const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
                        bool weighted_down, cudaStream_t stream);
+
+// Routed-MoE prefill: route, gather, grouped gate/up GEMMs, SiLU, grouped
+// down GEMM, weighted sum (see q4k_moe.cu).
+size_t moe_prefill_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k,
+                                  int64_t hidden, int64_t ffn);
+cudaError_t launch_moe_prefill(const void *w_gate, const void *w_up, const void *w_down,
+                               int64_t expert_stride, int32_t n_experts, int64_t hidden,
+                               int64_t ffn, const void *x, int32_t n_tokens, int64_t ldx,
+                               const int32_t *ids, const float *wts, int32_t top_k, float *y,
+                               int64_t ldy, void *workspace, cudaStream_t stream);
 
 // Workspace of the allocation-free MoE call (bytes of its device array).
 constexpr size_t kMoeScratchBytes = 8u << 20;

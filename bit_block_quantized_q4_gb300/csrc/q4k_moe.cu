@@ -104,6 +104,7 @@ struct MoeArgs {
   int weighted_down;  // route weight applied to h before the down projection
   int *counters;
   int n_counters, max_slots;
+  int slot_pairs;  // pairs per work slot at most (the route kernel's slot size)
   float *g, *u, *h, *p;
   __nv_bfloat16 *h_hi, *h_lo;
   unsigned *err;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
   int s = 0, act = 0;
   for (int e = e0; e < e1; ++e) {
     s += cnt[e];
-    act += (cnt[e] + kSlotPairs - 1) / kSlotPairs;
+    act += (cnt[e] + a.slot_pairs - 1) / a.slot_pairs;
   }
   int incl_s = s, incl_a = act;
   const int lane = tid & 31, wid = tid >> 5;
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
     start[e] = run_s;
     slot_of[e] = run_a;
     run_s += cnt[e];
-    run_a += (cnt[e] + kSlotPairs - 1) / kSlotPairs;
+    run_a += (cnt[e] + a.slot_pairs - 1) / a.slot_pairs;
   }
   if (tid == nt - 1) {
     a.meta[0] = run_a;  // work slots in use
@@ -192,10 +193,10 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeArgs a) {
   }
   __syncthreads();
   for (int e = tid; e < E; e += nt) {
-    for (int q = 0; q * kSlotPairs < cnt[e]; ++q) {
+    for (int q = 0; q * a.slot_pairs < cnt[e]; ++q) {
       a.slot_expert[slot_of[e] + q] = e;
-      a.slot_start[slot_of[e] + q] = start[e] + q * kSlotPairs;
-      a.slot_start[slot_of[e] + q + 1] = min(start[e] + (q + 1) * kSlotPairs, start[e] + cnt[e]);
+      a.slot_start[slot_of[e] + q] = start[e] + q * a.slot_pairs;
+      a.slot_start[slot_of[e] + q + 1] = min(start[e] + (q + 1) * a.slot_pairs, start[e] + cnt[e]);
     }
   }
   for (int q = tid; q < P; q += nt) {
@@ -704,6 +705,7 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
   a.counters = reinterpret_cast<int *>(ws + L.counters);
   a.n_counters = L.n_counters;
   a.max_slots = MoeLayout::max_slots(n_experts, P);
+  a.slot_pairs = kSlotPairs;
   a.slot_expert = reinterpret_cast<int *>(ws + L.slot_expert);
   a.slot_start = reinterpret_cast<int *>(ws + L.slot_start);
   a.pair_token = reinterpret_cast<int *>(ws + L.pair_token);
@@ -745,6 +747,174 @@ cudaError_t launch_moe(const void *w_gate, const void *w_up, const void *w_down,
                         (size_t)kExpertSmem, stream, mg, mu, md, a)
            : launch_pdl(moe_persistent_kernel<1, 2>, dim3((unsigned)grid), kMoeWarps * 32,
                         (size_t)kExpertSmem, stream, mg, mu, md, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace q4k
+
+// ---------------------------------------------------------------------------
+// Routed-MoE prefill (token blocks; "Layer Package Repository Spec", section
+// "Policy Resolution": routed gate/up/down expert matmuls, fused SwiGLU,
+// route-weighted sum).  The expert matmuls are grouped tcgen05 GEMMs over
+// expert-sorted token rows: every active expert's weights are dequantized once
+// per block of up to 256 of its (token, slot) pairs.  Seven launches on the
+// caller's stream, each a programmatic dependent of the one before:
+//   1. route    as for decode, with work slots of up to 256 pairs
+//   2. gather   Xs[pos] = x[token of pair pos]          (bf16 rows, expert-sorted)
+//   3. gate     G = Xs Wg_e^T, slot by slot             (grouped GEMM, bf16 out)
+//   4. up       U = Xs Wu_e^T                           (grouped GEMM, bf16 out)
+//   5. silu     H = bf16(silu(G) U), fp32 arithmetic
+//   6. down     Pd = H Wd_e^T                           (grouped GEMM, bf16 out)
+//   7. combine  y[t] = sum_j w[t, j] Pd[pos(t, j)]      (fp32, slots in order j)
+namespace q4k {
+
+namespace {
+
+constexpr int kPrefillSlot = 256;  // pairs per work slot: the grouped GEMM's token tile
+
+struct PrefillLayout {
+  size_t meta, slot_expert, slot_start, pair_token, pair_q, tj_pair, xs, g, u, h, p, total;
+  int max_slots;
+  PrefillLayout(int E, int P, int64_t H, int64_t F) {
+    auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    max_slots = std::min(E, P) + (P + kPrefillSlot - 1) / kPrefillSlot;
+    const size_t S = (size_t)max_slots;
+    size_t o = 0;
+    meta = o;        o = al(o + 16 * sizeof(int));
+    slot_expert = o; o = al(o + S * sizeof(int));
+    slot_start = o;  o = al(o + (S + 1) * sizeof(int));
+    pair_token = o;  o = al(o + (size_t)P * sizeof(int));
+    pair_q = o;      o = al(o + (size_t)P * sizeof(int));
+    tj_pair = o;     o = al(o + (size_t)P * sizeof(int));
+    xs = o;          o = al(o + (size_t)P * H * 2);
+    g = o;           o = al(o + (size_t)P * F * 2);
+    u = o;           o = al(o + (size_t)P * F * 2);
+    h = o;           o = al(o + (size_t)P * F * 2);
+    p = o;           o = al(o + (size_t)P * H * 2);
+    total = o;
+  }
+};
+
+// One CTA per pair position: copies the pair's token row of x.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const MoeArgs a, __nv_bfloat16 *xs) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int pos = blockIdx.x;
+  if (pos >= a.meta[1]) return;  // pairs with a valid expert id
+  const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)a.pair_token[pos] * a.ldx);
+  uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * a.hidden);
+  for (int i = threadIdx.x; i < a.hidden / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+// H = bf16(silu(G) * U) over the valid pairs' rows, 8 values per thread step.
+__global__ void __launch_bounds__(256) moe_silu_kernel(const int *meta, const __nv_bfloat16 *g,
+                                                       const __nv_bfloat16 *u, __nv_bfloat16 *h,
+                                                       int64_t ffn) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t total = (int64_t)meta[1] * ffn / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 gv = reinterpret_cast<const uint4 *>(g)[i];
+    const uint4 uv = reinterpret_cast<const uint4 *>(u)[i];
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t hw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g0 = __uint_as_float(gw[e] << 16), g1 = __uint_as_float(gw[e] & 0xFFFF0000u);
+      const float u0 = __uint_as_float(uw[e] << 16), u1 = __uint_as_float(uw[e] & 0xFFFF0000u);
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(g0 / (1.f + __expf(-g0)) * u0,
+                                                      g1 / (1.f + __expf(-g1)) * u1);
+      hw[e] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+    reinterpret_cast<uint4 *>(h)[i] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+}
+
+// y[t, i] = sum_j w[t, j] Pd[pos(t, j), i] in slot order j (skipped ids add nothing).
+__global__ void __launch_bounds__(256) moe_prefill_combine_kernel(const MoeArgs a,
+                                                                  const __nv_bfloat16 *pd) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int t = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.hidden) return;
+  float acc = 0.f;
+  for (int j = 0; j < a.top_k; ++j) {
+    const int q = t * a.top_k + j;
+    const int pos = a.tj_pair[q];
+    if (pos < 0) continue;
+    acc = fmaf(a.wts[q], __bfloat162float(pd[(size_t)pos * a.hidden + i]), acc);
+  }
+  a.y[(int64_t)t * a.ldy + i] = acc;
+}
+
+}  // namespace
+
+size_t moe_prefill_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k,
+                                  int64_t hidden, int64_t ffn) {
+  return PrefillLayout(n_experts, n_tokens * top_k, hidden, ffn).total;
+}
+
+cudaError_t launch_moe_prefill(const void *w_gate, const void *w_up, const void *w_down,
+                               int64_t expert_stride, int32_t n_experts, int64_t hidden,
+                               int64_t ffn, const void *x, int32_t n_tokens, int64_t ldx,
+                               const int32_t *ids, const float *wts, int32_t top_k, float *y,
+                               int64_t ldy, void *workspace, cudaStream_t stream) {
+  if (n_experts > kMaxExperts) return cudaErrorInvalidValue;
+  const int P = n_tokens * top_k;
+  const PrefillLayout L(n_experts, P, hidden, ffn);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  MoeArgs a = {};
+  a.x = static_cast<const __nv_bfloat16 *>(x);
+  a.ldx = ldx;
+  a.ids = ids;
+  a.wts = wts;
+  a.y = y;
+  a.ldy = ldy;
+  a.n_experts = n_experts;
+  a.n_tokens = n_tokens;
+  a.top_k = top_k;
+  a.hidden = (int)hidden;
+  a.ffn = (int)ffn;
+  a.meta = reinterpret_cast<int *>(ws + L.meta);
+  a.slot_expert = reinterpret_cast<int *>(ws + L.slot_expert);
+  a.slot_start = reinterpret_cast<int *>(ws + L.slot_start);
+  a.pair_token = reinterpret_cast<int *>(ws + L.pair_token);
+  a.pair_q = reinterpret_cast<int *>(ws + L.pair_q);
+  a.tj_pair = reinterpret_cast<int *>(ws + L.tj_pair);
+  a.counters = nullptr;
+  a.n_counters = 0;
+  a.max_slots = L.max_slots;
+  a.slot_pairs = kPrefillSlot;
+  a.err = device_error_word();
+  auto *xs = reinterpret_cast<__nv_bfloat16 *>(ws + L.xs);
+  auto *g = reinterpret_cast<__nv_bfloat16 *>(ws + L.g);
+  auto *u = reinterpret_cast<__nv_bfloat16 *>(ws + L.u);
+  auto *h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+  auto *pd = reinterpret_cast<__nv_bfloat16 *>(ws + L.p);
+  const DeviceFacts *f = device_facts();
+
+  cudaError_t e = launch_pdl(moe_route_kernel, dim3(1), 1024, 0, stream, a);
+  if (e == cudaSuccess) e = launch_pdl(moe_gather_kernel, dim3((unsigned)P), 256, 0, stream, a, xs);
+  if (e == cudaSuccess)
+    e = launch_gemm_grouped(w_gate, expert_stride, n_experts, ffn, hidden, xs, P, hidden, g, ffn,
+                            a.slot_expert, a.slot_start, a.meta, L.max_slots, stream);
+  if (e == cudaSuccess)
+    e = launch_gemm_grouped(w_up, expert_stride, n_experts, ffn, hidden, xs, P, hidden, u, ffn,
+                            a.slot_expert, a.slot_start, a.meta, L.max_slots, stream);
+  if (e == cudaSuccess)
+    e = launch_pdl(moe_silu_kernel, dim3((unsigned)(8 * f->sm_count)), 256, 0, stream,
+                   (const int *)a.meta, (const __nv_bfloat16 *)g, (const __nv_bfloat16 *)u, h,
+                   ffn);
+  if (e == cudaSuccess)
+    e = launch_gemm_grouped(w_down, expert_stride, n_experts, hidden, ffn, h, P, ffn, pd, hidden,
+                            a.slot_expert, a.slot_start, a.meta, L.max_slots, stream);
+  if (e == cudaSuccess)
+    e = launch_pdl(moe_prefill_combine_kernel,
+                   dim3((unsigned)((hidden + 255) / 256), (unsigned)n_tokens), 256, 0, stream, a,
+                   (const __nv_bfloat16 *)pd);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -315,6 +315,35 @@ int q4k_moe_gemv_ex(const void *w_gate, const void *w_up, const void *w_down,
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4k_moe_prefill -- routed mixture-of-experts FFN for a block of tokens
+ * (prefill), the expert matmuls as grouped tensor-core GEMMs.
+ * ("Layer Package Repository Spec", section "Policy Resolution": routed
+ *  gate/up/down expert matmuls (the MUL_MAT_ID path), fused SwiGLU,
+ *  route-weighted sum.)
+ * The same result as q4k_moe_gemv for any number of tokens: the (token, slot)
+ * pairs are sorted by expert into work slots of at most 256 pairs, and each
+ * active expert's weights are dequantized to bf16 once per slot and multiplied
+ * on the tensor cores (tcgen05, fp32 accumulation) with all of the slot's
+ * token rows.  Intermediates in bf16: g = Wg_e x and u = Wu_e x (rounded once
+ * from fp32), h = silu(g) * u (computed in fp32), p = Wd_e h; Y in fp32.
+ * Accuracy: each GEMM stage within 1e-2 * sum |w||x| of its exact result on
+ * its own inputs, propagated through SiLU and the weighted sum.
+ *   arguments as q4k_moe_gemv, except n_tokens 1..65535 (with
+ *   n_tokens * top_k * max(hidden, ffn) <= 2^31) and the workspace:
+ *   workspace   device, >= q4k_moe_prefill_workspace_size(...) bytes, 16-byte
+ *               aligned (it holds the sorted token rows and the intermediates)
+ * Seven launches on `stream`, each a programmatic dependent of the one before.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, DEVICE, MEMORY, CUDA.
+ */
+size_t q4k_moe_prefill_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k,
+                                      int64_t hidden, int64_t ffn);
+int q4k_moe_prefill(const void *w_gate, const void *w_up, const void *w_down,
+                    int64_t expert_stride, int32_t n_experts, int64_t hidden, int64_t ffn,
+                    const void *x, int32_t n_tokens, int64_t ldx, const int32_t *ids,
+                    const float *wts, int32_t top_k, float *y, int64_t ldy, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
  * q4k_moe_gemv_noalloc -- q4k_moe_gemv without a caller-provided workspace.
  * (The pages have no counterpart of this call; it is a convenience of this
  *  library.)  For callers that cannot allocate device memory per call: engines

@@ -214,6 +214,31 @@ def test_gemm_rmsnorm_argument_errors(L):
     assert call(x=P + 8) == 3
 
 
+def test_moe_prefill_argument_errors(L):
+    E, H, F, T, K = 8, 256, 512, 40, 2
+    stride = F * H // 256 * 144
+    ws = L.q4k_moe_prefill_workspace_size(E, T, K, H, F)
+    P_ = T * K   # sorted token rows and down outputs (P x H bf16), g, u, h (P x F bf16)
+    assert ws >= 2 * P_ * H * 2 + 3 * P_ * F * 2
+
+    def call(**kw):
+        a = dict(wg=P, wu=P, wd=P, stride=stride, E=E, H=H, F=F, x=P, T=T, ldx=H, ids=P, wts=P,
+                 k=K, y=P, ldy=H, ws=P, wsb=ws, stream=None)
+        a.update(kw)
+        return L.q4k_moe_prefill(*a.values())
+
+    assert call(H=300) == 2
+    assert call(T=70000) == 2
+    assert call(k=17) == 2
+    assert call(E=0) == 2
+    assert call(T=0) == 0
+    assert call(ids=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsb=ws - 1) == 4
+    assert call(stride=stride + 8) == 3
+    assert call(x=P + 2) == 3
+
+
 def test_get_device_error_rejects_null(L):
     assert L.q4k_get_device_error(None, None) == 1
 
@@ -256,6 +281,8 @@ int main(void) {
   st |= q4k_moe_gemv_ex(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256,
                         Q4K_MOE_WEIGHTED_DOWN, 0, 0, 0);
   st |= q4k_moe_gemv_noalloc(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0);
+  st |= (int)q4k_moe_prefill_workspace_size(8, 40, 2, 256, 256);
+  st |= q4k_moe_prefill(0, 0, 0, 0, 8, 256, 256, 0, 40, 256, 0, 0, 2, 0, 256, 0, 0, 0);
   st |= q4k_get_device_error(0, &bits);
   st |= q4k_selftest_wait_timeout(0);
   st |= (int)sizeof(q4k_gemv_op) == 64 ? 0 : 1 << 20;
