@@ -71,6 +71,11 @@ def _load():
         lib.oracle_moe.argtypes = [P, P, P, I64, I32, I64, I64, P, I32, I64, P, P, I32,
                                    P, P, P, P, ctypes.c_int]
         lib.oracle_rmsnorm_gemv.argtypes = [P, I64, I64, P, I64, I64, P, ctypes.c_float, P, P, P]
+        lib.oracle_kq_block_bytes.restype = ctypes.c_int
+        lib.oracle_kq_block_bytes.argtypes = [ctypes.c_int]
+        for fn in ("oracle_kq_dequant_f64", "oracle_kq_dequant_f32", "oracle_kq_dequant_bf16"):
+            getattr(lib, fn).argtypes = [ctypes.c_int, P, I64, I64, P]
+        lib.oracle_kq_gemv_bf16.argtypes = [ctypes.c_int, P, I64, I64, P, I64, I64, P, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -227,6 +232,64 @@ def rmsnorm_gemv(w, n: int, k: int, x_bf16, gamma, eps: float):
         _load().oracle_rmsnorm_gemv(_ptr(a), n, k, _ptr(x), batch, k, _ptr(g), float(eps), _ptr(y),
                                     _ptr(s), _ptr(rinv))
     return y, s, rinv
+
+
+# ---------------------------------------------------------------- other k-quants
+# format ids: 2 q2_K, 3 q3_K, 4 Q4_K, 5 Q5_K, 6 Q6_K (oracle_kq_*)
+KQ_FORMATS = {"q2_K": 2, "q3_K": 3, "Q4_K": 4, "Q5_K": 5, "Q6_K": 6}
+
+
+def kq_block_bytes(fmt: int) -> int:
+    return int(_load().oracle_kq_block_bytes(int(fmt)))
+
+
+def _check_kq(fmt: int, w, n: int, k: int) -> np.ndarray:
+    if k % 256:
+        raise ValueError("k must be a multiple of 256")
+    bb = kq_block_bytes(fmt)
+    if bb == 0:
+        raise ValueError("unknown format")
+    a = _u8(w)
+    if a.size != n * (k // 256) * bb:
+        raise ValueError("weight byte count does not match n x k")
+    return a
+
+
+def kq_dequant_f64(fmt: int, w, n: int, k: int) -> np.ndarray:
+    """Exact weights (fp64) [n, k] of format fmt (oracle_kq_dequant_f64)."""
+    a = _check_kq(fmt, w, n, k)
+    out = np.empty((n, k), np.float64)
+    _load().oracle_kq_dequant_f64(int(fmt), _ptr(a), n, k, _ptr(out))
+    return out
+
+
+def kq_dequant_f32(fmt: int, w, n: int, k: int) -> np.ndarray:
+    """Weights rounded once to fp32 (oracle_kq_dequant_f32)."""
+    a = _check_kq(fmt, w, n, k)
+    out = np.empty((n, k), np.float32)
+    _load().oracle_kq_dequant_f32(int(fmt), _ptr(a), n, k, _ptr(out))
+    return out
+
+
+def kq_dequant_bf16(fmt: int, w, n: int, k: int) -> np.ndarray:
+    """Weights as bf16 bits: fp32, then RNE to bf16 (oracle_kq_dequant_bf16)."""
+    a = _check_kq(fmt, w, n, k)
+    out = np.empty((n, k), np.uint16)
+    _load().oracle_kq_dequant_bf16(int(fmt), _ptr(a), n, k, _ptr(out))
+    return out
+
+
+def kq_gemv(fmt: int, w, n: int, k: int, x_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """(y, s) = (W x, |W| |x|) in fp64 for bf16 activations [batch, k] (oracle_kq_gemv_bf16)."""
+    a = _check_kq(fmt, w, n, k)
+    x = np.ascontiguousarray(np.atleast_2d(np.asarray(x_bf16, dtype=np.uint16)))
+    assert x.shape[1] == k
+    batch = x.shape[0]
+    y = np.empty((batch, n), np.float64)
+    s = np.empty((batch, n), np.float64)
+    if n and batch:
+        _load().oracle_kq_gemv_bf16(int(fmt), _ptr(a), n, k, _ptr(x), batch, k, _ptr(y), _ptr(s))
+    return y, s
 
 
 def moe(w_gate, w_up, w_down, expert_stride: int, n_experts: int, hidden: int, ffn: int,

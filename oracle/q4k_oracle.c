@@ -372,6 +372,173 @@ void oracle_rmsnorm_gemv(const uint8_t *w, int64_t n, int64_t k, const uint16_t 
     free(axh);
 }
 
+/*
+ * Other k-quant formats ("Layer Package Repository Spec", section "Policy
+ * Resolution": the q2_K / q3_K routed-down recipes; "UD-Q4_K_XL" mixes also
+ * carry Q5_K and Q6_K tensors).  The pages name these formats and print none of
+ * their bytes; the layouts below are the plain reading of the GGUF k-quant
+ * super-blocks (256 weights each), restated here.  Compatibility with real
+ * GGUF files is parity unpinned; the tests pin each layout against an
+ * independent packer, Q5_K against Q4_K, and the weight positions by probes.
+ * Every weight is exact in fp64 (at most 11 + 8 + 6 significant bits).
+ *
+ * q2_K, 84 bytes:  sc[16] | qs[64] | d (binary16) | dmin (binary16)
+ *   16 sub-blocks of 16 weights; byte sc[j]: scale = low nibble, min = high
+ *   nibble.  Weight i: half h = i/128, r = i%128, group g = r/32, l = r%32:
+ *   q = (qs[32h + l] >> 2g) & 3, sub-block j = 8h + 2g + (l >= 16);
+ *   w = d * scale_j * q - dmin * min_j.
+ * q3_K, 110 bytes: hmask[32] | qs[64] | s[12] | d (binary16)
+ *   16 six-bit scales: low 4 bits of scale j are the low nibble of s[j]
+ *   (j < 8) or the high nibble of s[j-8] (j >= 8); its top 2 bits are bits
+ *   2(j/4), 2(j/4)+1 of s[8 + j%4].  Weight i (h, g, l, j as for q2_K):
+ *   q = ((qs[32h + l] >> 2g) & 3) - (bit (4h + g) of hmask[l] ? 0 : 4),
+ *   w = d * (scale_j - 32) * q.
+ * Q5_K, 176 bytes: d | dmin | s[12] (as Q4_K) | qh[32] | qs[128]
+ *   as Q4_K with a fifth bit: weight i in chunk c = i/64, l = i%32, high
+ *   half (i%64 >= 32) or low: q = nibble of qs[32c + l] + 16 * bit (2c + high)
+ *   of qh[l];  w = d * sc_j * q - dmin * m_j, j = i/32.
+ * Q6_K, 210 bytes: ql[128] | qh[64] | sc[16] (int8) | d (binary16)
+ *   weight i: half h = i/128, r = i%128, quarter u = r/32, l = r%32:
+ *   low 4 bits: ql[64h + l + 32(u & 1)], low nibble for u < 2, high for u >= 2;
+ *   high 2 bits: bits 2u, 2u+1 of qh[32h + l];  q = that 6-bit value - 32;
+ *   w = d * sc[8h + 2u + l/16] * q.
+ */
+int oracle_kq_block_bytes(int fmt) {
+    switch (fmt) {
+        case 2: return 84;
+        case 3: return 110;
+        case 4: return Q4K_BYTES;
+        case 5: return 176;
+        case 6: return 210;
+        default: return 0;
+    }
+}
+
+static double half_at(const uint8_t *p) {
+    return oracle_fp16_to_f64((uint16_t)(p[0] | (p[1] << 8)));
+}
+
+static void dequant_q2k_block(const uint8_t *b, double out[256]) {
+    const uint8_t *sc = b, *qs = b + 16;
+    double d = half_at(b + 80), dmin = half_at(b + 82);
+    for (int i = 0; i < 256; ++i) {
+        int h = i / 128, r = i % 128, g = r / 32, l = r % 32;
+        int q = (qs[32 * h + l] >> (2 * g)) & 3;
+        int j = 8 * h + 2 * g + (l >= 16);
+        out[i] = d * (sc[j] & 15) * q - dmin * (sc[j] >> 4);
+    }
+}
+
+static int q3k_scale(const uint8_t s[12], int j) {
+    int lo = j < 8 ? (s[j] & 15) : (s[j - 8] >> 4);
+    int hi = (s[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return lo | (hi << 4);
+}
+
+static void dequant_q3k_block(const uint8_t *b, double out[256]) {
+    const uint8_t *hm = b, *qs = b + 32, *s = b + 96;
+    double d = half_at(b + 108);
+    for (int i = 0; i < 256; ++i) {
+        int h = i / 128, r = i % 128, g = r / 32, l = r % 32;
+        int q = ((qs[32 * h + l] >> (2 * g)) & 3) - (((hm[l] >> (4 * h + g)) & 1) ? 0 : 4);
+        int j = 8 * h + 2 * g + (l >= 16);
+        out[i] = d * (q3k_scale(s, j) - 32) * q;
+    }
+}
+
+static void dequant_q5k_block(const uint8_t *b, double out[256]) {
+    double d = half_at(b), dmin = half_at(b + 2);
+    int sc[8], m[8];
+    oracle_unpack_scales(b + 4, sc, m);
+    const uint8_t *qh = b + 16, *qs = b + 48;
+    for (int i = 0; i < 256; ++i) {
+        int c = i / 64, l = i % 32, high = (i % 64) >= 32;
+        int nib = high ? (qs[32 * c + l] >> 4) : (qs[32 * c + l] & 15);
+        int q = nib + 16 * ((qh[l] >> (2 * c + high)) & 1);
+        out[i] = d * sc[i / 32] * q - dmin * m[i / 32];
+    }
+}
+
+static void dequant_q6k_block(const uint8_t *b, double out[256]) {
+    const uint8_t *ql = b, *qh = b + 128;
+    const int8_t *sc = (const int8_t *)(b + 192);
+    double d = half_at(b + 208);
+    for (int i = 0; i < 256; ++i) {
+        int h = i / 128, r = i % 128, u = r / 32, l = r % 32;
+        uint8_t lb = ql[64 * h + l + 32 * (u & 1)];
+        int lo = u < 2 ? (lb & 15) : (lb >> 4);
+        int hi = (qh[32 * h + l] >> (2 * u)) & 3;
+        int q = (lo | (hi << 4)) - 32;
+        out[i] = d * sc[8 * h + 2 * u + l / 16] * q;
+    }
+}
+
+/* One super-block of format fmt -> its 256 weights, exact, in fp64. */
+void oracle_kq_dequant_block_f64(int fmt, const uint8_t *blk, double out[256]) {
+    switch (fmt) {
+        case 2: dequant_q2k_block(blk, out); break;
+        case 3: dequant_q3k_block(blk, out); break;
+        case 4: oracle_dequant_block_f64(blk, out); break;
+        case 5: dequant_q5k_block(blk, out); break;
+        case 6: dequant_q6k_block(blk, out); break;
+        default: memset(out, 0, sizeof(double) * 256);
+    }
+}
+
+static void kq_row_f64(int fmt, const uint8_t *w, int64_t k, int64_t r, double *out) {
+    int bb = oracle_kq_block_bytes(fmt);
+    const uint8_t *row = w + (size_t)r * (size_t)(k / 256) * (size_t)bb;
+    for (int64_t b = 0; b < k / 256; ++b) oracle_kq_dequant_block_f64(fmt, row + b * bb, out + b * 256);
+}
+
+void oracle_kq_dequant_f64(int fmt, const uint8_t *w, int64_t n, int64_t k, double *out) {
+    for (int64_t r = 0; r < n; ++r) kq_row_f64(fmt, w, k, r, out + r * k);
+}
+
+/* fp32: one round-to-nearest-even of the exact value; bf16: that, then RNE. */
+void oracle_kq_dequant_f32(int fmt, const uint8_t *w, int64_t n, int64_t k, float *out) {
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)k);
+    for (int64_t r = 0; r < n; ++r) {
+        kq_row_f64(fmt, w, k, r, tmp);
+        for (int64_t i = 0; i < k; ++i) out[r * k + i] = (float)tmp[i];
+    }
+    free(tmp);
+}
+
+void oracle_kq_dequant_bf16(int fmt, const uint8_t *w, int64_t n, int64_t k, uint16_t *out) {
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)k);
+    for (int64_t r = 0; r < n; ++r) {
+        kq_row_f64(fmt, w, k, r, tmp);
+        for (int64_t i = 0; i < k; ++i) out[r * k + i] = oracle_f32_to_bf16_rne((float)tmp[i]);
+    }
+    free(tmp);
+}
+
+/* y = W x and s = |W| |x| (fp64, natural k order) for bf16 activations
+ * [batch x k], row stride ldx; y and s are [batch x n]. */
+void oracle_kq_gemv_bf16(int fmt, const uint8_t *w, int64_t n, int64_t k, const uint16_t *x,
+                         int64_t batch, int64_t ldx, double *y, double *s) {
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(batch * k));
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t i = 0; i < k; ++i) xd[b * k + i] = oracle_bf16_to_f64(x[b * ldx + i]);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n; ++r) {
+        double *wr = (double *)malloc(sizeof(double) * (size_t)k);
+        kq_row_f64(fmt, w, k, r, wr);
+        for (int64_t b = 0; b < batch; ++b) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < k; ++i) {
+                acc += wr[i] * xd[b * k + i];
+                mag += fabs(wr[i]) * fabs(xd[b * k + i]);
+            }
+            y[b * n + r] = acc;
+            if (s) s[b * n + r] = mag;
+        }
+        free(wr);
+    }
+    free(xd);
+}
+
 /* Threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
