@@ -583,6 +583,34 @@ def bench_moe_prefill(q4k, dev, stream, reps=10):
             "pairs": T * K}
 
 
+def bench_kquant(q4k, dev, stream, reps=10):
+    """Batch-1 decode projection in the other k-quant formats on the 27B-class
+    down shape (5120 x 17408): a pool of 8 matrices per format (more than L2
+    for every format) multiplied in turn; bytes = weights + x + y."""
+    n, k, pool = 5120, 17408, 8
+    out = {}
+    names = {2: "q2_K", 3: "q3_K", 5: "Q5_K", 6: "Q6_K"}
+    for fmt, name in names.items():
+        ws = [synth.kq_weight(fmt, n, k, seed=synth.derive_seed(1008, name, i), device=dev)
+              for i in range(pool)]
+        x = synth.bf16_normal((1, k), seed=synth.derive_seed(1008, "x"), device=dev)
+        y = torch.empty((1, n), dtype=torch.float32, device=dev)
+
+        def step():
+            for w in ws:
+                q4k.q4k_kq_gemv(fmt, w, n, k, x, out=y, stream=stream)
+
+        ms, per, g = time_graph(step, reps, 3, stream)
+        del g
+        nbytes = pool * (ws[0].numel() + 2 * k + 4 * n)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us_per_gemv": round(ms * 1e3 / pool, 2), "gbs": round(gbs, 1),
+                     "bytes_per_weight": round(ws[0].numel() / (n * k), 4)}
+        del ws
+        torch.cuda.empty_cache()
+    return out
+
+
 KERNEL_SOURCES = ("q4k_stream.cu", "q4k_device.cuh", "q4k_internal.h")
 
 
@@ -846,6 +874,12 @@ def main():
             torch.cuda.empty_cache()
         with nvtx("moe 235b t16"):
             extra["moe_235b_a22b_t16"] = bench_moe(q4k, dev, stream)
+        torch.cuda.empty_cache()
+        with nvtx("k-quant gemv"):
+            kq = bench_kquant(q4k, dev, stream)
+        for v in kq.values():
+            v["frac_of_measured_hbm"] = round(v["gbs"] / pk["hbm_gbs"], 4)
+        extra["kquant_gemv_b1_down_5120x17408"] = kq
         torch.cuda.empty_cache()
         if world == 1:
             with nvtx("moe prefill 235b t512"):

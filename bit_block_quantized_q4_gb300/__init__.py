@@ -27,6 +27,7 @@ Q4K_FLAG_OVERLAP_WEIGHTS = 1
 Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm", "q4k_gemm_rmsnorm",
+           "q4k_kq_block_bytes", "q4k_kq_dequant", "q4k_kq_gemv",
            "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
            "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc", "q4k_moe_prefill",
            "q4k_moe_prefill_workspace_size",
@@ -76,6 +77,12 @@ def lib() -> ctypes.CDLL:
         L.q4k_gemv_seq.argtypes = [ctypes.POINTER(GemvOp), I64, I64, ctypes.c_uint32, P]
         L.q4k_gemm.restype = ctypes.c_int
         L.q4k_gemm.argtypes = [P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_kq_block_bytes.restype = ctypes.c_int
+        L.q4k_kq_block_bytes.argtypes = [I32]
+        L.q4k_kq_dequant.restype = ctypes.c_int
+        L.q4k_kq_dequant.argtypes = [I32, P, I64, I64, P, ctypes.c_int, P]
+        L.q4k_kq_gemv.restype = ctypes.c_int
+        L.q4k_kq_gemv.argtypes = [I32, P, I64, I64, P, I64, I64, P, I64, P]
         L.q4k_gemm_rmsnorm.restype = ctypes.c_int
         L.q4k_gemm_rmsnorm.argtypes = [P, I64, I64, P, I64, I64, P, ctypes.c_float, P, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
@@ -204,6 +211,32 @@ def q4k_gemm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=
         out = torch.empty((m, ld), dtype=torch.bfloat16, device=x.device)[:, :n]
     _check(lib().q4k_gemm(_ptr(w), n, k, _ptr(x), m, x.stride(0), _ptr(out), out.stride(0),
                           _stream(stream)), "q4k_gemm")
+    return out
+
+
+Q4K_FMT_Q2_K, Q4K_FMT_Q3_K, Q4K_FMT_Q4_K, Q4K_FMT_Q5_K, Q4K_FMT_Q6_K = 2, 3, 4, 5, 6
+
+
+def q4k_kq_block_bytes(fmt: int) -> int:
+    return int(lib().q4k_kq_block_bytes(fmt))
+
+
+def q4k_kq_dequant(fmt: int, w: torch.Tensor, n: int, k: int, dtype=torch.float32, stream=None):
+    """Dense weights of an n x k matrix of k-quant format fmt (fp32 or bf16)."""
+    out = torch.empty((n, k), dtype=dtype, device=w.device)
+    _check(lib().q4k_kq_dequant(fmt, _ptr(w), n, k, _ptr(out), 1 if dtype == torch.bfloat16 else 0,
+                                _stream(stream)), "q4k_kq_dequant")
+    return out
+
+
+def q4k_kq_gemv(fmt: int, w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=None, stream=None):
+    """Y = X W^T for x [batch, k] bf16 and a k-quant matrix of format fmt; fp32 [batch, n]."""
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    batch = x2.shape[0]
+    if out is None:
+        out = torch.empty((batch, n), dtype=torch.float32, device=x.device)
+    _check(lib().q4k_kq_gemv(fmt, _ptr(w), n, k, _ptr(x2), batch, x2.stride(0), _ptr(out),
+                             out.stride(0), _stream(stream)), "q4k_kq_gemv")
     return out
 
 

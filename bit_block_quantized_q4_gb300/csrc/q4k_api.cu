@@ -317,6 +317,44 @@ int q4k_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int q4k_kq_block_bytes(int32_t format) {
+  return format == 4 ? kBlockBytes : kq_block_bytes(format);
+}
+
+int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *out, int out_dtype,
+                   void *stream) {
+  if (format == 4) return q4k_dequant(w, n, k, out, out_dtype, stream);
+  if (kq_block_bytes(format) == 0) return Q4K_ERR_SHAPE;
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || (out_dtype != 0 && out_dtype != 1)) return Q4K_ERR_SHAPE;
+  if (n == 0) return Q4K_OK;
+  if (!w || !out) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(out, 16)) return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w, out});
+  if (st != Q4K_OK) return st;
+  return map_launch(
+      launch_kq_dequant(format, w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+                int64_t ldx, float *y, int64_t ldy, void *stream) {
+  if (format == 4) return q4k_gemv(w, n, k, x, batch, ldx, y, ldy, stream);
+  if (kq_block_bytes(format) == 0) return Q4K_ERR_SHAPE;
+  if (n < 0 || k <= 0 || (k % kQK) != 0 || batch < 0 || batch > 16) return Q4K_ERR_SHAPE;
+  if (n > INT32_MAX / 2 || kq_gemv_smem(format, k) > 227 * 1024) return Q4K_ERR_SHAPE;
+  if (n == 0 || batch == 0) return Q4K_OK;
+  if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
+  if (!w || !x || !y) return Q4K_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(x, 16) || (ldx % 8) != 0 || !aligned(y, 4)) return Q4K_ERR_ALIGN;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  st = check_device_memory({w, x, y});
+  if (st != Q4K_OK) return st;
+  return map_launch(launch_kq_gemv(format, w, n, k, x, batch, ldx, y, ldy,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,
                               int64_t ffn) {
   if (n_experts <= 0 || n_tokens < 0 || top_k <= 0 || hidden <= 0 || ffn <= 0) return 0;

@@ -94,6 +94,14 @@ cudaError_t launch_moe_prefill(const void *w_gate, const void *w_up, const void 
                                const int32_t *ids, const float *wts, int32_t top_k, float *y,
                                int64_t ldy, void *workspace, cudaStream_t stream);
 
+// Other k-quant formats (2 q2_K, 3 q3_K, 5 Q5_K, 6 Q6_K; q4k_kquant.cu).
+int kq_block_bytes(int format);  // 0 for an unknown format
+size_t kq_gemv_smem(int format, int64_t k);
+cudaError_t launch_kq_dequant(int format, const void *w, int64_t n, int64_t k, void *out,
+                              int out_dtype, cudaStream_t stream);
+cudaError_t launch_kq_gemv(int format, const void *w, int64_t n, int64_t k, const void *x,
+                           int64_t batch, int64_t ldx, float *y, int64_t ldy, cudaStream_t stream);
+
 // Workspace of the allocation-free MoE call (bytes of its device array).
 constexpr size_t kMoeScratchBytes = 8u << 20;
 

@@ -242,6 +242,52 @@ int q4k_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t
                      void *stream);
 
 /*
+ * Other k-quant formats ("Layer Package Repository Spec", section "Policy
+ * Resolution": q2_K / q3_K routed-down recipes; Q5_K / Q6_K tensors of "_XL"
+ * mixes).  The pages name the formats; the layouts are the GGUF k-quant
+ * super-blocks of 256 weights (all little-endian, binary16 scales):
+ *   Q4K_FMT_Q2_K  84 bytes: 16 scale bytes (scale | min << 4) of 16-weight
+ *                 sub-blocks, 64 bytes of 2-bit quants, d, dmin;
+ *                 w = d * scale * q - dmin * min.
+ *   Q4K_FMT_Q3_K 110 bytes: 32 high-bit mask bytes, 64 bytes of 2-bit quants,
+ *                 12 bytes of sixteen 6-bit scales, d;
+ *                 w = d * (scale - 32) * (2 bits - (mask bit ? 0 : 4)).
+ *   Q4K_FMT_Q4_K 144 bytes: the Q4_K of every other call in this header.
+ *   Q4K_FMT_Q5_K 176 bytes: d, dmin, the Q4_K scale bytes, 32 fifth-bit bytes,
+ *                 128 nibble bytes; w = d * sc * (nibble + 16 bit) - dmin * m.
+ *   Q4K_FMT_Q6_K 210 bytes: 128 low-nibble bytes, 64 bytes of 2-bit high
+ *                 parts, 16 int8 scales of 16-weight sub-blocks, d;
+ *                 w = d * scale * (6-bit value - 32).
+ * Dequantized weights are the exact value rounded once to fp32 (bit-exact);
+ * GEMV results satisfy |y - y_ref| <= 2e-3 * sum_k |w_k||x_k| (fp32 products
+ * of the rounded weights with x, fp32 accumulation).
+ */
+#define Q4K_FMT_Q2_K 2
+#define Q4K_FMT_Q3_K 3
+#define Q4K_FMT_Q4_K 4
+#define Q4K_FMT_Q5_K 5
+#define Q4K_FMT_Q6_K 6
+/* Bytes per 256-weight super-block of a format (0: not a format). */
+int q4k_kq_block_bytes(int32_t format);
+/*
+ * q4k_kq_dequant -- q4k_dequant for any of the formats (rows of K/256
+ * super-blocks of the format; format 4 is q4k_dequant itself).
+ * Errors: as q4k_dequant, and SHAPE for an unknown format.
+ */
+int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *out, int out_dtype,
+                   void *stream);
+/*
+ * q4k_kq_gemv -- q4k_gemv for any of the formats: Y[b, :] = W X[b, :],
+ * batch 1..16, arguments and layouts as q4k_gemv (format 4 is q4k_gemv
+ * itself).  Each weight row is read once for all batch rows.  K is limited so
+ * that 8 rows fit in shared memory (K/256 * block bytes <= 29 KB; e.g.
+ * K <= 36096 for Q6_K).
+ * Errors: as q4k_gemv, and SHAPE for an unknown format or too long a row.
+ */
+int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+                int64_t ldx, float *y, int64_t ldy, void *stream);
+
+/*
  * q4k_moe_workspace_size -- bytes of device workspace q4k_moe_gemv needs.
  */
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

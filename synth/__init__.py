@@ -72,6 +72,35 @@ def q4k_weight(n: int, k: int, seed: int, quants: str = "uniform", device="cpu",
     return out.view(n, (k // Q4K_VALUES) * Q4K_BYTES)
 
 
+# Other k-quant super-blocks: bytes per block and the byte offsets of their
+# binary16 scale fields (every other byte of a block is a valid field value).
+KQ_LAYOUT = {2: (84, (80, 82)), 3: (110, (108,)), 4: (144, (0, 2)), 5: (176, (0, 2)),
+             6: (210, (208,))}
+
+
+def kq_weight(fmt: int, n: int, k: int, seed: int, device="cpu", d_range=(1e-3, 2e-2),
+              chunk_blocks: int = 1 << 20) -> torch.Tensor:
+    """An n x k matrix of k-quant format id fmt (2 q2_K, 3 q3_K, 4 Q4_K, 5 Q5_K,
+    6 Q6_K) as uint8 [n, k/256 * block bytes]: uniform random bytes, with each
+    binary16 scale field drawn uniformly in d_range."""
+    if k % Q4K_VALUES:
+        raise ValueError("k must be a multiple of 256")
+    bb, halves = KQ_LAYOUT[fmt]
+    nsb = n * (k // Q4K_VALUES)
+    out = torch.empty((nsb, bb), dtype=torch.uint8, device=device)
+    g = _gen(seed, device)
+    lo, hi = d_range
+    for start in range(0, nsb, chunk_blocks):
+        cnt = min(chunk_blocks, nsb - start)
+        blk = out[start:start + cnt]
+        blk[:] = torch.randint(0, 256, (cnt, bb), generator=g, dtype=torch.uint8, device=device)
+        for off in halves:
+            dd = torch.rand((cnt, 1), generator=g, dtype=torch.float64, device=device)
+            dd = (lo + (hi - lo) * dd).to(torch.float16)
+            blk[:, off:off + 2] = dd.contiguous().view(torch.uint8).view(cnt, 2)
+    return out.view(n, (k // Q4K_VALUES) * bb)
+
+
 def bf16_normal(shape, seed: int, sigma: float = 1.0, device="cpu") -> torch.Tensor:
     """bf16 activations: fp32 N(0, sigma) draws rounded to nearest-even bf16."""
     g = _gen(seed, device)

@@ -239,6 +239,30 @@ def test_moe_prefill_argument_errors(L):
     assert call(x=P + 2) == 3
 
 
+def test_kq_argument_errors(L):
+    assert [L.q4k_kq_block_bytes(f) for f in (2, 3, 4, 5, 6)] == [84, 110, 144, 176, 210]
+    assert L.q4k_kq_block_bytes(1) == 0 and L.q4k_kq_block_bytes(7) == 0
+    assert L.q4k_kq_dequant(1, P, 4, 256, P, 0, None) == 2
+    assert L.q4k_kq_dequant(2, P, 4, 300, P, 0, None) == 2
+    assert L.q4k_kq_dequant(2, P, 4, 256, P, 2, None) == 2
+    assert L.q4k_kq_dequant(3, None, 4, 256, P, 0, None) == 1
+    assert L.q4k_kq_dequant(5, P + 2, 4, 256, P, 0, None) == 3
+    assert L.q4k_kq_dequant(6, P, 0, 256, P, 0, None) == 0
+
+    def gemv(fmt=2, n=8, k=512, x=P, batch=1, ldx=512, y=P, ldy=8, w=P):
+        return L.q4k_kq_gemv(fmt, w, n, k, x, batch, ldx, y, ldy, None)
+
+    assert gemv(fmt=7) == 2
+    assert gemv(batch=17) == 2
+    assert gemv(k=300) == 2
+    assert gemv(fmt=6, k=36096 + 256, ldx=36352) == 2     # 8 rows no longer fit in shared memory
+    assert gemv(batch=0) == 0
+    assert gemv(x=None) == 1
+    assert gemv(ldx=500) == 2
+    assert gemv(x=P + 8) == 3
+    assert gemv(ldx=516) == 3
+
+
 def test_get_device_error_rejects_null(L):
     assert L.q4k_get_device_error(None, None) == 1
 
@@ -275,6 +299,9 @@ int main(void) {
   st |= q4k_gemv_glu(0, 0, 4, 256, 0, 1, 256, 0, 4, 0u, 0);
   st |= q4k_gemv_seq(ops, 1, 1, 0u, 0);
   st |= q4k_gemm(0, 4, 256, 0, 1, 256, 0, 8, 0);
+  st |= q4k_kq_block_bytes(Q4K_FMT_Q2_K) == 84 ? 0 : 1 << 21;
+  st |= q4k_kq_dequant(Q4K_FMT_Q3_K, 0, 4, 256, 0, 0, 0);
+  st |= q4k_kq_gemv(Q4K_FMT_Q6_K, 0, 4, 256, 0, 1, 256, 0, 4, 0);
   st |= q4k_gemm_rmsnorm(0, 4, 256, 0, 1, 256, 0, 1e-6f, 0, 0, 8, 0);
   st |= (int)q4k_moe_workspace_size(8, 1, 2, 256, 256);
   st |= q4k_moe_gemv(0, 0, 0, 0, 8, 256, 256, 0, 1, 256, 0, 0, 2, 0, 256, 0, 0, 0);

@@ -1,0 +1,103 @@
+"""The other k-quant formats (q2_K, q3_K, Q5_K, Q6_K) on the GPU against the
+oracle: dequantization bit-exact (fp32: the exact weight rounded once; bf16:
+that, rounded to nearest even), the decode projection within 2e-3 * sum|w||x|
+per element, and one-hot activations that must return the oracle's fp32
+weights exactly."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import DEV, check_bound, xbits
+
+pytestmark = pytest.mark.gpu
+FMTS = (2, 3, 5, 6)
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def q4k():
+    from bit_block_quantized_q4_gb300 import build
+    build.build()
+    import bit_block_quantized_q4_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(1, 256), (7, 1024), (33, 5120), (3, 17408)])
+def test_kq_dequant_bit_exact(q4k, fmt, n, k):
+    w = synth.kq_weight(fmt, n, k, seed=fmt * 100 + n + k)
+    got32 = q4k.q4k_kq_dequant(fmt, w.to(DEV), n, k).cpu().numpy()
+    got16 = q4k.q4k_kq_dequant(fmt, w.to(DEV), n, k, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    assert np.array_equal(got32.view(np.uint32), oracle.kq_dequant_f32(fmt, w.numpy(), n, k).view(np.uint32))
+    bits = got16.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bits, oracle.kq_dequant_bf16(fmt, w.numpy(), n, k))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("batch", [1, 3, 4, 9, 16])
+@pytest.mark.parametrize("n,k", [(37, 256), (130, 2560), (64, 17408)])
+def test_kq_gemv_matches_oracle(q4k, fmt, batch, n, k):
+    w = synth.kq_weight(fmt, n, k, seed=fmt * 1000 + batch * 7 + n + k)
+    x = synth.bf16_normal((batch, k), seed=fmt + batch + k)
+    y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x.to(DEV))
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
+    check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, f"kq{fmt} b{batch} {n}x{k}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_kq_gemv_one_hot_returns_the_fp32_weights(q4k, fmt):
+    # x = e_i (one nonzero of value 1): every product but one is zero, so y is
+    # exactly the weight column, as the fp32 dequantization rounds it
+    n, k = 40, 1024
+    w = synth.kq_weight(fmt, n, k, seed=fmt + 500)
+    cols = [0, 7, 8, 15, 16, 31, 32, 63, 64, 127, 128, 255, 256, 511, 777, 1023]
+    x = torch.zeros((len(cols), k), dtype=torch.bfloat16)
+    for b, c in enumerate(cols):
+        x[b, c] = 1.0
+    wf = oracle.kq_dequant_f32(fmt, w.numpy(), n, k)
+    for lo in range(0, len(cols), 16):
+        y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x[lo:lo + 16].to(DEV))
+        torch.cuda.synchronize()
+        got = y.cpu().numpy()
+        for b, c in enumerate(cols[lo:lo + 16]):
+            assert np.array_equal(got[b], wf[:, c]), f"fmt {fmt} column {c}"
+
+
+def test_kq_gemv_strided_io_and_q4k_route(q4k):
+    n, k, batch = 96, 1536, 5
+    for fmt in (3, 4):
+        w = (synth.kq_weight(fmt, n, k, seed=600 + fmt) if fmt != 4
+             else synth.q4k_weight(n, k, seed=604))
+        xs = synth.bf16_normal((batch, k + 64), seed=601).to(DEV)
+        x = xs[:, 32:32 + k]
+        out = torch.full((batch, n + 8), float("nan"), dtype=torch.float32, device=DEV)
+        q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x, out=out[:, :n])
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert np.all(np.isnan(got[:, n:]))
+        yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x.cpu()))
+        check_bound(got[:, :n].astype(np.float64), yref, s, TOL, f"strided kq{fmt}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(5120, 17408), (4096, 1536)])
+def test_kq_gemv_full_size_sampled(q4k, fmt, n, k):
+    # the 27B-class down projection, and one routed expert's down projection
+    # of the 235B-class MoE (the q2_K / q3_K routed-down recipes)
+    w = synth.kq_weight(fmt, n, k, seed=700 + fmt + n, device=DEV)
+    x = synth.bf16_normal((1, k), seed=701 + fmt)
+    y = q4k.q4k_kq_gemv(fmt, w, n, k, x.to(DEV))
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.random.default_rng(n).choice(n, 48, replace=False),
+                                     [0, 1, n - 2, n - 1]]))
+    wsub = w[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    yref, s = oracle.kq_gemv(fmt, wsub, len(rows), k, xbits(x))
+    check_bound(y.cpu().numpy()[:, rows].astype(np.float64), yref, s, TOL, f"full kq{fmt} {n}x{k}")
