@@ -661,8 +661,8 @@ def run_case(case):
     """One small instance of a kernel, for ncu captures (no timing): one 27B-class
     layer of batch-1 projections (203 MB of weights) or of batch-4 and batch-16
     projections, the 512-token gate and
-    down prefill GEMMs (plain or with the RMSNorm prologue), or one routed-MoE
-    decode step."""
+    down prefill GEMMs (plain or with the RMSNorm prologue), one routed-MoE decode
+    or prefill step, or one batch-1 projection in each other k-quant format."""
     import bit_block_quantized_q4_gb300 as q4k
     from bit_block_quantized_q4_gb300 import build as qb
     qb.build()
@@ -690,6 +690,13 @@ def run_case(case):
             else:
                 gamma = torch.full((k,), 1.25, dtype=torch.float32, device=dev)
                 q4k.q4k_gemm_rmsnorm(w, n, k, x, gamma, 1e-6)
+    elif case == "kquant":
+        for fmt in (2, 3, 5, 6):  # one batch-1 projection per format, 27B down shape
+            n, k = 5120, 17408
+            w = synth.kq_weight(fmt, n, k, seed=synth.derive_seed(1008, "case", fmt), device=dev)
+            x = synth.bf16_normal((1, k), seed=synth.derive_seed(1008, "x"), device=dev)
+            torch.cuda.synchronize()
+            q4k.q4k_kq_gemv(fmt, w, n, k, x)
     elif case == "moe_prefill":
         bench_moe_prefill(q4k, dev, torch.cuda.Stream(device=dev), reps=1)
     else:
@@ -772,7 +779,7 @@ def main():
     ap.add_argument("--cpu-table", action="store_true",
                     help="time the oracle on the host cores for every configuration, then exit")
     ap.add_argument("--case", default=None, choices=["gemv_layer", "gemv_layer_batched", "gemm_prefill", "gemm_prefill_rmsnorm", "moe",
-                             "moe_prefill"],
+                             "moe_prefill", "kquant"],
                     help="run one small instance of a kernel for a profiler, then exit")
     args = ap.parse_args()
     if args.cpu_table:

@@ -280,8 +280,8 @@ int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *ou
  * q4k_kq_gemv -- q4k_gemv for any of the formats: Y[b, :] = W X[b, :],
  * batch 1..16, arguments and layouts as q4k_gemv (format 4 is q4k_gemv
  * itself).  Each weight row is read once for all batch rows.  K is limited so
- * that 8 rows fit in shared memory (K/256 * block bytes <= 29 KB; e.g.
- * K <= 36096 for Q6_K).
+ * that 8 rows fit in shared memory: K/256 * block bytes <= 29040 (e.g.
+ * K <= 35328 for Q6_K, 88320 for q2_K).
  * Errors: as q4k_gemv, and SHAPE for an unknown format or too long a row.
  */
 int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,

@@ -255,7 +255,8 @@ def test_kq_argument_errors(L):
     assert gemv(fmt=7) == 2
     assert gemv(batch=17) == 2
     assert gemv(k=300) == 2
-    assert gemv(fmt=6, k=36096 + 256, ldx=36352) == 2     # 8 rows no longer fit in shared memory
+    assert gemv(fmt=6, k=35328, ldx=35328, n=0) == 0       # the longest Q6_K row is accepted
+    assert gemv(fmt=6, k=35328 + 256, ldx=35584) == 2     # 8 rows no longer fit in shared memory
     assert gemv(batch=0) == 0
     assert gemv(x=None) == 1
     assert gemv(ldx=500) == 2

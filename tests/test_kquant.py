@@ -101,3 +101,19 @@ def test_kq_gemv_full_size_sampled(q4k, fmt, n, k):
     wsub = w[torch.from_numpy(rows).to(DEV)].cpu().numpy()
     yref, s = oracle.kq_gemv(fmt, wsub, len(rows), k, xbits(x))
     check_bound(y.cpu().numpy()[:, rows].astype(np.float64), yref, s, TOL, f"full kq{fmt} {n}x{k}")
+
+
+def test_kq_gemv_longest_row_and_host_memory_rejected(q4k):
+    # Q6_K at the longest K whose 8 row buffers fit in shared memory (138 super-blocks)
+    n, k = 5, 35328
+    w = synth.kq_weight(6, n, k, seed=800)
+    x = synth.bf16_normal((2, k), seed=801)
+    y = q4k.q4k_kq_gemv(6, w.to(DEV), n, k, x.to(DEV))
+    torch.cuda.synchronize()
+    yref, s = oracle.kq_gemv(6, w.numpy(), n, k, xbits(x))
+    check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, "Q6_K longest row")
+    # weights in host memory: refused before anything runs (Q4K_ERR_MEMORY)
+    wh = w.pin_memory()
+    with pytest.raises(q4k.Q4KError) as ei:
+        q4k.q4k_kq_gemv(6, wh, n, k, x.to(DEV))
+    assert ei.value.status == 8

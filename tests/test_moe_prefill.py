@@ -151,3 +151,41 @@ def test_moe_prefill_235b_class_sampled_tokens(q4k):
     tokens = [0, 255, 511]
     yref, bound = _bound(c, c["ids"], c["wts"], tokens)
     _check(y[tokens], yref, bound, "235B-class prefill")
+
+
+def test_moe_prefill_most_experts_and_slots_per_token(q4k):
+    # 2048 experts (the largest count), top-16 (the largest), 64 tokens
+    E, H, F, T, K = 2048, 256, 256, 64, 16
+    c = _make(E, H, F, T, K, seed=94)
+    y, err = _gpu(q4k, c)
+    assert err == 0
+    tokens = [0, 31, 63]
+    yref, bound = _bound(c, c["ids"], c["wts"], tokens)
+    _check(y[tokens], yref, bound, "2048 experts top-16")
+
+
+def test_moe_prefill_graph_replay_matches_eager(q4k):
+    # the seven launches captured in one CUDA graph and replayed: the result
+    # equals the eager call's (the path is deterministic)
+    c = _make(16, 512, 512, 120, 4, seed=95)
+    E, H, F = c["E"], c["H"], c["F"]
+    T, K = c["ids"].shape
+    args = [c[k].to(DEV) for k in ("wg", "wu", "wd")]
+    x, ids, wts = c["x"].to(DEV), c["ids"].to(DEV), c["wts"].to(DEV)
+    ws = torch.empty(q4k.q4k_moe_prefill_workspace_size(E, T, K, H, F), dtype=torch.uint8, device=DEV)
+    eager = q4k.q4k_moe_prefill(*args, c["stride"], E, H, F, x, ids, wts, workspace=ws).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream(device=DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        q4k.q4k_moe_prefill(*args, c["stride"], E, H, F, x, ids, wts, out=out, workspace=ws, stream=s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            q4k.q4k_moe_prefill(*args, c["stride"], E, H, F, x, ids, wts, out=out, workspace=ws,
+                                stream=s)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    assert torch.equal(out, eager)
