@@ -229,3 +229,35 @@ def test_moe_stagewise(q4k, E, H, F, T, K, sigma, weighted_down):
     if sigma < 0.1:
         assert gmax < 8.0          # the curved region of SiLU is what was tested
 
+
+
+def test_moe_graph_replay_matches_eager_and_oracle(q4k):
+    # route + persistent expert kernel captured in a CUDA graph and replayed
+    # three times (the route kernel clears the work counters on every replay):
+    # the output equals the eager call's and stays within the oracle bound
+    c = _make(32, 1024, 512, 16, 8, seed=77)
+    E, H, F = c["E"], c["H"], c["F"]
+    T, K = c["ids"].shape
+    wg, wu, wd = (c[k].to(DEV) for k in ("wg", "wu", "wd"))
+    x, ids, wts = c["x"].to(DEV), c["ids"].to(DEV), c["wts"].to(DEV)
+    ws = torch.empty(q4k.q4k_moe_workspace_size(E, T, K, H, F), dtype=torch.uint8, device=DEV)
+    eager = q4k.q4k_moe_gemv(wg, wu, wd, c["stride"], E, H, F, x, ids, wts, workspace=ws).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream(device=DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        q4k.q4k_moe_gemv(wg, wu, wd, c["stride"], E, H, F, x, ids, wts, out=out, workspace=ws,
+                         stream=s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            q4k.q4k_moe_gemv(wg, wu, wd, c["stride"], E, H, F, x, ids, wts, out=out, workspace=ws,
+                             stream=s)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    assert torch.equal(out, eager)
+    tokens = list(range(T))
+    yref, bound = _bound(c, c["ids"], c["wts"], tokens)
+    _check(out.cpu().numpy().astype(np.float64), yref, bound, "moe graph replay")
