@@ -504,15 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
     const uint32_t base = smem_u32(smem);
     if (acc_ready) {
+      // per 128-token sub-tile: the TMEM loads of all of this warp's pushed
+      // chunks first, one wait, then the pushes (the load latency is paid once
+      // per sub-tile, not once per chunk)
 #pragma unroll 1
       for (int sub = 0; sub < kSub; ++sub) {
-#pragma unroll 1
-        for (int c = c_lo; c < c_hi; ++c) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci)
+          if ((c_lo + ci) % KS != (int)krank)  // the same for every lane: a warp-wide load
+            tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * (c_lo + ci)), r[ci]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+          const int c = c_lo + ci;
           const int owner = c % KS;
           if (owner == (int)krank) continue;
-          uint32_t r[16];
-          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r);
-          tmem_ld_wait();
           const uint32_t peer = rank + CS * (uint32_t)owner;
           const int slot = (int)krank < owner ? (int)krank : (int)krank - 1;
           const uint32_t dst = peer_smem(base + block_off(sub, c, slot), peer);
@@ -520,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             st_async_v4(dst + unit_off(u),
-                        make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                    __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                        make_float4(__uint_as_float(r[ci][4 * u]), __uint_as_float(r[ci][4 * u + 1]),
+                                    __uint_as_float(r[ci][4 * u + 2]),
+                                    __uint_as_float(r[ci][4 * u + 3])),
                         bar);
         }
       }
@@ -530,12 +538,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (acc_ready && got) {
 #pragma unroll 1
       for (int sub = 0; sub < kSub; ++sub) {
-#pragma unroll 1
-        for (int c = c_lo; c < c_hi; ++c) {
+        uint32_t ro[4][16];  // this warp's owned chunks of the sub-tile, loaded together
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci)
+          if ((c_lo + ci) % KS == (int)krank)
+            tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * (c_lo + ci)), ro[ci]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+          const int c = c_lo + ci;
           if (c % KS != (int)krank) continue;
-          uint32_t r[16];
-          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r);
-          tmem_ld_wait();
+          const uint32_t (&r)[16] = ro[ci];
           float v[16];
 #pragma unroll
           for (int z = 0; z < KS; ++z) {
