@@ -443,28 +443,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (acc_ready) {
 #pragma unroll 1
       for (int sub = 0; sub < kSub && 128 * sub < np; ++sub) {
+        // the warp's four 16-column chunks of the sub-tile: loads together, one wait
+        uint32_t r[4][16];
 #pragma unroll
-        for (int c = c_lo; c < c_hi; c += 2) {
-          uint32_t r0[16], r1[16];
-          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c), r0);
-          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * c + 16), r1);
-          tmem_ld_wait();
-          __nv_bfloat16 *col = stage + (128 * sub + 16 * c) * kBN + row;
-          if (a.gamma) {
-            const float *rv = rinv_s + 128 * sub + 16 * c;
+        for (int ci = 0; ci < 4; ++ci)
+          tmem_ld_x16(tq + (uint32_t)(sub * 128 + 16 * (c_lo + ci)), r[ci]);
+        tmem_ld_wait();
+        __nv_bfloat16 *col = stage + (128 * sub + 16 * c_lo) * kBN + row;
+        const float *rv = rinv_s + 128 * sub + 16 * c_lo;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]) * rv[e]);
-              col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]) * rv[16 + e]);
-            }
-          } else {
+        for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              col[e * kBN] = __float2bfloat16_rn(__uint_as_float(r0[e]));
-              col[(16 + e) * kBN] = __float2bfloat16_rn(__uint_as_float(r1[e]));
-            }
+          for (int e = 0; e < 16; ++e) {
+            const float v = __uint_as_float(r[ci][e]);
+            col[(16 * ci + e) * kBN] = __float2bfloat16_rn(a.gamma ? v * rv[16 * ci + e] : v);
           }
-        }
       }
     }
     if (__syncthreads_and(acc_ready)) {
