@@ -276,14 +276,16 @@ __global__ void __launch_bounds__(256) gemv_bn_kernel(const __grid_constant__ CU
           for (int r = 0; r < 2; ++r) {
             const float ds = __shfl_sync(0xffffffffu, hi ? dsv[mi][mt][r][1] : dsv[mi][mt][r][0], src);
             const float ee = __shfl_sync(0xffffffffu, hi ? eev[mi][mt][r][1] : eev[mi][mt][r][0], src);
+            // columns 2t, 2t+1 share ds and e: one packed fma each (each lane
+            // of a pair rounds as fmaf)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                float &yv = yacc[mi][mt][nt][2 * r + e];
-                yv = fmaf(ds, acc[nt][2 * r + e], yv);
-                yv = fmaf(ee, xsum[nt][e], yv);
-              }
+            for (int nt = 0; nt < NT; ++nt) {
+              float2 yv = make_float2(yacc[mi][mt][nt][2 * r], yacc[mi][mt][nt][2 * r + 1]);
+              yv = __ffma2_rn(make_float2(ds, ds), make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]), yv);
+              yv = __ffma2_rn(make_float2(ee, ee), make_float2(xsum[nt][0], xsum[nt][1]), yv);
+              yacc[mi][mt][nt][2 * r] = yv.x;
+              yacc[mi][mt][nt][2 * r + 1] = yv.y;
+            }
           }
         }
     };

@@ -419,14 +419,16 @@ __device__ __forceinline__ bool expert_body(const CUtensorMap *map0p, const CUte
           for (int r = 0; r < 2; ++r) {
             const float ds = __shfl_sync(0xffffffffu, hi ? dsv[mi][r][1] : dsv[mi][r][0], srcl);
             const float ee = __shfl_sync(0xffffffffu, hi ? eev[mi][r][1] : eev[mi][r][0], srcl);
+            // columns 2t, 2t+1 share ds and e: one packed fma each (each lane
+            // of a pair rounds as fmaf)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                float &yv = yacc[mi][nt][2 * r + e];
-                yv = fmaf(ds, acc[nt][2 * r + e], yv);
-                yv = fmaf(ee, xsum[nt][e], yv);
-              }
+            for (int nt = 0; nt < NT; ++nt) {
+              float2 yv = make_float2(yacc[mi][nt][2 * r], yacc[mi][nt][2 * r + 1]);
+              yv = __ffma2_rn(make_float2(ds, ds), make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]), yv);
+              yv = __ffma2_rn(make_float2(ee, ee), make_float2(xsum[nt][0], xsum[nt][1]), yv);
+              yacc[mi][nt][2 * r] = yv.x;
+              yacc[mi][nt][2 * r + 1] = yv.y;
+            }
           }
         }
       };
