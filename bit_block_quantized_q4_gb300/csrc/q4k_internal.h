@@ -42,19 +42,21 @@ cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int o
 cudaError_t launch_gemv(const void *w, const void *w_up, int64_t n, int64_t k, const void *x,
                         int64_t batch, int64_t ldx, float *y, int64_t ldy, bool overlap,
                         cudaStream_t stream);
-// One projection of a batch-1 stream launch: y = W x, or for a fused gate/up
-// op (w_up != nullptr) y = silu(W x) * (W_up x).
+// One projection of a stream launch (batch 1..4): Y[b] = W X[b], or for a
+// fused gate/up op (w_up != nullptr) Y[b] = silu(W X[b]) * (W_up X[b]).
 struct StreamOpDesc {
   const void *w;     // weights; the gate matrix of a fused gate/up op
   const void *w_up;  // up matrix of a fused gate/up op, nullptr otherwise
-  const void *x;     // bf16 [k]
-  float *y;          // fp32 [n]
+  const void *x;     // bf16 [batch][ldx]
+  float *y;          // fp32 [batch][ldy]
   int64_t n, k;
+  int64_t ldx, ldy;  // batch-row strides (elements, < 2^31)
 };
 // The ops, in order, as one persistent launch (several when count exceeds the
-// kernel's op table); ops with n == 0 are skipped.
-cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
+// kernel's op table); ops with n == 0 are skipped.  batch 1..stream_max_batch().
+cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream);
+int stream_max_batch();
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
 // Grouped expert GEMM (routed-MoE prefill): for each work slot s < meta[0],

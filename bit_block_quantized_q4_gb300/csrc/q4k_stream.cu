@@ -1,10 +1,11 @@
-// q4k_stream.cu -- batch-1 decode projections y = W x with W in Q4_K, any
-// number of them in one persistent launch ("spec: specialized model runtimes",
-// sections "Architecture" (T0 GEMM, quant/dequant) and "Development sequence"
-// (decode throughput is the metric; graph-captured decode)), and the fused
-// gate/up projection h = silu(Wg x) * (Wu x) of a dense or shared-expert FFN
-// ("Layer Package Repository Spec", section "Policy Resolution": merged shared
-// gate/up).
+// q4k_stream.cu -- decode projections Y[b] = W X[b] with W in Q4_K for batch
+// 1..4, any number of them in one persistent launch ("spec: specialized model
+// runtimes", sections "Architecture" (T0 GEMM, quant/dequant) and "Development
+// sequence" (decode throughput is the metric; graph-captured decode); small
+// decode batches: "PRD: Performant Concurrent Distributed GGUF Runtime",
+// DGR-012), and the fused gate/up projection H[b] = silu(Wg X[b]) * (Wu X[b])
+// of a dense or shared-expert FFN ("Layer Package Repository Spec", section
+// "Policy Resolution": merged shared gate/up).
 //
 // Work: a tile is 16*MT weight rows of one op over the op's whole K (a GLU op's
 // tile is its gate rows, then the same up rows).  The ops of a launch form one
@@ -15,26 +16,30 @@
 // partial sums in warp order through shared memory (for launches with too few
 // tiles to occupy the GPU).
 //
-// Each warp owns a ring of shared-memory stages: one super-block of each of its
-// 16*MT rows (one bulk copy per row) plus the 512 bytes of x of that
-// super-block, all completing on the stage's mbarrier.  The ring runs ahead
-// across tile, part and op boundaries; with programmatic dependent launch the
-// first weight stages are requested before the wait for the previous kernel,
-// x only after it.
+// Each warp owns a ring of shared-memory stages: SB super-blocks of each of its
+// 16*MT rows (one bulk copy per row) plus the x of those super-blocks for each
+// of the NB batch rows (512 bytes per super-block and row), all completing on
+// the stage's mbarrier.  The ring runs ahead across tile, part and op
+// boundaries; with programmatic dependent launch the first weight stages are
+// requested before the wait for the previous kernel, x only after it.
 //
 // Contraction (tensor cores, mma.sync m16n8k16 bf16 -> fp32).  Sub-block j of a
 // row is taken in offset form: w = ds (q - c) + e with c the integer nearest to
 // dmin m_j / (d sc_j) (see offset_form), so the A operand is the exact small
 // integer q - c in bf16 ((128 + q) from one LOP3, minus 128 + c) and x enters
-// unconverted as bf16.  The eight MMA columns carry the eight sub-blocks of a
-// super-block: column n of B holds x only in the k-slots that carry
-// sub-block n, so one super-block is 16 MMAs per 16 rows and thread (g, t) ends
-// with exactly the (row, sub-block) sums of rows g, g+8 and sub-blocks 2t, 2t+1
-// whose scales it decodes itself.  X_j = sum of x over sub-block j comes from
-// two more MMAs with A = 1.  Per super-block the thread adds
-// ds * S_j + e * X_j for its four (row, sub-block) pairs; at the end of a tile a
-// quad shuffle adds the sub-blocks of a row.  Every sum is taken in a fixed
-// order: the result does not depend on timing.
+// unconverted as bf16.  Thread t's k-slots carry sub-block 2t (low nibbles, the
+// "E" MMAs) or 2t+1 (high nibbles, the "O" MMAs) of its rows g, g+8, and the
+// eight MMA columns are (slot s, batch row b): column 2s + (b & 1) of the MMAs
+// of batch-row pair b/2 holds x of row b only in the k-slots of thread s and
+// zeros elsewhere.  So one super-block is 16 MMAs per 16 rows and batch-row
+// pair, and thread (g, t) ends with exactly the (row, sub-block, batch row)
+// sums of rows g, g+8, sub-blocks 2t, 2t+1 and both rows of each pair, whose
+// scales it decodes itself: no shuffles and no per-sub-block epilogue outside
+// the thread.  X_j = sum of x over sub-block j comes from two more MMAs per
+// batch row with A = 1.  Per super-block the thread adds ds * S_j + e * X_j for
+// its (row, sub-block, batch row) triples; at the end of a tile a quad shuffle
+// adds the sub-blocks of a row.  Every sum is taken in a fixed order: the
+// result does not depend on timing.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -74,6 +79,28 @@
 #ifndef Q4K_STREAM_FORCE_KP
 #define Q4K_STREAM_FORCE_KP 0
 #endif
+// Batch rows 2 and 3..4 (NB = 2, 4): super-blocks per stage, ring stages and
+// resident CTAs per SM the register budget is sized for.  Two super-blocks per
+// stage measured best at both (one: 2.58 / 2.06 TB/s against 3.27 / 2.29 at
+// batch 2 / 4; more stages cost occupancy).
+#ifndef Q4K_STREAM_SB_NB2
+#define Q4K_STREAM_SB_NB2 2
+#endif
+#ifndef Q4K_STREAM_STAGES_NB2
+#define Q4K_STREAM_STAGES_NB2 2
+#endif
+#ifndef Q4K_STREAM_MINB_NB2
+#define Q4K_STREAM_MINB_NB2 4
+#endif
+#ifndef Q4K_STREAM_SB_NB4
+#define Q4K_STREAM_SB_NB4 2
+#endif
+#ifndef Q4K_STREAM_STAGES_NB4
+#define Q4K_STREAM_STAGES_NB4 2
+#endif
+#ifndef Q4K_STREAM_MINB_NB4
+#define Q4K_STREAM_MINB_NB4 3
+#endif
 
 namespace q4k {
 
@@ -82,8 +109,11 @@ namespace {
 constexpr int kWarps = 4;              // warps per CTA
 constexpr int kXBytes = kQK * 2;       // bf16 x of one super-block
 constexpr int kPermStride = 20;        // words per sub-block in the permuted x (16 used)
-constexpr int kPermWords = 8 * kPermStride;
-constexpr int kMaxOps = 512;           // ops per launch (kernel parameter table)
+// words of one batch row of one super-block in the permuted x: 4 more than the
+// eight sub-blocks, so that the B-fragment reads of batch rows 2P and 2P+1
+// fall on different banks
+constexpr int kPermWords = 8 * kPermStride + 4;
+constexpr int kMaxOps = 448;           // ops per launch (kernel parameter table, < 32 KB)
 
 struct StreamOp {
   const uint8_t *w;   // weights; the gate matrix of a GLU op
@@ -92,11 +122,13 @@ struct StreamOp {
   float *y;
   long long byte0;  // weight bytes of the ops before this one
   int n, nsb, ntiles, parts;
+  int ldx, ldy;     // batch-row strides of x and y (elements)
 };
 
 template <int NOPS>
 struct StreamParams {
   int nops;
+  int batch;     // batch rows (1 .. NB of the kernel)
   int kp;        // warps per tile stream (split of each tile's super-blocks)
   int pre;       // weight stages requested before the dependency wait
   int nstreams;  // tile streams in the grid
@@ -105,24 +137,34 @@ struct StreamParams {
   StreamOp op[NOPS];
 };
 
-template <int MT>
+template <int MT, int NB>
 struct StreamCfg {
   static constexpr int kRows = 16 * MT;
-  static constexpr int kSB = Q4K_STREAM_SB;  // super-blocks per stage
-  static constexpr int kStages = MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2;
+  static constexpr int kNB = NB;                   // batch rows the kernel carries
+  static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
+  static constexpr int kSB = NB == 1 ? Q4K_STREAM_SB : NB == 2 ? Q4K_STREAM_SB_NB2 : Q4K_STREAM_SB_NB4;
+  static constexpr int kStages = NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
+                                         : NB == 2 ? Q4K_STREAM_STAGES_NB2 : Q4K_STREAM_STAGES_NB4;
+  static constexpr int kMinBlocks = NB == 1 ? (MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
+                                            : NB == 2 ? Q4K_STREAM_MINB_NB2 : Q4K_STREAM_MINB_NB4;
   // a row's slot in a stage: its kSB super-blocks, padded by 16 bytes when
   // kSB is even so that the 16*MT rows fall on different shared-memory banks
   static constexpr int kRowBytes = kSB * kBlockBytes + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
-  static constexpr int kXStage = kSB * kXBytes;        // x bytes of a stage
-  // warp region: ring weights | ring x | 2 permuted-x buffers | 64 zero bytes |
+  static constexpr int kXStage = NB * kSB * kXBytes;   // x bytes of a stage: [batch row][sb]
+  // permuted-x buffers: two at NB = 1 (written and read on alternate
+  // super-blocks), one otherwise (a warp barrier separates the reads of one
+  // super-block from the writes of the next)
+  static constexpr int kPermBufs = NB == 1 ? 2 : 1;
+  static constexpr int kPermBuf = NB * kPermWords;     // words of one buffer: [batch row][sub-block]
+  // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes |
   // ring mbarriers
   static constexpr int kOffX = kStages * kWBytes;
   static constexpr int kOffPerm = kOffX + kStages * kXStage;
-  static constexpr int kOffZero = kOffPerm + 2 * kPermWords * 4;
+  static constexpr int kOffZero = kOffPerm + kPermBufs * kPermBuf * 4;
   static constexpr int kOffBar = kOffZero + 64;
   static constexpr int kWarpBytes = (kOffBar + kStages * 8 + 127) / 128 * 128;
-  static constexpr int kRedBytes = 2 * kWarps * 2 * kRows * 4;  // split-K partials
+  static constexpr int kRedBytes = 2 * kWarps * 2 * NB * kRows * 4;  // split-K partials
   static constexpr int kSmem = kWarps * kWarpBytes + kRedBytes;
 };
 
@@ -137,6 +179,7 @@ struct Pos {
   bool valid;
   const uint8_t *src;
   const __nv_bfloat16 *xsrc;
+  int ldx;
   uint32_t bytes;
 };
 
@@ -193,7 +236,8 @@ __device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, 
               ? (s.part ? o.w2 : o.w) + (size_t)(row0 + lane) * o.nsb * kBlockBytes
               : nullptr;
   s.xsrc = o.x;
-  s.bytes = (uint32_t)(nrows * kBlockBytes + kQK * 2);
+  s.ldx = o.ldx;
+  s.bytes = (uint32_t)(nrows * kBlockBytes + kQK * 2 * p.batch);
 }
 
 // Producer walk over the non-empty stages of a stream, for warp kp of KP:
@@ -216,10 +260,10 @@ __device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows
   if (s.valid) pos_load(p, rows, lane, s);
 }
 
-template <int NOPS>
+template <int SB, int NOPS>
 __device__ __forceinline__ void pos_next(const StreamParams<NOPS> &p, int rows, long long hi,
                                          int kp, int lane, Pos &s) {
-  if ((s.sb += Q4K_STREAM_SB) < s.kb1) return;
+  if ((s.sb += SB) < s.kb1) return;
   pos_settle(p, rows, hi, kp, lane, s);
 }
 
@@ -259,12 +303,11 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
 }
 
-template <int MT, int NOPS>
-__global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
-    gemv_stream_kernel(
-    const __grid_constant__ StreamParams<NOPS> p) {
-  using C = StreamCfg<MT>;
-  constexpr int TR = C::kRows, ST = C::kStages;
+template <int MT, int NOPS, int NB>
+__global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
+    gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
+  using C = StreamCfg<MT, NB>;
+  constexpr int TR = C::kRows, ST = C::kStages, NP = C::kPairs;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -273,6 +316,7 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
   const int sic = warp / KP;                       // stream within the CTA
   const int sid = blockIdx.x * (kWarps / KP) + sic;  // stream id
   const long long lo = p.total * sid / p.nstreams, hi = p.total * (sid + 1) / p.nstreams;
+  const int batch = NB == 1 ? 1 : p.batch;
 
   uint8_t *wreg = smem + (size_t)warp * C::kWarpBytes;
   uint8_t *ringw = wreg;
@@ -308,10 +352,14 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
       bulk_load_hint(ringw + slot * C::kWBytes + lane * C::kRowBytes,
                      s.src + (size_t)s.sb * kBlockBytes, cnt * kBlockBytes, &full[slot], policy);
   };
+  // x of batch row b goes to [b][0 .. SB) of the stage's x area, one copy per
+  // row from lane 31 - b.
   auto issue_x = [&](int slot, const Pos &s) {
     const uint32_t cnt = (uint32_t)min(SB, s.kb1 - s.sb);
-    if (lane == 31)
-      bulk_load(ringx + slot * C::kXStage, s.xsrc + (size_t)s.sb * kQK, cnt * kXBytes, &full[slot]);
+    const int b = 31 - lane;
+    if (b < batch)
+      bulk_load(ringx + slot * C::kXStage + b * (SB * kXBytes),
+                s.xsrc + (size_t)b * s.ldx + (size_t)s.sb * kQK, cnt * kXBytes, &full[slot]);
   };
 
   // With programmatic dependent launch the first p.pre stages' weights go out
@@ -322,7 +370,7 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
     Pos q = pp;
     for (; npre < p.pre && npre < ST && q.valid; ++npre) {
       issue_w(npre, q);
-      pos_next(p, TR, hi, kp, lane, q);
+      pos_next<SB>(p, TR, hi, kp, lane, q);
     }
   }
   grid_dependency_wait();
@@ -330,7 +378,7 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
   for (int s = 0; s < ST && pp.valid; ++s) {
     if (s >= npre) issue_w(s, pp);
     issue_x(s, pp);
-    pos_next(p, TR, hi, kp, lane, pp);
+    pos_next<SB>(p, TR, hi, kp, lane, pp);
     ++inflight;
   }
   grid_launch_dependents();
@@ -345,11 +393,18 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
   const uint32_t psel = k0 | ((k0 + 1) << 4) | ((k0 + 4) << 8) | ((k0 + 5) << 12);
   const uint32_t mlo4 = upper ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
   const uint32_t mhi4 = upper ? 0x30303030u : 0u;
-  // B fragments: lane (g, t) carries sub-block g on the steps of parity g & 1
-  // when t == g / 2 (its k-slots then hold sub-block 2t + (g & 1)); every
-  // other (lane, step) reads zeros.
+  // B fragments: lane (g, t) is column g of every MMA; when t == g / 2 its
+  // k-slots carry x of batch row 2P + (g & 1) of pair P (sub-block 2t in the E
+  // MMAs, 2t+1 in the O MMAs); every other lane, and a row past the batch,
+  // reads zeros.  bofs[P]: word offset of that row's sub-block 2t in a
+  // permuted-x buffer, or -1.
   const bool own = t == (g >> 1);
-  const bool own_e = own && !(g & 1), own_o = own && (g & 1);
+  int bofs[NP];
+#pragma unroll
+  for (int P = 0; P < NP; ++P) {
+    const int b = 2 * P + (g & 1);
+    bofs[P] = (own && b < batch) ? b * kPermWords + 2 * t * kPermStride : -1;
+  }
   uint32_t magic;
   asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kBf16Magic));
 
@@ -366,15 +421,21 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
     const StreamOp &o = p.op[op];
     int kb0, kb1;
     krange(o.nsb, kp, KP, kb0, kb1);
-    float yv[2][MT][2];  // per part: rows (g, g+8) of each m-tile, partial over sub-blocks 2t, 2t+1
+    // per part: rows (g, g+8) of each m-tile and each batch row, partial over
+    // sub-blocks 2t, 2t+1
+    float yv[2][MT][2][NB];
 #pragma unroll
     for (int pt = 0; pt < 2; ++pt)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) yv[pt][mt][0] = yv[pt][mt][1] = 0.f;
-    for (int part = 0; part < o.parts; ++part) {
-      float yacc[MT][2];
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) yacc[mt][0] = yacc[mt][1] = 0.f;
+        for (int b = 0; b < NB; ++b) yv[pt][mt][0][b] = yv[pt][mt][1][b] = 0.f;
+    for (int part = 0; part < o.parts; ++part) {
+      float yacc[MT][2][NB];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) yacc[mt][0][b] = yacc[mt][1][b] = 0.f;
       for (int sb = kb0; sb < kb1 && ok; sb += SB) {
 #if Q4K_STREAM_SLEEP_NS
         const bool landed = mbar_wait_sleepy(&full[cslot], phase, p.err, Q4K_STREAM_SLEEP_NS);
@@ -394,22 +455,26 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
         for (int u = 0; u < SB; ++u) {
           if (u >= cnt) break;
           const uint8_t *ws = wstage + u * kBlockBytes;
-          const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
-          // X_j of the eight sub-blocks: lane (g, t) holds values 8t .. 8t+7 of
-          // sub-block g, exactly the B fragment of column g of two MMAs.
-          float xs[4];
-          mma_bf16_zc(xs, kBf16One, kBf16One, kBf16One, kBf16One, raw.x, raw.y);
-          mma_bf16(xs, kBf16One, kBf16One, kBf16One, kBf16One, raw.z, raw.w);
-          // Permuted copy: word 2G of a sub-block holds (x[4G], x[4G+2]), word
-          // 2G+1 (x[4G+1], x[4G+3]) -- the pairs the nibble operands meet.
-          uint32_t *pw = perm + pbuf * kPermWords;
-          {
+          uint32_t *pw = perm + pbuf * C::kPermBuf;
+          if (C::kPermBufs == 1) __syncwarp();  // the previous super-block's reads are done
+          // X_j of the eight sub-blocks of each batch row: lane (g, t) holds
+          // values 8t .. 8t+7 of sub-block g, exactly the B fragment of column
+          // g of two MMAs.  Permuted copy: word 2G of a sub-block holds
+          // (x[4G], x[4G+2]), word 2G+1 (x[4G+1], x[4G+3]) -- the pairs the
+          // nibble operands meet.
+          float xs[NB][4];
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (b < batch) raw = reinterpret_cast<const uint4 *>(xstage + (b * SB + u) * kXBytes)[lane];
+            mma_bf16_zc(xs[b], kBf16One, kBf16One, kBf16One, kBf16One, raw.x, raw.y);
+            mma_bf16(xs[b], kBf16One, kBf16One, kBf16One, kBf16One, raw.z, raw.w);
             uint4 pm;
             pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
             pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
             pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
             pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
-            reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+            reinterpret_cast<uint4 *>(pw + b * kPermWords + g * kPermStride)[t] = pm;
           }
           uint4 hdr[MT][2], qa[MT][2][2];
 #pragma unroll
@@ -427,7 +492,7 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
             if (pp.valid) {  // refill this slot with the stream's next stage
               issue_w(cslot, pp);
               issue_x(cslot, pp);
-              pos_next(p, TR, hi, kp, lane, pp);
+              pos_next<SB>(p, TR, hi, kp, lane, pp);
               ++inflight;
             }
           }
@@ -435,7 +500,7 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
           // Offset form of this thread's (row, sub-block) pairs.
           float ds[MT][2][2], ee[MT][2][2];
           uint32_t sub[MT][2][2];
-  #pragma unroll
+#pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const uint4 h0 = hdr[mt][0], h1 = hdr[mt][1];
             const uint32_t py = __byte_perm(h0.y, h1.y, psel);
@@ -443,31 +508,39 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
             const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
             const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
             const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
-  #pragma unroll
+#pragma unroll
             for (int r = 0; r < 2; ++r) {
               const uint32_t hx = r ? h1.x : h0.x;
               const float d = half_lo_to_float(hx), dmin = half_hi_to_float(hx);
               const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 2; ++e)
                 offset_form(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e),
                             byte_magic(m4, 2 * r + e), ds[mt][r][e], ee[mt][r][e], sub[mt][r][e]);
             }
           }
 
-          const uint32_t *pe = own_e ? pw + g * kPermStride : zeros;
-          const uint32_t *po = own_o ? pw + g * kPermStride : zeros;
-          float accE[MT][4], accO[MT][4];
-  #pragma unroll
+          const uint32_t *pe[NP], *po[NP];
+#pragma unroll
+          for (int P = 0; P < NP; ++P) {
+            pe[P] = bofs[P] >= 0 ? pw + bofs[P] : zeros;
+            po[P] = bofs[P] >= 0 ? pw + bofs[P] + kPermStride : zeros;
+          }
+          // accE[mt][P] column 2t + i = sum (q - c) x over sub-block 2t of batch
+          // row 2P + i (rows g: [i], g+8: [2 + i]); accO likewise for 2t+1.
+          float accE[MT][NP][4], accO[MT][NP][4];
+#pragma unroll
           for (int G2 = 0; G2 < 4; ++G2) {
-            const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // the zero block is 4 uint4
-            const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
-  #pragma unroll
+            uint4 be[NP], bo[NP];
+#pragma unroll
+            for (int P = 0; P < NP; ++P) {
+              be[P] = reinterpret_cast<const uint4 *>(pe[P])[G2];  // the zero block is 4 uint4
+              bo[P] = reinterpret_cast<const uint4 *>(po[P])[G2];
+            }
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int G = 2 * G2 + h;
-              const uint32_t be0 = h ? be.z : be.x, be1 = h ? be.w : be.y;
-              const uint32_t bo0 = h ? bo.z : bo.x, bo1 = h ? bo.w : bo.y;
-  #pragma unroll
+#pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
                 const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
@@ -476,36 +549,41 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
                 const uint32_t a1 = sub_bf16x2(lop_nib(w1, magic), sub[mt][1][0]);
                 const uint32_t a2 = sub_bf16x2(lop_nib(shr<8>(w0), magic), sub[mt][0][0]);
                 const uint32_t a3 = sub_bf16x2(lop_nib(shr<8>(w1), magic), sub[mt][1][0]);
-                if (G == 0)
-                  mma_bf16_zc(accE[mt], a0, a1, a2, a3, be0, be1);
-                else
-                  mma_bf16(accE[mt], a0, a1, a2, a3, be0, be1);
                 // high nibbles: sub-block 2t+1
                 const uint32_t c0 = sub_bf16x2(lop_nib(shr<4>(w0), magic), sub[mt][0][1]);
                 const uint32_t c1 = sub_bf16x2(lop_nib(shr<4>(w1), magic), sub[mt][1][1]);
                 const uint32_t c2 = sub_bf16x2(lop_nib(shr<12>(w0), magic), sub[mt][0][1]);
                 const uint32_t c3 = sub_bf16x2(lop_nib(shr<12>(w1), magic), sub[mt][1][1]);
-                if (G == 0)
-                  mma_bf16_zc(accO[mt], c0, c1, c2, c3, bo0, bo1);
-                else
-                  mma_bf16(accO[mt], c0, c1, c2, c3, bo0, bo1);
+#pragma unroll
+                for (int P = 0; P < NP; ++P) {
+                  const uint32_t be0 = h ? be[P].z : be[P].x, be1 = h ? be[P].w : be[P].y;
+                  const uint32_t bo0 = h ? bo[P].z : bo[P].x, bo1 = h ? bo[P].w : bo[P].y;
+                  if (G == 0) {
+                    mma_bf16_zc(accE[mt][P], a0, a1, a2, a3, be0, be1);
+                    mma_bf16_zc(accO[mt][P], c0, c1, c2, c3, bo0, bo1);
+                  } else {
+                    mma_bf16(accE[mt][P], a0, a1, a2, a3, be0, be1);
+                    mma_bf16(accO[mt][P], c0, c1, c2, c3, bo0, bo1);
+                  }
+                }
               }
             }
           }
-          // accE column 2t = sum (q - c) x over sub-block 2t (rows g: [0], g+8:
-          // [2]); accO column 2t+1 likewise for sub-block 2t+1 ([1], [3]).
-  #pragma unroll
+#pragma unroll
           for (int mt = 0; mt < MT; ++mt)
-  #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float v = yacc[mt][r];
-              v = fmaf(ds[mt][r][0], accE[mt][2 * r], v);
-              v = fmaf(ee[mt][r][0], xs[0], v);
-              v = fmaf(ds[mt][r][1], accO[mt][2 * r + 1], v);
-              v = fmaf(ee[mt][r][1], xs[1], v);
-              yacc[mt][r] = v;
-            }
-          pbuf ^= 1;
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+              for (int b = 0; b < NB; ++b) {
+                const int P = b >> 1, i = 2 * r + (b & 1);
+                float v = yacc[mt][r][b];
+                v = fmaf(ds[mt][r][0], accE[mt][P][i], v);
+                v = fmaf(ee[mt][r][0], xs[b][0], v);
+                v = fmaf(ds[mt][r][1], accO[mt][P][i], v);
+                v = fmaf(ee[mt][r][1], xs[b][1], v);
+                yacc[mt][r][b] = v;
+              }
+          if (C::kPermBufs == 2) pbuf ^= 1;
         }
         if (++cslot == ST) {
           cslot = 0;
@@ -513,10 +591,12 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
         }
       }
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        yv[part & 1][mt][0] = yacc[mt][0];
-        yv[part & 1][mt][1] = yacc[mt][1];
-      }
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          yv[part & 1][mt][0][b] = yacc[mt][0][b];
+          yv[part & 1][mt][1][b] = yacc[mt][1][b];
+        }
     }
     // Rows: add the quad's sub-block pairs (t = 0..3).
 #pragma unroll
@@ -524,12 +604,14 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float v = yv[pt][mt][r];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          yv[pt][mt][r] = v;
-        }
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            float v = yv[pt][mt][r][b];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            yv[pt][mt][r][b] = v;
+          }
     const int row0 = tile * TR;
     if (KP == 1) {
       if (ok && t == 0) {
@@ -538,35 +620,45 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int row = row0 + mt * 16 + g + 8 * r;
-            if (row < o.n)
-              o.y[row] = o.parts == 2 ? silu_mul(yv[0][mt][r], yv[1][mt][r]) : yv[0][mt][r];
+            if (row < o.n) {
+#pragma unroll
+              for (int b = 0; b < NB; ++b)
+                if (b < batch)
+                  o.y[(size_t)b * o.ldy + row] =
+                      o.parts == 2 ? silu_mul(yv[0][mt][r][b], yv[1][mt][r][b]) : yv[0][mt][r][b];
+            }
           }
       }
     } else {
       // Split K: the KP warps of the stream add their partials in warp order.
-      float *rb = red + ((size_t)(par * kWarps + warp) * 2) * TR;
+      // A warp's partials: [part][batch row][row of the tile].
+      float *rb = red + ((size_t)(par * kWarps + warp) * 2 * NB) * TR;
       if (t == 0) {
         const float nanv = __int_as_float(0x7fc00000);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int rr = mt * 16 + g + 8 * r;
-            rb[rr] = ok ? yv[0][mt][r] : nanv;
-            rb[TR + rr] = ok ? yv[1][mt][r] : nanv;
-          }
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              const int rr = mt * 16 + g + 8 * r;
+              rb[b * TR + rr] = ok ? yv[0][mt][r][b] : nanv;
+              rb[(NB + b) * TR + rr] = ok ? yv[1][mt][r][b] : nanv;
+            }
       }
       asm volatile("bar.sync %0, %1;\n" ::"r"(1 + sic), "r"(32 * KP) : "memory");
       if (kp == 0) {
-        const float *base = red + ((size_t)(par * kWarps + sic * KP) * 2) * TR;
-        for (int rr = lane; rr < TR; rr += 32) {
+        const float *base = red + ((size_t)(par * kWarps + sic * KP) * 2 * NB) * TR;
+        for (int idx = lane; idx < NB * TR; idx += 32) {
+          const int b = idx / TR, rr = idx % TR;
           float gs = 0.f, us = 0.f;
           for (int w = 0; w < KP; ++w) {
-            gs += base[w * 2 * TR + rr];
-            us += base[w * 2 * TR + TR + rr];
+            gs += base[(w * 2 * NB + b) * TR + rr];
+            us += base[(w * 2 * NB + NB + b) * TR + rr];
           }
           const int row = row0 + rr;
-          if (row < o.n) o.y[row] = o.parts == 2 ? silu_mul(gs, us) : gs;
+          if (row < o.n && b < batch)
+            o.y[(size_t)b * o.ldy + row] = o.parts == 2 ? silu_mul(gs, us) : gs;
         }
       }
     }
@@ -578,38 +670,37 @@ __global__ void __launch_bounds__(kWarps * 32, MT == 1 ? Q4K_STREAM_MINB_MT1 : Q
 // ---------------------------------------------------------------- host side
 
 std::once_flag g_stream_attr[kMaxDevices];
-// Resident CTAs per SM of the four kernels ([MT - 1][op table small/large]),
-// queried once per device after the attributes are set.
-int g_occ[kMaxDevices][2][2];
+// Resident CTAs per SM of the kernels ([variant][op table small/large]; the
+// variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4)), queried once per
+// device after the attributes are set.
+int g_occ[kMaxDevices][4][2];
 
-template <int MT, int NOPS>
+template <int MT, int NOPS, int NB>
 constexpr auto stream_kernel() {
-  return gemv_stream_kernel<MT, NOPS>;
+  return gemv_stream_kernel<MT, NOPS, NB>;
 }
 
-template <int MT, int NOPS>
-int stream_occupancy() {
+template <int MT, int NOPS, int NB>
+int stream_setup() {
+  cudaFuncSetAttribute(stream_kernel<MT, NOPS, NB>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       StreamCfg<MT, NB>::kSmem);
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, stream_kernel<MT, NOPS>(),
-                                                    kWarps * 32, StreamCfg<MT>::kSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, stream_kernel<MT, NOPS, NB>(),
+                                                    kWarps * 32, StreamCfg<MT, NB>::kSmem) !=
       cudaSuccess)
     return 0;
   return blocks;
 }
 
 void stream_attributes(int dev) {
-  cudaFuncSetAttribute(stream_kernel<1, 1>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       StreamCfg<1>::kSmem);
-  cudaFuncSetAttribute(stream_kernel<2, 1>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       StreamCfg<2>::kSmem);
-  cudaFuncSetAttribute(stream_kernel<1, kMaxOps>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       StreamCfg<1>::kSmem);
-  cudaFuncSetAttribute(stream_kernel<2, kMaxOps>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       StreamCfg<2>::kSmem);
-  g_occ[dev][0][0] = stream_occupancy<1, 1>();
-  g_occ[dev][0][1] = stream_occupancy<1, kMaxOps>();
-  g_occ[dev][1][0] = stream_occupancy<2, 1>();
-  g_occ[dev][1][1] = stream_occupancy<2, kMaxOps>();
+  g_occ[dev][0][0] = stream_setup<1, 1, 1>();
+  g_occ[dev][0][1] = stream_setup<1, kMaxOps, 1>();
+  g_occ[dev][1][0] = stream_setup<2, 1, 1>();
+  g_occ[dev][1][1] = stream_setup<2, kMaxOps, 1>();
+  g_occ[dev][2][0] = stream_setup<1, 1, 2>();
+  g_occ[dev][2][1] = stream_setup<1, kMaxOps, 2>();
+  g_occ[dev][3][0] = stream_setup<1, 1, 4>();
+  g_occ[dev][3][1] = stream_setup<1, kMaxOps, 4>();
 }
 
 struct StreamPlan {
@@ -618,7 +709,8 @@ struct StreamPlan {
 
 // Split: the least splitting that still gives every resident warp a tile
 // (1, 2, else 4 warps per tile).  Tiles are 16 rows: 32-row tiles (fewer
-// resident warps, twice the registers) measured slower on the 27B-class pass.
+// resident warps, twice the registers) measured slower on the 27B-class pass
+// (occ2 <= 0: no 32-row kernel).
 StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
                        const DeviceFacts *f) {
   const int cand[3][2] = {{Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 1},
@@ -626,8 +718,9 @@ StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
                           {Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 4}};
   StreamPlan best;
   for (const auto &c : cand) {
-    const int mt = c[0], kp = c[1];
-    if (Q4K_STREAM_FORCE_MT && mt != Q4K_STREAM_FORCE_MT) continue;
+    int mt = c[0];
+    const int kp = c[1];
+    if (mt == 2 && occ2 <= 0) mt = 1;
     if (Q4K_STREAM_FORCE_KP && kp != Q4K_STREAM_FORCE_KP) continue;
     const int occ = mt == 1 ? occ1 : occ2;
     if (occ <= 0) continue;
@@ -642,8 +735,8 @@ StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
   return best;
 }
 
-template <int MT, int NOPS>
-cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int kp, int grid,
+template <int MT, int NOPS, int NB>
+cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, int kp, int grid,
                                 bool overlap, cudaStream_t stream) {
   StreamParams<NOPS> prm;
   memset(&prm, 0, sizeof prm);
@@ -662,11 +755,14 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int kp, int 
     o.nsb = (int)(d.k / kQK);
     o.ntiles = (int)((d.n + TR - 1) / TR);
     o.parts = d.w_up ? 2 : 1;
+    o.ldx = (int)d.ldx;
+    o.ldy = (int)d.ldy;
     o.byte0 = total;
     total += (long long)d.n * o.nsb * kBlockBytes * o.parts;
   }
   if (nops == 0) return cudaSuccess;
   prm.nops = nops;
+  prm.batch = batch;
   prm.kp = kp;
   prm.pre = overlap ? Q4K_STREAM_PRE : 0;
   prm.nstreams = grid * (kWarps / kp);
@@ -676,22 +772,37 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int kp, int 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)StreamCfg<MT>::kSmem;
+  cfg.dynamicSmemBytes = (size_t)StreamCfg<MT, NB>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, stream_kernel<MT, NOPS>(), prm);
+  return cudaLaunchKernelEx(&cfg, stream_kernel<MT, NOPS, NB>(), prm);
+}
+
+template <int NOPS>
+cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, const StreamPlan &pl,
+                             bool overlap, cudaStream_t stream) {
+  if (batch == 1)
+    return pl.mt == 1 ? launch_stream_chunk<1, NOPS, 1>(ops, count, 1, pl.kp, pl.grid, overlap, stream)
+                      : launch_stream_chunk<2, NOPS, 1>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+  if (batch == 2)
+    return launch_stream_chunk<1, NOPS, 2>(ops, count, 2, pl.kp, pl.grid, overlap, stream);
+  return launch_stream_chunk<1, NOPS, 4>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
+int stream_max_batch() { return 4; }
+
+cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream) {
+  if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
+  const int var1 = batch == 1 ? 0 : batch == 2 ? 2 : 3;  // 16-row kernel of this batch
   int64_t i = 0;
   while (i < count) {
     // a chunk: up to kMaxOps ops with rows
@@ -707,19 +818,14 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, bool overlap,
     }
     if (used > 0) {
       const bool single = used == 1;
-      const int occ1 = g_occ[f->device][0][single ? 0 : 1];
-      const int occ2 = g_occ[f->device][1][single ? 0 : 1];
+      const int occ1 = g_occ[f->device][var1][single ? 0 : 1];
+      const int occ2 = batch == 1 ? g_occ[f->device][1][single ? 0 : 1] : 0;
       const StreamPlan pl = plan_stream(tiles1, tiles2, occ1, occ2, f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const StreamOpDesc *chunk = ops + i;
       const int n = (int)(j - i);
-      cudaError_t e;
-      if (single)
-        e = pl.mt == 1 ? launch_stream_chunk<1, 1>(chunk, n, pl.kp, pl.grid, overlap, stream)
-                       : launch_stream_chunk<2, 1>(chunk, n, pl.kp, pl.grid, overlap, stream);
-      else
-        e = pl.mt == 1 ? launch_stream_chunk<1, kMaxOps>(chunk, n, pl.kp, pl.grid, overlap, stream)
-                       : launch_stream_chunk<2, kMaxOps>(chunk, n, pl.kp, pl.grid, overlap, stream);
+      const cudaError_t e = single ? launch_stream_nb<1>(chunk, n, batch, pl, overlap, stream)
+                                   : launch_stream_nb<kMaxOps>(chunk, n, batch, pl, overlap, stream);
       if (e != cudaSuccess) return e;
     }
     i = j;

@@ -35,7 +35,9 @@ def _run(q4k, w, n, k, x, flags=0):
 
 
 CASES = [(1, 256, 1), (7, 512, 1), (129, 1280, 1), (597, 5120, 1), (33, 17408, 1),
-         (4096, 4096, 1), (1000, 2560, 2), (597, 5120, 3), (300, 4096, 4), (130, 1536, 8),
+         (4096, 4096, 1), (1000, 2560, 2), (597, 5120, 3), (300, 4096, 4), (1, 256, 2),
+         (17, 768, 3), (33, 17408, 4), (4901, 1280, 2), (4901, 2304, 3), (39000, 256, 2),
+         (29200, 512, 3), (130, 1536, 8),
          (129, 5120, 9), (597, 5120, 16), (40, 8192, 16)]
 
 
@@ -66,7 +68,7 @@ def test_gemv_many_row_tiles(q4k, n, k):
     check_bound(y0, yref, s, TOL, f"per-tile {n}x{k}")
 
 
-@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (4, 1), (16, 0)])
+@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (2, 1), (3, 0), (4, 1), (5, 1), (16, 0)])
 def test_gemv_seq_matches_oracle(q4k, batch, flags):
     # one q4k_gemv_seq call over projections of different shapes (an empty one
     # and a fused gate/up op among them) matches the oracle; a second call gives
@@ -117,8 +119,9 @@ def check_glu(h, wg, wu, n, k, x, what):
     assert not bad.any(), f"{what}: {bad.sum()} outside, worst {np.max(err - bound)}"
 
 
-@pytest.mark.parametrize("n,k,batch", [(1, 256, 1), (77, 1024, 1), (1000, 2560, 1), (300, 4096, 4),
-                                       (130, 1536, 8), (129, 5120, 9), (597, 5120, 16)])
+@pytest.mark.parametrize("n,k,batch", [(1, 256, 1), (77, 1024, 1), (1000, 2560, 1), (1000, 2560, 2),
+                                       (77, 1024, 3), (300, 4096, 4), (130, 1536, 8), (129, 5120, 9),
+                                       (597, 5120, 16)])
 @pytest.mark.parametrize("sigma", [1.0, 0.02])
 def test_gemv_glu_matches_oracle(q4k, n, k, batch, sigma):
     # sigma 0.02: g in SiLU's curved region; 1.0: g large, SiLU near identity / 0
@@ -148,7 +151,8 @@ def test_gemv_glu_27b_gate_up_full_size_sampled_rows(q4k, batch):
               f"27b glu b{batch}")
 
 
-def test_gemv_seq_graph_replay_matches_oracle(q4k):
+@pytest.mark.parametrize("batch", [1, 4])
+def test_gemv_seq_graph_replay_matches_oracle(q4k, batch):
     # one 27B-class layer's five projections as one q4k_gemv_seq call with
     # programmatic dependent launch, captured in a CUDA graph; the graph is
     # replayed twice with x rewritten in between, and every replay's results
@@ -156,19 +160,19 @@ def test_gemv_seq_graph_replay_matches_oracle(q4k):
     shapes = [(10240, 5120), (5120, 8192), (17408, 5120), (17408, 5120), (5120, 17408)]
     ws = [synth.q4k_weight(n, k, seed=4500 + i, quants="normal", device=DEV)
           for i, (n, k) in enumerate(shapes)]
-    xs = [torch.empty((1, k), dtype=torch.bfloat16, device=DEV) for _, k in shapes]
-    ys = [torch.empty((1, n), dtype=torch.float32, device=DEV) for n, _ in shapes]
+    xs = [torch.empty((batch, k), dtype=torch.bfloat16, device=DEV) for _, k in shapes]
+    ys = [torch.empty((batch, n), dtype=torch.float32, device=DEV) for n, _ in shapes]
     ops = q4k.gemv_ops([(w, n, k, x, y) for w, (n, k), x, y in zip(ws, shapes, xs, ys)])
     stream = torch.cuda.Stream(device=DEV)
     for x in xs:
         x.normal_()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        q4k.q4k_gemv_seq(ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)  # warm-up
+        q4k.q4k_gemv_seq(ops, batch, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)  # warm-up
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        q4k.q4k_gemv_seq(ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
+        q4k.q4k_gemv_seq(ops, batch, q4k.Q4K_FLAG_OVERLAP_WEIGHTS, stream=stream)
     rng = np.random.default_rng(4600)
     for rep in range(2):
         for i, x in enumerate(xs):
@@ -222,7 +226,7 @@ def test_gemv_overlap_chain_reads_the_previous_output(q4k):
     check_bound(y2.cpu().numpy(), yref2, s2, TOL, "chain second")
 
 
-@pytest.mark.parametrize("batch", [1, 5, 16])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 16])
 def test_gemv_strided_x_and_y(q4k, batch):
     n, k = 77, 1024
     w = synth.q4k_weight(n, k, seed=3)
@@ -276,7 +280,7 @@ def test_gemv_unit_vectors_pick_columns(q4k):
     assert np.allclose(y1[0], wq[:, cols[3]], rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (6, 0)])
+@pytest.mark.parametrize("batch,flags", [(1, 0), (1, 1), (3, 1), (6, 0)])
 def test_gemv_homogeneous_and_deterministic_bitwise(q4k, batch, flags):
     n, k = 300, 2048
     w = synth.q4k_weight(n, k, seed=14).to(DEV)

@@ -81,7 +81,7 @@ def _gemv(q4k, w, n, k, x, flags=0):
     return y.cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("batch", [1, 4, 16])
+@pytest.mark.parametrize("batch", [1, 2, 4, 16])
 @pytest.mark.parametrize("k", [256, 1280, 5120])
 def test_cancelling_rows_give_exact_zero(q4k, batch, k):
     w = _cancel_matrix(k, seed=k + batch)
@@ -94,7 +94,7 @@ def test_cancelling_rows_give_exact_zero(q4k, batch, k):
     check_bound(y, yref, s, TOL, f"cancel k{k} b{batch}")
 
 
-@pytest.mark.parametrize("batch", [1, 16])
+@pytest.mark.parametrize("batch", [1, 3, 16])
 def test_cancelling_gate_rows_give_exact_zero_through_glu(q4k, batch):
     k = 1280
     wg = _cancel_matrix(k, seed=91)
@@ -133,7 +133,7 @@ def _bf16_from(values: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(values.astype(np.float32)).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("batch", [1, 4, 16])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 16])
 def test_huge_activation_at_a_zero_weight(q4k, batch):
     k, n, pos = 1024, 40, 300
     w = _zero_weight_at(k, n, pos, seed=11)
@@ -147,7 +147,7 @@ def test_huge_activation_at_a_zero_weight(q4k, batch):
     check_bound(y, yref, s, TOL, f"huge at zero weight b{batch}")
 
 
-@pytest.mark.parametrize("batch", [1, 4, 16])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 16])
 def test_activations_spanning_2e_minus60_to_2e60(q4k, batch):
     k, n = 2048, 64
     w = synth.q4k_weight(n, k, seed=13, quants="normal")
