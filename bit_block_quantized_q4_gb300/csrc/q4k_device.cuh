@@ -188,26 +188,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, err);
 }
-// The same wait for a warp that has nothing else to do meanwhile: between
-// polls it sleeps (32 ns, doubling up to max_ns), so that it leaves the issue
-// slots of its scheduler to warps that have work.
-static __device__ __noinline__ bool mbar_wait_sleepy_slow(uint64_t *bar, uint32_t parity,
-                                                          unsigned *err, uint32_t max_ns) {
-  const uint64_t t0 = global_ns();
-  uint32_t ns = 32;
-  for (;;) {
-    __nanosleep(ns);
-    if (mbar_try_wait(bar, parity, 0u)) return true;
-    ns = ns < max_ns ? 2 * ns : max_ns;
-    if (global_ns() - t0 > kWaitLimitNs) break;
-  }
-  set_device_error(err, kDevErrTimeout);
-  return false;
+// ----------------------------------------------------------------- cp.async
+// 16-byte copy global -> shared by this thread (both addresses 16-byte
+// aligned), L1 bypassed; the first src_bytes (0..16) bytes come from src, the
+// rest of the 16 are zero-filled.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
 }
-__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t *bar, uint32_t parity, unsigned *err,
-                                                 uint32_t max_ns) {
-  if (mbar_try_wait(bar, parity, 0u)) return true;
-  return mbar_wait_sleepy_slow(bar, parity, err, max_ns);
+// Close this thread's cp.async copies issued so far into a group; wait until
+// at most N of its groups are still in flight (their data is then visible to
+// the thread; other threads see it after a barrier).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 // ----------------------------------------------------------------- TMA

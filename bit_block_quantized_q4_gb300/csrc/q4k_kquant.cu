@@ -193,16 +193,6 @@ struct KqArgs {
   int buf_bytes;  // per row buffer: row bytes + 16, rounded up to 16
 };
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 // Copies row r's bytes [start, start + row bytes) from start rounded down to 16
 // into buf; returns the offset of the row's first byte in buf.

@@ -17,11 +17,13 @@
 // tiles to occupy the GPU).
 //
 // Each warp owns a ring of shared-memory stages: SB super-blocks of each of its
-// 16*MT rows (one bulk copy per row) plus the x of those super-blocks for each
-// of the NB batch rows (512 bytes per super-block and row), all completing on
-// the stage's mbarrier.  The ring runs ahead across tile, part and op
-// boundaries; with programmatic dependent launch the first weight stages are
-// requested before the wait for the previous kernel, x only after it.
+// 16*MT rows plus the x of those super-blocks for each of the NB batch rows
+// (512 bytes per super-block and row), copied by the warp's own lanes in
+// 16-byte cp.async chunks, one cp.async group per stage.  The ring runs ahead
+// across tile, part and op boundaries; with programmatic dependent launch the
+// first weight stages are requested before the wait for the previous kernel, x
+// only after it.  (There is no wait on another agent: a lane waits only for
+// its own copies, cp.async.wait_group.)
 //
 // Contraction (tensor cores, mma.sync m16n8k16 bf16 -> fp32).  Sub-block j of a
 // row is taken in offset form: w = ds (q - c) + e with c the integer nearest to
@@ -61,11 +63,8 @@
 #ifndef Q4K_STREAM_MINB_MT2
 #define Q4K_STREAM_MINB_MT2 4
 #endif
-#ifndef Q4K_STREAM_SB  // super-blocks per stage (one bulk copy of SB * 144 bytes per row)
+#ifndef Q4K_STREAM_SB  // super-blocks per stage (SB * 144 bytes of each row)
 #define Q4K_STREAM_SB 2
-#endif
-#ifndef Q4K_STREAM_SLEEP_NS  // 0: poll the stage barrier; else sleep between polls, up to this many ns
-#define Q4K_STREAM_SLEEP_NS 256
 #endif
 #ifndef Q4K_STREAM_SHIFT_MUL  // 1: nibble shifts as multiply-high (FMA pipe) instead of shifts (ALU)
 #define Q4K_STREAM_SHIFT_MUL 0
@@ -80,9 +79,10 @@
 #define Q4K_STREAM_FORCE_KP 0
 #endif
 // Batch rows 2 and 3..4 (NB = 2, 4): super-blocks per stage, ring stages and
-// resident CTAs per SM the register budget is sized for.  Two super-blocks per
-// stage measured best at both (one: 2.58 / 2.06 TB/s against 3.27 / 2.29 at
-// batch 2 / 4; more stages cost occupancy).
+// resident CTAs per SM the register budget is sized for (measured on the
+// 64-layer pass: batch 2 best at two super-blocks and two stages, 3.87 TB/s
+// against 3.72 at one and three; batch 4 at one and three, 2.89 against 2.69
+// at two and two, where the smaller stages let a third CTA fit per SM).
 #ifndef Q4K_STREAM_SB_NB2
 #define Q4K_STREAM_SB_NB2 2
 #endif
@@ -93,10 +93,10 @@
 #define Q4K_STREAM_MINB_NB2 4
 #endif
 #ifndef Q4K_STREAM_SB_NB4
-#define Q4K_STREAM_SB_NB4 2
+#define Q4K_STREAM_SB_NB4 1
 #endif
 #ifndef Q4K_STREAM_STAGES_NB4
-#define Q4K_STREAM_STAGES_NB4 2
+#define Q4K_STREAM_STAGES_NB4 3
 #endif
 #ifndef Q4K_STREAM_MINB_NB4
 #define Q4K_STREAM_MINB_NB4 3
@@ -133,7 +133,6 @@ struct StreamParams {
   int pre;       // weight stages requested before the dependency wait
   int nstreams;  // tile streams in the grid
   long long total;
-  unsigned *err;
   StreamOp op[NOPS];
 };
 
@@ -157,13 +156,11 @@ struct StreamCfg {
   // super-block from the writes of the next)
   static constexpr int kPermBufs = NB == 1 ? 2 : 1;
   static constexpr int kPermBuf = NB * kPermWords;     // words of one buffer: [batch row][sub-block]
-  // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes |
-  // ring mbarriers
+  // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes
   static constexpr int kOffX = kStages * kWBytes;
   static constexpr int kOffPerm = kOffX + kStages * kXStage;
   static constexpr int kOffZero = kOffPerm + kPermBufs * kPermBuf * 4;
-  static constexpr int kOffBar = kOffZero + 64;
-  static constexpr int kWarpBytes = (kOffBar + kStages * 8 + 127) / 128 * 128;
+  static constexpr int kWarpBytes = (kOffZero + 64 + 127) / 128 * 128;
   static constexpr int kRedBytes = 2 * kWarps * 2 * NB * kRows * 4;  // split-K partials
   static constexpr int kSmem = kWarps * kWarpBytes + kRedBytes;
 };
@@ -177,10 +174,11 @@ struct StreamCfg {
 struct Pos {
   int op, tile, part, sb, kb0, kb1;
   bool valid;
-  const uint8_t *src;
+  const uint8_t *src;   // the tile's first weight row (of this part's matrix)
   const __nv_bfloat16 *xsrc;
   int ldx;
-  uint32_t bytes;
+  int nrows;            // weight rows of the tile
+  long long rstride;    // bytes from one weight row to the next
 };
 
 template <int NOPS>
@@ -228,24 +226,22 @@ __device__ __forceinline__ void next_tile(const StreamParams<NOPS> &p, int rows,
 }
 
 template <int NOPS>
-__device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, int lane, Pos &s) {
+__device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, Pos &s) {
   const StreamOp &o = p.op[s.op];
   const int row0 = s.tile * rows;
-  const int nrows = min(rows, o.n - row0);
-  s.src = lane < nrows
-              ? (s.part ? o.w2 : o.w) + (size_t)(row0 + lane) * o.nsb * kBlockBytes
-              : nullptr;
+  s.nrows = min(rows, o.n - row0);
+  s.rstride = (long long)o.nsb * kBlockBytes;
+  s.src = (s.part ? o.w2 : o.w) + (size_t)row0 * s.rstride;
   s.xsrc = o.x;
   s.ldx = o.ldx;
-  s.bytes = (uint32_t)(nrows * kBlockBytes + kQK * 2 * p.batch);
 }
 
 // Producer walk over the non-empty stages of a stream, for warp kp of KP:
 // moves forward until the position names a stage (skips tiles whose share of
-// super-blocks is empty for this warp) and loads the lane's sources.
+// super-blocks is empty for this warp) and loads the tile's sources.
 template <int NOPS>
 __device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows, long long hi,
-                                        int kp, int lane, Pos &s) {
+                                        int kp, Pos &s) {
   while (s.valid && s.sb >= s.kb1) {
     if (++s.part < p.op[s.op].parts) {
       s.sb = s.kb0;
@@ -257,30 +253,14 @@ __device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows
     krange(p.op[s.op].nsb, kp, p.kp, s.kb0, s.kb1);
     s.sb = s.kb0;
   }
-  if (s.valid) pos_load(p, rows, lane, s);
+  if (s.valid) pos_load(p, rows, s);
 }
 
 template <int SB, int NOPS>
 __device__ __forceinline__ void pos_next(const StreamParams<NOPS> &p, int rows, long long hi,
-                                         int kp, int lane, Pos &s) {
+                                         int kp, Pos &s) {
   if ((s.sb += SB) < s.kb1) return;
-  pos_settle(p, rows, hi, kp, lane, s);
-}
-
-// After a timed-out wait: give the copies still in flight on the ring (slots
-// of stages it .. end-1) the same bounded time to land before the warp moves on
-// or its CTA exits.
-__device__ __noinline__ void drain_ring(uint64_t *bars, int stages, int slot, uint32_t phase,
-                                        int inflight) {
-  const uint64_t t0 = global_ns();
-  for (int j = 0; j < inflight; ++j) {
-    while (!mbar_try_wait(&bars[slot], phase, 1000u))
-      if (global_ns() - t0 > kWaitLimitNs) return;
-    if (++slot == stages) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
+  pos_settle(p, rows, hi, kp, s);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
@@ -323,16 +303,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
   uint8_t *ringx = wreg + C::kOffX;
   uint32_t *perm = reinterpret_cast<uint32_t *>(wreg + C::kOffPerm);
   const uint32_t *zeros = reinterpret_cast<const uint32_t *>(wreg + C::kOffZero);
-  uint64_t *full = reinterpret_cast<uint64_t *>(wreg + C::kOffBar);
   float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * C::kWarpBytes);
 
-  if (lane == 0) {
-    for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-  }
   if (lane < 16) reinterpret_cast<uint32_t *>(wreg + C::kOffZero)[lane] = 0u;
   __syncwarp();
-  const uint64_t policy = l2_evict_first_policy();
 
   // ---- producer: the stream's stages in order, STAGES ahead of the consumer
   Pos pp;
@@ -341,25 +315,40 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
   if (pp.valid) krange(p.op[pp.op].nsb, kp, KP, pp.kb0, pp.kb1);
   else pp.kb0 = pp.kb1 = 0;
   pp.sb = pp.kb0;
-  pos_settle(p, TR, hi, kp, lane, pp);  // the first stage (when there is one)
+  pos_settle(p, TR, hi, kp, pp);  // the first stage (when there is one)
 
   constexpr int SB = C::kSB;
+  // A stage's copies are 16-byte cp.async chunks.  Weights: the LPR lanes
+  // LPR r .. LPR r + LPR - 1 take row r of the tile, lane LPR r + i its chunks
+  // i, i + LPR, ... of the SB super-blocks (with 16-row tiles a lane pair
+  // moves 32 contiguous bytes per instruction); x: lane l takes chunk l of
+  // each (batch row, super-block).  Each lane closes a stage's copies into one
+  // cp.async group, and every ring slot the consumer releases gets one group
+  // (empty when the stream has no further stage), so the oldest stage in
+  // flight is always the group ST - 1 places back.
+  constexpr int LPR = 32 / TR;
+  const int crow = lane / LPR, csub = lane % LPR;
   auto issue_w = [&](int slot, const Pos &s) {
-    const uint32_t cnt = (uint32_t)min(SB, s.kb1 - s.sb);
-    if (lane == 0) mbar_arrive_expect_tx(&full[slot], cnt * s.bytes);
-    __syncwarp();
-    if (s.src)
-      bulk_load_hint(ringw + slot * C::kWBytes + lane * C::kRowBytes,
-                     s.src + (size_t)s.sb * kBlockBytes, cnt * kBlockBytes, &full[slot], policy);
+    const int nch = 9 * min(SB, s.kb1 - s.sb);  // chunks of a row in this stage
+    if (crow < s.nrows) {
+      uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
+      const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * kBlockBytes + csub * 16;
+#pragma unroll
+      for (int j = 0; j < (9 * SB + LPR - 1) / LPR; ++j)
+        if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + 16 * LPR * j);
+    }
   };
-  // x of batch row b goes to [b][0 .. SB) of the stage's x area, one copy per
-  // row from lane 31 - b.
+  // x of batch row b goes to [b][0 .. SB) of the stage's x area.
   auto issue_x = [&](int slot, const Pos &s) {
-    const uint32_t cnt = (uint32_t)min(SB, s.kb1 - s.sb);
-    const int b = 31 - lane;
-    if (b < batch)
-      bulk_load(ringx + slot * C::kXStage + b * (SB * kXBytes),
-                s.xsrc + (size_t)b * s.ldx + (size_t)s.sb * kQK, cnt * kXBytes, &full[slot]);
+    const int cnt = min(SB, s.kb1 - s.sb);
+    uint8_t *dst = ringx + slot * C::kXStage + lane * 16;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int u = 0; u < SB; ++u)
+        if (b < batch && u < cnt)
+          cp_async16(dst + (b * SB + u) * kXBytes,
+                     s.xsrc + (size_t)b * s.ldx + (size_t)(s.sb + u) * kQK + lane * 8);
   };
 
   // With programmatic dependent launch the first p.pre stages' weights go out
@@ -370,16 +359,17 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
     Pos q = pp;
     for (; npre < p.pre && npre < ST && q.valid; ++npre) {
       issue_w(npre, q);
-      pos_next<SB>(p, TR, hi, kp, lane, q);
+      pos_next<SB>(p, TR, hi, kp, q);
     }
   }
   grid_dependency_wait();
-  int inflight = 0;  // stages issued and not yet consumed
-  for (int s = 0; s < ST && pp.valid; ++s) {
-    if (s >= npre) issue_w(s, pp);
-    issue_x(s, pp);
-    pos_next<SB>(p, TR, hi, kp, lane, pp);
-    ++inflight;
+  for (int s = 0; s < ST; ++s) {
+    if (pp.valid) {
+      if (s >= npre) issue_w(s, pp);
+      issue_x(s, pp);
+      pos_next<SB>(p, TR, hi, kp, pp);
+    }
+    cp_async_commit();  // stage s (an empty group past the stream's end)
   }
   grid_launch_dependents();
 
@@ -410,9 +400,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
 
   // ---- consumer
   int cslot = 0;
-  uint32_t phase = 0;
   int pbuf = 0;
-  bool ok = true;
   int op, tile;
   bool tvalid;
   first_tile(p, TR, lo, hi, op, tile, tvalid);
@@ -436,18 +424,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int b = 0; b < NB; ++b) yacc[mt][0][b] = yacc[mt][1][b] = 0.f;
-      for (int sb = kb0; sb < kb1 && ok; sb += SB) {
-#if Q4K_STREAM_SLEEP_NS
-        const bool landed = mbar_wait_sleepy(&full[cslot], phase, p.err, Q4K_STREAM_SLEEP_NS);
-#else
-        const bool landed = mbar_wait(&full[cslot], phase, p.err);
-#endif
-        if (!landed) {
-          ok = false;
-          if (lane == 0) drain_ring(full, ST, cslot, phase, inflight);
-          __syncwarp();
-          break;
-        }
+      for (int sb = kb0; sb < kb1; sb += SB) {
+        cp_async_wait<ST - 1>();  // this lane's copies of the stage have landed
+        __syncwarp();             // ... and every lane's are visible
         const int cnt = min(SB, kb1 - sb);
         const uint8_t *wstage = ringw + cslot * C::kWBytes;
         const uint8_t *xstage = ringx + cslot * C::kXStage;
@@ -488,13 +467,12 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
             }
           __syncwarp();  // permuted x visible to every lane; the stage's last reads done
           if (u == cnt - 1) {
-            --inflight;
             if (pp.valid) {  // refill this slot with the stream's next stage
               issue_w(cslot, pp);
               issue_x(cslot, pp);
-              pos_next<SB>(p, TR, hi, kp, lane, pp);
-              ++inflight;
+              pos_next<SB>(p, TR, hi, kp, pp);
             }
+            cp_async_commit();
           }
 
           // Offset form of this thread's (row, sub-block) pairs.
@@ -585,10 +563,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
               }
           if (C::kPermBufs == 2) pbuf ^= 1;
         }
-        if (++cslot == ST) {
-          cslot = 0;
-          phase ^= 1u;
-        }
+        if (++cslot == ST) cslot = 0;
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -614,7 +589,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
           }
     const int row0 = tile * TR;
     if (KP == 1) {
-      if (ok && t == 0) {
+      if (t == 0) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -634,7 +609,6 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
       // A warp's partials: [part][batch row][row of the tile].
       float *rb = red + ((size_t)(par * kWarps + warp) * 2 * NB) * TR;
       if (t == 0) {
-        const float nanv = __int_as_float(0x7fc00000);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -642,8 +616,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
               const int rr = mt * 16 + g + 8 * r;
-              rb[b * TR + rr] = ok ? yv[0][mt][r][b] : nanv;
-              rb[(NB + b) * TR + rr] = ok ? yv[1][mt][r][b] : nanv;
+              rb[b * TR + rr] = yv[0][mt][r][b];
+              rb[(NB + b) * TR + rr] = yv[1][mt][r][b];
             }
       }
       asm volatile("bar.sync %0, %1;\n" ::"r"(1 + sic), "r"(32 * KP) : "memory");
@@ -663,8 +637,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
       }
     }
   }
-  // A warp that gave up on a wait has let its copies land (drain_ring); a warp
-  // that finished normally has consumed every stage it issued.
+  // Every stage the warp issued was consumed; nothing is left in flight.
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- host side
@@ -767,7 +741,6 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
   prm.pre = overlap ? Q4K_STREAM_PRE : 0;
   prm.nstreams = grid * (kWarps / kp);
   prm.total = total;
-  prm.err = device_error_word();
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
