@@ -42,7 +42,10 @@ namespace {
 
 constexpr int kRows = 16;                    // rows per CTA (one MMA m-tile)
 constexpr int kTile = kRows * kBlockBytes;   // 2304 bytes per super-block stage
-constexpr int kStagesMoe = 4;
+#ifndef Q4K_MOE_STAGES  // ring stages per warp stream
+#define Q4K_MOE_STAGES 3
+#endif
+constexpr int kStagesMoe = Q4K_MOE_STAGES;
 constexpr int kMoeWarps = 4;                 // warps (weight streams) per expert CTA
 constexpr int kMaxExperts = 2048;
 #ifndef Q4K_MOE_SLOT_PAIRS  // pairs per work slot at most
@@ -56,7 +59,13 @@ constexpr int kSlotPairs = Q4K_MOE_SLOT_PAIRS;
 // barriers; TMA destinations must be 128-byte aligned, so the region is
 // rounded up.
 constexpr int kStageStride = 2 * kTile;
-constexpr int kWarpBytes = (kStagesMoe * kStageStride + 8 * kStagesMoe + 127) / 128 * 128;
+// After the ring and its barriers: the permuted x (or h) of the two columns of
+// a small slot (expert_body_pair) and 64 zero bytes.
+constexpr int kPermStrideMoe = 20;                     // words per sub-block (16 used)
+constexpr int kPermWordsMoe = 8 * kPermStrideMoe + 4;  // one column; +4 staggers the banks
+constexpr int kOffPermMoe = (kStagesMoe * kStageStride + 8 * kStagesMoe + 15) / 16 * 16;
+constexpr int kOffZeroMoe = kOffPermMoe + 2 * kPermWordsMoe * 4;
+constexpr int kWarpBytes = (kOffZeroMoe + 64 + 127) / 128 * 128;
 constexpr int kMetaAbort = 2;  // workspace meta word: a wait timed out, stop taking items
 constexpr int kGuTilesPerItem = 4;  // 16-row tiles of ffn per gate/up item (one per warp)
 constexpr int kDnTilesPerItem = 8;  // 16-row tiles of hidden per down item (two per warp)
@@ -484,6 +493,276 @@ __device__ __forceinline__ bool expert_body(const CUtensorMap *map0p, const CUte
   return ok;
 }
 
+// A slot whose MMA columns fit one pair (gate/up: at most 2 pairs; down: one
+// pair, its h_hi and h_lo columns) takes the contraction of the batch-1..4
+// decode stream kernel instead: thread t's k-slots carry sub-block 2t (low
+// nibbles, the "E" MMAs) or 2t+1 (high nibbles, "O") of rows g, g+8, and MMA
+// column 2s + c holds column c's x (or h) only in the k-slots of thread s.
+// So each thread ends with the sums of its own sub-blocks for both columns and
+// applies the offset forms it decoded itself: no shuffles, 16 MMAs per
+// super-block and matrix, and the scale epilogue once per super-block.
+// X_j of each column: two MMAs with A = 1 per super-block.  The B fragments
+// come from a per-warp permuted copy of the super-block's x (h is stored in
+// that order already).  Same ring, item and result conventions as expert_body.
+template <bool DOWN>
+__device__ __forceinline__ bool expert_body_pair(const CUtensorMap *map0p, const CUtensorMap *map1p,
+                                                 const MoeArgs &a, int nsb, int rows_total,
+                                                 uint8_t *ring, uint64_t *bars, uint32_t &it0,
+                                                 int slot, int sid, int nsid, int tile_end) {
+  const CUtensorMap &map0 = *map0p, &map1 = *map1p;
+  constexpr int NM = DOWN ? 1 : 2;  // weight matrices per stage (gate and up)
+  constexpr int kStageBytes = NM * kTile;
+  const int expert = a.slot_expert[slot];
+  const int pstart = a.slot_start[slot];
+  const int np = a.slot_start[slot + 1] - pstart;  // pairs of this slot
+  const int ncols = DOWN ? 2 * np : np;             // 1 or 2
+
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int ntiles = min((rows_total + kRows - 1) / kRows, tile_end);
+  const int ntl = sid < ntiles ? (ntiles - sid + nsid - 1) / nsid : 0;  // tiles of this warp
+  const int total = ntl * nsb;                                          // ring iterations
+  const uint32_t base = it0;
+  const uint64_t policy = l2_evict_first_policy();
+  uint32_t *perm = reinterpret_cast<uint32_t *>(ring + kOffPermMoe);
+  const uint32_t *zeros = reinterpret_cast<const uint32_t *>(ring + kOffZeroMoe);
+  auto issue = [&](int q) {
+    const int j = q / nsb, u = q - j * nsb;
+    const int row0 = (sid + j * nsid) * kRows;
+    const uint32_t stage = (base + (uint32_t)q) % kStagesMoe;
+    mbar_arrive_expect_tx(&bars[stage], kStageBytes);
+    uint8_t *dst = ring + stage * kStageStride;
+    tma_load_3d_hint(dst, &map0, &bars[stage], u * (kBlockBytes / 8), row0, expert, policy);
+    if (NM == 2)
+      tma_load_3d_hint(dst + kTile, &map1, &bars[stage], u * (kBlockBytes / 8), row0, expert,
+                       policy);
+  };
+  if (lane == 0)
+    for (int q = 0; q < kStagesMoe && q < total; ++q) issue(q);
+
+  // Column c's source rows: gate/up the x row of pair c's token, down h_hi
+  // (c = 0) and h_lo (c = 1) of the pair.
+  const __nv_bfloat16 *src[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int cc = c < ncols ? c : 0;
+    if (DOWN)
+      src[c] = (cc ? a.h_lo : a.h_hi) + (size_t)pstart * a.ffn;
+    else
+      src[c] = a.x + (int64_t)a.pair_token[pstart + cc] * a.ldx;
+  }
+  // This lane's 16 bytes of super-block q of each column: values 8t .. 8t+7
+  // of sub-block g (of h: the same values, permuted within groups of four),
+  // loaded one super-block ahead of their use.
+  auto load_raw = [&](uint4(&dst)[2], int q) {
+    const int u = q % nsb;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 *ptr = reinterpret_cast<const uint4 *>(src[c] + (int64_t)u * kQK + 32 * g + 8 * t);
+      // h is written by this kernel's gate/up items: read it through L2
+      dst[c] = (c < ncols && q < total) ? (DOWN ? __ldcg(ptr) : __ldg(ptr)) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 raw[2];
+  load_raw(raw, 0);
+
+  // Scale/min decode of sub-blocks 2t, 2t+1 of rows g, g+8 (see the stream
+  // kernel): psel gathers bytes k0, k0+1 of rows g (bytes 0, 1) and g+8 (2, 3).
+  const bool upper = t >= 2;
+  const uint32_t k0 = 2 * (t & 1);
+  const uint32_t psel = k0 | ((k0 + 1) << 4) | ((k0 + 4) << 8) | ((k0 + 5) << 12);
+  const uint32_t mlo4 = upper ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+  const uint32_t mhi4 = upper ? 0x30303030u : 0u;
+  // B fragments: lane (g, t) is column g; when t == g / 2 its k-slots carry
+  // column g & 1 (sub-block 2t in the E MMAs, 2t+1 in the O MMAs).
+  const int col = g & 1;
+  const int bofs = (t == (g >> 1) && col < ncols) ? col * kPermWordsMoe + 2 * t * kPermStrideMoe : -1;
+  const uint32_t *pe = bofs >= 0 ? perm + bofs : zeros;
+  const uint32_t *po = bofs >= 0 ? perm + bofs + kPermStrideMoe : zeros;
+  uint32_t magic;
+  asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kBf16Magic));
+
+  bool ok = true;
+  for (int j = 0; j < ntl; ++j) {
+    const int row0 = (sid + j * nsid) * kRows;
+    float yacc[NM][2][2];  // [matrix][row g, g+8][column], over sub-blocks 2t, 2t+1
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+      yacc[mi][0][0] = yacc[mi][0][1] = yacc[mi][1][0] = yacc[mi][1][1] = 0.f;
+    for (int u = 0; u < nsb && ok; ++u) {
+      const int q = j * nsb + u;
+      const uint32_t gq = base + (uint32_t)q;
+      const uint32_t stage = gq % kStagesMoe;
+      if (!mbar_wait(&bars[stage], (gq / kStagesMoe) & 1u, a.err)) {
+        ok = false;
+        if (lane == 0) {
+          atomicExch(&a.meta[kMetaAbort], 1);  // every CTA stops taking items
+          // let this warp's copies in flight land (bounded)
+          const uint64_t t0 = global_ns();
+          for (int r = q; r < min(q + kStagesMoe, total); ++r) {
+            const uint32_t gr = base + (uint32_t)r;
+            while (!mbar_try_wait(&bars[gr % kStagesMoe], (gr / kStagesMoe) & 1u, 1000u))
+              if (global_ns() - t0 > kWaitLimitNs) break;
+          }
+        }
+        break;
+      }
+      const uint8_t *st = ring + stage * kStageStride;
+      __syncwarp();  // the previous super-block's B-fragment reads are done
+      // X_j of the eight sub-blocks of each column (A = 1; lane (g, t) holds
+      // eight values of sub-block g, the B fragment of column g), and the
+      // permuted copy: word 2G of a sub-block holds (x[4G], x[4G+2]), word
+      // 2G+1 (x[4G+1], x[4G+3]).
+      float xs[2][4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint4 v = raw[c];
+        mma_bf16_zc(xs[c], kBf16One, kBf16One, kBf16One, kBf16One, v.x, v.y);
+        mma_bf16(xs[c], kBf16One, kBf16One, kBf16One, kBf16One, v.z, v.w);
+        uint4 pm = v;
+        if (!DOWN) {
+          pm.x = __byte_perm(v.x, v.y, 0x5410u);
+          pm.y = __byte_perm(v.x, v.y, 0x7632u);
+          pm.z = __byte_perm(v.z, v.w, 0x5410u);
+          pm.w = __byte_perm(v.z, v.w, 0x7632u);
+        }
+        reinterpret_cast<uint4 *>(perm + c * kPermWordsMoe + g * kPermStrideMoe)[t] = pm;
+      }
+      uint4 hdr[NM][2], qa[NM][2][2];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint8_t *rp = st + mi * kTile + (g + 8 * r) * kBlockBytes;
+          hdr[mi][r] = *reinterpret_cast<const uint4 *>(rp);
+          qa[mi][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
+          qa[mi][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
+        }
+      __syncwarp();  // permuted copy visible; the stage's reads are done
+      if (lane == 0 && q + kStagesMoe < total) issue(q + kStagesMoe);
+      load_raw(raw, q + 1);
+
+      float ds[NM][2][2], ee[NM][2][2];
+      uint32_t sub[NM][2][2];
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi) {
+        const uint4 h0 = hdr[mi][0], h1 = hdr[mi][1];
+        const uint32_t py = __byte_perm(h0.y, h1.y, psel);
+        const uint32_t pz = __byte_perm(h0.z, h1.z, psel);
+        const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
+        const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
+        const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t hx = r ? h1.x : h0.x;
+          const float d = half_lo_to_float(hx), dmin = half_hi_to_float(hx);
+          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            offset_form(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e), byte_magic(m4, 2 * r + e),
+                        ds[mi][r][e], ee[mi][r][e], sub[mi][r][e]);
+        }
+      }
+      // accE[mi] column 2t + c = sum (q - c_j) x over sub-block 2t of column c
+      // (rows g: [c], g+8: [2 + c]); accO likewise for 2t+1.
+      float accE[NM][4], accO[NM][4];
+#pragma unroll
+      for (int G2 = 0; G2 < 4; ++G2) {
+        const uint4 be = reinterpret_cast<const uint4 *>(pe)[G2];  // the zero block is 4 uint4
+        const uint4 bo = reinterpret_cast<const uint4 *>(po)[G2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int G = 2 * G2 + h;
+          const uint32_t be0 = h ? be.z : be.x, be1 = h ? be.w : be.y;
+          const uint32_t bo0 = h ? bo.z : bo.x, bo1 = h ? bo.w : bo.y;
+#pragma unroll
+          for (int mi = 0; mi < NM; ++mi) {
+            const uint4 qv0 = qa[mi][0][G >> 2], qv1 = qa[mi][1][G >> 2];
+            const uint32_t w0 = (G & 3) == 0 ? qv0.x : (G & 3) == 1 ? qv0.y : (G & 3) == 2 ? qv0.z : qv0.w;
+            const uint32_t w1 = (G & 3) == 0 ? qv1.x : (G & 3) == 1 ? qv1.y : (G & 3) == 2 ? qv1.z : qv1.w;
+            // low nibbles: sub-block 2t, positions (4G, 4G+2) and (4G+1, 4G+3)
+            const uint32_t a0 = sub_bf16x2(lop_nib(w0, magic), sub[mi][0][0]);
+            const uint32_t a1 = sub_bf16x2(lop_nib(w1, magic), sub[mi][1][0]);
+            const uint32_t a2 = sub_bf16x2(lop_nib(w0 >> 8, magic), sub[mi][0][0]);
+            const uint32_t a3 = sub_bf16x2(lop_nib(w1 >> 8, magic), sub[mi][1][0]);
+            // high nibbles: sub-block 2t+1
+            const uint32_t c0 = sub_bf16x2(lop_nib(w0 >> 4, magic), sub[mi][0][1]);
+            const uint32_t c1 = sub_bf16x2(lop_nib(w1 >> 4, magic), sub[mi][1][1]);
+            const uint32_t c2 = sub_bf16x2(lop_nib(w0 >> 12, magic), sub[mi][0][1]);
+            const uint32_t c3 = sub_bf16x2(lop_nib(w1 >> 12, magic), sub[mi][1][1]);
+            if (G == 0) {
+              mma_bf16_zc(accE[mi], a0, a1, a2, a3, be0, be1);
+              mma_bf16_zc(accO[mi], c0, c1, c2, c3, bo0, bo1);
+            } else {
+              mma_bf16(accE[mi], a0, a1, a2, a3, be0, be1);
+              mma_bf16(accO[mi], c0, c1, c2, c3, bo0, bo1);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float v = yacc[mi][r][c];
+            v = fmaf(ds[mi][r][0], accE[mi][2 * r + c], v);
+            v = fmaf(ee[mi][r][0], xs[c][0], v);
+            v = fmaf(ds[mi][r][1], accO[mi][2 * r + c], v);
+            v = fmaf(ee[mi][r][1], xs[c][1], v);
+            yacc[mi][r][c] = v;
+          }
+    }
+    // Rows: add the quad's sub-block pairs (t = 0..3), then lanes t == 0
+    // write rows g, g+8.  After a timed-out wait the warp's remaining rows
+    // read NaN.
+#pragma unroll
+    for (int mi = 0; mi < NM; ++mi)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v = yacc[mi][r][c];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          yacc[mi][r][c] = v;
+        }
+    const float nan = __int_as_float(0x7fc00000);
+    if (t == 0) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int grow = row0 + g + 8 * r;
+        if (grow >= rows_total) continue;
+        if (DOWN) {
+          a.p[(size_t)pstart * a.hidden + grow] = ok ? yacc[0][r][0] + yacc[0][r][1] : nan;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            if (c >= np) continue;
+            const float gg = yacc[0][r][c], uu = yacc[NM - 1][r][c];
+            const float hv = ok ? gg / (1.f + __expf(-gg)) * uu : nan;
+            // the down projection's input: h, or r h in the weighted-down order
+            const float hd = a.weighted_down ? hv * a.wts[a.pair_q[pstart + c]] : hv;
+            const __nv_bfloat16 hh = __float2bfloat16_rn(hd);
+            const __nv_bfloat16 hl = __float2bfloat16_rn(hd - __bfloat162float(hh));
+            // h_hi / h_lo in B-fragment order (positions 1 and 2 of each group
+            // of four swapped)
+            const int pos = (grow & ~3) | ((grow & 1) << 1) | ((grow >> 1) & 1);
+            a.g[(size_t)(pstart + c) * a.ffn + grow] = ok ? gg : nan;
+            a.u[(size_t)(pstart + c) * a.ffn + grow] = ok ? uu : nan;
+            a.h[(size_t)(pstart + c) * a.ffn + grow] = hv;
+            a.h_hi[(size_t)(pstart + c) * a.ffn + pos] = hh;
+            a.h_lo[(size_t)(pstart + c) * a.ffn + pos] = hl;
+          }
+        }
+      }
+    }
+  }
+  it0 = base + (uint32_t)total;
+  return ok;
+}
+
 // One slot's share of an item: the MMA width follows the slot's pair count
 // (8 columns when its pairs fit, else 16 or 32, NTMAX n-tiles of 8 at most),
 // so a slot with few pairs does no work for empty columns.  Warp w of the CTA
@@ -497,6 +776,9 @@ __device__ __forceinline__ bool slot_item(const CUtensorMap *m0, const CUtensorM
   const int ncols = DOWN ? 2 * np : np;
   const int nt = ncols <= 8 ? 1 : ncols <= 16 ? 2 : 4;  // n-tiles this slot needs
   const int sid = t0 + (int)(threadIdx.x >> 5);
+  if (ncols <= 2)
+    return expert_body_pair<DOWN>(m0, m1, a, nsb, rows, ring, bars, it, slot, sid, kMoeWarps,
+                                  t0 + per_item);
   if (nt == 1 || NTMAX == 1)
     return expert_body<1, DOWN>(m0, m1, a, nsb, rows, ring, bars, it, slot, sid, kMoeWarps,
                                 t0 + per_item);
@@ -552,6 +834,7 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
     for (int s = 0; s < kStagesMoe; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
+  if (lane < 16) reinterpret_cast<uint32_t *>(ring + kOffZeroMoe)[lane] = 0u;
   if (threadIdx.x == 0) s_fail = 0;
   __syncthreads();
   uint32_t it = 0;  // this warp's ring iterations so far
