@@ -200,16 +200,17 @@ bool stream_batch(int64_t batch, int64_t ldx, int64_t ldy) {
 int64_t stream_stride(int64_t batch, int64_t ld) { return batch == 1 ? 0 : ld; }
 
 // One projection (plain, or fused gate/up when w_up is set) after its
-// arguments were checked: batch 1..4 runs in the stream kernel, 5..16 in the
-// batched kernel.
+// arguments were checked: batch 1..4 runs in the stream kernel; 5..16 in the
+// 64-row tile kernel when the op has enough tiles to occupy the GPU, else in
+// the per-op batched kernel.
 int run_gemv(const void *w, const void *w_up, int64_t n, int64_t k, const void *x, int64_t batch,
              int64_t ldx, float *y, int64_t ldy, uint32_t flags, void *stream) {
   const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (stream_batch(batch, ldx, ldy)) {
-    const StreamOpDesc d = {w, w_up, x, y, n, k, stream_stride(batch, ldx), stream_stride(batch, ldy)};
-    return map_launch(launch_stream(&d, 1, (int)batch, overlap, s));
-  }
+  const StreamOpDesc d = {w, w_up, x, y, n, k, stream_stride(batch, ldx), stream_stride(batch, ldy)};
+  if (stream_batch(batch, ldx, ldy)) return map_launch(launch_stream(&d, 1, (int)batch, overlap, s));
+  if (ldx <= INT32_MAX && ldy <= INT32_MAX && wide_worth_it(&d, 1, (int)batch))
+    return map_launch(launch_wide(&d, 1, (int)batch, overlap, s));
   return map_launch(launch_gemv(w, w_up, n, k, x, batch, ldx, y, ldy, overlap, s));
 }
 }  // namespace
@@ -269,10 +270,10 @@ int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t 
     if (st != Q4K_OK) return st;
   }
   const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
-  bool one_launch = batch <= stream_max_batch();
-  for (int64_t i = 0; i < count && one_launch; ++i)
-    one_launch = ops[i].n == 0 || stream_batch(batch, ops[i].ldx, ops[i].ldy);
-  if (one_launch) {  // one persistent launch streams every op's weights back to back
+  bool strides32 = true;
+  for (int64_t i = 0; i < count; ++i)
+    strides32 = strides32 && (ops[i].n == 0 || (ops[i].ldx <= INT32_MAX && ops[i].ldy <= INT32_MAX));
+  if (strides32 || batch == 1) {
     std::vector<StreamOpDesc> d;
     d.reserve((size_t)count);
     for (int64_t i = 0; i < count; ++i) {
@@ -280,8 +281,13 @@ int q4k_gemv_seq(const q4k_gemv_op *ops, int64_t count, int64_t batch, uint32_t 
       d.push_back(StreamOpDesc{o.w, o.w_up, o.x, o.y, o.n, o.k, stream_stride(batch, o.ldx),
                                stream_stride(batch, o.ldy)});
     }
-    return map_launch(
-        launch_stream(d.data(), count, (int)batch, overlap, static_cast<cudaStream_t>(stream)));
+    // one persistent launch streams every op's weights back to back
+    if (batch <= stream_max_batch())
+      return map_launch(
+          launch_stream(d.data(), count, (int)batch, overlap, static_cast<cudaStream_t>(stream)));
+    if (wide_worth_it(d.data(), count, (int)batch))
+      return map_launch(
+          launch_wide(d.data(), count, (int)batch, overlap, static_cast<cudaStream_t>(stream)));
   }
   for (int64_t i = 0; i < count; ++i) {
     const q4k_gemv_op &o = ops[i];

@@ -57,6 +57,11 @@ struct StreamOpDesc {
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream);
 int stream_max_batch();
+// Batch 5..16 as one persistent launch of 64-row tiles (q4k_wide.cu), for
+// lists of ops with enough tiles to occupy the GPU (wide_worth_it).
+bool wide_worth_it(const StreamOpDesc *ops, int64_t count, int batch);
+cudaError_t launch_wide(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
+                        cudaStream_t stream);
 cudaError_t launch_gemm(const void *w, int64_t n, int64_t k, const void *x, int64_t m, int64_t ldx,
                         void *y, int64_t ldy, cudaStream_t stream);
 // Grouped expert GEMM (routed-MoE prefill): for each work slot s < meta[0],

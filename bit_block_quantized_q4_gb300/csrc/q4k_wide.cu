@@ -1,0 +1,510 @@
+// q4k_wide.cu -- decode projections Y[b] = W X[b] with W in Q4_K for batch
+// 5..16, any number of them in one persistent launch ("PRD: Performant
+// Concurrent Distributed GGUF Runtime", DGR-012: batched decode steps; "spec:
+// specialized model runtimes", section "Architecture": the T0 GEMM), and the
+// fused gate/up projection H[b] = silu(Wg X[b]) * (Wu X[b]) ("Layer Package
+// Repository Spec", section "Policy Resolution": merged gate/up).
+//
+// Work: a tile is 64 weight rows of one op over the op's whole K (a gate/up
+// op's tile is its gate rows, then the same up rows).  The tiles of all ops of
+// a launch form one list; each CTA takes a contiguous run of it, balanced by
+// weight bytes, so a sequence of projections streams its weights back to back.
+//
+// The four warps of a CTA consume the same stages in lockstep: a stage is SB
+// super-blocks of the tile's 64 rows plus the x of those super-blocks for the
+// 8*NT batch rows, copied by all 128 threads in 16-byte cp.async chunks (one
+// cp.async group per thread and stage) and released by a CTA barrier.  So the
+// x of a super-block is read from L2 once per 64 rows and the warps hold no x
+// in registers between super-blocks.  Warp w contracts rows 16w .. 16w+15.
+//
+// Contraction (mma.sync m16n8k16 bf16 -> fp32), as in the per-op batched
+// kernel: the MMA columns are the batch rows (NT n-tiles of 8); sub-block j of
+// a row is taken in offset form (offset_form) and accumulated by two MMAs on
+// the exact small integers q - c; per (row, sub-block, column) the thread adds
+// ds * acc + e * X_j, X_j the column's sum of x over the sub-block (two MMAs
+// with A = 1).  Lane (g, t) decodes the offset forms of sub-blocks 2t, 2t+1 of
+// its rows g, g+8; the other lanes of its quad fetch them by shuffle.  Every
+// sum is taken in a fixed order: the result does not depend on timing.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+#ifndef Q4K_WIDE_SB_NT1  // super-blocks per stage, batch 5..8
+#define Q4K_WIDE_SB_NT1 1
+#endif
+#ifndef Q4K_WIDE_STAGES_NT1
+#define Q4K_WIDE_STAGES_NT1 3
+#endif
+#ifndef Q4K_WIDE_SB_NT2  // batch 9..16
+#define Q4K_WIDE_SB_NT2 1
+#endif
+#ifndef Q4K_WIDE_STAGES_NT2
+#define Q4K_WIDE_STAGES_NT2 3
+#endif
+#ifndef Q4K_WIDE_MINB  // resident CTAs per SM the register budget is sized for
+#define Q4K_WIDE_MINB 4
+#endif
+#ifndef Q4K_WIDE_PRE  // weight stages requested before the dependency wait (PDL)
+#define Q4K_WIDE_PRE 2
+#endif
+
+namespace q4k {
+
+namespace {
+
+constexpr int kWideWarps = 4;
+constexpr int kWideThreads = kWideWarps * 32;
+constexpr int kWideRows = 16 * kWideWarps;  // rows per tile
+constexpr int kWideMaxOps = 448;            // ops per launch (kernel parameter table)
+// x rows in a stage: 512 bytes of a super-block plus 64 bytes, so that the
+// 16-byte fragment reads of 8 batch rows by a quarter warp hit distinct banks.
+constexpr int kXRowBytes = 576;
+
+template <int NT>
+struct WideCfg {
+  static constexpr int kNB = 8 * NT;  // batch rows the kernel carries
+  static constexpr int kSB = NT == 1 ? Q4K_WIDE_SB_NT1 : Q4K_WIDE_SB_NT2;
+  static constexpr int kStages = NT == 1 ? Q4K_WIDE_STAGES_NT1 : Q4K_WIDE_STAGES_NT2;
+  // a row's slot in a stage: its kSB super-blocks, padded by 16 bytes when kSB
+  // is even so that rows fall on different banks
+  static constexpr int kRowBytes = kSB * kBlockBytes + (kSB % 2 == 0 ? 16 : 0);
+  static constexpr int kWBytes = kWideRows * kRowBytes;
+  static constexpr int kXBytes = kSB * kNB * kXRowBytes;  // [super-block][batch row][576]
+  static constexpr int kStageBytes = kWBytes + kXBytes;
+  static constexpr int kSmem = kStages * kStageBytes;
+};
+
+struct WideOp {
+  const uint8_t *w;   // weights; the gate matrix of a gate/up op
+  const uint8_t *w2;  // up matrix of a gate/up op, nullptr for a plain projection
+  const __nv_bfloat16 *x;
+  float *y;
+  long long byte0;    // weight bytes of the ops before this one
+  int n, nsb, ntiles, parts;
+  int ldx, ldy;       // batch-row strides of x and y (elements)
+};
+
+template <int NOPS>
+struct WideParams {
+  int nops;
+  int batch;
+  int pre;    // weight stages requested before the dependency wait
+  int nctas;  // CTAs of the grid (tile runs)
+  long long total;
+  WideOp op[NOPS];
+};
+
+// Stage walk: super-blocks sb .. sb+SB-1 of part `part` of tile `tile` of op
+// `op`, over the CTA's run of tiles [tiles starting in bytes lo .. hi).
+struct WPos {
+  int op, tile, part, sb;
+  bool valid;
+};
+
+template <int NOPS>
+__device__ __forceinline__ long long wide_tile_start(const WideParams<NOPS> &p, int op, int tile) {
+  const WideOp &o = p.op[op];
+  return o.byte0 + (long long)tile * kWideRows * o.nsb * kBlockBytes * o.parts;
+}
+
+// First tile of a run: the first tile that starts at or after byte lo.
+template <int NOPS>
+__device__ __forceinline__ void wide_first(const WideParams<NOPS> &p, long long lo, long long hi,
+                                           WPos &s) {
+  int a = 0, b = p.nops - 1;
+  while (a < b) {
+    const int m = (a + b + 1) >> 1;
+    if (p.op[m].byte0 <= lo) a = m; else b = m - 1;
+  }
+  s.op = a;
+  const WideOp &o = p.op[a];
+  const long long cost = (long long)kWideRows * o.nsb * kBlockBytes * o.parts;
+  s.tile = lo <= o.byte0 ? 0 : (int)((lo - o.byte0 + cost - 1) / cost);
+  if (s.tile >= o.ntiles) {
+    ++s.op;
+    s.tile = 0;
+  }
+  s.part = 0;
+  s.sb = 0;
+  s.valid = s.op < p.nops && wide_tile_start(p, s.op, s.tile) < hi;
+}
+
+template <int SB, int NOPS>
+__device__ __forceinline__ void wide_next(const WideParams<NOPS> &p, long long hi, WPos &s) {
+  const WideOp &o = p.op[s.op];
+  if ((s.sb += SB) < o.nsb) return;
+  s.sb = 0;
+  if (++s.part < o.parts) return;
+  s.part = 0;
+  if (++s.tile >= o.ntiles) {
+    ++s.op;
+    s.tile = 0;
+  }
+  s.valid = s.op < p.nops && wide_tile_start(p, s.op, s.tile) < hi;
+}
+
+__device__ __forceinline__ float silu_mul_w(float g, float u) {
+  return g / (1.f + __expf(-g)) * u;
+}
+
+template <int NT, int NOPS>
+__global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
+    gemv_wide_kernel(const __grid_constant__ WideParams<NOPS> p) {
+  using C = WideCfg<NT>;
+  constexpr int SB = C::kSB, ST = C::kStages, NB = C::kNB;
+  static_assert(ST >= 2, "the ring needs two stages");
+  static_assert((SB * NB) % kWideWarps == 0, "x rows per warp");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const long long lo = p.total * blockIdx.x / p.nctas, hi = p.total * (blockIdx.x + 1) / p.nctas;
+  const int batch = p.batch;
+
+  // ---- producer: every thread copies its chunks of a stage.  Weights:
+  // threads 2r, 2r+1 take row r (32 contiguous bytes per instruction); x:
+  // warp w takes the (super-block, batch row) blocks w, w+4, ..., lane l
+  // chunk l of each.
+  const int crow = tid >> 1, csub = tid & 1;
+  auto issue_w = [&](int slot, const WPos &s) {
+    const WideOp &o = p.op[s.op];
+    const int row0 = s.tile * kWideRows;
+    const int nrows = min(kWideRows, o.n - row0);
+    const int nch = 9 * min(SB, o.nsb - s.sb);  // chunks of a row in this stage
+    if (crow < nrows) {
+      const uint8_t *src =
+          (s.part ? o.w2 : o.w) + ((size_t)(row0 + crow) * o.nsb + s.sb) * kBlockBytes + csub * 16;
+      uint8_t *dst = smem + slot * C::kStageBytes + crow * C::kRowBytes + csub * 16;
+#pragma unroll
+      for (int j = 0; j < (9 * SB + 1) / 2; ++j)
+        if (2 * j + csub < nch) cp_async16(dst + 32 * j, src + 32 * j);
+    }
+  };
+  auto issue_x = [&](int slot, const WPos &s) {
+    const WideOp &o = p.op[s.op];
+    const int cnt = min(SB, o.nsb - s.sb);
+    uint8_t *dst = smem + slot * C::kStageBytes + C::kWBytes + lane * 16;
+#pragma unroll
+    for (int m = 0; m < SB * NB / kWideWarps; ++m) {
+      const int idx = warp + kWideWarps * m;  // block (super-block u, batch row b)
+      const int u = idx / NB, b = idx % NB;
+      if (b < batch && u < cnt)
+        cp_async16(dst + idx * kXRowBytes,
+                   o.x + (size_t)b * o.ldx + (size_t)(s.sb + u) * kQK + lane * 8);
+    }
+  };
+
+  // Ring: stage i lives in slot i % ST; every thread commits one cp.async
+  // group per stage (empty past the run's end), ST - 1 stages ahead.  With
+  // programmatic dependent launch the first weight stages go out before the
+  // wait for the previous kernel, their x after it.
+  WPos pp;
+  wide_first(p, lo, hi, pp);
+  int npre = 0;
+  {
+    WPos q = pp;
+    for (; npre < p.pre && npre < ST - 1 && q.valid; ++npre) {
+      issue_w(npre, q);
+      wide_next<SB>(p, hi, q);
+    }
+  }
+  grid_dependency_wait();
+  for (int s = 0; s < ST - 1; ++s) {
+    if (pp.valid) {
+      if (s >= npre) issue_w(s, pp);
+      issue_x(s, pp);
+      wide_next<SB>(p, hi, pp);
+    }
+    cp_async_commit();
+  }
+  grid_launch_dependents();
+
+  // ---- consumer
+  bool xval[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) xval[nt] = nt * 8 + g < batch;
+  const int wrow = warp * 16;  // this warp's rows of the tile
+  WPos cs;
+  wide_first(p, lo, hi, cs);
+  int slot = 0;
+  float yacc[NT][4], ygate[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) yacc[nt][e] = ygate[nt][e] = 0.f;
+  while (cs.valid) {
+    const WideOp &o = p.op[cs.op];
+    const int cnt = min(SB, o.nsb - cs.sb);
+    const int tile = cs.tile, part = cs.part;
+    const bool last_of_part = cs.sb + SB >= o.nsb;
+    cp_async_wait<ST - 2>();  // this thread's copies of the stage have landed
+    __syncthreads();          // every thread's have, and the previous stage is consumed
+    {
+      const int rs = slot == 0 ? ST - 1 : slot - 1;  // the slot the previous stage used
+      if (pp.valid) {
+        issue_w(rs, pp);
+        issue_x(rs, pp);
+        wide_next<SB>(p, hi, pp);
+      }
+      cp_async_commit();
+    }
+    const uint8_t *wst = smem + slot * C::kStageBytes;
+    const uint8_t *xst = wst + C::kWBytes;
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      if (u >= cnt) break;
+      // Super-block u of this stage for rows wrow + g, wrow + g + 8.
+      uint4 hdr[2];
+      uint2 qw[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint8_t *rp = wst + (wrow + g + 8 * r) * C::kRowBytes + u * kBlockBytes;
+        hdr[r] = *reinterpret_cast<const uint4 *>(rp);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          qw[r][c] = *reinterpret_cast<const uint2 *>(rp + kQsOffset + 32 * c + 8 * t);
+      }
+      // Offset forms of sub-blocks 2t, 2t+1 (e = 0, 1) of rows g, g+8 (r);
+      // the bf16 subtrahends of both rows travel packed in one word per e.
+      float dsv[2][2], eev[2][2];
+      uint32_t subp[2];
+      {
+        uint32_t sub[2][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          uint32_t sc2, m2;
+          scales_pair(hdr[r].y, hdr[r].z, hdr[r].w, t, &sc2, &m2);
+          const float d = half_lo_to_float(hdr[r].x), dmin = half_hi_to_float(hdr[r].x);
+          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            offset_form(d, nd23, dmin, ndm23, byte_magic(sc2, e), byte_magic(m2, e), dsv[r][e],
+                        eev[r][e], sub[r][e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) subp[e] = __byte_perm(sub[0][e], sub[1][e], 0x5410u);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = j >> 1;
+        const bool hi = j & 1;
+        // B fragments of sub-block j: this lane's 16 bytes (values 8t .. 8t+7)
+        // of batch row nt*8 + g, as (x[o], x[o+2]) and (x[o+1], x[o+3]).
+        uint32_t b0[2][NT], b1[2][NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 v = xval[nt] ? *reinterpret_cast<const uint4 *>(
+                                         xst + (u * NB + nt * 8 + g) * kXRowBytes + 64 * j + 16 * t)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+          b0[0][nt] = __byte_perm(v.x, v.y, 0x5410);
+          b1[0][nt] = __byte_perm(v.x, v.y, 0x7632);
+          b0[1][nt] = __byte_perm(v.z, v.w, 0x5410);
+          b1[1][nt] = __byte_perm(v.z, v.w, 0x7632);
+        }
+        // X_j of every column (A = 1: column 2t+e is xsum[nt][e]).
+        float xsum[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_zc(xsum[nt], kBf16One, kBf16One, kBf16One, kBf16One, b0[0][nt], b1[0][nt]);
+          mma_bf16(xsum[nt], kBf16One, kBf16One, kBf16One, kBf16One, b0[1][nt], b1[1][nt]);
+        }
+        // Offset forms of sub-block j for rows g, g+8 live in lane (g, j/2).
+        const int srcl = (lane & ~3) | (j >> 1);
+        const uint32_t sp = __shfl_sync(0xffffffffu, hi ? subp[1] : subp[0], srcl);
+        const uint32_t sg = __byte_perm(sp, 0u, 0x1010u), sg8 = __byte_perm(sp, 0u, 0x3232u);
+        float acc[NT][4];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const uint32_t w0 = s ? qw[0][c].y : qw[0][c].x;
+          const uint32_t w1 = s ? qw[1][c].y : qw[1][c].x;
+          const uint32_t a0 = sub_bf16x2(hi ? nib_hi(w0) : nib_lo(w0), sg);
+          const uint32_t a1 = sub_bf16x2(hi ? nib_hi(w1) : nib_lo(w1), sg8);
+          const uint32_t a2 = sub_bf16x2(hi ? nib_hi(w0 >> 8) : nib_lo(w0 >> 8), sg);
+          const uint32_t a3 = sub_bf16x2(hi ? nib_hi(w1 >> 8) : nib_lo(w1 >> 8), sg8);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (s == 0)
+              mma_bf16_zc(acc[nt], a0, a1, a2, a3, b0[0][nt], b1[0][nt]);
+            else
+              mma_bf16(acc[nt], a0, a1, a2, a3, b0[1][nt], b1[1][nt]);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float ds = __shfl_sync(0xffffffffu, hi ? dsv[r][1] : dsv[r][0], srcl);
+          const float ee = __shfl_sync(0xffffffffu, hi ? eev[r][1] : eev[r][0], srcl);
+          // columns 2t, 2t+1 share ds and e: one packed fma each (each lane
+          // of a pair rounds as fmaf)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float2 yv = make_float2(yacc[nt][2 * r], yacc[nt][2 * r + 1]);
+            yv = __ffma2_rn(make_float2(ds, ds), make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]), yv);
+            yv = __ffma2_rn(make_float2(ee, ee), make_float2(xsum[nt][0], xsum[nt][1]), yv);
+            yacc[nt][2 * r] = yv.x;
+            yacc[nt][2 * r + 1] = yv.y;
+          }
+        }
+      }
+    }
+    slot = slot == ST - 1 ? 0 : slot + 1;
+    wide_next<SB>(p, hi, cs);
+    if (last_of_part) {
+      if (o.parts == 2 && part == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ygate[nt][e] = yacc[nt][e];
+      } else {
+        // This warp's rows g, g+8 and columns nt*8 + 2t + (e & 1).
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = tile * kWideRows + wrow + g + 8 * (e >> 1);
+            const int col = nt * 8 + 2 * t + (e & 1);
+            if (row < o.n && col < batch)
+              o.y[(size_t)col * o.ldy + row] =
+                  o.parts == 2 ? silu_mul_w(ygate[nt][e], yacc[nt][e]) : yacc[nt][e];
+          }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) yacc[nt][e] = 0.f;
+    }
+  }
+  cp_async_wait<0>();  // nothing is left in flight (the trailing groups are empty)
+}
+
+// ---------------------------------------------------------------- host side
+
+std::once_flag g_wide_attr[kMaxDevices];
+int g_wide_occ[kMaxDevices][2][2];  // resident CTAs per SM: [NT - 1][op table small/large]
+
+template <int NT, int NOPS>
+int wide_setup() {
+  cudaFuncSetAttribute(gemv_wide_kernel<NT, NOPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       WideCfg<NT>::kSmem);
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_wide_kernel<NT, NOPS>,
+                                                    kWideThreads, WideCfg<NT>::kSmem) != cudaSuccess)
+    return 0;
+  return blocks;
+}
+
+void wide_attributes(int dev) {
+  g_wide_occ[dev][0][0] = wide_setup<1, 1>();
+  g_wide_occ[dev][0][1] = wide_setup<1, kWideMaxOps>();
+  g_wide_occ[dev][1][0] = wide_setup<2, 1>();
+  g_wide_occ[dev][1][1] = wide_setup<2, kWideMaxOps>();
+}
+
+template <int NT, int NOPS>
+cudaError_t wide_chunk(const StreamOpDesc *ops, int count, int batch, int grid, bool overlap,
+                       cudaStream_t stream) {
+  WideParams<NOPS> prm;
+  memset(&prm, 0, sizeof prm);
+  long long total = 0;
+  int nops = 0;
+  for (int i = 0; i < count; ++i) {
+    const StreamOpDesc &d = ops[i];
+    if (d.n <= 0) continue;
+    WideOp &o = prm.op[nops++];
+    o.w = static_cast<const uint8_t *>(d.w);
+    o.w2 = static_cast<const uint8_t *>(d.w_up);
+    o.x = static_cast<const __nv_bfloat16 *>(d.x);
+    o.y = d.y;
+    o.n = (int)d.n;
+    o.nsb = (int)(d.k / kQK);
+    o.ntiles = (int)((d.n + kWideRows - 1) / kWideRows);
+    o.parts = d.w_up ? 2 : 1;
+    o.ldx = (int)d.ldx;
+    o.ldy = (int)d.ldy;
+    o.byte0 = total;
+    total += (long long)d.n * o.nsb * kBlockBytes * o.parts;
+  }
+  if (nops == 0) return cudaSuccess;
+  prm.nops = nops;
+  prm.batch = batch;
+  prm.pre = overlap ? Q4K_WIDE_PRE : 0;
+  prm.nctas = grid;
+  prm.total = total;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kWideThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)WideCfg<NT>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemv_wide_kernel<NT, NOPS>, prm);
+}
+
+// Ops [i, j) of a launch chunk: at most kWideMaxOps ops with rows.
+int64_t wide_chunk_end(const StreamOpDesc *ops, int64_t count, int64_t i, long long *tiles) {
+  int64_t j = i, used = 0;
+  *tiles = 0;
+  while (j < count && used < kWideMaxOps) {
+    if (ops[j].n > 0) {
+      ++used;
+      *tiles += (ops[j].n + kWideRows - 1) / kWideRows;
+    }
+    ++j;
+  }
+  return j;
+}
+
+}  // namespace
+
+int wide_min_batch() { return 5; }
+
+bool wide_worth_it(const StreamOpDesc *ops, int64_t count, int batch) {
+  if (batch < wide_min_batch() || batch > 16) return false;
+  const DeviceFacts *f = device_facts();
+  std::call_once(g_wide_attr[f->device], wide_attributes, f->device);
+  const int occ = g_wide_occ[f->device][batch <= 8 ? 0 : 1][1];
+  if (occ <= 0) return false;
+  long long tiles = 0;
+  for (int64_t i = 0; i < count; ++i)
+    if (ops[i].n > 0) tiles += (ops[i].n + kWideRows - 1) / kWideRows;
+  // at least two tiles per resident CTA: fewer leave SMs idle or the ring
+  // fill exposed, where the per-op kernel's split of K does better
+  return tiles >= 2LL * occ * f->sm_count;
+}
+
+cudaError_t launch_wide(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
+                        cudaStream_t stream) {
+  if (batch < 1 || batch > 16) return cudaErrorInvalidValue;
+  const DeviceFacts *f = device_facts();
+  std::call_once(g_wide_attr[f->device], wide_attributes, f->device);
+  const int ntv = batch <= 8 ? 0 : 1;
+  int64_t i = 0;
+  while (i < count) {
+    long long tiles = 0;
+    const int64_t j = wide_chunk_end(ops, count, i, &tiles);
+    if (tiles > 0) {
+      const bool single = j - i == 1;
+      const int occ = g_wide_occ[f->device][ntv][single ? 0 : 1];
+      if (occ <= 0) return cudaErrorInvalidConfiguration;
+      const int grid = (int)std::min<long long>((long long)occ * f->sm_count, tiles);
+      const int n = (int)(j - i);
+      cudaError_t e;
+      if (ntv == 0)
+        e = single ? wide_chunk<1, 1>(ops + i, n, batch, grid, overlap, stream)
+                   : wide_chunk<1, kWideMaxOps>(ops + i, n, batch, grid, overlap, stream);
+      else
+        e = single ? wide_chunk<2, 1>(ops + i, n, batch, grid, overlap, stream)
+                   : wide_chunk<2, kWideMaxOps>(ops + i, n, batch, grid, overlap, stream);
+      if (e != cudaSuccess) return e;
+    }
+    i = j;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace q4k

@@ -170,10 +170,11 @@ int q4k_gemv_glu(const void *w_gate, const void *w_up, int64_t n, int64_t k, con
  *   count   >= 0 (0: nothing to do)
  *   batch   1..16, shared by all ops
  *   flags   as q4k_gemv_ex
- * At batch 1..4 the ops run as ONE persistent launch (a new launch every 448
- * ops) that streams their weights back to back, and ops may run concurrently;
- * at batch 5..16 each op is its own launch.  At every batch: no op of a
- * sequence may read what another op of the same sequence writes (split
+ * At batch 1..4, and at 5..16 when the ops hold at least two 64-row tiles per
+ * resident CTA of the GPU, the ops run as ONE persistent launch (a new launch
+ * every 448 ops) that streams their weights back to back, and ops may run
+ * concurrently; otherwise each op is its own launch.  At every batch: no op of
+ * a sequence may read what another op of the same sequence writes (split
  * dependent projections into separate calls; stream order holds between
  * calls).
  * Every op is checked before the first launch: on a NULL, SHAPE, ALIGN or

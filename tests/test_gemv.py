@@ -106,6 +106,52 @@ def test_gemv_seq_matches_oracle(q4k, batch, flags):
         assert torch.equal(a, b), "a sequence is deterministic"
 
 
+@pytest.mark.parametrize("batch,flags", [(5, 1), (8, 0), (9, 1), (16, 1)])
+def test_gemv_seq_persistent_64_row_tiles(q4k, batch, flags):
+    # batch 5..16 with enough 64-row tiles to fill the GPU (at least two per
+    # resident CTA) runs as one persistent launch: ragged row tails, an empty
+    # op, a fused gate/up op and strided x / y among the ops; every row is
+    # checked against the oracle
+    shapes = [(40000, 256), (0, 512), (30001, 512), (20000, 512), (9000, 768)]
+    glu = {3}
+    ws, wus, xs, xviews, ys, yviews = [], [], [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        ws.append(synth.q4k_weight(max(n, 1), k, seed=5100 + i, quants="normal"))
+        wus.append(synth.q4k_weight(max(n, 1), k, seed=5300 + i) if i in glu else None)
+        if i == 4:  # strided: ldx = k + 64 (offset 16 bytes), ldy = n + 3
+            xb = synth.bf16_normal((batch, k + 64), seed=5200 + i).to(DEV)
+            xs.append(xb)
+            xviews.append(xb[:, 8:8 + k])
+            yb = torch.full((batch, n + 3), float("nan"), device=DEV)
+            ys.append(yb)
+            yviews.append(yb[:, :n])
+        else:
+            x = synth.bf16_normal((batch, k), seed=5200 + i, sigma=0.05 if i in glu else 1.0).to(DEV)
+            xs.append(x)
+            xviews.append(x)
+            y = torch.full((batch, max(n, 1)), 7.0, device=DEV)
+            ys.append(y)
+            yviews.append(y)
+    tup = []
+    for w, wu, (n, k), x, y in zip(ws, wus, shapes, xviews, yviews):
+        dw = w.to(DEV)
+        tup.append((dw, n, k, x, y) if wu is None else (dw, n, k, x, y, wu.to(DEV)))
+    ops = q4k.gemv_ops(tup)
+    q4k.q4k_gemv_seq(ops, batch, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    for i, ((n, k), w, wu, x, y) in enumerate(zip(shapes, ws, wus, xviews, yviews)):
+        if n == 0:
+            assert bool((y == 7.0).all()), "an empty op writes nothing"
+            continue
+        if wu is None:
+            yref, s = oracle.gemv(w.numpy(), n, k, xbits(x.cpu()))
+            check_bound(y.cpu().numpy(), yref, s, TOL, f"wide op {i} {n}x{k} b{batch}")
+        else:
+            check_glu(y.cpu().numpy(), w, wu, n, k, x.cpu(), f"wide glu op {i} {n}x{k} b{batch}")
+    assert bool(torch.isnan(ys[4][:, shapes[4][0]:]).all()), "nothing written past a row"
+
+
 def check_glu(h, wg, wu, n, k, x, what):
     """h = silu(g) u against the oracle, with g and u each within the GEMV
     bound: |dh| <= 1.1 dg |u| + |silu(g)| du + 1.1 dg du + 2^-20 |h| (the last
@@ -151,13 +197,16 @@ def test_gemv_glu_27b_gate_up_full_size_sampled_rows(q4k, batch):
               f"27b glu b{batch}")
 
 
-@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("batch", [1, 4, 16])
 def test_gemv_seq_graph_replay_matches_oracle(q4k, batch):
-    # one 27B-class layer's five projections as one q4k_gemv_seq call with
+    # 27B-class layers' five projections as one q4k_gemv_seq call with
     # programmatic dependent launch, captured in a CUDA graph; the graph is
     # replayed twice with x rewritten in between, and every replay's results
-    # match the oracle on sampled rows
+    # match the oracle on sampled rows (batch 16: two layers, which is enough
+    # 64-row tiles for the persistent launch)
     shapes = [(10240, 5120), (5120, 8192), (17408, 5120), (17408, 5120), (5120, 17408)]
+    if batch == 16:
+        shapes = shapes * 2
     ws = [synth.q4k_weight(n, k, seed=4500 + i, quants="normal", device=DEV)
           for i, (n, k) in enumerate(shapes)]
     xs = [torch.empty((batch, k), dtype=torch.bfloat16, device=DEV) for _, k in shapes]
