@@ -659,8 +659,9 @@ def profiled_traffic(pass_bytes: float):
 
 def run_case(case):
     """One small instance of a kernel, for ncu captures (no timing): one 27B-class
-    layer of batch-1 projections (203 MB of weights) or of batch-4 and batch-16
-    projections, the 512-token gate and
+    layer of batch-1 projections (203 MB of weights) or two layers of batch-4
+    and batch-16 projections (two layers are enough 64-row tiles for the
+    persistent batch-16 launch), the 512-token gate and
     down prefill GEMMs (plain or with the RMSNorm prologue), one routed-MoE decode
     or prefill step, or one batch-1 projection in each other k-quant format."""
     import bit_block_quantized_q4_gb300 as q4k
@@ -669,9 +670,9 @@ def run_case(case):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     if case in ("gemv_layer", "gemv_layer_batched"):
-        # one layer's five projections as one q4k_gemv_seq call (at batch 1 one
-        # launch of the stream kernel over 203 MB of weights)
-        layers = Layers(dev, n_layers=1)
+        # one (batched: two) layer's projections as one q4k_gemv_seq call (at
+        # batch 1 one launch of the stream kernel over 203 MB of weights)
+        layers = Layers(dev, n_layers=1 if case == "gemv_layer" else 2)
         for batch in ((1,) if case == "gemv_layer" else (4, 16)):
             xs, ys = make_inputs(layers, batch, dev, seed=SEED_C1 + batch)
             ops = q4k.gemv_ops([(w, n, k, x, y) for (name, n, k, w), x, y in zip(layers.mats, xs, ys)])

@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
         if (2 * j + csub < nch) cp_async16(dst + 32 * j, src + 32 * j);
     }
   };
+  // Rows past the batch are zero-filled (a copy of 0 source bytes), so the
+  // consumer needs no test per column.
   auto issue_x = [&](int slot, const WPos &s) {
     const WideOp &o = p.op[s.op];
     const int cnt = min(SB, o.nsb - s.sb);
@@ -190,9 +192,33 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
     for (int m = 0; m < SB * NB / kWideWarps; ++m) {
       const int idx = warp + kWideWarps * m;  // block (super-block u, batch row b)
       const int u = idx / NB, b = idx % NB;
-      if (b < batch && u < cnt)
+      if (u < cnt) {
+        const bool in = b < batch;
         cp_async16(dst + idx * kXRowBytes,
-                   o.x + (size_t)b * o.ldx + (size_t)(s.sb + u) * kQK + lane * 8);
+                   o.x + (in ? (size_t)b * o.ldx + (size_t)(s.sb + u) * kQK + lane * 8 : 0),
+                   in ? 16 : 0);
+      }
+    }
+  };
+  // After its copies of a stage have landed, a thread puts its own x chunks in
+  // B-fragment order in place: 16 bytes hold values 8l .. 8l+7 of a sub-block
+  // and become (x0, x2), (x1, x3), (x4, x6), (x5, x7) -- the pairs the nibble
+  // operands meet -- so no warp permutes x again.
+  auto permute_x = [&](int slot, int cnt) {
+    uint8_t *dst = smem + slot * C::kStageBytes + C::kWBytes + lane * 16;
+#pragma unroll
+    for (int m = 0; m < SB * NB / kWideWarps; ++m) {
+      const int idx = warp + kWideWarps * m;
+      if (idx / NB < cnt) {
+        uint4 *q = reinterpret_cast<uint4 *>(dst + idx * kXRowBytes);
+        const uint4 v = *q;
+        uint4 pm;
+        pm.x = __byte_perm(v.x, v.y, 0x5410u);
+        pm.y = __byte_perm(v.x, v.y, 0x7632u);
+        pm.z = __byte_perm(v.z, v.w, 0x5410u);
+        pm.w = __byte_perm(v.z, v.w, 0x7632u);
+        *q = pm;
+      }
     }
   };
 
@@ -222,9 +248,6 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
   grid_launch_dependents();
 
   // ---- consumer
-  bool xval[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) xval[nt] = nt * 8 + g < batch;
   const int wrow = warp * 16;  // this warp's rows of the tile
   WPos cs;
   wide_first(p, lo, hi, cs);
@@ -240,6 +263,7 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
     const int tile = cs.tile, part = cs.part;
     const bool last_of_part = cs.sb + SB >= o.nsb;
     cp_async_wait<ST - 2>();  // this thread's copies of the stage have landed
+    permute_x(slot, cnt);
     __syncthreads();          // every thread's have, and the previous stage is consumed
     {
       const int rs = slot == 0 ? ST - 1 : slot - 1;  // the slot the previous stage used
@@ -290,18 +314,17 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
       for (int j = 0; j < 8; ++j) {
         const int c = j >> 1;
         const bool hi = j & 1;
-        // B fragments of sub-block j: this lane's 16 bytes (values 8t .. 8t+7)
-        // of batch row nt*8 + g, as (x[o], x[o+2]) and (x[o+1], x[o+3]).
+        // B fragments of sub-block j: this lane's 16 bytes (values 8t .. 8t+7,
+        // permuted) of batch row nt*8 + g: (x[o], x[o+2]) and (x[o+1], x[o+3]).
         uint32_t b0[2][NT], b1[2][NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint4 v = xval[nt] ? *reinterpret_cast<const uint4 *>(
-                                         xst + (u * NB + nt * 8 + g) * kXRowBytes + 64 * j + 16 * t)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-          b0[0][nt] = __byte_perm(v.x, v.y, 0x5410);
-          b1[0][nt] = __byte_perm(v.x, v.y, 0x7632);
-          b0[1][nt] = __byte_perm(v.z, v.w, 0x5410);
-          b1[1][nt] = __byte_perm(v.z, v.w, 0x7632);
+          const uint4 v = *reinterpret_cast<const uint4 *>(
+              xst + (u * NB + nt * 8 + g) * kXRowBytes + 64 * j + 16 * t);
+          b0[0][nt] = v.x;
+          b1[0][nt] = v.y;
+          b0[1][nt] = v.z;
+          b1[1][nt] = v.w;
         }
         // X_j of every column (A = 1: column 2t+e is xsum[nt][e]).
         float xsum[NT][4];
