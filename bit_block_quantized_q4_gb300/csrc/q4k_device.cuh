@@ -441,8 +441,9 @@ __device__ __forceinline__ void scales_all(uint32_t h1, uint32_t h2, uint32_t h3
 
 // ----------------------------------------------------------------- offset form
 // Every weight of sub-block j of a super-block is w = ds (q - c) + e with
-//   ds = d sc_j,  dm = dmin m_j,  c = an integer in [0, 16] nearest to dm / ds
-//   (clamped), e = ds c - dm rounded once,
+//   ds = d sc_j,  dm = dmin m_j,  c = an integer in [0, CMAX] nearest to dm / ds
+//   (clamped; CMAX = 16 for 4-bit quants, 32 for Q5_K's 5-bit ones),
+//   e = ds c - dm rounded once,
 // so  sum_i w_i x_i = ds sum_i (q_i - c) x_i + e sum_i x_i.  The tensor cores
 // take the small integers q - c (exact in bf16) against x, so a weight that is
 // exactly zero (ds q = dm) contributes an exact zero product, and the rounding
@@ -453,20 +454,29 @@ __device__ __forceinline__ void scales_all(uint32_t h1, uint32_t h2, uint32_t h3
 // ndm23 = -d 2^23 / -dmin 2^23: fma(d, 2^23 + sc, -d 2^23) is d sc exactly.
 // Outputs: ds, e, and sub = (128 + c) as bf16 in both halves (the value to
 // subtract from the 128 + q nibble operands).
+template <int CMAX>
+__device__ __forceinline__ void offset_form_c(float d, float nd23, float dmin, float ndm23,
+                                              uint32_t sc_magic, uint32_t m_magic, float &ds,
+                                              float &e, uint32_t &sub) {
+  static_assert(CMAX == 16 || CMAX == 32, "128 + c must stay in bf16's unit-step range");
+  ds = fmaf(d, __uint_as_float(sc_magic), nd23);
+  const float dm = fmaf(dmin, __uint_as_float(m_magic), ndm23);
+  // u = (dm/ds + 0.5) / CMAX saturated to [0, 1] (NaN -> 0), v = 128 + CMAX u
+  // in [128, 128 + CMAX]: the bf16 truncation of v is 128 + c with
+  // c = floor(dm/ds + 0.5) clamped to [0, CMAX] (exact for an integer ratio:
+  // the approximate reciprocal moves 128.5 + c by less than half an fp32
+  // ulp).  ds = 0 makes the ratio NaN or +-inf, which the saturation maps to
+  // c = 0 or CMAX.
+  const float u = __saturatef(fmaf(dm, rcp_approx((float)CMAX * ds), 0.5f / (float)CMAX));
+  const uint32_t vb = __float_as_uint(fmaf(u, (float)CMAX, 128.f));
+  sub = __byte_perm(vb, 0u, 0x3232u);
+  e = fmaf(ds, __uint_as_float(vb & 0xFFFF0000u) - 128.f, -dm);
+}
+// Q4_K: q in [0, 15], c in [0, 16].
 __device__ __forceinline__ void offset_form(float d, float nd23, float dmin, float ndm23,
                                             uint32_t sc_magic, uint32_t m_magic, float &ds,
                                             float &e, uint32_t &sub) {
-  ds = fmaf(d, __uint_as_float(sc_magic), nd23);
-  const float dm = fmaf(dmin, __uint_as_float(m_magic), ndm23);
-  // u = (dm/ds + 0.5) / 16 saturated to [0, 1] (NaN -> 0), v = 128 + 16 u in
-  // [128, 144]: the bf16 truncation of v is 128 + c with c = floor(dm/ds + 0.5)
-  // clamped to [0, 16] (exact for an integer ratio: the approximate
-  // reciprocal moves 128.5 + c by less than half an fp32 ulp).  ds = 0 makes
-  // the ratio NaN or +-inf, which the saturation maps to c = 0 or 16.
-  const float u = __saturatef(fmaf(dm, rcp_approx(16.f * ds), 0.03125f));
-  const uint32_t vb = __float_as_uint(fmaf(u, 16.f, 128.f));
-  sub = __byte_perm(vb, 0u, 0x3232u);
-  e = fmaf(ds, __uint_as_float(vb & 0xFFFF0000u) - 128.f, -dm);
+  offset_form_c<16>(d, nd23, dmin, ndm23, sc_magic, m_magic, ds, e, sub);
 }
 // Byte i of w as the float 2^23 + byte (bit pattern 0x4B0000bb).
 __device__ __forceinline__ uint32_t byte_magic(uint32_t w, int i) {

@@ -101,6 +101,13 @@
 #ifndef Q4K_STREAM_MINB_NB4
 #define Q4K_STREAM_MINB_NB4 3
 #endif
+// Q5_K at batch 1: super-blocks per stage and ring stages.
+#ifndef Q4K_STREAM_SB_Q5
+#define Q4K_STREAM_SB_Q5 2
+#endif
+#ifndef Q4K_STREAM_STAGES_Q5
+#define Q4K_STREAM_STAGES_Q5 2
+#endif
 
 namespace q4k {
 
@@ -136,19 +143,31 @@ struct StreamParams {
   StreamOp op[NOPS];
 };
 
-template <int MT, int NB>
+template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
+  static_assert(FMT == 4 || (FMT == 5 && NB == 1), "Q5_K runs at batch 1");
   static constexpr int kRows = 16 * MT;
+  // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
+  // fifth bits at 16, the low nibbles at 48).  The first 16 bytes (d, dmin,
+  // 12 scale bytes) are the same.
+  static constexpr int kBlock = FMT == 5 ? 176 : kBlockBytes;
+  static constexpr int kQs = FMT == 5 ? 48 : kQsOffset;
+  static constexpr int kChunks = kBlock / 16;  // 16-byte chunks per super-block
   static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
-  static constexpr int kSB = NB == 1 ? Q4K_STREAM_SB : NB == 2 ? Q4K_STREAM_SB_NB2 : Q4K_STREAM_SB_NB4;
-  static constexpr int kStages = NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
-                                         : NB == 2 ? Q4K_STREAM_STAGES_NB2 : Q4K_STREAM_STAGES_NB4;
+  static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
+                             : NB == 1 ? Q4K_STREAM_SB
+                             : NB == 2 ? Q4K_STREAM_SB_NB2
+                                       : Q4K_STREAM_SB_NB4;
+  static constexpr int kStages = FMT == 5  ? Q4K_STREAM_STAGES_Q5
+                                 : NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
+                                 : NB == 2 ? Q4K_STREAM_STAGES_NB2
+                                           : Q4K_STREAM_STAGES_NB4;
   static constexpr int kMinBlocks = NB == 1 ? (MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
                                             : NB == 2 ? Q4K_STREAM_MINB_NB2 : Q4K_STREAM_MINB_NB4;
   // a row's slot in a stage: its kSB super-blocks, padded by 16 bytes when
   // kSB is even so that the 16*MT rows fall on different shared-memory banks
-  static constexpr int kRowBytes = kSB * kBlockBytes + (kSB % 2 == 0 ? 16 : 0);
+  static constexpr int kRowBytes = kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
   static constexpr int kXStage = NB * kSB * kXBytes;   // x bytes of a stage: [batch row][sb]
   // permuted-x buffers: two at NB = 1 (written and read on alternate
@@ -156,11 +175,18 @@ struct StreamCfg {
   // super-block from the writes of the next)
   static constexpr int kPermBufs = NB == 1 ? 2 : 1;
   static constexpr int kPermBuf = NB * kPermWords;     // words of one buffer: [batch row][sub-block]
-  // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes
+  // Q5_K: the super-block's fifth bits (32 bytes per row) are copied out of
+  // the ring before the slot is refilled, into one of two buffers with rows
+  // 48 bytes apart (the reads of 8 rows by a warp then hit distinct banks).
+  static constexpr int kQhRow = 48;
+  static constexpr int kQhBuf = FMT == 5 ? kRows * kQhRow : 0;
+  // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes |
+  // fifth-bit buffers (Q5_K)
   static constexpr int kOffX = kStages * kWBytes;
   static constexpr int kOffPerm = kOffX + kStages * kXStage;
   static constexpr int kOffZero = kOffPerm + kPermBufs * kPermBuf * 4;
-  static constexpr int kWarpBytes = (kOffZero + 64 + 127) / 128 * 128;
+  static constexpr int kOffQh = kOffZero + 64;
+  static constexpr int kWarpBytes = (kOffQh + 2 * kQhBuf + 127) / 128 * 128;
   static constexpr int kRedBytes = 2 * kWarps * 2 * NB * kRows * 4;  // split-K partials
   static constexpr int kSmem = kWarps * kWarpBytes + kRedBytes;
 };
@@ -225,12 +251,15 @@ __device__ __forceinline__ void next_tile(const StreamParams<NOPS> &p, int rows,
   valid = op < p.nops && tile_start(p, op, tile, rows) < hi;
 }
 
-template <int NOPS>
+// (The walk measures work in units of 144 bytes per super-block whatever the
+// format: every op of a launch has the same format, so only the addresses
+// below use the real block size BLK.)
+template <int BLK, int NOPS>
 __device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, Pos &s) {
   const StreamOp &o = p.op[s.op];
   const int row0 = s.tile * rows;
   s.nrows = min(rows, o.n - row0);
-  s.rstride = (long long)o.nsb * kBlockBytes;
+  s.rstride = (long long)o.nsb * BLK;
   s.src = (s.part ? o.w2 : o.w) + (size_t)row0 * s.rstride;
   s.xsrc = o.x;
   s.ldx = o.ldx;
@@ -239,7 +268,7 @@ __device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, 
 // Producer walk over the non-empty stages of a stream, for warp kp of KP:
 // moves forward until the position names a stage (skips tiles whose share of
 // super-blocks is empty for this warp) and loads the tile's sources.
-template <int NOPS>
+template <int BLK, int NOPS>
 __device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows, long long hi,
                                         int kp, Pos &s) {
   while (s.valid && s.sb >= s.kb1) {
@@ -253,14 +282,22 @@ __device__ __forceinline__ void pos_settle(const StreamParams<NOPS> &p, int rows
     krange(p.op[s.op].nsb, kp, p.kp, s.kb0, s.kb1);
     s.sb = s.kb0;
   }
-  if (s.valid) pos_load(p, rows, s);
+  if (s.valid) pos_load<BLK>(p, rows, s);
 }
 
-template <int SB, int NOPS>
+template <int SB, int BLK, int NOPS>
 __device__ __forceinline__ void pos_next(const StreamParams<NOPS> &p, int rows, long long hi,
                                          int kp, Pos &s) {
   if ((s.sb += SB) < s.kb1) return;
-  pos_settle(p, rows, hi, kp, s);
+  pos_settle<BLK>(p, rows, hi, kp, s);
+}
+
+// (x & 0x00100010) | magic_reg as one LOP3: bit 4 of both halves of x over the
+// bf16 magic.
+__device__ __forceinline__ uint32_t lop_bit4(uint32_t x, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00100010, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
@@ -283,10 +320,10 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
 }
 
-template <int MT, int NOPS, int NB>
-__global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
+template <int MT, int NOPS, int NB, int FMT>
+__global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlocks)
     gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
-  using C = StreamCfg<MT, NB>;
+  using C = StreamCfg<MT, NB, FMT>;
   constexpr int TR = C::kRows, ST = C::kStages, NP = C::kPairs;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -315,7 +352,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
   if (pp.valid) krange(p.op[pp.op].nsb, kp, KP, pp.kb0, pp.kb1);
   else pp.kb0 = pp.kb1 = 0;
   pp.sb = pp.kb0;
-  pos_settle(p, TR, hi, kp, pp);  // the first stage (when there is one)
+  pos_settle<C::kBlock>(p, TR, hi, kp, pp);  // the first stage (when there is one)
 
   constexpr int SB = C::kSB;
   // A stage's copies are 16-byte cp.async chunks.  Weights: the LPR lanes
@@ -329,12 +366,12 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
   constexpr int LPR = 32 / TR;
   const int crow = lane / LPR, csub = lane % LPR;
   auto issue_w = [&](int slot, const Pos &s) {
-    const int nch = 9 * min(SB, s.kb1 - s.sb);  // chunks of a row in this stage
+    const int nch = C::kChunks * min(SB, s.kb1 - s.sb);  // chunks of a row in this stage
     if (crow < s.nrows) {
       uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
-      const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * kBlockBytes + csub * 16;
+      const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock + csub * 16;
 #pragma unroll
-      for (int j = 0; j < (9 * SB + LPR - 1) / LPR; ++j)
+      for (int j = 0; j < (C::kChunks * SB + LPR - 1) / LPR; ++j)
         if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + 16 * LPR * j);
     }
   };
@@ -359,7 +396,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
     Pos q = pp;
     for (; npre < p.pre && npre < ST && q.valid; ++npre) {
       issue_w(npre, q);
-      pos_next<SB>(p, TR, hi, kp, q);
+      pos_next<SB, C::kBlock>(p, TR, hi, kp, q);
     }
   }
   grid_dependency_wait();
@@ -367,7 +404,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
     if (pp.valid) {
       if (s >= npre) issue_w(s, pp);
       issue_x(s, pp);
-      pos_next<SB>(p, TR, hi, kp, pp);
+      pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
     }
     cp_async_commit();  // stage s (an empty group past the stream's end)
   }
@@ -397,6 +434,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
   }
   uint32_t magic;
   asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kBf16Magic));
+  // Q5_K: rotations that bring bit 2t (2t+1) of each qh byte to bit 4.
+  const uint32_t rot_e = (uint32_t)(2 * t - 4) & 31u, rot_o = (uint32_t)(2 * t - 3) & 31u;
 
   // ---- consumer
   int cslot = 0;
@@ -433,7 +472,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
           if (u >= cnt) break;
-          const uint8_t *ws = wstage + u * kBlockBytes;
+          const uint8_t *ws = wstage + u * C::kBlock;
           uint32_t *pw = perm + pbuf * C::kPermBuf;
           if (C::kPermBufs == 1) __syncwarp();  // the previous super-block's reads are done
           // X_j of the eight sub-blocks of each batch row: lane (g, t) holds
@@ -462,15 +501,25 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
             for (int r = 0; r < 2; ++r) {
               const uint8_t *rp = ws + (mt * 16 + g + 8 * r) * C::kRowBytes;
               hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
-              qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t);
-              qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + kQsOffset + 32 * t + 16);
+              qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + C::kQs + 32 * t);
+              qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + C::kQs + 32 * t + 16);
             }
+          uint8_t *qhb = wreg + C::kOffQh + pbuf * C::kQhBuf;
+          if constexpr (FMT == 5) {
+            // lanes 2r, 2r+1 copy the 32 fifth-bit bytes of row r (16 each)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const int row = mt * 16 + (lane >> 1);
+              *reinterpret_cast<uint4 *>(qhb + row * C::kQhRow + 16 * (lane & 1)) =
+                  *reinterpret_cast<const uint4 *>(ws + row * C::kRowBytes + 16 + 16 * (lane & 1));
+            }
+          }
           __syncwarp();  // permuted x visible to every lane; the stage's last reads done
           if (u == cnt - 1) {
             if (pp.valid) {  // refill this slot with the stream's next stage
               issue_w(cslot, pp);
               issue_x(cslot, pp);
-              pos_next<SB>(p, TR, hi, kp, pp);
+              pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
             }
             cp_async_commit();
           }
@@ -493,8 +542,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
               const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
 #pragma unroll
               for (int e = 0; e < 2; ++e)
-                offset_form(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e),
-                            byte_magic(m4, 2 * r + e), ds[mt][r][e], ee[mt][r][e], sub[mt][r][e]);
+                offset_form_c<FMT == 5 ? 32 : 16>(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e),
+                                                  byte_magic(m4, 2 * r + e), ds[mt][r][e],
+                                                  ee[mt][r][e], sub[mt][r][e]);
             }
           }
 
@@ -522,16 +572,38 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
               for (int mt = 0; mt < MT; ++mt) {
                 const uint32_t w0 = word_of(qa[mt][0][G >> 2], G & 3);
                 const uint32_t w1 = word_of(qa[mt][1][G >> 2], G & 3);
+                // The OR operands of the nibble LOP3s: the bf16 magic, and for
+                // Q5_K the fifth bit of each quant at bit 4 of its half.
+                uint32_t me0 = magic, me1 = magic, me2 = magic, me3 = magic;
+                uint32_t mo0 = magic, mo1 = magic, mo2 = magic, mo3 = magic;
+                if constexpr (FMT == 5) {
+                  // fifth bits of positions 4G .. 4G+3: bit 2t (sub-block 2t)
+                  // and 2t+1 (sub-block 2t+1) of qh bytes 4G .. 4G+3,
+                  // rotated to bit 4 of each byte
+                  const uint8_t *rq = qhb + (mt * 16 + g) * C::kQhRow + 4 * G;
+                  const uint32_t h0 = *reinterpret_cast<const uint32_t *>(rq);
+                  const uint32_t h1 = *reinterpret_cast<const uint32_t *>(rq + 8 * C::kQhRow);
+                  const uint32_t e0 = __funnelshift_r(h0, h0, rot_e), e1 = __funnelshift_r(h1, h1, rot_e);
+                  const uint32_t o0 = __funnelshift_r(h0, h0, rot_o), o1 = __funnelshift_r(h1, h1, rot_o);
+                  me0 = lop_bit4(e0, magic);
+                  me1 = lop_bit4(e1, magic);
+                  me2 = lop_bit4(e0 >> 8, magic);
+                  me3 = lop_bit4(e1 >> 8, magic);
+                  mo0 = lop_bit4(o0, magic);
+                  mo1 = lop_bit4(o1, magic);
+                  mo2 = lop_bit4(o0 >> 8, magic);
+                  mo3 = lop_bit4(o1 >> 8, magic);
+                }
                 // low nibbles: sub-block 2t, positions (4G, 4G+2) and (4G+1, 4G+3)
-                const uint32_t a0 = sub_bf16x2(lop_nib(w0, magic), sub[mt][0][0]);
-                const uint32_t a1 = sub_bf16x2(lop_nib(w1, magic), sub[mt][1][0]);
-                const uint32_t a2 = sub_bf16x2(lop_nib(shr<8>(w0), magic), sub[mt][0][0]);
-                const uint32_t a3 = sub_bf16x2(lop_nib(shr<8>(w1), magic), sub[mt][1][0]);
+                const uint32_t a0 = sub_bf16x2(lop_nib(w0, me0), sub[mt][0][0]);
+                const uint32_t a1 = sub_bf16x2(lop_nib(w1, me1), sub[mt][1][0]);
+                const uint32_t a2 = sub_bf16x2(lop_nib(shr<8>(w0), me2), sub[mt][0][0]);
+                const uint32_t a3 = sub_bf16x2(lop_nib(shr<8>(w1), me3), sub[mt][1][0]);
                 // high nibbles: sub-block 2t+1
-                const uint32_t c0 = sub_bf16x2(lop_nib(shr<4>(w0), magic), sub[mt][0][1]);
-                const uint32_t c1 = sub_bf16x2(lop_nib(shr<4>(w1), magic), sub[mt][1][1]);
-                const uint32_t c2 = sub_bf16x2(lop_nib(shr<12>(w0), magic), sub[mt][0][1]);
-                const uint32_t c3 = sub_bf16x2(lop_nib(shr<12>(w1), magic), sub[mt][1][1]);
+                const uint32_t c0 = sub_bf16x2(lop_nib(shr<4>(w0), mo0), sub[mt][0][1]);
+                const uint32_t c1 = sub_bf16x2(lop_nib(shr<4>(w1), mo1), sub[mt][1][1]);
+                const uint32_t c2 = sub_bf16x2(lop_nib(shr<12>(w0), mo2), sub[mt][0][1]);
+                const uint32_t c3 = sub_bf16x2(lop_nib(shr<12>(w1), mo3), sub[mt][1][1]);
 #pragma unroll
                 for (int P = 0; P < NP; ++P) {
                   const uint32_t be0 = h ? be[P].z : be[P].x, be1 = h ? be[P].w : be[P].y;
@@ -645,22 +717,23 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB>::kMinBlocks)
 
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
-// variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4)), queried once per
-// device after the attributes are set.
-int g_occ[kMaxDevices][4][2];
+// variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
+// for Q5_K (single ops only)), queried once per device after the attributes
+// are set.
+int g_occ[kMaxDevices][5][2];
 
-template <int MT, int NOPS, int NB>
+template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
-  return gemv_stream_kernel<MT, NOPS, NB>;
+  return gemv_stream_kernel<MT, NOPS, NB, FMT>;
 }
 
-template <int MT, int NOPS, int NB>
+template <int MT, int NOPS, int NB, int FMT = 4>
 int stream_setup() {
-  cudaFuncSetAttribute(stream_kernel<MT, NOPS, NB>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       StreamCfg<MT, NB>::kSmem);
+  cudaFuncSetAttribute(stream_kernel<MT, NOPS, NB, FMT>(),
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<MT, NB, FMT>::kSmem);
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, stream_kernel<MT, NOPS, NB>(),
-                                                    kWarps * 32, StreamCfg<MT, NB>::kSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, stream_kernel<MT, NOPS, NB, FMT>(),
+                                                    kWarps * 32, StreamCfg<MT, NB, FMT>::kSmem) !=
       cudaSuccess)
     return 0;
   return blocks;
@@ -675,6 +748,8 @@ void stream_attributes(int dev) {
   g_occ[dev][2][1] = stream_setup<1, kMaxOps, 2>();
   g_occ[dev][3][0] = stream_setup<1, 1, 4>();
   g_occ[dev][3][1] = stream_setup<1, kMaxOps, 4>();
+  g_occ[dev][4][0] = stream_setup<1, 1, 1, 5>();
+  g_occ[dev][4][1] = 0;
 }
 
 struct StreamPlan {
@@ -709,7 +784,7 @@ StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
   return best;
 }
 
-template <int MT, int NOPS, int NB>
+template <int MT, int NOPS, int NB, int FMT = 4>
 cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, int kp, int grid,
                                 bool overlap, cudaStream_t stream) {
   StreamParams<NOPS> prm;
@@ -745,14 +820,14 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)StreamCfg<MT, NB>::kSmem;
+  cfg.dynamicSmemBytes = (size_t)StreamCfg<MT, NB, FMT>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, stream_kernel<MT, NOPS, NB>(), prm);
+  return cudaLaunchKernelEx(&cfg, stream_kernel<MT, NOPS, NB, FMT>(), prm);
 }
 
 template <int NOPS>
@@ -771,10 +846,23 @@ cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, cons
 int stream_max_batch() { return 4; }
 
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
+  if (fmt != 4 && !(fmt == 5 && batch == 1)) return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
+  if (fmt == 5) {  // Q5_K: one launch per op
+    for (int64_t i = 0; i < count; ++i) {
+      if (ops[i].n <= 0) continue;
+      const long long tiles = (ops[i].n + 15) / 16;
+      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][4][0], 0, f);
+      if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
+      const cudaError_t e =
+          launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+  }
   const int var1 = batch == 1 ? 0 : batch == 2 ? 2 : 3;  // 16-row kernel of this batch
   int64_t i = 0;
   while (i < count) {
