@@ -442,7 +442,8 @@ __device__ __forceinline__ void scales_all(uint32_t h1, uint32_t h2, uint32_t h3
 // ----------------------------------------------------------------- offset form
 // Every weight of sub-block j of a super-block is w = ds (q - c) + e with
 //   ds = d sc_j,  dm = dmin m_j,  c = an integer in [0, CMAX] nearest to dm / ds
-//   (clamped; CMAX = 16 for 4-bit quants, 32 for Q5_K's 5-bit ones),
+//   (clamped; CMAX = 16 for 4-bit quants, 32 for Q5_K's 5-bit ones, 4 for
+//   q2_K's 2-bit ones),
 //   e = ds c - dm rounded once,
 // so  sum_i w_i x_i = ds sum_i (q_i - c) x_i + e sum_i x_i.  The tensor cores
 // take the small integers q - c (exact in bf16) against x, so a weight that is
@@ -458,7 +459,7 @@ template <int CMAX>
 __device__ __forceinline__ void offset_form_c(float d, float nd23, float dmin, float ndm23,
                                               uint32_t sc_magic, uint32_t m_magic, float &ds,
                                               float &e, uint32_t &sub) {
-  static_assert(CMAX == 16 || CMAX == 32, "128 + c must stay in bf16's unit-step range");
+  static_assert(CMAX == 4 || CMAX == 16 || CMAX == 32, "128 + c must stay in bf16's unit-step range");
   ds = fmaf(d, __uint_as_float(sc_magic), nd23);
   const float dm = fmaf(dmin, __uint_as_float(m_magic), ndm23);
   // u = (dm/ds + 0.5) / CMAX saturated to [0, 1] (NaN -> 0), v = 128 + CMAX u

@@ -101,6 +101,13 @@
 #ifndef Q4K_STREAM_MINB_NB4
 #define Q4K_STREAM_MINB_NB4 3
 #endif
+// q2_K at batch 1: super-blocks per stage and ring stages.
+#ifndef Q4K_STREAM_SB_Q2
+#define Q4K_STREAM_SB_Q2 2
+#endif
+#ifndef Q4K_STREAM_STAGES_Q2
+#define Q4K_STREAM_STAGES_Q2 2
+#endif
 // Q5_K at batch 1: super-blocks per stage and ring stages (measured on the
 // 5120 x 17408 projection: one and two, 2.01 TB/s, against 1.83 at two and
 // two, where the 368-byte row slots leave room for only 3 CTAs per SM).
@@ -147,29 +154,38 @@ struct StreamParams {
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
-  static_assert(FMT == 4 || (FMT == 5 && NB == 1), "Q5_K runs at batch 1");
+  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2) && NB == 1 && MT == 1),
+                "Q5_K and q2_K run at batch 1 with 16-row tiles");
   static constexpr int kRows = 16 * MT;
   // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
-  // fifth bits at 16, the low nibbles at 48).  The first 16 bytes (d, dmin,
-  // 12 scale bytes) are the same.
-  static constexpr int kBlock = FMT == 5 ? 176 : kBlockBytes;
+  // fifth bits at 16, the low nibbles at 48) -- the first 16 bytes (d, dmin,
+  // 12 scale bytes) are Q4_K's; q2_K 84 bytes (16 scale | min << 4 bytes,
+  // 64 bytes of 2-bit quants at 16, d and dmin at 80).
+  static constexpr int kBlock = FMT == 5 ? 176 : FMT == 2 ? 84 : kBlockBytes;
   static constexpr int kQs = FMT == 5 ? 48 : kQsOffset;
-  static constexpr int kChunks = kBlock / 16;  // 16-byte chunks per super-block
+  // q2_K blocks are only 4-byte aligned: a stage copies a row's bytes from
+  // its start rounded down to 16 (at most 12 bytes early).
+  static constexpr int kLead = FMT == 2 ? 12 : 0;
   static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
   static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
+                             : FMT == 2 ? Q4K_STREAM_SB_Q2
                              : NB == 1 ? Q4K_STREAM_SB
                              : NB == 2 ? Q4K_STREAM_SB_NB2
                                        : Q4K_STREAM_SB_NB4;
   static constexpr int kStages = FMT == 5  ? Q4K_STREAM_STAGES_Q5
+                                 : FMT == 2 ? Q4K_STREAM_STAGES_Q2
                                  : NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
                                  : NB == 2 ? Q4K_STREAM_STAGES_NB2
                                            : Q4K_STREAM_STAGES_NB4;
   static constexpr int kMinBlocks = NB == 1 ? (MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
                                             : NB == 2 ? Q4K_STREAM_MINB_NB2 : Q4K_STREAM_MINB_NB4;
-  // a row's slot in a stage: its kSB super-blocks, padded by 16 bytes when
-  // kSB is even so that the 16*MT rows fall on different shared-memory banks
-  static constexpr int kRowBytes = kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
+  // 16-byte chunks a row's stage copy needs at most
+  static constexpr int kChunks = (kLead + kSB * kBlock + 15) / 16;
+  // a row's slot in a stage: its kSB super-blocks (and the lead), padded by 16
+  // bytes when needed so that the 16*MT rows fall on different banks
+  static constexpr int kRowBytes =
+      FMT == 2 ? 16 * kChunks + 16 : kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
   static constexpr int kXStage = NB * kSB * kXBytes;   // x bytes of a stage: [batch row][sb]
   // permuted-x buffers: two at NB = 1 (written and read on alternate
@@ -207,6 +223,7 @@ struct Pos {
   int ldx;
   int nrows;            // weight rows of the tile
   long long rstride;    // bytes from one weight row to the next
+  const uint8_t *wend;  // end of this part's weight matrix
 };
 
 template <int NOPS>
@@ -262,7 +279,9 @@ __device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, 
   const int row0 = s.tile * rows;
   s.nrows = min(rows, o.n - row0);
   s.rstride = (long long)o.nsb * BLK;
-  s.src = (s.part ? o.w2 : o.w) + (size_t)row0 * s.rstride;
+  const uint8_t *w = s.part ? o.w2 : o.w;
+  s.src = w + (size_t)row0 * s.rstride;
+  s.wend = w + (size_t)o.n * s.rstride;
   s.xsrc = o.x;
   s.ldx = o.ldx;
 }
@@ -294,6 +313,13 @@ __device__ __forceinline__ void pos_next(const StreamParams<NOPS> &p, int rows, 
   pos_settle<BLK>(p, rows, hi, kp, s);
 }
 
+// (x & 0x00030003) | magic_reg as one LOP3: the 2-bit quants in bytes 0 and 2
+// of x as the bf16 pair (128 + q0, 128 + q2).
+__device__ __forceinline__ uint32_t lop_q2(uint32_t x, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00030003, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
+  return d;
+}
 // (x & 0x00100010) | magic_reg as one LOP3: bit 4 of both halves of x over the
 // bf16 magic.
 __device__ __forceinline__ uint32_t lop_bit4(uint32_t x, uint32_t magic_reg) {
@@ -368,13 +394,29 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   constexpr int LPR = 32 / TR;
   const int crow = lane / LPR, csub = lane % LPR;
   auto issue_w = [&](int slot, const Pos &s) {
-    const int nch = C::kChunks * min(SB, s.kb1 - s.sb);  // chunks of a row in this stage
-    if (crow < s.nrows) {
-      uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
-      const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock + csub * 16;
+    if (crow >= s.nrows) return;
+    const int cnt = min(SB, s.kb1 - s.sb);
+    uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
+    const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock;
+    if constexpr (FMT == 2) {
+      // from the row's stage start rounded down to 16 bytes; a chunk that
+      // reaches past the matrix takes only the bytes inside it (the rest of
+      // the 16 are zero-filled and never read)
+      const int lead = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
+      const uint8_t *src0 = src - lead + csub * 16;
+      const int nch = (lead + cnt * C::kBlock + 15) >> 4;
 #pragma unroll
-      for (int j = 0; j < (C::kChunks * SB + LPR - 1) / LPR; ++j)
-        if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + 16 * LPR * j);
+      for (int j = 0; j < (C::kChunks + LPR - 1) / LPR; ++j) {
+        if (LPR * j + csub >= nch) break;
+        const uint8_t *cs = src0 + 16 * LPR * j;
+        const long long left = s.wend - cs;
+        cp_async16(dst + 16 * LPR * j, left > 0 ? cs : src0, left >= 16 ? 16 : left > 0 ? (int)left : 0);
+      }
+    } else {
+      const int nch = (C::kBlock / 16) * cnt;  // chunks of a row in this stage
+#pragma unroll
+      for (int j = 0; j < ((C::kBlock / 16) * SB + LPR - 1) / LPR; ++j)
+        if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + csub * 16 + 16 * LPR * j);
     }
   };
   // x of batch row b goes to [b][0 .. SB) of the stage's x area.
@@ -477,6 +519,112 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
           const uint8_t *ws = wstage + u * C::kBlock;
           uint32_t *pw = perm + pbuf * C::kPermBuf;
           if (C::kPermBufs == 1) __syncwarp();  // the previous super-block's reads are done
+          if constexpr (FMT == 2) {
+            // q2_K: 16 sub-blocks of 16 weights; thread t owns sub-blocks
+            // 4t .. 4t+3 (a = 0..3) of rows g, g+8.  Column sums of x per
+            // 16 values: the first half of each 32-value block is held by
+            // lanes t < 2, the second by t >= 2, so two half-masked pairs of
+            // MMAs with A = 1 give thread t the sums X_{4t+a}.
+            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
+            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 rl = t < 2 ? raw : z4, rh = t < 2 ? z4 : raw;
+            float xl[4], xh[4];
+            mma_bf16_zc(xl, kBf16One, kBf16One, kBf16One, kBf16One, rl.x, rl.y);
+            mma_bf16(xl, kBf16One, kBf16One, kBf16One, kBf16One, rl.z, rl.w);
+            mma_bf16_zc(xh, kBf16One, kBf16One, kBf16One, kBf16One, rh.x, rh.y);
+            mma_bf16(xh, kBf16One, kBf16One, kBf16One, kBf16One, rh.z, rh.w);
+            {
+              uint4 pm;
+              pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
+              pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
+              pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
+              pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
+              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+            }
+            // Rows g, g+8: the stage copy of row r began (row's stage start) &
+            // 15 bytes early; with the matrix 16-byte aligned that lead is
+            // 4 ((row * nsb + sb) mod 4) (84 = 4 * 21).  Words: d | dmin << 16
+            // at 80, the scale | min << 4 bytes of sub-blocks 4t .. 4t+3 at
+            // 4t, and quant bytes 16 + 32h .. +31 (h = t / 2).
+            uint32_t dw[2], scw[2], qw[2][8];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int row = g + 8 * r;
+              const int lead = 4 * (((tile * TR + row) * o.nsb + sb) & 3);
+              const uint8_t *bp = wstage + row * C::kRowBytes + lead + u * C::kBlock;
+              dw[r] = *reinterpret_cast<const uint32_t *>(bp + 80);
+              scw[r] = *reinterpret_cast<const uint32_t *>(bp + 4 * t);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                qw[r][k] = *reinterpret_cast<const uint32_t *>(bp + 16 + 32 * (t >> 1) + 4 * k);
+            }
+            __syncwarp();  // permuted x visible to every lane; the stage's last reads done
+            if (u == cnt - 1) {
+              if (pp.valid) {  // refill this slot with the stream's next stage
+                issue_w(cslot, pp);
+                issue_x(cslot, pp);
+                pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+              }
+              cp_async_commit();
+            }
+            // Offset forms (c in [0, 4]) of the thread's (row, sub-block) pairs.
+            float ds2[2][4], ee2[2][4];
+            uint32_t sub2[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float d = half_lo_to_float(dw[r]), dmin = half_hi_to_float(dw[r]);
+              const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+              const uint32_t scl = scw[r] & 0x0F0F0F0Fu, mhi = (scw[r] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                offset_form_c<4>(d, nd23, dmin, ndm23, byte_magic(scl, a), byte_magic(mhi, a),
+                                 ds2[r][a], ee2[r][a], sub2[r][a]);
+            }
+            // B fragments: lane (g, t) with g = 2t carries sub-block 4t + a
+            // (32-value block 2t + a/2, its half a & 1) in column g; every
+            // other lane reads zeros.  MMA (a, b): positions 4b .. 4b+3 of
+            // the sub-block; acc[a] column 2t sums (q - c) x over it.
+            const bool own2 = t == (g >> 1) && !(g & 1);
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              const uint32_t sh = 2u * (uint32_t)((2 * t + (a >> 1)) & 3);  // quant bits in a byte
+              const uint32_t *pb = own2 ? pw + (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1) : zeros;
+#pragma unroll
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int b = 2 * c2 + h, k = 4 * (a & 1) + b;
+                  const uint32_t w0 = qw[0][k] >> sh, w1 = qw[1][k] >> sh;
+                  const uint32_t a0 = sub_bf16x2(lop_q2(w0, magic), sub2[0][a]);
+                  const uint32_t a1 = sub_bf16x2(lop_q2(w1, magic), sub2[1][a]);
+                  const uint32_t a2 = sub_bf16x2(lop_q2(w0 >> 8, magic), sub2[0][a]);
+                  const uint32_t a3 = sub_bf16x2(lop_q2(w1 >> 8, magic), sub2[1][a]);
+                  const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
+                  if (b == 0)
+                    mma_bf16_zc(acc[a], a0, a1, a2, a3, b0, b1);
+                  else
+                    mma_bf16(acc[a], a0, a1, a2, a3, b0, b1);
+                }
+              }
+            }
+            // X_{4t + a}: halves lo / hi of 32-value blocks 2t (column 2t) and
+            // 2t+1 (column 2t+1).
+            const float xsa[4] = {xl[0], xh[0], xl[1], xh[1]};
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float v = yacc[0][r][0];
+#pragma unroll
+              for (int a = 0; a < 4; ++a) {
+                v = fmaf(ds2[r][a], acc[a][2 * r], v);
+                v = fmaf(ee2[r][a], xsa[a], v);
+              }
+              yacc[0][r][0] = v;
+            }
+            pbuf ^= 1;
+            continue;
+          }
           // X_j of the eight sub-blocks of each batch row: lane (g, t) holds
           // values 8t .. 8t+7 of sub-block g, exactly the B fragment of column
           // g of two MMAs.  Permuted copy: word 2G of a sub-block holds
@@ -720,9 +868,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
 // variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
-// for Q5_K (single ops only)), queried once per device after the attributes
-// are set.
-int g_occ[kMaxDevices][5][2];
+// for Q5_K and q2_K (single ops only)), queried once per device after the
+// attributes are set.
+int g_occ[kMaxDevices][6][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
@@ -752,6 +900,8 @@ void stream_attributes(int dev) {
   g_occ[dev][3][1] = stream_setup<1, kMaxOps, 4>();
   g_occ[dev][4][0] = stream_setup<1, 1, 1, 5>();
   g_occ[dev][4][1] = 0;
+  g_occ[dev][5][0] = stream_setup<1, 1, 1, 2>();
+  g_occ[dev][5][1] = 0;
 }
 
 struct StreamPlan {
@@ -850,17 +1000,18 @@ int stream_max_batch() { return 4; }
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
-  if (fmt != 4 && !(fmt == 5 && batch == 1)) return cudaErrorInvalidValue;
+  if (fmt != 4 && !((fmt == 5 || fmt == 2) && batch == 1)) return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
-  if (fmt == 5) {  // Q5_K: one launch per op
+  if (fmt != 4) {  // Q5_K, q2_K: one launch per op
     for (int64_t i = 0; i < count; ++i) {
       if (ops[i].n <= 0) continue;
       const long long tiles = (ops[i].n + 15) / 16;
-      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][4][0], 0, f);
+      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][fmt == 5 ? 4 : 5][0], 0, f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const cudaError_t e =
-          launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
+          fmt == 5 ? launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
+                   : launch_stream_chunk<1, 1, 1, 2>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
       if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -119,11 +119,11 @@ def test_kq_gemv_longest_row_and_host_memory_rejected(q4k):
     assert ei.value.status == 8
 
 
-def _q5k_cancel_matrix(k, seed):
-    """Rows of Q5_K blocks; every third row has all weights exactly 0
-    (d sc q = dmin m with q = c for every weight of every sub-block, c up to 31
-    so that the fifth quant bit is set), the others random."""
-    from _kq_fields import pack_q5k, random_block
+def _cancel_matrix(fmt, k, seed):
+    """Rows of q2_K or Q5_K blocks; every third row has all weights exactly 0
+    (d sc q = dmin m with q = c for every weight of every sub-block; Q5_K's c
+    up to 31, so that the fifth quant bit is set), the others random."""
+    from _kq_fields import pack_q2k, pack_q5k, random_block
     from _q4k_fields import half_bits
     rng = np.random.default_rng(seed)
     rows = []
@@ -132,39 +132,49 @@ def _q5k_cancel_matrix(k, seed):
         for _ in range(k // 256):
             if r % 3 == 0:
                 # d = 1/64, sc = 2 (ds = 1/32); dmin = 1/32, m = c: w = (q - c)/32
-                c = [int(v) for v in rng.integers(0, 32, 8)]
-                q = [c[i // 32] for i in range(256)]
-                blks.append(pack_q5k(half_bits(1 / 64), half_bits(1 / 32), [2] * 8, c, q))
+                if fmt == 5:
+                    c = [int(v) for v in rng.integers(0, 32, 8)]
+                    q = [c[i // 32] for i in range(256)]
+                    blks.append(pack_q5k(half_bits(1 / 64), half_bits(1 / 32), [2] * 8, c, q))
+                else:
+                    c = [int(v) for v in rng.integers(0, 4, 16)]
+                    q = [c[i // 16] for i in range(256)]
+                    blks.append(pack_q2k(half_bits(1 / 64), half_bits(1 / 32), [2] * 16, c, q))
             else:
-                blks.append(random_block(5, rng)[0])
+                blks.append(random_block(fmt, rng)[0])
         rows.append(b"".join(blks))
     return torch.frombuffer(bytearray(b"".join(rows)), dtype=torch.uint8).view(len(rows), -1)
 
 
+@pytest.mark.parametrize("fmt", [2, 5])
 @pytest.mark.parametrize("k", [256, 1280, 5120])
-def test_q5k_cancelling_rows_give_exact_zero_at_batch_1(q4k, k):
-    # batch 1 runs Q5_K through the tensor-core offset form (c up to 32): rows
-    # whose weights all cancel must come out exactly 0, the rest within the bound
-    w = _q5k_cancel_matrix(k, seed=k)
+def test_cancelling_rows_give_exact_zero_at_batch_1(q4k, fmt, k):
+    # batch 1 runs q2_K and Q5_K through the tensor-core offset form (c up to 4
+    # and 32): rows whose weights all cancel must come out exactly 0, the rest
+    # within the bound
+    w = _cancel_matrix(fmt, k, seed=k + fmt)
     n = w.shape[0]
-    x = synth.bf16_normal((1, k), seed=3 * k)
-    y = q4k.q4k_kq_gemv(5, w.to(DEV), n, k, x.to(DEV))
+    x = synth.bf16_normal((1, k), seed=3 * k + fmt)
+    y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x.to(DEV))
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     got = y.cpu().numpy().astype(np.float64)
-    yref, s = oracle.kq_gemv(5, w.numpy(), n, k, xbits(x))
+    yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
     assert np.all(s[:, 0::3] == 0.0) and np.all(yref[:, 0::3] == 0.0)
-    assert np.all(got[:, 0::3] == 0.0), "Q5_K rows whose weights all cancel must be exactly 0"
-    check_bound(got, yref, s, TOL, f"q5k cancel k{k}")
+    assert np.all(got[:, 0::3] == 0.0), f"kq{fmt}: rows whose weights all cancel must be exactly 0"
+    check_bound(got, yref, s, TOL, f"kq{fmt} cancel k{k}")
 
 
-@pytest.mark.parametrize("n,k", [(4901, 1280), (16 * 152 * 2 + 3, 512)])
-def test_q5k_batch_1_many_row_tiles(q4k, n, k):
-    # many 16-row tiles (more than one per warp) with a ragged last tile
-    w = synth.kq_weight(5, n, k, seed=900 + n)
-    x = synth.bf16_normal((1, k), seed=901)
-    y = q4k.q4k_kq_gemv(5, w.to(DEV), n, k, x.to(DEV))
+@pytest.mark.parametrize("fmt", [2, 5])
+@pytest.mark.parametrize("n,k", [(4901, 1280), (16 * 152 * 2 + 3, 512), (3, 3 * 256), (1000, 17408)])
+def test_batch_1_tensor_core_formats_many_shapes(q4k, fmt, n, k):
+    # many 16-row tiles (more than one per warp) with a ragged last tile, a
+    # single odd row count with an odd number of super-blocks (q2_K rows then
+    # start at every 4-byte offset mod 16), and long rows (many ring turns)
+    w = synth.kq_weight(fmt, n, k, seed=900 + n + fmt)
+    x = synth.bf16_normal((1, k), seed=901 + fmt)
+    y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x.to(DEV))
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
-    yref, s = oracle.kq_gemv(5, w.numpy(), n, k, xbits(x))
-    check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, f"q5k b1 {n}x{k}")
+    yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
+    check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, f"kq{fmt} b1 {n}x{k}")
