@@ -101,6 +101,17 @@
 #ifndef Q4K_STREAM_MINB_NB4
 #define Q4K_STREAM_MINB_NB4 3
 #endif
+// Q6_K at batch 1: super-blocks per stage and ring stages (its slot is
+// refilled only after the super-block's contraction, which reads the quants
+// from shared memory as it goes; measured on the 5120 x 17408 projection: one
+// super-block and two stages 1.68 TB/s, three stages 1.65, four 1.62, two
+// super-blocks 1.20).
+#ifndef Q4K_STREAM_SB_Q6
+#define Q4K_STREAM_SB_Q6 1
+#endif
+#ifndef Q4K_STREAM_STAGES_Q6
+#define Q4K_STREAM_STAGES_Q6 2
+#endif
 // q2_K at batch 1: super-blocks per stage and ring stages.
 #ifndef Q4K_STREAM_SB_Q2
 #define Q4K_STREAM_SB_Q2 2
@@ -154,27 +165,32 @@ struct StreamParams {
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
-  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2) && NB == 1 && MT == 1),
-                "Q5_K and q2_K run at batch 1 with 16-row tiles");
+  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2 || FMT == 6) && NB == 1 && MT == 1),
+                "Q5_K, q2_K and Q6_K run at batch 1 with 16-row tiles");
   static constexpr int kRows = 16 * MT;
   // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
   // fifth bits at 16, the low nibbles at 48) -- the first 16 bytes (d, dmin,
   // 12 scale bytes) are Q4_K's; q2_K 84 bytes (16 scale | min << 4 bytes,
-  // 64 bytes of 2-bit quants at 16, d and dmin at 80).
-  static constexpr int kBlock = FMT == 5 ? 176 : FMT == 2 ? 84 : kBlockBytes;
+  // 64 bytes of 2-bit quants at 16, d and dmin at 80); Q6_K 210 bytes (128
+  // low-nibble bytes, 64 bytes of high bits at 128, 16 int8 scales at 192,
+  // d at 208).
+  static constexpr int kBlock = FMT == 5 ? 176 : FMT == 2 ? 84 : FMT == 6 ? 210 : kBlockBytes;
   static constexpr int kQs = FMT == 5 ? 48 : kQsOffset;
-  // q2_K blocks are only 4-byte aligned: a stage copies a row's bytes from
-  // its start rounded down to 16 (at most 12 bytes early).
-  static constexpr int kLead = FMT == 2 ? 12 : 0;
+  // q2_K blocks are only 4-byte aligned, Q6_K ones 2-byte aligned: a stage
+  // copies a row's bytes from its start rounded down to 16 (at most 12 or 14
+  // bytes early).
+  static constexpr int kLead = FMT == 2 ? 12 : FMT == 6 ? 14 : 0;
   static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
   static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
                              : FMT == 2 ? Q4K_STREAM_SB_Q2
+                             : FMT == 6 ? Q4K_STREAM_SB_Q6
                              : NB == 1 ? Q4K_STREAM_SB
                              : NB == 2 ? Q4K_STREAM_SB_NB2
                                        : Q4K_STREAM_SB_NB4;
   static constexpr int kStages = FMT == 5  ? Q4K_STREAM_STAGES_Q5
                                  : FMT == 2 ? Q4K_STREAM_STAGES_Q2
+                                 : FMT == 6 ? Q4K_STREAM_STAGES_Q6
                                  : NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
                                  : NB == 2 ? Q4K_STREAM_STAGES_NB2
                                            : Q4K_STREAM_STAGES_NB4;
@@ -185,7 +201,7 @@ struct StreamCfg {
   // a row's slot in a stage: its kSB super-blocks (and the lead), padded by 16
   // bytes when needed so that the 16*MT rows fall on different banks
   static constexpr int kRowBytes =
-      FMT == 2 ? 16 * kChunks + 16 : kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
+      (FMT == 2 || FMT == 6) ? 16 * kChunks + 16 : kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
   static constexpr int kXStage = NB * kSB * kXBytes;   // x bytes of a stage: [batch row][sb]
   // permuted-x buffers: two at NB = 1 (written and read on alternate
@@ -320,6 +336,13 @@ __device__ __forceinline__ uint32_t lop_q2(uint32_t x, uint32_t magic_reg) {
   asm("lop3.b32 %0, %1, 0x00030003, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
   return d;
 }
+// (x & 0x00300030) | magic_reg as one LOP3: bits 4, 5 of both halves of x
+// over the bf16 magic.
+__device__ __forceinline__ uint32_t lop_bits45(uint32_t x, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00300030, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
+  return d;
+}
 // (x & 0x00100010) | magic_reg as one LOP3: bit 4 of both halves of x over the
 // bf16 magic.
 __device__ __forceinline__ uint32_t lop_bit4(uint32_t x, uint32_t magic_reg) {
@@ -398,7 +421,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
     const int cnt = min(SB, s.kb1 - s.sb);
     uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
     const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock;
-    if constexpr (FMT == 2) {
+    if constexpr (FMT == 2 || FMT == 6) {
       // from the row's stage start rounded down to 16 bytes; a chunk that
       // reaches past the matrix takes only the bytes inside it (the rest of
       // the 16 are zero-filled and never read)
@@ -621,6 +644,126 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 v = fmaf(ee2[r][a], xsa[a], v);
               }
               yacc[0][r][0] = v;
+            }
+            pbuf ^= 1;
+            continue;
+          }
+          if constexpr (FMT == 6) {
+            // Q6_K: 16 sub-blocks of 16 weights, w = d sc (q - 32) with q the
+            // 6-bit value (low nibble in ql, two high bits in qh) and sc an
+            // int8: no min term, so the A operand is the exact q - 32 and no
+            // column sums are needed.  Thread t owns sub-blocks 4t .. 4t+3
+            // (a = 0..3) of rows g, g+8: half h = t / 2 of the block, 32-value
+            // group v = (2t + a/2) mod 4 (low nibbles for v < 2, high ones
+            // for v >= 2; high bits 2v, 2v+1 of the qh bytes).
+            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
+            {
+              uint4 pm;
+              pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
+              pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
+              pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
+              pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
+              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+            }
+            __syncwarp();  // permuted x visible to every lane
+            // Rows g, g+8: the stage copy of row r began (row's stage start) &
+            // 15 bytes early; with the matrix 16-byte aligned that lead is
+            // 2 ((row * nsb + sb) mod 8) (210 = 2 * 105), so the block is only
+            // 2-byte aligned: a word at byte offset o is read as the two
+            // aligned words around it, funnel-shifted by 8 (o & 3) bits.
+            const uint8_t *bp[2];
+            uint32_t qh[2][8];
+            float ds6[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int row = g + 8 * r;
+              const int lead = 2 * (((tile * TR + row) * o.nsb + sb) & 7);
+              bp[r] = wstage + row * C::kRowBytes + lead + u * C::kBlock;
+              // qh bytes 128 + 32h .. +31
+              const uint8_t *qa = bp[r] + 128 + 32 * (t >> 1);
+              const uint32_t *al = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(qa) & ~uintptr_t(3));
+              const uint32_t fs = 8u * (uint32_t)(reinterpret_cast<uintptr_t>(qa) & 3u);
+              uint32_t prev = al[0];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t next = al[k + 1];
+                qh[r][k] = __funnelshift_r(prev, next, fs);
+                prev = next;
+              }
+              // scales of sub-blocks 4t .. 4t+3 (int8) at 192 + 4t, d at 208
+              const uint8_t *sa = bp[r] + 192 + 4 * t;
+              const uint32_t *sl = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(sa) & ~uintptr_t(3));
+              const uint32_t scw = __funnelshift_r(sl[0], sl[1], 8u * (uint32_t)(reinterpret_cast<uintptr_t>(sa) & 3u));
+              const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(bp[r] + 208)));
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                ds6[r][a] = d * (float)(int)(int8_t)(scw >> (8 * a));  // exact
+            }
+            const bool own2 = t == (g >> 1) && !(g & 1);
+            const uint32_t nsh = (t & 1) ? 4u : 0u;  // high nibbles for v >= 2
+            uint32_t sub32;
+            asm volatile("mov.b32 %0, %1;\n" : "=r"(sub32) : "n"(0x43204320u));  // bf16 (160, 160)
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              const uint32_t v = (uint32_t)((2 * t + (a >> 1)) & 3);
+              const uint32_t rot = (2u * v - 4u) & 31u;  // high bits 2v, 2v+1 -> bits 4, 5
+              // ql bytes 64h + 16a .. +15 of each row, as four words
+              uint32_t ql[2][4];
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const uint8_t *qa = bp[r] + 64 * (t >> 1) + 16 * a;
+                const uint32_t *al = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(qa) & ~uintptr_t(3));
+                const uint32_t fs = 8u * (uint32_t)(reinterpret_cast<uintptr_t>(qa) & 3u);
+                uint32_t prev = al[0];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                  const uint32_t next = al[b + 1];
+                  ql[r][b] = __funnelshift_r(prev, next, fs);
+                  prev = next;
+                }
+              }
+              const uint32_t *pb = own2 ? pw + (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1) : zeros;
+#pragma unroll
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int b = 2 * c2 + h, kq = 4 * (a & 1) + b;
+                  uint32_t av[4];
+#pragma unroll
+                  for (int r = 0; r < 2; ++r) {
+                    const uint32_t lw = ql[r][b] >> nsh;
+                    const uint32_t hw = __funnelshift_r(qh[r][kq], qh[r][kq], rot);
+                    // (128 + q) for bytes 0, 2 and 1, 3: the nibble over the
+                    // two high bits at bits 4, 5 and the bf16 magic
+                    const uint32_t m02 = lop_bits45(hw, magic), m13 = lop_bits45(hw >> 8, magic);
+                    av[r] = sub_bf16x2(lop_nib(lw, m02), sub32);
+                    av[2 + r] = sub_bf16x2(lop_nib(lw >> 8, m13), sub32);
+                  }
+                  const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
+                  if (b == 0)
+                    mma_bf16_zc(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+                  else
+                    mma_bf16(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+                }
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float yv = yacc[0][r][0];
+#pragma unroll
+              for (int a = 0; a < 4; ++a) yv = fmaf(ds6[r][a], acc[a][2 * r], yv);
+              yacc[0][r][0] = yv;
+            }
+            __syncwarp();  // every lane's reads of the stage are done
+            if (u == cnt - 1) {
+              if (pp.valid) {  // refill this slot with the stream's next stage
+                issue_w(cslot, pp);
+                issue_x(cslot, pp);
+                pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+              }
+              cp_async_commit();
             }
             pbuf ^= 1;
             continue;
@@ -868,9 +1011,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
 // variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
-// for Q5_K and q2_K (single ops only)), queried once per device after the
-// attributes are set.
-int g_occ[kMaxDevices][6][2];
+// for Q5_K, q2_K and Q6_K (single ops only)), queried once per device after
+// the attributes are set.
+int g_occ[kMaxDevices][7][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
@@ -902,6 +1045,8 @@ void stream_attributes(int dev) {
   g_occ[dev][4][1] = 0;
   g_occ[dev][5][0] = stream_setup<1, 1, 1, 2>();
   g_occ[dev][5][1] = 0;
+  g_occ[dev][6][0] = stream_setup<1, 1, 1, 6>();
+  g_occ[dev][6][1] = 0;
 }
 
 struct StreamPlan {
@@ -1000,18 +1145,20 @@ int stream_max_batch() { return 4; }
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
-  if (fmt != 4 && !((fmt == 5 || fmt == 2) && batch == 1)) return cudaErrorInvalidValue;
+  if (fmt != 4 && !((fmt == 5 || fmt == 2 || fmt == 6) && batch == 1)) return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
-  if (fmt != 4) {  // Q5_K, q2_K: one launch per op
+  if (fmt != 4) {  // Q5_K, q2_K, Q6_K: one launch per op
     for (int64_t i = 0; i < count; ++i) {
       if (ops[i].n <= 0) continue;
       const long long tiles = (ops[i].n + 15) / 16;
-      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][fmt == 5 ? 4 : 5][0], 0, f);
+      const int var = fmt == 5 ? 4 : fmt == 2 ? 5 : 6;
+      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][var][0], 0, f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const cudaError_t e =
-          fmt == 5 ? launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
-                   : launch_stream_chunk<1, 1, 1, 2>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
+          fmt == 5   ? launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
+          : fmt == 2 ? launch_stream_chunk<1, 1, 1, 2>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
+                     : launch_stream_chunk<1, 1, 1, 6>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
       if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

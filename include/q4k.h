@@ -262,9 +262,9 @@ int q4k_gemm_rmsnorm(const void *w, int64_t n, int64_t k, const void *x, int64_t
  *                 w = d * scale * (6-bit value - 32).
  * Dequantized weights are the exact value rounded once to fp32 (bit-exact);
  * GEMV results satisfy |y - y_ref| <= 2e-3 * sum_k |w_k||x_k| (fp32 products
- * of the rounded weights with x, fp32 accumulation; Q5_K at batch 1: the
- * Q4_K kernels' offset form on the tensor cores, so a row whose weights all
- * cancel gives exactly 0).
+ * of the rounded weights with x, fp32 accumulation; q2_K, Q5_K and Q6_K at
+ * batch 1: the Q4_K kernels' exact small-integer operands on the tensor
+ * cores, so a row whose weights are all zero gives exactly 0).
  */
 #define Q4K_FMT_Q2_K 2
 #define Q4K_FMT_Q3_K 3
