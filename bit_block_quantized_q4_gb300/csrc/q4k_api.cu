@@ -369,7 +369,7 @@ int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void 
   if (st != Q4K_OK) return st;
   st = check_device_memory({w, x, y});
   if (st != Q4K_OK) return st;
-  if ((format == 5 || format == 2 || format == 6) && batch == 1) {  // tensor cores, as Q4_K
+  if (format != 4 && batch == 1) {  // tensor cores, as Q4_K
     const StreamOpDesc d = {w, nullptr, x, y, n, k, 0, 0};
     return map_launch(launch_stream(&d, 1, 1, false, static_cast<cudaStream_t>(stream), format));
   }

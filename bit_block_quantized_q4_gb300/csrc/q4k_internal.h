@@ -54,8 +54,8 @@ struct StreamOpDesc {
 };
 // The ops, in order, as one persistent launch (several when count exceeds the
 // kernel's op table); ops with n == 0 are skipped.  batch 1..stream_max_batch().
-// fmt 4 (Q4_K, batch 1..4), 5 (Q5_K), 2 (q2_K) or 6 (Q6_K) (batch 1: a
-// decode projection of the k-quant entry points).
+// fmt 4 (Q4_K, batch 1..4), or 2, 3, 5, 6 (q2_K, q3_K, Q5_K, Q6_K; batch 1:
+// a decode projection of the k-quant entry points).
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt = 4);
 int stream_max_batch();

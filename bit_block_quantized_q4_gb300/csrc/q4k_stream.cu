@@ -112,6 +112,14 @@
 #ifndef Q4K_STREAM_STAGES_Q6
 #define Q4K_STREAM_STAGES_Q6 2
 #endif
+// q3_K at batch 1: super-blocks per stage and ring stages (refilled after the
+// contraction, as Q6_K).
+#ifndef Q4K_STREAM_SB_Q3
+#define Q4K_STREAM_SB_Q3 1
+#endif
+#ifndef Q4K_STREAM_STAGES_Q3
+#define Q4K_STREAM_STAGES_Q3 2
+#endif
 // q2_K at batch 1: super-blocks per stage and ring stages.
 #ifndef Q4K_STREAM_SB_Q2
 #define Q4K_STREAM_SB_Q2 2
@@ -165,32 +173,36 @@ struct StreamParams {
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
-  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2 || FMT == 6) && NB == 1 && MT == 1),
-                "Q5_K, q2_K and Q6_K run at batch 1 with 16-row tiles");
+  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2 || FMT == 3 || FMT == 6) && NB == 1 && MT == 1),
+                "the other k-quants run at batch 1 with 16-row tiles");
   static constexpr int kRows = 16 * MT;
   // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
   // fifth bits at 16, the low nibbles at 48) -- the first 16 bytes (d, dmin,
   // 12 scale bytes) are Q4_K's; q2_K 84 bytes (16 scale | min << 4 bytes,
   // 64 bytes of 2-bit quants at 16, d and dmin at 80); Q6_K 210 bytes (128
   // low-nibble bytes, 64 bytes of high bits at 128, 16 int8 scales at 192,
-  // d at 208).
-  static constexpr int kBlock = FMT == 5 ? 176 : FMT == 2 ? 84 : FMT == 6 ? 210 : kBlockBytes;
+  // d at 208); q3_K 110 bytes (32 mask bytes, 64 bytes of 2-bit quants at 32,
+  // 12 bytes of 6-bit scales at 96, d at 108).
+  static constexpr int kBlock =
+      FMT == 5 ? 176 : FMT == 2 ? 84 : FMT == 6 ? 210 : FMT == 3 ? 110 : kBlockBytes;
   static constexpr int kQs = FMT == 5 ? 48 : kQsOffset;
-  // q2_K blocks are only 4-byte aligned, Q6_K ones 2-byte aligned: a stage
-  // copies a row's bytes from its start rounded down to 16 (at most 12 or 14
-  // bytes early).
-  static constexpr int kLead = FMT == 2 ? 12 : FMT == 6 ? 14 : 0;
+  // q2_K blocks are only 4-byte aligned, q3_K and Q6_K ones 2-byte aligned: a
+  // stage copies a row's bytes from its start rounded down to 16 (at most 12
+  // or 14 bytes early).
+  static constexpr int kLead = FMT == 2 ? 12 : (FMT == 3 || FMT == 6) ? 14 : 0;
   static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
   static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
                              : FMT == 2 ? Q4K_STREAM_SB_Q2
                              : FMT == 6 ? Q4K_STREAM_SB_Q6
+                             : FMT == 3 ? Q4K_STREAM_SB_Q3
                              : NB == 1 ? Q4K_STREAM_SB
                              : NB == 2 ? Q4K_STREAM_SB_NB2
                                        : Q4K_STREAM_SB_NB4;
   static constexpr int kStages = FMT == 5  ? Q4K_STREAM_STAGES_Q5
                                  : FMT == 2 ? Q4K_STREAM_STAGES_Q2
                                  : FMT == 6 ? Q4K_STREAM_STAGES_Q6
+                                 : FMT == 3 ? Q4K_STREAM_STAGES_Q3
                                  : NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
                                  : NB == 2 ? Q4K_STREAM_STAGES_NB2
                                            : Q4K_STREAM_STAGES_NB4;
@@ -201,7 +213,8 @@ struct StreamCfg {
   // a row's slot in a stage: its kSB super-blocks (and the lead), padded by 16
   // bytes when needed so that the 16*MT rows fall on different banks
   static constexpr int kRowBytes =
-      (FMT == 2 || FMT == 6) ? 16 * kChunks + 16 : kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
+      (FMT == 2 || FMT == 3 || FMT == 6) ? 16 * kChunks + 16
+                                         : kSB * kBlock + (kSB % 2 == 0 ? 16 : 0);
   static constexpr int kWBytes = kRows * kRowBytes;    // weight bytes of a stage
   static constexpr int kXStage = NB * kSB * kXBytes;   // x bytes of a stage: [batch row][sb]
   // permuted-x buffers: two at NB = 1 (written and read on alternate
@@ -336,6 +349,13 @@ __device__ __forceinline__ uint32_t lop_q2(uint32_t x, uint32_t magic_reg) {
   asm("lop3.b32 %0, %1, 0x00030003, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
   return d;
 }
+// (x & 0x00040004) | magic_reg as one LOP3: bit 2 of both halves of x over
+// the bf16 magic.
+__device__ __forceinline__ uint32_t lop_bit2(uint32_t x, uint32_t magic_reg) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00040004, %2, 0xEA;\n" : "=r"(d) : "r"(x), "r"(magic_reg));
+  return d;
+}
 // (x & 0x00300030) | magic_reg as one LOP3: bits 4, 5 of both halves of x
 // over the bf16 magic.
 __device__ __forceinline__ uint32_t lop_bits45(uint32_t x, uint32_t magic_reg) {
@@ -421,7 +441,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
     const int cnt = min(SB, s.kb1 - s.sb);
     uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
     const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock;
-    if constexpr (FMT == 2 || FMT == 6) {
+    if constexpr (FMT == 2 || FMT == 3 || FMT == 6) {
       // from the row's stage start rounded down to 16 bytes; a chunk that
       // reaches past the matrix takes only the bytes inside it (the rest of
       // the 16 are zero-filled and never read)
@@ -644,6 +664,116 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 v = fmaf(ee2[r][a], xsa[a], v);
               }
               yacc[0][r][0] = v;
+            }
+            pbuf ^= 1;
+            continue;
+          }
+          if constexpr (FMT == 3) {
+            // q3_K: 16 sub-blocks of 16 weights, w = d (sc - 32) (u - 4) with u
+            // the 3-bit value (two bits in qs, the top bit in the mask bytes)
+            // and sc 6 bits: no min term, so the A operand is the exact u - 4
+            // and no column sums are needed.  Thread t owns sub-blocks 4t ..
+            // 4t+3 (a = 0..3) of rows g, g+8: half h = t / 2, bit pair
+            // g2 = (2t + a/2) mod 4 of the qs bytes, mask bit 4h + g2.
+            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
+            {
+              uint4 pm;
+              pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
+              pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
+              pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
+              pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
+              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+            }
+            __syncwarp();  // permuted x visible to every lane
+            // Rows g, g+8: the stage copy of row r began (row's stage start) &
+            // 15 bytes early; with the matrix 16-byte aligned that lead is
+            // 14 ((row * nsb + sb) mod 8) mod 16 (110 = 2 * 55), so the block is
+            // only 2-byte aligned: words are read as funnel-shifted aligned pairs.
+            auto word_at = [](const uint8_t *q) -> uint32_t {
+              const uint32_t *al =
+                  reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(q) & ~uintptr_t(3));
+              return __funnelshift_r(al[0], al[1], 8u * (uint32_t)(reinterpret_cast<uintptr_t>(q) & 3u));
+            };
+            const uint8_t *bp[2];
+            float ds3[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int row = g + 8 * r;
+              const int lead = (14 * (((tile * TR + row) * o.nsb + sb) & 7)) & 15;
+              bp[r] = wstage + row * C::kRowBytes + lead + u * C::kBlock;
+              // scales of sub-blocks j = 4t .. 4t+3: low nibbles of bytes
+              // 4t .. 4t+3 (t < 2) or high nibbles of bytes 4t-8 .. 4t-5
+              // (t >= 2) at 96, top two bits in bits 2t of bytes 8 .. 11
+              const uint32_t lo4 = (word_at(bp[r] + 96 + 4 * (t & 1)) >> (4 * (t >> 1))) & 0x0F0F0F0Fu;
+              const uint32_t hi2 = (word_at(bp[r] + 104) >> (2 * t)) & 0x03030303u;
+              const uint32_t sc6 = lo4 | (hi2 << 4);
+              const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(bp[r] + 108)));
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                ds3[r][a] = d * (float)((int)((sc6 >> (8 * a)) & 0xFFu) - 32);  // exact
+            }
+            const bool own2 = t == (g >> 1) && !(g & 1);
+            uint32_t sub4;
+            asm volatile("mov.b32 %0, %1;\n" : "=r"(sub4) : "n"(0x43044304u));  // bf16 (132, 132)
+            float acc[4][4];
+#pragma unroll
+            for (int ah = 0; ah < 2; ++ah) {  // a & 1: bytes 16 (a & 1) .. +15 of the quant / mask runs
+              uint32_t qs[2][4], hm[2][4];
+#pragma unroll
+              for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                  qs[r][b] = word_at(bp[r] + 32 + 32 * (t >> 1) + 16 * ah + 4 * b);
+                  hm[r][b] = word_at(bp[r] + 16 * ah + 4 * b);
+                }
+#pragma unroll
+              for (int a2 = 0; a2 < 2; ++a2) {
+                const int a = 2 * a2 + ah;
+                const uint32_t g2 = (uint32_t)((2 * t + a2) & 3);
+                const uint32_t qsh = 2u * g2;                                   // quant bits in a byte
+                const uint32_t mrot = (4u * (uint32_t)(t >> 1) + g2 - 2u) & 31u;  // mask bit -> bit 2
+                const uint32_t *pb = own2 ? pw + (2 * t + a2) * kPermStride + 8 * ah : zeros;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                  const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * c2 + h;
+                    uint32_t av[4];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                      const uint32_t lw = qs[r][b] >> qsh;
+                      const uint32_t hw = __funnelshift_r(hm[r][b], hm[r][b], mrot);
+                      // (128 + u) for bytes 0, 2 and 1, 3: the two low bits over
+                      // the top bit at bit 2 and the bf16 magic
+                      const uint32_t m02 = lop_bit2(hw, magic), m13 = lop_bit2(hw >> 8, magic);
+                      av[r] = sub_bf16x2(lop_q2(lw, m02), sub4);
+                      av[2 + r] = sub_bf16x2(lop_q2(lw >> 8, m13), sub4);
+                    }
+                    const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
+                    if (b == 0)
+                      mma_bf16_zc(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+                    else
+                      mma_bf16(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float yv = yacc[0][r][0];
+#pragma unroll
+              for (int a = 0; a < 4; ++a) yv = fmaf(ds3[r][a], acc[a][2 * r], yv);
+              yacc[0][r][0] = yv;
+            }
+            __syncwarp();  // every lane's reads of the stage are done
+            if (u == cnt - 1) {
+              if (pp.valid) {  // refill this slot with the stream's next stage
+                issue_w(cslot, pp);
+                issue_x(cslot, pp);
+                pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+              }
+              cp_async_commit();
             }
             pbuf ^= 1;
             continue;
@@ -1011,9 +1141,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
 // variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
-// for Q5_K, q2_K and Q6_K (single ops only)), queried once per device after
-// the attributes are set.
-int g_occ[kMaxDevices][7][2];
+// for Q5_K, q2_K, Q6_K and q3_K (single ops only)), queried once per device
+// after the attributes are set.
+int g_occ[kMaxDevices][8][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
@@ -1047,6 +1177,8 @@ void stream_attributes(int dev) {
   g_occ[dev][5][1] = 0;
   g_occ[dev][6][0] = stream_setup<1, 1, 1, 6>();
   g_occ[dev][6][1] = 0;
+  g_occ[dev][7][0] = stream_setup<1, 1, 1, 3>();
+  g_occ[dev][7][1] = 0;
 }
 
 struct StreamPlan {
@@ -1145,20 +1277,22 @@ int stream_max_batch() { return 4; }
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
-  if (fmt != 4 && !((fmt == 5 || fmt == 2 || fmt == 6) && batch == 1)) return cudaErrorInvalidValue;
+  if (fmt != 4 && !((fmt == 5 || fmt == 2 || fmt == 3 || fmt == 6) && batch == 1))
+    return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
-  if (fmt != 4) {  // Q5_K, q2_K, Q6_K: one launch per op
+  if (fmt != 4) {  // Q5_K, q2_K, q3_K, Q6_K: one launch per op
     for (int64_t i = 0; i < count; ++i) {
       if (ops[i].n <= 0) continue;
       const long long tiles = (ops[i].n + 15) / 16;
-      const int var = fmt == 5 ? 4 : fmt == 2 ? 5 : 6;
+      const int var = fmt == 5 ? 4 : fmt == 2 ? 5 : fmt == 6 ? 6 : 7;
       const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][var][0], 0, f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const cudaError_t e =
           fmt == 5   ? launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
           : fmt == 2 ? launch_stream_chunk<1, 1, 1, 2>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
-                     : launch_stream_chunk<1, 1, 1, 6>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
+          : fmt == 6 ? launch_stream_chunk<1, 1, 1, 6>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
+                     : launch_stream_chunk<1, 1, 1, 3>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
       if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

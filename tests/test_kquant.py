@@ -120,11 +120,11 @@ def test_kq_gemv_longest_row_and_host_memory_rejected(q4k):
 
 
 def _cancel_matrix(fmt, k, seed):
-    """Rows of q2_K, Q5_K or Q6_K blocks; every third row has all weights
+    """Rows of q2_K, q3_K, Q5_K or Q6_K blocks; every third row has all weights
     exactly 0 (q2_K, Q5_K: d sc q = dmin m with q = c for every weight of every
-    sub-block, Q5_K's c up to 31 so that the fifth quant bit is set; Q6_K: every
-    quant at its zero point), the others random."""
-    from _kq_fields import pack_q2k, pack_q5k, pack_q6k, random_block
+    sub-block, Q5_K's c up to 31 so that the fifth quant bit is set; q3_K,
+    Q6_K: every quant at its zero point), the others random."""
+    from _kq_fields import pack_q2k, pack_q3k, pack_q5k, pack_q6k, random_block
     from _q4k_fields import half_bits
     rng = np.random.default_rng(seed)
     rows = []
@@ -136,6 +136,9 @@ def _cancel_matrix(fmt, k, seed):
                 if fmt == 6:  # no min term: every quant at the zero point (u = 32)
                     sc = [int(v) for v in rng.integers(-128, 128, 16)]
                     blks.append(pack_q6k(half_bits(rng.uniform(1e-3, 2e-2)), sc, [0] * 256))
+                elif fmt == 3:  # no min term: every quant at the zero point (u = 4)
+                    sc = [int(v) for v in rng.integers(0, 64, 16)]
+                    blks.append(pack_q3k(half_bits(rng.uniform(1e-3, 2e-2)), sc, [0] * 256))
                 elif fmt == 5:
                     c = [int(v) for v in rng.integers(0, 32, 8)]
                     q = [c[i // 32] for i in range(256)]
@@ -150,12 +153,12 @@ def _cancel_matrix(fmt, k, seed):
     return torch.frombuffer(bytearray(b"".join(rows)), dtype=torch.uint8).view(len(rows), -1)
 
 
-@pytest.mark.parametrize("fmt", [2, 5, 6])
+@pytest.mark.parametrize("fmt", [2, 3, 5, 6])
 @pytest.mark.parametrize("k", [256, 1280, 5120])
 def test_cancelling_rows_give_exact_zero_at_batch_1(q4k, fmt, k):
-    # batch 1 runs q2_K, Q5_K (offset form, c up to 4 and 32) and Q6_K (exact
-    # q - 32) on the tensor cores: rows whose weights are all zero must come
-    # out exactly 0, the rest within the bound
+    # batch 1 runs q2_K, Q5_K (offset form, c up to 4 and 32), q3_K and Q6_K
+    # (exact q - 4, q - 32) on the tensor cores: rows whose weights are all zero
+    # must come out exactly 0, the rest within the bound
     w = _cancel_matrix(fmt, k, seed=k + fmt)
     n = w.shape[0]
     x = synth.bf16_normal((1, k), seed=3 * k + fmt)
@@ -169,13 +172,13 @@ def test_cancelling_rows_give_exact_zero_at_batch_1(q4k, fmt, k):
     check_bound(got, yref, s, TOL, f"kq{fmt} cancel k{k}")
 
 
-@pytest.mark.parametrize("fmt", [2, 5, 6])
+@pytest.mark.parametrize("fmt", [2, 3, 5, 6])
 @pytest.mark.parametrize("n,k", [(4901, 1280), (16 * 152 * 2 + 3, 512), (3, 3 * 256), (1000, 17408)])
 def test_batch_1_tensor_core_formats_many_shapes(q4k, fmt, n, k):
     # many 16-row tiles (more than one per warp) with a ragged last tile, a
-    # single odd row count with an odd number of super-blocks (q2_K and Q6_K
-    # rows then start at every 4- or 2-byte offset mod 16), and long rows (many
-    # ring turns)
+    # single odd row count with an odd number of super-blocks (q2_K, q3_K and
+    # Q6_K rows then start at every 4- or 2-byte offset mod 16), and long rows
+    # (many ring turns)
     w = synth.kq_weight(fmt, n, k, seed=900 + n + fmt)
     x = synth.bf16_normal((1, k), seed=901 + fmt)
     y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x.to(DEV))
