@@ -1,7 +1,8 @@
 // q4k_kquant.cu -- the other k-quant formats: q2_K, q3_K (the routed-down
 // recipes of "Layer Package Repository Spec", section "Policy Resolution"),
 // Q5_K and Q6_K (found in "_XL" mixes): dequantization and the decode
-// projection Y = W X for batch 1..16.
+// projection Y = W X for batch 2..16 (batch 1 runs on the tensor cores in the
+// stream kernel, q4k_stream.cu).
 //
 // Super-blocks of 256 weights (the GGUF k-quant layouts; field offsets below):
 //   q2_K  84 B: sc[16] (scale | min << 4) @0, qs[64] @16, d @80, dmin @82;

@@ -5,7 +5,10 @@
 // decode batches: "PRD: Performant Concurrent Distributed GGUF Runtime",
 // DGR-012), and the fused gate/up projection H[b] = silu(Wg X[b]) * (Wu X[b])
 // of a dense or shared-expert FFN ("Layer Package Repository Spec", section
-// "Policy Resolution": merged shared gate/up).
+// "Policy Resolution": merged shared gate/up).  The same kernel takes batch-1
+// projections of the other k-quant formats (FMT = 2, 3, 5, 6: q2_K, q3_K,
+// Q5_K, Q6_K; "Layer Package Repository Spec", sections "Policy Resolution"
+// and "Repository Identity"), each with its own unpack of the super-block.
 //
 // Work: a tile is 16*MT weight rows of one op over the op's whole K (a GLU op's
 // tile is its gate rows, then the same up rows).  The ops of a launch form one
