@@ -193,6 +193,7 @@ struct StreamCfg {
   // stage copies a row's bytes from its start rounded down to 16 (at most 12
   // or 14 bytes early).
   static constexpr int kLead = FMT == 2 ? 12 : (FMT == 3 || FMT == 6) ? 14 : 0;
+  static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
   static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
                              : FMT == 2 ? Q4K_STREAM_SB_Q2
