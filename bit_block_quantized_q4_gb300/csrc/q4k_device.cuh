@@ -473,6 +473,34 @@ __device__ __forceinline__ void offset_form_c(float d, float nd23, float dmin, f
   sub = __byte_perm(vb, 0u, 0x3232u);
   e = fmaf(ds, __uint_as_float(vb & 0xFFFF0000u) - 128.f, -dm);
 }
+// The offset forms of one sub-block in each of two rows (x: the first row,
+// y: the second) with the paired operations on the packed fp32 pipe; the same
+// c and sub as offset_form_c, and ds, e as exact or as singly rounded.  d and
+// dmin are the two rows' scales, nd23 = -2^23 d and pdm23 = 2^23 dmin; sc_*
+// are the scale bytes as the float 2^23 + sc (byte_magic) and nm_* the min
+// bytes as -(2^23 + m) (byte_magic_neg), so that the fmas below give d sc and
+// -dmin m exactly.  (-dm) * rcp(-CMAX ds) is the ratio of offset_form_c with
+// both signs flipped; ds = +-0 and dm = 0 map to c = 0 or CMAX as there.
+template <int CMAX>
+__device__ __forceinline__ void offset_form_rows2(float2 d, float2 nd23, float2 dmin, float2 pdm23,
+                                                  uint32_t sc_x, uint32_t sc_y, uint32_t nm_x,
+                                                  uint32_t nm_y, float2 &ds, float2 &e,
+                                                  uint32_t &sub_x, uint32_t &sub_y) {
+  static_assert(CMAX == 4 || CMAX == 16 || CMAX == 32, "128 + c must stay in bf16's unit-step range");
+  ds = __ffma2_rn(d, make_float2(__uint_as_float(sc_x), __uint_as_float(sc_y)), nd23);
+  const float2 ndm = __ffma2_rn(dmin, make_float2(__uint_as_float(nm_x), __uint_as_float(nm_y)), pdm23);
+  const float2 t = __fmul2_rn(make_float2(-(float)CMAX, -(float)CMAX), ds);
+  const float ux = __saturatef(fmaf(ndm.x, rcp_approx(t.x), 0.5f / (float)CMAX));
+  const float uy = __saturatef(fmaf(ndm.y, rcp_approx(t.y), 0.5f / (float)CMAX));
+  const float2 v = __ffma2_rn(make_float2(ux, uy), make_float2((float)CMAX, (float)CMAX),
+                              make_float2(128.f, 128.f));
+  const uint32_t vx = __float_as_uint(v.x), vy = __float_as_uint(v.y);
+  sub_x = __byte_perm(vx, 0u, 0x3232u);
+  sub_y = __byte_perm(vy, 0u, 0x3232u);
+  const float2 c = __fadd2_rn(make_float2(__uint_as_float(vx & 0xFFFF0000u), __uint_as_float(vy & 0xFFFF0000u)),
+                              make_float2(-128.f, -128.f));
+  e = __ffma2_rn(ds, c, ndm);
+}
 // Q4_K: q in [0, 15], c in [0, 16].
 __device__ __forceinline__ void offset_form(float d, float nd23, float dmin, float ndm23,
                                             uint32_t sc_magic, uint32_t m_magic, float &ds,
@@ -482,6 +510,10 @@ __device__ __forceinline__ void offset_form(float d, float nd23, float dmin, flo
 // Byte i of w as the float 2^23 + byte (bit pattern 0x4B0000bb).
 __device__ __forceinline__ uint32_t byte_magic(uint32_t w, int i) {
   return __byte_perm(w, 0x4B000000u, 0x7540u + (uint32_t)i);
+}
+// Byte i of w as the float -(2^23 + byte) (bit pattern 0xCB0000bb).
+__device__ __forceinline__ uint32_t byte_magic_neg(uint32_t w, int i) {
+  return __byte_perm(w, 0xCB000000u, 0x7540u + (uint32_t)i);
 }
 
 __device__ __forceinline__ float half_lo_to_float(uint32_t h) {

@@ -151,7 +151,9 @@ constexpr int kPermStride = 20;        // words per sub-block in the permuted x 
 // eight sub-blocks, so that the B-fragment reads of batch rows 2P and 2P+1
 // fall on different banks
 constexpr int kPermWords = 8 * kPermStride + 4;
-constexpr int kMaxOps = 448;           // ops per launch (kernel parameter table, < 32 KB)
+// Q4_K ops (and weight tensor maps) per launch: with a 128-byte map per
+// matrix the kernel parameter table stays under 32 KB.
+constexpr int kMaxOps = 150;
 
 struct StreamOp {
   const uint8_t *w;   // weights; the gate matrix of a GLU op
@@ -161,18 +163,24 @@ struct StreamOp {
   long long byte0;  // weight bytes of the ops before this one
   int n, nsb, ntiles, parts;
   int ldx, ldy;     // batch-row strides of x and y (elements)
+  int map;          // Q4_K: index of the weight matrix's tensor map (the up matrix's is map + 1)
 };
 
 template <int NOPS>
 struct StreamParams {
+  // Q4_K: 2-D tensor maps over the weight matrices (unused by the other
+  // formats); first, for their 64-byte alignment
+  CUtensorMap map[NOPS == 1 ? 2 : NOPS];
+  StreamOp op[NOPS];
+  unsigned *err;  // device error word (a timed-out wait on a stage)
   int nops;
   int batch;     // batch rows (1 .. NB of the kernel)
   int kp;        // warps per tile stream (split of each tile's super-blocks)
   int pre;       // weight stages requested before the dependency wait
   int nstreams;  // tile streams in the grid
   long long total;
-  StreamOp op[NOPS];
 };
+static_assert(sizeof(StreamParams<kMaxOps>) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
@@ -230,13 +238,22 @@ struct StreamCfg {
   // 48 bytes apart (the reads of 8 rows by a warp then hit distinct banks).
   static constexpr int kQhRow = 48;
   static constexpr int kQhBuf = FMT == 5 ? kRows * kQhRow : 0;
+  // Q4_K stages are one TMA tile of the weight matrix (16*MT rows by the row
+  // slot's bytes: with the 16-byte pad the tile reaches 16 bytes into the next
+  // stage, or past the row's end, which reads as zeros) and one bulk copy of x
+  // per batch row, both completing on the slot's mbarrier.  The other formats
+  // copy 16-byte chunks with cp.async.
+  static constexpr bool kTma = FMT == 4;
   // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes |
-  // fifth-bit buffers (Q5_K)
+  // fifth-bit buffers (Q5_K) | ring mbarriers (Q4_K)
   static constexpr int kOffX = kStages * kWBytes;
   static constexpr int kOffPerm = kOffX + kStages * kXStage;
   static constexpr int kOffZero = kOffPerm + kPermBufs * kPermBuf * 4;
   static constexpr int kOffQh = kOffZero + 64;
-  static constexpr int kWarpBytes = (kOffQh + 2 * kQhBuf + 127) / 128 * 128;
+  static constexpr int kOffBar = (kOffQh + 2 * kQhBuf + 7) / 8 * 8;
+  static constexpr int kWarpBytes = (kOffBar + (kTma ? 8 * kStages : 0) + 127) / 128 * 128;
+  static_assert(!kTma || (kWBytes % 128 == 0 && kXStage % 128 == 0 && kRowBytes % 16 == 0),
+                "TMA destinations 128-byte aligned, tile rows whole 16-byte units");
   static constexpr int kRedBytes = 2 * kWarps * 2 * NB * kRows * 4;  // split-K partials
   static constexpr int kSmem = kWarps * kWarpBytes + kRedBytes;
 };
@@ -256,6 +273,7 @@ struct Pos {
   int nrows;            // weight rows of the tile
   long long rstride;    // bytes from one weight row to the next
   const uint8_t *wend;  // end of this part's weight matrix
+  int map;              // Q4_K: tensor map of this part's matrix
 };
 
 template <int NOPS>
@@ -316,6 +334,7 @@ __device__ __forceinline__ void pos_load(const StreamParams<NOPS> &p, int rows, 
   s.wend = w + (size_t)o.n * s.rstride;
   s.xsrc = o.x;
   s.ldx = o.ldx;
+  s.map = o.map + s.part;
 }
 
 // Producer walk over the non-empty stages of a stream, for warp kp of KP:
@@ -378,6 +397,22 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// After a timed-out wait on a Q4_K stage: give the copies still in flight on
+// the ring (the `inflight` stages from slot `slot` on) the same bounded time to
+// land before the warp walks on and its CTA exits.
+__device__ __noinline__ void drain_ring(uint64_t *bars, int stages, int slot, uint32_t phase,
+                                        int inflight) {
+  const uint64_t t0 = global_ns();
+  for (int j = 0; j < inflight; ++j) {
+    while (!mbar_try_wait(&bars[slot], phase, 1000u))
+      if (global_ns() - t0 > kWaitLimitNs) return;
+    if (++slot == stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
 // w >> n, as a shift (ALU pipe) or as the high half of w * 2^(32-n) (FMA pipe).
 template <int N>
 __device__ __forceinline__ uint32_t shr(uint32_t w) {
@@ -417,6 +452,11 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * C::kWarpBytes);
 
   if (lane < 16) reinterpret_cast<uint32_t *>(wreg + C::kOffZero)[lane] = 0u;
+  uint64_t *full = reinterpret_cast<uint64_t *>(wreg + C::kOffBar);  // Q4_K ring mbarriers
+  if (C::kTma && lane == 0) {
+    for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
   __syncwarp();
 
   // ---- producer: the stream's stages in order, STAGES ahead of the consumer
@@ -429,7 +469,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   pos_settle<C::kBlock>(p, TR, hi, kp, pp);  // the first stage (when there is one)
 
   constexpr int SB = C::kSB;
-  // A stage's copies are 16-byte cp.async chunks.  Weights: the LPR lanes
+  // Q4_K: lane 0 arms the slot's mbarrier with the stage's bytes (the whole
+  // weight tile, out-of-range parts included, and x) and requests the weight
+  // tile; lanes b < batch each request x of batch row b.
+  // The other formats: a stage's copies are 16-byte cp.async chunks.  Weights: the LPR lanes
   // LPR r .. LPR r + LPR - 1 take row r of the tile, lane LPR r + i its chunks
   // i, i + LPR, ... of the SB super-blocks (with 16-row tiles a lane pair
   // moves 32 contiguous bytes per instruction); x: lane l takes chunk l of
@@ -439,9 +482,18 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   // flight is always the group ST - 1 places back.
   constexpr int LPR = 32 / TR;
   const int crow = lane / LPR, csub = lane % LPR;
+  const uint64_t pol = C::kTma ? l2_evict_first_policy() : 0ull;
   auto issue_w = [&](int slot, const Pos &s) {
-    if (crow >= s.nrows) return;
     const int cnt = min(SB, s.kb1 - s.sb);
+    if constexpr (C::kTma) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(C::kWBytes + batch * cnt * kXBytes));
+        tma_load_2d_hint(ringw + slot * C::kWBytes, &p.map[s.map], &full[slot],
+                         s.sb * (kBlockBytes / 8), s.tile * TR, pol);
+      }
+      return;
+    }
+    if (crow >= s.nrows) return;
     uint8_t *dst = ringw + slot * C::kWBytes + crow * C::kRowBytes + csub * 16;
     const uint8_t *src = s.src + (size_t)crow * s.rstride + (size_t)s.sb * C::kBlock;
     if constexpr (FMT == 2 || FMT == 3 || FMT == 6) {
@@ -459,15 +511,31 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
         cp_async16(dst + 16 * LPR * j, left > 0 ? cs : src0, left >= 16 ? 16 : left > 0 ? (int)left : 0);
       }
     } else {
-      const int nch = (C::kBlock / 16) * cnt;  // chunks of a row in this stage
+      constexpr int kFull = (C::kBlock / 16) * SB;  // chunks of a row in a full stage
+      if (cnt == SB) {  // (every stage but the last of a warp's share of a tile)
 #pragma unroll
-      for (int j = 0; j < ((C::kBlock / 16) * SB + LPR - 1) / LPR; ++j)
-        if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + csub * 16 + 16 * LPR * j);
+        for (int j = 0; j < kFull / LPR; ++j) cp_async16(dst + 16 * LPR * j, src + csub * 16 + 16 * LPR * j);
+        constexpr int jt = kFull / LPR;
+        if (kFull % LPR != 0 && LPR * jt + csub < kFull)
+          cp_async16(dst + 16 * LPR * jt, src + csub * 16 + 16 * LPR * jt);
+      } else {
+        const int nch = (C::kBlock / 16) * cnt;  // chunks of a row in this stage
+#pragma unroll
+        for (int j = 0; j < (kFull + LPR - 1) / LPR; ++j)
+          if (LPR * j + csub < nch) cp_async16(dst + 16 * LPR * j, src + csub * 16 + 16 * LPR * j);
+      }
     }
   };
   // x of batch row b goes to [b][0 .. SB) of the stage's x area.
   auto issue_x = [&](int slot, const Pos &s) {
     const int cnt = min(SB, s.kb1 - s.sb);
+    if constexpr (C::kTma) {
+      if (lane < batch)
+        bulk_load(ringx + slot * C::kXStage + lane * (SB * kXBytes),
+                  s.xsrc + (size_t)lane * s.ldx + (size_t)s.sb * kQK, (uint32_t)(cnt * kXBytes),
+                  &full[slot]);
+      return;
+    }
     uint8_t *dst = ringx + slot * C::kXStage + lane * 16;
 #pragma unroll
     for (int b = 0; b < NB; ++b)
@@ -490,13 +558,15 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
     }
   }
   grid_dependency_wait();
+  int inflight = 0;  // Q4_K: stages requested and not yet consumed
   for (int s = 0; s < ST; ++s) {
     if (pp.valid) {
       if (s >= npre) issue_w(s, pp);
       issue_x(s, pp);
       pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+      ++inflight;
     }
-    cp_async_commit();  // stage s (an empty group past the stream's end)
+    if constexpr (!C::kTma) cp_async_commit();  // stage s (an empty group past the stream's end)
   }
   grid_launch_dependents();
 
@@ -529,6 +599,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 
   // ---- consumer
   int cslot = 0;
+  uint32_t phase = 0;  // Q4_K: parity of the slot's next phase (flips when cslot wraps)
+  bool ok = true;      // Q4_K: false once a wait on a stage has timed out
   int pbuf = 0;
   int op, tile;
   bool tvalid;
@@ -554,8 +626,21 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 #pragma unroll
         for (int b = 0; b < NB; ++b) yacc[mt][0][b] = yacc[mt][1][b] = 0.f;
       for (int sb = kb0; sb < kb1; sb += SB) {
-        cp_async_wait<ST - 1>();  // this lane's copies of the stage have landed
-        __syncwarp();             // ... and every lane's are visible
+        if constexpr (C::kTma) {
+          // After a timed-out wait the warp walks on without waiting or
+          // computing (so that split-K partners meet it at their barriers).
+          if (!ok) continue;
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[cslot], phase, p.err))) {
+            ok = false;
+            if (lane == 0) drain_ring(full, ST, cslot, phase, inflight);
+            __syncwarp();
+            continue;
+          }
+          --inflight;
+        } else {
+          cp_async_wait<ST - 1>();  // this lane's copies of the stage have landed
+          __syncwarp();             // ... and every lane's are visible
+        }
         const int cnt = min(SB, kb1 - sb);
         const uint8_t *wstage = ringw + cslot * C::kWBytes;
         const uint8_t *xstage = ringx + cslot * C::kXStage;
@@ -610,8 +695,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 issue_w(cslot, pp);
                 issue_x(cslot, pp);
                 pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+                ++inflight;
               }
-              cp_async_commit();
+              if constexpr (!C::kTma) cp_async_commit();
             }
             // Offset forms (c in [0, 4]) of the thread's (row, sub-block) pairs.
             float ds2[2][4], ee2[2][4];
@@ -775,8 +861,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 issue_w(cslot, pp);
                 issue_x(cslot, pp);
                 pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+                ++inflight;
               }
-              cp_async_commit();
+              if constexpr (!C::kTma) cp_async_commit();
             }
             pbuf ^= 1;
             continue;
@@ -895,8 +982,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 issue_w(cslot, pp);
                 issue_x(cslot, pp);
                 pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+                ++inflight;
               }
-              cp_async_commit();
+              if constexpr (!C::kTma) cp_async_commit();
             }
             pbuf ^= 1;
             continue;
@@ -946,8 +1034,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               issue_w(cslot, pp);
               issue_x(cslot, pp);
               pos_next<SB, C::kBlock>(p, TR, hi, kp, pp);
+              ++inflight;
             }
-            cp_async_commit();
+            if constexpr (!C::kTma) cp_async_commit();
           }
 
           // Offset form of this thread's (row, sub-block) pairs.
@@ -961,16 +1050,22 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
             const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
             const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+            // rows g, g+8 as the two lanes of the packed fp32 operations
+            const float2 d2 = make_float2(half_lo_to_float(h0.x), half_lo_to_float(h1.x));
+            const float2 dmin2 = make_float2(half_hi_to_float(h0.x), half_hi_to_float(h1.x));
+            const float2 nd23 = __fmul2_rn(d2, make_float2(-8388608.f, -8388608.f));
+            const float2 pdm23 = __fmul2_rn(dmin2, make_float2(8388608.f, 8388608.f));
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const uint32_t hx = r ? h1.x : h0.x;
-              const float d = half_lo_to_float(hx), dmin = half_hi_to_float(hx);
-              const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
-#pragma unroll
-              for (int e = 0; e < 2; ++e)
-                offset_form_c<FMT == 5 ? 32 : 16>(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e),
-                                                  byte_magic(m4, 2 * r + e), ds[mt][r][e],
-                                                  ee[mt][r][e], sub[mt][r][e]);
+            for (int e = 0; e < 2; ++e) {
+              float2 ds2, ee2;
+              offset_form_rows2<FMT == 5 ? 32 : 16>(d2, nd23, dmin2, pdm23, byte_magic(sc4, e),
+                                                    byte_magic(sc4, 2 + e), byte_magic_neg(m4, e),
+                                                    byte_magic_neg(m4, 2 + e), ds2, ee2,
+                                                    sub[mt][0][e], sub[mt][1][e]);
+              ds[mt][0][e] = ds2.x;
+              ds[mt][1][e] = ds2.y;
+              ee[mt][0][e] = ee2.x;
+              ee[mt][1][e] = ee2.y;
             }
           }
 
@@ -1061,7 +1156,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               }
           if (C::kPermBufs == 2) pbuf ^= 1;
         }
-        if (++cslot == ST) cslot = 0;
+        if (++cslot == ST) {
+          cslot = 0;
+          phase ^= 1u;
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -1135,8 +1233,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
       }
     }
   }
-  // Every stage the warp issued was consumed; nothing is left in flight.
-  cp_async_wait<0>();
+  // Every stage the warp issued was consumed (or, after a timed-out wait,
+  // given the bounded time to land); nothing is left in flight.
+  if constexpr (!C::kTma) cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- host side
@@ -1223,7 +1322,20 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
   memset(&prm, 0, sizeof prm);
   const int TR = 16 * MT;
   long long total = 0;
-  int nops = 0;
+  int nops = 0, nmaps = 0;
+  constexpr int kMapCap = (int)(sizeof prm.map / sizeof prm.map[0]);
+  // Q4_K: the matrix as a 2-D array of 8-byte words, one row per weight row;
+  // a tile is the row slot's words of TR rows
+  auto weight_map = [&](const uint8_t *w, int n, int nsb) -> cudaError_t {
+    if (nmaps >= kMapCap) return cudaErrorInvalidValue;
+    const uint64_t dims[2] = {(uint64_t)nsb * (kBlockBytes / 8), (uint64_t)n};
+    const uint64_t strides[1] = {(uint64_t)nsb * kBlockBytes};
+    const uint32_t box[2] = {(uint32_t)(StreamCfg<MT, NB, FMT>::kRowBytes / 8), (uint32_t)TR};
+    const CUresult r = encode_tiled(&prm.map[nmaps++], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+                                    const_cast<uint8_t *>(w), dims, strides, box,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  };
   for (int i = 0; i < count; ++i) {
     const StreamOpDesc &d = ops[i];
     if (d.n <= 0) continue;
@@ -1239,9 +1351,16 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
     o.ldx = (int)d.ldx;
     o.ldy = (int)d.ldy;
     o.byte0 = total;
+    o.map = nmaps;
+    if (StreamCfg<MT, NB, FMT>::kTma) {
+      cudaError_t e = weight_map(o.w, o.n, o.nsb);
+      if (e == cudaSuccess && o.w2) e = weight_map(o.w2, o.n, o.nsb);
+      if (e != cudaSuccess) return e;
+    }
     total += (long long)d.n * o.nsb * kBlockBytes * o.parts;
   }
   if (nops == 0) return cudaSuccess;
+  prm.err = device_error_word();
   prm.nops = nops;
   prm.batch = batch;
   prm.kp = kp;
@@ -1303,11 +1422,14 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
   const int var1 = batch == 1 ? 0 : batch == 2 ? 2 : 3;  // 16-row kernel of this batch
   int64_t i = 0;
   while (i < count) {
-    // a chunk: up to kMaxOps ops with rows
-    int64_t j = i, used = 0;
+    // a chunk: up to kMaxOps ops with rows and kMaxOps weight matrices
+    int64_t j = i, used = 0, maps = 0;
     long long tiles1 = 0, tiles2 = 0;
     while (j < count && used < kMaxOps) {
       if (ops[j].n > 0) {
+        const int need = ops[j].w_up ? 2 : 1;  // tensor maps of the op's matrices
+        if (maps + need > kMaxOps) break;
+        maps += need;
         ++used;
         tiles1 += (ops[j].n + 15) / 16;
         tiles2 += (ops[j].n + 31) / 32;
