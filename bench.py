@@ -218,7 +218,8 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
         ms, per, g = time_graph(step, steps, warmup, stream)
     del g
     nbytes = layers.algorithmic_bytes(batch)
-    launches = (len(layers.mats) + 511) // 512 if batch == 1 else len(layers.mats)
+    per_launch = q4k.Q4K_SEQ_MATRICES_PER_LAUNCH if batch <= 4 else q4k.Q4K_SEQ_WIDE_OPS_PER_LAUNCH
+    launches = -(-len(layers.mats) // per_launch)
     return {"ms_per_step": ms, "ms_min": min(per), "gbs": nbytes / (ms * 1e-3) / 1e9,
             "bytes_per_step": nbytes, "launches_per_step": launches,
             "verified": verify_decode(layers, xs, ys)}
@@ -917,8 +918,8 @@ def main():
                          "traffic": profiled_traffic(nbytes / launches), "peak_source": pk["source"],
                          "algorithmic_bytes_per_launch": round(nbytes / launches),
                          "kernel": "gemv_stream_kernel (q4k_gemv_seq, batch 1: the 320 projections "
-                                   "as one persistent launch)",
-                         "note": "CUDA events around each graph replay of the one launch; "
+                                   "as %d persistent launches of %d)" % (launches, -(-320 // launches)),
+                         "note": "CUDA events around each graph replay of the pass's launches; "
                                  "peak = measured copy bandwidth (read + write)"},
             "verified_worst_err_over_bound": head["verified"],
             "cpu_baseline": cpu,

@@ -51,6 +51,7 @@
 #include <mutex>
 #include <vector>
 
+#include "q4k.h"
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
@@ -151,9 +152,9 @@ constexpr int kPermStride = 20;        // words per sub-block in the permuted x 
 // eight sub-blocks, so that the B-fragment reads of batch rows 2P and 2P+1
 // fall on different banks
 constexpr int kPermWords = 8 * kPermStride + 4;
-// Q4_K ops (and weight tensor maps) per launch: with a 128-byte map per
-// matrix the kernel parameter table stays under 32 KB.
-constexpr int kMaxOps = 150;
+// Q4_K weight matrices (tensor maps) and ops per launch: with a 128-byte map
+// per matrix the kernel parameter table stays under 32 KB.
+constexpr int kMaxOps = Q4K_SEQ_MATRICES_PER_LAUNCH;
 
 struct StreamOp {
   const uint8_t *w;   // weights; the gate matrix of a GLU op
@@ -644,6 +645,46 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
         const int cnt = min(SB, kb1 - sb);
         const uint8_t *wstage = ringw + cslot * C::kWBytes;
         const uint8_t *xstage = ringx + cslot * C::kXStage;
+        // Q4_K, Q5_K: the offset forms of this thread's (row, sub-block)
+        // pairs for every super-block of the stage first, so that their
+        // dependency chains (header loads, reciprocals) run side by side and
+        // under the unpack of the first super-block.
+        float dsS[SB][MT][2][2], eeS[SB][MT][2][2];
+        uint32_t subS[SB][MT][2][2];
+        if constexpr (FMT == 4 || FMT == 5) {
+#pragma unroll
+          for (int u = 0; u < SB; ++u) {
+            if (u >= cnt) break;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const uint8_t *rp = wstage + u * C::kBlock + (mt * 16 + g) * C::kRowBytes;
+              const uint4 h0 = *reinterpret_cast<const uint4 *>(rp);
+              const uint4 h1 = *reinterpret_cast<const uint4 *>(rp + 8 * C::kRowBytes);
+              const uint32_t py = __byte_perm(h0.y, h1.y, psel);
+              const uint32_t pz = __byte_perm(h0.z, h1.z, psel);
+              const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
+              const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
+              const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+              // rows g, g+8 as the two lanes of the packed fp32 operations
+              const float2 d2 = make_float2(half_lo_to_float(h0.x), half_lo_to_float(h1.x));
+              const float2 dmin2 = make_float2(half_hi_to_float(h0.x), half_hi_to_float(h1.x));
+              const float2 nd23 = __fmul2_rn(d2, make_float2(-8388608.f, -8388608.f));
+              const float2 pdm23 = __fmul2_rn(dmin2, make_float2(8388608.f, 8388608.f));
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float2 ds2, ee2;
+                offset_form_rows2<FMT == 5 ? 32 : 16>(d2, nd23, dmin2, pdm23, byte_magic(sc4, e),
+                                                      byte_magic(sc4, 2 + e), byte_magic_neg(m4, e),
+                                                      byte_magic_neg(m4, 2 + e), ds2, ee2,
+                                                      subS[u][mt][0][e], subS[u][mt][1][e]);
+                dsS[u][mt][0][e] = ds2.x;
+                dsS[u][mt][1][e] = ds2.y;
+                eeS[u][mt][0][e] = ee2.x;
+                eeS[u][mt][1][e] = ee2.y;
+              }
+            }
+          }
+        }
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
           if (u >= cnt) break;
@@ -1008,13 +1049,12 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
             reinterpret_cast<uint4 *>(pw + b * kPermWords + g * kPermStride)[t] = pm;
           }
-          uint4 hdr[MT][2], qa[MT][2][2];
+          uint4 qa[MT][2][2];
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
               const uint8_t *rp = ws + (mt * 16 + g + 8 * r) * C::kRowBytes;
-              hdr[mt][r] = *reinterpret_cast<const uint4 *>(rp);
               qa[mt][r][0] = *reinterpret_cast<const uint4 *>(rp + C::kQs + 32 * t);
               qa[mt][r][1] = *reinterpret_cast<const uint4 *>(rp + C::kQs + 32 * t + 16);
             }
@@ -1039,35 +1079,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             if constexpr (!C::kTma) cp_async_commit();
           }
 
-          // Offset form of this thread's (row, sub-block) pairs.
-          float ds[MT][2][2], ee[MT][2][2];
-          uint32_t sub[MT][2][2];
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint4 h0 = hdr[mt][0], h1 = hdr[mt][1];
-            const uint32_t py = __byte_perm(h0.y, h1.y, psel);
-            const uint32_t pz = __byte_perm(h0.z, h1.z, psel);
-            const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
-            const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
-            const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
-            // rows g, g+8 as the two lanes of the packed fp32 operations
-            const float2 d2 = make_float2(half_lo_to_float(h0.x), half_lo_to_float(h1.x));
-            const float2 dmin2 = make_float2(half_hi_to_float(h0.x), half_hi_to_float(h1.x));
-            const float2 nd23 = __fmul2_rn(d2, make_float2(-8388608.f, -8388608.f));
-            const float2 pdm23 = __fmul2_rn(dmin2, make_float2(8388608.f, 8388608.f));
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float2 ds2, ee2;
-              offset_form_rows2<FMT == 5 ? 32 : 16>(d2, nd23, dmin2, pdm23, byte_magic(sc4, e),
-                                                    byte_magic(sc4, 2 + e), byte_magic_neg(m4, e),
-                                                    byte_magic_neg(m4, 2 + e), ds2, ee2,
-                                                    sub[mt][0][e], sub[mt][1][e]);
-              ds[mt][0][e] = ds2.x;
-              ds[mt][1][e] = ds2.y;
-              ee[mt][0][e] = ee2.x;
-              ee[mt][1][e] = ee2.y;
-            }
-          }
+          // this super-block's offset forms (computed above)
+          const float(&ds)[MT][2][2] = dsS[u];
+          const float(&ee)[MT][2][2] = eeS[u];
+          const uint32_t(&sub)[MT][2][2] = subS[u];
 
           const uint32_t *pe[NP], *po[NP];
 #pragma unroll
@@ -1420,15 +1435,22 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
     return cudaGetLastError();
   }
   const int var1 = batch == 1 ? 0 : batch == 2 ? 2 : 3;  // 16-row kernel of this batch
+  // Launches: as few as the kMaxOps weight matrices per launch allow, each
+  // taking about the same number of matrices.
+  long long mats = 0;
+  for (int64_t i = 0; i < count; ++i)
+    if (ops[i].n > 0) mats += ops[i].w_up ? 2 : 1;
+  const long long nlaunch = (mats + kMaxOps - 1) / kMaxOps;
+  const long long per = nlaunch > 0 ? (mats + nlaunch - 1) / nlaunch : kMaxOps;
   int64_t i = 0;
   while (i < count) {
-    // a chunk: up to kMaxOps ops with rows and kMaxOps weight matrices
+    // a chunk: ops with rows holding at most `per` weight matrices
     int64_t j = i, used = 0, maps = 0;
     long long tiles1 = 0, tiles2 = 0;
-    while (j < count && used < kMaxOps) {
+    while (j < count) {
       if (ops[j].n > 0) {
         const int need = ops[j].w_up ? 2 : 1;  // tensor maps of the op's matrices
-        if (maps + need > kMaxOps) break;
+        if (used > 0 && maps + need > per) break;
         maps += need;
         ++used;
         tiles1 += (ops[j].n + 15) / 16;

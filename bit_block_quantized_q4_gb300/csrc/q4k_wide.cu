@@ -29,6 +29,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "q4k.h"
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
@@ -58,7 +59,7 @@ namespace {
 constexpr int kWideWarps = 4;
 constexpr int kWideThreads = kWideWarps * 32;
 constexpr int kWideRows = 16 * kWideWarps;  // rows per tile
-constexpr int kWideMaxOps = 448;            // ops per launch (kernel parameter table)
+constexpr int kWideMaxOps = Q4K_SEQ_WIDE_OPS_PER_LAUNCH;  // ops per launch (kernel parameter table)
 // x rows in a stage: 512 bytes of a super-block plus 64 bytes, so that the
 // 16-byte fragment reads of 8 batch rows by a quarter warp hit distinct banks.
 constexpr int kXRowBytes = 576;

@@ -109,6 +109,17 @@ def test_gemv_op_struct_layout_matches_the_header():
     assert GemvOp.w_up.offset == 56
 
 
+def test_binding_constants_match_the_header():
+    import bit_block_quantized_q4_gb300 as q4k
+    text = open(HEADER).read()
+    for name in ("Q4K_ABI_VERSION", "Q4K_FLAG_OVERLAP_WEIGHTS", "Q4K_MOE_WEIGHTED_DOWN",
+                 "Q4K_SEQ_MATRICES_PER_LAUNCH", "Q4K_SEQ_WIDE_OPS_PER_LAUNCH"):
+        m = re.search(r"#define %s (\d+)u?\b" % name, text)
+        assert m, name
+        if hasattr(q4k, name):
+            assert getattr(q4k, name) == int(m.group(1)), name
+
+
 def test_gemv_seq_checks_every_op_before_launching(L):
     from bit_block_quantized_q4_gb300 import GemvOp
     good = GemvOp(P, 4, 256, P, 256, P, 4)
