@@ -475,17 +475,18 @@ __device__ __forceinline__ void offset_form_c(float d, float nd23, float dmin, f
 }
 // The offset forms of one sub-block in each of two rows (x: the first row,
 // y: the second) with the paired operations on the packed fp32 pipe; the same
-// c and sub as offset_form_c, and ds, e as exact or as singly rounded.  d and
+// c as offset_form_c (v_*: the fp32 128 + CMAX u, whose bf16 truncation is
+// 128 + c), and ds, e as exact or as singly rounded.  d and
 // dmin are the two rows' scales, nd23 = -2^23 d and pdm23 = 2^23 dmin; sc_*
 // are the scale bytes as the float 2^23 + sc (byte_magic) and nm_* the min
 // bytes as -(2^23 + m) (byte_magic_neg), so that the fmas below give d sc and
 // -dmin m exactly.  (-dm) * rcp(-CMAX ds) is the ratio of offset_form_c with
 // both signs flipped; ds = +-0 and dm = 0 map to c = 0 or CMAX as there.
 template <int CMAX>
-__device__ __forceinline__ void offset_form_rows2(float2 d, float2 nd23, float2 dmin, float2 pdm23,
-                                                  uint32_t sc_x, uint32_t sc_y, uint32_t nm_x,
-                                                  uint32_t nm_y, float2 &ds, float2 &e,
-                                                  uint32_t &sub_x, uint32_t &sub_y) {
+__device__ __forceinline__ void offset_form_rows2_v(float2 d, float2 nd23, float2 dmin, float2 pdm23,
+                                                    uint32_t sc_x, uint32_t sc_y, uint32_t nm_x,
+                                                    uint32_t nm_y, float2 &ds, float2 &e,
+                                                    uint32_t &v_x, uint32_t &v_y) {
   static_assert(CMAX == 4 || CMAX == 16 || CMAX == 32, "128 + c must stay in bf16's unit-step range");
   ds = __ffma2_rn(d, make_float2(__uint_as_float(sc_x), __uint_as_float(sc_y)), nd23);
   const float2 ndm = __ffma2_rn(dmin, make_float2(__uint_as_float(nm_x), __uint_as_float(nm_y)), pdm23);
@@ -494,12 +495,43 @@ __device__ __forceinline__ void offset_form_rows2(float2 d, float2 nd23, float2 
   const float uy = __saturatef(fmaf(ndm.y, rcp_approx(t.y), 0.5f / (float)CMAX));
   const float2 v = __ffma2_rn(make_float2(ux, uy), make_float2((float)CMAX, (float)CMAX),
                               make_float2(128.f, 128.f));
-  const uint32_t vx = __float_as_uint(v.x), vy = __float_as_uint(v.y);
-  sub_x = __byte_perm(vx, 0u, 0x3232u);
-  sub_y = __byte_perm(vy, 0u, 0x3232u);
-  const float2 c = __fadd2_rn(make_float2(__uint_as_float(vx & 0xFFFF0000u), __uint_as_float(vy & 0xFFFF0000u)),
+  v_x = __float_as_uint(v.x);
+  v_y = __float_as_uint(v.y);
+  const float2 c = __fadd2_rn(make_float2(__uint_as_float(v_x & 0xFFFF0000u), __uint_as_float(v_y & 0xFFFF0000u)),
                               make_float2(-128.f, -128.f));
   e = __ffma2_rn(ds, c, ndm);
+}
+// ... with the subtrahends as bf16 pairs (128 + c, 128 + c) of each row.
+template <int CMAX>
+__device__ __forceinline__ void offset_form_rows2(float2 d, float2 nd23, float2 dmin, float2 pdm23,
+                                                  uint32_t sc_x, uint32_t sc_y, uint32_t nm_x,
+                                                  uint32_t nm_y, float2 &ds, float2 &e,
+                                                  uint32_t &sub_x, uint32_t &sub_y) {
+  uint32_t v_x, v_y;
+  offset_form_rows2_v<CMAX>(d, nd23, dmin, pdm23, sc_x, sc_y, nm_x, nm_y, ds, e, v_x, v_y);
+  sub_x = __byte_perm(v_x, 0u, 0x3232u);
+  sub_y = __byte_perm(v_y, 0u, 0x3232u);
+}
+// ... with the subtrahends of both rows packed in one word: (128 + c_x, 128 + c_y).
+template <int CMAX>
+__device__ __forceinline__ void offset_form_rows2_packed(float2 d, float2 nd23, float2 dmin,
+                                                         float2 pdm23, uint32_t sc_x, uint32_t sc_y,
+                                                         uint32_t nm_x, uint32_t nm_y, float2 &ds,
+                                                         float2 &e, uint32_t &sub_xy) {
+  uint32_t v_x, v_y;
+  offset_form_rows2_v<CMAX>(d, nd23, dmin, pdm23, sc_x, sc_y, nm_x, nm_y, ds, e, v_x, v_y);
+  sub_xy = __byte_perm(v_x, v_y, 0x7632u);
+}
+// d, dmin of two rows' super-blocks (the first words of their headers) as the
+// pairs offset_form_rows2 takes, with nd23 = -2^23 d and pdm23 = 2^23 dmin.
+__device__ __forceinline__ void scale_pairs(uint32_t h_x, uint32_t h_y, float2 &d, float2 &nd23,
+                                            float2 &dmin, float2 &pdm23) {
+  d = make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h_x & 0xFFFFu))),
+                  __half2float(__ushort_as_half(static_cast<unsigned short>(h_y & 0xFFFFu))));
+  dmin = make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h_x >> 16))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(h_y >> 16))));
+  nd23 = __fmul2_rn(d, make_float2(-8388608.f, -8388608.f));
+  pdm23 = __fmul2_rn(dmin, make_float2(8388608.f, 8388608.f));
 }
 // Q4_K: q in [0, 15], c in [0, 16].
 __device__ __forceinline__ void offset_form(float d, float nd23, float dmin, float ndm23,

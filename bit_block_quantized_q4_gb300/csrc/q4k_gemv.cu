@@ -210,21 +210,26 @@ __global__ void __launch_bounds__(256) gemv_bn_kernel(const __grid_constant__ CU
     for (int mi = 0; mi < NM; ++mi)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        uint32_t sub[2][2];
+        uint32_t sc2[2], m2[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const uint4 h = hdr[mi][mt][r];
-          uint32_t sc2, m2;
-          scales_pair(h.y, h.z, h.w, t, &sc2, &m2);
-          const float d = half_lo_to_float(h.x), dmin = half_hi_to_float(h.x);
-          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            offset_form(d, nd23, dmin, ndm23, byte_magic(sc2, e), byte_magic(m2, e),
-                        dsv[mi][mt][r][e], eev[mi][mt][r][e], sub[r][e]);
+          scales_pair(h.y, h.z, h.w, t, &sc2[r], &m2[r]);
         }
+        // rows g, g+8 as the two lanes of the packed fp32 operations
+        float2 d2, nd23, dmin2, pdm23;
+        scale_pairs(hdr[mi][mt][0].x, hdr[mi][mt][1].x, d2, nd23, dmin2, pdm23);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) subp[mi][mt][e] = __byte_perm(sub[0][e], sub[1][e], 0x5410u);
+        for (int e = 0; e < 2; ++e) {
+          float2 ds2, ee2;
+          offset_form_rows2_packed<16>(d2, nd23, dmin2, pdm23, byte_magic(sc2[0], e),
+                                       byte_magic(sc2[1], e), byte_magic_neg(m2[0], e),
+                                       byte_magic_neg(m2[1], e), ds2, ee2, subp[mi][mt][e]);
+          dsv[mi][mt][0][e] = ds2.x;
+          dsv[mi][mt][1][e] = ds2.y;
+          eev[mi][mt][0][e] = ee2.x;
+          eev[mi][mt][1][e] = ee2.y;
+        }
       }
     auto sub_block = [&](int j, const uint4(&xv)[NT]) {
       const int c = j >> 1;

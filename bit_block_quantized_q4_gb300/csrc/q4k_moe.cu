@@ -356,20 +356,24 @@ __device__ __forceinline__ bool expert_body(const CUtensorMap *map0p, const CUte
       uint32_t subp[NM][2];
 #pragma unroll
       for (int mi = 0; mi < NM; ++mi) {
-        uint32_t sub[2][2];
+        uint32_t sc2[2], m2[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          uint32_t sc2, m2;
-          scales_pair(hdr[mi][r].y, hdr[mi][r].z, hdr[mi][r].w, t, &sc2, &m2);
-          const float d = half_lo_to_float(hdr[mi][r].x), dmin = half_hi_to_float(hdr[mi][r].x);
-          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+        for (int r = 0; r < 2; ++r)
+          scales_pair(hdr[mi][r].y, hdr[mi][r].z, hdr[mi][r].w, t, &sc2[r], &m2[r]);
+        // rows g, g+8 as the two lanes of the packed fp32 operations
+        float2 d2, nd23, dmin2, pdm23;
+        scale_pairs(hdr[mi][0].x, hdr[mi][1].x, d2, nd23, dmin2, pdm23);
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            offset_form(d, nd23, dmin, ndm23, byte_magic(sc2, e), byte_magic(m2, e),
-                        dsv[mi][r][e], eev[mi][r][e], sub[r][e]);
+        for (int e = 0; e < 2; ++e) {
+          float2 ds2, ee2;
+          offset_form_rows2_packed<16>(d2, nd23, dmin2, pdm23, byte_magic(sc2[0], e),
+                                       byte_magic(sc2[1], e), byte_magic_neg(m2[0], e),
+                                       byte_magic_neg(m2[1], e), ds2, ee2, subp[mi][e]);
+          dsv[mi][0][e] = ds2.x;
+          dsv[mi][1][e] = ds2.y;
+          eev[mi][0][e] = ee2.x;
+          eev[mi][1][e] = ee2.y;
         }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) subp[mi][e] = __byte_perm(sub[0][e], sub[1][e], 0x5410u);
       }
       auto sub_block = [&](int jb, const uint4(&xv)[NT]) {
         const int c = jb >> 1;
@@ -652,15 +656,19 @@ __device__ __forceinline__ bool expert_body_pair(const CUtensorMap *map0p, const
         const uint32_t pw4 = __byte_perm(h0.w, h1.w, psel);
         const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
         const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
+        // rows g, g+8 as the two lanes of the packed fp32 operations
+        float2 d2, nd23, dmin2, pdm23;
+        scale_pairs(h0.x, h1.x, d2, nd23, dmin2, pdm23);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint32_t hx = r ? h1.x : h0.x;
-          const float d = half_lo_to_float(hx), dmin = half_hi_to_float(hx);
-          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            offset_form(d, nd23, dmin, ndm23, byte_magic(sc4, 2 * r + e), byte_magic(m4, 2 * r + e),
-                        ds[mi][r][e], ee[mi][r][e], sub[mi][r][e]);
+        for (int e = 0; e < 2; ++e) {
+          float2 ds2, ee2;
+          offset_form_rows2<16>(d2, nd23, dmin2, pdm23, byte_magic(sc4, e), byte_magic(sc4, 2 + e),
+                                byte_magic_neg(m4, e), byte_magic_neg(m4, 2 + e), ds2, ee2,
+                                sub[mi][0][e], sub[mi][1][e]);
+          ds[mi][0][e] = ds2.x;
+          ds[mi][1][e] = ds2.y;
+          ee[mi][0][e] = ee2.x;
+          ee[mi][1][e] = ee2.y;
         }
       }
       // accE[mi] column 2t + c = sum (q - c_j) x over sub-block 2t of column c

@@ -666,10 +666,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               const uint32_t sc4 = ((upper ? pw4 : py) & mlo4) | ((py >> 2) & mhi4);
               const uint32_t m4 = ((upper ? (pw4 >> 4) : pz) & mlo4) | ((pz >> 2) & mhi4);
               // rows g, g+8 as the two lanes of the packed fp32 operations
-              const float2 d2 = make_float2(half_lo_to_float(h0.x), half_lo_to_float(h1.x));
-              const float2 dmin2 = make_float2(half_hi_to_float(h0.x), half_hi_to_float(h1.x));
-              const float2 nd23 = __fmul2_rn(d2, make_float2(-8388608.f, -8388608.f));
-              const float2 pdm23 = __fmul2_rn(dmin2, make_float2(8388608.f, 8388608.f));
+              float2 d2, nd23, dmin2, pdm23;
+              scale_pairs(h0.x, h1.x, d2, nd23, dmin2, pdm23);
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 float2 ds2, ee2;

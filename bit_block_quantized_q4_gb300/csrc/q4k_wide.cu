@@ -296,20 +296,23 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
       float dsv[2][2], eev[2][2];
       uint32_t subp[2];
       {
-        uint32_t sub[2][2];
+        uint32_t sc2[2], m2[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          uint32_t sc2, m2;
-          scales_pair(hdr[r].y, hdr[r].z, hdr[r].w, t, &sc2, &m2);
-          const float d = half_lo_to_float(hdr[r].x), dmin = half_hi_to_float(hdr[r].x);
-          const float nd23 = d * -8388608.f, ndm23 = dmin * -8388608.f;
+        for (int r = 0; r < 2; ++r) scales_pair(hdr[r].y, hdr[r].z, hdr[r].w, t, &sc2[r], &m2[r]);
+        // rows g, g+8 as the two lanes of the packed fp32 operations
+        float2 d2, nd23, dmin2, pdm23;
+        scale_pairs(hdr[0].x, hdr[1].x, d2, nd23, dmin2, pdm23);
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            offset_form(d, nd23, dmin, ndm23, byte_magic(sc2, e), byte_magic(m2, e), dsv[r][e],
-                        eev[r][e], sub[r][e]);
+        for (int e = 0; e < 2; ++e) {
+          float2 ds2, ee2;
+          offset_form_rows2_packed<16>(d2, nd23, dmin2, pdm23, byte_magic(sc2[0], e),
+                                       byte_magic(sc2[1], e), byte_magic_neg(m2[0], e),
+                                       byte_magic_neg(m2[1], e), ds2, ee2, subp[e]);
+          dsv[0][e] = ds2.x;
+          dsv[1][e] = ds2.y;
+          eev[0][e] = ee2.x;
+          eev[1][e] = ee2.y;
         }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) subp[e] = __byte_perm(sub[0][e], sub[1][e], 0x5410u);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
