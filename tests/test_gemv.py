@@ -106,6 +106,43 @@ def test_gemv_seq_matches_oracle(q4k, batch, flags):
         assert torch.equal(a, b), "a sequence is deterministic"
 
 
+@pytest.mark.parametrize("batch,flags,count", [(1, 1, 170), (1, 0, 341), (2, 1, 170), (4, 1, 200)])
+def test_gemv_seq_several_launches(q4k, batch, flags, count):
+    # at batch 1..4 a launch takes Q4K_SEQ_MATRICES_PER_LAUNCH weight matrices
+    # (a fused gate/up op counts two): sequences of 170-341 small ops (empty
+    # ops and fused gate/up ops among them) run as two or three launches, and
+    # every op matches the oracle
+    rng = np.random.default_rng(4100 + count + batch)
+    shapes = [(int(rng.integers(0, 48)), int(rng.choice([256, 512, 768]))) for _ in range(count)]
+    glu = {i for i in range(count) if i % 7 == 3}
+    mats = sum((2 if i in glu else 1) for i, (n, _) in enumerate(shapes) if n > 0)
+    assert mats > q4k.Q4K_SEQ_MATRICES_PER_LAUNCH
+    ws, wus, xs, ys, tup = [], [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        w = synth.q4k_weight(max(n, 1), k, seed=6100 + i, quants="normal")
+        wu = synth.q4k_weight(max(n, 1), k, seed=6400 + i) if i in glu else None
+        x = synth.bf16_normal((batch, k), seed=6700 + i, sigma=0.05 if i in glu else 1.0)
+        y = torch.full((batch, max(n, 1)), 7.0, device=DEV)
+        ws.append(w)
+        wus.append(wu)
+        xs.append(x)
+        ys.append(y)
+        dw, dx = w.to(DEV), x.to(DEV)
+        tup.append((dw, n, k, dx, y) if wu is None else (dw, n, k, dx, y, wu.to(DEV)))
+    ops = q4k.gemv_ops(tup)
+    q4k.q4k_gemv_seq(ops, batch, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    for i, ((n, k), w, wu, x, y) in enumerate(zip(shapes, ws, wus, xs, ys)):
+        if n == 0:
+            assert bool((y == 7.0).all()), "an empty op writes nothing"
+        elif wu is None:
+            yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+            check_bound(y.cpu().numpy(), yref, s, TOL, f"seq op {i} {n}x{k} b{batch}")
+        else:
+            check_glu(y.cpu().numpy(), w, wu, n, k, x, f"seq glu op {i} {n}x{k} b{batch}")
+
+
 @pytest.mark.parametrize("batch,flags", [(5, 1), (8, 0), (9, 1), (16, 1)])
 def test_gemv_seq_persistent_64_row_tiles(q4k, batch, flags):
     # batch 5..16 with enough 64-row tiles to fill the GPU (at least two per
