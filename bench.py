@@ -587,7 +587,8 @@ def bench_moe_prefill(q4k, dev, stream, reps=10):
 def bench_kquant(q4k, dev, stream, reps=10):
     """Batch-1 decode projection in the other k-quant formats on the 27B-class
     down shape (5120 x 17408): a pool of 8 matrices per format (more than L2
-    for every format) multiplied in turn; bytes = weights + x + y."""
+    for every format) multiplied in turn, as one q4k_kq_gemv call each and as
+    one q4k_kq_gemv_seq call over the pool; bytes = weights + x + y."""
     n, k, pool = 5120, 17408, 8
     out = {}
     names = {2: "q2_K", 3: "q3_K", 5: "Q5_K", 6: "Q6_K"}
@@ -595,17 +596,23 @@ def bench_kquant(q4k, dev, stream, reps=10):
         ws = [synth.kq_weight(fmt, n, k, seed=synth.derive_seed(1008, name, i), device=dev)
               for i in range(pool)]
         x = synth.bf16_normal((1, k), seed=synth.derive_seed(1008, "x"), device=dev)
-        y = torch.empty((1, n), dtype=torch.float32, device=dev)
+        ys = [torch.empty((1, n), dtype=torch.float32, device=dev) for _ in range(pool)]
 
         def step():
-            for w in ws:
+            for w, y in zip(ws, ys):
                 q4k.q4k_kq_gemv(fmt, w, n, k, x, out=y, stream=stream)
 
         ms, per, g = time_graph(step, reps, 3, stream)
         del g
+        ops = q4k.gemv_ops([(w, n, k, x, y) for w, y in zip(ws, ys)])
+        ms_seq, _, g = time_graph(lambda: q4k.q4k_kq_gemv_seq(fmt, ops, 1, q4k.Q4K_FLAG_OVERLAP_WEIGHTS,
+                                                                stream=stream), reps, 3, stream)
+        del g
         nbytes = pool * (ws[0].numel() + 2 * k + 4 * n)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"us_per_gemv": round(ms * 1e3 / pool, 2), "gbs": round(gbs, 1),
+                     "us_per_gemv_seq": round(ms_seq * 1e3 / pool, 2),
+                     "gbs_seq": round(nbytes / (ms_seq * 1e-3) / 1e9, 1),
                      "bytes_per_weight": round(ws[0].numel() / (n * k), 4)}
         del ws
         torch.cuda.empty_cache()

@@ -29,7 +29,7 @@ Q4K_SEQ_WIDE_OPS_PER_LAUNCH = 448
 Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm", "q4k_gemm_rmsnorm",
-           "q4k_kq_block_bytes", "q4k_kq_dequant", "q4k_kq_gemv",
+           "q4k_kq_block_bytes", "q4k_kq_dequant", "q4k_kq_gemv", "q4k_kq_gemv_seq",
            "q4k_moe_workspace_size", "q4k_moe_workspace_views", "q4k_moe_gemv",
            "q4k_moe_gemv_ex", "q4k_moe_gemv_noalloc", "q4k_moe_prefill",
            "q4k_moe_prefill_workspace_size",
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.q4k_kq_dequant.argtypes = [I32, P, I64, I64, P, ctypes.c_int, P]
         L.q4k_kq_gemv.restype = ctypes.c_int
         L.q4k_kq_gemv.argtypes = [I32, P, I64, I64, P, I64, I64, P, I64, P]
+        L.q4k_kq_gemv_seq.restype = ctypes.c_int
+        L.q4k_kq_gemv_seq.argtypes = [I32, ctypes.POINTER(GemvOp), I64, I64, ctypes.c_uint32, P]
         L.q4k_gemm_rmsnorm.restype = ctypes.c_int
         L.q4k_gemm_rmsnorm.argtypes = [P, I64, I64, P, I64, I64, P, ctypes.c_float, P, P, I64, P]
         L.q4k_moe_workspace_size.restype = SZ
@@ -240,6 +242,14 @@ def q4k_kq_gemv(fmt: int, w: torch.Tensor, n: int, k: int, x: torch.Tensor, out=
     _check(lib().q4k_kq_gemv(fmt, _ptr(w), n, k, _ptr(x2), batch, x2.stride(0), _ptr(out),
                              out.stride(0), _stream(stream)), "q4k_kq_gemv")
     return out
+
+
+def q4k_kq_gemv_seq(fmt: int, ops, batch: int, flags: int = 0, stream=None) -> None:
+    """q4k_gemv_seq for k-quant matrices of format fmt (ops: gemv_ops(...) of
+    (w, n, k, x, y) tuples, or such a list), as q4k_kq_gemv for each in turn."""
+    arr = ops if isinstance(ops, ctypes.Array) else gemv_ops(ops)
+    _check(lib().q4k_kq_gemv_seq(fmt, arr, len(arr), batch, flags, _stream(stream)),
+           "q4k_kq_gemv_seq")
 
 
 def q4k_gemm_rmsnorm(w: torch.Tensor, n: int, k: int, x: torch.Tensor, gamma: torch.Tensor,

@@ -355,26 +355,87 @@ int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *ou
       launch_kq_dequant(format, w, n, k, out, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
-int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
-                int64_t ldx, float *y, int64_t ldy, void *stream) {
-  if (format == 4) return q4k_gemv(w, n, k, x, batch, ldx, y, ldy, stream);
+namespace {
+// Argument checks of one k-quant projection (format != 4), before any launch.
+int check_kq(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+             int64_t ldx, const float *y, int64_t ldy, bool *empty) {
+  *empty = false;
   if (kq_block_bytes(format) == 0) return Q4K_ERR_SHAPE;
   if (n < 0 || k <= 0 || (k % kQK) != 0 || batch < 0 || batch > 16) return Q4K_ERR_SHAPE;
   if (n > INT32_MAX / 2 || kq_gemv_smem(format, k) > 227 * 1024) return Q4K_ERR_SHAPE;
-  if (n == 0 || batch == 0) return Q4K_OK;
+  if (n == 0 || batch == 0) {
+    *empty = true;
+    return Q4K_OK;
+  }
   if (ldx < k || ldy < n) return Q4K_ERR_SHAPE;
   if (!w || !x || !y) return Q4K_ERR_NULL;
   if (!aligned(w, 16) || !aligned(x, 16) || (ldx % 8) != 0 || !aligned(y, 4)) return Q4K_ERR_ALIGN;
-  int st = check_device();
+  return Q4K_OK;
+}
+}  // namespace
+
+int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
+                int64_t ldx, float *y, int64_t ldy, void *stream) {
+  if (format == 4) return q4k_gemv(w, n, k, x, batch, ldx, y, ldy, stream);
+  bool empty = false;
+  int st = check_kq(format, w, n, k, x, batch, ldx, y, ldy, &empty);
+  if (st != Q4K_OK || empty) return st;
+  st = check_device();
   if (st != Q4K_OK) return st;
   st = check_device_memory({w, x, y});
   if (st != Q4K_OK) return st;
-  if (format != 4 && batch == 1) {  // tensor cores, as Q4_K
+  if (batch == 1) {  // tensor cores, as Q4_K
     const StreamOpDesc d = {w, nullptr, x, y, n, k, 0, 0};
     return map_launch(launch_stream(&d, 1, 1, false, static_cast<cudaStream_t>(stream), format));
   }
   return map_launch(launch_kq_gemv(format, w, n, k, x, batch, ldx, y, ldy,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+int q4k_kq_gemv_seq(int32_t format, const q4k_gemv_op *ops, int64_t count, int64_t batch,
+                    uint32_t flags, void *stream) {
+  if (format == 4) return q4k_gemv_seq(ops, count, batch, flags, stream);
+  if (kq_block_bytes(format) == 0 || count < 0) return Q4K_ERR_SHAPE;
+  if (flags & ~(uint32_t)Q4K_FLAG_OVERLAP_WEIGHTS) return Q4K_ERR_SHAPE;
+  if (count == 0) return Q4K_OK;
+  if (!ops) return Q4K_ERR_NULL;
+  bool any = false;
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    bool empty = false;
+    const int st = check_kq(format, o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy, &empty);
+    if (st != Q4K_OK) return st;
+    if (o.w_up) return Q4K_ERR_SHAPE;  // no fused gate/up for these formats
+    any = any || !empty;
+  }
+  if (!any) return Q4K_OK;
+  int st = check_device();
+  if (st != Q4K_OK) return st;
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    if (o.n == 0) continue;
+    st = check_device_memory({o.w, o.x, o.y});
+    if (st != Q4K_OK) return st;
+  }
+  const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
+  if (batch == 1) {  // persistent launches of the tensor-core stream kernel
+    std::vector<StreamOpDesc> d;
+    d.reserve((size_t)count);
+    for (int64_t i = 0; i < count; ++i) {
+      const q4k_gemv_op &o = ops[i];
+      d.push_back(StreamOpDesc{o.w, nullptr, o.x, o.y, o.n, o.k, 0, 0});
+    }
+    return map_launch(
+        launch_stream(d.data(), count, 1, overlap, static_cast<cudaStream_t>(stream), format));
+  }
+  for (int64_t i = 0; i < count; ++i) {
+    const q4k_gemv_op &o = ops[i];
+    if (o.n == 0) continue;
+    st = map_launch(launch_kq_gemv(format, o.w, o.n, o.k, o.x, batch, o.ldx, o.y, o.ldy,
+                                   static_cast<cudaStream_t>(stream)));
+    if (st != Q4K_OK) return st;
+  }
+  return Q4K_OK;
 }
 
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

@@ -1256,8 +1256,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
 // variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
-// for Q5_K, q2_K, Q6_K and q3_K (single ops only)), queried once per device
-// after the attributes are set.
+// for Q5_K, q2_K, Q6_K and q3_K), queried once per device after the
+// attributes are set.
 int g_occ[kMaxDevices][8][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
@@ -1287,13 +1287,13 @@ void stream_attributes(int dev) {
   g_occ[dev][3][0] = stream_setup<1, 1, 4>();
   g_occ[dev][3][1] = stream_setup<1, kMaxOps, 4>();
   g_occ[dev][4][0] = stream_setup<1, 1, 1, 5>();
-  g_occ[dev][4][1] = 0;
+  g_occ[dev][4][1] = stream_setup<1, kMaxOps, 1, 5>();
   g_occ[dev][5][0] = stream_setup<1, 1, 1, 2>();
-  g_occ[dev][5][1] = 0;
+  g_occ[dev][5][1] = stream_setup<1, kMaxOps, 1, 2>();
   g_occ[dev][6][0] = stream_setup<1, 1, 1, 6>();
-  g_occ[dev][6][1] = 0;
+  g_occ[dev][6][1] = stream_setup<1, kMaxOps, 1, 6>();
   g_occ[dev][7][0] = stream_setup<1, 1, 1, 3>();
-  g_occ[dev][7][1] = 0;
+  g_occ[dev][7][1] = stream_setup<1, kMaxOps, 1, 3>();
 }
 
 struct StreamPlan {
@@ -1405,6 +1405,19 @@ cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, cons
   return launch_stream_chunk<1, NOPS, 4>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
 }
 
+// The other k-quant formats (batch 1, 16-row tiles).
+template <int NOPS>
+cudaError_t launch_stream_kq(int fmt, const StreamOpDesc *ops, int count, const StreamPlan &pl,
+                             bool overlap, cudaStream_t stream) {
+  switch (fmt) {
+    case 2: return launch_stream_chunk<1, NOPS, 1, 2>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    case 3: return launch_stream_chunk<1, NOPS, 1, 3>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    case 5: return launch_stream_chunk<1, NOPS, 1, 5>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    case 6: return launch_stream_chunk<1, NOPS, 1, 6>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 int stream_max_batch() { return 4; }
@@ -1416,23 +1429,17 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
     return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
-  if (fmt != 4) {  // Q5_K, q2_K, q3_K, Q6_K: one launch per op
-    for (int64_t i = 0; i < count; ++i) {
-      if (ops[i].n <= 0) continue;
-      const long long tiles = (ops[i].n + 15) / 16;
-      const int var = fmt == 5 ? 4 : fmt == 2 ? 5 : fmt == 6 ? 6 : 7;
-      const StreamPlan pl = plan_stream(tiles, tiles, g_occ[f->device][var][0], 0, f);
-      if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
-      const cudaError_t e =
-          fmt == 5   ? launch_stream_chunk<1, 1, 1, 5>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
-          : fmt == 2 ? launch_stream_chunk<1, 1, 1, 2>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
-          : fmt == 6 ? launch_stream_chunk<1, 1, 1, 6>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream)
-                     : launch_stream_chunk<1, 1, 1, 3>(ops + i, 1, 1, pl.kp, pl.grid, overlap, stream);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaGetLastError();
-  }
-  const int var1 = batch == 1 ? 0 : batch == 2 ? 2 : 3;  // 16-row kernel of this batch
+  if (fmt != 4)
+    for (int64_t i = 0; i < count; ++i)
+      if (ops[i].n > 0 && ops[i].w_up) return cudaErrorInvalidValue;  // no fused gate/up
+  // 16-row kernel of this format and batch
+  const int var1 = fmt == 5   ? 4
+                   : fmt == 2 ? 5
+                   : fmt == 6 ? 6
+                   : fmt == 3 ? 7
+                   : batch == 1 ? 0
+                   : batch == 2 ? 2
+                                : 3;
   // Launches: as few as the kMaxOps weight matrices per launch allow, each
   // taking about the same number of matrices.
   long long mats = 0;
@@ -1459,13 +1466,16 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
     if (used > 0) {
       const bool single = used == 1;
       const int occ1 = g_occ[f->device][var1][single ? 0 : 1];
-      const int occ2 = batch == 1 ? g_occ[f->device][1][single ? 0 : 1] : 0;
+      const int occ2 = fmt == 4 && batch == 1 ? g_occ[f->device][1][single ? 0 : 1] : 0;
       const StreamPlan pl = plan_stream(tiles1, tiles2, occ1, occ2, f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const StreamOpDesc *chunk = ops + i;
       const int n = (int)(j - i);
-      const cudaError_t e = single ? launch_stream_nb<1>(chunk, n, batch, pl, overlap, stream)
-                                   : launch_stream_nb<kMaxOps>(chunk, n, batch, pl, overlap, stream);
+      const cudaError_t e =
+          fmt != 4 ? (single ? launch_stream_kq<1>(fmt, chunk, n, pl, overlap, stream)
+                             : launch_stream_kq<kMaxOps>(fmt, chunk, n, pl, overlap, stream))
+          : single ? launch_stream_nb<1>(chunk, n, batch, pl, overlap, stream)
+                   : launch_stream_nb<kMaxOps>(chunk, n, batch, pl, overlap, stream);
       if (e != cudaSuccess) return e;
     }
     i = j;

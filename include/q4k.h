@@ -296,6 +296,28 @@ int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void 
                 int64_t ldx, float *y, int64_t ldy, void *stream);
 
 /*
+ * q4k_kq_gemv_seq -- a sequence of q4k_kq_gemv projections of one format,
+ * run in order on one stream by one call: the same results as calling
+ * q4k_kq_gemv(format, ...) for ops[0], ops[1], .. with the same batch (a
+ * decode step of a model whose layers are stored in that format: "Layer
+ * Package Repository Spec", section "Repository Identity").
+ *   format  Q4K_FMT_* (Q4K_FMT_Q4_K is q4k_gemv_seq itself)
+ *   ops     host array of `count` q4k_gemv_op as for q4k_gemv_seq, each w
+ *           in `format`; w_up must be NULL (no fused gate/up here)
+ *   batch   1..16, shared by all ops
+ *   flags   as q4k_gemv_ex
+ * At batch 1 the ops run as persistent launches of the tensor-core kernel
+ * (one per Q4K_SEQ_MATRICES_PER_LAUNCH ops, split evenly) that stream their
+ * weights back to back, and ops may run concurrently: no op may read what
+ * another op of the same sequence writes.  At batch 2..16 each op is its own
+ * launch.  Every op is checked before the first launch.
+ * Errors: as q4k_kq_gemv; SHAPE also for w_up != NULL or unknown flags; NULL
+ * for ops == NULL with count > 0.
+ */
+int q4k_kq_gemv_seq(int32_t format, const q4k_gemv_op *ops, int64_t count, int64_t batch,
+                    uint32_t flags, void *stream);
+
+/*
  * q4k_moe_workspace_size -- bytes of device workspace q4k_moe_gemv needs.
  */
 size_t q4k_moe_workspace_size(int32_t n_experts, int32_t n_tokens, int32_t top_k, int64_t hidden,

@@ -275,6 +275,31 @@ def test_kq_argument_errors(L):
     assert gemv(ldx=516) == 3
 
 
+def test_kq_gemv_seq_checks_every_op_before_launching(L):
+    from bit_block_quantized_q4_gb300 import GemvOp
+    good = GemvOp(P, 4, 512, P, 512, P, 4)
+    ops = (GemvOp * 3)(good, good, good)
+    assert L.q4k_kq_gemv_seq(2, ops, 0, 1, 0, None) == 0       # nothing to do
+    assert L.q4k_kq_gemv_seq(7, ops, 3, 1, 0, None) == 2       # unknown format
+    assert L.q4k_kq_gemv_seq(3, None, 3, 1, 0, None) == 1
+    assert L.q4k_kq_gemv_seq(5, ops, -1, 1, 0, None) == 2
+    assert L.q4k_kq_gemv_seq(6, ops, 3, 17, 0, None) == 2      # batch shared by all ops
+    assert L.q4k_kq_gemv_seq(2, ops, 3, 1, 2, None) == 2       # unknown flag bit
+    # an error in the last op is found before anything is launched (a launch
+    # on this GPU-less machine would report the device instead)
+    for bad, status in ((GemvOp(None, 4, 512, P, 512, P, 4), 1),
+                        (GemvOp(P, 4, 300, P, 304, P, 4), 2),
+                        (GemvOp(P, 4, 512, P, 256, P, 4), 2),
+                        (GemvOp(P + 4, 4, 512, P, 512, P, 4), 3),
+                        (GemvOp(P, 4, 512, P + 8, 512, P, 4), 3),
+                        (GemvOp(P, 4, 512, P, 512, P, 4, P), 2)):   # no fused gate/up
+        ops[2] = bad
+        for fmt in (2, 3, 5, 6):
+            assert L.q4k_kq_gemv_seq(fmt, ops, 3, 1, 0, None) == status, (fmt, status)
+    ops[2] = GemvOp(P, 0, 512, None, 512, None, 4)              # an empty op is skipped
+    assert L.q4k_kq_gemv_seq(2, ops, 3, 1, 0, None) != 2
+
+
 def test_get_device_error_rejects_null(L):
     assert L.q4k_get_device_error(None, None) == 1
 

@@ -186,3 +186,35 @@ def test_batch_1_tensor_core_formats_many_shapes(q4k, fmt, n, k):
     assert q4k.q4k_get_device_error() == 0
     yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
     check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, f"kq{fmt} b1 {n}x{k}")
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 5, 6])
+@pytest.mark.parametrize("batch,flags,count", [(1, 1, 12), (1, 0, 175), (3, 0, 5)])
+def test_kq_gemv_seq_matches_oracle(q4k, fmt, batch, flags, count):
+    # one q4k_kq_gemv_seq call over projections of different shapes (empty
+    # ops, single rows, odd super-block counts and ragged tiles among them):
+    # at batch 1 one or two persistent launches, at batch 3 one launch per op;
+    # every op matches the oracle and an empty op writes nothing
+    rng = np.random.default_rng(7100 + 10 * fmt + count)
+    shapes = [(int(rng.choice([0, 1, 17, 40, 129, 700])), int(rng.choice([256, 768, 1280])))
+              for _ in range(count)]
+    shapes[0] = (333, 2304)
+    ws, xs, ys, tup = [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        w = synth.kq_weight(fmt, max(n, 1), k, seed=7200 + 7 * i + fmt)
+        x = synth.bf16_normal((batch, k), seed=7300 + i)
+        y = torch.full((batch, max(n, 1)), 7.0, device=DEV)
+        ws.append(w)
+        xs.append(x)
+        ys.append(y)
+        tup.append((w.to(DEV), n, k, x.to(DEV), y))
+    ops = q4k.gemv_ops(tup)
+    q4k.q4k_kq_gemv_seq(fmt, ops, batch, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    for i, ((n, k), w, x, y) in enumerate(zip(shapes, ws, xs, ys)):
+        if n == 0:
+            assert bool((y == 7.0).all()), "an empty op writes nothing"
+            continue
+        yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
+        check_bound(y.cpu().numpy().astype(np.float64), yref, s, TOL, f"kq{fmt} seq op {i} {n}x{k} b{batch}")
