@@ -141,3 +141,28 @@ def test_gemm_chain_reads_the_previous_output(q4k):
     ref = q4k.q4k_gemm(w2, n2, n1, y1c)
     torch.cuda.synchronize()
     assert torch.equal(y2, ref)
+
+
+def test_gemm_rejects_memory_of_the_host(q4k):
+    # the GEMM multicasts X within a cluster through a tensor map over x: a
+    # pinned host buffer (not device memory of the current device) as x, w or
+    # y fails with Q4K_ERR_MEMORY and launches nothing, with and without the
+    # RMSNorm prologue
+    m, n, k = 128, 256, 512
+    w = synth.q4k_weight(n, k, seed=4900).to(DEV)
+    x = synth.bf16_normal((m, k), seed=4901)
+    xh = x.pin_memory()
+    xd = x.to(DEV)
+    y = torch.full((m, n), 3.0, dtype=torch.bfloat16, device=DEV)
+    gamma = torch.ones(k, dtype=torch.float32, device=DEV)
+    rinv = torch.full((m,), 5.0, dtype=torch.float32, device=DEV)
+    L = q4k.lib()
+    assert L.q4k_gemm(w.data_ptr(), n, k, xh.data_ptr(), m, k, y.data_ptr(), n, None) == 8
+    wh = w.cpu().pin_memory()
+    assert L.q4k_gemm(wh.data_ptr(), n, k, xd.data_ptr(), m, k, y.data_ptr(), n, None) == 8
+    yh = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+    assert L.q4k_gemm(w.data_ptr(), n, k, xd.data_ptr(), m, k, yh.data_ptr(), n, None) == 8
+    assert L.q4k_gemm_rmsnorm(w.data_ptr(), n, k, xh.data_ptr(), m, k, gamma.data_ptr(), 1e-6,
+                              rinv.data_ptr(), y.data_ptr(), n, None) == 8
+    torch.cuda.synchronize()
+    assert bool((y == 3.0).all()) and bool((rinv == 5.0).all())
