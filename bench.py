@@ -895,6 +895,7 @@ def main():
             kq = bench_kquant(q4k, dev, stream)
         for v in kq.values():
             v["frac_of_measured_hbm"] = round(v["gbs"] / pk["hbm_gbs"], 4)
+            v["frac_of_measured_hbm_seq"] = round(v["gbs_seq"] / pk["hbm_gbs"], 4)
         extra["kquant_gemv_b1_down_5120x17408"] = kq
         torch.cuda.empty_cache()
         if world == 1:

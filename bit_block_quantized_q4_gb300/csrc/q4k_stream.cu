@@ -164,12 +164,12 @@ struct StreamOp {
   long long byte0;  // weight bytes of the ops before this one
   int n, nsb, ntiles, parts;
   int ldx, ldy;     // batch-row strides of x and y (elements)
-  int map;          // Q4_K: index of the weight matrix's tensor map (the up matrix's is map + 1)
+  int map;          // Q4_K, Q5_K: index of the weight matrix's tensor map (the up matrix's is map + 1)
 };
 
 template <int NOPS>
 struct StreamParams {
-  // Q4_K: 2-D tensor maps over the weight matrices (unused by the other
+  // Q4_K, Q5_K: 2-D tensor maps over the weight matrices (unused by the other
   // formats); first, for their 64-byte alignment
   CUtensorMap map[NOPS == 1 ? 2 : NOPS];
   StreamOp op[NOPS];
@@ -239,12 +239,13 @@ struct StreamCfg {
   // 48 bytes apart (the reads of 8 rows by a warp then hit distinct banks).
   static constexpr int kQhRow = 48;
   static constexpr int kQhBuf = FMT == 5 ? kRows * kQhRow : 0;
-  // Q4_K stages are one TMA tile of the weight matrix (16*MT rows by the row
-  // slot's bytes: with the 16-byte pad the tile reaches 16 bytes into the next
-  // stage, or past the row's end, which reads as zeros) and one bulk copy of x
-  // per batch row, both completing on the slot's mbarrier.  The other formats
-  // copy 16-byte chunks with cp.async.
-  static constexpr bool kTma = FMT == 4;
+  // Q4_K and Q5_K stages are one TMA tile of the weight matrix (16*MT rows by
+  // the row slot's bytes: with the 16-byte pad the tile reaches 16 bytes into
+  // the next stage, or past the row's end, which reads as zeros) and one bulk
+  // copy of x per batch row, both completing on the slot's mbarrier.  The
+  // other formats (blocks not 16-byte aligned) copy 16-byte chunks with
+  // cp.async.
+  static constexpr bool kTma = FMT == 4 || FMT == 5;
   // warp region: ring weights | ring x | permuted-x buffers | 64 zero bytes |
   // fifth-bit buffers (Q5_K) | ring mbarriers (Q4_K)
   static constexpr int kOffX = kStages * kWBytes;
@@ -274,7 +275,7 @@ struct Pos {
   int nrows;            // weight rows of the tile
   long long rstride;    // bytes from one weight row to the next
   const uint8_t *wend;  // end of this part's weight matrix
-  int map;              // Q4_K: tensor map of this part's matrix
+  int map;              // Q4_K, Q5_K: tensor map of this part's matrix
 };
 
 template <int NOPS>
@@ -398,7 +399,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// After a timed-out wait on a Q4_K stage: give the copies still in flight on
+// After a timed-out wait on a TMA stage (Q4_K, Q5_K): give the copies still in flight on
 // the ring (the `inflight` stages from slot `slot` on) the same bounded time to
 // land before the warp walks on and its CTA exits.
 __device__ __noinline__ void drain_ring(uint64_t *bars, int stages, int slot, uint32_t phase,
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * C::kWarpBytes);
 
   if (lane < 16) reinterpret_cast<uint32_t *>(wreg + C::kOffZero)[lane] = 0u;
-  uint64_t *full = reinterpret_cast<uint64_t *>(wreg + C::kOffBar);  // Q4_K ring mbarriers
+  uint64_t *full = reinterpret_cast<uint64_t *>(wreg + C::kOffBar);  // TMA ring mbarriers
   if (C::kTma && lane == 0) {
     for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   pos_settle<C::kBlock>(p, TR, hi, kp, pp);  // the first stage (when there is one)
 
   constexpr int SB = C::kSB;
-  // Q4_K: lane 0 arms the slot's mbarrier with the stage's bytes (the whole
+  // Q4_K, Q5_K: lane 0 arms the slot's mbarrier with the stage's bytes (the whole
   // weight tile, out-of-range parts included, and x) and requests the weight
   // tile; lanes b < batch each request x of batch row b.
   // The other formats: a stage's copies are 16-byte cp.async chunks.  Weights: the LPR lanes
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[slot], (uint32_t)(C::kWBytes + batch * cnt * kXBytes));
         tma_load_2d_hint(ringw + slot * C::kWBytes, &p.map[s.map], &full[slot],
-                         s.sb * (kBlockBytes / 8), s.tile * TR, pol);
+                         s.sb * (C::kBlock / 8), s.tile * TR, pol);
       }
       return;
     }
@@ -559,7 +560,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
     }
   }
   grid_dependency_wait();
-  int inflight = 0;  // Q4_K: stages requested and not yet consumed
+  int inflight = 0;  // TMA stages requested and not yet consumed
   for (int s = 0; s < ST; ++s) {
     if (pp.valid) {
       if (s >= npre) issue_w(s, pp);
@@ -600,8 +601,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 
   // ---- consumer
   int cslot = 0;
-  uint32_t phase = 0;  // Q4_K: parity of the slot's next phase (flips when cslot wraps)
-  bool ok = true;      // Q4_K: false once a wait on a stage has timed out
+  uint32_t phase = 0;  // TMA: parity of the slot's next phase (flips when cslot wraps)
+  bool ok = true;      // TMA: false once a wait on a stage has timed out
   int pbuf = 0;
   int op, tile;
   bool tvalid;
@@ -1337,12 +1338,13 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
   long long total = 0;
   int nops = 0, nmaps = 0;
   constexpr int kMapCap = (int)(sizeof prm.map / sizeof prm.map[0]);
-  // Q4_K: the matrix as a 2-D array of 8-byte words, one row per weight row;
+  // Q4_K, Q5_K: the matrix as a 2-D array of 8-byte words, one row per weight row;
   // a tile is the row slot's words of TR rows
   auto weight_map = [&](const uint8_t *w, int n, int nsb) -> cudaError_t {
     if (nmaps >= kMapCap) return cudaErrorInvalidValue;
-    const uint64_t dims[2] = {(uint64_t)nsb * (kBlockBytes / 8), (uint64_t)n};
-    const uint64_t strides[1] = {(uint64_t)nsb * kBlockBytes};
+    constexpr int kBlk = StreamCfg<MT, NB, FMT>::kBlock;
+    const uint64_t dims[2] = {(uint64_t)nsb * (kBlk / 8), (uint64_t)n};
+    const uint64_t strides[1] = {(uint64_t)nsb * kBlk};
     const uint32_t box[2] = {(uint32_t)(StreamCfg<MT, NB, FMT>::kRowBytes / 8), (uint32_t)TR};
     const CUresult r = encode_tiled(&prm.map[nmaps++], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
                                     const_cast<uint8_t *>(w), dims, strides, box,
