@@ -218,8 +218,7 @@ def bench_decode(q4k, layers, batch, steps, warmup, dev, stream, sampler=None, o
         ms, per, g = time_graph(step, steps, warmup, stream)
     del g
     nbytes = layers.algorithmic_bytes(batch)
-    per_launch = q4k.Q4K_SEQ_MATRICES_PER_LAUNCH if batch <= 4 else q4k.Q4K_SEQ_WIDE_OPS_PER_LAUNCH
-    launches = -(-len(layers.mats) // per_launch)
+    launches = -(-len(layers.mats) // q4k.Q4K_SEQ_MATRICES_PER_LAUNCH)
     return {"ms_per_step": ms, "ms_min": min(per), "gbs": nbytes / (ms * 1e-3) / 1e9,
             "bytes_per_step": nbytes, "launches_per_step": launches,
             "verified": verify_decode(layers, xs, ys)}

@@ -25,7 +25,6 @@ STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN"
           8: "Q4K_ERR_MEMORY"}
 Q4K_FLAG_OVERLAP_WEIGHTS = 1
 Q4K_SEQ_MATRICES_PER_LAUNCH = 160
-Q4K_SEQ_WIDE_OPS_PER_LAUNCH = 448
 Q4K_MOE_WEIGHTED_DOWN = 1
 EXPORTS = ("q4k_abi_version", "q4k_status_str", "q4k_dequant", "q4k_gemv", "q4k_gemv_ex",
            "q4k_gemv_glu", "q4k_gemv_seq", "q4k_gemm", "q4k_gemm_rmsnorm",

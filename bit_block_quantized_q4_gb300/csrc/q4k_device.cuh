@@ -188,6 +188,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, err);
 }
+// After a timed-out wait on a ring of TMA stages: give the copies still in
+// flight (the `inflight` stages from slot `slot` on, whose next phase has
+// parity `phase`) the same bounded time to land before the caller moves on
+// and its CTA exits.
+__device__ __noinline__ inline void drain_ring(uint64_t *bars, int stages, int slot,
+                                               uint32_t phase, int inflight) {
+  const uint64_t t0 = global_ns();
+  for (int j = 0; j < inflight; ++j) {
+    while (!mbar_try_wait(&bars[slot], phase, 1000u))
+      if (global_ns() - t0 > kWaitLimitNs) return;
+    if (++slot == stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
 // ----------------------------------------------------------------- cp.async
 // 16-byte copy global -> shared by this thread (both addresses 16-byte
 // aligned), L1 bypassed; the first src_bytes (0..16) bytes come from src, the

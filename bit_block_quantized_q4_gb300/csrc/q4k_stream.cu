@@ -399,22 +399,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// After a timed-out wait on a TMA stage (Q4_K, Q5_K): give the copies still in flight on
-// the ring (the `inflight` stages from slot `slot` on) the same bounded time to
-// land before the warp walks on and its CTA exits.
-__device__ __noinline__ void drain_ring(uint64_t *bars, int stages, int slot, uint32_t phase,
-                                        int inflight) {
-  const uint64_t t0 = global_ns();
-  for (int j = 0; j < inflight; ++j) {
-    while (!mbar_try_wait(&bars[slot], phase, 1000u))
-      if (global_ns() - t0 > kWaitLimitNs) return;
-    if (++slot == stages) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-}
-
 // w >> n, as a shift (ALU pipe) or as the high half of w * 2^(32-n) (FMA pipe).
 template <int N>
 __device__ __forceinline__ uint32_t shr(uint32_t w) {

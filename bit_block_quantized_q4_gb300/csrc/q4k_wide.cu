@@ -11,11 +11,14 @@
 // weight bytes, so a sequence of projections streams its weights back to back.
 //
 // The four warps of a CTA consume the same stages in lockstep: a stage is SB
-// super-blocks of the tile's 64 rows plus the x of those super-blocks for the
-// 8*NT batch rows, copied by all 128 threads in 16-byte cp.async chunks (one
-// cp.async group per thread and stage) and released by a CTA barrier.  So the
-// x of a super-block is read from L2 once per 64 rows and the warps hold no x
-// in registers between super-blocks.  Warp w contracts rows 16w .. 16w+15.
+// super-blocks of the tile's 64 rows (one TMA tile) plus the x of those
+// super-blocks for the 8*NT batch rows (one bulk copy per super-block and
+// batch row), completing on the slot's mbarrier and released by a CTA
+// barrier.  So the x of a super-block is read from L2 once per 64 rows and the
+// warps hold no x in registers between super-blocks.  Warp w contracts rows
+// 16w .. 16w+15.  (With 16-byte cp.async chunks copied by every thread, the
+// chunk addresses and predicates cost each thread about a hundred integer
+// instructions per stage.)
 //
 // Contraction (mma.sync m16n8k16 bf16 -> fp32), as in the per-op batched
 // kernel: the MMA columns are the batch rows (NT n-tiles of 8); sub-block j of
@@ -33,17 +36,22 @@
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
-#ifndef Q4K_WIDE_SB_NT1  // super-blocks per stage, batch 5..8
+// Super-blocks per stage and ring stages, batch 5..8 (NT1) and 9..16 (NT2);
+// measured on the 64-layer pass with TMA stages: two stages of one
+// super-block 2.73 / 2.67 / 2.00 TB/s at batch 5 / 8 / 16, against 2.70 /
+// 2.64 / 1.96 with three stages, 2.71 / 2.64 / 1.75 with four, 2.75 / 2.67 /
+// 1.96 with two of two super-blocks.
+#ifndef Q4K_WIDE_SB_NT1
 #define Q4K_WIDE_SB_NT1 1
 #endif
 #ifndef Q4K_WIDE_STAGES_NT1
-#define Q4K_WIDE_STAGES_NT1 3
+#define Q4K_WIDE_STAGES_NT1 2
 #endif
-#ifndef Q4K_WIDE_SB_NT2  // batch 9..16
+#ifndef Q4K_WIDE_SB_NT2
 #define Q4K_WIDE_SB_NT2 1
 #endif
 #ifndef Q4K_WIDE_STAGES_NT2
-#define Q4K_WIDE_STAGES_NT2 3
+#define Q4K_WIDE_STAGES_NT2 2
 #endif
 #ifndef Q4K_WIDE_MINB  // resident CTAs per SM the register budget is sized for
 #define Q4K_WIDE_MINB 4
@@ -59,7 +67,9 @@ namespace {
 constexpr int kWideWarps = 4;
 constexpr int kWideThreads = kWideWarps * 32;
 constexpr int kWideRows = 16 * kWideWarps;  // rows per tile
-constexpr int kWideMaxOps = Q4K_SEQ_WIDE_OPS_PER_LAUNCH;  // ops per launch (kernel parameter table)
+// weight matrices (tensor maps) and ops per launch: with a 128-byte map per
+// matrix the kernel parameter table stays under 32 KB
+constexpr int kWideMaxOps = Q4K_SEQ_MATRICES_PER_LAUNCH;
 // x rows in a stage: 512 bytes of a super-block plus 64 bytes, so that the
 // 16-byte fragment reads of 8 batch rows by a quarter warp hit distinct banks.
 constexpr int kXRowBytes = 576;
@@ -75,7 +85,10 @@ struct WideCfg {
   static constexpr int kWBytes = kWideRows * kRowBytes;
   static constexpr int kXBytes = kSB * kNB * kXRowBytes;  // [super-block][batch row][576]
   static constexpr int kStageBytes = kWBytes + kXBytes;
-  static constexpr int kSmem = kStages * kStageBytes;
+  static constexpr int kOffBar = kStages * kStageBytes;  // the ring's mbarriers
+  static constexpr int kSmem = kOffBar + 8 * kStages;
+  static_assert(kWBytes % 128 == 0 && kStageBytes % 128 == 0 && kRowBytes % 16 == 0,
+                "TMA destinations 128-byte aligned, tile rows whole 16-byte units");
 };
 
 struct WideOp {
@@ -86,17 +99,21 @@ struct WideOp {
   long long byte0;    // weight bytes of the ops before this one
   int n, nsb, ntiles, parts;
   int ldx, ldy;       // batch-row strides of x and y (elements)
+  int map;            // index of the weight matrix's tensor map (the up matrix's is map + 1)
 };
 
 template <int NOPS>
 struct WideParams {
+  CUtensorMap map[NOPS == 1 ? 2 : NOPS];  // 2-D maps over the weight matrices (first: aligned)
+  WideOp op[NOPS];
+  unsigned *err;  // device error word (a timed-out wait on a stage)
   int nops;
   int batch;
   int pre;    // weight stages requested before the dependency wait
   int nctas;  // CTAs of the grid (tile runs)
   long long total;
-  WideOp op[NOPS];
 };
+static_assert(sizeof(WideParams<kWideMaxOps>) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 // Stage walk: super-blocks sb .. sb+SB-1 of part `part` of tile `tile` of op
 // `op`, over the CTA's run of tiles [tiles starting in bytes lo .. hi).
@@ -164,42 +181,43 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
   const long long lo = p.total * blockIdx.x / p.nctas, hi = p.total * (blockIdx.x + 1) / p.nctas;
   const int batch = p.batch;
 
-  // ---- producer: every thread copies its chunks of a stage.  Weights:
-  // threads 2r, 2r+1 take row r (32 contiguous bytes per instruction); x:
-  // warp w takes the (super-block, batch row) blocks w, w+4, ..., lane l
-  // chunk l of each.
-  const int crow = tid >> 1, csub = tid & 1;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);  // one mbarrier per ring slot
+  // x rows past the batch stay zero in every slot (the copies below fill
+  // rows b < batch only), so the consumer needs no test per column
+  for (int idx = tid; idx < ST * SB * NB * (kQK * 2 / 16); idx += kWideThreads) {
+    const int c16 = idx % (kQK * 2 / 16), rowi = idx / (kQK * 2 / 16);  // rowi = (slot, u, b)
+    const int b = rowi % NB, su = rowi / NB;
+    if (b >= batch)
+      *reinterpret_cast<uint4 *>(smem + (su / SB) * C::kStageBytes + C::kWBytes +
+                                 ((su % SB) * NB + b) * kXRowBytes + 16 * c16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid == 0) {
+    for (int st = 0; st < ST; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- producer (warp 0): a stage is one TMA tile of the weight matrix (64
+  // rows by the row slot's bytes; rows past the matrix read as zeros) and one
+  // bulk copy of 512 bytes of x per (super-block, batch row), both completing
+  // on the slot's mbarrier, which thread 0 arms with the stage's bytes.
   auto issue_w = [&](int slot, const WPos &s) {
-    const WideOp &o = p.op[s.op];
-    const int row0 = s.tile * kWideRows;
-    const int nrows = min(kWideRows, o.n - row0);
-    const int nch = 9 * min(SB, o.nsb - s.sb);  // chunks of a row in this stage
-    if (crow < nrows) {
-      const uint8_t *src =
-          (s.part ? o.w2 : o.w) + ((size_t)(row0 + crow) * o.nsb + s.sb) * kBlockBytes + csub * 16;
-      uint8_t *dst = smem + slot * C::kStageBytes + crow * C::kRowBytes + csub * 16;
-#pragma unroll
-      for (int j = 0; j < (9 * SB + 1) / 2; ++j)
-        if (2 * j + csub < nch) cp_async16(dst + 32 * j, src + 32 * j);
+    if (tid == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // weights are read once
+      const WideOp &o = p.op[s.op];
+      const int cnt = min(SB, o.nsb - s.sb);
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)(C::kWBytes + batch * cnt * kQK * 2));
+      tma_load_2d_hint(smem + slot * C::kStageBytes, &p.map[o.map + s.part], &full[slot],
+                       s.sb * (kBlockBytes / 8), s.tile * kWideRows, pol);
     }
   };
-  // Rows past the batch are zero-filled (a copy of 0 source bytes), so the
-  // consumer needs no test per column.
   auto issue_x = [&](int slot, const WPos &s) {
     const WideOp &o = p.op[s.op];
     const int cnt = min(SB, o.nsb - s.sb);
-    uint8_t *dst = smem + slot * C::kStageBytes + C::kWBytes + lane * 16;
-#pragma unroll
-    for (int m = 0; m < SB * NB / kWideWarps; ++m) {
-      const int idx = warp + kWideWarps * m;  // block (super-block u, batch row b)
-      const int u = idx / NB, b = idx % NB;
-      if (u < cnt) {
-        const bool in = b < batch;
-        cp_async16(dst + idx * kXRowBytes,
-                   o.x + (in ? (size_t)b * o.ldx + (size_t)(s.sb + u) * kQK + lane * 8 : 0),
-                   in ? 16 : 0);
-      }
-    }
+    const int u = lane / NB, b = lane % NB;  // lane = (super-block u, batch row b)
+    if (warp == 0 && lane < SB * NB && u < cnt && b < batch)
+      bulk_load(smem + slot * C::kStageBytes + C::kWBytes + lane * kXRowBytes,
+                o.x + (size_t)b * o.ldx + (size_t)(s.sb + u) * kQK, (uint32_t)(kQK * 2), &full[slot]);
   };
   // After its copies of a stage have landed, a thread puts its own x chunks in
   // B-fragment order in place: 16 bytes hold values 8l .. 8l+7 of a sub-block
@@ -223,10 +241,9 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
     }
   };
 
-  // Ring: stage i lives in slot i % ST; every thread commits one cp.async
-  // group per stage (empty past the run's end), ST - 1 stages ahead.  With
-  // programmatic dependent launch the first weight stages go out before the
-  // wait for the previous kernel, their x after it.
+  // Ring: stage i lives in slot i % ST, ST - 1 stages ahead of the consumer.
+  // With programmatic dependent launch the first weight stages go out before
+  // the wait for the previous kernel, their x after it.
   WPos pp;
   wide_first(p, lo, hi, pp);
   int npre = 0;
@@ -238,13 +255,14 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
     }
   }
   grid_dependency_wait();
+  int inflight = 0;  // stages requested and not yet consumed
   for (int s = 0; s < ST - 1; ++s) {
     if (pp.valid) {
       if (s >= npre) issue_w(s, pp);
       issue_x(s, pp);
       wide_next<SB>(p, hi, pp);
+      ++inflight;
     }
-    cp_async_commit();
   }
   grid_launch_dependents();
 
@@ -253,6 +271,7 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
   WPos cs;
   wide_first(p, lo, hi, cs);
   int slot = 0;
+  uint32_t phase = 0;  // parity of the slot's next phase (flips when slot wraps)
   float yacc[NT][4], ygate[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -263,17 +282,25 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
     const int cnt = min(SB, o.nsb - cs.sb);
     const int tile = cs.tile, part = cs.part;
     const bool last_of_part = cs.sb + SB >= o.nsb;
-    cp_async_wait<ST - 2>();  // this thread's copies of the stage have landed
+    const bool landed = mbar_wait(&full[slot], phase, p.err);  // the stage's copies
     permute_x(slot, cnt);
-    __syncthreads();          // every thread's have, and the previous stage is consumed
+    fence_proxy_async_smem();  // the in-place x writes come before a later TMA refill of the slot
+    // every thread's permuted x is visible, and the previous stage is consumed;
+    // after a timed-out wait the CTA lets its copies in flight land and stops
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) drain_ring(full, ST, slot, phase, inflight);
+      __syncthreads();
+      break;
+    }
+    --inflight;
     {
       const int rs = slot == 0 ? ST - 1 : slot - 1;  // the slot the previous stage used
       if (pp.valid) {
         issue_w(rs, pp);
         issue_x(rs, pp);
         wide_next<SB>(p, hi, pp);
+        ++inflight;
       }
-      cp_async_commit();
     }
     const uint8_t *wst = smem + slot * C::kStageBytes;
     const uint8_t *xst = wst + C::kWBytes;
@@ -375,7 +402,10 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
         }
       }
     }
-    slot = slot == ST - 1 ? 0 : slot + 1;
+    if (++slot == ST) {
+      slot = 0;
+      phase ^= 1u;
+    }
     wide_next<SB>(p, hi, cs);
     if (last_of_part) {
       if (o.parts == 2 && part == 0) {
@@ -402,7 +432,8 @@ __global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
         for (int e = 0; e < 4; ++e) yacc[nt][e] = 0.f;
     }
   }
-  cp_async_wait<0>();  // nothing is left in flight (the trailing groups are empty)
+  // Every stage requested was consumed (or, after a timed-out wait, given the
+  // bounded time to land); nothing is left in flight.
 }
 
 // ---------------------------------------------------------------- host side
@@ -434,7 +465,20 @@ cudaError_t wide_chunk(const StreamOpDesc *ops, int count, int batch, int grid, 
   WideParams<NOPS> prm;
   memset(&prm, 0, sizeof prm);
   long long total = 0;
-  int nops = 0;
+  int nops = 0, nmaps = 0;
+  constexpr int kMapCap = (int)(sizeof prm.map / sizeof prm.map[0]);
+  // the matrix as a 2-D array of 8-byte words, one row per weight row; a tile
+  // is the row slot's words of 64 rows
+  auto weight_map = [&](const uint8_t *w, int n, int nsb) -> cudaError_t {
+    if (nmaps >= kMapCap) return cudaErrorInvalidValue;
+    const uint64_t dims[2] = {(uint64_t)nsb * (kBlockBytes / 8), (uint64_t)n};
+    const uint64_t strides[1] = {(uint64_t)nsb * kBlockBytes};
+    const uint32_t box[2] = {(uint32_t)(WideCfg<NT>::kRowBytes / 8), (uint32_t)kWideRows};
+    const CUresult r = encode_tiled(&prm.map[nmaps++], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+                                    const_cast<uint8_t *>(w), dims, strides, box,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  };
   for (int i = 0; i < count; ++i) {
     const StreamOpDesc &d = ops[i];
     if (d.n <= 0) continue;
@@ -450,9 +494,14 @@ cudaError_t wide_chunk(const StreamOpDesc *ops, int count, int batch, int grid, 
     o.ldx = (int)d.ldx;
     o.ldy = (int)d.ldy;
     o.byte0 = total;
+    o.map = nmaps;
+    cudaError_t e = weight_map(o.w, o.n, o.nsb);
+    if (e == cudaSuccess && o.w2) e = weight_map(o.w2, o.n, o.nsb);
+    if (e != cudaSuccess) return e;
     total += (long long)d.n * o.nsb * kBlockBytes * o.parts;
   }
   if (nops == 0) return cudaSuccess;
+  prm.err = device_error_word();
   prm.nops = nops;
   prm.batch = batch;
   prm.pre = overlap ? Q4K_WIDE_PRE : 0;
@@ -472,12 +521,17 @@ cudaError_t wide_chunk(const StreamOpDesc *ops, int count, int batch, int grid, 
   return cudaLaunchKernelEx(&cfg, gemv_wide_kernel<NT, NOPS>, prm);
 }
 
-// Ops [i, j) of a launch chunk: at most kWideMaxOps ops with rows.
-int64_t wide_chunk_end(const StreamOpDesc *ops, int64_t count, int64_t i, long long *tiles) {
-  int64_t j = i, used = 0;
+// Ops [i, j) of a launch chunk: ops with rows holding at most `per` weight
+// matrices (a fused gate/up op holds two).
+int64_t wide_chunk_end(const StreamOpDesc *ops, int64_t count, int64_t i, long long per,
+                       long long *tiles) {
+  int64_t j = i, used = 0, maps = 0;
   *tiles = 0;
-  while (j < count && used < kWideMaxOps) {
+  while (j < count) {
     if (ops[j].n > 0) {
+      const int need = ops[j].w_up ? 2 : 1;
+      if (used > 0 && maps + need > per) break;
+      maps += need;
       ++used;
       *tiles += (ops[j].n + kWideRows - 1) / kWideRows;
     }
@@ -510,10 +564,17 @@ cudaError_t launch_wide(const StreamOpDesc *ops, int64_t count, int batch, bool 
   const DeviceFacts *f = device_facts();
   std::call_once(g_wide_attr[f->device], wide_attributes, f->device);
   const int ntv = batch <= 8 ? 0 : 1;
+  // Launches: as few as the kWideMaxOps weight matrices per launch allow, each
+  // taking about the same number of matrices.
+  long long mats = 0;
+  for (int64_t i = 0; i < count; ++i)
+    if (ops[i].n > 0) mats += ops[i].w_up ? 2 : 1;
+  const long long nlaunch = (mats + kWideMaxOps - 1) / kWideMaxOps;
+  const long long per = nlaunch > 0 ? (mats + nlaunch - 1) / nlaunch : kWideMaxOps;
   int64_t i = 0;
   while (i < count) {
     long long tiles = 0;
-    const int64_t j = wide_chunk_end(ops, count, i, &tiles);
+    const int64_t j = wide_chunk_end(ops, count, i, per, &tiles);
     if (tiles > 0) {
       const bool single = j - i == 1;
       const int occ = g_wide_occ[f->device][ntv][single ? 0 : 1];

@@ -172,10 +172,10 @@ int q4k_gemv_glu(const void *w_gate, const void *w_up, int64_t n, int64_t k, con
  *   flags   as q4k_gemv_ex
  * At batch 1..4, and at 5..16 when the ops hold at least two 64-row tiles per
  * resident CTA of the GPU, the ops run as persistent launches that stream
- * their weights back to back, and ops may run concurrently: at batch 1..4 one
- * launch per Q4K_SEQ_MATRICES_PER_LAUNCH weight matrices (a fused gate/up op
- * counts two; the ops are split evenly over the launches), at 5..16 one per
- * Q4K_SEQ_WIDE_OPS_PER_LAUNCH ops; otherwise each op is its own launch.  At every batch: no op of
+ * their weights back to back, one launch per Q4K_SEQ_MATRICES_PER_LAUNCH
+ * weight matrices (a fused gate/up op counts two; the ops are split evenly
+ * over the launches), and ops may run concurrently; otherwise each op is its
+ * own launch.  At every batch: no op of
  * a sequence may read what another op of the same sequence writes (split
  * dependent projections into separate calls; stream order holds between
  * calls).
@@ -186,7 +186,6 @@ int q4k_gemv_glu(const void *w_gate, const void *w_up, int64_t n, int64_t k, con
  * CUDA.
  */
 #define Q4K_SEQ_MATRICES_PER_LAUNCH 160
-#define Q4K_SEQ_WIDE_OPS_PER_LAUNCH 448
 typedef struct q4k_gemv_op {
   const void *w;
   int64_t n, k;

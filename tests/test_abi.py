@@ -113,7 +113,7 @@ def test_binding_constants_match_the_header():
     import bit_block_quantized_q4_gb300 as q4k
     text = open(HEADER).read()
     for name in ("Q4K_ABI_VERSION", "Q4K_FLAG_OVERLAP_WEIGHTS", "Q4K_MOE_WEIGHTED_DOWN",
-                 "Q4K_SEQ_MATRICES_PER_LAUNCH", "Q4K_SEQ_WIDE_OPS_PER_LAUNCH"):
+                 "Q4K_SEQ_MATRICES_PER_LAUNCH"):
         m = re.search(r"#define %s (\d+)u?\b" % name, text)
         assert m, name
         if hasattr(q4k, name):

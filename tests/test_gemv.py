@@ -143,6 +143,45 @@ def test_gemv_seq_several_launches(q4k, batch, flags, count):
             check_glu(y.cpu().numpy(), w, wu, n, k, x, f"seq glu op {i} {n}x{k} b{batch}")
 
 
+@pytest.mark.parametrize("batch,flags", [(6, 1), (16, 0)])
+def test_gemv_seq_64_row_tiles_several_launches(q4k, batch, flags):
+    # batch 5..16 with enough 64-row tiles to fill the GPU and more than
+    # Q4K_SEQ_MATRICES_PER_LAUNCH weight matrices (fused gate/up ops count
+    # two): the 64-row tile kernel runs two launches; every op matches the
+    # oracle and an empty op writes nothing
+    count = 170
+    rng = np.random.default_rng(4300 + batch)
+    shapes = [(int(rng.integers(400, 700)), int(rng.choice([256, 512]))) for _ in range(count)]
+    shapes[5] = (0, 256)
+    glu = {i for i in range(count) if i % 7 == 3}
+    mats = sum((2 if i in glu else 1) for i, (n, _) in enumerate(shapes) if n > 0)
+    assert mats > q4k.Q4K_SEQ_MATRICES_PER_LAUNCH
+    ws, wus, xs, ys, tup = [], [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        w = synth.q4k_weight(max(n, 1), k, seed=6900 + i, quants="normal")
+        wu = synth.q4k_weight(max(n, 1), k, seed=7900 + i) if i in glu else None
+        x = synth.bf16_normal((batch, k), seed=8900 + i, sigma=0.05 if i in glu else 1.0)
+        y = torch.full((batch, max(n, 1)), 7.0, device=DEV)
+        ws.append(w)
+        wus.append(wu)
+        xs.append(x)
+        ys.append(y)
+        dw, dx = w.to(DEV), x.to(DEV)
+        tup.append((dw, n, k, dx, y) if wu is None else (dw, n, k, dx, y, wu.to(DEV)))
+    ops = q4k.gemv_ops(tup)
+    q4k.q4k_gemv_seq(ops, batch, flags)
+    torch.cuda.synchronize()
+    assert q4k.q4k_get_device_error() == 0
+    for i, ((n, k), w, wu, x, y) in enumerate(zip(shapes, ws, wus, xs, ys)):
+        if n == 0:
+            assert bool((y == 7.0).all()), "an empty op writes nothing"
+        elif wu is None:
+            yref, s = oracle.gemv(w.numpy(), n, k, xbits(x))
+            check_bound(y.cpu().numpy(), yref, s, TOL, f"wide seq op {i} {n}x{k} b{batch}")
+        else:
+            check_glu(y.cpu().numpy(), w, wu, n, k, x, f"wide seq glu op {i} {n}x{k} b{batch}")
+
+
 @pytest.mark.parametrize("batch,flags", [(5, 1), (8, 0), (9, 1), (16, 1)])
 def test_gemv_seq_persistent_64_row_tiles(q4k, batch, flags):
     # batch 5..16 with enough 64-row tiles to fill the GPU (at least two per
