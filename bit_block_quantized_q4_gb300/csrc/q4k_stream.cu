@@ -58,14 +58,8 @@
 #ifndef Q4K_STREAM_STAGES_MT1  // ring stages per warp, 16-row tiles
 #define Q4K_STREAM_STAGES_MT1 2
 #endif
-#ifndef Q4K_STREAM_STAGES_MT2  // ring stages per warp, 32-row tiles
-#define Q4K_STREAM_STAGES_MT2 2
-#endif
 #ifndef Q4K_STREAM_MINB_MT1  // resident CTAs per SM the register budget is sized for
 #define Q4K_STREAM_MINB_MT1 4
-#endif
-#ifndef Q4K_STREAM_MINB_MT2
-#define Q4K_STREAM_MINB_MT2 4
 #endif
 #ifndef Q4K_STREAM_SB  // super-blocks per stage (SB * 144 bytes of each row)
 #define Q4K_STREAM_SB 2
@@ -75,9 +69,6 @@
 #endif
 #ifndef Q4K_STREAM_PRE  // weight stages requested before the dependency wait (PDL)
 #define Q4K_STREAM_PRE 2
-#endif
-#ifndef Q4K_STREAM_FORCE_MT  // 0: planner's choice
-#define Q4K_STREAM_FORCE_MT 0
 #endif
 #ifndef Q4K_STREAM_FORCE_KP
 #define Q4K_STREAM_FORCE_KP 0
@@ -215,10 +206,10 @@ struct StreamCfg {
                                  : FMT == 2 ? Q4K_STREAM_STAGES_Q2
                                  : FMT == 6 ? Q4K_STREAM_STAGES_Q6
                                  : FMT == 3 ? Q4K_STREAM_STAGES_Q3
-                                 : NB == 1 ? (MT == 1 ? Q4K_STREAM_STAGES_MT1 : Q4K_STREAM_STAGES_MT2)
+                                 : NB == 1 ? Q4K_STREAM_STAGES_MT1
                                  : NB == 2 ? Q4K_STREAM_STAGES_NB2
                                            : Q4K_STREAM_STAGES_NB4;
-  static constexpr int kMinBlocks = NB == 1 ? (MT == 1 ? Q4K_STREAM_MINB_MT1 : Q4K_STREAM_MINB_MT2)
+  static constexpr int kMinBlocks = NB == 1 ? Q4K_STREAM_MINB_MT1
                                             : NB == 2 ? Q4K_STREAM_MINB_NB2 : Q4K_STREAM_MINB_NB4;
   // 16-byte chunks a row's stage copy needs at most
   static constexpr int kChunks = (kLead + kSB * kBlock + 15) / 16;
@@ -1240,8 +1231,8 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
-// variants are (MT, NB) = (1, 1), (2, 1), (1, 2), (1, 4) for Q4_K and (1, 1)
-// for Q5_K, q2_K, Q6_K and q3_K), queried once per device after the
+// variants are NB = 1, 2, 4 for Q4_K (0, 2, 3) and NB = 1 for Q5_K, q2_K,
+// Q6_K and q3_K (4 .. 7); 1 is unused), queried once per device after the
 // attributes are set.
 int g_occ[kMaxDevices][8][2];
 
@@ -1265,8 +1256,6 @@ int stream_setup() {
 void stream_attributes(int dev) {
   g_occ[dev][0][0] = stream_setup<1, 1, 1>();
   g_occ[dev][0][1] = stream_setup<1, kMaxOps, 1>();
-  g_occ[dev][1][0] = stream_setup<2, 1, 1>();
-  g_occ[dev][1][1] = stream_setup<2, kMaxOps, 1>();
   g_occ[dev][2][0] = stream_setup<1, 1, 2>();
   g_occ[dev][2][1] = stream_setup<1, kMaxOps, 2>();
   g_occ[dev][3][0] = stream_setup<1, 1, 4>();
@@ -1282,29 +1271,19 @@ void stream_attributes(int dev) {
 }
 
 struct StreamPlan {
-  int mt = 0, kp = 1, grid = 0;
+  int kp = 1, grid = 0;
 };
 
 // Split: the least splitting that still gives every resident warp a tile
-// (1, 2, else 4 warps per tile).  Tiles are 16 rows: 32-row tiles (fewer
-// resident warps, twice the registers) measured slower on the 27B-class pass
-// (occ2 <= 0: no 32-row kernel).
-StreamPlan plan_stream(long long tiles1, long long tiles2, int occ1, int occ2,
-                       const DeviceFacts *f) {
-  const int cand[3][2] = {{Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 1},
-                          {Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 2},
-                          {Q4K_STREAM_FORCE_MT == 2 ? 2 : 1, 4}};
+// (1, 2, else 4 warps per tile).  Tiles are 16 rows (the kernels are written
+// for 16*MT; 32-row tiles, with fewer resident warps and twice the registers,
+// measured slower on the 27B-class pass and are not instantiated).
+StreamPlan plan_stream(long long tiles, int occ, const DeviceFacts *f) {
   StreamPlan best;
-  for (const auto &c : cand) {
-    int mt = c[0];
-    const int kp = c[1];
-    if (mt == 2 && occ2 <= 0) mt = 1;
+  for (const int kp : {1, 2, 4}) {
     if (Q4K_STREAM_FORCE_KP && kp != Q4K_STREAM_FORCE_KP) continue;
-    const int occ = mt == 1 ? occ1 : occ2;
     if (occ <= 0) continue;
-    const long long tiles = mt == 1 ? tiles1 : tiles2;
     const long long warps = (long long)occ * f->sm_count * kWarps;
-    best.mt = mt;
     best.kp = kp;
     const long long ctas_needed = (tiles * kp + kWarps - 1) / kWarps;
     best.grid = (int)std::min<long long>((long long)occ * f->sm_count, ctas_needed);
@@ -1383,9 +1362,7 @@ cudaError_t launch_stream_chunk(const StreamOpDesc *ops, int count, int batch, i
 template <int NOPS>
 cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, const StreamPlan &pl,
                              bool overlap, cudaStream_t stream) {
-  if (batch == 1)
-    return pl.mt == 1 ? launch_stream_chunk<1, NOPS, 1>(ops, count, 1, pl.kp, pl.grid, overlap, stream)
-                      : launch_stream_chunk<2, NOPS, 1>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+  if (batch == 1) return launch_stream_chunk<1, NOPS, 1>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
   if (batch == 2)
     return launch_stream_chunk<1, NOPS, 2>(ops, count, 2, pl.kp, pl.grid, overlap, stream);
   return launch_stream_chunk<1, NOPS, 4>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
@@ -1437,23 +1414,20 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
   while (i < count) {
     // a chunk: ops with rows holding at most `per` weight matrices
     int64_t j = i, used = 0, maps = 0;
-    long long tiles1 = 0, tiles2 = 0;
+    long long tiles = 0;
     while (j < count) {
       if (ops[j].n > 0) {
         const int need = ops[j].w_up ? 2 : 1;  // tensor maps of the op's matrices
         if (used > 0 && maps + need > per) break;
         maps += need;
         ++used;
-        tiles1 += (ops[j].n + 15) / 16;
-        tiles2 += (ops[j].n + 31) / 32;
+        tiles += (ops[j].n + 15) / 16;
       }
       ++j;
     }
     if (used > 0) {
       const bool single = used == 1;
-      const int occ1 = g_occ[f->device][var1][single ? 0 : 1];
-      const int occ2 = fmt == 4 && batch == 1 ? g_occ[f->device][1][single ? 0 : 1] : 0;
-      const StreamPlan pl = plan_stream(tiles1, tiles2, occ1, occ2, f);
+      const StreamPlan pl = plan_stream(tiles, g_occ[f->device][var1][single ? 0 : 1], f);
       if (pl.grid <= 0) return cudaErrorInvalidConfiguration;
       const StreamOpDesc *chunk = ops + i;
       const int n = (int)(j - i);
