@@ -21,11 +21,28 @@ __device__ __forceinline__ void st_out(uint4 *p, uint4 v) { __stcs(p, v); }
 // Super-blocks per warp per loop step, their loads issued together: measured
 // best at 8 for fp32 output (5.4 against 4.3 TB/s at 1) and 2 for bf16 (4.7
 // against 4.3; 8 fell to 3.2).
+#ifndef Q4K_DQ_UNROLL_F32
+#define Q4K_DQ_UNROLL_F32 8
+#endif
+#ifndef Q4K_DQ_UNROLL_BF16
+#define Q4K_DQ_UNROLL_BF16 2
+#endif
+// Warps per CTA and the grid cap (CTAs per SM; CTAs beyond the resident ones
+// run in later waves, and a CTA loops over further super-blocks only past the
+// cap): measured on the 17408 x 5120 matrix, 4 warps and 128 per SM 5.67 /
+// 5.06 TB/s (fp32 / bf16), against 5.40 / 4.70 at 8 warps and 16 per SM, 5.66
+// / 4.98 at 4 warps and 64, 5.52 / 4.83 at 4 warps and 32.
+#ifndef Q4K_DQ_CTAS_PER_SM
+#define Q4K_DQ_CTAS_PER_SM 128
+#endif
+#ifndef Q4K_DQ_WARPS
+#define Q4K_DQ_WARPS 4
+#endif
 template <int OUT_BF16>
-__host__ __device__ constexpr int dq_unroll() { return OUT_BF16 ? 2 : 8; }
+__host__ __device__ constexpr int dq_unroll() { return OUT_BF16 ? Q4K_DQ_UNROLL_BF16 : Q4K_DQ_UNROLL_F32; }
 
 template <int OUT_BF16>
-__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w,
+__global__ void __launch_bounds__(Q4K_DQ_WARPS * 32) dequant_kernel(const uint8_t *__restrict__ w,
                                                       int64_t nblocks, void *__restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -89,10 +106,10 @@ cudaError_t launch_dequant(const void *w, int64_t n, int64_t k, void *out, int o
                            cudaStream_t stream) {
   const DeviceFacts *f = device_facts();
   const int64_t nblocks = n * (k / kQK);
-  const int warps_per_cta = 8;
+  const int warps_per_cta = Q4K_DQ_WARPS;
   const int64_t per_cta = (int64_t)warps_per_cta * (out_dtype == 1 ? dq_unroll<1>() : dq_unroll<0>());
   int64_t grid = (nblocks + per_cta - 1) / per_cta;
-  const int64_t cap = (int64_t)f->sm_count * 16;
+  const int64_t cap = (int64_t)f->sm_count * Q4K_DQ_CTAS_PER_SM;
   if (grid > cap) grid = cap;
   if (out_dtype == 1) {
     dequant_kernel<1><<<(unsigned)grid, warps_per_cta * 32, 0, stream>>>(
