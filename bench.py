@@ -587,7 +587,8 @@ def bench_kquant(q4k, dev, stream, reps=10):
     """Batch-1 decode projection in the other k-quant formats on the 27B-class
     down shape (5120 x 17408): a pool of 8 matrices per format (more than L2
     for every format) multiplied in turn, as one q4k_kq_gemv call each and as
-    one q4k_kq_gemv_seq call over the pool; bytes = weights + x + y."""
+    one q4k_kq_gemv_seq call over the pool, and at batch 4 as one call each;
+    bytes = weights + x + y."""
     n, k, pool = 5120, 17408, 8
     out = {}
     names = {2: "q2_K", 3: "q3_K", 5: "Q5_K", 6: "Q6_K"}
@@ -609,7 +610,15 @@ def bench_kquant(q4k, dev, stream, reps=10):
         del g
         nbytes = pool * (ws[0].numel() + 2 * k + 4 * n)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        # batch 4: Q5_K on the tensor cores, the others on the fp32 kernel
+        x4 = synth.bf16_normal((4, k), seed=synth.derive_seed(1008, "x4"), device=dev)
+        y4 = [torch.empty((4, n), dtype=torch.float32, device=dev) for _ in range(pool)]
+        ms4, _, g = time_graph(lambda: [q4k.q4k_kq_gemv(fmt, w, n, k, x4, out=y, stream=stream)
+                                        for w, y in zip(ws, y4)], reps, 3, stream)
+        del g
+        nbytes4 = pool * (ws[0].numel() + 4 * (2 * k + 4 * n))
         out[name] = {"us_per_gemv": round(ms * 1e3 / pool, 2), "gbs": round(gbs, 1),
+                     "gbs_b4": round(nbytes4 / (ms4 * 1e-3) / 1e9, 1),
                      "us_per_gemv_seq": round(ms_seq * 1e3 / pool, 2),
                      "gbs_seq": round(nbytes / (ms_seq * 1e-3) / 1e9, 1),
                      "bytes_per_weight": round(ws[0].numel() / (n * k), 4)}

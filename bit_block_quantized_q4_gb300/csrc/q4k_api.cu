@@ -356,6 +356,12 @@ int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *ou
 }
 
 namespace {
+// The k-quant projections the tensor-core stream kernel takes: batch 1 for
+// every format, and Q5_K (the Q4_K contraction with a fifth bit) at batch
+// 1..4 with 32-bit batch-row strides.
+bool kq_stream(int32_t format, int64_t batch, int64_t ldx, int64_t ldy) {
+  return batch == 1 || (format == 5 && stream_batch(batch, ldx, ldy));
+}
 // Argument checks of one k-quant projection (format != 4), before any launch.
 int check_kq(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,
              int64_t ldx, const float *y, int64_t ldy, bool *empty) {
@@ -384,9 +390,10 @@ int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void 
   if (st != Q4K_OK) return st;
   st = check_device_memory({w, x, y});
   if (st != Q4K_OK) return st;
-  if (batch == 1) {  // tensor cores, as Q4_K
-    const StreamOpDesc d = {w, nullptr, x, y, n, k, 0, 0};
-    return map_launch(launch_stream(&d, 1, 1, false, static_cast<cudaStream_t>(stream), format));
+  if (kq_stream(format, batch, ldx, ldy)) {  // tensor cores, as Q4_K
+    const StreamOpDesc d = {w, nullptr, x, y, n, k, stream_stride(batch, ldx), stream_stride(batch, ldy)};
+    return map_launch(
+        launch_stream(&d, 1, (int)batch, false, static_cast<cudaStream_t>(stream), format));
   }
   return map_launch(launch_kq_gemv(format, w, n, k, x, batch, ldx, y, ldy,
                                    static_cast<cudaStream_t>(stream)));
@@ -418,15 +425,19 @@ int q4k_kq_gemv_seq(int32_t format, const q4k_gemv_op *ops, int64_t count, int64
     if (st != Q4K_OK) return st;
   }
   const bool overlap = (flags & Q4K_FLAG_OVERLAP_WEIGHTS) != 0;
-  if (batch == 1) {  // persistent launches of the tensor-core stream kernel
+  bool on_stream = true;
+  for (int64_t i = 0; i < count; ++i)
+    on_stream = on_stream && (ops[i].n == 0 || kq_stream(format, batch, ops[i].ldx, ops[i].ldy));
+  if (on_stream) {  // persistent launches of the tensor-core stream kernel
     std::vector<StreamOpDesc> d;
     d.reserve((size_t)count);
     for (int64_t i = 0; i < count; ++i) {
       const q4k_gemv_op &o = ops[i];
-      d.push_back(StreamOpDesc{o.w, nullptr, o.x, o.y, o.n, o.k, 0, 0});
+      d.push_back(StreamOpDesc{o.w, nullptr, o.x, o.y, o.n, o.k, stream_stride(batch, o.ldx),
+                               stream_stride(batch, o.ldy)});
     }
-    return map_launch(
-        launch_stream(d.data(), count, 1, overlap, static_cast<cudaStream_t>(stream), format));
+    return map_launch(launch_stream(d.data(), count, (int)batch, overlap,
+                                    static_cast<cudaStream_t>(stream), format));
   }
   for (int64_t i = 0; i < count; ++i) {
     const q4k_gemv_op &o = ops[i];

@@ -176,8 +176,9 @@ static_assert(sizeof(StreamParams<kMaxOps>) <= 32764, "kernel parameters are lim
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
-  static_assert(FMT == 4 || ((FMT == 5 || FMT == 2 || FMT == 3 || FMT == 6) && NB == 1 && MT == 1),
-                "the other k-quants run at batch 1 with 16-row tiles");
+  static_assert(FMT == 4 || (FMT == 5 && MT == 1) ||
+                    ((FMT == 2 || FMT == 3 || FMT == 6) && NB == 1 && MT == 1),
+                "Q5_K runs at batch 1..4, the other k-quants at batch 1, with 16-row tiles");
   static constexpr int kRows = 16 * MT;
   // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
   // fifth bits at 16, the low nibbles at 48) -- the first 16 bytes (d, dmin,
@@ -1231,10 +1232,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
-// variants are NB = 1, 2, 4 for Q4_K (0, 2, 3) and NB = 1 for Q5_K, q2_K,
-// Q6_K and q3_K (4 .. 7); 1 is unused), queried once per device after the
-// attributes are set.
-int g_occ[kMaxDevices][8][2];
+// variants are NB = 1, 2, 4 for Q4_K (0, 2, 3), NB = 1 for Q5_K, q2_K, Q6_K
+// and q3_K (4 .. 7) and NB = 2, 4 for Q5_K (8, 9); 1 is unused), queried once
+// per device after the attributes are set.
+int g_occ[kMaxDevices][10][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
@@ -1268,6 +1269,10 @@ void stream_attributes(int dev) {
   g_occ[dev][6][1] = stream_setup<1, kMaxOps, 1, 6>();
   g_occ[dev][7][0] = stream_setup<1, 1, 1, 3>();
   g_occ[dev][7][1] = stream_setup<1, kMaxOps, 1, 3>();
+  g_occ[dev][8][0] = stream_setup<1, 1, 2, 5>();
+  g_occ[dev][8][1] = stream_setup<1, kMaxOps, 2, 5>();
+  g_occ[dev][9][0] = stream_setup<1, 1, 4, 5>();
+  g_occ[dev][9][1] = stream_setup<1, kMaxOps, 4, 5>();
 }
 
 struct StreamPlan {
@@ -1368,14 +1373,17 @@ cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, cons
   return launch_stream_chunk<1, NOPS, 4>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
 }
 
-// The other k-quant formats (batch 1, 16-row tiles).
+// The other k-quant formats (16-row tiles; batch 1, and Q5_K at 1..4).
 template <int NOPS>
-cudaError_t launch_stream_kq(int fmt, const StreamOpDesc *ops, int count, const StreamPlan &pl,
-                             bool overlap, cudaStream_t stream) {
+cudaError_t launch_stream_kq(int fmt, const StreamOpDesc *ops, int count, int batch,
+                             const StreamPlan &pl, bool overlap, cudaStream_t stream) {
   switch (fmt) {
     case 2: return launch_stream_chunk<1, NOPS, 1, 2>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
     case 3: return launch_stream_chunk<1, NOPS, 1, 3>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
-    case 5: return launch_stream_chunk<1, NOPS, 1, 5>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    case 5:
+      return batch == 1   ? launch_stream_chunk<1, NOPS, 1, 5>(ops, count, 1, pl.kp, pl.grid, overlap, stream)
+             : batch == 2 ? launch_stream_chunk<1, NOPS, 2, 5>(ops, count, 2, pl.kp, pl.grid, overlap, stream)
+                          : launch_stream_chunk<1, NOPS, 4, 5>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
     case 6: return launch_stream_chunk<1, NOPS, 1, 6>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
     default: return cudaErrorInvalidValue;
   }
@@ -1388,7 +1396,7 @@ int stream_max_batch() { return 4; }
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
-  if (fmt != 4 && !((fmt == 5 || fmt == 2 || fmt == 3 || fmt == 6) && batch == 1))
+  if (fmt != 4 && fmt != 5 && !((fmt == 2 || fmt == 3 || fmt == 6) && batch == 1))
     return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
@@ -1396,7 +1404,7 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
     for (int64_t i = 0; i < count; ++i)
       if (ops[i].n > 0 && ops[i].w_up) return cudaErrorInvalidValue;  // no fused gate/up
   // 16-row kernel of this format and batch
-  const int var1 = fmt == 5   ? 4
+  const int var1 = fmt == 5   ? (batch == 1 ? 4 : batch == 2 ? 8 : 9)
                    : fmt == 2 ? 5
                    : fmt == 6 ? 6
                    : fmt == 3 ? 7
@@ -1432,8 +1440,8 @@ cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, boo
       const StreamOpDesc *chunk = ops + i;
       const int n = (int)(j - i);
       const cudaError_t e =
-          fmt != 4 ? (single ? launch_stream_kq<1>(fmt, chunk, n, pl, overlap, stream)
-                             : launch_stream_kq<kMaxOps>(fmt, chunk, n, pl, overlap, stream))
+          fmt != 4 ? (single ? launch_stream_kq<1>(fmt, chunk, n, batch, pl, overlap, stream)
+                             : launch_stream_kq<kMaxOps>(fmt, chunk, n, batch, pl, overlap, stream))
           : single ? launch_stream_nb<1>(chunk, n, batch, pl, overlap, stream)
                    : launch_stream_nb<kMaxOps>(chunk, n, batch, pl, overlap, stream);
       if (e != cudaSuccess) return e;

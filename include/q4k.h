@@ -305,10 +305,11 @@ int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void 
  *           in `format`; w_up must be NULL (no fused gate/up here)
  *   batch   1..16, shared by all ops
  *   flags   as q4k_gemv_ex
- * At batch 1 the ops run as persistent launches of the tensor-core kernel
- * (one per Q4K_SEQ_MATRICES_PER_LAUNCH ops, split evenly) that stream their
- * weights back to back, and ops may run concurrently: no op may read what
- * another op of the same sequence writes.  At batch 2..16 each op is its own
+ * At batch 1 (Q5_K: batch 1..4) the ops run as persistent launches of the
+ * tensor-core kernel (one per Q4K_SEQ_MATRICES_PER_LAUNCH ops, split evenly)
+ * that stream their weights back to back, and ops may run concurrently: no op
+ * may read what another op of the same sequence writes.  At larger batches
+ * each op is its own
  * launch.  Every op is checked before the first launch.
  * Errors: as q4k_kq_gemv; SHAPE also for w_up != NULL or unknown flags; NULL
  * for ops == NULL with count > 0.
