@@ -356,11 +356,11 @@ int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *ou
 }
 
 namespace {
-// The k-quant projections the tensor-core stream kernel takes: batch 1 for
-// every format, and Q5_K (the Q4_K contraction with a fifth bit) at batch
-// 1..4 with 32-bit batch-row strides.
+// The k-quant projections the tensor-core stream kernel takes: batch 1..4
+// (with 32-bit batch-row strides beyond batch 1), as for Q4_K.
 bool kq_stream(int32_t format, int64_t batch, int64_t ldx, int64_t ldy) {
-  return batch == 1 || (format == 5 && stream_batch(batch, ldx, ldy));
+  (void)format;
+  return stream_batch(batch, ldx, ldy);
 }
 // Argument checks of one k-quant projection (format != 4), before any launch.
 int check_kq(int32_t format, const void *w, int64_t n, int64_t k, const void *x, int64_t batch,

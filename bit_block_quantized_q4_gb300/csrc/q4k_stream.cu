@@ -176,9 +176,7 @@ static_assert(sizeof(StreamParams<kMaxOps>) <= 32764, "kernel parameters are lim
 
 template <int MT, int NB, int FMT = 4>
 struct StreamCfg {
-  static_assert(FMT == 4 || (FMT == 5 && MT == 1) ||
-                    ((FMT == 2 || FMT == 3 || FMT == 6) && NB == 1 && MT == 1),
-                "Q5_K runs at batch 1..4, the other k-quants at batch 1, with 16-row tiles");
+  static_assert(FMT == 4 || MT == 1, "the other k-quants run with 16-row tiles");
   static constexpr int kRows = 16 * MT;
   // Super-block layout: Q4_K 144 bytes (quants at 16); Q5_K 176 bytes (the
   // fifth bits at 16, the low nibbles at 48) -- the first 16 bytes (d, dmin,
@@ -194,7 +192,6 @@ struct StreamCfg {
   // stage copies a row's bytes from its start rounded down to 16 (at most 12
   // or 14 bytes early).
   static constexpr int kLead = FMT == 2 ? 12 : (FMT == 3 || FMT == 6) ? 14 : 0;
-  static constexpr int kNB = NB;                   // batch rows the kernel carries
   static constexpr int kPairs = (NB + 1) / 2;      // MMA column groups (batch-row pairs)
   static constexpr int kSB = FMT == 5  ? Q4K_STREAM_SB_Q5
                              : FMT == 2 ? Q4K_STREAM_SB_Q2
@@ -572,6 +569,22 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
   }
   uint32_t magic;
   asm volatile("mov.b32 %0, %1;\n" : "=r"(magic) : "n"(kBf16Magic));
+  // q2_K, q3_K, Q6_K: x of super-block u of every batch row in B-fragment
+  // order (word 2G of a 16-value half holds (x[4G], x[4G+2]), word 2G+1
+  // (x[4G+1], x[4G+3])); rows past the batch read as zeros
+  auto perm_x_rows = [&](uint32_t *pwb, const uint8_t *xst, int u) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (b < batch) raw = reinterpret_cast<const uint4 *>(xst + (b * C::kSB + u) * kXBytes)[lane];
+      uint4 pm;
+      pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
+      pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
+      pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
+      pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
+      reinterpret_cast<uint4 *>(pwb + b * kPermWords + g * kPermStride)[t] = pm;
+    }
+  };
   // Q5_K: rotations that bring bit 2t (2t+1) of each qh byte to bit 4.
   const uint32_t rot_e = (uint32_t)(2 * t - 4) & 31u, rot_o = (uint32_t)(2 * t - 3) & 31u;
 
@@ -671,22 +684,26 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             // 4t .. 4t+3 (a = 0..3) of rows g, g+8.  Column sums of x per
             // 16 values: the first half of each 32-value block is held by
             // lanes t < 2, the second by t >= 2, so two half-masked pairs of
-            // MMAs with A = 1 give thread t the sums X_{4t+a}.
-            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
-            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 rl = t < 2 ? raw : z4, rh = t < 2 ? z4 : raw;
-            float xl[4], xh[4];
-            mma_bf16_zc(xl, kBf16One, kBf16One, kBf16One, kBf16One, rl.x, rl.y);
-            mma_bf16(xl, kBf16One, kBf16One, kBf16One, kBf16One, rl.z, rl.w);
-            mma_bf16_zc(xh, kBf16One, kBf16One, kBf16One, kBf16One, rh.x, rh.y);
-            mma_bf16(xh, kBf16One, kBf16One, kBf16One, kBf16One, rh.z, rh.w);
-            {
+            // MMAs with A = 1 give thread t the sums X_{4t+a} of each batch
+            // row.  The MMA columns of the contraction are (slot, batch row)
+            // as for Q4_K.
+            float xl[NB][4], xh[NB][4];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+              if (b < batch) raw = reinterpret_cast<const uint4 *>(xstage + (b * SB + u) * kXBytes)[lane];
+              const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+              const uint4 rl = t < 2 ? raw : z4, rh = t < 2 ? z4 : raw;
+              mma_bf16_zc(xl[b], kBf16One, kBf16One, kBf16One, kBf16One, rl.x, rl.y);
+              mma_bf16(xl[b], kBf16One, kBf16One, kBf16One, kBf16One, rl.z, rl.w);
+              mma_bf16_zc(xh[b], kBf16One, kBf16One, kBf16One, kBf16One, rh.x, rh.y);
+              mma_bf16(xh[b], kBf16One, kBf16One, kBf16One, kBf16One, rh.z, rh.w);
               uint4 pm;
               pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
               pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
               pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
               pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
-              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
+              reinterpret_cast<uint4 *>(pw + b * kPermWords + g * kPermStride)[t] = pm;
             }
             // Rows g, g+8: the stage copy of row r began (row's stage start) &
             // 15 bytes early; with the matrix 16-byte aligned that lead is
@@ -728,19 +745,27 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 offset_form_c<4>(d, nd23, dmin, ndm23, byte_magic(scl, a), byte_magic(mhi, a),
                                  ds2[r][a], ee2[r][a], sub2[r][a]);
             }
-            // B fragments: lane (g, t) with g = 2t carries sub-block 4t + a
-            // (32-value block 2t + a/2, its half a & 1) in column g; every
-            // other lane reads zeros.  MMA (a, b): positions 4b .. 4b+3 of
-            // the sub-block; acc[a] column 2t sums (q - c) x over it.
-            const bool own2 = t == (g >> 1) && !(g & 1);
-            float acc[4][4];
+            // B fragments: lane (g, t) with t = g / 2 carries sub-block
+            // 4t + a (32-value block 2t + a/2, its half a & 1) of batch row
+            // 2P + (g & 1) in column g of pair P; every other lane reads
+            // zeros.  MMA (a, b): positions 4b .. 4b+3 of the sub-block;
+            // acc[P][a] column 2t + i sums (q - c) x over it for batch row
+            // 2P + i.
+            float acc[NP][4][4];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
               const uint32_t sh = 2u * (uint32_t)((2 * t + (a >> 1)) & 3);  // quant bits in a byte
-              const uint32_t *pb = own2 ? pw + (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1) : zeros;
 #pragma unroll
               for (int c2 = 0; c2 < 2; ++c2) {
-                const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+                uint4 bv[NP];
+#pragma unroll
+                for (int P = 0; P < NP; ++P) {
+                  const bool own = t == (g >> 1) && 2 * P + (g & 1) < batch;
+                  const uint32_t *pb = own ? pw + (2 * P + (g & 1)) * kPermWords +
+                                                 (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1)
+                                           : zeros;
+                  bv[P] = reinterpret_cast<const uint4 *>(pb)[own ? c2 : 0];
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int b = 2 * c2 + h, k = 4 * (a & 1) + b;
@@ -749,28 +774,33 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                   const uint32_t a1 = sub_bf16x2(lop_q2(w1, magic), sub2[1][a]);
                   const uint32_t a2 = sub_bf16x2(lop_q2(w0 >> 8, magic), sub2[0][a]);
                   const uint32_t a3 = sub_bf16x2(lop_q2(w1 >> 8, magic), sub2[1][a]);
-                  const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
-                  if (b == 0)
-                    mma_bf16_zc(acc[a], a0, a1, a2, a3, b0, b1);
-                  else
-                    mma_bf16(acc[a], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+                  for (int P = 0; P < NP; ++P) {
+                    const uint32_t b0 = h ? bv[P].z : bv[P].x, b1 = h ? bv[P].w : bv[P].y;
+                    if (b == 0)
+                      mma_bf16_zc(acc[P][a], a0, a1, a2, a3, b0, b1);
+                    else
+                      mma_bf16(acc[P][a], a0, a1, a2, a3, b0, b1);
+                  }
                 }
               }
             }
-            // X_{4t + a}: halves lo / hi of 32-value blocks 2t (column 2t) and
-            // 2t+1 (column 2t+1).
-            const float xsa[4] = {xl[0], xh[0], xl[1], xh[1]};
+            // X_{4t + a} of batch row b: halves lo / hi of 32-value blocks 2t
+            // (column 2t) and 2t+1 (column 2t+1) of its column-sum MMAs.
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float v = yacc[0][r][0];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-              for (int a = 0; a < 4; ++a) {
-                v = fmaf(ds2[r][a], acc[a][2 * r], v);
-                v = fmaf(ee2[r][a], xsa[a], v);
+              for (int b = 0; b < NB; ++b) {
+                const float xsa[4] = {xl[b][0], xh[b][0], xl[b][1], xh[b][1]};
+                float v = yacc[0][r][b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                  v = fmaf(ds2[r][a], acc[b >> 1][a][2 * r + (b & 1)], v);
+                  v = fmaf(ee2[r][a], xsa[a], v);
+                }
+                yacc[0][r][b] = v;
               }
-              yacc[0][r][0] = v;
-            }
-            pbuf ^= 1;
+            if (C::kPermBufs == 2) pbuf ^= 1;
             continue;
           }
           if constexpr (FMT == 3) {
@@ -779,16 +809,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             // and sc 6 bits: no min term, so the A operand is the exact u - 4
             // and no column sums are needed.  Thread t owns sub-blocks 4t ..
             // 4t+3 (a = 0..3) of rows g, g+8: half h = t / 2, bit pair
-            // g2 = (2t + a/2) mod 4 of the qs bytes, mask bit 4h + g2.
-            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
-            {
-              uint4 pm;
-              pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
-              pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
-              pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
-              pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
-              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
-            }
+            // g2 = (2t + a/2) mod 4 of the qs bytes, mask bit 4h + g2.  The
+            // MMA columns are (slot, batch row) as for Q6_K.
+            perm_x_rows(pw, xstage, u);
             __syncwarp();  // permuted x visible to every lane
             // Rows g, g+8: the stage copy of row r began (row's stage start) &
             // 15 bytes early; with the matrix 16-byte aligned that lead is
@@ -817,10 +840,9 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               for (int a = 0; a < 4; ++a)
                 ds3[r][a] = d * (float)((int)((sc6 >> (8 * a)) & 0xFFu) - 32);  // exact
             }
-            const bool own2 = t == (g >> 1) && !(g & 1);
             uint32_t sub4;
             asm volatile("mov.b32 %0, %1;\n" : "=r"(sub4) : "n"(0x43044304u));  // bf16 (132, 132)
-            float acc[4][4];
+            float acc[NP][4][4];
 #pragma unroll
             for (int ah = 0; ah < 2; ++ah) {  // a & 1: bytes 16 (a & 1) .. +15 of the quant / mask runs
               uint32_t qs[2][4], hm[2][4];
@@ -837,10 +859,17 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                 const uint32_t g2 = (uint32_t)((2 * t + a2) & 3);
                 const uint32_t qsh = 2u * g2;                                   // quant bits in a byte
                 const uint32_t mrot = (4u * (uint32_t)(t >> 1) + g2 - 2u) & 31u;  // mask bit -> bit 2
-                const uint32_t *pb = own2 ? pw + (2 * t + a2) * kPermStride + 8 * ah : zeros;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                  const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+                  uint4 bv[NP];
+#pragma unroll
+                  for (int P = 0; P < NP; ++P) {
+                    const bool own = t == (g >> 1) && 2 * P + (g & 1) < batch;
+                    const uint32_t *pb = own ? pw + (2 * P + (g & 1)) * kPermWords +
+                                                   (2 * t + a2) * kPermStride + 8 * ah
+                                             : zeros;
+                    bv[P] = reinterpret_cast<const uint4 *>(pb)[own ? c2 : 0];
+                  }
 #pragma unroll
                   for (int h = 0; h < 2; ++h) {
                     const int b = 2 * c2 + h;
@@ -855,22 +884,28 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                       av[r] = sub_bf16x2(lop_q2(lw, m02), sub4);
                       av[2 + r] = sub_bf16x2(lop_q2(lw >> 8, m13), sub4);
                     }
-                    const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
-                    if (b == 0)
-                      mma_bf16_zc(acc[a], av[0], av[1], av[2], av[3], b0, b1);
-                    else
-                      mma_bf16(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+#pragma unroll
+                    for (int P = 0; P < NP; ++P) {
+                      const uint32_t b0 = h ? bv[P].z : bv[P].x, b1 = h ? bv[P].w : bv[P].y;
+                      if (b == 0)
+                        mma_bf16_zc(acc[P][a], av[0], av[1], av[2], av[3], b0, b1);
+                      else
+                        mma_bf16(acc[P][a], av[0], av[1], av[2], av[3], b0, b1);
+                    }
                   }
                 }
               }
             }
+            // column 2t + (b & 1) of pair b / 2 holds batch row b
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float yv = yacc[0][r][0];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-              for (int a = 0; a < 4; ++a) yv = fmaf(ds3[r][a], acc[a][2 * r], yv);
-              yacc[0][r][0] = yv;
-            }
+              for (int b = 0; b < NB; ++b) {
+                float yv = yacc[0][r][b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) yv = fmaf(ds3[r][a], acc[b >> 1][a][2 * r + (b & 1)], yv);
+                yacc[0][r][b] = yv;
+              }
             __syncwarp();  // every lane's reads of the stage are done
             if (u == cnt - 1) {
               if (pp.valid) {  // refill this slot with the stream's next stage
@@ -881,7 +916,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               }
               if constexpr (!C::kTma) cp_async_commit();
             }
-            pbuf ^= 1;
+            if (C::kPermBufs == 2) pbuf ^= 1;
             continue;
           }
           if constexpr (FMT == 6) {
@@ -891,16 +926,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
             // column sums are needed.  Thread t owns sub-blocks 4t .. 4t+3
             // (a = 0..3) of rows g, g+8: half h = t / 2 of the block, 32-value
             // group v = (2t + a/2) mod 4 (low nibbles for v < 2, high ones
-            // for v >= 2; high bits 2v, 2v+1 of the qh bytes).
-            const uint4 raw = reinterpret_cast<const uint4 *>(xstage + u * kXBytes)[lane];
-            {
-              uint4 pm;
-              pm.x = __byte_perm(raw.x, raw.y, 0x5410u);
-              pm.y = __byte_perm(raw.x, raw.y, 0x7632u);
-              pm.z = __byte_perm(raw.z, raw.w, 0x5410u);
-              pm.w = __byte_perm(raw.z, raw.w, 0x7632u);
-              reinterpret_cast<uint4 *>(pw + g * kPermStride)[t] = pm;
-            }
+            // for v >= 2; high bits 2v, 2v+1 of the qh bytes).  The MMA
+            // columns are (slot, batch row) as for Q4_K: lane (g, t) with
+            // t = g / 2 carries batch row 2P + (g & 1) of pair P.
+            perm_x_rows(pw, xstage, u);
             __syncwarp();  // permuted x visible to every lane
             // Rows g, g+8: the stage copy of row r began (row's stage start) &
             // 15 bytes early; with the matrix 16-byte aligned that lead is
@@ -935,11 +964,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               for (int a = 0; a < 4; ++a)
                 ds6[r][a] = d * (float)(int)(int8_t)(scw >> (8 * a));  // exact
             }
-            const bool own2 = t == (g >> 1) && !(g & 1);
             const uint32_t nsh = (t & 1) ? 4u : 0u;  // high nibbles for v >= 2
             uint32_t sub32;
             asm volatile("mov.b32 %0, %1;\n" : "=r"(sub32) : "n"(0x43204320u));  // bf16 (160, 160)
-            float acc[4][4];
+            float acc[NP][4][4];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
               const uint32_t v = (uint32_t)((2 * t + (a >> 1)) & 3);
@@ -959,10 +987,17 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                   prev = next;
                 }
               }
-              const uint32_t *pb = own2 ? pw + (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1) : zeros;
 #pragma unroll
               for (int c2 = 0; c2 < 2; ++c2) {
-                const uint4 bv = reinterpret_cast<const uint4 *>(pb)[own2 ? c2 : 0];
+                uint4 bv[NP];
+#pragma unroll
+                for (int P = 0; P < NP; ++P) {
+                  const bool own = t == (g >> 1) && 2 * P + (g & 1) < batch;
+                  const uint32_t *pb = own ? pw + (2 * P + (g & 1)) * kPermWords +
+                                                 (2 * t + (a >> 1)) * kPermStride + 8 * (a & 1)
+                                           : zeros;
+                  bv[P] = reinterpret_cast<const uint4 *>(pb)[own ? c2 : 0];
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int b = 2 * c2 + h, kq = 4 * (a & 1) + b;
@@ -977,21 +1012,27 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
                     av[r] = sub_bf16x2(lop_nib(lw, m02), sub32);
                     av[2 + r] = sub_bf16x2(lop_nib(lw >> 8, m13), sub32);
                   }
-                  const uint32_t b0 = h ? bv.z : bv.x, b1 = h ? bv.w : bv.y;
-                  if (b == 0)
-                    mma_bf16_zc(acc[a], av[0], av[1], av[2], av[3], b0, b1);
-                  else
-                    mma_bf16(acc[a], av[0], av[1], av[2], av[3], b0, b1);
+#pragma unroll
+                  for (int P = 0; P < NP; ++P) {
+                    const uint32_t b0 = h ? bv[P].z : bv[P].x, b1 = h ? bv[P].w : bv[P].y;
+                    if (b == 0)
+                      mma_bf16_zc(acc[P][a], av[0], av[1], av[2], av[3], b0, b1);
+                    else
+                      mma_bf16(acc[P][a], av[0], av[1], av[2], av[3], b0, b1);
+                  }
                 }
               }
             }
+            // column 2t + (b & 1) of pair b / 2 holds batch row b
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float yv = yacc[0][r][0];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-              for (int a = 0; a < 4; ++a) yv = fmaf(ds6[r][a], acc[a][2 * r], yv);
-              yacc[0][r][0] = yv;
-            }
+              for (int b = 0; b < NB; ++b) {
+                float yv = yacc[0][r][b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) yv = fmaf(ds6[r][a], acc[b >> 1][a][2 * r + (b & 1)], yv);
+                yacc[0][r][b] = yv;
+              }
             __syncwarp();  // every lane's reads of the stage are done
             if (u == cnt - 1) {
               if (pp.valid) {  // refill this slot with the stream's next stage
@@ -1002,7 +1043,7 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
               }
               if constexpr (!C::kTma) cp_async_commit();
             }
-            pbuf ^= 1;
+            if (C::kPermBufs == 2) pbuf ^= 1;
             continue;
           }
           // X_j of the eight sub-blocks of each batch row: lane (g, t) holds
@@ -1233,9 +1274,10 @@ __global__ void __launch_bounds__(kWarps * 32, StreamCfg<MT, NB, FMT>::kMinBlock
 std::once_flag g_stream_attr[kMaxDevices];
 // Resident CTAs per SM of the kernels ([variant][op table small/large]; the
 // variants are NB = 1, 2, 4 for Q4_K (0, 2, 3), NB = 1 for Q5_K, q2_K, Q6_K
-// and q3_K (4 .. 7) and NB = 2, 4 for Q5_K (8, 9); 1 is unused), queried once
-// per device after the attributes are set.
-int g_occ[kMaxDevices][10][2];
+// and q3_K (4 .. 7) and NB = 2, 4 for Q5_K (8, 9), q2_K (10, 11), q3_K (12,
+// 13) and Q6_K (14, 15); 1 is unused), queried once per device after the
+// attributes are set.
+int g_occ[kMaxDevices][16][2];
 
 template <int MT, int NOPS, int NB, int FMT = 4>
 constexpr auto stream_kernel() {
@@ -1273,6 +1315,18 @@ void stream_attributes(int dev) {
   g_occ[dev][8][1] = stream_setup<1, kMaxOps, 2, 5>();
   g_occ[dev][9][0] = stream_setup<1, 1, 4, 5>();
   g_occ[dev][9][1] = stream_setup<1, kMaxOps, 4, 5>();
+  g_occ[dev][10][0] = stream_setup<1, 1, 2, 2>();
+  g_occ[dev][10][1] = stream_setup<1, kMaxOps, 2, 2>();
+  g_occ[dev][11][0] = stream_setup<1, 1, 4, 2>();
+  g_occ[dev][11][1] = stream_setup<1, kMaxOps, 4, 2>();
+  g_occ[dev][12][0] = stream_setup<1, 1, 2, 3>();
+  g_occ[dev][12][1] = stream_setup<1, kMaxOps, 2, 3>();
+  g_occ[dev][13][0] = stream_setup<1, 1, 4, 3>();
+  g_occ[dev][13][1] = stream_setup<1, kMaxOps, 4, 3>();
+  g_occ[dev][14][0] = stream_setup<1, 1, 2, 6>();
+  g_occ[dev][14][1] = stream_setup<1, kMaxOps, 2, 6>();
+  g_occ[dev][15][0] = stream_setup<1, 1, 4, 6>();
+  g_occ[dev][15][1] = stream_setup<1, kMaxOps, 4, 6>();
 }
 
 struct StreamPlan {
@@ -1373,18 +1427,22 @@ cudaError_t launch_stream_nb(const StreamOpDesc *ops, int count, int batch, cons
   return launch_stream_chunk<1, NOPS, 4>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
 }
 
-// The other k-quant formats (16-row tiles; batch 1, and Q5_K at 1..4).
+// The other k-quant formats (16-row tiles, batch 1..4).
+template <int NOPS, int FMT>
+cudaError_t launch_stream_kq_nb(const StreamOpDesc *ops, int count, int batch, const StreamPlan &pl,
+                                bool overlap, cudaStream_t stream) {
+  return batch == 1   ? launch_stream_chunk<1, NOPS, 1, FMT>(ops, count, 1, pl.kp, pl.grid, overlap, stream)
+         : batch == 2 ? launch_stream_chunk<1, NOPS, 2, FMT>(ops, count, 2, pl.kp, pl.grid, overlap, stream)
+                      : launch_stream_chunk<1, NOPS, 4, FMT>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
+}
 template <int NOPS>
 cudaError_t launch_stream_kq(int fmt, const StreamOpDesc *ops, int count, int batch,
                              const StreamPlan &pl, bool overlap, cudaStream_t stream) {
   switch (fmt) {
-    case 2: return launch_stream_chunk<1, NOPS, 1, 2>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
-    case 3: return launch_stream_chunk<1, NOPS, 1, 3>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
-    case 5:
-      return batch == 1   ? launch_stream_chunk<1, NOPS, 1, 5>(ops, count, 1, pl.kp, pl.grid, overlap, stream)
-             : batch == 2 ? launch_stream_chunk<1, NOPS, 2, 5>(ops, count, 2, pl.kp, pl.grid, overlap, stream)
-                          : launch_stream_chunk<1, NOPS, 4, 5>(ops, count, batch, pl.kp, pl.grid, overlap, stream);
-    case 6: return launch_stream_chunk<1, NOPS, 1, 6>(ops, count, 1, pl.kp, pl.grid, overlap, stream);
+    case 2: return launch_stream_kq_nb<NOPS, 2>(ops, count, batch, pl, overlap, stream);
+    case 3: return launch_stream_kq_nb<NOPS, 3>(ops, count, batch, pl, overlap, stream);
+    case 5: return launch_stream_kq_nb<NOPS, 5>(ops, count, batch, pl, overlap, stream);
+    case 6: return launch_stream_kq_nb<NOPS, 6>(ops, count, batch, pl, overlap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1396,18 +1454,16 @@ int stream_max_batch() { return 4; }
 cudaError_t launch_stream(const StreamOpDesc *ops, int64_t count, int batch, bool overlap,
                           cudaStream_t stream, int fmt) {
   if (batch < 1 || batch > stream_max_batch()) return cudaErrorInvalidValue;
-  if (fmt != 4 && fmt != 5 && !((fmt == 2 || fmt == 3 || fmt == 6) && batch == 1))
-    return cudaErrorInvalidValue;
+  if (fmt < 2 || fmt > 6) return cudaErrorInvalidValue;
   const DeviceFacts *f = device_facts();
   std::call_once(g_stream_attr[f->device], stream_attributes, f->device);
   if (fmt != 4)
     for (int64_t i = 0; i < count; ++i)
       if (ops[i].n > 0 && ops[i].w_up) return cudaErrorInvalidValue;  // no fused gate/up
   // 16-row kernel of this format and batch
-  const int var1 = fmt == 5   ? (batch == 1 ? 4 : batch == 2 ? 8 : 9)
-                   : fmt == 2 ? 5
-                   : fmt == 6 ? 6
-                   : fmt == 3 ? 7
+  const int nbi = batch == 1 ? 0 : batch == 2 ? 1 : 2;  // NB = 1, 2, 4
+  static const int kVar[7][3] = {{0}, {0}, {5, 10, 11}, {7, 12, 13}, {0}, {4, 8, 9}, {6, 14, 15}};
+  const int var1 = fmt != 4   ? kVar[fmt][nbi]
                    : batch == 1 ? 0
                    : batch == 2 ? 2
                                 : 3;

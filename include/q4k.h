@@ -286,7 +286,9 @@ int q4k_kq_dequant(int32_t format, const void *w, int64_t n, int64_t k, void *ou
 /*
  * q4k_kq_gemv -- q4k_gemv for any of the formats: Y[b, :] = W X[b, :],
  * batch 1..16, arguments and layouts as q4k_gemv (format 4 is q4k_gemv
- * itself).  Each weight row is read once for all batch rows.  K is limited so
+ * itself).  Each weight row is read once for all batch rows.  Batch 1..4 runs
+ * on the tensor cores (exact small-integer operands, as Q4_K), batch 5..16
+ * forms each weight in fp32 and contracts in fp32.  K is limited so
  * that 8 rows fit in shared memory: K/256 * block bytes <= 29040 (e.g.
  * K <= 35328 for Q6_K, 88320 for q2_K).
  * Errors: as q4k_gemv, and SHAPE for an unknown format or too long a row.
@@ -305,8 +307,8 @@ int q4k_kq_gemv(int32_t format, const void *w, int64_t n, int64_t k, const void 
  *           in `format`; w_up must be NULL (no fused gate/up here)
  *   batch   1..16, shared by all ops
  *   flags   as q4k_gemv_ex
- * At batch 1 (Q5_K: batch 1..4) the ops run as persistent launches of the
- * tensor-core kernel (one per Q4K_SEQ_MATRICES_PER_LAUNCH ops, split evenly)
+ * At batch 1..4 the ops run as persistent launches of the tensor-core kernel
+ * (one per Q4K_SEQ_MATRICES_PER_LAUNCH ops, split evenly)
  * that stream their weights back to back, and ops may run concurrently: no op
  * may read what another op of the same sequence writes.  At larger batches
  * each op is its own
