@@ -172,23 +172,24 @@ def test_cancelling_rows_give_exact_zero_at_batch_1(q4k, fmt, k):
     check_bound(got, yref, s, TOL, f"kq{fmt} cancel k{k}")
 
 
+@pytest.mark.parametrize("fmt", [2, 3, 5, 6])
 @pytest.mark.parametrize("batch", [2, 3, 4])
 @pytest.mark.parametrize("k", [256, 5120])
-def test_q5k_cancelling_rows_give_exact_zero_at_batch_2_to_4(q4k, batch, k):
-    # Q5_K at batch 2..4 also runs on the tensor cores (the Q4_K contraction
-    # with a fifth bit, MMA columns = (sub-block slot, batch row)): rows whose
-    # weights all cancel come out exactly 0 for every batch row
-    w = _cancel_matrix(5, k, seed=k + 50 + batch)
+def test_cancelling_rows_give_exact_zero_at_batch_2_to_4(q4k, fmt, batch, k):
+    # batch 2..4 runs on the tensor cores too (MMA columns = (sub-block slot,
+    # batch row)): rows whose weights all cancel come out exactly 0 for every
+    # batch row, the rest within the bound
+    w = _cancel_matrix(fmt, k, seed=k + 10 * fmt + batch)
     n = w.shape[0]
-    x = synth.bf16_normal((batch, k), seed=5 * k + batch)
-    y = q4k.q4k_kq_gemv(5, w.to(DEV), n, k, x.to(DEV))
+    x = synth.bf16_normal((batch, k), seed=5 * k + batch + fmt)
+    y = q4k.q4k_kq_gemv(fmt, w.to(DEV), n, k, x.to(DEV))
     torch.cuda.synchronize()
     assert q4k.q4k_get_device_error() == 0
     got = y.cpu().numpy().astype(np.float64)
-    yref, s = oracle.kq_gemv(5, w.numpy(), n, k, xbits(x))
+    yref, s = oracle.kq_gemv(fmt, w.numpy(), n, k, xbits(x))
     assert np.all(s[:, 0::3] == 0.0) and np.all(yref[:, 0::3] == 0.0)
-    assert np.all(got[:, 0::3] == 0.0), f"Q5_K b{batch}: rows whose weights all cancel must be exactly 0"
-    check_bound(got, yref, s, TOL, f"Q5_K cancel k{k} b{batch}")
+    assert np.all(got[:, 0::3] == 0.0), f"kq{fmt} b{batch}: rows whose weights all cancel must be exactly 0"
+    check_bound(got, yref, s, TOL, f"kq{fmt} cancel k{k} b{batch}")
 
 
 @pytest.mark.parametrize("fmt", [2, 3, 5, 6])
