@@ -110,6 +110,23 @@ def test_moe_one_expert_for_all_tokens_spans_slots(q4k):
     _check(y, yref, bound, "single expert")
 
 
+@pytest.mark.parametrize("weighted_down", [False, True])
+def test_moe_every_slot_width(q4k, weighted_down):
+    # expert e (e = 0..7) gets exactly e + 1 pairs: slots of 1 to 8 pairs in one
+    # step, so every contraction width of the expert kernel runs (gate/up 1..8
+    # columns, down 2..16)
+    E, T, K = 8, 12, 3
+    c = _make(E, 512, 512, T, K, seed=41)
+    order = [e for e in range(E) for _ in range(e + 1)]  # 36 = T * K pairs
+    # slot k of token t is pair k * T + t: an expert spans at most 8 < T
+    # consecutive pairs, so no token meets one expert twice
+    ids = torch.tensor(order, dtype=torch.int32).view(K, T).t().contiguous()
+    y, err = _gpu(q4k, c, ids, c["wts"], flags=int(weighted_down))
+    assert err == 0
+    yref, bound = _bound(c, ids, c["wts"], list(range(T)), weighted_down)
+    _check(y, yref, bound, f"slot widths wd{int(weighted_down)}")
+
+
 def test_moe_duplicate_ids_and_bad_ids(q4k):
     c = _make(8, 512, 256, 4, 3, seed=7)
     ids = c["ids"].clone()
