@@ -11,7 +11,7 @@
 //               and clears the work counters of launch 2.
 //   2. experts  one persistent kernel, every CTA resident.  CTAs pull work items
 //               in order from a counter: first the gate/up items (work slot,
-//               64 rows of ffn), then the down items (work slot, 128 rows of
+//               64 rows of ffn), then the down items (work slot, 64 rows of
 //               hidden).  A gate/up item streams the expert's gate and up rows
 //               once (TMA) and contracts them with all of the slot's tokens on
 //               the tensor cores (MMA columns = tokens); it writes g, u and
@@ -23,7 +23,7 @@
 //               down outputs unweighted.  A down item waits (bounded)
 //               until every gate/up item of its slot is done, streams the
 //               expert's down rows and writes p = Wd h per pair.  The CTA that
-//               completes the last down item of a 128-row group of hidden adds
+//               completes the last down item of a 64-row group of hidden adds
 //               y[t] = sum_j w[t, j] * p[t, j] over the slots j = 0..k-1 of
 //               every token, in that order.
 // Items are claimed in order and every CTA is resident, so a down item only
@@ -43,7 +43,7 @@ namespace {
 constexpr int kRows = 16;                    // rows per CTA (one MMA m-tile)
 constexpr int kTile = kRows * kBlockBytes;   // 2304 bytes per super-block stage
 #ifndef Q4K_MOE_STAGES  // ring stages per warp stream
-#define Q4K_MOE_STAGES 3
+#define Q4K_MOE_STAGES 2
 #endif
 constexpr int kStagesMoe = Q4K_MOE_STAGES;
 constexpr int kMoeWarps = 4;                 // warps (weight streams) per expert CTA
@@ -68,7 +68,10 @@ constexpr int kOffZeroMoe = kOffPermMoe + 2 * kPermWordsMoe * 4;
 constexpr int kWarpBytes = (kOffZeroMoe + 64 + 127) / 128 * 128;
 constexpr int kMetaAbort = 2;  // workspace meta word: a wait timed out, stop taking items
 constexpr int kGuTilesPerItem = 4;  // 16-row tiles of ffn per gate/up item (one per warp)
-constexpr int kDnTilesPerItem = 8;  // 16-row tiles of hidden per down item (two per warp)
+// 16-row tiles of hidden per down item (one per warp): each CTA's last item is
+// a down item, so a small one keeps the step's tail short (measured on 128
+// experts, 16 tokens, top-8: 8 tiles 2.36 TB/s, 4 tiles 2.50, 16 tiles 2.02)
+constexpr int kDnTilesPerItem = 4;
 
 struct MoeLayout {
   size_t meta, counters, slot_expert, slot_start, pair_token, pair_q, tj_pair, g, u, h, h_hi, h_lo, p,
@@ -80,7 +83,7 @@ struct MoeLayout {
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t S = (size_t)max_slots(E, P);
     // work counters: [0] next item, [1 .. 1+S) gate/up items done per slot,
-    // [1+S ..) down items done per 128-row group of hidden
+    // [1+S ..) down items done per 64-row group of hidden
     n_counters = 1 + (int)S + dn_groups(H);
     size_t o = 0;
     meta = o;        o = al(o + 16 * sizeof(int));
@@ -828,7 +831,7 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
     const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mu,
     const __grid_constant__ CUtensorMap md, const MoeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_item, s_last, s_fail;
+  __shared__ int s_item[2], s_last, s_fail;
   // Each warp's ring and barriers, set up once: items only carry the ring
   // iteration count on, so no barrier is ever initialised twice and no copy
   // lands in memory that held a barrier.
@@ -856,22 +859,28 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
   const int n_gu = S * gu_groups, n_items = n_gu + S * dn_groups;
   int *next = a.counters, *slot_done = a.counters + 1, *grp_done = a.counters + 1 + a.max_slots;
   int *abort_word = a.meta + kMetaAbort;
-  for (;;) {
-    // after a timed-out wait anywhere, no CTA takes another item
-    if (threadIdx.x == 0) s_item = load_acquire(abort_word) ? n_items : atomicAdd(next, 1);
+  for (int par = 0;; par ^= 1) {
+    // after a timed-out wait anywhere, no CTA takes another item; the claim
+    // alternates between two words, so the item's own barriers separate each
+    // word's reads from its next write
+    if (threadIdx.x == 0) s_item[par] = load_acquire(abort_word) ? n_items : atomicAdd(next, 1);
     __syncthreads();
-    const int item = s_item;
-    __syncthreads();  // every thread has read s_item before it is written again
+    const int item = s_item[par];
     if (item >= n_items) break;
     if (item < n_gu) {
       const int slot = item / gu_groups, grp = item - slot * gu_groups;
       if (!slot_item<NTGU, false>(&mg, &mu, a, nsb_gu, a.ffn, ring, bars, it, slot,
                                   grp * kGuTilesPerItem, kGuTilesPerItem))
         s_fail = 1;
-      __threadfence();  // this thread's g, u, h writes are visible GPU-wide ...
-      __syncthreads();  // ... for every thread of the CTA, before the count goes up
+      // Every thread's g, u, h writes come before the barrier; thread 0's
+      // GPU-scope fence after it is cumulative over them (a release of the
+      // whole CTA's writes), so one fence per item, not one per thread.
+      __syncthreads();
       if (s_fail) break;
-      if (threadIdx.x == 0) atomicAdd(&slot_done[slot], 1);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&slot_done[slot], 1);
+      }
     } else {
       const int j = item - n_gu, slot = j / dn_groups, grp = j - slot * dn_groups;
       if (threadIdx.x == 0 && !wait_count(&slot_done[slot], gu_groups, abort_word, a.err))
@@ -881,12 +890,12 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_persistent_kernel(
       if (!slot_item<NTDN, true>(&md, &md, a, nsb_dn, a.hidden, ring, bars, it, slot,
                                  grp * kDnTilesPerItem, kDnTilesPerItem))
         s_fail = 1;
-      __threadfence();  // this thread's down outputs are visible GPU-wide ...
-      __syncthreads();  // ... before the group's count goes up
+      __syncthreads();  // every thread's down outputs precede thread 0's release
       if (s_fail) break;
       if (threadIdx.x == 0) {
-        s_last = atomicAdd(&grp_done[grp], 1) == S - 1;
         __threadfence();
+        s_last = atomicAdd(&grp_done[grp], 1) == S - 1;
+        __threadfence();  // the last one acquires every other CTA's outputs
       }
       __syncthreads();
       if (s_last) {
