@@ -53,8 +53,15 @@
 #ifndef Q4K_WIDE_STAGES_NT2
 #define Q4K_WIDE_STAGES_NT2 2
 #endif
-#ifndef Q4K_WIDE_MINB  // resident CTAs per SM the register budget is sized for
-#define Q4K_WIDE_MINB 4
+// Resident CTAs per SM the register budget is sized for, batch 5..8 and
+// 9..16 (measured on the 64-layer pass: 6 CTAs at batch 5 / 8 2.78 / 2.73
+// TB/s against 2.74 / 2.67 at 4 and 2.53 / 2.44 at 3; batch 16 2.00 at 4,
+// 1.97 at 5, 1.99 at 6, 1.81 at 3).
+#ifndef Q4K_WIDE_MINB_NT1
+#define Q4K_WIDE_MINB_NT1 6
+#endif
+#ifndef Q4K_WIDE_MINB_NT2
+#define Q4K_WIDE_MINB_NT2 4
 #endif
 #ifndef Q4K_WIDE_PRE  // weight stages requested before the dependency wait (PDL)
 #define Q4K_WIDE_PRE 2
@@ -169,7 +176,7 @@ __device__ __forceinline__ float silu_mul_w(float g, float u) {
 }
 
 template <int NT, int NOPS>
-__global__ void __launch_bounds__(kWideThreads, Q4K_WIDE_MINB)
+__global__ void __launch_bounds__(kWideThreads, NT == 1 ? Q4K_WIDE_MINB_NT1 : Q4K_WIDE_MINB_NT2)
     gemv_wide_kernel(const __grid_constant__ WideParams<NOPS> p) {
   using C = WideCfg<NT>;
   constexpr int SB = C::kSB, ST = C::kStages, NB = C::kNB;

@@ -151,7 +151,8 @@ def test_gemv_seq_64_row_tiles_several_launches(q4k, batch, flags):
     # oracle and an empty op writes nothing
     count = 170
     rng = np.random.default_rng(4300 + batch)
-    shapes = [(int(rng.integers(400, 700)), int(rng.choice([256, 512]))) for _ in range(count)]
+    # about 2000 tiles of 64 rows: at least two per resident CTA at batch 5..16
+    shapes = [(int(rng.integers(700, 1000)), int(rng.choice([256, 512]))) for _ in range(count)]
     shapes[5] = (0, 256)
     glu = {i for i in range(count) if i % 7 == 3}
     mats = sum((2 if i in glu else 1) for i, (n, _) in enumerate(shapes) if n > 0)
